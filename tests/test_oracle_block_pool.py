@@ -1,0 +1,147 @@
+"""Pins for the allocator model (oracle/block_pool.py)."""
+import copy
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle.block_pool import BlockPool, SequencePool
+
+
+def test_fork_cow_example_of_the_vllm_page(golden_dir):
+    with open(os.path.join(golden_dir, "block_pool_fork_cow.json")) as f:
+        fx = json.load(f)
+    ex = fx["expected"]
+    pool = BlockPool(fx["num_blocks"], fx["block_size"])
+    original = []
+    for tok in fx["original_tokens"]:
+        original = pool.append(original, tok).table
+    branch = pool.fork(original)
+    res = pool.append(branch, fx["branch_token"])
+    branch = res.table
+    assert pool.read(original) == ex["read_original"]
+    assert pool.read(branch) == ex["read_branch"]
+    assert original[-1] != branch[-1]
+    assert pool.refs[original[0]] == ex["refs_original_first"]
+    assert pool.refs[original[-1]] == ex["refs_original_last"]
+    assert original == ex["original_table"] and branch == ex["branch_table"]
+    assert list(res.cow) == ex["branch_cow_pair"]
+    assert pool.free == ex["free_after"]
+
+
+def test_block_counts_of_the_source_analysis_mapping_example():
+    # requests of 32, 16 and 48 tokens need 2, 1 and 3 blocks of 16 (order-free property)
+    pool = SequencePool(16, 16)
+    ids = []
+    for n in (32, 16, 48):
+        sid = pool.create()
+        for _ in range(n):
+            pool.append(sid)
+        ids.append(sid)
+    assert [len(pool.tables[s]) for s in ids] == [2, 1, 3]
+    used = [b for s in ids for b in pool.tables[s]]
+    assert len(set(used)) == 6 and pool.num_free() == 10
+    assert pool.invariants() == []
+
+
+def test_slots_are_block_times_size_plus_offset():
+    pool = SequencePool(4, 4)
+    sid = pool.create()
+    slots = [pool.append(sid).slot for _ in range(6)]
+    # LIFO: first block is 3, second is 2
+    assert slots == [12, 13, 14, 15, 8, 9]
+
+
+def snapshot(pool):
+    return copy.deepcopy((pool.pool.free, pool.pool.refs, pool.pool.data, pool.tables, pool.lens))
+
+
+def test_exhaustion_leaves_state_unchanged():
+    pool = SequencePool(3, 2)
+    a = pool.create()
+    for _ in range(5):
+        pool.append(a)  # blocks 2, 1, 0; the tail holds one token; nothing is free
+    b = pool.fork(a)
+    snap = snapshot(pool)
+    with pytest.raises(MemoryError):
+        pool.append(b)  # copy-on-write of the shared tail needs a block
+    assert snapshot(pool) == snap
+    with pytest.raises(MemoryError):
+        pool.append(a)  # a shares the tail as well
+    assert snapshot(pool) == snap
+    pool.release(b)
+    assert pool.append(a).cow is None  # sole holder again: written in place
+    full = snapshot(pool)  # a's tail is now full and the pool is empty
+    with pytest.raises(MemoryError):
+        pool.append(a)
+    assert snapshot(pool) == full
+    assert pool.invariants() == []
+
+
+def test_last_sharer_writes_in_place():
+    pool = SequencePool(8, 4)
+    a = pool.create()
+    for _ in range(6):
+        pool.append(a)
+    b = pool.fork(a)
+    r1 = pool.append(b)
+    assert r1.cow is not None  # b copies the shared tail
+    r2 = pool.append(a)
+    assert r2.cow is None  # a is now the only holder: in place
+    assert pool.invariants() == []
+
+
+@pytest.mark.parametrize("prefix,expected_copies", [(2048, 0), (2056, 63)])
+def test_prefix_workload_copy_count(prefix, expected_copies):
+    pool = SequencePool(1000, 16)
+    parent = pool.create()
+    for _ in range(prefix):
+        pool.append(parent)
+    seqs = [parent] + [pool.fork(parent) for _ in range(63)]
+    shared = pool.tables[parent][0]
+    assert pool.refcount(shared) == 64
+    copies = 0
+    for sid in seqs:
+        copies += pool.append(sid).cow is not None
+    assert copies == expected_copies
+    assert pool.invariants() == []
+
+
+def test_release_returns_blocks_and_keeps_shared_ones():
+    pool = SequencePool(10, 2)
+    a = pool.create()
+    for _ in range(5):
+        pool.append(a)
+    b = pool.fork(a)
+    pool.append(b)
+    free_before = pool.num_free()
+    pool.release(a)
+    # a's first two blocks are still held by b; its old tail (now private to a) is freed
+    assert pool.num_free() == free_before + 1
+    assert pool.invariants() == []
+    pool.release(b)
+    assert pool.num_free() == 10
+    assert pool.invariants() == []
+
+
+def test_random_operations_keep_invariants():
+    rng = np.random.default_rng(0)
+    pool = SequencePool(64, 4, free_order=rng.permutation(64))
+    live = []
+    for step in range(3000):
+        op = rng.integers(0, 10)
+        try:
+            if op == 0 or not live:
+                live.append(pool.create())
+            elif op == 1:
+                live.append(pool.fork(live[rng.integers(len(live))]))
+            elif op == 2:
+                sid = live.pop(rng.integers(len(live)))
+                pool.release(sid)
+            else:
+                pool.append(live[rng.integers(len(live))])
+        except MemoryError:
+            sid = live.pop(rng.integers(len(live)))
+            pool.release(sid)
+        assert pool.invariants() == [], step

@@ -1,0 +1,602 @@
+#!/usr/bin/env python3
+"""Benchmark of one paged decode step on GB300: pa_write_kv + pa_decode.
+
+A step is one pass of the hot path over one batch: the new token of every
+sequence is written through its slot (pa_write_kv), then decode attention runs
+over the whole paged context (pa_decode: the decode kernel, plus the split-KV
+merge kernel when contexts are partitioned).  Block tables and slots come from
+the host block pool (pa_pool), built before the timed region.
+
+Prints one JSON line (rank 0).  ``value`` is KV GB/s over the algorithmic
+bytes (K+V of the valid tokens + q + out + block-table entries + lengths, plus
+the write's bytes), device-timed with CUDA events with inputs resident in HBM;
+``e2e`` is the same metric through the Python API with the step's inputs
+copied from pinned host memory and the output copied back inside the timed
+region.  ``--impl reference`` times the fp64 CPU oracle instead.
+
+Under torchrun each rank runs its own batch of the same shape (weak scaling,
+no collective on the data path); the time is the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+METRIC = "paged-decode KV GB/s and % of GB300 HBM peak; decode queries/s"
+UNIT = "GB/s"
+FALLBACK_HBM_GBS = 6800.0
+L2_BYTES_DEFAULT = 129 * 1024 * 1024
+
+WORKLOAD_DESCRIPTIONS = {
+    "qwen_gqa": "Qwen-style GQA layer: batch 64, 28 q / 4 kv heads, head_dim 128, bf16, block_size 16, "
+                "context_lens uniform in [512,4096], pool 20000 blocks shuffled, q/K/V ~ N(0,1), "
+                "one new token per sequence written via slot_mapping before the decode",
+    "long_context": "long-context split-KV: batch 8, 32 q / 8 kv heads, head_dim 128, bf16, block_size 16, "
+                    "context_lens uniform in [32768,131072], pool sized to fit (+1%), shuffled",
+    "mha_short_bs16": "many short requests, MHA: batch 256, 32/32 heads, head_dim 128, fp16, block_size 16, "
+                      "context_lens lognormal(median 256, sigma 1) clipped to [16,2048]",
+    "mha_short_bs32": "many short requests, MHA: batch 256, 32/32 heads, head_dim 128, fp16, block_size 32, "
+                      "context_lens lognormal(median 256, sigma 1) clipped to [16,2048]",
+}
+DTYPE_NAMES = {"f32": "f32", "f16": "f16", "bf16": "bf16"}
+
+
+# ---- host-side pieces (no GPU needed; covered by the gloo tests) ------------------------------
+def rank_seed(base_seed: int, rank: int) -> int:
+    """Every rank decodes its own batch of the same shape: the seed is offset by the rank."""
+    return base_seed + 1000003 * rank
+
+
+def decode_bytes(context_lens, num_heads: int, num_kv_heads: int, head_dim: int, elem_bytes: int,
+                 block_size: int) -> int:
+    """Algorithmic bytes of one decode call: K+V of the valid tokens, q, out, table entries, lengths."""
+    lens = np.asarray(context_lens, dtype=np.int64)
+    kv = 2 * int(lens.sum()) * num_kv_heads * head_dim * elem_bytes
+    qo = 2 * len(lens) * num_heads * head_dim * elem_bytes
+    tables = 4 * int(((lens + block_size - 1) // block_size).sum())
+    return kv + qo + tables + 4 * len(lens)
+
+
+def pages_touched_bytes(context_lens, num_kv_heads: int, head_dim: int, elem_bytes: int, block_size: int) -> int:
+    lens = np.asarray(context_lens, dtype=np.int64)
+    pages = int(((lens + block_size - 1) // block_size).sum())
+    return 2 * pages * block_size * num_kv_heads * head_dim * elem_bytes
+
+
+def write_bytes(num_tokens: int, num_kv_heads: int, head_dim: int, elem_bytes: int) -> int:
+    """Read new K and V, write them into the caches, read the slots."""
+    return 4 * num_tokens * num_kv_heads * head_dim * elem_bytes + 8 * num_tokens
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64)
+    if dist.get_backend() == "nccl":
+        t = t.cuda()
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def sum_over_ranks(value: float, world: int) -> float:
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor([value], dtype=torch.float64)
+    if dist.get_backend() == "nccl":
+        t = t.cuda()
+    dist.all_reduce(t, op=dist.ReduceOp.SUM)
+    return float(t.item())
+
+
+def barrier(world: int) -> None:
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+def measured_peaks() -> dict:
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return json.load(f)
+    except (OSError, ValueError):
+        return {}
+
+
+def kernel_sources_digest() -> str:
+    """sha256 over the decode kernel's sources: ties a stored ncu traffic figure to the code it measured."""
+    h = hashlib.sha256()
+    for name in ("decode_kernel.cuh", "pa_common.cuh", "decode_bf16.cu", "decode_launch.h"):
+        with open(os.path.join(ROOT, "paged_kv_cache_129_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()
+
+
+def stored_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it measured the current sources."""
+    path = os.path.join(ROOT, "profiles", f"ncu_paged_decode_{workload}.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    fields = {}
+    for line in text.splitlines():
+        if ":" in line and line.strip().startswith("- "):
+            k, v = line.strip()[2:].split(":", 1)
+            fields[k.strip()] = v.strip().strip("`")
+    if fields.get("kernel_sources_sha256") != kernel_sources_digest():
+        return None
+    try:
+        return int(fields["traffic_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def gpu_selector(device) -> str:
+    """nvidia-smi -i argument for a torch device (its UUID; CUDA_VISIBLE_DEVICES may renumber)."""
+    import torch
+
+    try:
+        uid = str(torch.cuda.get_device_properties(device).uuid)
+        return uid if uid.startswith("GPU-") else "GPU-" + uid
+    except (AttributeError, RuntimeError):
+        return str(device.index or 0)
+
+
+class ClockSampler:
+    """Samples SM clocks and throttle reasons with nvidia-smi while running."""
+
+    QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,clocks_event_reasons.hw_slowdown,"
+             "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+             "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: str, period_s: float = 0.1):
+        self.device_index = device_index
+        self.period_s = period_s
+        self.samples = []
+        self._stop = threading.Event()
+        self._thread = None
+        self.window = None
+
+    def _one(self):
+        try:
+            r = subprocess.run(["nvidia-smi", "-i", str(self.device_index), f"--query-gpu={self.QUERY}",
+                                "--format=csv,noheader,nounits"], capture_output=True, text=True, timeout=5)
+        except (OSError, subprocess.SubprocessError):
+            return None
+        if r.returncode != 0 or not r.stdout.strip():
+            return None
+        return [x.strip() for x in r.stdout.strip().splitlines()[0].split(",")]
+
+    def _loop(self):
+        while not self._stop.is_set():
+            t0 = time.monotonic()
+            s = self._one()
+            t1 = time.monotonic()
+            if s:
+                self.samples.append(((t0 + t1) / 2, s))
+            self._stop.wait(max(0.0, self.period_s - (t1 - t0)))
+
+    def start(self):
+        self._thread = threading.Thread(target=self._loop, daemon=True)
+        self._thread.start()
+
+    def stop(self):
+        self._stop.set()
+        if self._thread:
+            self._thread.join(timeout=10)
+
+    def summary(self, t_begin: float, t_end: float) -> dict:
+        inside = [s for t, s in self.samples if t_begin <= t <= t_end]
+        used = inside if inside else [s for _, s in self.samples]
+        if not used:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(s[0]) for s in used if num(s[0]) is not None]
+        reasons = set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for s in used:
+            for name, flag in zip(names, s[4:8]):
+                if flag.strip().lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": num(used[0][1]),
+                "reasons": sorted(reasons), "samples": len(used),
+                "samples_inside_timed_region": len(inside),
+                "power_w_max": max((num(s[2]) or 0.0) for s in used)}
+
+
+# ---- the CPU oracle leg -------------------------------------------------------------------------
+def time_oracle(inp, budget_s: float, rows_cap: int = 0):
+    """Time the fp64 oracle on the first sequences of the batch (all heads), about `budget_s` seconds."""
+    import oracle
+
+    per_seq = []
+    rows_done = 0
+    seqs = 0
+    bytes_done = 0
+    t_total = 0.0
+    eb = inp.elem_bytes
+    for b in range(inp.num_seqs):
+        rows = [(b, h) for h in range(inp.num_heads)]
+        if rows_cap:
+            rows = rows[:rows_cap]
+        t0 = time.perf_counter()
+        oracle.decode_inputs(inp, rows=rows)
+        dt = time.perf_counter() - t0
+        t_total += dt
+        per_seq.append(dt)
+        rows_done += len(rows)
+        seqs += 1
+        L = int(inp.context_lens[b])
+        frac = len(rows) / inp.num_heads
+        bytes_done += frac * decode_bytes([L], inp.num_heads, inp.num_kv_heads, inp.head_dim, eb, inp.block_size)
+        if t_total >= budget_s:
+            break
+    return {"seconds": t_total, "seqs": seqs, "rows": rows_done, "bytes": bytes_done}
+
+
+# ---- GPU arm ---------------------------------------------------------------------------------------
+def build_batch(workload: str, seed: int):
+    from paged_kv_cache_129_gb300 import workloads as wl
+
+    gen = {"qwen_gqa": lambda s: wl.qwen_gqa(s), "long_context": lambda s: wl.long_context(s),
+           "mha_short_bs16": lambda s: wl.mha_short(16, s), "mha_short_bs32": lambda s: wl.mha_short(32, s)}[workload]
+    return gen(seed)
+
+
+def pool_tables(inp):
+    """Block tables and new-token slots from the host block pool (a shuffled free list).
+
+    Each sequence appends its L-1 context tokens, then the step's new token is
+    appended for all sequences at once; the decode attends over L tokens.
+    """
+    import paged_kv_cache_129_gb300 as pa
+
+    rng = np.random.default_rng(12345)
+    pool = pa.BlockPool(inp.num_blocks, inp.block_size, free_order=rng.permutation(inp.num_blocks))
+    ids = [pool.create() for _ in range(inp.num_seqs)]
+    for sid, L in zip(ids, inp.context_lens):
+        for _ in range(int(L) - 1):
+            pool.append(sid)
+    if inp.new_key is not None:
+        slots, pairs = pool.append_batch(ids)
+        assert len(pairs) == 0
+    else:
+        for sid in ids:
+            pool.append(sid)
+        slots = None
+    width = int((int(inp.context_lens.max()) + inp.block_size - 1) // inp.block_size)
+    tables, lens = pool.block_tables(ids, width)
+    assert np.array_equal(lens, inp.context_lens)
+    pool.check_invariants()
+    return tables, lens, slots
+
+
+def run_ours(args, rank: int, world: int, local_rank: int) -> None:
+    import torch
+
+    import paged_kv_cache_129_gb300 as pa
+
+    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    pa.library()
+
+    inp = build_batch(args.workload, rank_seed(args.seed, rank))
+    tables, lens, slots = pool_tables(inp)
+    inp.block_tables = tables
+    tdtype = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[inp.dtype]
+
+    def up(a):
+        a = np.ascontiguousarray(a)
+        if inp.dtype in ("bf16", "f16"):
+            return torch.from_numpy(a.view(np.int16)).to(device).view(tdtype)
+        return torch.from_numpy(a).to(device)
+
+    eb = inp.elem_bytes
+    B, Hq, Hkv, d, bs = inp.num_seqs, inp.num_heads, inp.num_kv_heads, inp.head_dim, inp.block_size
+    dec_bytes = decode_bytes(lens, Hq, Hkv, d, eb, bs)
+    ntok = 0 if slots is None else len(slots)
+    wr_bytes = write_bytes(ntok, Hkv, d, eb)
+    step_bytes = dec_bytes + wr_bytes
+    touched = pages_touched_bytes(lens, Hkv, d, eb, bs)
+
+    l2 = L2_BYTES_DEFAULT
+    try:
+        l2 = torch.cuda.get_device_properties(device).L2_cache_size or l2
+    except AttributeError:
+        pass
+    # Rotate over cache replicas so that a step never finds its pages in L2 from the previous one.
+    replicas = 1 if touched >= 3 * l2 else max(2, math.ceil(2 * l2 / touched) + 1)
+    kc0, vc0 = up(inp.key_cache), up(inp.value_cache)
+    kcs, vcs = [kc0], [vc0]
+    for _ in range(replicas - 1):
+        kcs.append(kc0.clone())
+        vcs.append(vc0.clone())
+    q = up(inp.q)
+    bt = torch.from_numpy(tables).to(device)
+    dl = torch.from_numpy(lens).to(device)
+    out = torch.empty_like(q)
+    has_write = slots is not None
+    if has_write:
+        nk, nv = up(inp.new_key), up(inp.new_value)
+        sl = torch.from_numpy(slots).to(device)
+    max_ctx = int(lens.max())
+    plan = pa.decode_plan(B, Hq, Hkv, d, bs, tables.shape[1], tdtype, max_context_len=max_ctx,
+                          partition_pages=args.partition_pages, kernel=args.kernel)
+    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
+    lib = pa.library()
+    stream = torch.cuda.current_stream(device)
+    sptr = int(stream.cuda_stream)
+    code = {"f32": 0, "f16": 1, "bf16": 2}[inp.dtype]
+    kern = pa.KERNELS[args.kernel]
+
+    # Pre-marshalled C-ABI argument lists (the timed loop only calls the library).
+    dec_args = [[out.data_ptr(), q.data_ptr(), kcs[r].data_ptr(), vcs[r].data_ptr(), bt.data_ptr(), dl.data_ptr(),
+                 B, Hq, Hkv, d, bs, tables.shape[1], inp.num_blocks, float(inp.scale), code, ws.data_ptr(),
+                 ws.numel(), max_ctx, args.partition_pages, kern, sptr] for r in range(replicas)]
+    wr_args = ([[nk.data_ptr(), nv.data_ptr(), kcs[r].data_ptr(), vcs[r].data_ptr(), sl.data_ptr(), ntok, Hkv, d, bs,
+                 inp.num_blocks, code, sptr] for r in range(replicas)] if has_write else None)
+    launches_per_step = (1 if has_write else 0) + 1 + (1 if plan.max_parts > 1 else 0)
+
+    def step(i, ev_d0=None, ev_d1=None):
+        r = i % replicas
+        if has_write and lib.pa_write_kv(*wr_args[r]) != 0:
+            raise RuntimeError(lib.pa_last_error_string().decode())
+        if ev_d0 is not None:
+            ev_d0.record(stream)
+        if lib.pa_decode_ex(*dec_args[r]) != 0:
+            raise RuntimeError(lib.pa_last_error_string().decode())
+        if ev_d1 is not None:
+            ev_d1.record(stream)
+
+    sampler = ClockSampler(gpu_selector(device))
+    sampler.start()
+    for i in range(args.warmup):
+        step(i)
+    torch.cuda.synchronize()
+    pa.check_error()
+
+    K = args.steps
+    d0 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    d1 = [torch.cuda.Event(enable_timing=True) for _ in range(K)]
+    ev_start, ev_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_begin = time.monotonic()
+    ev_start.record(stream)
+    for i in range(K):
+        step(i, d0[i], d1[i])
+    ev_end.record(stream)
+    torch.cuda.synchronize()
+    t_end = time.monotonic()
+    barrier(world)
+    sampler.stop()
+    pa.check_error()
+    elapsed_ms = ev_start.elapsed_time(ev_end)
+    decode_ms = [a.elapsed_time(b) for a, b in zip(d0, d1)]
+    elapsed_ms_max = max_over_ranks(elapsed_ms, world)
+    total_bytes = sum_over_ranks(float(step_bytes) * K, world)
+    total_seqs = sum_over_ranks(float(B) * K, world)
+    value = total_bytes / (elapsed_ms_max / 1e3) / 1e9
+    ms_per_step = elapsed_ms_max / K
+
+    # e2e: public API, inputs from pinned host memory, output back to pinned host memory
+    e2e = None
+    if not args.no_e2e:
+        def pinned(a):
+            a = np.ascontiguousarray(a)
+            t = torch.from_numpy(a.view(np.int16) if inp.dtype in ("bf16", "f16") else a).pin_memory()
+            return t.view(tdtype) if inp.dtype in ("bf16", "f16") else t
+
+        q_h = pinned(inp.q)
+        bt_h, dl_h = torch.from_numpy(tables).pin_memory(), torch.from_numpy(lens).pin_memory()
+        out_h = torch.empty(out.shape, dtype=tdtype).pin_memory()
+        if has_write:
+            nk_h, nv_h = pinned(inp.new_key), pinned(inp.new_value)
+            sl_h = torch.from_numpy(slots).pin_memory()
+        q_d, bt_d, dl_d = torch.empty_like(q), torch.empty_like(bt), torch.empty_like(dl)
+        if has_write:
+            nk_d, nv_d, sl_d = torch.empty_like(nk), torch.empty_like(nv), torch.empty_like(sl)
+        h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + dl_h.numel() * 4
+        if has_write:
+            h2d += 2 * nk_h.numel() * nk_h.element_size() + sl_h.numel() * 8
+        d2h = out_h.numel() * out_h.element_size()
+
+        def e2e_step(i):
+            r = i % replicas
+            q_d.copy_(q_h, non_blocking=True)
+            bt_d.copy_(bt_h, non_blocking=True)
+            dl_d.copy_(dl_h, non_blocking=True)
+            if has_write:
+                nk_d.copy_(nk_h, non_blocking=True)
+                nv_d.copy_(nv_h, non_blocking=True)
+                sl_d.copy_(sl_h, non_blocking=True)
+                pa.write_kv(nk_d, nv_d, kcs[r], vcs[r], sl_d)
+            pa.decode(q_d, kcs[r], vcs[r], bt_d, dl_d, scale=inp.scale, out=out, workspace=ws,
+                      max_context_len=max_ctx, partition_pages=args.partition_pages, kernel=args.kernel)
+            out_h.copy_(out, non_blocking=True)
+
+        for i in range(min(args.warmup, 20)):
+            e2e_step(i)
+        torch.cuda.synchronize()
+        Ke = max(1, min(K, args.e2e_steps))
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        barrier(world)
+        torch.cuda.synchronize()
+        e0.record(stream)
+        for i in range(Ke):
+            e2e_step(i)
+        e1.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        pa.check_error()
+        e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+        e_bytes = sum_over_ranks(float(step_bytes) * Ke, world)
+        e2e = {"value": round(e_bytes / (e_ms / 1e3) / 1e9, 2), "unit": UNIT, "steps": Ke,
+               "ms_per_step": round(e_ms / Ke, 5), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "note": "pa.write_kv + pa.decode through the Python API; inputs copied from pinned host memory "
+                       "and the output copied back every step, inside the timed region"}
+
+    peaks = measured_peaks()
+    peak = peaks.get("hbm_gbs")
+    peak_src = "of measured (MEASURED_PEAKS.json hbm_gbs)" if peak else "of fallback"
+    peak = float(peak or FALLBACK_HBM_GBS)
+    dec_avg_ms = statistics.mean(decode_ms)
+    achieved = dec_bytes / (dec_avg_ms / 1e3) / 1e9
+    roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                "frac": round(achieved / peak, 4), "traffic": stored_traffic(args.workload),
+                "kernel": "pa_decode call (paged_decode_kernel" + (" + splitkv_merge_kernel)" if plan.max_parts > 1
+                                                                  else ")"),
+                "algorithmic_bytes_per_launch": dec_bytes, "pages_touched_bytes": touched,
+                "avg_launch_ms": round(dec_avg_ms, 5), "median_launch_ms": round(statistics.median(decode_ms), 5),
+                "min_launch_ms": round(min(decode_ms), 5), "peak_source": peak_src}
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        if has_write:
+            import oracle
+
+            oracle.write_kv(inp.new_key, inp.new_value, inp.key_cache, inp.value_cache, slots)
+        r = time_oracle(inp, args.cpu_budget)
+        cpu = {"value": round(r["bytes"] / r["seconds"] / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"first {r['seqs']} of {B} sequences, all {Hq} heads ({r['rows']} output rows), "
+                         f"fp64 C oracle, single thread, {r['seconds']:.1f} s",
+               "seconds": round(r["seconds"], 2)}
+
+    clocks = sampler.summary(t_begin, t_end)
+    if rank != 0:
+        return
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAMES[inp.dtype], "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESCRIPTIONS[args.workload], "name": args.workload,
+                   "step": "pa_write_kv (new token per sequence) + pa_decode",
+                   "l2": f"{replicas} cache replicas rotated per step (pages touched per step "
+                         f"{touched / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB)",
+                   "kernel": {1: "mma", 2: "simt"}[plan.kernel], "partition_pages": plan.partition_pages,
+                   "max_parts": plan.max_parts, "grid_ctas": plan.grid_ctas,
+                   "parallelism": f"{world} independent replicas (one batch per GPU)"},
+        "pct_of_hbm_peak": round(100 * value / peak, 2),
+        "queries_per_s": round(total_seqs / (elapsed_ms_max / 1e3), 1),
+        "head_queries_per_s": round(total_seqs * Hq / (elapsed_ms_max / 1e3), 1),
+        "step_bytes": step_bytes,
+        "roofline": roofline,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": launches_per_step * K,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_reference(args, rank: int, world: int) -> None:
+    """The oracle as the reference arm: each step decodes a bounded sample of the batch on the host."""
+    if rank != 0:
+        return
+    import oracle
+
+    inp = build_batch(args.workload, rank_seed(args.seed, 0))
+    if inp.new_key is not None:
+        pos = inp.new_token_pos
+        slots = np.array([int(inp.block_tables[b, p // inp.block_size]) * inp.block_size + p % inp.block_size
+                          for b, p in enumerate(pos)], dtype=np.int64)
+        oracle.write_kv(inp.new_key, inp.new_value, inp.key_cache, inp.value_cache, slots)
+    # size the per-step sample so that warmup + steps fit in about two minutes
+    t0 = time.perf_counter()
+    oracle.decode_inputs(inp, rows=[(0, 0)])
+    t_row = max(time.perf_counter() - t0, 1e-4)
+    n_steps = args.steps + args.warmup
+    rows_per_step = int(max(1, min(inp.num_heads, 120.0 / n_steps / t_row)))
+    rows = [(0, h) for h in range(rows_per_step)]
+    L0 = int(inp.context_lens[0])
+    eb = inp.elem_bytes
+    bytes_per_step = rows_per_step / inp.num_heads * decode_bytes([L0], inp.num_heads, inp.num_kv_heads,
+                                                                  inp.head_dim, eb, inp.block_size)
+    for _ in range(args.warmup):
+        oracle.decode_inputs(inp, rows=rows)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        oracle.decode_inputs(inp, rows=rows)
+    dt = time.perf_counter() - t0
+    value = bytes_per_step * args.steps / dt / 1e9
+    sample = (f"sequence 0 (L={L0}), {rows_per_step} of {inp.num_heads} heads per step, fp64 C oracle, "
+              f"single thread")
+    line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT, "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 4),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAMES[inp.dtype],
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESCRIPTIONS[args.workload], "name": args.workload},
+            "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main(argv=None) -> None:
+    ap = argparse.ArgumentParser(description=__doc__.splitlines()[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20000)
+    ap.add_argument("--warmup", type=int, default=200)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", choices=sorted(WORKLOAD_DESCRIPTIONS), default="qwen_gqa")
+    ap.add_argument("--kernel", choices=["auto", "mma", "simt"], default="auto")
+    ap.add_argument("--partition-pages", type=int, default=0)
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--e2e-steps", type=int, default=5000)
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    args.warmup = max(args.warmup, 3)
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+
+        backend = "nccl" if torch.cuda.is_available() and args.impl == "ours" else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local_rank)
+        dist.init_process_group(backend)
+    try:
+        if args.impl == "reference":
+            run_reference(args, rank, world)
+        else:
+            run_ours(args, rank, world, local_rank)
+    finally:
+        if world > 1:
+            import torch.distributed as dist
+
+            dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,244 @@
+/*
+ * Paged decode attention on GB300 (sm_103a) — C ABI.
+ *
+ * The library implements single-step decode attention over a paged KV cache
+ * (PagedAttention) and the two cache-maintenance kernels around it, plus a
+ * host block pool that produces block tables, slot mappings and copy-on-write
+ * pairs.  All signatures use plain C types: device buffers are raw pointers,
+ * a stream is a `cudaStream_t` passed as `void*` (NULL = the legacy default
+ * stream), sizes are ints.
+ *
+ * Conventions shared by every call:
+ *  - Every call returns an int status (PA_OK = 0, else one of PA_ERR_*);
+ *    pa_last_error_string() gives a thread-local message for the last failure.
+ *  - Device buffers are owned by the caller; the library never allocates or
+ *    frees device memory in these calls.
+ *  - Kernel calls are asynchronous on the given stream.  Argument and launch
+ *    errors come back synchronously.  Bad data found by a kernel (a block id
+ *    outside the pool, a slot past the pool, a context longer than its table)
+ *    does not fault: the kernel skips the access and sets a bit in a device
+ *    error word, which pa_check_error() reads (it synchronises the stream).
+ *  - Cache layout (MiniPaged-Qwen, section 8.2): key_cache and value_cache are
+ *    contiguous [num_blocks, num_kv_heads, block_size, head_dim] arrays of the
+ *    element type `dtype`; slice [pb, kvh, :, :] of one block and head is
+ *    contiguous.  query/out are [num_seqs, num_heads, head_dim], key/value
+ *    of the write are [num_tokens, num_kv_heads, head_dim], all contiguous.
+ *  - dtype is one of PA_F32, PA_F16, PA_BF16; query, caches and out share it.
+ */
+#ifndef PAGED_KV_GB300_PA_H
+#define PAGED_KV_GB300_PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ------------------------------------------------------------------- */
+enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,    /* a null pointer, a bad size, misalignment, ... */
+    PA_ERR_UNSUPPORTED = 2,    /* head_dim / block_size / dtype combination not compiled */
+    PA_ERR_CUDA = 3,           /* a CUDA runtime call failed */
+    PA_ERR_POOL_EXHAUSTED = 4, /* the block pool has no free block (state unchanged) */
+    PA_ERR_BAD_TABLE = 5,      /* a block id outside [0, num_blocks) was met */
+    PA_ERR_BAD_SLOT = 6,       /* a slot at or past num_blocks * block_size was met */
+    PA_ERR_BAD_CONTEXT = 7,    /* a context length < 0 or longer than its block table */
+    PA_ERR_TIMEOUT = 8,        /* a kernel-internal wait gave up (should never happen) */
+    PA_ERR_NOT_FOUND = 9       /* unknown sequence id, or a block id not in use */
+};
+
+/* ---- element types ------------------------------------------------------------------- */
+enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 };
+
+/* ---- decode kernel choice (pa_decode_ex) ---------------------------------------------- */
+enum {
+    PA_KERNEL_AUTO = 0, /* tensor-core kernel for f16/bf16, CUDA-core kernel for f32 */
+    PA_KERNEL_MMA = 1,  /* f16/bf16 only: QK^T and PV on warp-level tensor-core MMA */
+    PA_KERNEL_SIMT = 2  /* all dtypes: CUDA-core FMA */
+};
+
+/* Thread-local message describing the last non-OK status of this thread. */
+const char* pa_last_error_string(void);
+
+/* Library version string. */
+const char* pa_version(void);
+
+/*
+ * Synchronise `stream`, then read and clear the device error word of the
+ * current device.  Returns PA_OK, or the first of PA_ERR_BAD_TABLE,
+ * PA_ERR_BAD_SLOT, PA_ERR_BAD_CONTEXT, PA_ERR_TIMEOUT whose bit was set by a
+ * kernel since the last check, or PA_ERR_CUDA if the stream failed.
+ */
+int pa_check_error(void* stream);
+
+/*
+ * pa_write_kv — the reshape-and-cache writer (MiniPaged-Qwen, sections 8.1-8.2:
+ * append_token returns the token's linear slot; the cache write kernel stores
+ * the token's K/V there).
+ *
+ * For every token t and kv head h:
+ *     key_cache  [slot / block_size, h, slot % block_size, :] = key  [t, h, :]
+ *     value_cache[slot / block_size, h, slot % block_size, :] = value[t, h, :]
+ * where slot = slot_mapping[t] (device int64 array of num_tokens entries).
+ * A negative slot means "no write" (padding).  A slot >= num_blocks *
+ * block_size is skipped and sets PA_ERR_BAD_SLOT in the device error word.
+ * Bit-exact: elements are copied as raw bytes.  Slots of one call must be
+ * distinct (duplicate slots race).  num_tokens == 0 is a no-op.
+ */
+int pa_write_kv(const void* key, const void* value, void* key_cache, void* value_cache,
+                const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
+                int block_size, int num_blocks, int dtype, void* stream);
+
+/*
+ * pa_copy_blocks — copy-on-write block copy (vLLM and PagedAttention page,
+ * copy-on-write section: a branch that appends to a shared, non-full tail
+ * block first copies it into a private block).
+ *
+ * src_dst_pairs is a device int64 array [num_pairs, 2] of (src, dst) block
+ * ids.  For every pair, block dst of key_cache and of value_cache becomes a
+ * byte copy of block src (all kv heads, all slots).  The dst ids of one call
+ * must be distinct and no dst may be a src of the same call (otherwise the
+ * result depends on scheduling).  An id outside [0, num_blocks) skips the pair
+ * and sets PA_ERR_BAD_TABLE in the device error word.  num_pairs == 0 is a
+ * no-op.
+ */
+int pa_copy_blocks(void* key_cache, void* value_cache, const int64_t* src_dst_pairs, int num_pairs,
+                   int num_kv_heads, int head_dim, int block_size, int num_blocks, int dtype,
+                   void* stream);
+
+/*
+ * pa_decode — single-step decode attention over the paged cache
+ * (MiniPaged-Qwen, section 1 formula, sections 5.1-5.2 and 6.2; GQA mapping of
+ * section 9.1).
+ *
+ * For every sequence b and query head qh, with g = num_heads / num_kv_heads,
+ * kvh = qh / g and L = context_lens[b]:
+ *     pos -> logical block pos / block_size -> pb = block_tables[b, that block],
+ *     k_pos = key_cache[pb, kvh, pos % block_size, :], v_pos likewise,
+ *     out[b, qh, :] = sum_pos softmax_pos(scale * <query[b, qh, :], k_pos>) * v_pos
+ * with the softmax taken over all L positions (online: running max and
+ * running denominator, fp32 accumulation).  L == 0 gives a zero row.
+ *
+ *  block_tables   device int32 [num_seqs, max_blocks_per_seq]; only the first
+ *                 ceil(L / block_size) entries of a row are read.
+ *  context_lens   device int32 [num_seqs].
+ *  scale          softmax scale, usually 1/sqrt(head_dim).
+ *  workspace      device scratch for the split-KV partials, or NULL.  With
+ *                 NULL every (sequence, kv head) is done by one CTA in one
+ *                 pass.  Otherwise it must hold workspace_bytes >= the size
+ *                 pa_decode_workspace_size() returns for the same arguments
+ *                 to use the default plan; no initialisation is needed.  A
+ *                 smaller workspace is allowed: the call then uses longer
+ *                 partitions.  256-byte aligned.  Calls that share a workspace
+ *                 must not overlap on the GPU.
+ * Requires num_heads % num_kv_heads == 0, head_dim in {64, 128, 256},
+ * block_size in {16, 32} (f32: head_dim in {64, 128}), 16-byte aligned caches,
+ * 4-byte aligned query/out, num_blocks * num_kv_heads * block_size < 2^31.
+ */
+int pa_decode(void* out, const void* query, const void* key_cache, const void* value_cache,
+              const int32_t* block_tables, const int32_t* context_lens, int num_seqs, int num_heads,
+              int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
+              float scale, int dtype, void* workspace, size_t workspace_bytes, void* stream);
+
+/*
+ * pa_decode_ex — pa_decode with explicit planning controls.
+ *  max_context_len  an upper bound of context_lens (0 = max_blocks_per_seq *
+ *                   block_size); only used to size the partitions.  A context
+ *                   longer than this bound sets PA_ERR_BAD_CONTEXT.
+ *  partition_pages  pages (blocks) per CTA partition: 0 = heuristic, > 0 =
+ *                   exactly this (needs a workspace when it splits a context),
+ *                   < 0 = one partition per context (no workspace used).
+ *  kernel           PA_KERNEL_AUTO / PA_KERNEL_MMA / PA_KERNEL_SIMT.
+ */
+int pa_decode_ex(void* out, const void* query, const void* key_cache, const void* value_cache,
+                 const int32_t* block_tables, const int32_t* context_lens, int num_seqs, int num_heads,
+                 int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
+                 float scale, int dtype, void* workspace, size_t workspace_bytes, int max_context_len,
+                 int partition_pages, int kernel, void* stream);
+
+/* The partition plan pa_decode_ex would use on the current device. */
+typedef struct pa_decode_plan {
+    int kernel;            /* PA_KERNEL_MMA or PA_KERNEL_SIMT */
+    int partition_pages;   /* pages per CTA partition */
+    int max_parts;         /* partitions of the longest context */
+    int heads_per_cta;     /* query heads handled by one CTA */
+    int grid_ctas;         /* CTAs launched */
+    int threads_per_cta;
+    int smem_bytes;        /* dynamic shared memory per CTA */
+    size_t workspace_bytes; /* workspace this plan needs (0 when max_parts == 1) */
+} pa_decode_plan;
+
+int pa_decode_make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                        int max_blocks_per_seq, int dtype, size_t workspace_bytes, int max_context_len,
+                        int partition_pages, int kernel, pa_decode_plan* plan);
+
+/*
+ * Workspace bytes pa_decode needs to use its own (heuristic) partition plan
+ * on the current device, for these sizes.  0 means one pass, no workspace.
+ */
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                                int block_size, int max_blocks_per_seq, int dtype);
+
+/* ---- host block pool ----------------------------------------------------------------- */
+/*
+ * Fixed-size block allocator with reference counts, fork and copy-on-write
+ * append.  Semantics of the BlockPool simulation on the vLLM and
+ * PagedAttention page (section "最小分页与 COW 模拟"):
+ *  - allocation takes the LAST id of the free list (LIFO); the list starts as
+ *    0..num_blocks-1, or as `free_order` when given;
+ *  - append: a fresh block if the sequence has none or its tail block is full
+ *    (no copy, even if that full tail is shared); otherwise, if the tail is
+ *    shared (refcount > 1), a private block is allocated, the shared tail loses
+ *    one reference and the caller must copy src -> dst (cow_src/cow_dst)
+ *    before writing the token; otherwise the token goes into the tail in place;
+ *  - fork: the child lists the same blocks; each block's refcount + 1;
+ *  - release: each block of the sequence loses one reference; a block at zero
+ *    goes back to the end of the free list, in table order.
+ * Every failing call leaves the pool unchanged (rollback).  Not thread-safe:
+ * one pool per thread, or external locking.  Host memory only.
+ */
+typedef struct pa_pool pa_pool;
+
+int pa_pool_create(int num_blocks, int block_size, const int32_t* free_order, pa_pool** out);
+void pa_pool_destroy(pa_pool* pool);
+int pa_seq_create(pa_pool* pool, int64_t* seq_id);
+/* slot = pb * block_size + offset of the new token; cow_src/cow_dst = -1 when no copy is needed. */
+int pa_seq_append(pa_pool* pool, int64_t seq_id, int64_t* slot, int64_t* cow_src, int64_t* cow_dst);
+/*
+ * Append one token to each of `n` sequences (in order).  slots[n] receive the
+ * slots; cow_pairs (capacity n pairs, [n, 2] int64) receives the copy pairs in
+ * order and *num_cow their count.  All-or-nothing: on failure nothing changed.
+ */
+int pa_seq_append_batch(pa_pool* pool, const int64_t* seq_ids, int n, int64_t* slots, int64_t* cow_pairs,
+                        int* num_cow);
+int pa_seq_fork(pa_pool* pool, int64_t parent_id, int64_t* child_id);
+int pa_seq_release(pa_pool* pool, int64_t seq_id);
+int pa_seq_length(const pa_pool* pool, int64_t seq_id, int64_t* length);
+/*
+ * Host export of block tables: tables [n, max_blocks] int32 (unused entries
+ * -1) and lens [n] int32 for the given sequence ids.  PA_ERR_INVALID_ARG if a
+ * table is wider than max_blocks.  The caller uploads them.
+ */
+int pa_pool_block_tables(const pa_pool* pool, const int64_t* seq_ids, int n, int32_t* tables, int max_blocks,
+                         int32_t* lens);
+int pa_pool_num_free(const pa_pool* pool);
+int pa_pool_num_blocks(const pa_pool* pool);
+int pa_pool_block_size(const pa_pool* pool);
+/* Reference count of `block` (0 if free); -1 if the id is outside the pool. */
+int pa_pool_refcount(const pa_pool* pool, int32_t block);
+/*
+ * Check the pool's invariants (free and used blocks partition the pool,
+ * refcount = number of tables holding the block, every table holds
+ * ceil(len / block_size) blocks).  PA_OK or PA_ERR_INVALID_ARG with a message.
+ */
+int pa_pool_check_invariants(const pa_pool* pool);
+/* Copy the free list (bottom first) into out[capacity]; returns its length or -1. */
+int pa_pool_free_list(const pa_pool* pool, int32_t* out, int capacity);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGED_KV_GB300_PA_H */

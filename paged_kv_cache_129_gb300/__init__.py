@@ -1,0 +1,28 @@
+"""Paged decode attention (PagedAttention) for GB300, behind a C ABI.
+
+The compute path is the CUDA library built from ``csrc/`` (see
+``include/pa.h``); this package only marshals torch tensors into it.
+"""
+from .binding import (  # noqa: F401
+    KERNELS,
+    LIB_PATH,
+    BlockPool,
+    DecodePlan,
+    PAError,
+    PoolExhausted,
+    check_error,
+    copy_blocks,
+    decode,
+    decode_plan,
+    decode_workspace_size,
+    library,
+    version,
+    write_kv,
+)
+
+
+def build(force: bool = False) -> str:
+    """Compile the CUDA library in-tree (nvcc, sm_103a)."""
+    from .build import build as _build
+
+    return _build(force=force)

@@ -1,0 +1,312 @@
+"""Thin ctypes binding of the C ABI in ``include/pa.h``.
+
+Argument marshalling only: every step of the path runs in the CUDA library
+(``_build/libpagedkv.so``).  PyTorch supplies device memory and streams.  There
+is no fallback: if the library is missing, the first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+from typing import Optional, Sequence, Tuple
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "_build", "libpagedkv.so")
+
+PA_OK = 0
+STATUS_NAMES = {
+    0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED", 3: "PA_ERR_CUDA", 4: "PA_ERR_POOL_EXHAUSTED",
+    5: "PA_ERR_BAD_TABLE", 6: "PA_ERR_BAD_SLOT", 7: "PA_ERR_BAD_CONTEXT", 8: "PA_ERR_TIMEOUT", 9: "PA_ERR_NOT_FOUND",
+}
+PA_F32, PA_F16, PA_BF16 = 0, 1, 2
+KERNELS = {"auto": 0, "mma": 1, "simt": 2}
+_TORCH_DTYPES = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+class PAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+
+
+class PoolExhausted(PAError, MemoryError):
+    pass
+
+
+class DecodePlan(ctypes.Structure):
+    _fields_ = [("kernel", ctypes.c_int), ("partition_pages", ctypes.c_int), ("max_parts", ctypes.c_int),
+                ("heads_per_cta", ctypes.c_int), ("grid_ctas", ctypes.c_int), ("threads_per_cta", ctypes.c_int),
+                ("smem_bytes", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t)]
+
+    def as_dict(self) -> dict:
+        return {name: getattr(self, name) for name, _ in self._fields_}
+
+
+# (name, restype, argtypes) of every exported function.
+_P, _I, _I64, _SZ, _F = ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+_SIGNATURES = [
+    ("pa_last_error_string", ctypes.c_char_p, []),
+    ("pa_version", ctypes.c_char_p, []),
+    ("pa_check_error", _I, [_P]),
+    ("pa_write_kv", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    ("pa_copy_blocks", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    ("pa_decode", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    ("pa_decode_ex", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _I, _I, _I, _P]),
+    ("pa_decode_make_plan", _I, [_I, _I, _I, _I, _I, _I, _I, _SZ, _I, _I, _I, ctypes.POINTER(DecodePlan)]),
+    ("pa_decode_workspace_size", _SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    ("pa_pool_create", _I, [_I, _I, _P, ctypes.POINTER(_P)]),
+    ("pa_pool_destroy", None, [_P]),
+    ("pa_seq_create", _I, [_P, ctypes.POINTER(_I64)]),
+    ("pa_seq_append", _I, [_P, _I64, ctypes.POINTER(_I64), ctypes.POINTER(_I64), ctypes.POINTER(_I64)]),
+    ("pa_seq_append_batch", _I, [_P, _P, _I, _P, _P, ctypes.POINTER(_I)]),
+    ("pa_seq_fork", _I, [_P, _I64, ctypes.POINTER(_I64)]),
+    ("pa_seq_release", _I, [_P, _I64]),
+    ("pa_seq_length", _I, [_P, _I64, ctypes.POINTER(_I64)]),
+    ("pa_pool_block_tables", _I, [_P, _P, _I, _P, _I, _P]),
+    ("pa_pool_num_free", _I, [_P]),
+    ("pa_pool_num_blocks", _I, [_P]),
+    ("pa_pool_block_size", _I, [_P]),
+    ("pa_pool_refcount", _I, [_P, ctypes.c_int32]),
+    ("pa_pool_check_invariants", _I, [_P]),
+    ("pa_pool_free_list", _I, [_P, _P, _I]),
+]
+
+
+def library() -> ctypes.CDLL:
+    """Load the CUDA library (raises if it has not been built)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            if not os.path.exists(LIB_PATH):
+                raise RuntimeError(f"CUDA library not built: {LIB_PATH} is missing (run __graft_entry__.build())")
+            lib = ctypes.CDLL(LIB_PATH)
+            for name, res, args in _SIGNATURES:
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+        return _lib
+
+
+def _check(status: int) -> None:
+    if status != PA_OK:
+        msg = library().pa_last_error_string()
+        msg = msg.decode() if msg else ""
+        if status == 4:
+            raise PoolExhausted(status, msg)
+        raise PAError(status, msg)
+
+
+def _stream_ptr(stream, device: torch.device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    try:
+        return _TORCH_DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}") from None
+
+
+def _need(cond: bool, what: str) -> None:
+    if not cond:
+        raise ValueError(what)
+
+
+def _cuda(t: torch.Tensor, name: str) -> None:
+    _need(t.is_cuda, f"{name} must be a CUDA tensor")
+    _need(t.is_contiguous(), f"{name} must be contiguous")
+
+
+def version() -> str:
+    return library().pa_version().decode()
+
+
+def check_error(stream=None, device=None) -> None:
+    """Synchronise the stream and raise if a kernel flagged bad data since the last check."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    _check(library().pa_check_error(_stream_ptr(stream, dev)))
+
+
+def write_kv(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+             slot_mapping: torch.Tensor, stream=None) -> None:
+    """``pa_write_kv``: scatter key/value ``[T, H_kv, d]`` into the caches at ``slot_mapping`` (int64)."""
+    for name, t in (("key", key), ("value", value), ("key_cache", key_cache), ("value_cache", value_cache),
+                    ("slot_mapping", slot_mapping)):
+        _cuda(t, name)
+    _need(key_cache.dim() == 4 and value_cache.shape == key_cache.shape, "caches must be [N, H_kv, bs, d]")
+    num_blocks, hkv, bs, d = key_cache.shape
+    _need(key.shape == value.shape and key.dim() == 3 and key.shape[1:] == (hkv, d), "key/value must be [T, H_kv, d]")
+    _need(slot_mapping.dtype == torch.int64 and slot_mapping.numel() == key.shape[0], "slot_mapping: int64 [T]")
+    _need(key.dtype == value.dtype == key_cache.dtype == value_cache.dtype, "dtypes must match")
+    _check(library().pa_write_kv(key.data_ptr(), value.data_ptr(), key_cache.data_ptr(), value_cache.data_ptr(),
+                                 slot_mapping.data_ptr(), key.shape[0], hkv, d, bs, num_blocks,
+                                 _dtype_code(key_cache), _stream_ptr(stream, key_cache.device)))
+
+
+def copy_blocks(key_cache: torch.Tensor, value_cache: torch.Tensor, src_dst_pairs: torch.Tensor, stream=None) -> None:
+    """``pa_copy_blocks``: for each (src, dst) row of ``src_dst_pairs`` (int64 [n, 2]) copy block src -> dst."""
+    for name, t in (("key_cache", key_cache), ("value_cache", value_cache), ("src_dst_pairs", src_dst_pairs)):
+        _cuda(t, name)
+    _need(key_cache.dim() == 4 and value_cache.shape == key_cache.shape, "caches must be [N, H_kv, bs, d]")
+    _need(src_dst_pairs.dtype == torch.int64 and (src_dst_pairs.numel() % 2 == 0), "pairs: int64 [n, 2]")
+    num_blocks, hkv, bs, d = key_cache.shape
+    _check(library().pa_copy_blocks(key_cache.data_ptr(), value_cache.data_ptr(), src_dst_pairs.data_ptr(),
+                                    src_dst_pairs.numel() // 2, hkv, d, bs, num_blocks, _dtype_code(key_cache),
+                                    _stream_ptr(stream, key_cache.device)))
+
+
+def decode_plan(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                max_blocks_per_seq: int, dtype: torch.dtype, workspace_bytes: int = 1 << 62,
+                max_context_len: int = 0, partition_pages: int = 0, kernel: str = "auto") -> DecodePlan:
+    """The partition plan ``pa_decode_ex`` would use on the current device."""
+    plan = DecodePlan()
+    _check(library().pa_decode_make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                         max_blocks_per_seq, _TORCH_DTYPES[dtype], workspace_bytes, max_context_len,
+                                         partition_pages, KERNELS[kernel], ctypes.byref(plan)))
+    return plan
+
+
+def decode_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                          max_blocks_per_seq: int, dtype: torch.dtype) -> int:
+    return int(library().pa_decode_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                                  max_blocks_per_seq, _TORCH_DTYPES[dtype]))
+
+
+def decode(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor, block_tables: torch.Tensor,
+           context_lens: torch.Tensor, scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+           workspace: Optional[torch.Tensor] = None, max_context_len: int = 0, partition_pages: int = 0,
+           kernel: str = "auto", stream=None) -> torch.Tensor:
+    """``pa_decode_ex``: paged decode attention; returns ``out`` ``[B, H_q, d]``.
+
+    ``workspace`` (any dtype, contiguous, on the same device) enables the
+    split-KV partitions; ``None`` runs one partition per context.
+    """
+    for name, t in (("query", query), ("key_cache", key_cache), ("value_cache", value_cache),
+                    ("block_tables", block_tables), ("context_lens", context_lens)):
+        _cuda(t, name)
+    _need(key_cache.dim() == 4 and value_cache.shape == key_cache.shape, "caches must be [N, H_kv, bs, d]")
+    num_blocks, hkv, bs, d = key_cache.shape
+    _need(query.dim() == 3 and query.shape[2] == d, "query must be [B, H_q, d]")
+    b, hq, _ = query.shape
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == b,
+          "block_tables: int32 [B, max_blocks]")
+    _need(context_lens.dtype == torch.int32 and context_lens.numel() == b, "context_lens: int32 [B]")
+    _need(query.dtype == key_cache.dtype == value_cache.dtype, "query and caches must share a dtype")
+    if out is None:
+        out = torch.empty_like(query)
+    _cuda(out, "out")
+    _need(out.shape == query.shape and out.dtype == query.dtype, "out must match query")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    ws_ptr, ws_bytes = 0, 0
+    if workspace is not None:
+        _cuda(workspace, "workspace")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check(library().pa_decode_ex(out.data_ptr(), query.data_ptr(), key_cache.data_ptr(), value_cache.data_ptr(),
+                                  block_tables.data_ptr(), context_lens.data_ptr(), b, hq, hkv, d, bs,
+                                  block_tables.shape[1], num_blocks, float(scale), _dtype_code(query), ws_ptr or None,
+                                  ws_bytes, max_context_len, partition_pages, KERNELS[kernel],
+                                  _stream_ptr(stream, query.device)))
+    return out
+
+
+class BlockPool:
+    """Host block pool (``pa_pool``): free list, refcounts, fork, copy-on-write append."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order: Optional[Sequence[int]] = None):
+        lib = library()
+        handle = _P()
+        order = None
+        if free_order is not None:
+            order = (ctypes.c_int32 * num_blocks)(*[int(x) for x in free_order])
+        _check(lib.pa_pool_create(num_blocks, block_size, ctypes.cast(order, _P) if order is not None else None,
+                                  ctypes.byref(handle)))
+        self._h = handle
+        self._lib = lib
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            self._lib.pa_pool_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def create(self) -> int:
+        sid = _I64()
+        _check(self._lib.pa_seq_create(self._h, ctypes.byref(sid)))
+        return sid.value
+
+    def append(self, seq_id: int) -> Tuple[int, Optional[Tuple[int, int]]]:
+        """Append one token; returns (slot, (cow_src, cow_dst) or None)."""
+        slot, src, dst = _I64(), _I64(), _I64()
+        _check(self._lib.pa_seq_append(self._h, seq_id, ctypes.byref(slot), ctypes.byref(src), ctypes.byref(dst)))
+        return slot.value, ((src.value, dst.value) if src.value >= 0 else None)
+
+    def append_batch(self, seq_ids):
+        """Append one token to each sequence; returns (slots int64 [n], cow pairs int64 [k, 2]) as numpy."""
+        import numpy as np
+
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = ids.size
+        slots = np.empty(n, dtype=np.int64)
+        pairs = np.empty((max(n, 1), 2), dtype=np.int64)
+        k = _I()
+        _check(self._lib.pa_seq_append_batch(self._h, ids.ctypes.data, n, slots.ctypes.data, pairs.ctypes.data,
+                                             ctypes.byref(k)))
+        return slots, pairs[:k.value].copy()
+
+    def fork(self, seq_id: int) -> int:
+        child = _I64()
+        _check(self._lib.pa_seq_fork(self._h, seq_id, ctypes.byref(child)))
+        return child.value
+
+    def release(self, seq_id: int) -> None:
+        _check(self._lib.pa_seq_release(self._h, seq_id))
+
+    def length(self, seq_id: int) -> int:
+        n = _I64()
+        _check(self._lib.pa_seq_length(self._h, seq_id, ctypes.byref(n)))
+        return n.value
+
+    def block_tables(self, seq_ids, max_blocks: int):
+        """Host int32 tables [n, max_blocks] (-1 padded) and int32 lengths [n] (numpy)."""
+        import numpy as np
+
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        tables = np.empty((ids.size, max_blocks), dtype=np.int32)
+        lens = np.empty(ids.size, dtype=np.int32)
+        _check(self._lib.pa_pool_block_tables(self._h, ids.ctypes.data, ids.size, tables.ctypes.data, max_blocks,
+                                              lens.ctypes.data))
+        return tables, lens
+
+    def num_free(self) -> int:
+        return self._lib.pa_pool_num_free(self._h)
+
+    def refcount(self, block: int) -> int:
+        return self._lib.pa_pool_refcount(self._h, block)
+
+    def free_list(self):
+        import numpy as np
+
+        out = np.empty(self.num_blocks, dtype=np.int32)
+        n = self._lib.pa_pool_free_list(self._h, out.ctypes.data, self.num_blocks)
+        return out[:n].tolist()
+
+    def check_invariants(self) -> None:
+        _check(self._lib.pa_pool_check_invariants(self._h))

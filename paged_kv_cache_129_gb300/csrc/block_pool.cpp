@@ -1,0 +1,315 @@
+// Host block pool: free list, reference counts, fork and copy-on-write append.
+//
+// Semantics follow the BlockPool simulation on the "vLLM 与 PagedAttention"
+// page (section 最小分页与 COW 模拟): LIFO free list, a fresh block when the
+// tail is absent or full, a private copy when the tail is shared and not full,
+// in-place otherwise.  Release (absent there) drops one reference per block and
+// returns blocks that reach zero to the end of the free list, in table order.
+// Instead of the simulation's token lists the pool keeps a fill count per
+// block, which is all the allocation decisions need.
+//
+// Every failing call leaves the pool exactly as it was: single appends check
+// before mutating; batch appends keep an undo log.
+#include <algorithm>
+#include <cstdint>
+#include <cstring>
+#include <new>
+#include <unordered_map>
+#include <vector>
+
+#include "pa.h"
+#include "pa_internal.h"
+
+struct pa_pool {
+    struct Seq {
+        std::vector<int32_t> table;
+        int64_t length = 0;
+    };
+    int num_blocks = 0;
+    int block_size = 0;
+    std::vector<int32_t> free_list;  // back() is the next block handed out
+    std::vector<int32_t> refs;       // per block; 0 = free
+    std::vector<int32_t> fill;       // tokens stored in the block
+    std::unordered_map<int64_t, Seq> seqs;
+    int64_t next_id = 0;
+};
+
+namespace {
+
+enum AppendKind { kInPlace = 0, kFreshBlock = 1, kCopyOnWrite = 2 };
+
+struct AppendRecord {
+    int64_t seq_id;
+    int kind;
+    int32_t block;      // fresh or private block (kinds 1, 2)
+    int32_t shared;     // the shared tail that was copied (kind 2)
+};
+
+// Allocation decision for one append; checks only (no mutation).
+int plan_append(const pa_pool* p, const pa_pool::Seq& s, int* kind) {
+    if (s.table.empty() || p->fill[s.table.back()] == p->block_size) {
+        *kind = kFreshBlock;
+    } else if (p->refs[s.table.back()] > 1) {
+        *kind = kCopyOnWrite;
+    } else {
+        *kind = kInPlace;
+    }
+    if (*kind != kInPlace && p->free_list.empty()) return PA_ERR_POOL_EXHAUSTED;
+    return PA_OK;
+}
+
+int32_t take_block(pa_pool* p) {
+    int32_t b = p->free_list.back();
+    p->free_list.pop_back();
+    p->refs[b] = 1;
+    p->fill[b] = 0;
+    return b;
+}
+
+void give_back(pa_pool* p, int32_t b) {
+    p->refs[b] = 0;
+    p->fill[b] = 0;
+    p->free_list.push_back(b);
+}
+
+// Performs an append whose plan succeeded.  Returns the record.
+AppendRecord do_append(pa_pool* p, int64_t seq_id, pa_pool::Seq& s, int kind, int64_t* slot) {
+    AppendRecord rec{seq_id, kind, -1, -1};
+    if (kind == kFreshBlock) {
+        rec.block = take_block(p);
+        s.table.push_back(rec.block);
+    } else if (kind == kCopyOnWrite) {
+        rec.shared = s.table.back();
+        rec.block = take_block(p);
+        p->fill[rec.block] = p->fill[rec.shared];  // the private copy holds the same tokens
+        p->refs[rec.shared] -= 1;
+        s.table.back() = rec.block;
+    }
+    const int32_t tail = s.table.back();
+    *slot = static_cast<int64_t>(tail) * p->block_size + p->fill[tail];
+    p->fill[tail] += 1;
+    s.length += 1;
+    return rec;
+}
+
+void undo_append(pa_pool* p, const AppendRecord& rec) {
+    pa_pool::Seq& s = p->seqs[rec.seq_id];
+    const int32_t tail = s.table.back();
+    p->fill[tail] -= 1;
+    s.length -= 1;
+    if (rec.kind == kFreshBlock) {
+        s.table.pop_back();
+        give_back(p, rec.block);
+    } else if (rec.kind == kCopyOnWrite) {
+        s.table.back() = rec.shared;
+        p->refs[rec.shared] += 1;
+        give_back(p, rec.block);
+    }
+}
+
+pa_pool::Seq* find_seq(pa_pool* p, int64_t id) {
+    auto it = p->seqs.find(id);
+    return it == p->seqs.end() ? nullptr : &it->second;
+}
+
+const pa_pool::Seq* find_seq(const pa_pool* p, int64_t id) {
+    auto it = p->seqs.find(id);
+    return it == p->seqs.end() ? nullptr : &it->second;
+}
+
+}  // namespace
+
+extern "C" {
+
+int pa_pool_create(int num_blocks, int block_size, const int32_t* free_order, pa_pool** out) {
+    if (!out) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_create: out is NULL");
+    *out = nullptr;
+    if (num_blocks < 0 || block_size <= 0)
+        return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_create: num_blocks=%d block_size=%d", num_blocks, block_size);
+    pa_pool* p = new (std::nothrow) pa_pool();
+    if (!p) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_create: out of host memory");
+    p->num_blocks = num_blocks;
+    p->block_size = block_size;
+    p->refs.assign(num_blocks, 0);
+    p->fill.assign(num_blocks, 0);
+    p->free_list.resize(num_blocks);
+    if (free_order) {
+        std::vector<char> seen(num_blocks, 0);
+        for (int i = 0; i < num_blocks; ++i) {
+            int32_t b = free_order[i];
+            if (b < 0 || b >= num_blocks || seen[b]) {
+                delete p;
+                return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_create: free_order is not a permutation (entry %d)", i);
+            }
+            seen[b] = 1;
+            p->free_list[i] = b;
+        }
+    } else {
+        for (int i = 0; i < num_blocks; ++i) p->free_list[i] = i;
+    }
+    *out = p;
+    return PA_OK;
+}
+
+void pa_pool_destroy(pa_pool* pool) { delete pool; }
+
+int pa_seq_create(pa_pool* pool, int64_t* seq_id) {
+    if (!pool || !seq_id) return pa::fail(PA_ERR_INVALID_ARG, "pa_seq_create: NULL argument");
+    const int64_t id = pool->next_id++;
+    pool->seqs.emplace(id, pa_pool::Seq{});
+    *seq_id = id;
+    return PA_OK;
+}
+
+int pa_seq_append(pa_pool* pool, int64_t seq_id, int64_t* slot, int64_t* cow_src, int64_t* cow_dst) {
+    if (!pool || !slot) return pa::fail(PA_ERR_INVALID_ARG, "pa_seq_append: NULL argument");
+    pa_pool::Seq* s = find_seq(pool, seq_id);
+    if (!s) return pa::fail(PA_ERR_NOT_FOUND, "pa_seq_append: unknown sequence %lld", (long long)seq_id);
+    int kind = 0;
+    if (plan_append(pool, *s, &kind) != PA_OK)
+        return pa::fail(PA_ERR_POOL_EXHAUSTED, "KV pool exhausted (sequence %lld)", (long long)seq_id);
+    AppendRecord rec = do_append(pool, seq_id, *s, kind, slot);
+    if (cow_src) *cow_src = rec.kind == kCopyOnWrite ? rec.shared : -1;
+    if (cow_dst) *cow_dst = rec.kind == kCopyOnWrite ? rec.block : -1;
+    return PA_OK;
+}
+
+int pa_seq_append_batch(pa_pool* pool, const int64_t* seq_ids, int n, int64_t* slots, int64_t* cow_pairs,
+                        int* num_cow) {
+    if (!pool || n < 0 || (n > 0 && (!seq_ids || !slots || !cow_pairs)) || !num_cow)
+        return pa::fail(PA_ERR_INVALID_ARG, "pa_seq_append_batch: bad arguments");
+    std::vector<AppendRecord> log;
+    log.reserve(n);
+    int cows = 0;
+    for (int i = 0; i < n; ++i) {
+        pa_pool::Seq* s = find_seq(pool, seq_ids[i]);
+        int kind = 0;
+        int status = s ? plan_append(pool, *s, &kind) : PA_ERR_NOT_FOUND;
+        if (status != PA_OK) {
+            for (auto it = log.rbegin(); it != log.rend(); ++it) undo_append(pool, *it);
+            if (status == PA_ERR_NOT_FOUND)
+                return pa::fail(status, "pa_seq_append_batch: unknown sequence %lld", (long long)seq_ids[i]);
+            return pa::fail(status, "KV pool exhausted at batch entry %d (nothing appended)", i);
+        }
+        log.push_back(do_append(pool, seq_ids[i], *s, kind, &slots[i]));
+        if (log.back().kind == kCopyOnWrite) {
+            cow_pairs[2 * cows] = log.back().shared;
+            cow_pairs[2 * cows + 1] = log.back().block;
+            ++cows;
+        }
+    }
+    *num_cow = cows;
+    return PA_OK;
+}
+
+int pa_seq_fork(pa_pool* pool, int64_t parent_id, int64_t* child_id) {
+    if (!pool || !child_id) return pa::fail(PA_ERR_INVALID_ARG, "pa_seq_fork: NULL argument");
+    const pa_pool::Seq* parent = find_seq(pool, parent_id);
+    if (!parent) return pa::fail(PA_ERR_NOT_FOUND, "pa_seq_fork: unknown sequence %lld", (long long)parent_id);
+    pa_pool::Seq child = *parent;  // copy before emplace may rehash
+    for (int32_t b : child.table) pool->refs[b] += 1;
+    const int64_t id = pool->next_id++;
+    pool->seqs.emplace(id, std::move(child));
+    *child_id = id;
+    return PA_OK;
+}
+
+int pa_seq_release(pa_pool* pool, int64_t seq_id) {
+    if (!pool) return pa::fail(PA_ERR_INVALID_ARG, "pa_seq_release: NULL pool");
+    auto it = pool->seqs.find(seq_id);
+    if (it == pool->seqs.end())
+        return pa::fail(PA_ERR_NOT_FOUND, "pa_seq_release: unknown sequence %lld", (long long)seq_id);
+    for (int32_t b : it->second.table) {
+        pool->refs[b] -= 1;
+        if (pool->refs[b] == 0) give_back(pool, b);
+    }
+    pool->seqs.erase(it);
+    return PA_OK;
+}
+
+int pa_seq_length(const pa_pool* pool, int64_t seq_id, int64_t* length) {
+    if (!pool || !length) return pa::fail(PA_ERR_INVALID_ARG, "pa_seq_length: NULL argument");
+    const pa_pool::Seq* s = find_seq(pool, seq_id);
+    if (!s) return pa::fail(PA_ERR_NOT_FOUND, "pa_seq_length: unknown sequence %lld", (long long)seq_id);
+    *length = s->length;
+    return PA_OK;
+}
+
+int pa_pool_block_tables(const pa_pool* pool, const int64_t* seq_ids, int n, int32_t* tables, int max_blocks,
+                         int32_t* lens) {
+    if (!pool || n < 0 || max_blocks < 0 || (n > 0 && (!seq_ids || !tables || !lens)))
+        return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_block_tables: bad arguments");
+    for (int i = 0; i < n; ++i) {
+        const pa_pool::Seq* s = find_seq(pool, seq_ids[i]);
+        if (!s) return pa::fail(PA_ERR_NOT_FOUND, "pa_pool_block_tables: unknown sequence %lld", (long long)seq_ids[i]);
+        if (static_cast<int64_t>(s->table.size()) > max_blocks)
+            return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_block_tables: sequence %lld needs %zu blocks > %d",
+                            (long long)seq_ids[i], s->table.size(), max_blocks);
+        if (s->length > INT32_MAX)
+            return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_block_tables: length does not fit int32");
+    }
+    for (int i = 0; i < n; ++i) {
+        const pa_pool::Seq* s = find_seq(pool, seq_ids[i]);
+        int32_t* row = tables + static_cast<int64_t>(i) * max_blocks;
+        std::copy(s->table.begin(), s->table.end(), row);
+        std::fill(row + s->table.size(), row + max_blocks, -1);
+        lens[i] = static_cast<int32_t>(s->length);
+    }
+    return PA_OK;
+}
+
+int pa_pool_num_free(const pa_pool* pool) { return pool ? static_cast<int>(pool->free_list.size()) : -1; }
+int pa_pool_num_blocks(const pa_pool* pool) { return pool ? pool->num_blocks : -1; }
+int pa_pool_block_size(const pa_pool* pool) { return pool ? pool->block_size : -1; }
+
+int pa_pool_refcount(const pa_pool* pool, int32_t block) {
+    if (!pool || block < 0 || block >= pool->num_blocks) return -1;
+    return pool->refs[block];
+}
+
+int pa_pool_free_list(const pa_pool* pool, int32_t* out, int capacity) {
+    if (!pool || (capacity > 0 && !out)) return -1;
+    const int n = static_cast<int>(pool->free_list.size());
+    if (n > capacity) return -1;
+    std::copy(pool->free_list.begin(), pool->free_list.end(), out);
+    return n;
+}
+
+int pa_pool_check_invariants(const pa_pool* pool) {
+    if (!pool) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_check_invariants: NULL pool");
+    const int bs = pool->block_size;
+    std::vector<int32_t> counted(pool->num_blocks, 0);
+    for (const auto& kv : pool->seqs) {
+        const pa_pool::Seq& s = kv.second;
+        const int64_t need = (s.length + bs - 1) / bs;
+        if (static_cast<int64_t>(s.table.size()) != need)
+            return pa::fail(PA_ERR_INVALID_ARG, "sequence %lld holds %zu blocks for %lld tokens", (long long)kv.first,
+                            s.table.size(), (long long)s.length);
+        for (size_t j = 0; j < s.table.size(); ++j) {
+            const int32_t b = s.table[j];
+            if (b < 0 || b >= pool->num_blocks)
+                return pa::fail(PA_ERR_INVALID_ARG, "sequence %lld lists block %d", (long long)kv.first, b);
+            counted[b] += 1;
+            const int64_t expect = (j + 1 < s.table.size()) ? bs : s.length - static_cast<int64_t>(j) * bs;
+            if (pool->fill[b] != expect)
+                return pa::fail(PA_ERR_INVALID_ARG, "block %d holds %d tokens, sequence %lld expects %lld", b,
+                                pool->fill[b], (long long)kv.first, (long long)expect);
+        }
+    }
+    std::vector<char> is_free(pool->num_blocks, 0);
+    for (int32_t b : pool->free_list) {
+        if (b < 0 || b >= pool->num_blocks || is_free[b])
+            return pa::fail(PA_ERR_INVALID_ARG, "free list holds %d twice or out of range", b);
+        is_free[b] = 1;
+    }
+    for (int b = 0; b < pool->num_blocks; ++b) {
+        if (counted[b] != pool->refs[b])
+            return pa::fail(PA_ERR_INVALID_ARG, "block %d: refcount %d but %d tables hold it", b, pool->refs[b],
+                            counted[b]);
+        if (is_free[b] == (counted[b] > 0))
+            return pa::fail(PA_ERR_INVALID_ARG, "block %d is %s", b, is_free[b] ? "free and used" : "lost");
+    }
+    return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,425 @@
+// C-ABI entry points: argument checks, the split-KV plan, TMA descriptors, the
+// device error word and the thread-local error message.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+#include <string>
+
+#include <cudaTypedefs.h>
+
+#include "decode_launch.h"
+#include "kv_ops.h"
+#include "pa.h"
+#include "pa_common.cuh"
+#include "pa_internal.h"
+
+// One error word per device, set by kernels with atomicOr (see pa_common.cuh).
+__device__ unsigned int g_pa_device_error_word;
+
+namespace pa {
+
+namespace {
+thread_local std::string g_message;
+constexpr int kMaxDevices = 64;
+}  // namespace
+
+int fail(int code, const char* fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof buf, fmt, ap);
+    va_end(ap);
+    g_message = buf;
+    return code;
+}
+
+void clear_error() { g_message.clear(); }
+
+bool decode_kernel_info(int dtype, int head_dim, int block_size, int kind, int gmax, KernelInfo* info) {
+    switch (dtype) {
+        case PA_F32: return decode_kernel_info_f32(head_dim, block_size, kind, gmax, info);
+        case PA_F16: return decode_kernel_info_f16(head_dim, block_size, kind, gmax, info);
+        case PA_BF16: return decode_kernel_info_bf16(head_dim, block_size, kind, gmax, info);
+        default: return false;
+    }
+}
+
+cudaError_t decode_launch(int dtype, int head_dim, int block_size, int kind, int gmax, const CUtensorMap& k,
+                          const CUtensorMap& v, const DecodeArgs& a, int grid, cudaStream_t s) {
+    switch (dtype) {
+        case PA_F32: return decode_launch_f32(head_dim, block_size, kind, gmax, k, v, a, grid, s);
+        case PA_F16: return decode_launch_f16(head_dim, block_size, kind, gmax, k, v, a, grid, s);
+        case PA_BF16: return decode_launch_bf16(head_dim, block_size, kind, gmax, k, v, a, grid, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+cudaError_t merge_launch(int dtype, int head_dim, const MergeArgs& a, cudaStream_t s) {
+    switch (dtype) {
+        case PA_F32: return merge_launch_f32(head_dim, a, s);
+        case PA_F16: return merge_launch_f16(head_dim, a, s);
+        case PA_BF16: return merge_launch_bf16(head_dim, a, s);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+namespace {
+
+int elem_bytes(int dtype) { return dtype == PA_F32 ? 4 : 2; }
+bool dtype_ok(int dtype) { return dtype == PA_F32 || dtype == PA_F16 || dtype == PA_BF16; }
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
+
+int cuda_fail(cudaError_t e, const char* what) {
+    return fail(PA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+struct DeviceState {
+    unsigned* error_word = nullptr;
+    int num_sms = 0;
+};
+
+std::mutex g_dev_mutex;
+DeviceState g_dev[kMaxDevices];
+
+int current_device_state(DeviceState** out) {
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (device < 0 || device >= kMaxDevices) return fail(PA_ERR_UNSUPPORTED, "device index %d", device);
+    std::lock_guard<std::mutex> lock(g_dev_mutex);
+    DeviceState& st = g_dev[device];
+    if (!st.error_word) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_pa_device_error_word);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+        e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, device);
+        if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute(SM count)");
+        st.error_word = static_cast<unsigned*>(p);
+    }
+    *out = &st;
+    return PA_OK;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q = cudaDriverEntryPointSymbolNotFound;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D view of a cache: rows = num_blocks * H_kv * bs (one row per slot and head), columns = d.
+// The box is 128 bytes of d by bs rows, loaded with the 128-byte swizzle.
+int encode_cache_map(CUtensorMap* map, const void* base, int dtype, int num_blocks, int num_kv_heads,
+                     int block_size, int head_dim) {
+    PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
+    if (!encode) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
+    const int eb = elem_bytes(dtype);
+    const CUtensorMapDataType type = dtype == PA_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                     : dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)num_blocks * num_kv_heads * block_size};
+    cuuint64_t strides[1] = {(cuuint64_t)head_dim * eb};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / eb), (cuuint32_t)block_size};
+    cuuint32_t estrides[2] = {1, 1};
+    CUresult r = encode(map, type, 2, const_cast<void*>(base), dims, strides, box, estrides,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return PA_OK;
+}
+
+struct Plan {
+    int kind = 0;
+    int gmax = 8;
+    int head_chunks = 1;
+    int units = 0;
+    int partition_pages = 1;
+    int max_parts = 1;
+    long long grid = 0;
+    size_t ws_bytes = 0;
+    size_t off_l = 0, off_o = 0;
+    KernelInfo ki{};
+};
+
+void workspace_layout(int num_seqs, int num_heads, int head_dim, int max_parts, Plan* p) {
+    if (max_parts <= 1) {
+        p->ws_bytes = p->off_l = p->off_o = 0;
+        return;
+    }
+    const size_t rows = (size_t)num_seqs * num_heads * max_parts;
+    p->off_l = align256(rows * sizeof(float));
+    p->off_o = p->off_l + align256(rows * sizeof(float));
+    p->ws_bytes = p->off_o + align256(rows * head_dim * sizeof(float));
+}
+
+// has_ws: false means no workspace is usable (single pass forced).
+int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks, int dtype,
+              bool has_ws, size_t ws_avail, int max_context_len, int partition_pages, int kernel, Plan* plan) {
+    if (!dtype_ok(dtype)) return fail(PA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
+    if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
+        return fail(PA_ERR_INVALID_ARG, "num_heads=%d must be a positive multiple of num_kv_heads=%d", num_heads,
+                    num_kv_heads);
+    if (head_dim <= 0 || block_size <= 0 || max_blocks <= 0)
+        return fail(PA_ERR_INVALID_ARG, "head_dim=%d block_size=%d max_blocks_per_seq=%d", head_dim, block_size,
+                    max_blocks);
+    if ((long long)max_blocks * block_size >= (1ll << 31))
+        return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq * block_size must be < 2^31");
+    Plan p;
+    const int group = num_heads / num_kv_heads;
+    if (kernel == PA_KERNEL_AUTO) {
+        p.kind = dtype == PA_F32 ? PA_KERNEL_SIMT : PA_KERNEL_MMA;
+    } else if (kernel == PA_KERNEL_MMA || kernel == PA_KERNEL_SIMT) {
+        p.kind = kernel;
+    } else {
+        return fail(PA_ERR_INVALID_ARG, "unknown kernel choice %d", kernel);
+    }
+    if (p.kind == PA_KERNEL_MMA && dtype == PA_F32)
+        return fail(PA_ERR_UNSUPPORTED, "the tensor-core kernel needs f16 or bf16");
+    p.gmax = 8;
+    if (p.kind == PA_KERNEL_SIMT) {
+        const int g = group < 8 ? group : 8;
+        p.gmax = g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 8;
+    }
+    if (!decode_kernel_info(dtype, head_dim, block_size, p.kind, p.gmax, &p.ki))
+        return fail(PA_ERR_UNSUPPORTED, "no %s decode kernel for dtype=%d head_dim=%d block_size=%d",
+                    p.kind == PA_KERNEL_MMA ? "tensor-core" : "CUDA-core", dtype, head_dim, block_size);
+    p.head_chunks = (group + p.ki.heads_per_cta - 1) / p.ki.heads_per_cta;
+    p.units = num_seqs * num_kv_heads * p.head_chunks;
+
+    long long max_ctx = (long long)max_blocks * block_size;
+    if (max_context_len > 0 && max_context_len < max_ctx) max_ctx = max_context_len;
+    int nblk_max = (int)((max_ctx + block_size - 1) / block_size);
+    if (nblk_max < 1) nblk_max = 1;
+
+    DeviceState* dev = nullptr;
+    int st = current_device_state(&dev);
+    if (st != PA_OK) return st;
+    const long long slots = (long long)dev->num_sms * p.ki.ctas_per_sm;
+
+    int pp;
+    if (partition_pages < 0 || !has_ws) {
+        if (partition_pages > 0 && partition_pages < nblk_max)
+            return fail(PA_ERR_INVALID_ARG, "partition_pages=%d splits contexts but no workspace was given",
+                        partition_pages);
+        pp = nblk_max;
+    } else if (partition_pages > 0) {
+        pp = partition_pages < nblk_max ? partition_pages : nblk_max;
+    } else {
+        // About 512 tokens per partition; shorter when that leaves fewer than two waves of CTAs.
+        pp = 512 / block_size > 8 ? 512 / block_size : 8;
+        while (pp > 8 && (long long)p.units * ((nblk_max + pp - 1) / pp) < 2 * slots) pp /= 2;
+        if (pp > nblk_max) pp = nblk_max;
+    }
+    for (;;) {
+        p.partition_pages = pp;
+        p.max_parts = (nblk_max + pp - 1) / pp;
+        workspace_layout(num_seqs, num_heads, head_dim, p.max_parts, &p);
+        const bool fits = p.max_parts == 1 || (p.ws_bytes <= ws_avail && p.max_parts <= p.ki.merge_parts_cap);
+        if (fits) break;
+        if (partition_pages > 0)
+            return fail(PA_ERR_INVALID_ARG,
+                        "workspace of %zu bytes is too small for partition_pages=%d (needs %zu, or too many parts)",
+                        ws_avail, partition_pages, p.ws_bytes);
+        pp = pp * 2 < nblk_max ? pp * 2 : nblk_max;
+    }
+    p.grid = (long long)p.max_parts * p.units;
+    if (p.grid >= (1ll << 31)) return fail(PA_ERR_UNSUPPORTED, "grid of %lld CTAs is too large", p.grid);
+    *plan = p;
+    return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char* pa_last_error_string(void) { return g_message.c_str(); }
+
+const char* pa_version(void) { return "paged_kv_cache_129_gb300 0.1.0 (sm_103a)"; }
+
+int pa_check_error(void* stream) {
+    clear_error();
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+    DeviceState* dev = nullptr;
+    int st = current_device_state(&dev);
+    if (st != PA_OK) return st;
+    unsigned word = 0;
+    e = cudaMemcpy(&word, dev->error_word, sizeof word, cudaMemcpyDeviceToHost);
+    if (e != cudaSuccess) return cuda_fail(e, "reading the device error word");
+    if (word == 0) return PA_OK;
+    const unsigned zero = 0;
+    e = cudaMemcpy(dev->error_word, &zero, sizeof zero, cudaMemcpyHostToDevice);
+    if (e != cudaSuccess) return cuda_fail(e, "clearing the device error word");
+    if (word & kErrBadTable) return fail(PA_ERR_BAD_TABLE, "a kernel met a block id outside the pool (word 0x%x)", word);
+    if (word & kErrBadSlot) return fail(PA_ERR_BAD_SLOT, "a kernel met a slot past the pool (word 0x%x)", word);
+    if (word & kErrBadContext)
+        return fail(PA_ERR_BAD_CONTEXT, "a context length was negative or longer than its table (word 0x%x)", word);
+    return fail(PA_ERR_TIMEOUT, "a kernel-internal wait gave up (word 0x%x)", word);
+}
+
+int pa_write_kv(const void* key, const void* value, void* key_cache, void* value_cache, const int64_t* slot_mapping,
+                int num_tokens, int num_kv_heads, int head_dim, int block_size, int num_blocks, int dtype,
+                void* stream) {
+    clear_error();
+    if (!dtype_ok(dtype)) return fail(PA_ERR_INVALID_ARG, "pa_write_kv: unknown dtype %d", dtype);
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
+        return fail(PA_ERR_INVALID_ARG, "pa_write_kv: bad sizes");
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !key_cache || !value_cache || !slot_mapping)
+        return fail(PA_ERR_INVALID_ARG, "pa_write_kv: NULL pointer");
+    if (!aligned(slot_mapping, 8)) return fail(PA_ERR_INVALID_ARG, "pa_write_kv: slot_mapping must be 8-byte aligned");
+    const int eb = elem_bytes(dtype);
+    if (!aligned(key, eb) || !aligned(value, eb) || !aligned(key_cache, eb) || !aligned(value_cache, eb))
+        return fail(PA_ERR_INVALID_ARG, "pa_write_kv: buffers must be aligned to the element size");
+    DeviceState* dev = nullptr;
+    int st = current_device_state(&dev);
+    if (st != PA_OK) return st;
+    WriteArgs a{key, value, key_cache, value_cache, slot_mapping, num_tokens, num_kv_heads, head_dim, block_size,
+                num_blocks, eb, dev->error_word};
+    cudaError_t e = write_kv_launch(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pa_write_kv launch");
+    return PA_OK;
+}
+
+int pa_copy_blocks(void* key_cache, void* value_cache, const int64_t* src_dst_pairs, int num_pairs, int num_kv_heads,
+                   int head_dim, int block_size, int num_blocks, int dtype, void* stream) {
+    clear_error();
+    if (!dtype_ok(dtype)) return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: unknown dtype %d", dtype);
+    if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
+        return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: bad sizes");
+    if (num_pairs == 0) return PA_OK;
+    if (!key_cache || !value_cache || !src_dst_pairs) return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: NULL pointer");
+    if (!aligned(src_dst_pairs, 8)) return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: pairs must be 8-byte aligned");
+    const int eb = elem_bytes(dtype);
+    if (!aligned(key_cache, eb) || !aligned(value_cache, eb))
+        return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: caches must be aligned to the element size");
+    DeviceState* dev = nullptr;
+    int st = current_device_state(&dev);
+    if (st != PA_OK) return st;
+    CopyArgs a{key_cache, value_cache, src_dst_pairs, num_pairs, num_kv_heads, head_dim, block_size, num_blocks, eb,
+               dev->error_word};
+    cudaError_t e = copy_blocks_launch(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pa_copy_blocks launch");
+    return PA_OK;
+}
+
+int pa_decode_make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                        int max_blocks_per_seq, int dtype, size_t workspace_bytes, int max_context_len,
+                        int partition_pages, int kernel, pa_decode_plan* out) {
+    clear_error();
+    if (!out) return fail(PA_ERR_INVALID_ARG, "pa_decode_make_plan: out is NULL");
+    Plan p;
+    int st = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, dtype,
+                       workspace_bytes > 0, workspace_bytes, max_context_len, partition_pages, kernel, &p);
+    if (st != PA_OK) return st;
+    out->kernel = p.kind;
+    out->partition_pages = p.partition_pages;
+    out->max_parts = p.max_parts;
+    out->heads_per_cta = p.ki.heads_per_cta;
+    out->grid_ctas = (int)p.grid;
+    out->threads_per_cta = p.ki.threads;
+    out->smem_bytes = p.ki.smem_bytes;
+    out->workspace_bytes = p.ws_bytes;
+    return PA_OK;
+}
+
+size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                int max_blocks_per_seq, int dtype) {
+    Plan p;
+    if (make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, dtype, true,
+                  (size_t)-1, 0, 0, PA_KERNEL_AUTO, &p) != PA_OK)
+        return 0;
+    return p.ws_bytes;
+}
+
+int pa_decode_ex(void* out, const void* query, const void* key_cache, const void* value_cache,
+                 const int32_t* block_tables, const int32_t* context_lens, int num_seqs, int num_heads,
+                 int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq, int num_blocks, float scale,
+                 int dtype, void* workspace, size_t workspace_bytes, int max_context_len, int partition_pages,
+                 int kernel, void* stream) {
+    clear_error();
+    if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "pa_decode: num_seqs=%d", num_seqs);
+    if (num_seqs == 0) return PA_OK;
+    if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens)
+        return fail(PA_ERR_INVALID_ARG, "pa_decode: NULL pointer");
+    if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "pa_decode: num_blocks=%d", num_blocks);
+    if (num_kv_heads <= 0 || (long long)num_blocks * num_kv_heads * block_size >= (1ll << 31))
+        return fail(PA_ERR_INVALID_ARG, "pa_decode: num_blocks * num_kv_heads * block_size must be < 2^31");
+    if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "pa_decode: scale is not finite");
+    if (!aligned(key_cache, 16) || !aligned(value_cache, 16))
+        return fail(PA_ERR_INVALID_ARG, "pa_decode: caches must be 16-byte aligned");
+    if (!aligned(query, 4) || !aligned(out, 4) || !aligned(block_tables, 4) || !aligned(context_lens, 4))
+        return fail(PA_ERR_INVALID_ARG, "pa_decode: query/out/tables/lens must be 4-byte aligned");
+    if (workspace && !aligned(workspace, 256))
+        return fail(PA_ERR_INVALID_ARG, "pa_decode: workspace must be 256-byte aligned");
+    Plan p;
+    int st = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, dtype,
+                       workspace != nullptr && workspace_bytes > 0, workspace ? workspace_bytes : 0, max_context_len,
+                       partition_pages, kernel, &p);
+    if (st != PA_OK) return st;
+    DeviceState* dev = nullptr;
+    st = current_device_state(&dev);
+    if (st != PA_OK) return st;
+
+    CUtensorMap tk, tv;
+    st = encode_cache_map(&tk, key_cache, dtype, num_blocks, num_kv_heads, block_size, head_dim);
+    if (st != PA_OK) return st;
+    st = encode_cache_map(&tv, value_cache, dtype, num_blocks, num_kv_heads, block_size, head_dim);
+    if (st != PA_OK) return st;
+
+    DecodeArgs a{};
+    a.out = out;
+    a.q = query;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    char* ws = static_cast<char*>(workspace);
+    a.ws_m = p.max_parts > 1 ? reinterpret_cast<float*>(ws) : nullptr;
+    a.ws_l = p.max_parts > 1 ? reinterpret_cast<float*>(ws + p.off_l) : nullptr;
+    a.ws_o = p.max_parts > 1 ? reinterpret_cast<float*>(ws + p.off_o) : nullptr;
+    a.err = dev->error_word;
+    a.num_seqs = num_seqs;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.group = num_heads / num_kv_heads;
+    a.head_chunks = p.head_chunks;
+    a.max_blocks = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.partition_pages = p.partition_pages;
+    a.max_parts = p.max_parts;
+    a.scale_log2 = (float)((double)scale * 1.4426950408889634);  // log2(e)
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaError_t e = decode_launch(dtype, head_dim, block_size, p.kind, p.gmax, tk, tv, a, (int)p.grid, s);
+    if (e != cudaSuccess) return cuda_fail(e, "pa_decode: decode kernel launch");
+    if (p.max_parts > 1) {
+        MergeArgs m{out,        context_lens, a.ws_m,     a.ws_l,          a.ws_o,
+                    num_seqs,   num_heads,    block_size, max_blocks_per_seq, p.partition_pages,
+                    p.max_parts};
+        e = merge_launch(dtype, head_dim, m, s);
+        if (e != cudaSuccess) return cuda_fail(e, "pa_decode: merge kernel launch");
+    }
+    return PA_OK;
+}
+
+int pa_decode(void* out, const void* query, const void* key_cache, const void* value_cache,
+              const int32_t* block_tables, const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+              int head_dim, int block_size, int max_blocks_per_seq, int num_blocks, float scale, int dtype,
+              void* workspace, size_t workspace_bytes, void* stream) {
+    return pa_decode_ex(out, query, key_cache, value_cache, block_tables, context_lens, num_seqs, num_heads,
+                        num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype, workspace,
+                        workspace_bytes, 0, 0, PA_KERNEL_AUTO, stream);
+}
+
+}  // extern "C"

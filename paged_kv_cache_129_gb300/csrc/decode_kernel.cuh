@@ -1,0 +1,691 @@
+// Paged decode attention kernel (one CTA per (sequence, kv head, head chunk,
+// partition)) and the split-KV merge kernel.
+//
+// The method (MiniPaged-Qwen, sections 5.1-5.2 and 6.2): for every logical
+// position pos of the context, pb = block_table[pos / bs] and the key/value
+// rows are key_cache[pb, kvh, pos % bs, :]; scores s = scale * q.k are
+// normalised over the whole context with a running maximum m, a running
+// denominator l and an unnormalised output o~ (online softmax):
+//     m' = max(m, max s),  l' = l * 2^(m - m') + sum 2^(s - m'),
+//     o~' = o~ * 2^(m - m') + sum 2^(s - m') v,    o = o~ / l.
+// (Scores are kept in the log2 domain: s is pre-multiplied by log2(e), so
+// 2^(s - m) equals the page's e^(s - m).)  GQA: kv head kvh serves the query
+// heads kvh*g .. kvh*g + g - 1 (section 9.1), so one CTA reads every K/V page
+// once for all of them.  Long contexts are cut into partitions of
+// `partition_pages` pages (the "partitioned reduction" of section 10.2); each
+// partition emits (m, l, o~) and the merge kernel combines them with the same
+// rescaling rule.
+//
+// CTA layout: warps 0..NW-1 consume pages, warp NW produces them.  The
+// producer reads the block-table entries of its partition (one 32-entry chunk
+// ahead, through registers) and issues TMA tile loads of each page's K and V
+// slices ([pb, kvh, :, :] is bs * d contiguous elements) into a shared-memory
+// ring of NSLOT page slots; every page's arrival is tracked by an mbarrier
+// with transaction bytes.  Page i lands in slot i % NSLOT and is consumed by
+// warp i % NW, which then releases the slot.  Tiles are 128-byte-swizzled so
+// that the consumers' shared-memory reads are free of bank conflicts.
+//
+// Consumers:
+//  * tensor-core path (f16/bf16): per 16-token sub-tile,
+//      S[16 heads x 8 tok]  = Q[16 x d] . K^T   (m16n8k16, heads padded to 16)
+//      O^T[16 d x 8 heads] += V^T[16 x 16 tok] . P^T[16 tok x 8 heads]
+//    The fp32 score fragment of QK^T is exactly the B fragment PV needs, so
+//    P never goes through shared memory.
+//  * CUDA-core path (all dtypes): one or two lanes per token for QK^T (q in
+//    shared memory as fp32), one lane per d-slice for PV.
+#pragma once
+
+#include <cfloat>
+
+#include "decode_launch.h"
+#include "pa_common.cuh"
+
+namespace pa {
+
+constexpr int kConsumerWarps = 4;
+
+template <typename T, int D, int BS, bool MMA, int GMAX>
+struct DecodeCfg {
+    static constexpr int kEB = sizeof(T);
+    static constexpr int kNW = kConsumerWarps;
+    static constexpr int kThreads = (kNW + 1) * 32;
+    static constexpr int kBoxElems = 128 / kEB;           // one 128-byte swizzle row of d
+    static constexpr int kNBox = D / kBoxElems;           // boxes per page
+    static constexpr int kBoxBytes = BS * 128;            // BS rows of 128 bytes
+    static constexpr int kPageBytes = kNBox * kBoxBytes;  // = BS * D * sizeof(T)
+    static constexpr int kSlotBytes = 2 * kPageBytes;     // K page + V page
+    static constexpr int kRingTarget = 64 * 1024;
+    static constexpr int kNSlotRaw = (kRingTarget / kSlotBytes) / kNW * kNW;
+    static constexpr int kNSlot = kNSlotRaw < kNW ? kNW : kNSlotRaw;
+    static constexpr int kRingBytes = kNSlot * kSlotBytes;
+    static constexpr int kHeads = MMA ? 8 : GMAX;          // query heads per CTA
+    static constexpr int kOStride = D + 4;                 // padded fp32 row of the combine buffer
+    static constexpr int kCombineFloats = kNW * kHeads * kOStride + 2 * kNW * kHeads;
+    static constexpr int kBarOffset = kRingBytes;
+    static constexpr int kIssuedOffset = kBarOffset + 2 * kNSlot * 8;
+    static constexpr int kQsOffset = kIssuedOffset + kNSlot * 4;
+    static constexpr int kQsBytes = MMA ? 0 : GMAX * D * 4;
+    static constexpr int kPsOffset = kQsOffset + kQsBytes;
+    static constexpr int kPsBytes = MMA ? 0 : kNW * GMAX * BS * 4;
+    static constexpr int kStatOffset = kPsOffset + kPsBytes;  // per head: M, W, then per-warp weights
+    static constexpr int kStatBytes = kHeads * (2 + kNW) * 4;
+    static constexpr int kFlagOffset = kStatOffset + kStatBytes;
+    static constexpr int kSmemBytes = kFlagOffset + 16 + 1024;  // + slack to align the base to 1024
+
+    static_assert(D % kBoxElems == 0, "head_dim must be a multiple of 128 bytes");
+    static_assert(BS <= 256 && BS >= 8, "TMA box height");
+    static_assert(!MMA || BS % 16 == 0, "the tensor-core path needs 16-token sub-tiles");
+    static_assert(!MMA || D % 16 == 0, "k-steps of 16");
+    static_assert(MMA || (32 % BS == 0 || BS == 32), "CUDA-core path: 32 must be a multiple of BS");
+    static_assert(kCombineFloats * 4 <= kRingBytes, "combine buffer must fit in the ring");
+    static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
+};
+
+// Byte offset of (row, element) in a 128-byte-swizzled page of kNBox boxes.
+template <typename T, int BS>
+__device__ __forceinline__ uint32_t swz_offset(int row, int elem) {
+    constexpr int kBoxElems = 128 / sizeof(T);
+    const int box = elem / kBoxElems;
+    const int byte = (elem % kBoxElems) * (int)sizeof(T);
+    const int chunk = byte >> 4;
+    return (uint32_t)(box * BS * 128 + row * 128 + (((chunk ^ (row & 7)) << 4) | (byte & 15)));
+}
+
+// ------------------------------------------------------------------------------------------
+// Tensor-core consumer (f16 / bf16).
+template <typename T, int D, int BS>
+struct MmaConsumer {
+    static constexpr int KS = D / 16;  // k-steps of QK^T, m-tiles of PV
+    uint32_t qa[KS][2];                // Q rows 0..7 (heads) of the A fragment; rows 8..15 are zero
+    float o[KS][4];                    // O^T fragments: rows d, columns heads
+    float m, l;                        // running max (quad-uniform) and this thread's part of l
+
+    __device__ __forceinline__ void init(const T* q_rows, int gc, int lane) {
+        const int g = lane >> 2, t = lane & 3;
+        const uint32_t* row = reinterpret_cast<const uint32_t*>(q_rows + (size_t)g * D);
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            qa[kk][0] = g < gc ? __ldg(row + (kk * 16 + 2 * t) / 2) : 0u;
+            qa[kk][1] = g < gc ? __ldg(row + (kk * 16 + 8 + 2 * t) / 2) : 0u;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[kk][e] = 0.f;
+        }
+        m = -INFINITY;
+        l = 0.f;
+    }
+
+    // One page (BS tokens, nvalid of them inside the context).
+    __device__ __forceinline__ void page(uint8_t* kpage, uint8_t* vpage, int nvalid, float scale_log2, int lane) {
+        const int t = lane & 3;
+        const int j = lane >> 3, r8 = lane & 7;
+        const uint32_t kbase = smem_addr(kpage);
+        const uint32_t vbase = smem_addr(vpage);
+#pragma unroll
+        for (int sub = 0; sub < BS / 16; ++sub) {
+            const int nv = nvalid - sub * 16;
+            if (nv <= 0) break;
+            if (nv < 16) {
+                // Rows past the context may hold anything (NaN included): zero them so
+                // that p = 0 times v stays 0 in the MMA.
+                const int rows = 16 - nv;
+                constexpr int kChunksPerRow = (D * (int)sizeof(T)) / 16;
+                for (int idx = lane; idx < rows * kChunksPerRow; idx += 32) {
+                    const int r = sub * 16 + nv + idx / kChunksPerRow;
+                    const int c = idx % kChunksPerRow;
+                    *reinterpret_cast<uint4*>(vpage + (c / 8) * BS * 128 + r * 128 + (c % 8) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                }
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            // ---- S = Q K^T : two n-tiles of 8 tokens ----
+            float s0[4] = {0.f, 0.f, 0.f, 0.f};
+            float s1[4] = {0.f, 0.f, 0.f, 0.f};
+            const int row = sub * 16 + (j >> 1) * 8 + r8;
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+                uint32_t bf[4];
+                ldmatrix_x4(bf, kbase + swz_offset<T, BS>(row, kk * 16 + (j & 1) * 8));
+                Mma<T>::run(s0, qa[kk][0], 0u, qa[kk][1], 0u, bf[0], bf[1]);
+                Mma<T>::run(s1, qa[kk][0], 0u, qa[kk][1], 0u, bf[2], bf[3]);
+            }
+            // ---- online softmax for head g over tokens 2t, 2t+1, 8+2t, 9+2t ----
+            float x0 = (2 * t < nv) ? s0[0] * scale_log2 : -INFINITY;
+            float x1 = (2 * t + 1 < nv) ? s0[1] * scale_log2 : -INFINITY;
+            float x2 = (8 + 2 * t < nv) ? s1[0] * scale_log2 : -INFINITY;
+            float x3 = (9 + 2 * t < nv) ? s1[1] * scale_log2 : -INFINITY;
+            float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float m_new = fmaxf(m, mx);  // finite: token 0 of a sub-tile is always valid
+            const float alpha = exp2f(m - m_new);
+            float r0, r1, r2, r3;
+            const uint32_t pb0 = Mma<T>::pack(exp2f(x0 - m_new), exp2f(x1 - m_new), r0, r1);
+            const uint32_t pb1 = Mma<T>::pack(exp2f(x2 - m_new), exp2f(x3 - m_new), r2, r3);
+            l = l * alpha + ((r0 + r1) + (r2 + r3));
+            m = m_new;
+            // O^T columns 2t and 2t+1 are heads 2t, 2t+1: fetch their rescale factors.
+            const float a_lo = __shfl_sync(0xffffffffu, alpha, (2 * t) * 4);
+            const float a_hi = __shfl_sync(0xffffffffu, alpha, (2 * t + 1) * 4);
+            // ---- O^T += V^T P^T ----
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+                o[mt][0] *= a_lo;
+                o[mt][1] *= a_hi;
+                o[mt][2] *= a_lo;
+                o[mt][3] *= a_hi;
+                uint32_t af[4];
+                ldmatrix_x4_trans(af, vbase + swz_offset<T, BS>(row, mt * 16 + (j & 1) * 8));
+                Mma<T>::run(o[mt], af[0], af[1], af[2], af[3], pb0, pb1);
+            }
+        }
+    }
+
+    // Write this warp's state into the CTA combine buffer.
+    __device__ __forceinline__ void store(float* co, float* cm, float* cl, int warp, int lane, int ostride) {
+        const int g = lane >> 2, t = lane & 3;
+        l += __shfl_xor_sync(0xffffffffu, l, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+        if (t == 0) {
+            cm[warp * 8 + g] = m;
+            cl[warp * 8 + g] = l;
+        }
+        float* lo = co + (size_t)(warp * 8 + 2 * t) * ostride;
+        float* hi = co + (size_t)(warp * 8 + 2 * t + 1) * ostride;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            lo[mt * 16 + g] = o[mt][0];
+            hi[mt * 16 + g] = o[mt][1];
+            lo[mt * 16 + 8 + g] = o[mt][2];
+            hi[mt * 16 + 8 + g] = o[mt][3];
+        }
+    }
+};
+
+// ------------------------------------------------------------------------------------------
+// CUDA-core consumer (all dtypes).
+template <typename T, int D, int BS, int GMAX>
+struct SimtConsumer {
+    static constexpr int LPT = 32 / BS;          // lanes per token in QK^T
+    static constexpr int E = 16 / sizeof(T);     // elements per 16-byte chunk
+    static constexpr int NCHUNK = D / E;
+    static constexpr int DPL = D / 32;           // output elements per lane in PV
+    static constexpr int VBYTES = DPL * sizeof(T);
+    static_assert(VBYTES == 4 || VBYTES == 8 || VBYTES == 16, "PV load width");
+    float o[GMAX][DPL];
+    float m[GMAX], l[GMAX];
+
+    __device__ __forceinline__ void init() {
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+            m[h] = -INFINITY;
+            l[h] = 0.f;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) o[h][e] = 0.f;
+        }
+    }
+
+    __device__ __forceinline__ void load_v(const uint8_t* p, float* vf) {
+        if constexpr (VBYTES == 16) {
+            unpack16<T>(*reinterpret_cast<const uint4*>(p), vf);
+        } else if constexpr (VBYTES == 8) {
+            const uint2 raw = *reinterpret_cast<const uint2*>(p);
+            const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) vf[i] = to_float(e[i]);
+        } else {
+            const uint32_t raw = *reinterpret_cast<const uint32_t*>(p);
+            const T* e = reinterpret_cast<const T*>(&raw);
+#pragma unroll
+            for (int i = 0; i < DPL; ++i) vf[i] = to_float(e[i]);
+        }
+    }
+
+    __device__ __forceinline__ void page(const uint8_t* kpage, const uint8_t* vpage, int nvalid, float scale_log2,
+                                         const float* q_s, float* p_s, int lane) {
+        const int tok = lane % BS;
+        const int part = lane / BS;
+        float acc[GMAX];
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) acc[h] = 0.f;
+        if (tok < nvalid) {
+#pragma unroll 4
+            for (int c = part; c < NCHUNK; c += LPT) {
+                float kf[E];
+                unpack16<T>(*reinterpret_cast<const uint4*>(kpage + swz_offset<T, BS>(tok, c * E)), kf);
+#pragma unroll
+                for (int h = 0; h < GMAX; ++h) {
+                    const float4* qv = reinterpret_cast<const float4*>(q_s + h * D + c * E);
+#pragma unroll
+                    for (int e4 = 0; e4 < E / 4; ++e4) {
+                        const float4 qq = qv[e4];
+                        acc[h] = fmaf(qq.x, kf[4 * e4 + 0], acc[h]);
+                        acc[h] = fmaf(qq.y, kf[4 * e4 + 1], acc[h]);
+                        acc[h] = fmaf(qq.z, kf[4 * e4 + 2], acc[h]);
+                        acc[h] = fmaf(qq.w, kf[4 * e4 + 3], acc[h]);
+                    }
+                }
+            }
+        }
+#pragma unroll
+        for (int off = BS; off < 32; off <<= 1)
+#pragma unroll
+            for (int h = 0; h < GMAX; ++h) acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], off);
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+            const float x = tok < nvalid ? acc[h] * scale_log2 : -INFINITY;
+            float mx = x;
+#pragma unroll
+            for (int off = 1; off < BS; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+            const float m_new = fmaxf(m[h], mx);  // finite: token 0 of a page is always valid
+            const float alpha = exp2f(m[h] - m_new);
+            const float p = exp2f(x - m_new);
+            l[h] = l[h] * alpha + (part == 0 ? p : 0.f);
+            m[h] = m_new;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) o[h][e] *= alpha;
+            if (part == 0) p_s[h * BS + tok] = p;
+        }
+        __syncwarp();
+        for (int tk = 0; tk < nvalid; ++tk) {
+            float vf[DPL];
+            load_v(vpage + swz_offset<T, BS>(tk, lane * DPL), vf);
+#pragma unroll
+            for (int h = 0; h < GMAX; ++h) {
+                const float pp = p_s[h * BS + tk];
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) o[h][e] = fmaf(pp, vf[e], o[h][e]);
+            }
+        }
+        __syncwarp();
+    }
+
+    __device__ __forceinline__ void store(float* co, float* cm, float* cl, int warp, int lane, int ostride) {
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+            float lh = l[h];
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) lh += __shfl_xor_sync(0xffffffffu, lh, off);
+            if (lane == 0) {
+                cm[warp * GMAX + h] = m[h];
+                cl[warp * GMAX + h] = lh;
+            }
+            float* row = co + (size_t)(warp * GMAX + h) * ostride + lane * DPL;
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) row[e] = o[h][e];
+        }
+    }
+};
+
+// ------------------------------------------------------------------------------------------
+template <typename T, int D, int BS, bool MMA, int GMAX>
+__global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
+    paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                        const DecodeArgs a) {
+    using C = DecodeCfg<T, D, BS, MMA, GMAX>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ring = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+    uint64_t* empty = full + C::kNSlot;
+    int* issued = reinterpret_cast<int*>(smem + C::kIssuedOffset);
+    float* stat = reinterpret_cast<float*>(smem + C::kStatOffset);
+    volatile int* flags = reinterpret_cast<volatile int*>(smem + C::kFlagOffset);  // [0]: abort
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+
+    // Let the merge kernel (launched with programmatic stream serialisation) get
+    // resident early; it waits for this grid's completion before reading anything.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+
+    // ---- which work unit ----
+    const int units = a.num_seqs * a.num_kv_heads * a.head_chunks;
+    const int p = blockIdx.x / units;
+    const int unit = blockIdx.x - p * units;
+    const int hc = unit % a.head_chunks;
+    const int bk = unit / a.head_chunks;
+    const int kvh = bk % a.num_kv_heads;
+    const int b = bk / a.num_kv_heads;
+    const int head0 = kvh * a.group + hc * C::kHeads;
+    const int gc = min(C::kHeads, a.group - hc * C::kHeads);
+
+    int L = __ldg(a.context_lens + b);
+    const int l_cap = min(a.max_blocks, a.max_parts * a.partition_pages) * BS;
+    if (L < 0 || L > l_cap) {
+        if (p == 0 && tid == 0) atomicOr(a.err, kErrBadContext);
+        L = L < 0 ? 0 : l_cap;
+    }
+    const int nblk = (L + BS - 1) / BS;
+    const int nparts = (nblk + a.partition_pages - 1) / a.partition_pages;
+    T* out = static_cast<T*>(a.out);
+
+    if (L == 0) {  // empty context: a zero row (partition 0 writes it)
+        if (p == 0)
+            for (int idx = tid; idx < gc * D; idx += C::kThreads)
+                out[((size_t)b * a.num_heads + head0 + idx / D) * D + idx % D] = from_float<T>(0.f);
+        return;
+    }
+    const int first = p * a.partition_pages;
+    if (first >= nblk) return;
+    const int npages = min(a.partition_pages, nblk - first);
+
+    if (tid == 0) {
+        for (int s = 0; s < C::kNSlot; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            issued[s] = 0;
+        }
+        flags[0] = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == C::kNW) {
+        // ================= producer warp =================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_k);
+            tma_prefetch_desc(&tmap_v);
+        }
+        const int32_t* bt = a.block_tables + (size_t)b * a.max_blocks + first;
+        int next = lane < npages ? __ldg(bt + lane) : 0;
+        bool ok = true;
+        for (int c = 0; c < npages && ok; c += 32) {
+            const int cur = next;
+            if (c + 32 + lane < npages) next = __ldg(bt + c + 32 + lane);
+            const int n = min(32, npages - c);
+            for (int jj = 0; jj < n; ++jj) {
+                const int pb = __shfl_sync(0xffffffffu, cur, jj);
+                int good = 1;
+                if (lane == 0) {
+                    const int i = c + jj;
+                    const int s = i % C::kNSlot;
+                    if (i >= C::kNSlot)
+                        good = mbar_wait_bounded(&empty[s], ((i / C::kNSlot) - 1) & 1, a.err, flags) ? 1 : 0;
+                    if (good) {
+                        issued[s] += 1;
+                        if ((unsigned)pb < (unsigned)a.num_blocks) {
+                            mbar_arrive_expect_tx(&full[s], C::kSlotBytes);
+                            const int row = (pb * a.num_kv_heads + kvh) * BS;
+                            uint8_t* kdst = ring + s * C::kSlotBytes;
+                            uint8_t* vdst = kdst + C::kPageBytes;
+#pragma unroll
+                            for (int bx = 0; bx < C::kNBox; ++bx)
+                                tma_load_2d(kdst + bx * C::kBoxBytes, &tmap_k, bx * C::kBoxElems, row, &full[s]);
+#pragma unroll
+                            for (int bx = 0; bx < C::kNBox; ++bx)
+                                tma_load_2d(vdst + bx * C::kBoxBytes, &tmap_v, bx * C::kBoxElems, row, &full[s]);
+                        } else {
+                            atomicOr(a.err, kErrBadTable);  // skip the load; the slot keeps stale data
+                            mbar_arrive(&full[s]);
+                        }
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+                if (!ok) break;
+            }
+        }
+    } else {
+        // ================= consumer warps =================
+        const T* qrows = static_cast<const T*>(a.q) + ((size_t)b * a.num_heads + head0) * D;
+        if constexpr (MMA) {
+            MmaConsumer<T, D, BS> cons;
+            cons.init(qrows, gc, lane);
+            for (int i = warp; i < npages; i += C::kNW) {
+                const int s = i % C::kNSlot;
+                const bool got = mbar_wait_bounded(&full[s], (i / C::kNSlot) & 1, a.err, flags);
+                if (!__all_sync(0xffffffffu, got)) break;
+                const int nvalid = min(BS, L - (first + i) * BS);
+                uint8_t* kp = ring + s * C::kSlotBytes;
+                cons.page(kp, kp + C::kPageBytes, nvalid, a.scale_log2, lane);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            // All consumers are past their last page, so every TMA into the ring has
+            // landed and been read: the ring can hold the combine buffer.
+            asm volatile("bar.sync 1, %0;" ::"r"(C::kNW * 32) : "memory");
+            if (!flags[0]) {
+                float* co = reinterpret_cast<float*>(ring);
+                float* cm = co + C::kNW * C::kHeads * C::kOStride;
+                float* cl = cm + C::kNW * C::kHeads;
+                cons.store(co, cm, cl, warp, lane, C::kOStride);
+            }
+        } else {
+            float* q_s = reinterpret_cast<float*>(smem + C::kQsOffset);
+            float* p_s = reinterpret_cast<float*>(smem + C::kPsOffset) + warp * GMAX * BS;
+            for (int idx = tid; idx < GMAX * D; idx += C::kNW * 32) {
+                const int h = idx / D;
+                q_s[idx] = h < gc ? to_float(qrows[idx]) : 0.f;
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(C::kNW * 32) : "memory");
+            SimtConsumer<T, D, BS, GMAX> cons;
+            cons.init();
+            for (int i = warp; i < npages; i += C::kNW) {
+                const int s = i % C::kNSlot;
+                const bool got = mbar_wait_bounded(&full[s], (i / C::kNSlot) & 1, a.err, flags);
+                if (!__all_sync(0xffffffffu, got)) break;
+                const int nvalid = min(BS, L - (first + i) * BS);
+                const uint8_t* kp = ring + s * C::kSlotBytes;
+                cons.page(kp, kp + C::kPageBytes, nvalid, a.scale_log2, q_s, p_s, lane);
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            asm volatile("bar.sync 1, %0;" ::"r"(C::kNW * 32) : "memory");
+            if (!flags[0]) {
+                float* co = reinterpret_cast<float*>(ring);
+                float* cm = co + C::kNW * C::kHeads * C::kOStride;
+                float* cl = cm + C::kNW * C::kHeads;
+                cons.store(co, cm, cl, warp, lane, C::kOStride);
+            }
+        }
+    }
+    __syncthreads();  // pipeline finished (or abandoned); combine buffer written
+
+    if (flags[0]) {
+        // A wait gave up: let every issued copy land before the CTA's shared memory goes away.
+        if (tid == 0)
+            for (int s = 0; s < C::kNSlot; ++s)
+                if (issued[s] > 0) {
+                    const unsigned long long start = global_timer_ns();
+                    while (!mbar_try_wait(&full[s], (issued[s] - 1) & 1) &&
+                           global_timer_ns() - start < kWaitLimitNs) {
+                    }
+                }
+        return;
+    }
+
+    // ---- combine the consumer warps' states ----
+    const float* co = reinterpret_cast<const float*>(ring);
+    const float* cm = co + C::kNW * C::kHeads * C::kOStride;
+    const float* cl = cm + C::kNW * C::kHeads;
+    float* stat_m = stat;
+    float* stat_w = stat + C::kHeads;
+    float* wgt = stat + 2 * C::kHeads;  // [kNW][kHeads]
+    if (tid < gc) {
+        float mm = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < C::kNW; ++w) mm = fmaxf(mm, cm[w * C::kHeads + tid]);
+        float ws = 0.f;
+#pragma unroll
+        for (int w = 0; w < C::kNW; ++w) {
+            const float f = exp2f(cm[w * C::kHeads + tid] - mm);  // 0 for a warp that saw no page
+            wgt[w * C::kHeads + tid] = f;
+            ws += f * cl[w * C::kHeads + tid];
+        }
+        stat_m[tid] = mm;
+        stat_w[tid] = ws;
+    }
+    __syncthreads();
+    const bool single = nparts == 1;
+    for (int idx = tid; idx < gc * D; idx += C::kThreads) {
+        const int h = idx / D;
+        const int d = idx - h * D;
+        float acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < C::kNW; ++w) acc += wgt[w * C::kHeads + h] * co[(w * C::kHeads + h) * C::kOStride + d];
+        const size_t row = (size_t)b * a.num_heads + head0 + h;
+        if (single) {
+            out[row * D + d] = from_float<T>(acc / stat_w[h]);
+        } else {
+            a.ws_o[(row * a.max_parts + p) * D + d] = acc;
+        }
+    }
+    if (!single && tid < gc) {
+        const size_t row = (size_t)b * a.num_heads + head0 + tid;
+        a.ws_m[row * a.max_parts + p] = stat_m[tid];
+        a.ws_l[row * a.max_parts + p] = stat_w[tid];
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Split-KV merge: one CTA per output row (b, qh); rows whose context fits one
+// partition were finished by the decode kernel and are skipped.
+//     M = max_p m_p,  W = sum_p 2^(m_p - M) l_p,  o = sum_p 2^(m_p - M) o~_p / W.
+constexpr int kMergeThreads = 256;
+constexpr int kMergeMaxParts = 4096;
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kMergeThreads) splitkv_merge_kernel(const MergeArgs a) {
+    constexpr int kWarps = kMergeThreads / 32;
+    constexpr int DPL = D / 32;
+    __shared__ float wts[kMergeMaxParts];
+    __shared__ float red[kWarps];
+    __shared__ float part_o[kWarps][D];
+    const int row = blockIdx.x;
+    const int b = row / a.num_heads;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+    // Wait for the decode kernel's partials (programmatic dependent launch).
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    int L = __ldg(a.context_lens + b);
+    const int l_cap = min(a.max_blocks, a.max_parts * a.partition_pages) * a.block_size;
+    L = L < 0 ? 0 : (L > l_cap ? l_cap : L);
+    const int nblk = (L + a.block_size - 1) / a.block_size;
+    const int n = (nblk + a.partition_pages - 1) / a.partition_pages;
+    if (n <= 1) return;
+
+    const float* mrow = a.ws_m + (size_t)row * a.max_parts;
+    const float* lrow = a.ws_l + (size_t)row * a.max_parts;
+    // 1) global max over partitions
+    float mm = -INFINITY;
+    for (int pp = tid; pp < n; pp += kMergeThreads) mm = fmaxf(mm, __ldcg(mrow + pp));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
+    if (lane == 0) red[warp] = mm;
+    __syncthreads();
+    mm = red[0];
+#pragma unroll
+    for (int w = 1; w < kWarps; ++w) mm = fmaxf(mm, red[w]);
+    __syncthreads();
+    // 2) weights and the merged denominator
+    float ws = 0.f;
+    for (int pp = tid; pp < n; pp += kMergeThreads) {
+        const float f = exp2f(__ldcg(mrow + pp) - mm);
+        wts[pp] = f;
+        ws += f * __ldcg(lrow + pp);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, off);
+    if (lane == 0) red[warp] = ws;
+    __syncthreads();
+    ws = 0.f;
+#pragma unroll
+    for (int w = 0; w < kWarps; ++w) ws += red[w];
+    // 3) weighted sum of the partial outputs: warp w takes partitions w, w + 8, ...
+    float acc[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+    const float* obase = a.ws_o + (size_t)row * a.max_parts * D + lane * DPL;
+#pragma unroll 4
+    for (int pp = warp; pp < n; pp += kWarps) {
+        const float f = wts[pp];
+        const float* src = obase + (size_t)pp * D;
+        if constexpr (DPL % 4 == 0) {
+#pragma unroll
+            for (int e = 0; e < DPL; e += 4) {
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(src + e));
+                acc[e] += f * v.x;
+                acc[e + 1] += f * v.y;
+                acc[e + 2] += f * v.z;
+                acc[e + 3] += f * v.w;
+            }
+        } else {
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc[e] += f * __ldcg(src + e);
+        }
+    }
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) part_o[warp][lane * DPL + e] = acc[e];
+    __syncthreads();
+    T* out = static_cast<T*>(a.out) + (size_t)row * D;
+    const float inv = 1.f / ws;
+    for (int d = tid; d < D; d += kMergeThreads) {
+        float s = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) s += part_o[w][d];
+        out[d] = from_float<T>(s * inv);
+    }
+}
+
+// ------------------------------------------------------------------------------------------
+// Host-side helpers for the per-dtype translation units.
+template <typename T, int D, int BS, bool MMA, int GMAX>
+struct DecodeKernel {
+    using C = DecodeCfg<T, D, BS, MMA, GMAX>;
+
+    static bool configure(int device) {
+        static unsigned long long done_mask = 0;  // one bit per device (< 64)
+        const unsigned long long bit = 1ull << (device & 63);
+        if (done_mask & bit) return true;
+        if (cudaFuncSetAttribute(paged_decode_kernel<T, D, BS, MMA, GMAX>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
+            return false;
+        done_mask |= bit;
+        return true;
+    }
+
+    static bool info(KernelInfo* info) {
+        int device = 0;
+        if (cudaGetDevice(&device) != cudaSuccess) return false;
+        info->threads = C::kThreads;
+        info->smem_bytes = C::kSmemBytes;
+        info->heads_per_cta = C::kHeads;
+        info->merge_parts_cap = kMergeMaxParts;
+        info->ctas_per_sm = 1;
+        if (!configure(device)) return false;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_kernel<T, D, BS, MMA, GMAX>, C::kThreads,
+                                                          C::kSmemBytes) == cudaSuccess &&
+            n > 0)
+            info->ctas_per_sm = n;
+        return true;
+    }
+
+    static cudaError_t launch(const CUtensorMap& k, const CUtensorMap& v, const DecodeArgs& a, int grid,
+                              cudaStream_t stream) {
+        int device = 0;
+        cudaError_t e = cudaGetDevice(&device);
+        if (e != cudaSuccess) return e;
+        if (!configure(device)) return cudaGetLastError();
+        paged_decode_kernel<T, D, BS, MMA, GMAX><<<grid, C::kThreads, C::kSmemBytes, stream>>>(k, v, a);
+        return cudaGetLastError();
+    }
+};
+
+template <typename T, int D>
+cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.num_seqs * a.num_heads);
+    cfg.blockDim = dim3(kMergeThreads);
+    cfg.dynamicSmemBytes = 0;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, splitkv_merge_kernel<T, D>, a);
+}
+
+}  // namespace pa

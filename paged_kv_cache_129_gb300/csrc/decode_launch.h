@@ -1,0 +1,65 @@
+// Interface between the C-ABI layer and the per-dtype decode translation units.
+#pragma once
+
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace pa {
+
+// Arguments of the paged decode kernel (plain data, passed by value).
+struct DecodeArgs {
+    void* out;                   // [B, Hq, D] element type T
+    const void* q;               // [B, Hq, D]
+    const int32_t* block_tables; // [B, max_blocks]
+    const int32_t* context_lens; // [B]
+    float* ws_m;                 // [B * Hq, max_parts]   running max (log2 domain) per partition
+    float* ws_l;                 // [B * Hq, max_parts]   running denominator per partition
+    float* ws_o;                 // [B * Hq, max_parts, D] unnormalised output per partition
+    unsigned* err;               // device error word
+    int num_seqs, num_heads, num_kv_heads, group, head_chunks;
+    int max_blocks, num_blocks;
+    int partition_pages, max_parts;
+    float scale_log2;            // softmax scale * log2(e)
+};
+
+// Arguments of the split-KV merge kernel.
+struct MergeArgs {
+    void* out;
+    const int32_t* context_lens;
+    const float* ws_m;
+    const float* ws_l;
+    const float* ws_o;
+    int num_seqs, num_heads, block_size, max_blocks, partition_pages, max_parts;
+};
+
+struct KernelInfo {
+    int threads;       // threads per CTA
+    int smem_bytes;    // dynamic shared memory per CTA
+    int heads_per_cta; // query heads one CTA serves (the head-chunk width)
+    int ctas_per_sm;   // resident CTAs per SM (occupancy query)
+    int merge_parts_cap; // partitions the merge kernel can combine
+};
+
+// kind: 1 = tensor-core (mma) kernel, 2 = CUDA-core kernel; gmax: head-chunk width of the CUDA-core kernel.
+// Return false when the combination is not compiled.
+bool decode_kernel_info(int dtype, int head_dim, int block_size, int kind, int gmax, KernelInfo* info);
+cudaError_t decode_launch(int dtype, int head_dim, int block_size, int kind, int gmax, const CUtensorMap& tmap_k,
+                          const CUtensorMap& tmap_v, const DecodeArgs& args, int grid, cudaStream_t stream);
+cudaError_t merge_launch(int dtype, int head_dim, const MergeArgs& args, cudaStream_t stream);
+
+// Per-dtype entry points (one translation unit each).
+bool decode_kernel_info_f32(int head_dim, int block_size, int kind, int gmax, KernelInfo* info);
+bool decode_kernel_info_f16(int head_dim, int block_size, int kind, int gmax, KernelInfo* info);
+bool decode_kernel_info_bf16(int head_dim, int block_size, int kind, int gmax, KernelInfo* info);
+cudaError_t decode_launch_f32(int head_dim, int block_size, int kind, int gmax, const CUtensorMap& tmap_k,
+                              const CUtensorMap& tmap_v, const DecodeArgs& args, int grid, cudaStream_t stream);
+cudaError_t decode_launch_f16(int head_dim, int block_size, int kind, int gmax, const CUtensorMap& tmap_k,
+                              const CUtensorMap& tmap_v, const DecodeArgs& args, int grid, cudaStream_t stream);
+cudaError_t decode_launch_bf16(int head_dim, int block_size, int kind, int gmax, const CUtensorMap& tmap_k,
+                               const CUtensorMap& tmap_v, const DecodeArgs& args, int grid, cudaStream_t stream);
+cudaError_t merge_launch_f32(int head_dim, const MergeArgs& args, cudaStream_t stream);
+cudaError_t merge_launch_f16(int head_dim, const MergeArgs& args, cudaStream_t stream);
+cudaError_t merge_launch_bf16(int head_dim, const MergeArgs& args, cudaStream_t stream);
+
+}  // namespace pa

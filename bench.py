@@ -349,7 +349,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     max_ctx = int(lens.max())
     plan = pa.decode_plan(B, Hq, Hkv, d, bs, tables.shape[1], tdtype, max_context_len=max_ctx,
                           partition_pages=args.partition_pages, kernel=args.kernel)
-    ws = torch.empty(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
+    ws = torch.zeros(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
     lib = pa.library()
     stream = torch.cuda.current_stream(device)
     sptr = int(stream.cuda_stream)
@@ -471,8 +471,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     achieved = dec_bytes / (dec_avg_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": stored_traffic(args.workload),
-                "kernel": "pa_decode call (paged_decode_kernel" + (" + splitkv_merge_kernel)" if plan.max_parts > 1
-                                                                  else ")"),
+                "kernel": ("pa_decode call (paged_decode_lean_kernel)" if plan.schedule == 1 else
+                           "pa_decode call (paged_decode_kernel" + (" + splitkv_merge_kernel)" if plan.max_parts > 1
+                                                                    else ")")),
                 "algorithmic_bytes_per_launch": dec_bytes, "pages_touched_bytes": touched,
                 "avg_launch_ms": round(dec_avg_ms, 5), "median_launch_ms": round(statistics.median(decode_ms), 5),
                 "min_launch_ms": round(min(decode_ms), 5), "peak_source": peak_src}
@@ -500,7 +501,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
                    "step": "pa_write_kv (new token per sequence) + pa_decode",
                    "l2": f"{replicas} cache replicas rotated per step (pages touched per step "
                          f"{touched / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB)",
-                   "kernel": {1: "mma", 2: "simt"}[plan.kernel], "partition_pages": plan.partition_pages,
+                   "kernel": {1: "mma", 2: "simt"}[plan.kernel],
+                   "schedule": {0: "partitioned grid", 1: "lean persistent wave"}[plan.schedule],
+                   "partition_pages": plan.partition_pages,
                    "max_parts": plan.max_parts, "grid_ctas": plan.grid_ctas,
                    "parallelism": f"{world} independent replicas (one batch per GPU)"},
         "pct_of_hbm_peak": round(100 * value / peak, 2),

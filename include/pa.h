@@ -127,11 +127,15 @@ int pa_copy_blocks(void* key_cache, void* value_cache, const int64_t* src_dst_pa
  *  scale          softmax scale, usually 1/sqrt(head_dim).
  *  workspace      device scratch for the split-KV partials, or NULL.  With
  *                 NULL every (sequence, kv head) is done by one CTA in one
- *                 pass.  Otherwise it must hold workspace_bytes >= the size
- *                 pa_decode_workspace_size() returns for the same arguments
- *                 to use the default plan; no initialisation is needed.  A
- *                 smaller workspace is allowed: the call then uses longer
- *                 partitions.  256-byte aligned.  Calls that share a workspace
+ *                 pass.  With at least pa_decode_workspace_size() bytes the
+ *                 default (lean) schedule runs: one persistent wave of CTAs
+ *                 whose warps each stream an equal share of all pages, with
+ *                 the contexts cut at share boundaries merged in the same
+ *                 launch.  A smaller workspace selects partitioned contexts
+ *                 (a decode kernel plus a merge kernel).  The workspace must
+ *                 be zero-filled before its first use; every successful call
+ *                 leaves it ready for the next one (after PA_ERR_TIMEOUT, zero
+ *                 it again).  256-byte aligned.  Calls that share a workspace
  *                 must not overlap on the GPU.
  * Requires num_heads % num_kv_heads == 0, head_dim in {64, 128, 256},
  * block_size in {16, 32} (f32: head_dim in {64, 128}), 16-byte aligned caches,
@@ -147,9 +151,12 @@ int pa_decode(void* out, const void* query, const void* key_cache, const void* v
  *  max_context_len  an upper bound of context_lens (0 = max_blocks_per_seq *
  *                   block_size); only used to size the partitions.  A context
  *                   longer than this bound sets PA_ERR_BAD_CONTEXT.
- *  partition_pages  pages (blocks) per CTA partition: 0 = heuristic, > 0 =
- *                   exactly this (needs a workspace when it splits a context),
- *                   < 0 = one partition per context (no workspace used).
+ *  partition_pages  0 = default plan (the lean schedule when the workspace
+ *                   is large enough and num_seqs <= 4096, else partitions of
+ *                   about 512 tokens); > 0 = partitioned contexts of exactly
+ *                   this many pages (blocks) per CTA (needs a workspace when
+ *                   it splits a context); < 0 = one CTA per context (no
+ *                   workspace used).
  *  kernel           PA_KERNEL_AUTO / PA_KERNEL_MMA / PA_KERNEL_SIMT.
  */
 int pa_decode_ex(void* out, const void* query, const void* key_cache, const void* value_cache,
@@ -161,13 +168,14 @@ int pa_decode_ex(void* out, const void* query, const void* key_cache, const void
 /* The partition plan pa_decode_ex would use on the current device. */
 typedef struct pa_decode_plan {
     int kernel;            /* PA_KERNEL_MMA or PA_KERNEL_SIMT */
-    int partition_pages;   /* pages per CTA partition */
-    int max_parts;         /* partitions of the longest context */
+    int schedule;          /* 0: partitioned grid (+ merge kernel), 1: lean persistent wave */
+    int partition_pages;   /* pages per CTA partition (grid schedule; 0 for lean) */
+    int max_parts;         /* partitions of the longest context (grid schedule; 0 for lean) */
     int heads_per_cta;     /* query heads handled by one CTA */
     int grid_ctas;         /* CTAs launched */
     int threads_per_cta;
     int smem_bytes;        /* dynamic shared memory per CTA */
-    size_t workspace_bytes; /* workspace this plan needs (0 when max_parts == 1) */
+    size_t workspace_bytes; /* workspace this plan needs (0 for a single-pass grid) */
 } pa_decode_plan;
 
 int pa_decode_make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,

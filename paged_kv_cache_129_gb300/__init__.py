@@ -23,6 +23,6 @@ from .binding import (  # noqa: F401
 
 def build(force: bool = False) -> str:
     """Compile the CUDA library in-tree (nvcc, sm_103a)."""
-    from .build import build as _build
+    from .native_build import build as _build
 
     return _build(force=force)

@@ -41,7 +41,8 @@ class PoolExhausted(PAError, MemoryError):
 
 
 class DecodePlan(ctypes.Structure):
-    _fields_ = [("kernel", ctypes.c_int), ("partition_pages", ctypes.c_int), ("max_parts", ctypes.c_int),
+    _fields_ = [("kernel", ctypes.c_int), ("schedule", ctypes.c_int), ("partition_pages", ctypes.c_int),
+                ("max_parts", ctypes.c_int),
                 ("heads_per_cta", ctypes.c_int), ("grid_ctas", ctypes.c_int), ("threads_per_cta", ctypes.c_int),
                 ("smem_bytes", ctypes.c_int), ("workspace_bytes", ctypes.c_size_t)]
 

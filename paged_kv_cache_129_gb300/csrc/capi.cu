@@ -37,21 +37,22 @@ int fail(int code, const char* fmt, ...) {
 
 void clear_error() { g_message.clear(); }
 
-bool decode_kernel_info(int dtype, int head_dim, int block_size, int kind, int gmax, KernelInfo* info) {
+bool decode_kernel_info(int dtype, int head_dim, int block_size, int kind, int gmax, int num_seqs, KernelInfo* info) {
     switch (dtype) {
-        case PA_F32: return decode_kernel_info_f32(head_dim, block_size, kind, gmax, info);
-        case PA_F16: return decode_kernel_info_f16(head_dim, block_size, kind, gmax, info);
-        case PA_BF16: return decode_kernel_info_bf16(head_dim, block_size, kind, gmax, info);
+        case PA_F32: return decode_kernel_info_f32(head_dim, block_size, kind, gmax, num_seqs, info);
+        case PA_F16: return decode_kernel_info_f16(head_dim, block_size, kind, gmax, num_seqs, info);
+        case PA_BF16: return decode_kernel_info_bf16(head_dim, block_size, kind, gmax, num_seqs, info);
         default: return false;
     }
 }
 
-cudaError_t decode_launch(int dtype, int head_dim, int block_size, int kind, int gmax, const CUtensorMap& k,
-                          const CUtensorMap& v, const DecodeArgs& a, int grid, cudaStream_t s) {
+cudaError_t decode_launch(int dtype, int head_dim, int block_size, int kind, int gmax, int schedule,
+                          const CUtensorMap& k, const CUtensorMap& v, const DecodeArgs& a, int grid, int num_seqs,
+                          cudaStream_t s) {
     switch (dtype) {
-        case PA_F32: return decode_launch_f32(head_dim, block_size, kind, gmax, k, v, a, grid, s);
-        case PA_F16: return decode_launch_f16(head_dim, block_size, kind, gmax, k, v, a, grid, s);
-        case PA_BF16: return decode_launch_bf16(head_dim, block_size, kind, gmax, k, v, a, grid, s);
+        case PA_F32: return decode_launch_f32(head_dim, block_size, kind, gmax, schedule, k, v, a, grid, num_seqs, s);
+        case PA_F16: return decode_launch_f16(head_dim, block_size, kind, gmax, schedule, k, v, a, grid, num_seqs, s);
+        case PA_BF16: return decode_launch_bf16(head_dim, block_size, kind, gmax, schedule, k, v, a, grid, num_seqs, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -140,6 +141,7 @@ int encode_cache_map(CUtensorMap* map, const void* base, int dtype, int num_bloc
 
 struct Plan {
     int kind = 0;
+    int schedule = kScheduleGrid;
     int gmax = 8;
     int head_chunks = 1;
     int units = 0;
@@ -147,7 +149,8 @@ struct Plan {
     int max_parts = 1;
     long long grid = 0;
     size_t ws_bytes = 0;
-    size_t off_l = 0, off_o = 0;
+    size_t off_l = 0, off_o = 0;  // partitioned grid: offsets of l and o~ (m at 0)
+    size_t off_part = 0;          // lean: offset of the partial records (counters at 0)
     KernelInfo ki{};
 };
 
@@ -190,7 +193,7 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
         const int g = group < 8 ? group : 8;
         p.gmax = g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 8;
     }
-    if (!decode_kernel_info(dtype, head_dim, block_size, p.kind, p.gmax, &p.ki))
+    if (!decode_kernel_info(dtype, head_dim, block_size, p.kind, p.gmax, num_seqs, &p.ki))
         return fail(PA_ERR_UNSUPPORTED, "no %s decode kernel for dtype=%d head_dim=%d block_size=%d",
                     p.kind == PA_KERNEL_MMA ? "tensor-core" : "CUDA-core", dtype, head_dim, block_size);
     p.head_chunks = (group + p.ki.heads_per_cta - 1) / p.ki.heads_per_cta;
@@ -205,6 +208,26 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
     int st = current_device_state(&dev);
     if (st != PA_OK) return st;
     const long long slots = (long long)dev->num_sms * p.ki.ctas_per_sm;
+
+    // Lean schedule: one persistent wave; every consumer warp streams an equal share of all pages.
+    if (partition_pages == 0 && has_ws && num_seqs <= p.ki.lean_max_seqs &&
+        (long long)num_seqs * max_blocks < (1ll << 31)) {
+        const long long ctas = (long long)dev->num_sms * p.ki.lean_ctas_per_sm;
+        const size_t units = (size_t)num_seqs * num_kv_heads * p.head_chunks;
+        const size_t off_part = align256(units * sizeof(int));
+        const size_t need =
+            off_part + align256((size_t)ctas * p.ki.lean_warps_per_cta * 2 * p.ki.lean_record_floats * sizeof(float));
+        if (need <= ws_avail) {
+            p.schedule = kScheduleLean;
+            p.partition_pages = 0;
+            p.max_parts = 0;
+            p.grid = ctas;
+            p.ws_bytes = need;
+            p.off_part = off_part;
+            *plan = p;
+            return PA_OK;
+        }
+    }
 
     int pp;
     if (partition_pages < 0 || !has_ws) {
@@ -326,6 +349,7 @@ int pa_decode_make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_
                        workspace_bytes > 0, workspace_bytes, max_context_len, partition_pages, kernel, &p);
     if (st != PA_OK) return st;
     out->kernel = p.kind;
+    out->schedule = p.schedule;
     out->partition_pages = p.partition_pages;
     out->max_parts = p.max_parts;
     out->heads_per_cta = p.ki.heads_per_cta;
@@ -386,9 +410,12 @@ int pa_decode_ex(void* out, const void* query, const void* key_cache, const void
     a.block_tables = block_tables;
     a.context_lens = context_lens;
     char* ws = static_cast<char*>(workspace);
-    a.ws_m = p.max_parts > 1 ? reinterpret_cast<float*>(ws) : nullptr;
-    a.ws_l = p.max_parts > 1 ? reinterpret_cast<float*>(ws + p.off_l) : nullptr;
-    a.ws_o = p.max_parts > 1 ? reinterpret_cast<float*>(ws + p.off_o) : nullptr;
+    const bool grid_split = p.schedule == kScheduleGrid && p.max_parts > 1;
+    a.ws_m = grid_split ? reinterpret_cast<float*>(ws) : nullptr;
+    a.ws_l = grid_split ? reinterpret_cast<float*>(ws + p.off_l) : nullptr;
+    a.ws_o = grid_split ? reinterpret_cast<float*>(ws + p.off_o) : nullptr;
+    a.ws_count = p.schedule == kScheduleLean ? reinterpret_cast<int*>(ws) : nullptr;
+    a.ws_part = p.schedule == kScheduleLean ? reinterpret_cast<float*>(ws + p.off_part) : nullptr;
     a.err = dev->error_word;
     a.num_seqs = num_seqs;
     a.num_heads = num_heads;
@@ -401,9 +428,10 @@ int pa_decode_ex(void* out, const void* query, const void* key_cache, const void
     a.max_parts = p.max_parts;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);  // log2(e)
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e = decode_launch(dtype, head_dim, block_size, p.kind, p.gmax, tk, tv, a, (int)p.grid, s);
+    cudaError_t e =
+        decode_launch(dtype, head_dim, block_size, p.kind, p.gmax, p.schedule, tk, tv, a, (int)p.grid, num_seqs, s);
     if (e != cudaSuccess) return cuda_fail(e, "pa_decode: decode kernel launch");
-    if (p.max_parts > 1) {
+    if (grid_split) {
         MergeArgs m{out,        context_lens, a.ws_m,     a.ws_l,          a.ws_o,
                     num_seqs,   num_heads,    block_size, max_blocks_per_seq, p.partition_pages,
                     p.max_parts};

@@ -31,17 +31,20 @@ bool dispatch(int d, int bs, int kind, int gmax, F&& f) {
 
 }  // namespace
 
-bool decode_kernel_info_f32(int head_dim, int block_size, int kind, int gmax, KernelInfo* info) {
+bool decode_kernel_info_f32(int head_dim, int block_size, int kind, int gmax, int num_seqs, KernelInfo* info) {
     bool ok = false;
-    const bool found = dispatch(head_dim, block_size, kind, gmax, [&](auto k) { ok = decltype(k)::info(info); });
+    const bool found =
+        dispatch(head_dim, block_size, kind, gmax, [&](auto k) { ok = decltype(k)::info(num_seqs, info); });
     return found && ok;
 }
 
-cudaError_t decode_launch_f32(int head_dim, int block_size, int kind, int gmax, const CUtensorMap& tmap_k,
-                              const CUtensorMap& tmap_v, const DecodeArgs& args, int grid, cudaStream_t stream) {
+cudaError_t decode_launch_f32(int head_dim, int block_size, int kind, int gmax, int schedule,
+                              const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, const DecodeArgs& args,
+                              int grid, int num_seqs, cudaStream_t stream) {
     cudaError_t err = cudaErrorInvalidValue;
-    dispatch(head_dim, block_size, kind, gmax,
-             [&](auto k) { err = decltype(k)::launch(tmap_k, tmap_v, args, grid, stream); });
+    dispatch(head_dim, block_size, kind, gmax, [&](auto k) {
+        err = decltype(k)::launch(schedule, tmap_k, tmap_v, args, grid, num_seqs, stream);
+    });
     return err;
 }
 

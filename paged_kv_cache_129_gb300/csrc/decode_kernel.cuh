@@ -36,6 +36,7 @@
 #pragma once
 
 #include <cfloat>
+#include <type_traits>
 
 #include "decode_launch.h"
 #include "pa_common.cuh"
@@ -181,6 +182,54 @@ struct MmaConsumer {
         }
     }
 
+    // Complete the per-head denominators (sum over the quad); call once after a unit's last page.
+    __device__ __forceinline__ void finish() {
+        l += __shfl_xor_sync(0xffffffffu, l, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+    }
+
+    // out_rows[h * D + d] = o~ / l for the gc heads (after finish()).
+    __device__ __forceinline__ void write_out(T* out_rows, int gc, int lane) const {
+        const int g = lane >> 2, t = lane & 3;
+        const float inv_lo = 1.f / __shfl_sync(0xffffffffu, l, (2 * t) * 4);
+        const float inv_hi = 1.f / __shfl_sync(0xffffffffu, l, (2 * t + 1) * 4);
+        T* lo = out_rows + (size_t)(2 * t) * D;
+        T* hi = out_rows + (size_t)(2 * t + 1) * D;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            if (2 * t < gc) {
+                lo[mt * 16 + g] = from_float<T>(o[mt][0] * inv_lo);
+                lo[mt * 16 + 8 + g] = from_float<T>(o[mt][2] * inv_lo);
+            }
+            if (2 * t + 1 < gc) {
+                hi[mt * 16 + g] = from_float<T>(o[mt][1] * inv_hi);
+                hi[mt * 16 + 8 + g] = from_float<T>(o[mt][3] * inv_hi);
+            }
+        }
+    }
+
+    // Partial record of kHeads = 8 heads: m[8], l[8], o~[8][D] (after finish()).
+    __device__ __forceinline__ void write_partial(float* rec, int gc, int lane) const {
+        const int g = lane >> 2, t = lane & 3;
+        if (t == 0 && g < gc) {
+            rec[g] = m;
+            rec[8 + g] = l;
+        }
+        float* lo = rec + 16 + (size_t)(2 * t) * D;
+        float* hi = rec + 16 + (size_t)(2 * t + 1) * D;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            if (2 * t < gc) {
+                lo[mt * 16 + g] = o[mt][0];
+                lo[mt * 16 + 8 + g] = o[mt][2];
+            }
+            if (2 * t + 1 < gc) {
+                hi[mt * 16 + g] = o[mt][1];
+                hi[mt * 16 + 8 + g] = o[mt][3];
+            }
+        }
+    }
+
     // Write this warp's state into the CTA combine buffer.
     __device__ __forceinline__ void store(float* co, float* cm, float* cl, int warp, int lane, int ostride) {
         const int g = lane >> 2, t = lane & 3;
@@ -298,6 +347,39 @@ struct SimtConsumer {
             }
         }
         __syncwarp();
+    }
+
+    __device__ __forceinline__ void finish() {
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h)
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
+    }
+
+    __device__ __forceinline__ void write_out(T* out_rows, int gc, int lane) const {
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+            if (h >= gc) break;
+            const float inv = 1.f / l[h];
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) out_rows[(size_t)h * D + lane * DPL + e] = from_float<T>(o[h][e] * inv);
+        }
+    }
+
+    // Partial record of GMAX heads: m[GMAX], l[GMAX], then o~[GMAX][D] at a 16-byte
+    // aligned offset (after finish()).
+    __device__ __forceinline__ void write_partial(float* rec, int gc, int lane) const {
+        constexpr int kOOff = ((2 * GMAX + 3) / 4) * 4;
+#pragma unroll
+        for (int h = 0; h < GMAX; ++h) {
+            if (h >= gc) break;
+            if (lane == 0) {
+                rec[h] = m[h];
+                rec[GMAX + h] = l[h];
+            }
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) rec[kOOff + (size_t)h * D + lane * DPL + e] = o[h][e];
+        }
     }
 
     __device__ __forceinline__ void store(float* co, float* cm, float* cl, int warp, int lane, int ostride) {
@@ -628,11 +710,371 @@ __global__ void __launch_bounds__(kMergeThreads) splitkv_merge_kernel(const Merg
     }
 }
 
+
+// ------------------------------------------------------------------------------------------
+// Lean (stream-K) schedule.  A persistent grid of C CTAs (one wave); the pages
+// of all (sequence, kv head, head chunk) units are laid end to end (sequence-
+// major, then kv head, then head chunk, pages in logical order) and cut into
+// C * NW equal contiguous ranges, one per consumer warp.  So every warp streams
+// the same number of pages whatever the context lengths are.  A warp finishes
+// every unit that lies wholly inside its range (o = o~ / l straight to out);
+// for a unit cut by a range boundary it writes a partial (m, l, o~) record, and
+// the last of that unit's warps to finish (per-unit arrival counters in the
+// workspace, reset by the merging warp) merges the records in warp order, with
+// the same rescaling rule as the online softmax.
+constexpr int kLeanMaxSeqs = 4096;
+
+template <typename T, int D, int BS, bool MMA, int GMAX>
+struct LeanCfg {
+    using Base = DecodeCfg<T, D, BS, MMA, GMAX>;
+    static constexpr int kNW = Base::kNW;
+    static constexpr int kThreads = Base::kThreads;
+    // Page slots per consumer warp: about 64 KB of ring per CTA, between 1 and 3 slots a warp.
+    static constexpr int kSPWRaw = 65536 / (kNW * Base::kSlotBytes);
+    static constexpr int kSPW = kSPWRaw < 1 ? 1 : (kSPWRaw > 3 ? 3 : kSPWRaw);
+    static constexpr int kNSlot = kNW * kSPW;
+    static constexpr int kSlotBytes = Base::kSlotBytes;
+    static constexpr int kPageBytes = Base::kPageBytes;
+    static constexpr int kRingBytes = kNSlot * kSlotBytes;
+    static constexpr int kHeads = Base::kHeads;
+    static constexpr int kOOff = ((2 * kHeads + 3) / 4) * 4;  // o~ offset in a partial record
+    static constexpr int kRecFloats = kOOff + kHeads * D;      // one partial record
+    static constexpr int kBarOffset = kRingBytes;
+    static constexpr int kIssuedOffset = kBarOffset + 2 * kNSlot * 8;
+    static constexpr int kFlagOffset = kIssuedOffset + kNSlot * 4;
+    static constexpr int kScanOffset = kFlagOffset + 16;
+    static constexpr int kQsOffset = kScanOffset + 32;
+    static constexpr int kQsBytes = MMA ? 0 : kNW * GMAX * D * 4;  // one fp32 q block per warp
+    static constexpr int kPsOffset = kQsOffset + kQsBytes;
+    static constexpr int kPsBytes = MMA ? 0 : kNW * GMAX * BS * 4;
+    static constexpr int kPrefixOffset = kPsOffset + kPsBytes;      // then (num_seqs + 1) ints
+    static constexpr int kFixedSmemBytes = kPrefixOffset + 1024;      // + slack to align the base
+    static constexpr int kMaxSmemBytes = kFixedSmemBytes + (kLeanMaxSeqs + 1) * 4;
+    static int smem_bytes(int num_seqs) { return kFixedSmemBytes + (num_seqs + 1) * 4; }
+    static_assert(kMaxSmemBytes <= 227 * 1024, "shared memory per CTA");
+    static_assert(kOOff % 4 == 0 && kRecFloats % 4 == 0, "16-byte aligned records");
+};
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+
+__device__ __forceinline__ float warp_sum(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v += __shfl_xor_sync(0xffffffffu, v, off);
+    return v;
+}
+
+// Exclusive prefix sum over the CTA's threads; *total receives the sum of all values.
+__device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int nwarps, int* total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int x = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, x, off);
+        if (lane >= off) x += y;
+    }
+    if (lane == 31) warp_sums[warp] = x;
+    __syncthreads();
+    int base = 0, tot = 0;
+    for (int w = 0; w < nwarps; ++w) {
+        const int ws = warp_sums[w];
+        if (w < warp) base += ws;
+        tot += ws;
+    }
+    *total = tot;
+    return base + x - v;
+}
+
+// Global page g -> sequence b, unit within the sequence uu, page j within the unit, pages per unit nb.
+__device__ __forceinline__ void lean_locate(const int* pre, int num_seqs, int upb, long long g, int& b, int& uu,
+                                            int& j, int& nb) {
+    int lo = 0, hi = num_seqs - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if ((long long)pre[mid] * upb <= g) lo = mid;
+        else hi = mid - 1;
+    }
+    b = lo;
+    nb = pre[b + 1] - pre[b];
+    const long long r = g - (long long)pre[b] * upb;
+    uu = (int)(r / nb);
+    j = (int)(r - (long long)uu * nb);
+}
+
+// Merge the partial records of one unit (warps w_lo..w_hi) into out_rows.
+template <typename T, int D, int H>
+__device__ void lean_merge(const float* ws_part, long long w_lo, long long w_hi, long long unit_first, long long q,
+                           int gc, T* out_rows, int lane) {
+    constexpr int kOOff = ((2 * H + 3) / 4) * 4;
+    constexpr int kRec = kOOff + H * D;
+    constexpr int DPL = D / 32;
+    const int n = (int)(w_hi - w_lo + 1);
+    // The first warp keeps this unit in slot 1 (its last unit) unless its range starts at the unit.
+    const int slot0 = unit_first != w_lo * q ? 1 : 0;
+    auto rec = [&](int p) -> const float* {
+        return ws_part + ((size_t)(w_lo + p) * 2 + (p == 0 ? slot0 : 0)) * kRec;
+    };
+    for (int h = 0; h < gc; ++h) {
+        float mx = -INFINITY;
+        for (int p = lane; p < n; p += 32) mx = fmaxf(mx, __ldcg(rec(p) + h));
+        mx = warp_max(mx);
+        float den = 0.f;
+        for (int p = lane; p < n; p += 32) den += exp2f(__ldcg(rec(p) + h) - mx) * __ldcg(rec(p) + H + h);
+        den = warp_sum(den);
+        float acc[DPL];
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+#pragma unroll 4
+        for (int p = 0; p < n; ++p) {
+            const float* r = rec(p);
+            const float f = exp2f(__ldcg(r + h) - mx);
+            const float* src = r + kOOff + h * D + lane * DPL;
+            if constexpr (DPL % 4 == 0) {
+#pragma unroll
+                for (int e = 0; e < DPL; e += 4) {
+                    const float4 v = __ldcg(reinterpret_cast<const float4*>(src + e));
+                    acc[e] += f * v.x;
+                    acc[e + 1] += f * v.y;
+                    acc[e + 2] += f * v.z;
+                    acc[e + 3] += f * v.w;
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) acc[e] += f * __ldcg(src + e);
+            }
+        }
+        const float inv = 1.f / den;
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) out_rows[(size_t)h * D + lane * DPL + e] = from_float<T>(acc[e] * inv);
+    }
+}
+
+template <typename T, int D, int BS, bool MMA, int GMAX>
+__global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
+    paged_decode_lean_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                             const DecodeArgs a) {
+    using C = LeanCfg<T, D, BS, MMA, GMAX>;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ring = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+    uint64_t* empty = full + C::kNSlot;
+    int* issued = reinterpret_cast<int*>(smem + C::kIssuedOffset);
+    volatile int* flags = reinterpret_cast<volatile int*>(smem + C::kFlagOffset);  // [0]: abort
+    int* warp_sums = reinterpret_cast<int*>(smem + C::kScanOffset);
+    int* pre = reinterpret_cast<int*>(smem + C::kPrefixOffset);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int B = a.num_seqs;
+    const int l_cap = a.max_blocks * BS;
+    T* out = static_cast<T*>(a.out);
+
+    // ---- pages per sequence (context lengths clamped to the table), prefix sums ----
+    const int per = (B + C::kThreads - 1) / C::kThreads;
+    const int b_lo = min(B, tid * per);
+    const int b_hi = min(B, b_lo + per);
+    int mine = 0;
+    for (int b = b_lo; b < b_hi; ++b) {
+        int L = __ldg(a.context_lens + b);
+        if (L < 0 || L > l_cap) {
+            if (blockIdx.x == 0) atomicOr(a.err, kErrBadContext);
+            L = L < 0 ? 0 : l_cap;
+        }
+        pre[b] = (L + BS - 1) / BS;
+        mine += pre[b];
+    }
+    int total_pages = 0;
+    int acc = block_exclusive_scan(mine, warp_sums, C::kNW + 1, &total_pages);
+    for (int b = b_lo; b < b_hi; ++b) {
+        const int n = pre[b];
+        pre[b] = acc;
+        acc += n;
+    }
+    if (tid == 0) {
+        pre[B] = total_pages;
+        for (int s = 0; s < C::kNSlot; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            issued[s] = 0;
+        }
+        flags[0] = 0;
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    const int upb = a.num_kv_heads * a.head_chunks;  // units per sequence
+    const long long total = (long long)total_pages * upb;
+    const long long q_per_warp = (total + (long long)gridDim.x * C::kNW - 1) / ((long long)gridDim.x * C::kNW);
+
+    // Empty contexts produce zero rows (spread over the CTAs).
+    for (int b = warp; b < B; b += C::kNW + 1)
+        if (pre[b] == pre[b + 1] && (b % (int)gridDim.x) == (int)blockIdx.x)
+            for (int idx = lane; idx < a.num_heads * D; idx += 32)
+                out[(size_t)b * a.num_heads * D + idx] = from_float<T>(0.f);
+    if (total == 0) return;
+
+    if (warp == C::kNW) {
+        // ================= producer warp =================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_k);
+            tma_prefetch_desc(&tmap_v);
+        }
+        // Lane l serves consumer warp (l & 3), page offsets k + (l >> 2) of each round of 8.
+        const int w = lane & 3;
+        const long long lo_w = min(total, ((long long)blockIdx.x * C::kNW + w) * q_per_warp);
+        const long long hi_w = min(total, lo_w + q_per_warp);
+        const int n_w = (int)(hi_w - lo_w);
+        const int n_max = __reduce_max_sync(0xffffffffu, n_w);
+        bool ok = true;
+        for (int k = 0; k < n_max && ok; k += 8) {
+            const int off = k + (lane >> 2);
+            int row = 0, bad = 0;
+            if (off < n_w) {
+                int b, uu, j, nb;
+                lean_locate(pre, B, upb, lo_w + off, b, uu, j, nb);
+                const int kvh = uu / a.head_chunks;
+                const int pb = __ldg(a.block_tables + (size_t)b * a.max_blocks + j);
+                if ((unsigned)pb < (unsigned)a.num_blocks) row = (pb * a.num_kv_heads + kvh) * BS;
+                else bad = 1;
+            }
+            for (int i = 0; i < 32; ++i) {
+                const int off_i = k + (i >> 2);
+                const int n_i = __shfl_sync(0xffffffffu, n_w, i & 3);
+                const int row_i = __shfl_sync(0xffffffffu, row, i);
+                const int bad_i = __shfl_sync(0xffffffffu, bad, i);
+                if (off_i >= n_i) continue;  // uniform over the warp
+                int good = 1;
+                if (lane == 0) {
+                    const int s = (i & 3) * C::kSPW + off_i % C::kSPW;
+                    const int use = off_i / C::kSPW;
+                    if (use >= 1) good = mbar_wait_bounded(&empty[s], (use - 1) & 1, a.err, flags) ? 1 : 0;
+                    if (good) {
+                        issued[s] += 1;
+                        if (!bad_i) {
+                            mbar_arrive_expect_tx(&full[s], C::kSlotBytes);
+                            uint8_t* kdst = ring + s * C::kSlotBytes;
+                            uint8_t* vdst = kdst + C::kPageBytes;
+#pragma unroll
+                            for (int bx = 0; bx < C::Base::kNBox; ++bx)
+                                tma_load_2d(kdst + bx * C::Base::kBoxBytes, &tmap_k, bx * C::Base::kBoxElems, row_i,
+                                            &full[s]);
+#pragma unroll
+                            for (int bx = 0; bx < C::Base::kNBox; ++bx)
+                                tma_load_2d(vdst + bx * C::Base::kBoxBytes, &tmap_v, bx * C::Base::kBoxElems, row_i,
+                                            &full[s]);
+                        } else {
+                            atomicOr(a.err, kErrBadTable);  // skip the load; the slot keeps stale data
+                            mbar_arrive(&full[s]);
+                        }
+                    }
+                }
+                ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+                if (!ok) break;
+            }
+        }
+    } else {
+        // ================= consumer warps =================
+        const long long wg = (long long)blockIdx.x * C::kNW + warp;
+        const long long lo = min(total, wg * q_per_warp);
+        const long long hi = min(total, lo + q_per_warp);
+        const int n = (int)(hi - lo);
+        long long unit_first = 0, unit_last = -1;
+        int b = 0, uu = 0, nb = 0, L = 0, head0 = 0, gc = 0;
+        std::conditional_t<MMA, MmaConsumer<T, D, BS>, SimtConsumer<T, D, BS, GMAX>> cons;
+        float* q_s = reinterpret_cast<float*>(smem + C::kQsOffset) + warp * GMAX * D;
+        float* p_s = reinterpret_cast<float*>(smem + C::kPsOffset) + warp * GMAX * BS;
+        for (int off = 0; off < n; ++off) {
+            const long long g = lo + off;
+            if (g > unit_last) {  // a new unit starts
+                int j0;
+                lean_locate(pre, B, upb, g, b, uu, j0, nb);
+                unit_first = g - j0;
+                unit_last = unit_first + nb - 1;
+                const int kvh = uu / a.head_chunks;
+                const int hc = uu - kvh * a.head_chunks;
+                head0 = kvh * a.group + hc * C::kHeads;
+                gc = min(C::kHeads, a.group - hc * C::kHeads);
+                L = __ldg(a.context_lens + b);
+                L = L < 0 ? 0 : (L > l_cap ? l_cap : L);
+                const T* qrows = static_cast<const T*>(a.q) + ((size_t)b * a.num_heads + head0) * D;
+                if constexpr (MMA) {
+                    cons.init(qrows, gc, lane);
+                } else {
+                    __syncwarp();
+                    for (int idx = lane; idx < GMAX * D; idx += 32)
+                        q_s[idx] = idx / D < gc ? to_float(qrows[idx]) : 0.f;
+                    __syncwarp();
+                    cons.init();
+                }
+            }
+            const int j = (int)(g - unit_first);
+            const int s = warp * C::kSPW + off % C::kSPW;
+            const bool got = mbar_wait_bounded(&full[s], (off / C::kSPW) & 1, a.err, flags);
+            if (!__all_sync(0xffffffffu, got)) break;
+            const int nvalid = min(BS, L - j * BS);
+            uint8_t* kp = ring + s * C::kSlotBytes;
+            if constexpr (MMA) {
+                cons.page(kp, kp + C::kPageBytes, nvalid, a.scale_log2, lane);
+                __syncwarp();
+            } else {
+                cons.page(kp, kp + C::kPageBytes, nvalid, a.scale_log2, q_s, p_s, lane);
+            }
+            if (lane == 0) mbar_arrive(&empty[s]);
+
+            if (g == unit_last || off == n - 1) {  // this warp is done with the unit
+                cons.finish();
+                T* out_rows = out + ((size_t)b * a.num_heads + head0) * D;
+                if (unit_first >= lo && unit_last < hi) {
+                    cons.write_out(out_rows, gc, lane);
+                } else {
+                    const int slot = unit_first <= lo ? 0 : 1;  // 0: the warp's first unit, 1: its last
+                    float* rec = a.ws_part + ((size_t)wg * 2 + slot) * C::kRecFloats;
+                    cons.write_partial(rec, gc, lane);
+                    __threadfence();
+                    __syncwarp();
+                    const long long w_lo = unit_first / q_per_warp;
+                    const long long w_hi = unit_last / q_per_warp;
+                    int last = 0;
+                    if (lane == 0) {
+                        int* cnt = a.ws_count + (size_t)b * upb + uu;
+                        last = atomicAdd(cnt, 1) == (int)(w_hi - w_lo);
+                        if (last) *cnt = 0;  // ready for the next call
+                    }
+                    last = __shfl_sync(0xffffffffu, last, 0);
+                    if (last) {
+                        __threadfence();
+                        lean_merge<T, D, C::kHeads>(a.ws_part, w_lo, w_hi, unit_first, q_per_warp, gc, out_rows,
+                                                    lane);
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (flags[0]) {
+        // A wait gave up: let every issued copy land before the CTA's shared memory goes away.
+        if (tid == 0)
+            for (int s = 0; s < C::kNSlot; ++s)
+                if (issued[s] > 0) {
+                    const unsigned long long start = global_timer_ns();
+                    while (!mbar_try_wait(&full[s], (issued[s] - 1) & 1) &&
+                           global_timer_ns() - start < kWaitLimitNs) {
+                    }
+                }
+    }
+}
+
 // ------------------------------------------------------------------------------------------
 // Host-side helpers for the per-dtype translation units.
 template <typename T, int D, int BS, bool MMA, int GMAX>
 struct DecodeKernel {
     using C = DecodeCfg<T, D, BS, MMA, GMAX>;
+    using LC = LeanCfg<T, D, BS, MMA, GMAX>;
 
     static bool configure(int device) {
         static unsigned long long done_mask = 0;  // one bit per device (< 64)
@@ -641,34 +1083,63 @@ struct DecodeKernel {
         if (cudaFuncSetAttribute(paged_decode_kernel<T, D, BS, MMA, GMAX>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
             return false;
+        if (cudaFuncSetAttribute(paged_decode_lean_kernel<T, D, BS, MMA, GMAX>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, LC::kMaxSmemBytes) != cudaSuccess)
+            return false;
         done_mask |= bit;
         return true;
     }
 
-    static bool info(KernelInfo* info) {
+    // Resident lean CTAs per SM for a given dynamic shared-memory size (memoised per device and KB).
+    static int lean_occupancy(int device, int smem) {
+        static int cache[64][232] = {};
+        const int kb = (smem + 1023) / 1024;
+        int& slot = cache[device & 63][kb < 232 ? kb : 231];
+        if (slot) return slot;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_lean_kernel<T, D, BS, MMA, GMAX>,
+                                                          LC::kThreads, kb * 1024) != cudaSuccess ||
+            n <= 0)
+            n = 1;
+        slot = n;
+        return n;
+    }
+
+    static bool info(int num_seqs, KernelInfo* info) {
         int device = 0;
         if (cudaGetDevice(&device) != cudaSuccess) return false;
+        if (!configure(device)) return false;
         info->threads = C::kThreads;
         info->smem_bytes = C::kSmemBytes;
         info->heads_per_cta = C::kHeads;
         info->merge_parts_cap = kMergeMaxParts;
         info->ctas_per_sm = 1;
-        if (!configure(device)) return false;
         int n = 0;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_kernel<T, D, BS, MMA, GMAX>, C::kThreads,
                                                           C::kSmemBytes) == cudaSuccess &&
             n > 0)
             info->ctas_per_sm = n;
+        const int seqs = num_seqs < 1 ? 1 : (num_seqs > kLeanMaxSeqs ? kLeanMaxSeqs : num_seqs);
+        info->lean_smem_bytes = LC::smem_bytes(seqs);
+        info->lean_ctas_per_sm = lean_occupancy(device, info->lean_smem_bytes);
+        info->lean_warps_per_cta = LC::kNW;
+        info->lean_record_floats = LC::kRecFloats;
+        info->lean_max_seqs = kLeanMaxSeqs;
         return true;
     }
 
-    static cudaError_t launch(const CUtensorMap& k, const CUtensorMap& v, const DecodeArgs& a, int grid,
-                              cudaStream_t stream) {
+    static cudaError_t launch(int schedule, const CUtensorMap& k, const CUtensorMap& v, const DecodeArgs& a, int grid,
+                              int num_seqs, cudaStream_t stream) {
         int device = 0;
         cudaError_t e = cudaGetDevice(&device);
         if (e != cudaSuccess) return e;
         if (!configure(device)) return cudaGetLastError();
-        paged_decode_kernel<T, D, BS, MMA, GMAX><<<grid, C::kThreads, C::kSmemBytes, stream>>>(k, v, a);
+        if (schedule == kScheduleLean) {
+            paged_decode_lean_kernel<T, D, BS, MMA, GMAX>
+                <<<grid, LC::kThreads, LC::smem_bytes(num_seqs), stream>>>(k, v, a);
+        } else {
+            paged_decode_kernel<T, D, BS, MMA, GMAX><<<grid, C::kThreads, C::kSmemBytes, stream>>>(k, v, a);
+        }
         return cudaGetLastError();
     }
 };

@@ -16,6 +16,8 @@ struct DecodeArgs {
     float* ws_m;                 // [B * Hq, max_parts]   running max (log2 domain) per partition
     float* ws_l;                 // [B * Hq, max_parts]   running denominator per partition
     float* ws_o;                 // [B * Hq, max_parts, D] unnormalised output per partition
+    int* ws_count;               // lean schedule: per-unit arrival counters (zero between calls)
+    float* ws_part;              // lean schedule: two partial records per consumer warp
     unsigned* err;               // device error word
     int num_seqs, num_heads, num_kv_heads, group, head_chunks;
     int max_blocks, num_blocks;
@@ -34,30 +36,41 @@ struct MergeArgs {
 };
 
 struct KernelInfo {
-    int threads;       // threads per CTA
-    int smem_bytes;    // dynamic shared memory per CTA
-    int heads_per_cta; // query heads one CTA serves (the head-chunk width)
-    int ctas_per_sm;   // resident CTAs per SM (occupancy query)
-    int merge_parts_cap; // partitions the merge kernel can combine
+    int threads;          // threads per CTA
+    int smem_bytes;       // dynamic shared memory per CTA (partitioned-grid schedule)
+    int heads_per_cta;    // query heads one CTA (or warp) serves: the head-chunk width
+    int ctas_per_sm;      // resident CTAs per SM, partitioned-grid schedule
+    int merge_parts_cap;  // partitions the merge kernel can combine
+    int lean_smem_bytes;  // dynamic shared memory per CTA, lean schedule, for the given num_seqs
+    int lean_ctas_per_sm; // resident CTAs per SM, lean schedule
+    int lean_warps_per_cta;
+    int lean_record_floats; // floats of one partial record
+    int lean_max_seqs;
 };
+
+enum Schedule { kScheduleGrid = 0, kScheduleLean = 1 };
 
 // kind: 1 = tensor-core (mma) kernel, 2 = CUDA-core kernel; gmax: head-chunk width of the CUDA-core kernel.
 // Return false when the combination is not compiled.
-bool decode_kernel_info(int dtype, int head_dim, int block_size, int kind, int gmax, KernelInfo* info);
-cudaError_t decode_launch(int dtype, int head_dim, int block_size, int kind, int gmax, const CUtensorMap& tmap_k,
-                          const CUtensorMap& tmap_v, const DecodeArgs& args, int grid, cudaStream_t stream);
+bool decode_kernel_info(int dtype, int head_dim, int block_size, int kind, int gmax, int num_seqs, KernelInfo* info);
+cudaError_t decode_launch(int dtype, int head_dim, int block_size, int kind, int gmax, int schedule,
+                          const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, const DecodeArgs& args, int grid,
+                          int num_seqs, cudaStream_t stream);
 cudaError_t merge_launch(int dtype, int head_dim, const MergeArgs& args, cudaStream_t stream);
 
 // Per-dtype entry points (one translation unit each).
-bool decode_kernel_info_f32(int head_dim, int block_size, int kind, int gmax, KernelInfo* info);
-bool decode_kernel_info_f16(int head_dim, int block_size, int kind, int gmax, KernelInfo* info);
-bool decode_kernel_info_bf16(int head_dim, int block_size, int kind, int gmax, KernelInfo* info);
-cudaError_t decode_launch_f32(int head_dim, int block_size, int kind, int gmax, const CUtensorMap& tmap_k,
-                              const CUtensorMap& tmap_v, const DecodeArgs& args, int grid, cudaStream_t stream);
-cudaError_t decode_launch_f16(int head_dim, int block_size, int kind, int gmax, const CUtensorMap& tmap_k,
-                              const CUtensorMap& tmap_v, const DecodeArgs& args, int grid, cudaStream_t stream);
-cudaError_t decode_launch_bf16(int head_dim, int block_size, int kind, int gmax, const CUtensorMap& tmap_k,
-                               const CUtensorMap& tmap_v, const DecodeArgs& args, int grid, cudaStream_t stream);
+bool decode_kernel_info_f32(int head_dim, int block_size, int kind, int gmax, int num_seqs, KernelInfo* info);
+bool decode_kernel_info_f16(int head_dim, int block_size, int kind, int gmax, int num_seqs, KernelInfo* info);
+bool decode_kernel_info_bf16(int head_dim, int block_size, int kind, int gmax, int num_seqs, KernelInfo* info);
+cudaError_t decode_launch_f32(int head_dim, int block_size, int kind, int gmax, int schedule,
+                              const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, const DecodeArgs& args,
+                              int grid, int num_seqs, cudaStream_t stream);
+cudaError_t decode_launch_f16(int head_dim, int block_size, int kind, int gmax, int schedule,
+                              const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, const DecodeArgs& args,
+                              int grid, int num_seqs, cudaStream_t stream);
+cudaError_t decode_launch_bf16(int head_dim, int block_size, int kind, int gmax, int schedule,
+                              const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, const DecodeArgs& args,
+                              int grid, int num_seqs, cudaStream_t stream);
 cudaError_t merge_launch_f32(int head_dim, const MergeArgs& args, cudaStream_t stream);
 cudaError_t merge_launch_f16(int head_dim, const MergeArgs& args, cudaStream_t stream);
 cudaError_t merge_launch_bf16(int head_dim, const MergeArgs& args, cudaStream_t stream);

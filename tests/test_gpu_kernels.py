@@ -44,7 +44,7 @@ def gpu_decode(inp, dev=None, partition_pages=0, kernel="auto", max_context_len=
                               inp.max_blocks_per_seq, dev["q"].dtype, max_context_len=max_context_len,
                               partition_pages=partition_pages, kernel=kernel)
         if plan.workspace_bytes:
-            ws = torch.empty(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+            ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
     out = pa.decode(dev["q"], dev["kc"], dev["vc"], dev["bt"], dev["lens"], scale=inp.scale, workspace=ws,
                     partition_pages=partition_pages, kernel=kernel, max_context_len=max_context_len)
     torch.cuda.synchronize()
@@ -257,3 +257,49 @@ def test_write_then_decode_sees_the_new_token():
     got = to_f64(gpu_decode(inp, dev=dev))
     assert oracle.write_kv(newk, newv, inp.key_cache, inp.value_cache, slots) == 0
     assert_decode_close(got, oracle.decode_inputs(inp), "bf16")
+
+
+# ---- lean (stream-K) schedule ------------------------------------------------------------------
+LEAN_LENS = [
+    (1,),
+    (0, 0, 0),
+    (5, 0, 2000, 0, 17),
+    tuple(range(0, 700, 7)),
+    (4096,) * 3 + (1,) * 40,
+]
+
+
+@pytest.mark.parametrize("lens", LEAN_LENS, ids=["one", "all_empty", "mixed", "ramp100", "skewed"])
+@pytest.mark.parametrize("dtype,kernel,hq,hkv", [("bf16", "mma", 28, 4), ("f16", "mma", 32, 2),
+                                                  ("f16", "simt", 8, 2), ("f32", "simt", 4, 2)])
+def test_lean_schedule_matches_oracle(lens, dtype, kernel, hq, hkv):
+    inp = case(dtype, 128, 16, hq, hkv, lens, seed=len(lens) + hq)
+    plan = pa.decode_plan(inp.num_seqs, hq, hkv, 128, 16, inp.max_blocks_per_seq, TORCH[dtype], kernel=kernel)
+    assert plan.schedule == 1
+    got = to_f64(gpu_decode(inp, kernel=kernel))
+    assert_decode_close(got, oracle.decode_inputs(inp), dtype)
+    pa.check_error()
+
+
+def test_lean_workspace_is_reusable_across_calls():
+    # the per-unit arrival counters must be back at zero after every call
+    plan = pa.decode_plan(64, 28, 4, 128, 16, 300, torch.bfloat16)
+    ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    for seed, lens in ((1, (300 * 16, 17, 4000, 1)), (2, (1000,) * 9), (3, tuple(range(1, 4800, 97)))):
+        inp = case("bf16", 128, 16, 28, 4, lens, seed=seed)
+        dev = upload(inp)
+        for _ in range(2):
+            out = pa.decode(dev["q"], dev["kc"], dev["vc"], dev["bt"], dev["lens"], scale=inp.scale, workspace=ws)
+            torch.cuda.synchronize()
+            assert_decode_close(to_f64(out), oracle.decode_inputs(inp), "bf16")
+    pa.check_error()
+
+
+def test_many_sequences_fall_back_to_the_partitioned_grid():
+    inp = case("bf16", 128, 16, 4, 4, (1, 3) * 2100, seed=30)
+    plan = pa.decode_plan(inp.num_seqs, 4, 4, 128, 16, inp.max_blocks_per_seq, torch.bfloat16)
+    assert plan.schedule == 0
+    assert_decode_close(to_f64(gpu_decode(inp)), oracle.decode_inputs(inp), "bf16")
+
+
+TORCH = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}

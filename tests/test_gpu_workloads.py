@@ -29,7 +29,7 @@ def gpu():
 def run_default(inp, dev):
     ws_bytes = pa.decode_workspace_size(inp.num_seqs, inp.num_heads, inp.num_kv_heads, inp.head_dim,
                                         inp.block_size, inp.max_blocks_per_seq, TORCH_DTYPE[inp.dtype])
-    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda") if ws_bytes else None
+    ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device="cuda") if ws_bytes else None
     out = pa.decode(dev["q"], dev["kc"], dev["vc"], dev["bt"], dev["lens"], scale=inp.scale, workspace=ws)
     torch.cuda.synchronize()
     pa.check_error()
@@ -116,7 +116,7 @@ def test_prefix_sharing_with_copy_on_write(prefix_len, expected_copies):
     bt, dl = torch.from_numpy(tables).cuda(), torch.from_numpy(lens).cuda()
     ws_bytes = pa.decode_workspace_size(w.num_seqs, w.num_heads, w.num_kv_heads, w.head_dim, bs, width,
                                         torch.bfloat16)
-    ws = torch.empty(max(ws_bytes, 1), dtype=torch.uint8, device="cuda") if ws_bytes else None
+    ws = torch.zeros(max(ws_bytes, 1), dtype=torch.uint8, device="cuda") if ws_bytes else None
     out = pa.decode(q, kc, vc, bt, dl, scale=wl.default_scale(w.head_dim), workspace=ws)
     torch.cuda.synchronize()
     pa.check_error()

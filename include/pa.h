@@ -133,10 +133,11 @@ int pa_copy_blocks(void* key_cache, void* value_cache, const int64_t* src_dst_pa
  *                 the contexts cut at share boundaries merged in the same
  *                 launch.  A smaller workspace selects partitioned contexts
  *                 (a decode kernel plus a merge kernel).  The workspace must
- *                 be zero-filled before its first use; every successful call
- *                 leaves it ready for the next one (after PA_ERR_TIMEOUT, zero
- *                 it again).  256-byte aligned.  Calls that share a workspace
- *                 must not overlap on the GPU.
+ *                 be zero-filled before its first use: its first MiB holds
+ *                 arrival counters that every successful call leaves at zero,
+ *                 so it can be reused by later calls of any size (after
+ *                 PA_ERR_TIMEOUT, zero it again).  256-byte aligned.  Calls
+ *                 that share a workspace must not overlap on the GPU.
  * Requires num_heads % num_kv_heads == 0, head_dim in {64, 128, 256},
  * block_size in {16, 32} (f32: head_dim in {64, 128}), 16-byte aligned caches,
  * 4-byte aligned query/out, num_blocks * num_kv_heads * block_size < 2^31.

@@ -73,6 +73,13 @@ bool dtype_ok(int dtype) { return dtype == PA_F32 || dtype == PA_F16 || dtype ==
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
+// The workspace starts with a fixed region of per-unit arrival counters used by the
+// lean schedule only; its kernels leave every counter at zero.  Because the region's
+// place and size never depend on the call's sizes, no other buffer of any call
+// (partials of either schedule) ever lands on a counter.
+constexpr size_t kLeanMaxUnits = 4096 * 64;
+constexpr size_t kCounterRegionBytes = kLeanMaxUnits * sizeof(int);
+
 int cuda_fail(cudaError_t e, const char* what) {
     return fail(PA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
 }
@@ -149,18 +156,19 @@ struct Plan {
     int max_parts = 1;
     long long grid = 0;
     size_t ws_bytes = 0;
-    size_t off_l = 0, off_o = 0;  // partitioned grid: offsets of l and o~ (m at 0)
-    size_t off_part = 0;          // lean: offset of the partial records (counters at 0)
+    size_t off_m = 0, off_l = 0, off_o = 0;  // partitioned grid: offsets of m, l and o~
+    size_t off_part = 0;                     // lean: offset of the partial records (counters at 0)
     KernelInfo ki{};
 };
 
 void workspace_layout(int num_seqs, int num_heads, int head_dim, int max_parts, Plan* p) {
     if (max_parts <= 1) {
-        p->ws_bytes = p->off_l = p->off_o = 0;
+        p->ws_bytes = p->off_m = p->off_l = p->off_o = 0;
         return;
     }
     const size_t rows = (size_t)num_seqs * num_heads * max_parts;
-    p->off_l = align256(rows * sizeof(float));
+    p->off_m = kCounterRegionBytes;
+    p->off_l = p->off_m + align256(rows * sizeof(float));
     p->off_o = p->off_l + align256(rows * sizeof(float));
     p->ws_bytes = p->off_o + align256(rows * head_dim * sizeof(float));
 }
@@ -211,10 +219,10 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
 
     // Lean schedule: one persistent wave; every consumer warp streams an equal share of all pages.
     if (partition_pages == 0 && has_ws && num_seqs <= p.ki.lean_max_seqs &&
+        (size_t)num_seqs * num_kv_heads * p.head_chunks <= kLeanMaxUnits &&
         (long long)num_seqs * max_blocks < (1ll << 31)) {
         const long long ctas = (long long)dev->num_sms * p.ki.lean_ctas_per_sm;
-        const size_t units = (size_t)num_seqs * num_kv_heads * p.head_chunks;
-        const size_t off_part = align256(units * sizeof(int));
+        const size_t off_part = kCounterRegionBytes;
         const size_t need =
             off_part + align256((size_t)ctas * p.ki.lean_warps_per_cta * 2 * p.ki.lean_record_floats * sizeof(float));
         if (need <= ws_avail) {
@@ -411,7 +419,7 @@ int pa_decode_ex(void* out, const void* query, const void* key_cache, const void
     a.context_lens = context_lens;
     char* ws = static_cast<char*>(workspace);
     const bool grid_split = p.schedule == kScheduleGrid && p.max_parts > 1;
-    a.ws_m = grid_split ? reinterpret_cast<float*>(ws) : nullptr;
+    a.ws_m = grid_split ? reinterpret_cast<float*>(ws + p.off_m) : nullptr;
     a.ws_l = grid_split ? reinterpret_cast<float*>(ws + p.off_l) : nullptr;
     a.ws_o = grid_split ? reinterpret_cast<float*>(ws + p.off_o) : nullptr;
     a.ws_count = p.schedule == kScheduleLean ? reinterpret_cast<int*>(ws) : nullptr;

@@ -284,14 +284,17 @@ def test_lean_schedule_matches_oracle(lens, dtype, kernel, hq, hkv):
 def test_lean_workspace_is_reusable_across_calls():
     # the per-unit arrival counters must be back at zero after every call
     plan = pa.decode_plan(64, 28, 4, 128, 16, 300, torch.bfloat16)
-    ws = torch.zeros(plan.workspace_bytes, dtype=torch.uint8, device="cuda")
+    grid = pa.decode_plan(64, 28, 4, 128, 16, 300, torch.bfloat16, partition_pages=3)
+    ws = torch.zeros(max(plan.workspace_bytes, grid.workspace_bytes), dtype=torch.uint8, device="cuda")
     for seed, lens in ((1, (300 * 16, 17, 4000, 1)), (2, (1000,) * 9), (3, tuple(range(1, 4800, 97)))):
         inp = case("bf16", 128, 16, 28, 4, lens, seed=seed)
         dev = upload(inp)
-        for _ in range(2):
-            out = pa.decode(dev["q"], dev["kc"], dev["vc"], dev["bt"], dev["lens"], scale=inp.scale, workspace=ws)
+        ref = oracle.decode_inputs(inp)
+        for pp in (0, 3, 0):  # lean, partitioned grid, lean again on the same workspace
+            out = pa.decode(dev["q"], dev["kc"], dev["vc"], dev["bt"], dev["lens"], scale=inp.scale, workspace=ws,
+                            partition_pages=pp)
             torch.cuda.synchronize()
-            assert_decode_close(to_f64(out), oracle.decode_inputs(inp), "bf16")
+            assert_decode_close(to_f64(out), ref, "bf16")
     pa.check_error()
 
 

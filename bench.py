@@ -362,7 +362,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
                  ws.numel(), max_ctx, args.partition_pages, kern, sptr] for r in range(replicas)]
     wr_args = ([[nk.data_ptr(), nv.data_ptr(), kcs[r].data_ptr(), vcs[r].data_ptr(), sl.data_ptr(), ntok, Hkv, d, bs,
                  inp.num_blocks, code, sptr] for r in range(replicas)] if has_write else None)
-    launches_per_step = (1 if has_write else 0) + 1 + (1 if plan.max_parts > 1 else 0)
+    # decode kernel, plus the merge kernel (always for the lean schedule, when split for the grid one)
+    launches_per_step = (1 if has_write else 0) + 1 + (1 if (plan.schedule == 1 or plan.max_parts > 1) else 0)
 
     def step(i, ev_d0=None, ev_d1=None):
         r = i % replicas
@@ -471,7 +472,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     achieved = dec_bytes / (dec_avg_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": stored_traffic(args.workload),
-                "kernel": ("pa_decode call (paged_decode_lean_kernel)" if plan.schedule == 1 else
+                "kernel": ("pa_decode call (paged_decode_lean_kernel + lean_merge_kernel)" if plan.schedule == 1 else
                            "pa_decode call (paged_decode_kernel" + (" + splitkv_merge_kernel)" if plan.max_parts > 1
                                                                     else ")")),
                 "algorithmic_bytes_per_launch": dec_bytes, "pages_touched_bytes": touched,
@@ -502,7 +503,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
                    "l2": f"{replicas} cache replicas rotated per step (pages touched per step "
                          f"{touched / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB)",
                    "kernel": {1: "mma", 2: "simt"}[plan.kernel],
-                   "schedule": {0: "partitioned grid", 1: "lean persistent wave"}[plan.schedule],
+                   "schedule": {0: "partitioned grid", 1: "lean persistent wave + merge"}[plan.schedule],
                    "partition_pages": plan.partition_pages,
                    "max_parts": plan.max_parts, "grid_ctas": plan.grid_ctas,
                    "parallelism": f"{world} independent replicas (one batch per GPU)"},

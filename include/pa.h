@@ -129,15 +129,12 @@ int pa_copy_blocks(void* key_cache, void* value_cache, const int64_t* src_dst_pa
  *                 NULL every (sequence, kv head) is done by one CTA in one
  *                 pass.  With at least pa_decode_workspace_size() bytes the
  *                 default (lean) schedule runs: one persistent wave of CTAs
- *                 whose warps each stream an equal share of all pages, with
- *                 the contexts cut at share boundaries merged in the same
- *                 launch.  A smaller workspace selects partitioned contexts
- *                 (a decode kernel plus a merge kernel).  The workspace must
- *                 be zero-filled before its first use: its first MiB holds
- *                 arrival counters that every successful call leaves at zero,
- *                 so it can be reused by later calls of any size (after
- *                 PA_ERR_TIMEOUT, zero it again).  256-byte aligned.  Calls
- *                 that share a workspace must not overlap on the GPU.
+ *                 whose warps each stream an equal share of all pages, and a
+ *                 small merge kernel that combines the contexts cut at share
+ *                 boundaries.  A smaller workspace selects partitioned
+ *                 contexts (a decode kernel plus a merge kernel).  No
+ *                 initialisation is needed.  256-byte aligned.  Calls that
+ *                 share a workspace must not overlap on the GPU.
  * Requires num_heads % num_kv_heads == 0, head_dim in {64, 128, 256},
  * block_size in {16, 32} (f32: head_dim in {64, 128}), 16-byte aligned caches,
  * 4-byte aligned query/out, num_blocks * num_kv_heads * block_size < 2^31.

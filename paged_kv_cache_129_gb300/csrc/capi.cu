@@ -73,12 +73,8 @@ bool dtype_ok(int dtype) { return dtype == PA_F32 || dtype == PA_F16 || dtype ==
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// The workspace starts with a fixed region of per-unit arrival counters used by the
-// lean schedule only; its kernels leave every counter at zero.  Because the region's
-// place and size never depend on the call's sizes, no other buffer of any call
-// (partials of either schedule) ever lands on a counter.
-constexpr size_t kLeanMaxUnits = 4096 * 64;
-constexpr size_t kCounterRegionBytes = kLeanMaxUnits * sizeof(int);
+// Lean schedule workspace: two partial records per consumer warp.
+constexpr size_t kLeanMetaBytes = 0;
 
 int cuda_fail(cudaError_t e, const char* what) {
     return fail(PA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
@@ -157,7 +153,7 @@ struct Plan {
     long long grid = 0;
     size_t ws_bytes = 0;
     size_t off_m = 0, off_l = 0, off_o = 0;  // partitioned grid: offsets of m, l and o~
-    size_t off_part = 0;                     // lean: offset of the partial records (counters at 0)
+    size_t off_part = 0;                     // lean: warp partial records
     KernelInfo ki{};
 };
 
@@ -167,7 +163,7 @@ void workspace_layout(int num_seqs, int num_heads, int head_dim, int max_parts, 
         return;
     }
     const size_t rows = (size_t)num_seqs * num_heads * max_parts;
-    p->off_m = kCounterRegionBytes;
+    p->off_m = 0;
     p->off_l = p->off_m + align256(rows * sizeof(float));
     p->off_o = p->off_l + align256(rows * sizeof(float));
     p->ws_bytes = p->off_o + align256(rows * head_dim * sizeof(float));
@@ -218,13 +214,17 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
     const long long slots = (long long)dev->num_sms * p.ki.ctas_per_sm;
 
     // Lean schedule: one persistent wave; every consumer warp streams an equal share of all pages.
+    // (Worth it when there are fewer units than consumer warps: then units must be split
+    // to keep every SM streaming, and equal shares balance them.  With more units than
+    // that, whole-unit CTAs already balance and need no merge.)
+    const long long lean_ctas = (long long)dev->num_sms * p.ki.lean_ctas_per_sm;
     if (partition_pages == 0 && has_ws && num_seqs <= p.ki.lean_max_seqs &&
-        (size_t)num_seqs * num_kv_heads * p.head_chunks <= kLeanMaxUnits &&
-        (long long)num_seqs * max_blocks < (1ll << 31)) {
-        const long long ctas = (long long)dev->num_sms * p.ki.lean_ctas_per_sm;
-        const size_t off_part = kCounterRegionBytes;
-        const size_t need =
-            off_part + align256((size_t)ctas * p.ki.lean_warps_per_cta * 2 * p.ki.lean_record_floats * sizeof(float));
+        (long long)p.units < lean_ctas * p.ki.lean_warps_per_cta &&
+        (long long)num_seqs * max_blocks * num_kv_heads * p.head_chunks < (1ll << 31)) {
+        const long long ctas = lean_ctas;
+        const size_t off_part = kLeanMetaBytes;
+        const size_t rec_bytes = (size_t)p.ki.lean_record_floats * sizeof(float);
+        const size_t need = off_part + align256((size_t)ctas * p.ki.lean_warps_per_cta * 2 * rec_bytes);
         if (need <= ws_avail) {
             p.schedule = kScheduleLean;
             p.partition_pages = 0;
@@ -246,10 +246,14 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
     } else if (partition_pages > 0) {
         pp = partition_pages < nblk_max ? partition_pages : nblk_max;
     } else {
-        // About 512 tokens per partition; shorter when that leaves fewer than two waves of CTAs.
-        pp = 512 / block_size > 8 ? 512 / block_size : 8;
-        while (pp > 8 && (long long)p.units * ((nblk_max + pp - 1) / pp) < 2 * slots) pp /= 2;
-        if (pp > nblk_max) pp = nblk_max;
+        if ((long long)p.units >= 4 * slots) {
+            pp = nblk_max;  // whole contexts: at least four waves of CTAs already
+        } else {
+            // About 512 tokens per partition; shorter when that leaves fewer than two waves of CTAs.
+            pp = 512 / block_size > 8 ? 512 / block_size : 8;
+            while (pp > 8 && (long long)p.units * ((nblk_max + pp - 1) / pp) < 2 * slots) pp /= 2;
+            if (pp > nblk_max) pp = nblk_max;
+        }
     }
     for (;;) {
         p.partition_pages = pp;
@@ -422,8 +426,8 @@ int pa_decode_ex(void* out, const void* query, const void* key_cache, const void
     a.ws_m = grid_split ? reinterpret_cast<float*>(ws + p.off_m) : nullptr;
     a.ws_l = grid_split ? reinterpret_cast<float*>(ws + p.off_l) : nullptr;
     a.ws_o = grid_split ? reinterpret_cast<float*>(ws + p.off_o) : nullptr;
-    a.ws_count = p.schedule == kScheduleLean ? reinterpret_cast<int*>(ws) : nullptr;
     a.ws_part = p.schedule == kScheduleLean ? reinterpret_cast<float*>(ws + p.off_part) : nullptr;
+    a.lean_warps_per_cta = p.ki.lean_warps_per_cta;
     a.err = dev->error_word;
     a.num_seqs = num_seqs;
     a.num_heads = num_heads;

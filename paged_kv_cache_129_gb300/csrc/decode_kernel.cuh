@@ -41,6 +41,15 @@
 #include "decode_launch.h"
 #include "pa_common.cuh"
 
+// Lean-kernel tuning knobs (compile time): resident CTAs per SM the register
+// allocation must allow, and the page ring per CTA in KB.
+#ifndef PA_LEAN_MIN_BLOCKS
+#define PA_LEAN_MIN_BLOCKS 3
+#endif
+#ifndef PA_LEAN_RING_KB
+#define PA_LEAN_RING_KB 64
+#endif
+
 namespace pa {
 
 constexpr int kConsumerWarps = 4;
@@ -62,15 +71,16 @@ struct DecodeCfg {
     static constexpr int kHeads = MMA ? 8 : GMAX;          // query heads per CTA
     static constexpr int kOStride = D + 4;                 // padded fp32 row of the combine buffer
     static constexpr int kCombineFloats = kNW * kHeads * kOStride + 2 * kNW * kHeads;
+    static constexpr int a16(int x) { return (x + 15) & ~15; }
     static constexpr int kBarOffset = kRingBytes;
-    static constexpr int kIssuedOffset = kBarOffset + 2 * kNSlot * 8;
-    static constexpr int kQsOffset = kIssuedOffset + kNSlot * 4;
+    static constexpr int kIssuedOffset = a16(kBarOffset + 2 * kNSlot * 8);
+    static constexpr int kQsOffset = a16(kIssuedOffset + kNSlot * 4);
     static constexpr int kQsBytes = MMA ? 0 : GMAX * D * 4;
-    static constexpr int kPsOffset = kQsOffset + kQsBytes;
+    static constexpr int kPsOffset = a16(kQsOffset + kQsBytes);
     static constexpr int kPsBytes = MMA ? 0 : kNW * GMAX * BS * 4;
-    static constexpr int kStatOffset = kPsOffset + kPsBytes;  // per head: M, W, then per-warp weights
+    static constexpr int kStatOffset = a16(kPsOffset + kPsBytes);  // per head: M, W, then per-warp weights
     static constexpr int kStatBytes = kHeads * (2 + kNW) * 4;
-    static constexpr int kFlagOffset = kStatOffset + kStatBytes;
+    static constexpr int kFlagOffset = a16(kStatOffset + kStatBytes);
     static constexpr int kSmemBytes = kFlagOffset + 16 + 1024;  // + slack to align the base to 1024
 
     static_assert(D % kBoxElems == 0, "head_dim must be a multiple of 128 bytes");
@@ -79,6 +89,7 @@ struct DecodeCfg {
     static_assert(!MMA || D % 16 == 0, "k-steps of 16");
     static_assert(MMA || (32 % BS == 0 || BS == 32), "CUDA-core path: 32 must be a multiple of BS");
     static_assert(kCombineFloats * 4 <= kRingBytes, "combine buffer must fit in the ring");
+    static_assert(kQsOffset % 16 == 0 && kPsOffset % 16 == 0, "float4 access to q_s");
     static_assert(kSmemBytes <= 227 * 1024, "shared memory per CTA");
 };
 
@@ -186,6 +197,18 @@ struct MmaConsumer {
     __device__ __forceinline__ void finish() {
         l += __shfl_xor_sync(0xffffffffu, l, 1);
         l += __shfl_xor_sync(0xffffffffu, l, 2);
+    }
+
+    // Forget the unit (init() sets everything again): keeps its registers free meanwhile.
+    __device__ __forceinline__ void clear() {
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            qa[kk][0] = qa[kk][1] = 0u;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[kk][e] = 0.f;
+        }
+        m = -INFINITY;
+        l = 0.f;
     }
 
     // out_rows[h * D + d] = o~ / l for the gc heads (after finish()).
@@ -355,6 +378,8 @@ struct SimtConsumer {
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
     }
+
+    __device__ __forceinline__ void clear() { init(); }
 
     __device__ __forceinline__ void write_out(T* out_rows, int gc, int lane) const {
 #pragma unroll
@@ -729,9 +754,9 @@ struct LeanCfg {
     using Base = DecodeCfg<T, D, BS, MMA, GMAX>;
     static constexpr int kNW = Base::kNW;
     static constexpr int kThreads = Base::kThreads;
-    // Page slots per consumer warp: about 64 KB of ring per CTA, between 1 and 3 slots a warp.
-    static constexpr int kSPWRaw = 65536 / (kNW * Base::kSlotBytes);
-    static constexpr int kSPW = kSPWRaw < 1 ? 1 : (kSPWRaw > 3 ? 3 : kSPWRaw);
+    // Page slots per consumer warp: about PA_LEAN_RING_KB of ring per CTA, 1 to 6 slots a warp.
+    static constexpr int kSPWRaw = (PA_LEAN_RING_KB * 1024) / (kNW * Base::kSlotBytes);
+    static constexpr int kSPW = kSPWRaw < 1 ? 1 : (kSPWRaw > 6 ? 6 : kSPWRaw);
     static constexpr int kNSlot = kNW * kSPW;
     static constexpr int kSlotBytes = Base::kSlotBytes;
     static constexpr int kPageBytes = Base::kPageBytes;
@@ -739,20 +764,32 @@ struct LeanCfg {
     static constexpr int kHeads = Base::kHeads;
     static constexpr int kOOff = ((2 * kHeads + 3) / 4) * 4;  // o~ offset in a partial record
     static constexpr int kRecFloats = kOOff + kHeads * D;      // one partial record
-    static constexpr int kBarOffset = kRingBytes;
-    static constexpr int kIssuedOffset = kBarOffset + 2 * kNSlot * 8;
-    static constexpr int kFlagOffset = kIssuedOffset + kNSlot * 4;
-    static constexpr int kScanOffset = kFlagOffset + 16;
-    static constexpr int kQsOffset = kScanOffset + 32;
-    static constexpr int kQsBytes = MMA ? 0 : kNW * GMAX * D * 4;  // one fp32 q block per warp
-    static constexpr int kPsOffset = kQsOffset + kQsBytes;
+    static constexpr int kRowQueue = 64;  // published page rows per consumer warp (two chunks of 32)
+    // Shared-memory regions after the ring, each 16-byte aligned.
+    static constexpr int a16(int x) { return (x + 15) & ~15; }
+    static constexpr int kBarOffset = kRingBytes;                                   // full[], empty[]
+    static constexpr int kIssuedOffset = a16(kBarOffset + 2 * kNSlot * 8);          // int issued[kNSlot]
+    static constexpr int kFlagOffset = a16(kIssuedOffset + kNSlot * 4);             // int abort flag
+    static constexpr int kScanOffset = a16(kFlagOffset + 4);                        // int warp sums[8]
+    static constexpr int kRowsOffset = a16(kScanOffset + 8 * 4);                    // int rows[kNW][kRowQueue]
+    static constexpr int kCountOffset = a16(kRowsOffset + kNW * kRowQueue * 4);     // int fill_cnt[kNW]
+    static constexpr int kQsOffset = a16(kCountOffset + kNW * 4);                   // fp32 q per warp
+    static constexpr int kQsBytes = MMA ? 0 : kNW * GMAX * D * 4;
+    static constexpr int kPsOffset = a16(kQsOffset + kQsBytes);                     // fp32 p per warp
     static constexpr int kPsBytes = MMA ? 0 : kNW * GMAX * BS * 4;
-    static constexpr int kPrefixOffset = kPsOffset + kPsBytes;      // then (num_seqs + 1) ints
+    static constexpr int kPrefixOffset = a16(kPsOffset + kPsBytes);                 // (num_seqs + 1) ints
     static constexpr int kFixedSmemBytes = kPrefixOffset + 1024;      // + slack to align the base
     static constexpr int kMaxSmemBytes = kFixedSmemBytes + (kLeanMaxSeqs + 1) * 4;
     static int smem_bytes(int num_seqs) { return kFixedSmemBytes + (num_seqs + 1) * 4; }
+    // Resident CTAs per SM the register allocation aims for: PA_LEAN_MIN_BLOCKS, but no more
+    // than shared memory allows (for short batches), and 2 for head_dim 256 (larger fragments).
+    static constexpr int kSmemBlocks = (228 * 1024) / (kFixedSmemBytes + 1024);
+    static constexpr int kMinBlocksRaw = PA_LEAN_MIN_BLOCKS < kSmemBlocks ? PA_LEAN_MIN_BLOCKS : kSmemBlocks;
+    static constexpr int kMinBlocks = D > 128 ? (kMinBlocksRaw < 2 ? kMinBlocksRaw : 2)
+                                              : (kMinBlocksRaw < 1 ? 1 : kMinBlocksRaw);
     static_assert(kMaxSmemBytes <= 227 * 1024, "shared memory per CTA");
     static_assert(kOOff % 4 == 0 && kRecFloats % 4 == 0, "16-byte aligned records");
+    static_assert(kQsOffset % 16 == 0 && kPsOffset % 16 == 0, "alignment");
 };
 
 __device__ __forceinline__ float warp_max(float v) {
@@ -789,71 +826,25 @@ __device__ __forceinline__ int block_exclusive_scan(int v, int* warp_sums, int n
 }
 
 // Global page g -> sequence b, unit within the sequence uu, page j within the unit, pages per unit nb.
-__device__ __forceinline__ void lean_locate(const int* pre, int num_seqs, int upb, long long g, int& b, int& uu,
-                                            int& j, int& nb) {
+// (The plan guarantees that all page indices, times units per sequence, fit in int.)
+__device__ __forceinline__ void lean_locate(const int* pre, int num_seqs, int upb, int g, int& b, int& uu, int& j,
+                                            int& nb) {
     int lo = 0, hi = num_seqs - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if ((long long)pre[mid] * upb <= g) lo = mid;
+        if (pre[mid] * upb <= g) lo = mid;
         else hi = mid - 1;
     }
     b = lo;
     nb = pre[b + 1] - pre[b];
-    const long long r = g - (long long)pre[b] * upb;
-    uu = (int)(r / nb);
-    j = (int)(r - (long long)uu * nb);
+    const int r = g - pre[b] * upb;
+    uu = r / nb;
+    j = r - uu * nb;
 }
 
-// Merge the partial records of one unit (warps w_lo..w_hi) into out_rows.
-template <typename T, int D, int H>
-__device__ void lean_merge(const float* ws_part, long long w_lo, long long w_hi, long long unit_first, long long q,
-                           int gc, T* out_rows, int lane) {
-    constexpr int kOOff = ((2 * H + 3) / 4) * 4;
-    constexpr int kRec = kOOff + H * D;
-    constexpr int DPL = D / 32;
-    const int n = (int)(w_hi - w_lo + 1);
-    // The first warp keeps this unit in slot 1 (its last unit) unless its range starts at the unit.
-    const int slot0 = unit_first != w_lo * q ? 1 : 0;
-    auto rec = [&](int p) -> const float* {
-        return ws_part + ((size_t)(w_lo + p) * 2 + (p == 0 ? slot0 : 0)) * kRec;
-    };
-    for (int h = 0; h < gc; ++h) {
-        float mx = -INFINITY;
-        for (int p = lane; p < n; p += 32) mx = fmaxf(mx, __ldcg(rec(p) + h));
-        mx = warp_max(mx);
-        float den = 0.f;
-        for (int p = lane; p < n; p += 32) den += exp2f(__ldcg(rec(p) + h) - mx) * __ldcg(rec(p) + H + h);
-        den = warp_sum(den);
-        float acc[DPL];
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
-#pragma unroll 4
-        for (int p = 0; p < n; ++p) {
-            const float* r = rec(p);
-            const float f = exp2f(__ldcg(r + h) - mx);
-            const float* src = r + kOOff + h * D + lane * DPL;
-            if constexpr (DPL % 4 == 0) {
-#pragma unroll
-                for (int e = 0; e < DPL; e += 4) {
-                    const float4 v = __ldcg(reinterpret_cast<const float4*>(src + e));
-                    acc[e] += f * v.x;
-                    acc[e + 1] += f * v.y;
-                    acc[e + 2] += f * v.z;
-                    acc[e + 3] += f * v.w;
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < DPL; ++e) acc[e] += f * __ldcg(src + e);
-            }
-        }
-        const float inv = 1.f / den;
-#pragma unroll
-        for (int e = 0; e < DPL; ++e) out_rows[(size_t)h * D + lane * DPL + e] = from_float<T>(acc[e] * inv);
-    }
-}
 
 template <typename T, int D, int BS, bool MMA, int GMAX>
-__global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
+__global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (LeanCfg<T, D, BS, MMA, GMAX>::kMinBlocks))
     paged_decode_lean_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                              const DecodeArgs a) {
     using C = LeanCfg<T, D, BS, MMA, GMAX>;
@@ -873,6 +864,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
     const int B = a.num_seqs;
     const int l_cap = a.max_blocks * BS;
     T* out = static_cast<T*>(a.out);
+
+    // Let the merge kernel (programmatic dependent launch) get scheduled as early as possible;
+    // it reads nothing this kernel writes before its griddepcontrol.wait.
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
     // ---- pages per sequence (context lengths clamped to the table), prefix sums ----
     const int per = (B + C::kThreads - 1) / C::kThreads;
@@ -902,14 +897,16 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
             mbar_init(&empty[s], 1);
             issued[s] = 0;
         }
+        int* fills = reinterpret_cast<int*>(smem + C::kCountOffset);
+        for (int w = 0; w < C::kNW; ++w) fills[w] = 0;  // no page rows published yet
         flags[0] = 0;
         fence_barrier_init();
     }
     __syncthreads();
 
     const int upb = a.num_kv_heads * a.head_chunks;  // units per sequence
-    const long long total = (long long)total_pages * upb;
-    const long long q_per_warp = (total + (long long)gridDim.x * C::kNW - 1) / ((long long)gridDim.x * C::kNW);
+    const int total = total_pages * upb;
+    const int q_per_warp = (total + (int)gridDim.x * C::kNW - 1) / ((int)gridDim.x * C::kNW);
 
     // Empty contexts produce zero rows (spread over the CTAs).
     for (int b = warp; b < B; b += C::kNW + 1)
@@ -918,78 +915,132 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
                 out[(size_t)b * a.num_heads * D + idx] = from_float<T>(0.f);
     if (total == 0) return;
 
+    int* row_queue = reinterpret_cast<int*>(smem + C::kRowsOffset);        // [kNW][kRowQueue]
+    volatile int* fill_cnt = reinterpret_cast<volatile int*>(smem + C::kCountOffset);  // [kNW]
     if (warp == C::kNW) {
         // ================= producer warp =================
+        // Each consumer warp publishes the TMA rows of its own pages well ahead
+        // (row_queue / fill_cnt); lane 0 only polls the page slots and issues the
+        // next published page of every warp that has a free slot.  It never
+        // waits on global memory and never waits behind one particular warp.
         if (lane == 0) {
             tma_prefetch_desc(&tmap_k);
             tma_prefetch_desc(&tmap_v);
-        }
-        // Lane l serves consumer warp (l & 3), page offsets k + (l >> 2) of each round of 8.
-        const int w = lane & 3;
-        const long long lo_w = min(total, ((long long)blockIdx.x * C::kNW + w) * q_per_warp);
-        const long long hi_w = min(total, lo_w + q_per_warp);
-        const int n_w = (int)(hi_w - lo_w);
-        const int n_max = __reduce_max_sync(0xffffffffu, n_w);
-        bool ok = true;
-        for (int k = 0; k < n_max && ok; k += 8) {
-            const int off = k + (lane >> 2);
-            int row = 0, bad = 0;
-            if (off < n_w) {
-                int b, uu, j, nb;
-                lean_locate(pre, B, upb, lo_w + off, b, uu, j, nb);
-                const int kvh = uu / a.head_chunks;
-                const int pb = __ldg(a.block_tables + (size_t)b * a.max_blocks + j);
-                if ((unsigned)pb < (unsigned)a.num_blocks) row = (pb * a.num_kv_heads + kvh) * BS;
-                else bad = 1;
+            static_assert(C::kNW == 4, "the issue loop is unrolled for four consumer warps");
+            int iss[C::kNW], n_w[C::kNW];
+#pragma unroll
+            for (int wi = 0; wi < C::kNW; ++wi) {
+                iss[wi] = 0;
+                const int lo_w = min(total, ((int)blockIdx.x * C::kNW + wi) * q_per_warp);
+                n_w[wi] = min(total, lo_w + q_per_warp) - lo_w;
             }
-            for (int i = 0; i < 32; ++i) {
-                const int off_i = k + (i >> 2);
-                const int n_i = __shfl_sync(0xffffffffu, n_w, i & 3);
-                const int row_i = __shfl_sync(0xffffffffu, row, i);
-                const int bad_i = __shfl_sync(0xffffffffu, bad, i);
-                if (off_i >= n_i) continue;  // uniform over the warp
-                int good = 1;
-                if (lane == 0) {
-                    const int s = (i & 3) * C::kSPW + off_i % C::kSPW;
-                    const int use = off_i / C::kSPW;
-                    if (use >= 1) good = mbar_wait_bounded(&empty[s], (use - 1) & 1, a.err, flags) ? 1 : 0;
-                    if (good) {
+            unsigned long long last_progress = global_timer_ns();
+            while (true) {
+                bool progress = false, done = true;
+#pragma unroll
+                for (int wi = 0; wi < C::kNW; ++wi) {
+                    const int avail = fill_cnt[wi];
+                    __threadfence_block();  // the rows below were written before fill_cnt
+                    while (iss[wi] < avail) {
+                        const int s = wi * C::kSPW + iss[wi] % C::kSPW;
+                        const int use = iss[wi] / C::kSPW;
+                        if (use >= 1 && !mbar_test_wait(&empty[s], (use - 1) & 1)) break;
+                        const int r = row_queue[wi * C::kRowQueue + iss[wi] % C::kRowQueue];
                         issued[s] += 1;
-                        if (!bad_i) {
+                        if (r >= 0) {
                             mbar_arrive_expect_tx(&full[s], C::kSlotBytes);
                             uint8_t* kdst = ring + s * C::kSlotBytes;
                             uint8_t* vdst = kdst + C::kPageBytes;
 #pragma unroll
                             for (int bx = 0; bx < C::Base::kNBox; ++bx)
-                                tma_load_2d(kdst + bx * C::Base::kBoxBytes, &tmap_k, bx * C::Base::kBoxElems, row_i,
+                                tma_load_2d(kdst + bx * C::Base::kBoxBytes, &tmap_k, bx * C::Base::kBoxElems, r,
                                             &full[s]);
 #pragma unroll
                             for (int bx = 0; bx < C::Base::kNBox; ++bx)
-                                tma_load_2d(vdst + bx * C::Base::kBoxBytes, &tmap_v, bx * C::Base::kBoxElems, row_i,
+                                tma_load_2d(vdst + bx * C::Base::kBoxBytes, &tmap_v, bx * C::Base::kBoxElems, r,
                                             &full[s]);
                         } else {
                             atomicOr(a.err, kErrBadTable);  // skip the load; the slot keeps stale data
                             mbar_arrive(&full[s]);
                         }
+                        ++iss[wi];
+                        progress = true;
                     }
+                    done = done && iss[wi] >= n_w[wi];
                 }
-                ok = __shfl_sync(0xffffffffu, good, 0) != 0;
-                if (!ok) break;
+                if (done) break;
+                if (progress) {
+                    last_progress = global_timer_ns();
+                } else {
+                    if (flags[0]) break;
+                    if (global_timer_ns() - last_progress > kWaitLimitNs) {
+                        atomicOr(a.err, kErrTimeout);
+                        flags[0] = 1;
+                        break;
+                    }
+                    __nanosleep(20);
+                }
             }
         }
     } else {
         // ================= consumer warps =================
-        const long long wg = (long long)blockIdx.x * C::kNW + warp;
-        const long long lo = min(total, wg * q_per_warp);
-        const long long hi = min(total, lo + q_per_warp);
-        const int n = (int)(hi - lo);
-        long long unit_first = 0, unit_last = -1;
+        const int wg = (int)blockIdx.x * C::kNW + warp;
+        const int lo = min(total, wg * q_per_warp);
+        const int hi = min(total, lo + q_per_warp);
+        const int n = hi - lo;
+        int unit_first = 0, unit_last = -1;
         int b = 0, uu = 0, nb = 0, L = 0, head0 = 0, gc = 0;
         std::conditional_t<MMA, MmaConsumer<T, D, BS>, SimtConsumer<T, D, BS, GMAX>> cons;
         float* q_s = reinterpret_cast<float*>(smem + C::kQsOffset) + warp * GMAX * D;
         float* p_s = reinterpret_cast<float*>(smem + C::kPsOffset) + warp * GMAX * BS;
+        // Page rows for the producer, published in chunks of 32: chunk c + 1 when this warp
+        // reaches page 32c + 16, with the block-table loads of chunk c + 2 then left in flight.
+        int* queue = row_queue + warp * C::kRowQueue;
+        int pend_pb = -1, pend_kvh = 0;
+        for (int chunk = 0; chunk < 2; ++chunk) {
+            const int page = 32 * chunk + lane;
+            pend_pb = -1;
+            if (page < n) {
+                int sb, su, sj, sn;
+                lean_locate(pre, B, upb, lo + page, sb, su, sj, sn);
+                pend_kvh = su / a.head_chunks;
+                pend_pb = __ldg(a.block_tables + (size_t)sb * a.max_blocks + sj);
+            }
+            if (chunk == 0) {
+                if (page < n)
+                    queue[page] = (unsigned)pend_pb < (unsigned)a.num_blocks
+                                      ? (pend_pb * a.num_kv_heads + pend_kvh) * BS
+                                      : -1;
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence_block();
+                    fill_cnt[warp] = min(n, 32);
+                }
+            }
+        }
         for (int off = 0; off < n; ++off) {
-            const long long g = lo + off;
+            if ((off & 31) == 16) {
+                const int c = (off >> 5) + 1;  // the chunk published now
+                const int page = 32 * c + lane;
+                if (page < n)
+                    queue[page % C::kRowQueue] = (unsigned)pend_pb < (unsigned)a.num_blocks
+                                                     ? (pend_pb * a.num_kv_heads + pend_kvh) * BS
+                                                     : -1;
+                __syncwarp();
+                if (lane == 0) {
+                    __threadfence_block();
+                    fill_cnt[warp] = min(n, 32 * (c + 1));
+                }
+                const int next = page + 32;
+                pend_pb = -1;
+                if (next < n) {
+                    int sb, su, sj, sn;
+                    lean_locate(pre, B, upb, lo + next, sb, su, sj, sn);
+                    pend_kvh = su / a.head_chunks;
+                    pend_pb = __ldg(a.block_tables + (size_t)sb * a.max_blocks + sj);
+                }
+            }
+            const int g = lo + off;
             if (g > unit_last) {  // a new unit starts
                 int j0;
                 lean_locate(pre, B, upb, g, b, uu, j0, nb);
@@ -1012,7 +1063,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
                     cons.init();
                 }
             }
-            const int j = (int)(g - unit_first);
+            const int j = g - unit_first;
             const int s = warp * C::kSPW + off % C::kSPW;
             const bool got = mbar_wait_bounded(&full[s], (off / C::kSPW) & 1, a.err, flags);
             if (!__all_sync(0xffffffffu, got)) break;
@@ -1031,26 +1082,12 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
                 T* out_rows = out + ((size_t)b * a.num_heads + head0) * D;
                 if (unit_first >= lo && unit_last < hi) {
                     cons.write_out(out_rows, gc, lane);
+                    cons.clear();
                 } else {
                     const int slot = unit_first <= lo ? 0 : 1;  // 0: the warp's first unit, 1: its last
                     float* rec = a.ws_part + ((size_t)wg * 2 + slot) * C::kRecFloats;
                     cons.write_partial(rec, gc, lane);
-                    __threadfence();
-                    __syncwarp();
-                    const long long w_lo = unit_first / q_per_warp;
-                    const long long w_hi = unit_last / q_per_warp;
-                    int last = 0;
-                    if (lane == 0) {
-                        int* cnt = a.ws_count + (size_t)b * upb + uu;
-                        last = atomicAdd(cnt, 1) == (int)(w_hi - w_lo);
-                        if (last) *cnt = 0;  // ready for the next call
-                    }
-                    last = __shfl_sync(0xffffffffu, last, 0);
-                    if (last) {
-                        __threadfence();
-                        lean_merge<T, D, C::kHeads>(a.ws_part, w_lo, w_hi, unit_first, q_per_warp, gc, out_rows,
-                                                    lane);
-                    }
+                    cons.clear();
                 }
             }
         }
@@ -1066,6 +1103,153 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
                            global_timer_ns() - start < kWaitLimitNs) {
                     }
                 }
+    }
+}
+
+
+// Lean merge: one CTA per (sequence, kv head, head chunk) unit.  A unit that the
+// lean decode cut between consumer warps w_lo..w_hi left one partial record per
+// warp (m, l, o~ per head); this kernel combines them in warp order,
+//     M = max_p m_p,  W = sum_p 2^(m_p - M) l_p,  o = sum_p 2^(m_p - M) o~_p / W.
+// Units that fit in one warp's range were finished by the decode kernel.
+// Launched with programmatic stream serialisation: it becomes resident while the
+// decode kernel drains and waits for its completion before reading anything.
+#ifndef PA_LEAN_MERGE_THREADS
+#define PA_LEAN_MERGE_THREADS 256
+#endif
+#ifndef PA_LEAN_MERGE_MINB
+#define PA_LEAN_MERGE_MINB 2
+#endif
+constexpr int kLeanMergeThreads = PA_LEAN_MERGE_THREADS;
+constexpr int kLeanMergeBatch = 8;  // records whose loads a thread keeps in flight together
+
+// Lean merge: one CTA per (sequence, kv head, head chunk) unit.  A unit that the lean
+// decode cut between consumer warps w_lo..w_hi left one partial record per warp
+// (m, l, o~ per head); the merge combines them with the online-softmax rule,
+//     M = max_p m_p,  W = sum_p 2^(m_p - M) l_p,  o = sum_p 2^(m_p - M) o~_p / W.
+// The unit's place in the page order is recomputed from the context lengths, which
+// the decode does not write, before waiting for the decode (programmatic dependent
+// launch), so that part overlaps the decode.  After the wait every thread merges
+// its own float4 columns of o~ over all records on its own: no barriers, all loads
+// of a batch of records issued before any is used.
+template <typename T, int D, int H, int BS>
+__global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_merge_kernel(const DecodeArgs a) {
+    constexpr int kOOff = ((2 * H + 3) / 4) * 4;
+    constexpr int kRec = kOOff + H * D;
+    __shared__ int warp_sums[kLeanMergeThreads / 32];
+    __shared__ int seq_before[2];  // pages of the sequences before b, pages of b
+    const int tid = threadIdx.x;
+    const int upb = a.num_kv_heads * a.head_chunks;
+    const int u = blockIdx.x;
+    const int b = u / upb, uu = u - b * upb;
+    const int B = a.num_seqs;
+    const int l_cap = a.max_blocks * BS;
+
+    // pages per sequence (clamped like the decode), their total, and the prefix up to b
+    int before = 0, all = 0;
+    for (int s = tid; s < B; s += kLeanMergeThreads) {
+        int L = __ldg(a.context_lens + s);
+        L = L < 0 ? 0 : (L > l_cap ? l_cap : L);
+        const int n = (L + BS - 1) / BS;
+        all += n;
+        if (s < b) before += n;
+        if (s == b) seq_before[1] = n;
+    }
+    int tot = 0, pre_b = 0;
+    block_exclusive_scan(all, warp_sums, kLeanMergeThreads / 32, &tot);
+    __syncthreads();
+    block_exclusive_scan(before, warp_sums, kLeanMergeThreads / 32, &pre_b);
+    __syncthreads();
+    const int nb = seq_before[1];
+    const int total = tot * upb;
+    const int warps = a.lean_grid * a.lean_warps_per_cta;
+    const int q = (total + warps - 1) / warps;
+    if (nb == 0 || q <= 0) return;
+    const int first = pre_b * upb + uu * nb;
+    const int w_lo = first / q, w_hi = (first + nb - 1) / q;
+    if (w_lo == w_hi) return;  // finished by the decode kernel
+    const int n = w_hi - w_lo + 1;
+    const int slot0 = first != w_lo * q ? 1 : 0;  // w_lo holds the unit in slot 1 unless its range starts here
+    const int kvh = uu / a.head_chunks, hc = uu - kvh * a.head_chunks;
+    const int head0 = kvh * a.group + hc * H;
+    const int gc = min(H, a.group - hc * H);
+    const float* base = a.ws_part + (size_t)w_lo * 2 * kRec;
+
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+
+    // thread = (float4 column of the gc live heads, slice of the records): each thread folds
+    // its records (online), then slice 0 folds the slices' (max, denominator, o~) triples.
+    __shared__ float red[6][kLeanMergeThreads];
+    const int cols = gc * (D / 4);
+    const int slices = kLeanMergeThreads >= cols ? kLeanMergeThreads / cols : 1;
+    for (int cbase = 0; cbase < cols; cbase += kLeanMergeThreads) {
+    const int col = slices > 1 ? tid % cols : cbase + tid;
+    const int slice = slices > 1 ? tid / cols : (col < cols ? 0 : 1);
+    const int h = col / (D / 4);
+    float mm = -INFINITY, ww = 0.f;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    if (slice < slices) {
+        for (int p0 = slice; p0 < n; p0 += kLeanMergeBatch * slices) {
+            float mv[kLeanMergeBatch], lv[kLeanMergeBatch];
+            float4 ov[kLeanMergeBatch];
+#pragma unroll
+            for (int k = 0; k < kLeanMergeBatch; ++k) {
+                const int p = p0 + k * slices;
+                if (p < n) {
+                    const float* r = base + ((size_t)p * 2 + (p == 0 ? slot0 : 0)) * kRec;
+                    mv[k] = __ldcg(r + h);
+                    lv[k] = __ldcg(r + H + h);
+                    ov[k] = __ldcg(reinterpret_cast<const float4*>(r + kOOff) + col);
+                }
+            }
+#pragma unroll
+            for (int k = 0; k < kLeanMergeBatch; ++k) {
+                if (p0 + k * slices < n) {
+                    const float m_new = fmaxf(mm, mv[k]);
+                    const float keep = exp2f(mm - m_new);  // 0 on the first record
+                    const float f = exp2f(mv[k] - m_new);
+                    ww = ww * keep + f * lv[k];
+                    acc.x = acc.x * keep + f * ov[k].x;
+                    acc.y = acc.y * keep + f * ov[k].y;
+                    acc.z = acc.z * keep + f * ov[k].z;
+                    acc.w = acc.w * keep + f * ov[k].w;
+                    mm = m_new;
+                }
+            }
+        }
+    }
+    if (slices > 1) {
+        red[0][tid] = mm;
+        red[1][tid] = ww;
+        red[2][tid] = acc.x;
+        red[3][tid] = acc.y;
+        red[4][tid] = acc.z;
+        red[5][tid] = acc.w;
+        __syncthreads();
+        if (slice == 0) {
+            for (int k = 1; k < slices; ++k) {
+                const int t = k * cols + col;
+                const float m2 = red[0][t];
+                const float m_new = fmaxf(mm, m2);
+                if (m_new == -INFINITY) continue;  // both slices empty
+                const float k1 = exp2f(mm - m_new), k2 = exp2f(m2 - m_new);
+                ww = ww * k1 + red[1][t] * k2;
+                acc.x = acc.x * k1 + red[2][t] * k2;
+                acc.y = acc.y * k1 + red[3][t] * k2;
+                acc.z = acc.z * k1 + red[4][t] * k2;
+                acc.w = acc.w * k1 + red[5][t] * k2;
+                mm = m_new;
+            }
+        }
+    }
+    if (slice == 0) {
+        const float inv = 1.f / ww;
+        T* out = static_cast<T*>(a.out) + ((size_t)b * a.num_heads + head0) * D + col * 4;
+        out[0] = from_float<T>(acc.x * inv);
+        out[1] = from_float<T>(acc.y * inv);
+        out[2] = from_float<T>(acc.z * inv);
+        out[3] = from_float<T>(acc.w * inv);
+    }
     }
 }
 
@@ -1137,6 +1321,21 @@ struct DecodeKernel {
         if (schedule == kScheduleLean) {
             paged_decode_lean_kernel<T, D, BS, MMA, GMAX>
                 <<<grid, LC::kThreads, LC::smem_bytes(num_seqs), stream>>>(k, v, a);
+            e = cudaGetLastError();
+            if (e != cudaSuccess) return e;
+            cudaLaunchConfig_t cfg = {};
+            DecodeArgs m = a;
+            m.lean_grid = grid;
+            cfg.gridDim = dim3(a.num_seqs * a.num_kv_heads * a.head_chunks);  // one CTA per unit
+            cfg.blockDim = dim3(kLeanMergeThreads);
+            cfg.dynamicSmemBytes = 0;
+            cfg.stream = stream;
+            cudaLaunchAttribute attr[1];
+            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[0].val.programmaticStreamSerializationAllowed = 1;
+            cfg.attrs = attr;
+            cfg.numAttrs = 1;
+            return cudaLaunchKernelEx(&cfg, lean_merge_kernel<T, D, LC::kHeads, BS>, m);
         } else {
             paged_decode_kernel<T, D, BS, MMA, GMAX><<<grid, C::kThreads, C::kSmemBytes, stream>>>(k, v, a);
         }

@@ -16,13 +16,14 @@ struct DecodeArgs {
     float* ws_m;                 // [B * Hq, max_parts]   running max (log2 domain) per partition
     float* ws_l;                 // [B * Hq, max_parts]   running denominator per partition
     float* ws_o;                 // [B * Hq, max_parts, D] unnormalised output per partition
-    int* ws_count;               // lean schedule: per-unit arrival counters (zero between calls)
     float* ws_part;              // lean schedule: two partial records per consumer warp
     unsigned* err;               // device error word
     int num_seqs, num_heads, num_kv_heads, group, head_chunks;
     int max_blocks, num_blocks;
     int partition_pages, max_parts;
     float scale_log2;            // softmax scale * log2(e)
+    int lean_warps_per_cta;      // consumer warps per lean CTA
+    int lean_grid;               // CTAs of the lean decode launch (set for the merge kernel)
 };
 
 // Arguments of the split-KV merge kernel.

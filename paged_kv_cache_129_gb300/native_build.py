@@ -34,12 +34,24 @@ def nvcc() -> str:
 
 def _deps() -> list:
     files = [os.path.join(CSRC, f) for f in os.listdir(CSRC)]
+    files.append(os.path.join(BUILD, ".flags"))
     files.append(os.path.join(INCLUDE, "pa.h"))
     files.append(os.path.abspath(__file__))
     return files
 
 
+def _flags_file_current() -> None:
+    """Record the extra flags; a change of flags makes the library stale."""
+    os.makedirs(BUILD, exist_ok=True)
+    path = os.path.join(BUILD, ".flags")
+    flags = os.environ.get("PA_NVCC_EXTRA", "")
+    if not os.path.exists(path) or open(path).read() != flags:
+        with open(path, "w") as f:
+            f.write(flags)
+
+
 def up_to_date() -> bool:
+    _flags_file_current()
     if not os.path.exists(LIB):
         return False
     t = os.path.getmtime(LIB)
@@ -61,6 +73,8 @@ def build(force: bool = False, verbose_ptxas: bool = False, jobs: int = 0) -> st
     os.makedirs(BUILD, exist_ok=True)
     cc = nvcc()
     common = ["-std=c++17", "-O3", "-I", INCLUDE, "-I", CSRC, "-Xcompiler", "-fPIC"]
+    # Optional extra nvcc flags for tuning builds (e.g. -DPA_LEAN_RING_KB=96).
+    common += os.environ.get("PA_NVCC_EXTRA", "").split()
     cmds, objs = [], []
     for src in CUDA_SOURCES:
         obj = os.path.join(BUILD, src + ".o")

@@ -1,0 +1,66 @@
+"""Host logic of bench.py on CPU: byte accounting, per-rank seeds, and the
+max/sum over ranks with a world-size-2 gloo process group."""
+import os
+import socket
+
+import numpy as np
+import pytest
+import torch.distributed as dist
+import torch.multiprocessing as mp
+
+import bench
+
+
+def test_decode_bytes_counts_valid_tokens_q_out_tables_lengths():
+    lens = [1, 16, 17]
+    got = bench.decode_bytes(lens, num_heads=8, num_kv_heads=2, head_dim=64, elem_bytes=2, block_size=16)
+    kv = 2 * sum(lens) * 2 * 64 * 2
+    qo = 2 * 3 * 8 * 64 * 2
+    tables = 4 * (1 + 1 + 2)
+    assert got == kv + qo + tables + 4 * 3
+
+
+def test_kv_size_formula_matches_the_pages_worked_numbers():
+    # M_KV = 2 L b H_kv d_h sum T: LLaMA-7B (32 layers, 32 kv heads, d 128, fp16) at 4096 tokens ~ 2.15 GB,
+    # and 32 layers x hidden 4096 x batch 8 x seq 2048 fp16 ~ 8.6 GB.
+    per_layer = bench.decode_bytes([4096], 32, 32, 128, 2, 16) - 2 * 32 * 128 * 2 - 4 * 256 - 4
+    assert abs(32 * per_layer / 1e9 - 2.147) < 0.01
+    per_layer8 = bench.decode_bytes([2048] * 8, 32, 32, 128, 2, 16) - 2 * 8 * 32 * 128 * 2 - 4 * 8 * 128 - 32
+    assert abs(32 * per_layer8 / 1e9 - 8.59) < 0.01
+
+
+def test_rank_seeds_differ_and_rank0_keeps_the_base_seed():
+    seeds = {bench.rank_seed(7, r) for r in range(8)}
+    assert len(seeds) == 8 and bench.rank_seed(7, 0) == 7
+
+
+def _worker(rank, world, port, out):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
+    dist.init_process_group("gloo", rank=rank, world_size=world)
+    try:
+        t = bench.max_over_ranks(10.0 + rank, world)
+        s = bench.sum_over_ranks(1.5 * (rank + 1), world)
+        bench.barrier(world)
+        out[rank] = (t, s)
+    finally:
+        dist.destroy_process_group()
+
+
+def _free_port():
+    with socket.socket() as sck:
+        sck.bind(("127.0.0.1", 0))
+        return sck.getsockname()[1]
+
+
+def test_max_and_sum_over_two_gloo_ranks():
+    ctx = mp.get_context("spawn")
+    manager = ctx.Manager()
+    out = manager.dict()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, out)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(120)
+        assert p.exitcode == 0
+    assert out[0] == out[1] == (11.0, 4.5)

@@ -187,6 +187,38 @@ int pa_decode_make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_
 size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                                 int block_size, int max_blocks_per_seq, int dtype);
 
+/*
+ * pa_decode without a caller workspace: the split-KV scratch comes from one
+ * fixed array of PA_STATIC_SCRATCH_BYTES compiled into the library (one copy
+ * per device).  The method on the pages has no counterpart to this call; it is
+ * a library convenience.
+ *
+ * For callers that cannot allocate device memory around a decode step: a C
+ * host or plugin handed only a stream and its tensors, with no allocator to
+ * ask; or a serving loop that must not call cudaMalloc/cudaFree on the step
+ * path, because those can synchronise the device and fragment memory already
+ * sized for the KV cache.  The call itself allocates nothing.
+ *
+ * Arguments, layout and results are those of pa_decode; the plan is the one
+ * pa_decode uses with a workspace of pa_decode_workspace_size() bytes.
+ *  - Limit: sizes whose plan needs more than PA_STATIC_SCRATCH_BYTES of scratch
+ *    (for example head_dim 256 on a 152-SM GPU) are refused with
+ *    PA_ERR_UNSUPPORTED and a message giving the bytes needed; use pa_decode
+ *    with a workspace for those.
+ *  - Nothing in the scratch has to start at zero, so nothing is cleared.
+ *  - The first call on each device does setup (resolves the scratch address,
+ *    loads and configures kernels): make it before any stream capture.
+ *  - Calls that overlap on the GPU race on the one scratch: calls on one
+ *    stream are ordered and safe; calls on different streams of one device
+ *    must be ordered by the caller (events), or use pa_decode.
+ */
+#define PA_STATIC_SCRATCH_BYTES (16u * 1024u * 1024u)
+
+int pa_decode_static_scratch(void* out, const void* query, const void* key_cache, const void* value_cache,
+                             const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                             int num_heads, int num_kv_heads, int head_dim, int block_size,
+                             int max_blocks_per_seq, int num_blocks, float scale, int dtype, void* stream);
+
 /* ---- host block pool ----------------------------------------------------------------- */
 /*
  * Fixed-size block allocator with reference counts, fork and copy-on-write

@@ -5,6 +5,7 @@ The compute path is the CUDA library built from ``csrc/`` (see
 """
 from .binding import (  # noqa: F401
     KERNELS,
+    STATIC_SCRATCH_BYTES,
     LIB_PATH,
     BlockPool,
     DecodePlan,
@@ -14,6 +15,7 @@ from .binding import (  # noqa: F401
     copy_blocks,
     decode,
     decode_plan,
+    decode_static_scratch,
     decode_workspace_size,
     library,
     version,

@@ -24,6 +24,7 @@ STATUS_NAMES = {
 }
 PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 KERNELS = {"auto": 0, "mma": 1, "simt": 2}
+STATIC_SCRATCH_BYTES = 16 * 1024 * 1024  # PA_STATIC_SCRATCH_BYTES
 _TORCH_DTYPES = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
 
 _lock = threading.Lock()
@@ -62,6 +63,7 @@ _SIGNATURES = [
     ("pa_decode_ex", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _I, _I, _I, _P]),
     ("pa_decode_make_plan", _I, [_I, _I, _I, _I, _I, _I, _I, _SZ, _I, _I, _I, ctypes.POINTER(DecodePlan)]),
     ("pa_decode_workspace_size", _SZ, [_I, _I, _I, _I, _I, _I, _I]),
+    ("pa_decode_static_scratch", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
     ("pa_pool_create", _I, [_I, _I, _P, ctypes.POINTER(_P)]),
     ("pa_pool_destroy", None, [_P]),
     ("pa_seq_create", _I, [_P, ctypes.POINTER(_I64)]),
@@ -220,6 +222,38 @@ def decode(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tens
                                   _stream_ptr(stream, query.device)))
     return out
 
+
+def decode_static_scratch(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                          block_tables: torch.Tensor, context_lens: torch.Tensor, out: torch.Tensor,
+                          scale: Optional[float] = None, stream=None) -> torch.Tensor:
+    """``pa_decode_static_scratch``: ``decode`` with the library's built-in scratch.
+
+    For callers that may not allocate device memory on the step path: nothing
+    is allocated here either, so ``out`` is required.  Calls that overlap on
+    the GPU (different streams) race on the one scratch; make the first call
+    before any stream capture.  Sizes needing more than
+    ``STATIC_SCRATCH_BYTES`` of scratch raise ``PAError`` (PA_ERR_UNSUPPORTED).
+    """
+    for name, t in (("query", query), ("key_cache", key_cache), ("value_cache", value_cache),
+                    ("block_tables", block_tables), ("context_lens", context_lens), ("out", out)):
+        _cuda(t, name)
+    _need(key_cache.dim() == 4 and value_cache.shape == key_cache.shape, "caches must be [N, H_kv, bs, d]")
+    num_blocks, hkv, bs, d = key_cache.shape
+    _need(query.dim() == 3 and query.shape[2] == d, "query must be [B, H_q, d]")
+    b, hq, _ = query.shape
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == b,
+          "block_tables: int32 [B, max_blocks]")
+    _need(context_lens.dtype == torch.int32 and context_lens.numel() == b, "context_lens: int32 [B]")
+    _need(query.dtype == key_cache.dtype == value_cache.dtype, "query and caches must share a dtype")
+    _need(out.shape == query.shape and out.dtype == query.dtype, "out must match query")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    _check(library().pa_decode_static_scratch(out.data_ptr(), query.data_ptr(), key_cache.data_ptr(),
+                                              value_cache.data_ptr(), block_tables.data_ptr(),
+                                              context_lens.data_ptr(), b, hq, hkv, d, bs, block_tables.shape[1],
+                                              num_blocks, float(scale), _dtype_code(query),
+                                              _stream_ptr(stream, query.device)))
+    return out
 
 class BlockPool:
     """Host block pool (``pa_pool``): free list, refcounts, fork, copy-on-write append."""

@@ -222,3 +222,9 @@ def test_pool_unknown_sequence_and_bad_free_order(lib):
         pool.append(sid)  # two blocks
     with pytest.raises(pa.PAError):
         pool.block_tables([sid], 1)
+
+
+def test_static_scratch_size_matches_the_header():
+    text = open(os.path.join(ROOT, "include", "pa.h")).read()
+    m = re.search(r"#define PA_STATIC_SCRATCH_BYTES \((\d+)u \* 1024u \* 1024u\)", text)
+    assert m and int(m.group(1)) * 1024 * 1024 == pa.STATIC_SCRATCH_BYTES

@@ -443,9 +443,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
     const int warp = tid >> 5;
     const int lane = tid & 31;
 
-    // Let the merge kernel (launched with programmatic stream serialisation) get
-    // resident early; it waits for this grid's completion before reading anything.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Wait for the previous grid in the stream (programmatic dependent launch), then let
+    // the next one (the merge, when there is one) get resident early; it waits for this
+    // grid's completion before reading anything.
+    griddep_wait();
+    griddep_launch_dependents();
 
     // ---- which work unit ----
     const int units = a.num_seqs * a.num_kv_heads * a.head_chunks;
@@ -495,6 +497,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
             tma_prefetch_desc(&tmap_k);
             tma_prefetch_desc(&tmap_v);
         }
+        // Pages are read once per call: let them leave L2 first.
+        const uint64_t stream_policy = l2_policy_evict_first();
         const int32_t* bt = a.block_tables + (size_t)b * a.max_blocks + first;
         int next = lane < npages ? __ldg(bt + lane) : 0;
         bool ok = true;
@@ -519,10 +523,12 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
                             uint8_t* vdst = kdst + C::kPageBytes;
 #pragma unroll
                             for (int bx = 0; bx < C::kNBox; ++bx)
-                                tma_load_2d(kdst + bx * C::kBoxBytes, &tmap_k, bx * C::kBoxElems, row, &full[s]);
+                                tma_load_2d_hint(kdst + bx * C::kBoxBytes, &tmap_k, bx * C::kBoxElems, row, &full[s],
+                                                 stream_policy);
 #pragma unroll
                             for (int bx = 0; bx < C::kNBox; ++bx)
-                                tma_load_2d(vdst + bx * C::kBoxBytes, &tmap_v, bx * C::kBoxElems, row, &full[s]);
+                                tma_load_2d_hint(vdst + bx * C::kBoxBytes, &tmap_v, bx * C::kBoxElems, row, &full[s],
+                                                 stream_policy);
                         } else {
                             atomicOr(a.err, kErrBadTable);  // skip the load; the slot keeps stale data
                             mbar_arrive(&full[s]);
@@ -662,8 +668,10 @@ __global__ void __launch_bounds__(kMergeThreads) splitkv_merge_kernel(const Merg
     const int b = row / a.num_heads;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
-    // Wait for the decode kernel's partials (programmatic dependent launch).
-    asm volatile("griddepcontrol.wait;" ::: "memory");
+    // Wait for the decode kernel's partials (programmatic dependent launch); then the
+    // next grid in the stream may start launching.
+    griddep_wait();
+    griddep_launch_dependents();
 
     int L = __ldg(a.context_lens + b);
     const int l_cap = min(a.max_blocks, a.max_parts * a.partition_pages) * a.block_size;
@@ -743,10 +751,9 @@ __global__ void __launch_bounds__(kMergeThreads) splitkv_merge_kernel(const Merg
 // C * NW equal contiguous ranges, one per consumer warp.  So every warp streams
 // the same number of pages whatever the context lengths are.  A warp finishes
 // every unit that lies wholly inside its range (o = o~ / l straight to out);
-// for a unit cut by a range boundary it writes a partial (m, l, o~) record, and
-// the last of that unit's warps to finish (per-unit arrival counters in the
-// workspace, reset by the merging warp) merges the records in warp order, with
-// the same rescaling rule as the online softmax.
+// for a unit cut by a range boundary it writes a partial (m, l, o~) record (two
+// record slots per warp: its first and its last unit), which lean_merge_kernel
+// combines with the same rescaling rule as the online softmax.
 constexpr int kLeanMaxSeqs = 4096;
 
 template <typename T, int D, int BS, bool MMA, int GMAX>
@@ -865,9 +872,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Lea
     const int l_cap = a.max_blocks * BS;
     T* out = static_cast<T*>(a.out);
 
-    // Let the merge kernel (programmatic dependent launch) get scheduled as early as possible;
-    // it reads nothing this kernel writes before its griddepcontrol.wait.
-    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+    // Wait for the previous grid in the stream, then let the merge kernel get scheduled as
+    // early as possible; it reads nothing this kernel writes before its own wait.
+    griddep_wait();
+    griddep_launch_dependents();
 
     // ---- pages per sequence (context lengths clamped to the table), prefix sums ----
     const int per = (B + C::kThreads - 1) / C::kThreads;
@@ -926,6 +934,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Lea
         if (lane == 0) {
             tma_prefetch_desc(&tmap_k);
             tma_prefetch_desc(&tmap_v);
+            // Pages are read once per call: let them leave L2 first, so that the partial
+            // records the merge reads stay resident.
+            const uint64_t stream_policy = l2_policy_evict_first();
             static_assert(C::kNW == 4, "the issue loop is unrolled for four consumer warps");
             int iss[C::kNW], n_w[C::kNW];
 #pragma unroll
@@ -953,12 +964,12 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Lea
                             uint8_t* vdst = kdst + C::kPageBytes;
 #pragma unroll
                             for (int bx = 0; bx < C::Base::kNBox; ++bx)
-                                tma_load_2d(kdst + bx * C::Base::kBoxBytes, &tmap_k, bx * C::Base::kBoxElems, r,
-                                            &full[s]);
+                                tma_load_2d_hint(kdst + bx * C::Base::kBoxBytes, &tmap_k, bx * C::Base::kBoxElems, r,
+                                                 &full[s], stream_policy);
 #pragma unroll
                             for (int bx = 0; bx < C::Base::kNBox; ++bx)
-                                tma_load_2d(vdst + bx * C::Base::kBoxBytes, &tmap_v, bx * C::Base::kBoxElems, r,
-                                            &full[s]);
+                                tma_load_2d_hint(vdst + bx * C::Base::kBoxBytes, &tmap_v, bx * C::Base::kBoxElems, r,
+                                                 &full[s], stream_policy);
                         } else {
                             atomicOr(a.err, kErrBadTable);  // skip the load; the slot keeps stale data
                             mbar_arrive(&full[s]);
@@ -1107,13 +1118,6 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Lea
 }
 
 
-// Lean merge: one CTA per (sequence, kv head, head chunk) unit.  A unit that the
-// lean decode cut between consumer warps w_lo..w_hi left one partial record per
-// warp (m, l, o~ per head); this kernel combines them in warp order,
-//     M = max_p m_p,  W = sum_p 2^(m_p - M) l_p,  o = sum_p 2^(m_p - M) o~_p / W.
-// Units that fit in one warp's range were finished by the decode kernel.
-// Launched with programmatic stream serialisation: it becomes resident while the
-// decode kernel drains and waits for its completion before reading anything.
 #ifndef PA_LEAN_MERGE_THREADS
 #define PA_LEAN_MERGE_THREADS 256
 #endif
@@ -1127,17 +1131,20 @@ constexpr int kLeanMergeBatch = 8;  // records whose loads a thread keeps in fli
 // decode cut between consumer warps w_lo..w_hi left one partial record per warp
 // (m, l, o~ per head); the merge combines them with the online-softmax rule,
 //     M = max_p m_p,  W = sum_p 2^(m_p - M) l_p,  o = sum_p 2^(m_p - M) o~_p / W.
-// The unit's place in the page order is recomputed from the context lengths, which
-// the decode does not write, before waiting for the decode (programmatic dependent
-// launch), so that part overlaps the decode.  After the wait every thread merges
-// its own float4 columns of o~ over all records on its own: no barriers, all loads
-// of a batch of records issued before any is used.
+// Units that fit in one warp's range were finished by the decode kernel.  The unit's
+// place in the page order is recomputed from the context lengths before waiting for
+// the decode (programmatic dependent launch), so that part overlaps the decode.  That
+// read is safe: this grid can only start once every decode CTA has passed its own
+// wait for the grids before it, so any writer of the lengths has completed.  After
+// the wait every thread merges its own float4 columns of o~ over all records on its
+// own: no barriers, all loads of a batch of records issued before any is used.
 template <typename T, int D, int H, int BS>
 __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_merge_kernel(const DecodeArgs a) {
     constexpr int kOOff = ((2 * H + 3) / 4) * 4;
     constexpr int kRec = kOOff + H * D;
     __shared__ int warp_sums[kLeanMergeThreads / 32];
     __shared__ int seq_before[2];  // pages of the sequences before b, pages of b
+    griddep_launch_dependents();  // the next grid waits for this one's completion itself
     const int tid = threadIdx.x;
     const int upb = a.num_kv_heads * a.head_chunks;
     const int u = blockIdx.x;
@@ -1164,6 +1171,10 @@ __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_me
     const int total = tot * upb;
     const int warps = a.lean_grid * a.lean_warps_per_cta;
     const int q = (total + warps - 1) / warps;
+    // Every CTA waits for the decode, also those with nothing to merge: a grid that
+    // follows this one waits only for this grid, so this grid must not end before the
+    // decode has.
+    griddep_wait();
     if (nb == 0 || q <= 0) return;
     const int first = pre_b * upb + uu * nb;
     const int w_lo = first / q, w_hi = (first + nb - 1) / q;
@@ -1174,8 +1185,6 @@ __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_me
     const int head0 = kvh * a.group + hc * H;
     const int gc = min(H, a.group - hc * H);
     const float* base = a.ws_part + (size_t)w_lo * 2 * kRec;
-
-    asm volatile("griddepcontrol.wait;" ::: "memory");
 
     // thread = (float4 column of the gc live heads, slice of the records): each thread folds
     // its records (online), then slice 0 folds the slices' (max, denominator, o~) triples.
@@ -1319,43 +1328,25 @@ struct DecodeKernel {
         if (e != cudaSuccess) return e;
         if (!configure(device)) return cudaGetLastError();
         if (schedule == kScheduleLean) {
-            paged_decode_lean_kernel<T, D, BS, MMA, GMAX>
-                <<<grid, LC::kThreads, LC::smem_bytes(num_seqs), stream>>>(k, v, a);
-            e = cudaGetLastError();
+            e = launch_pdl(paged_decode_lean_kernel<T, D, BS, MMA, GMAX>, dim3(grid), dim3(LC::kThreads),
+                           LC::smem_bytes(num_seqs), stream, k, v, a);
             if (e != cudaSuccess) return e;
-            cudaLaunchConfig_t cfg = {};
             DecodeArgs m = a;
             m.lean_grid = grid;
-            cfg.gridDim = dim3(a.num_seqs * a.num_kv_heads * a.head_chunks);  // one CTA per unit
-            cfg.blockDim = dim3(kLeanMergeThreads);
-            cfg.dynamicSmemBytes = 0;
-            cfg.stream = stream;
-            cudaLaunchAttribute attr[1];
-            attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-            attr[0].val.programmaticStreamSerializationAllowed = 1;
-            cfg.attrs = attr;
-            cfg.numAttrs = 1;
-            return cudaLaunchKernelEx(&cfg, lean_merge_kernel<T, D, LC::kHeads, BS>, m);
+            // one CTA per unit
+            return launch_pdl(lean_merge_kernel<T, D, LC::kHeads, BS>,
+                              dim3(a.num_seqs * a.num_kv_heads * a.head_chunks), dim3(kLeanMergeThreads), 0, stream,
+                              m);
         } else {
-            paged_decode_kernel<T, D, BS, MMA, GMAX><<<grid, C::kThreads, C::kSmemBytes, stream>>>(k, v, a);
+            return launch_pdl(paged_decode_kernel<T, D, BS, MMA, GMAX>, dim3(grid), dim3(C::kThreads), C::kSmemBytes,
+                              stream, k, v, a);
         }
-        return cudaGetLastError();
     }
 };
 
 template <typename T, int D>
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(a.num_seqs * a.num_heads);
-    cfg.blockDim = dim3(kMergeThreads);
-    cfg.dynamicSmemBytes = 0;
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, splitkv_merge_kernel<T, D>, a);
+    return launch_pdl(splitkv_merge_kernel<T, D>, dim3(a.num_seqs * a.num_heads), dim3(kMergeThreads), 0, stream, a);
 }
 
 }  // namespace pa

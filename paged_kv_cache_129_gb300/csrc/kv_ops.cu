@@ -16,6 +16,8 @@ __global__ void __launch_bounds__(256) write_kv_kernel(const V* __restrict__ key
                                                        const int64_t* __restrict__ slots, int num_tokens,
                                                        int num_kv_heads, int row_vecs, int block_size,
                                                        long long num_slots, unsigned* err) {
+    griddep_wait();
+    griddep_launch_dependents();
     const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
     if (gw >= (long long)num_tokens * num_kv_heads) return;
     const int lane = threadIdx.x & 31;
@@ -41,6 +43,8 @@ __global__ void __launch_bounds__(256) write_kv_kernel(const V* __restrict__ key
 template <typename V>
 __global__ void __launch_bounds__(256) copy_blocks_kernel(V* key_cache, V* value_cache, const int64_t* __restrict__ pairs,
                                                           long long block_vecs, int num_blocks, unsigned* err) {
+    griddep_wait();
+    griddep_launch_dependents();
     const int pidx = blockIdx.x;
     const long long src = __ldg(pairs + 2 * pidx);
     const long long dst = __ldg(pairs + 2 * pidx + 1);
@@ -75,11 +79,10 @@ cudaError_t write_typed(const WriteArgs& a, long long row_bytes, cudaStream_t st
     const long long warps = (long long)a.num_tokens * a.num_kv_heads;
     const int threads = 256;
     const long long grid = (warps + (threads / 32) - 1) / (threads / 32);
-    write_kv_kernel<V><<<(unsigned)grid, threads, 0, stream>>>(
-        static_cast<const V*>(a.key), static_cast<const V*>(a.value), static_cast<V*>(a.key_cache),
-        static_cast<V*>(a.value_cache), a.slot_mapping, a.num_tokens, a.num_kv_heads, row_vecs, a.block_size,
-        (long long)a.num_blocks * a.block_size, a.err);
-    return cudaGetLastError();
+    return launch_pdl(write_kv_kernel<V>, dim3((unsigned)grid), dim3(threads), 0, stream, static_cast<const V*>(a.key),
+                      static_cast<const V*>(a.value), static_cast<V*>(a.key_cache), static_cast<V*>(a.value_cache),
+                      a.slot_mapping, a.num_tokens, a.num_kv_heads, row_vecs, a.block_size,
+                      (long long)a.num_blocks * a.block_size, a.err);
 }
 
 template <typename V>
@@ -89,9 +92,8 @@ cudaError_t copy_typed(const CopyArgs& a, long long block_bytes, cudaStream_t st
     long long chunks = (block_vecs + threads * 4 - 1) / (threads * 4);
     if (chunks > 65535) chunks = 65535;
     dim3 grid((unsigned)a.num_pairs, 2, (unsigned)chunks);
-    copy_blocks_kernel<V><<<grid, threads, 0, stream>>>(static_cast<V*>(a.key_cache), static_cast<V*>(a.value_cache),
-                                                         a.pairs, block_vecs, a.num_blocks, a.err);
-    return cudaGetLastError();
+    return launch_pdl(copy_blocks_kernel<V>, grid, dim3(threads), 0, stream, static_cast<V*>(a.key_cache),
+                      static_cast<V*>(a.value_cache), a.pairs, block_vecs, a.num_blocks, a.err);
 }
 
 }  // namespace

@@ -1,11 +1,14 @@
 #!/usr/bin/env python3
-"""Benchmark of one paged decode step on GB300: pa_write_kv + pa_decode.
+"""Benchmark of one paged decode step on GB300.
 
 A step is one pass of the hot path over one batch: the new token of every
-sequence is written through its slot (pa_write_kv), then decode attention runs
-over the whole paged context (pa_decode: the decode kernel, plus the split-KV
-merge kernel when contexts are partitioned).  Block tables and slots come from
-the host block pool (pa_pool), built before the timed region.
+sequence is written into its slot, then decode attention runs over the whole
+paged context.  By default both happen in one call, pa_decode_append (the
+write folded into the decode kernel; plus the split-KV merge kernel when
+contexts are split); ``--step write+decode`` times pa_write_kv followed by
+pa_decode instead.  Block tables and slots come from the host block pool
+(pa_pool), built before the timed region; the pool's slots are checked to be
+the slots of positions L - 1 that pa_decode_append derives.
 
 Prints one JSON line (rank 0).  ``value`` is KV GB/s over the algorithmic
 bytes (K+V of the valid tokens + q + out + block-table entries + lengths, plus
@@ -356,24 +359,43 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     code = {"f32": 0, "f16": 1, "bf16": 2}[inp.dtype]
     kern = pa.KERNELS[args.kernel]
 
+    fused = has_write and args.step == "append"
+    if fused:
+        # pa_decode_append writes at the slot of position L - 1: the pool handed out exactly those
+        live = lens >= 1
+        derived = tables[np.arange(B), (lens - 1) // bs].astype(np.int64) * bs + (lens - 1) % bs
+        assert np.array_equal(np.asarray(slots)[live], derived[live])
+
     # Pre-marshalled C-ABI argument lists (the timed loop only calls the library).
     dec_args = [[out.data_ptr(), q.data_ptr(), kcs[r].data_ptr(), vcs[r].data_ptr(), bt.data_ptr(), dl.data_ptr(),
                  B, Hq, Hkv, d, bs, tables.shape[1], inp.num_blocks, float(inp.scale), code, ws.data_ptr(),
                  ws.numel(), max_ctx, args.partition_pages, kern, sptr] for r in range(replicas)]
     wr_args = ([[nk.data_ptr(), nv.data_ptr(), kcs[r].data_ptr(), vcs[r].data_ptr(), sl.data_ptr(), ntok, Hkv, d, bs,
                  inp.num_blocks, code, sptr] for r in range(replicas)] if has_write else None)
-    # decode kernel, plus the merge kernel (always for the lean schedule, when split for the grid one)
-    launches_per_step = (1 if has_write else 0) + 1 + (1 if (plan.schedule == 1 or plan.max_parts > 1) else 0)
+    app_args = ([[out.data_ptr(), q.data_ptr(), nk.data_ptr(), nv.data_ptr(), kcs[r].data_ptr(), vcs[r].data_ptr(),
+                  bt.data_ptr(), dl.data_ptr(), B, Hq, Hkv, d, bs, tables.shape[1], inp.num_blocks, float(inp.scale),
+                  code, ws.data_ptr(), ws.numel(), max_ctx, args.partition_pages, kern, sptr]
+                 for r in range(replicas)] if fused else None)
+    # the decode kernel, plus the merge kernel (always for the lean schedule, when split for
+    # the grid one), plus the write kernel when it is a call of its own
+    merge_launches = 1 if (plan.schedule == 1 or plan.max_parts > 1) else 0
+    launches_per_step = (1 if (has_write and not fused) else 0) + 1 + merge_launches
 
     def step(i):
         r = i % replicas
+        if fused:
+            if lib.pa_decode_append(*app_args[r]) != 0:
+                raise RuntimeError(lib.pa_last_error_string().decode())
+            return
         if has_write and lib.pa_write_kv(*wr_args[r]) != 0:
             raise RuntimeError(lib.pa_last_error_string().decode())
         if lib.pa_decode_ex(*dec_args[r]) != 0:
             raise RuntimeError(lib.pa_last_error_string().decode())
 
     def decode_call(i):
-        if lib.pa_decode_ex(*dec_args[i % replicas]) != 0:
+        # the step's decode call: pa_decode_append (rewriting the same rows) or pa_decode_ex
+        status = lib.pa_decode_append(*app_args[i % replicas]) if fused else lib.pa_decode_ex(*dec_args[i % replicas])
+        if status != 0:
             raise RuntimeError(lib.pa_last_error_string().decode())
 
     sampler = ClockSampler(gpu_selector(device))
@@ -437,7 +459,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
             nk_d, nv_d, sl_d = torch.empty_like(nk), torch.empty_like(nv), torch.empty_like(sl)
         h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + dl_h.numel() * 4
         if has_write:
-            h2d += 2 * nk_h.numel() * nk_h.element_size() + sl_h.numel() * 8
+            h2d += 2 * nk_h.numel() * nk_h.element_size() + (0 if fused else sl_h.numel() * 8)
         d2h = out_h.numel() * out_h.element_size()
 
         def e2e_step(i):
@@ -445,13 +467,20 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
             q_d.copy_(q_h, non_blocking=True)
             bt_d.copy_(bt_h, non_blocking=True)
             dl_d.copy_(dl_h, non_blocking=True)
-            if has_write:
+            if fused:
                 nk_d.copy_(nk_h, non_blocking=True)
                 nv_d.copy_(nv_h, non_blocking=True)
-                sl_d.copy_(sl_h, non_blocking=True)
-                pa.write_kv(nk_d, nv_d, kcs[r], vcs[r], sl_d)
-            pa.decode(q_d, kcs[r], vcs[r], bt_d, dl_d, scale=inp.scale, out=out, workspace=ws,
-                      max_context_len=max_ctx, partition_pages=args.partition_pages, kernel=args.kernel)
+                pa.decode_append(q_d, nk_d, nv_d, kcs[r], vcs[r], bt_d, dl_d, scale=inp.scale, out=out,
+                                 workspace=ws, max_context_len=max_ctx, partition_pages=args.partition_pages,
+                                 kernel=args.kernel)
+            else:
+                if has_write:
+                    nk_d.copy_(nk_h, non_blocking=True)
+                    nv_d.copy_(nv_h, non_blocking=True)
+                    sl_d.copy_(sl_h, non_blocking=True)
+                    pa.write_kv(nk_d, nv_d, kcs[r], vcs[r], sl_d)
+                pa.decode(q_d, kcs[r], vcs[r], bt_d, dl_d, scale=inp.scale, out=out, workspace=ws,
+                          max_context_len=max_ctx, partition_pages=args.partition_pages, kernel=args.kernel)
             out_h.copy_(out, non_blocking=True)
 
         for i in range(min(args.warmup, 20)):
@@ -472,22 +501,24 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         e_bytes = sum_over_ranks(float(step_bytes) * Ke, world)
         e2e = {"value": round(e_bytes / (e_ms / 1e3) / 1e9, 2), "unit": UNIT, "steps": Ke,
                "ms_per_step": round(e_ms / Ke, 5), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "note": "pa.write_kv + pa.decode through the Python API; inputs copied from pinned host memory "
+               "note": f"{'pa.decode_append' if fused else 'pa.write_kv + pa.decode'} through the Python API; "
+                       "inputs copied from pinned host memory "
                        "and the output copied back every step, inside the timed region"}
 
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
     peak_src = "of measured (MEASURED_PEAKS.json hbm_gbs)" if peak else "of fallback"
     peak = float(peak or FALLBACK_HBM_GBS)
-    achieved = dec_bytes / (dec_avg_ms / 1e3) / 1e9
+    call_bytes = step_bytes if fused else dec_bytes  # the appending call also does the write
+    achieved = call_bytes / (dec_avg_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": stored_traffic(args.workload),
-                "kernel": ("pa_decode call (paged_decode_lean_kernel + lean_merge_kernel)" if plan.schedule == 1 else
-                           "pa_decode call (paged_decode_kernel" + (" + splitkv_merge_kernel)" if plan.max_parts > 1
-                                                                    else ")")),
-                "algorithmic_bytes_per_launch": dec_bytes, "pages_touched_bytes": touched,
+                "kernel": (("pa_decode_append" if fused else "pa_decode") + " call (" +
+                           ("paged_decode_lean_kernel + lean_merge_kernel)" if plan.schedule == 1 else
+                            "paged_decode_kernel" + (" + splitkv_merge_kernel)" if plan.max_parts > 1 else ")"))),
+                "algorithmic_bytes_per_launch": call_bytes, "pages_touched_bytes": touched,
                 "avg_launch_ms": round(dec_avg_ms, 5),
-                "timing": f"CUDA events around {K} back-to-back pa_decode calls on the launch stream",
+                "timing": f"CUDA events around {K} back-to-back calls on the launch stream",
                 "peak_source": peak_src}
 
     cpu = None
@@ -510,7 +541,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAMES[inp.dtype], "data": "synthetic",
         "config": {"workload": WORKLOAD_DESCRIPTIONS[args.workload], "name": args.workload,
-                   "step": "pa_write_kv (new token per sequence) + pa_decode",
+                   "step": ("pa_decode_append (new token per sequence written at L - 1, then decode)" if fused
+                            else "pa_write_kv (new token per sequence) + pa_decode"),
                    "l2": f"{replicas} cache replicas rotated per step (pages touched per step "
                          f"{touched / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB)",
                    "kernel": {1: "mma", 2: "simt"}[plan.kernel],
@@ -582,6 +614,8 @@ def main(argv=None) -> None:
     ap.add_argument("--workload", choices=sorted(WORKLOAD_DESCRIPTIONS), default="qwen_gqa")
     ap.add_argument("--kernel", choices=["auto", "mma", "simt"], default="auto")
     ap.add_argument("--partition-pages", type=int, default=0)
+    ap.add_argument("--step", choices=["append", "write+decode"], default="append",
+                    help="one fused call per step, or the write and the decode as two calls")
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--e2e-steps", type=int, default=5000)
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")

@@ -163,6 +163,28 @@ int pa_decode_ex(void* out, const void* query, const void* key_cache, const void
                  float scale, int dtype, void* workspace, size_t workspace_bytes, int max_context_len,
                  int partition_pages, int kernel, void* stream);
 
+/*
+ * pa_decode_append — one decode step with its cache write folded in: the new
+ * token of every sequence is appended at position L - 1 and attended to.
+ * Equivalent to pa_write_kv with slot_mapping[b] = block_tables[b, (L_b - 1) /
+ * block_size] * block_size + (L_b - 1) % block_size for every b with L_b >= 1
+ * (sequences with L_b == 0 write nothing), followed by pa_decode_ex; the write
+ * is the MiniPaged-Qwen append of section 8.1 (the token's slot from the block
+ * table), and the attention reads the new row from the staged page instead of
+ * re-reading it.
+ *  new_key, new_value  device [num_seqs, num_kv_heads, head_dim] of `dtype`,
+ *                      16-byte aligned.
+ *  key_cache, value_cache  written: one row per (sequence, kv head).
+ * Other arguments as pa_decode_ex.  The page holding position L_b - 1 must not
+ * be read by another sequence of the same call (a block pool with copy-on-write
+ * guarantees it: an append never writes a shared block).
+ */
+int pa_decode_append(void* out, const void* query, const void* new_key, const void* new_value, void* key_cache,
+                     void* value_cache, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                     int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                     int num_blocks, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                     int max_context_len, int partition_pages, int kernel, void* stream);
+
 /* The partition plan pa_decode_ex would use on the current device. */
 typedef struct pa_decode_plan {
     int kernel;            /* PA_KERNEL_MMA or PA_KERNEL_SIMT */

@@ -14,6 +14,7 @@ from .binding import (  # noqa: F401
     check_error,
     copy_blocks,
     decode,
+    decode_append,
     decode_plan,
     decode_static_scratch,
     decode_workspace_size,

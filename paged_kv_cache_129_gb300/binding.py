@@ -61,6 +61,8 @@ _SIGNATURES = [
     ("pa_copy_blocks", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     ("pa_decode", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     ("pa_decode_ex", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _I, _I, _I, _P]),
+    ("pa_decode_append", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _I, _I, _I,
+                              _P]),
     ("pa_decode_make_plan", _I, [_I, _I, _I, _I, _I, _I, _I, _SZ, _I, _I, _I, ctypes.POINTER(DecodePlan)]),
     ("pa_decode_workspace_size", _SZ, [_I, _I, _I, _I, _I, _I, _I]),
     ("pa_decode_static_scratch", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
@@ -220,6 +222,47 @@ def decode(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tens
                                   block_tables.shape[1], num_blocks, float(scale), _dtype_code(query), ws_ptr or None,
                                   ws_bytes, max_context_len, partition_pages, KERNELS[kernel],
                                   _stream_ptr(stream, query.device)))
+    return out
+
+
+def decode_append(query: torch.Tensor, new_key: torch.Tensor, new_value: torch.Tensor, key_cache: torch.Tensor,
+                  value_cache: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+                  scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                  workspace: Optional[torch.Tensor] = None, max_context_len: int = 0, partition_pages: int = 0,
+                  kernel: str = "auto", stream=None) -> torch.Tensor:
+    """``pa_decode_append``: write the new token of every sequence at position L - 1, then decode.
+
+    ``new_key`` / ``new_value``: ``[B, H_kv, d]``.  Same result as ``write_kv`` with the
+    slots of positions L - 1 followed by ``decode``, in one kernel.
+    """
+    for name, t in (("query", query), ("new_key", new_key), ("new_value", new_value), ("key_cache", key_cache),
+                    ("value_cache", value_cache), ("block_tables", block_tables), ("context_lens", context_lens)):
+        _cuda(t, name)
+    _need(key_cache.dim() == 4 and value_cache.shape == key_cache.shape, "caches must be [N, H_kv, bs, d]")
+    num_blocks, hkv, bs, d = key_cache.shape
+    _need(query.dim() == 3 and query.shape[2] == d, "query must be [B, H_q, d]")
+    b, hq, _ = query.shape
+    _need(new_key.shape == (b, hkv, d) and new_value.shape == new_key.shape, "new_key/new_value must be [B, H_kv, d]")
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == b,
+          "block_tables: int32 [B, max_blocks]")
+    _need(context_lens.dtype == torch.int32 and context_lens.numel() == b, "context_lens: int32 [B]")
+    _need(query.dtype == key_cache.dtype == value_cache.dtype == new_key.dtype == new_value.dtype,
+          "query, new key/value and caches must share a dtype")
+    if out is None:
+        out = torch.empty_like(query)
+    _cuda(out, "out")
+    _need(out.shape == query.shape and out.dtype == query.dtype, "out must match query")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    ws_ptr, ws_bytes = 0, 0
+    if workspace is not None:
+        _cuda(workspace, "workspace")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check(library().pa_decode_append(out.data_ptr(), query.data_ptr(), new_key.data_ptr(), new_value.data_ptr(),
+                                      key_cache.data_ptr(), value_cache.data_ptr(), block_tables.data_ptr(),
+                                      context_lens.data_ptr(), b, hq, hkv, d, bs, block_tables.shape[1], num_blocks,
+                                      float(scale), _dtype_code(query), ws_ptr or None, ws_bytes, max_context_len,
+                                      partition_pages, KERNELS[kernel], _stream_ptr(stream, query.device)))
     return out
 
 

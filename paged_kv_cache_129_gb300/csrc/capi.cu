@@ -381,13 +381,21 @@ size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, i
     return p.ws_bytes;
 }
 
-int pa_decode_ex(void* out, const void* query, const void* key_cache, const void* value_cache,
-                 const int32_t* block_tables, const int32_t* context_lens, int num_seqs, int num_heads,
-                 int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq, int num_blocks, float scale,
-                 int dtype, void* workspace, size_t workspace_bytes, int max_context_len, int partition_pages,
-                 int kernel, void* stream) {
+}  // extern "C"
+
+namespace pa {
+namespace {
+
+// pa_decode_ex, and pa_decode_append when new_key != nullptr.
+int decode_impl(void* out, const void* query, const void* new_key, const void* new_value, const void* key_cache,
+                const void* value_cache, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                int num_blocks, float scale, int dtype, void* workspace, size_t workspace_bytes, int max_context_len,
+                int partition_pages, int kernel, void* stream) {
     clear_error();
     if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "pa_decode: num_seqs=%d", num_seqs);
+    if (new_key && (!new_value || !aligned(new_key, 16) || !aligned(new_value, 16)))
+        return fail(PA_ERR_INVALID_ARG, "pa_decode_append: new_key/new_value must be non-NULL and 16-byte aligned");
     if (num_seqs == 0) return PA_OK;
     if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens)
         return fail(PA_ERR_INVALID_ARG, "pa_decode: NULL pointer");
@@ -427,6 +435,10 @@ int pa_decode_ex(void* out, const void* query, const void* key_cache, const void
     a.ws_l = grid_split ? reinterpret_cast<float*>(ws + p.off_l) : nullptr;
     a.ws_o = grid_split ? reinterpret_cast<float*>(ws + p.off_o) : nullptr;
     a.ws_part = p.schedule == kScheduleLean ? reinterpret_cast<float*>(ws + p.off_part) : nullptr;
+    a.new_key = new_key;
+    a.new_value = new_key ? new_value : nullptr;
+    a.key_cache = new_key ? const_cast<void*>(key_cache) : nullptr;
+    a.value_cache = new_key ? const_cast<void*>(value_cache) : nullptr;
     a.lean_warps_per_cta = p.ki.lean_warps_per_cta;
     a.err = dev->error_word;
     a.num_seqs = num_seqs;
@@ -451,6 +463,35 @@ int pa_decode_ex(void* out, const void* query, const void* key_cache, const void
         if (e != cudaSuccess) return cuda_fail(e, "pa_decode: merge kernel launch");
     }
     return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+extern "C" {
+
+int pa_decode_ex(void* out, const void* query, const void* key_cache, const void* value_cache,
+                 const int32_t* block_tables, const int32_t* context_lens, int num_seqs, int num_heads,
+                 int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq, int num_blocks, float scale,
+                 int dtype, void* workspace, size_t workspace_bytes, int max_context_len, int partition_pages,
+                 int kernel, void* stream) {
+    return decode_impl(out, query, nullptr, nullptr, key_cache, value_cache, block_tables, context_lens, num_seqs,
+                       num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype,
+                       workspace, workspace_bytes, max_context_len, partition_pages, kernel, stream);
+}
+
+int pa_decode_append(void* out, const void* query, const void* new_key, const void* new_value, void* key_cache,
+                     void* value_cache, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                     int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                     int num_blocks, float scale, int dtype, void* workspace, size_t workspace_bytes,
+                     int max_context_len, int partition_pages, int kernel, void* stream) {
+    if (!new_key) {
+        clear_error();
+        return fail(PA_ERR_INVALID_ARG, "pa_decode_append: new_key is NULL");
+    }
+    return decode_impl(out, query, new_key, new_value, key_cache, value_cache, block_tables, context_lens, num_seqs,
+                       num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype,
+                       workspace, workspace_bytes, max_context_len, partition_pages, kernel, stream);
 }
 
 int pa_decode(void* out, const void* query, const void* key_cache, const void* value_cache,

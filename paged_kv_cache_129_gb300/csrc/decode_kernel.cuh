@@ -104,6 +104,61 @@ __device__ __forceinline__ uint32_t swz_offset(int row, int elem) {
 }
 
 // ------------------------------------------------------------------------------------------
+// The step's new token in append mode.  Its K and V rows (D elements each) are held by
+// one warp as 16-byte chunks: chunks 0..kChunks-1 of K, then those of V, lane-strided.
+// The warp that consumes the page holding position L - 1 overwrites that row of its
+// staged K and V tiles (so the page need not be re-read after the cache write) and, for
+// one head chunk of the kv head, stores the rows into the cache: the same bytes
+// pa_write_kv would store, with the slot the block table gives position L - 1.
+template <typename T, int D, int BS>
+struct NewToken {
+    static constexpr int kChunks = D * (int)sizeof(T) / 16;      // 16-byte chunks per row
+    static constexpr int kPerLane = (2 * kChunks + 31) / 32;
+    uint4 c[kPerLane];
+
+    // key_row, value_row: new_key[b, kvh, :], new_value[b, kvh, :] (16-byte aligned).
+    __device__ __forceinline__ void load(const T* key_row, const T* value_row, int lane) {
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            const int idx = lane + 32 * i;
+            if (idx < kChunks)
+                c[i] = __ldg(reinterpret_cast<const uint4*>(key_row) + idx);
+            else if (idx < 2 * kChunks)
+                c[i] = __ldg(reinterpret_cast<const uint4*>(value_row) + idx - kChunks);
+        }
+    }
+
+    // Overwrite row r of the 128-byte-swizzled K and V tiles; then order these generic
+    // writes before the async-proxy (TMA) writes that will later refill the slot.
+    __device__ __forceinline__ void patch(uint8_t* kpage, uint8_t* vpage, int r, int lane) const {
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            const int idx = lane + 32 * i;
+            if (idx < 2 * kChunks) {
+                const int ch = idx < kChunks ? idx : idx - kChunks;
+                uint8_t* tile = idx < kChunks ? kpage : vpage;
+                const int box = ch >> 3, cc = ch & 7;
+                *reinterpret_cast<uint4*>(tile + box * BS * 128 + r * 128 + ((cc ^ (r & 7)) << 4)) = c[i];
+            }
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+    }
+
+    // Store the rows at cache row `row` = (pb * Hkv + kvh) * BS + r of both caches.
+    __device__ __forceinline__ void store(void* key_cache, void* value_cache, int row, int lane) const {
+#pragma unroll
+        for (int i = 0; i < kPerLane; ++i) {
+            const int idx = lane + 32 * i;
+            if (idx < kChunks)
+                reinterpret_cast<uint4*>(static_cast<T*>(key_cache) + (size_t)row * D)[idx] = c[i];
+            else if (idx < 2 * kChunks)
+                reinterpret_cast<uint4*>(static_cast<T*>(value_cache) + (size_t)row * D)[idx - kChunks] = c[i];
+        }
+    }
+};
+
+// ------------------------------------------------------------------------------------------
 // Tensor-core consumer (f16 / bf16).
 template <typename T, int D, int BS>
 struct MmaConsumer {
@@ -542,6 +597,18 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
     } else {
         // ================= consumer warps =================
         const T* qrows = static_cast<const T*>(a.q) + ((size_t)b * a.num_heads + head0) * D;
+        // Append mode: the warp that consumes the page holding position L - 1 takes the
+        // new token into its staged copy of the page, and (head chunk 0) into the cache.
+        const int i_tok = nblk - 1 - first;  // that page's index in this partition
+        const bool tok_mine = a.new_key != nullptr && i_tok < npages && i_tok % C::kNW == warp;
+        NewToken<T, D, BS> tok;
+        int tok_row = -1;
+        if (tok_mine) {
+            const size_t nt = ((size_t)b * a.num_kv_heads + kvh) * D;
+            tok.load(static_cast<const T*>(a.new_key) + nt, static_cast<const T*>(a.new_value) + nt, lane);
+            const int pb = __ldg(a.block_tables + (size_t)b * a.max_blocks + nblk - 1);
+            tok_row = (unsigned)pb < (unsigned)a.num_blocks ? (pb * a.num_kv_heads + kvh) * BS : -1;
+        }
         if constexpr (MMA) {
             MmaConsumer<T, D, BS> cons;
             cons.init(qrows, gc, lane);
@@ -551,6 +618,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
                 if (!__all_sync(0xffffffffu, got)) break;
                 const int nvalid = min(BS, L - (first + i) * BS);
                 uint8_t* kp = ring + s * C::kSlotBytes;
+                if (tok_mine && i == i_tok) {
+                    tok.patch(kp, kp + C::kPageBytes, nvalid - 1, lane);
+                    if (hc == 0 && tok_row >= 0) tok.store(a.key_cache, a.value_cache, tok_row + nvalid - 1, lane);
+                }
                 cons.page(kp, kp + C::kPageBytes, nvalid, a.scale_log2, lane);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
@@ -579,7 +650,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
                 const bool got = mbar_wait_bounded(&full[s], (i / C::kNSlot) & 1, a.err, flags);
                 if (!__all_sync(0xffffffffu, got)) break;
                 const int nvalid = min(BS, L - (first + i) * BS);
-                const uint8_t* kp = ring + s * C::kSlotBytes;
+                uint8_t* kp = ring + s * C::kSlotBytes;
+                if (tok_mine && i == i_tok) {
+                    tok.patch(kp, kp + C::kPageBytes, nvalid - 1, lane);
+                    if (hc == 0 && tok_row >= 0) tok.store(a.key_cache, a.value_cache, tok_row + nvalid - 1, lane);
+                }
                 cons.page(kp, kp + C::kPageBytes, nvalid, a.scale_log2, q_s, p_s, lane);
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
@@ -1000,7 +1075,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Lea
         const int hi = min(total, lo + q_per_warp);
         const int n = hi - lo;
         int unit_first = 0, unit_last = -1;
-        int b = 0, uu = 0, nb = 0, L = 0, head0 = 0, gc = 0;
+        int b = 0, uu = 0, nb = 0, L = 0, head0 = 0, gc = 0, kvh = 0;
+        const bool append = a.new_key != nullptr;
+        NewToken<T, D, BS> tok;
+        bool tok_ready = false, tok_writer = false;
         std::conditional_t<MMA, MmaConsumer<T, D, BS>, SimtConsumer<T, D, BS, GMAX>> cons;
         float* q_s = reinterpret_cast<float*>(smem + C::kQsOffset) + warp * GMAX * D;
         float* p_s = reinterpret_cast<float*>(smem + C::kPsOffset) + warp * GMAX * BS;
@@ -1057,8 +1135,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Lea
                 lean_locate(pre, B, upb, g, b, uu, j0, nb);
                 unit_first = g - j0;
                 unit_last = unit_first + nb - 1;
-                const int kvh = uu / a.head_chunks;
+                kvh = uu / a.head_chunks;
                 const int hc = uu - kvh * a.head_chunks;
+                tok_writer = hc == 0;
                 head0 = kvh * a.group + hc * C::kHeads;
                 gc = min(C::kHeads, a.group - hc * C::kHeads);
                 L = __ldg(a.context_lens + b);
@@ -1075,11 +1154,24 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Lea
                 }
             }
             const int j = g - unit_first;
+            // Append mode: fetch the new token one page ahead of the page holding L - 1.
+            const bool tok_page = append && g == unit_last;
+            if (append && (g + 1 == unit_last || (tok_page && !tok_ready))) {
+                const size_t nt = ((size_t)b * a.num_kv_heads + kvh) * D;
+                tok.load(static_cast<const T*>(a.new_key) + nt, static_cast<const T*>(a.new_value) + nt, lane);
+                tok_ready = true;
+            }
             const int s = warp * C::kSPW + off % C::kSPW;
             const bool got = mbar_wait_bounded(&full[s], (off / C::kSPW) & 1, a.err, flags);
             if (!__all_sync(0xffffffffu, got)) break;
             const int nvalid = min(BS, L - j * BS);
             uint8_t* kp = ring + s * C::kSlotBytes;
+            if (tok_page) {
+                tok.patch(kp, kp + C::kPageBytes, nvalid - 1, lane);
+                const int row = queue[off % C::kRowQueue];  // (pb * Hkv + kvh) * BS, or -1
+                if (tok_writer && row >= 0) tok.store(a.key_cache, a.value_cache, row + nvalid - 1, lane);
+                tok_ready = false;
+            }
             if constexpr (MMA) {
                 cons.page(kp, kp + C::kPageBytes, nvalid, a.scale_log2, lane);
                 __syncwarp();

@@ -18,6 +18,13 @@ struct DecodeArgs {
     float* ws_o;                 // [B * Hq, max_parts, D] unnormalised output per partition
     float* ws_part;              // lean schedule: two partial records per consumer warp
     unsigned* err;               // device error word
+    // Append mode (new_key != nullptr): the new token of sequence b, new_key/new_value
+    // [B, Hkv, D], sits at position L_b - 1; the kernel copies it into its staged copy of
+    // that page and stores it into the cache (raw pointers below) before attending.
+    const void* new_key;
+    const void* new_value;
+    void* key_cache;
+    void* value_cache;
     int num_seqs, num_heads, num_kv_heads, group, head_chunks;
     int max_blocks, num_blocks;
     int partition_pages, max_parts;

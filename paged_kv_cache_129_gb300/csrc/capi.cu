@@ -4,7 +4,10 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <atomic>
+#include <chrono>
 #include <mutex>
+#include <random>
 #include <string>
 
 #include <cudaTypedefs.h>
@@ -73,8 +76,20 @@ bool dtype_ok(int dtype) { return dtype == PA_F32 || dtype == PA_F16 || dtype ==
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
 
-// Lean schedule workspace: two partial records per consumer warp.
-constexpr size_t kLeanMetaBytes = 0;
+// A value for DecodeArgs::epoch that no earlier call of this process has used, and
+// that a workspace left by another process (or holding any other data) is most
+// unlikely to contain: a 64-bit counter that starts at a random value, never 0.
+unsigned long long next_epoch() {
+    static std::atomic<unsigned long long> counter{[] {
+        std::random_device rd;
+        const unsigned long long t =
+            (unsigned long long)std::chrono::steady_clock::now().time_since_epoch().count();
+        return (((unsigned long long)rd() << 32) ^ (unsigned long long)rd()) ^ (t * 0x9E3779B97F4A7C15ull);
+    }()};
+    unsigned long long e = 0;
+    while (e == 0) e = counter.fetch_add(1, std::memory_order_relaxed) + 1;
+    return e;
+}
 
 int cuda_fail(cudaError_t e, const char* what) {
     return fail(PA_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
@@ -154,6 +169,7 @@ struct Plan {
     size_t ws_bytes = 0;
     size_t off_m = 0, off_l = 0, off_o = 0;  // partitioned grid: offsets of m, l and o~
     size_t off_part = 0;                     // lean: warp partial records
+    size_t off_flag = 0;                     // lean: one flag per record
     KernelInfo ki{};
 };
 
@@ -222,16 +238,18 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
         (long long)p.units < lean_ctas * p.ki.lean_warps_per_cta &&
         (long long)num_seqs * max_blocks * num_kv_heads * p.head_chunks < (1ll << 31)) {
         const long long ctas = lean_ctas;
-        const size_t off_part = kLeanMetaBytes;
+        const size_t records = (size_t)ctas * p.ki.lean_warps_per_cta * 2;  // two per consumer warp
         const size_t rec_bytes = (size_t)p.ki.lean_record_floats * sizeof(float);
-        const size_t need = off_part + align256((size_t)ctas * p.ki.lean_warps_per_cta * 2 * rec_bytes);
+        const size_t off_flag = align256(records * rec_bytes);
+        const size_t need = off_flag + align256(records * sizeof(unsigned long long));
         if (need <= ws_avail) {
             p.schedule = kScheduleLean;
             p.partition_pages = 0;
             p.max_parts = 0;
             p.grid = ctas;
             p.ws_bytes = need;
-            p.off_part = off_part;
+            p.off_part = 0;
+            p.off_flag = off_flag;
             *plan = p;
             return PA_OK;
         }
@@ -435,6 +453,8 @@ int decode_impl(void* out, const void* query, const void* new_key, const void* n
     a.ws_l = grid_split ? reinterpret_cast<float*>(ws + p.off_l) : nullptr;
     a.ws_o = grid_split ? reinterpret_cast<float*>(ws + p.off_o) : nullptr;
     a.ws_part = p.schedule == kScheduleLean ? reinterpret_cast<float*>(ws + p.off_part) : nullptr;
+    a.ws_flag = p.schedule == kScheduleLean ? reinterpret_cast<unsigned long long*>(ws + p.off_flag) : nullptr;
+    a.epoch = p.schedule == kScheduleLean ? next_epoch() : 0;
     a.new_key = new_key;
     a.new_value = new_key ? new_value : nullptr;
     a.key_cache = new_key ? const_cast<void*>(key_cache) : nullptr;

@@ -1076,6 +1076,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Lea
         const int n = hi - lo;
         int unit_first = 0, unit_last = -1;
         int b = 0, uu = 0, nb = 0, L = 0, head0 = 0, gc = 0, kvh = 0;
+        int wrote = 0;  // bit s: a partial record was written to slot s
         const bool append = a.new_key != nullptr;
         NewToken<T, D, BS> tok;
         bool tok_ready = false, tok_writer = false;
@@ -1191,6 +1192,17 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Lea
                     float* rec = a.ws_part + ((size_t)wg * 2 + slot) * C::kRecFloats;
                     cons.write_partial(rec, gc, lane);
                     cons.clear();
+                    wrote |= 1 << slot;
+                }
+            }
+            if (off == n - 1 && wrote) {
+                // Publish the records for the merge kernel, once, after the warp's last page
+                // (a GPU-scope fence in the middle of the page stream would stall it).
+                __syncwarp();  // every lane's record stores before lane 0's fence
+                if (lane == 0) {
+                    __threadfence();
+                    if (wrote & 1) st_release_gpu(a.ws_flag + (size_t)wg * 2, a.epoch);
+                    if (wrote & 2) st_release_gpu(a.ws_flag + (size_t)wg * 2 + 1, a.epoch);
                 }
             }
         }
@@ -1223,12 +1235,15 @@ constexpr int kLeanMergeBatch = 8;  // records whose loads a thread keeps in fli
 // decode cut between consumer warps w_lo..w_hi left one partial record per warp
 // (m, l, o~ per head); the merge combines them with the online-softmax rule,
 //     M = max_p m_p,  W = sum_p 2^(m_p - M) l_p,  o = sum_p 2^(m_p - M) o~_p / W.
-// Units that fit in one warp's range were finished by the decode kernel.  The unit's
-// place in the page order is recomputed from the context lengths before waiting for
-// the decode (programmatic dependent launch), so that part overlaps the decode.  That
-// read is safe: this grid can only start once every decode CTA has passed its own
-// wait for the grids before it, so any writer of the lengths has completed.  After
-// the wait every thread merges its own float4 columns of o~ over all records on its
+// Units that fit in one warp's range were finished by the decode kernel.
+// Launched with programmatic stream serialisation, the merge runs while the decode
+// drains: the unit's place in the page order is recomputed from the context lengths,
+// then the CTA waits for the flags of its unit's records (each warp of the decode
+// publishes its records once its pages are done) rather than for the whole decode
+// grid, merges, and only then waits for the decode grid to complete, so that a grid
+// after this one still sees the decode finished.  Reading the lengths early is safe:
+// this grid starts only once every decode CTA has passed its own wait for the grids
+// before it.  Every thread merges its own float4 columns of o~ over all records on its
 // own: no barriers, all loads of a batch of records issued before any is used.
 template <typename T, int D, int H, int BS>
 __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_merge_kernel(const DecodeArgs a) {
@@ -1263,16 +1278,41 @@ __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_me
     const int total = tot * upb;
     const int warps = a.lean_grid * a.lean_warps_per_cta;
     const int q = (total + warps - 1) / warps;
-    // Every CTA waits for the decode, also those with nothing to merge: a grid that
-    // follows this one waits only for this grid, so this grid must not end before the
-    // decode has.
-    griddep_wait();
-    if (nb == 0 || q <= 0) return;
     const int first = pre_b * upb + uu * nb;
-    const int w_lo = first / q, w_hi = (first + nb - 1) / q;
-    if (w_lo == w_hi) return;  // finished by the decode kernel
+    const int w_lo = q > 0 ? first / q : 0, w_hi = q > 0 ? (first + nb - 1) / q : 0;
+    if (nb == 0 || q <= 0 || w_lo == w_hi) {
+        // Nothing to merge (the decode kernel finished the unit).  Every CTA still waits
+        // for the decode grid before it ends: a grid that follows this one waits only for
+        // this grid, so this grid must not end before the decode has.
+        griddep_wait();
+        return;
+    }
     const int n = w_hi - w_lo + 1;
     const int slot0 = first != w_lo * q ? 1 : 0;  // w_lo holds the unit in slot 1 unless its range starts here
+    // Wait until every piece's record is published (flag == epoch), not for the whole
+    // decode grid: the merge of a unit starts as soon as the warps holding it are done.
+    // Bounded; a wait that gives up reports kErrTimeout and merges nothing.
+    __shared__ volatile int gave_up;
+    if (tid == 0) gave_up = 0;
+    __syncthreads();
+    for (int p = tid; p < n; p += kLeanMergeThreads) {
+        const unsigned long long* f = a.ws_flag + (size_t)(w_lo + p) * 2 + (p == 0 ? slot0 : 0);
+        if (ld_acquire_gpu(f) == a.epoch) continue;
+        const unsigned long long start = global_timer_ns();
+        while (ld_acquire_gpu(f) != a.epoch) {
+            if (gave_up || global_timer_ns() - start > kWaitLimitNs) {
+                if (!gave_up) atomicOr(a.err, kErrTimeout);
+                gave_up = 1;
+                break;
+            }
+            __nanosleep(128);
+        }
+    }
+    __syncthreads();
+    if (gave_up) {
+        griddep_wait();
+        return;
+    }
     const int kvh = uu / a.head_chunks, hc = uu - kvh * a.head_chunks;
     const int head0 = kvh * a.group + hc * H;
     const int gc = min(H, a.group - hc * H);
@@ -1352,6 +1392,7 @@ __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_me
         out[3] = from_float<T>(acc.w * inv);
     }
     }
+    griddep_wait();  // this grid must not end before the decode grid has
 }
 
 // ------------------------------------------------------------------------------------------

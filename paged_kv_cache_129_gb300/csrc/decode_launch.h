@@ -17,6 +17,8 @@ struct DecodeArgs {
     float* ws_l;                 // [B * Hq, max_parts]   running denominator per partition
     float* ws_o;                 // [B * Hq, max_parts, D] unnormalised output per partition
     float* ws_part;              // lean schedule: two partial records per consumer warp
+    unsigned long long* ws_flag; // lean schedule: one flag per record, set to `epoch` when published
+    unsigned long long epoch;    // lean schedule: a value no earlier call has used (never 0)
     unsigned* err;               // device error word
     // Append mode (new_key != nullptr): the new token of sequence b, new_key/new_value
     // [B, Hkv, D], sits at position L_b - 1; the kernel copies it into its staged copy of

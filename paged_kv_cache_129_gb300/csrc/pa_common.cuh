@@ -132,6 +132,20 @@ __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     return policy;
 }
 
+// ---- flags between grids running at the same time ------------------------------------------
+// Release store / acquire load at GPU scope: data written before the release (by this
+// thread, or by threads that synchronised with it first) is visible to a thread whose
+// acquire load returns the stored value.
+__device__ __forceinline__ void st_release_gpu(unsigned long long* p, unsigned long long v) {
+    asm volatile("st.release.gpu.global.u64 [%0], %1;" ::"l"(p), "l"(v) : "memory");
+}
+
+__device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.acquire.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // ---- programmatic dependent launch ---------------------------------------------------------
 // Every kernel of the library is launched with programmatic stream serialisation, so
 // that its CTAs can become resident while the previous grid in the stream drains.  Each

@@ -54,6 +54,12 @@ WORKLOAD_DESCRIPTIONS = {
                       "context_lens lognormal(median 256, sigma 1) clipped to [16,2048]",
     "mha_short_bs32": "many short requests, MHA: batch 256, 32/32 heads, head_dim 128, fp16, block_size 32, "
                       "context_lens lognormal(median 256, sigma 1) clipped to [16,2048]",
+    "prefix_cow": "prefix sharing: 64 sequences (one parent + 63 forks through the block pool) share a "
+                  "2048-token prefix (full shared tail: no copy-on-write), private tails uniform in [1,256], "
+                  "28 q / 4 kv heads, head_dim 128, bf16, block_size 16; value = effective GB/s (every "
+                  "sequence's K/V counted), roofline over the unique pages",
+    "prefix_cow_2056": "prefix sharing, copy-on-write variant: as prefix_cow with a 2056-token prefix, so the "
+                       "first append of 63 sequences copies the shared partial block (pa_copy_blocks)",
 }
 DTYPE_NAMES = {"f32": "f32", "f16": "f16", "bf16": "bf16"}
 
@@ -234,6 +240,56 @@ class ClockSampler:
 
 
 # ---- the CPU oracle leg -------------------------------------------------------------------------
+def cpu_model() -> str:
+    try:
+        fields = {}
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if ":" in line:
+                    k, v = line.split(":", 1)
+                    fields.setdefault(k.strip(), v.strip())
+        if "model name" in fields:
+            return fields["model name"]
+        parts = [f"{k} {fields[k]}" for k in ("CPU implementer", "CPU part") if k in fields]
+        return " ".join(parts) or os.uname().machine
+    except OSError:
+        return os.uname().machine
+
+
+def time_oracle_parallel(inp, budget_s: float, threads: int):
+    """Time the fp64 oracle over whole sequences (all heads) on `threads` host threads.
+
+    One sequence is timed alone first; then as many sequences as fit in about
+    `budget_s` of wall time are decoded, one task per sequence (the C oracle
+    releases the GIL).  Returns the seconds, the sequences and rows done, the
+    algorithmic bytes, and the single-thread figure of the first sequence.
+    """
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+
+    eb = inp.elem_bytes
+
+    def seq_bytes(b):
+        return decode_bytes([int(inp.context_lens[b])], inp.num_heads, inp.num_kv_heads, inp.head_dim, eb,
+                            inp.block_size)
+
+    def run(b):
+        oracle.decode_inputs(inp, rows=[(b, h) for h in range(inp.num_heads)])
+
+    t0 = time.perf_counter()
+    run(0)
+    t_one = max(time.perf_counter() - t0, 1e-6)
+    single = seq_bytes(0) / t_one
+    n = int(min(inp.num_seqs, max(threads, budget_s * threads / t_one)))
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        t0 = time.perf_counter()
+        list(ex.map(run, range(n)))
+        dt = time.perf_counter() - t0
+    return {"seconds": dt, "seqs": n, "rows": n * inp.num_heads, "bytes": sum(seq_bytes(b) for b in range(n)),
+            "single_thread_gbs": single / 1e9, "single_thread_seconds": t_one}
+
+
 def time_oracle(inp, budget_s: float, rows_cap: int = 0):
     """Time the fp64 oracle on the first sequences of the batch (all heads), about `budget_s` seconds."""
     import oracle
@@ -270,6 +326,60 @@ def build_batch(workload: str, seed: int):
     gen = {"qwen_gqa": lambda s: wl.qwen_gqa(s), "long_context": lambda s: wl.long_context(s),
            "mha_short_bs16": lambda s: wl.mha_short(16, s), "mha_short_bs32": lambda s: wl.mha_short(32, s)}[workload]
     return gen(seed)
+
+
+def prefix_batch(workload: str, seed: int):
+    """The prefix-sharing workload built through the product block pool.
+
+    A parent appends the shared prefix, 63 forks share it; every sequence then
+    appends its tail but the last token (copy-on-write pairs are copied, tail
+    tokens written, on the host copy of the caches), and the step's new token
+    (each tail's last) is appended for all sequences at once.  Returns the
+    decode inputs, tables, lengths, new-token slots, the number of copy-on-write
+    copies, and the bytes of the distinct pages the decode reads.
+    """
+    import paged_kv_cache_129_gb300 as pa
+    from paged_kv_cache_129_gb300 import workloads as wl
+
+    prefix = 2056 if workload == "prefix_cow_2056" else 2048
+    w = wl.prefix_cow(seed, prefix_len=prefix)
+    bs = w.block_size
+    pool = pa.BlockPool(w.num_blocks, bs, free_order=np.random.default_rng(12345).permutation(w.num_blocks))
+    parent = pool.create()
+    for _ in range(prefix):
+        pool.append(parent)
+    seqs = [parent] + [pool.fork(parent) for _ in range(w.num_seqs - 1)]
+    kc, vc = w.key_cache.copy(), w.value_cache.copy()
+    cum = np.concatenate([[0], np.cumsum(w.tail_lens)]).astype(np.int64)
+    n_cow = 0
+
+    def cow(pair):
+        kc[pair[1]] = kc[pair[0]]
+        vc[pair[1]] = vc[pair[0]]
+
+    for i, sid in enumerate(seqs):
+        for t in range(int(w.tail_lens[i]) - 1):
+            slot, pair = pool.append(sid)
+            if pair:
+                cow(pair)
+                n_cow += 1
+            kc[slot // bs, :, slot % bs, :] = w.tail_key[cum[i] + t]
+            vc[slot // bs, :, slot % bs, :] = w.tail_value[cum[i] + t]
+    slots, pairs = pool.append_batch(seqs)
+    for pair in pairs:
+        cow(pair)
+    n_cow += len(pairs)
+    last = cum[1:] - 1
+    tables, lens = pool.block_tables(seqs, int((int(max(prefix + t for t in w.tail_lens)) + bs - 1) // bs))
+    pool.check_invariants()
+    inp = wl.DecodeInputs(name=workload, dtype="bf16", num_heads=w.num_heads, num_kv_heads=w.num_kv_heads,
+                          head_dim=w.head_dim, block_size=bs, num_blocks=w.num_blocks, q=w.q, key_cache=kc,
+                          value_cache=vc, block_tables=tables, context_lens=lens,
+                          scale=wl.default_scale(w.head_dim), new_key=w.tail_key[last], new_value=w.tail_value[last],
+                          new_token_pos=lens.astype(np.int64) - 1)
+    used = {int(tables[b, j]) for b in range(len(seqs)) for j in range((int(lens[b]) + bs - 1) // bs)}
+    unique_bytes = len(used) * 2 * w.num_kv_heads * bs * w.head_dim * 2
+    return inp, tables, lens, np.asarray(slots, dtype=np.int64), n_cow, unique_bytes
 
 
 def pool_tables(inp):
@@ -310,8 +420,13 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     device = torch.device("cuda", local_rank)
     pa.library()
 
-    inp = build_batch(args.workload, rank_seed(args.seed, rank))
-    tables, lens, slots = pool_tables(inp)
+    prefix = args.workload.startswith("prefix_cow")
+    n_cow, unique_bytes = 0, None
+    if prefix:
+        inp, tables, lens, slots, n_cow, unique_bytes = prefix_batch(args.workload, rank_seed(args.seed, rank))
+    else:
+        inp = build_batch(args.workload, rank_seed(args.seed, rank))
+        tables, lens, slots = pool_tables(inp)
     inp.block_tables = tables
     tdtype = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}[inp.dtype]
 
@@ -328,6 +443,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     wr_bytes = write_bytes(ntok, Hkv, d, eb)
     step_bytes = dec_bytes + wr_bytes
     touched = pages_touched_bytes(lens, Hkv, d, eb, bs)
+    if prefix:
+        touched = unique_bytes  # shared pages are read once per step
 
     l2 = L2_BYTES_DEFAULT
     try:
@@ -510,6 +627,10 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     peak_src = "of measured (MEASURED_PEAKS.json hbm_gbs)" if peak else "of fallback"
     peak = float(peak or FALLBACK_HBM_GBS)
     call_bytes = step_bytes if fused else dec_bytes  # the appending call also does the write
+    if prefix:
+        # every sequence's K/V would exceed HBM peak through L2 hits on the shared prefix:
+        # the roofline counts each distinct page once (plus q, out, tables, lengths, write)
+        call_bytes = unique_bytes + (call_bytes - 2 * int(lens.sum()) * Hkv * d * eb)
     achieved = call_bytes / (dec_avg_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": stored_traffic(args.workload),
@@ -527,11 +648,14 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
             import oracle
 
             oracle.write_kv(inp.new_key, inp.new_value, inp.key_cache, inp.value_cache, slots)
-        r = time_oracle(inp, args.cpu_budget)
-        cpu = {"value": round(r["bytes"] / r["seconds"] / 1e9, 4), "unit": UNIT, "cores": 1, "kind": "oracle",
+        threads = os.cpu_count() or 1
+        r = time_oracle_parallel(inp, args.cpu_budget, threads)
+        cpu = {"value": round(r["bytes"] / r["seconds"] / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"first {r['seqs']} of {B} sequences, all {Hq} heads ({r['rows']} output rows), "
-                         f"fp64 C oracle, single thread, {r['seconds']:.1f} s",
-               "seconds": round(r["seconds"], 2)}
+                         f"fp64 C oracle, one sequence per task on {threads} threads, {r['seconds']:.1f} s",
+               "seconds": round(r["seconds"], 2), "cpu_model": cpu_model(),
+               "single_thread": {"value": round(r["single_thread_gbs"], 4), "unit": UNIT,
+                                 "sample": f"sequence 0, all heads, {r['single_thread_seconds']:.2f} s"}}
 
     clocks = sampler.summary(t_begin, t_end)
     if rank != 0:
@@ -545,6 +669,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
                             else "pa_write_kv (new token per sequence) + pa_decode"),
                    "l2": f"{replicas} cache replicas rotated per step (pages touched per step "
                          f"{touched / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB)",
+                   **({"copy_on_write_copies": n_cow, "unique_page_bytes": unique_bytes,
+                       "value_kind": "effective GB/s: every sequence's K/V counted, shared pages once per "
+                                     "sequence (above HBM peak through L2 hits)"} if prefix else {}),
                    "kernel": {1: "mma", 2: "simt"}[plan.kernel],
                    "schedule": {0: "partitioned grid", 1: "lean persistent wave + merge"}[plan.schedule],
                    "partition_pages": plan.partition_pages,
@@ -564,43 +691,54 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
 
 
 def run_reference(args, rank: int, world: int) -> None:
-    """The oracle as the reference arm: each step decodes a bounded sample of the batch on the host."""
+    """The oracle as the reference arm: each step decodes a bounded sample of the batch on the host cores."""
     if rank != 0:
         return
+    from concurrent.futures import ThreadPoolExecutor
+
     import oracle
 
-    inp = build_batch(args.workload, rank_seed(args.seed, 0))
-    if inp.new_key is not None:
-        pos = inp.new_token_pos
-        slots = np.array([int(inp.block_tables[b, p // inp.block_size]) * inp.block_size + p % inp.block_size
-                          for b, p in enumerate(pos)], dtype=np.int64)
+    if args.workload.startswith("prefix_cow"):
+        inp, tables, lens, slots, _, _ = prefix_batch(args.workload, rank_seed(args.seed, 0))
+    else:
+        inp = build_batch(args.workload, rank_seed(args.seed, 0))
+        tables, lens, slots = pool_tables(inp)
+    inp.block_tables = tables
+    if slots is not None:
         oracle.write_kv(inp.new_key, inp.new_value, inp.key_cache, inp.value_cache, slots)
-    # size the per-step sample so that warmup + steps fit in about two minutes
+    threads = os.cpu_count() or 1
+    # size the per-step sample (heads of sequence 0, one task per head) so that warmup + steps
+    # fit in about two minutes on `threads` threads
     t0 = time.perf_counter()
     oracle.decode_inputs(inp, rows=[(0, 0)])
     t_row = max(time.perf_counter() - t0, 1e-4)
     n_steps = args.steps + args.warmup
-    rows_per_step = int(max(1, min(inp.num_heads, 120.0 / n_steps / t_row)))
-    rows = [(0, h) for h in range(rows_per_step)]
+    rows_per_step = int(max(1, min(inp.num_heads, 120.0 * threads / n_steps / t_row)))
     L0 = int(inp.context_lens[0])
     eb = inp.elem_bytes
     bytes_per_step = rows_per_step / inp.num_heads * decode_bytes([L0], inp.num_heads, inp.num_kv_heads,
                                                                   inp.head_dim, eb, inp.block_size)
-    for _ in range(args.warmup):
-        oracle.decode_inputs(inp, rows=rows)
-    t0 = time.perf_counter()
-    for _ in range(args.steps):
-        oracle.decode_inputs(inp, rows=rows)
-    dt = time.perf_counter() - t0
+    used = min(threads, rows_per_step)
+    with ThreadPoolExecutor(max_workers=used) as ex:
+        def one_step():
+            list(ex.map(lambda h: oracle.decode_inputs(inp, rows=[(0, h)]), range(rows_per_step)))
+
+        for _ in range(args.warmup):
+            one_step()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            one_step()
+        dt = time.perf_counter() - t0
     value = bytes_per_step * args.steps / dt / 1e9
-    sample = (f"sequence 0 (L={L0}), {rows_per_step} of {inp.num_heads} heads per step, fp64 C oracle, "
-              f"single thread")
+    sample = (f"sequence 0 (L={L0}), {rows_per_step} of {inp.num_heads} heads per step, one head per task, "
+              f"fp64 C oracle on {used} threads")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAMES[inp.dtype],
             "data": "synthetic",
             "config": {"workload": WORKLOAD_DESCRIPTIONS[args.workload], "name": args.workload},
-            "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": 1, "kind": "oracle", "sample": sample},
+            "cpu_baseline": {"value": round(value, 5), "unit": UNIT, "cores": used, "kind": "oracle",
+                             "sample": sample, "cpu_model": cpu_model()},
             "e2e": {"value": round(value, 5), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 

@@ -158,6 +158,21 @@ struct NewToken {
     }
 };
 
+// Partitioned-grid kernel: fetch the new token of (b, kvh) and put it into the staged page
+// `lb` (the page holding position L - 1; nvalid of its rows are in the context), and, for
+// head chunk 0, into the cache at the slot the block table gives.
+template <typename T, int D, int BS>
+__device__ __noinline__ void append_token(const DecodeArgs& a, int b, int kvh, int hc, int lb, uint8_t* kpage,
+                                          uint8_t* vpage, int nvalid, int lane) {
+    NewToken<T, D, BS> tok;
+    const size_t nt = ((size_t)b * a.num_kv_heads + kvh) * D;
+    tok.load(static_cast<const T*>(a.new_key) + nt, static_cast<const T*>(a.new_value) + nt, lane);
+    tok.patch(kpage, vpage, nvalid - 1, lane);
+    if (hc != 0) return;
+    const int pb = __ldg(a.block_tables + (size_t)b * a.max_blocks + lb);
+    if ((unsigned)pb < (unsigned)a.num_blocks) tok.store(a.key_cache, a.value_cache, (pb * a.num_kv_heads + kvh) * BS + nvalid - 1, lane);
+}
+
 // ------------------------------------------------------------------------------------------
 // Tensor-core consumer (f16 / bf16).
 template <typename T, int D, int BS>
@@ -599,16 +614,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
         const T* qrows = static_cast<const T*>(a.q) + ((size_t)b * a.num_heads + head0) * D;
         // Append mode: the warp that consumes the page holding position L - 1 takes the
         // new token into its staged copy of the page, and (head chunk 0) into the cache.
-        const int i_tok = nblk - 1 - first;  // that page's index in this partition
-        const bool tok_mine = a.new_key != nullptr && i_tok < npages && i_tok % C::kNW == warp;
-        NewToken<T, D, BS> tok;
-        int tok_row = -1;
-        if (tok_mine) {
-            const size_t nt = ((size_t)b * a.num_kv_heads + kvh) * D;
-            tok.load(static_cast<const T*>(a.new_key) + nt, static_cast<const T*>(a.new_value) + nt, lane);
-            const int pb = __ldg(a.block_tables + (size_t)b * a.max_blocks + nblk - 1);
-            tok_row = (unsigned)pb < (unsigned)a.num_blocks ? (pb * a.num_kv_heads + kvh) * BS : -1;
-        }
+        // The token is fetched when that page comes up (holding it in registers across the
+        // page loop would cost this kernel its occupancy).
+        const int i_tok = a.new_key != nullptr ? nblk - 1 - first : -1;  // that page's index here
         if constexpr (MMA) {
             MmaConsumer<T, D, BS> cons;
             cons.init(qrows, gc, lane);
@@ -618,10 +626,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
                 if (!__all_sync(0xffffffffu, got)) break;
                 const int nvalid = min(BS, L - (first + i) * BS);
                 uint8_t* kp = ring + s * C::kSlotBytes;
-                if (tok_mine && i == i_tok) {
-                    tok.patch(kp, kp + C::kPageBytes, nvalid - 1, lane);
-                    if (hc == 0 && tok_row >= 0) tok.store(a.key_cache, a.value_cache, tok_row + nvalid - 1, lane);
-                }
+                if (i == i_tok) append_token<T, D, BS>(a, b, kvh, hc, nblk - 1, kp, kp + C::kPageBytes, nvalid, lane);
                 cons.page(kp, kp + C::kPageBytes, nvalid, a.scale_log2, lane);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
@@ -651,10 +656,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
                 if (!__all_sync(0xffffffffu, got)) break;
                 const int nvalid = min(BS, L - (first + i) * BS);
                 uint8_t* kp = ring + s * C::kSlotBytes;
-                if (tok_mine && i == i_tok) {
-                    tok.patch(kp, kp + C::kPageBytes, nvalid - 1, lane);
-                    if (hc == 0 && tok_row >= 0) tok.store(a.key_cache, a.value_cache, tok_row + nvalid - 1, lane);
-                }
+                if (i == i_tok) append_token<T, D, BS>(a, b, kvh, hc, nblk - 1, kp, kp + C::kPageBytes, nvalid, lane);
                 cons.page(kp, kp + C::kPageBytes, nvalid, a.scale_log2, q_s, p_s, lane);
                 if (lane == 0) mbar_arrive(&empty[s]);
             }

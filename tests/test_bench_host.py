@@ -64,3 +64,19 @@ def test_max_and_sum_over_two_gloo_ranks():
         p.join(120)
         assert p.exitcode == 0
     assert out[0] == out[1] == (11.0, 4.5)
+
+
+@pytest.mark.parametrize("workload,copies", [("prefix_cow", 0), ("prefix_cow_2056", 63)])
+def test_prefix_setup_through_the_block_pool(workload, copies):
+    inp, tables, lens, slots, n_cow, unique = bench.prefix_batch(workload, 0)
+    assert n_cow == copies
+    bs = inp.block_size
+    # the step's new token sits at position L - 1 of every sequence
+    derived = tables[np.arange(len(lens)), (lens - 1) // bs].astype(np.int64) * bs + (lens - 1) % bs
+    assert np.array_equal(slots, derived)
+    # the shared prefix blocks are the same physical blocks in every table
+    shared = (2056 if copies else 2048) // bs
+    assert (tables[:, :shared] == tables[0, :shared]).all()
+    # distinct pages are far fewer than the pages all sequences read
+    touched = bench.pages_touched_bytes(lens, inp.num_kv_heads, inp.head_dim, 2, bs)
+    assert unique < touched / 8

@@ -558,59 +558,45 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     value = total_bytes / (elapsed_ms_max / 1e3) / 1e9
     ms_per_step = elapsed_ms_max / K
 
-    # e2e: public API, inputs from pinned host memory, output back to pinned host memory
+    # e2e: the public step runner (pa.DecodeStepper): every step one packed upload of the step's inputs
+    # from pinned host memory, the decode call, one download of the output; two slots, so the upload of
+    # step i + 1 overlaps the decode of step i.
     e2e = None
-    if not args.no_e2e:
-        def pinned(a):
-            a = np.ascontiguousarray(a)
-            t = torch.from_numpy(a.view(np.int16) if inp.dtype in ("bf16", "f16") else a).pin_memory()
-            return t.view(tdtype) if inp.dtype in ("bf16", "f16") else t
+    if not args.no_e2e and not (has_write and not fused):  # the runner does not split write and decode
+        stepper = pa.DecodeStepper(kcs[0], vcs[0], B, Hq, tables.shape[1], scale=inp.scale, append=fused,
+                                   max_context_len=max_ctx, partition_pages=args.partition_pages,
+                                   kernel=args.kernel)
 
-        q_h = pinned(inp.q)
-        bt_h, dl_h = torch.from_numpy(tables).pin_memory(), torch.from_numpy(lens).pin_memory()
-        out_h = torch.empty(out.shape, dtype=tdtype).pin_memory()
-        if has_write:
-            nk_h, nv_h = pinned(inp.new_key), pinned(inp.new_value)
-            sl_h = torch.from_numpy(slots).pin_memory()
-        q_d, bt_d, dl_d = torch.empty_like(q), torch.empty_like(bt), torch.empty_like(dl)
-        if has_write:
-            nk_d, nv_d, sl_d = torch.empty_like(nk), torch.empty_like(nv), torch.empty_like(sl)
-        h2d = q_h.numel() * q_h.element_size() + bt_h.numel() * 4 + dl_h.numel() * 4
-        if has_write:
-            h2d += 2 * nk_h.numel() * nk_h.element_size() + (0 if fused else sl_h.numel() * 8)
-        d2h = out_h.numel() * out_h.element_size()
+        def fill(view, arr):
+            a = np.ascontiguousarray(arr)
+            t = torch.from_numpy(a.view(np.int16) if inp.dtype in ("bf16", "f16") else a)
+            view.copy_(t.view(view.dtype) if inp.dtype in ("bf16", "f16") else t)
 
-        def e2e_step(i):
-            r = i % replicas
-            q_d.copy_(q_h, non_blocking=True)
-            bt_d.copy_(bt_h, non_blocking=True)
-            dl_d.copy_(dl_h, non_blocking=True)
+        for sl in range(stepper.slots):
+            v = stepper.inputs(sl)
+            fill(v.query, inp.q)
+            v.block_tables.copy_(torch.from_numpy(tables))
+            v.context_lens.copy_(torch.from_numpy(lens))
             if fused:
-                nk_d.copy_(nk_h, non_blocking=True)
-                nv_d.copy_(nv_h, non_blocking=True)
-                pa.decode_append(q_d, nk_d, nv_d, kcs[r], vcs[r], bt_d, dl_d, scale=inp.scale, out=out,
-                                 workspace=ws, max_context_len=max_ctx, partition_pages=args.partition_pages,
-                                 kernel=args.kernel)
-            else:
-                if has_write:
-                    nk_d.copy_(nk_h, non_blocking=True)
-                    nv_d.copy_(nv_h, non_blocking=True)
-                    sl_d.copy_(sl_h, non_blocking=True)
-                    pa.write_kv(nk_d, nv_d, kcs[r], vcs[r], sl_d)
-                pa.decode(q_d, kcs[r], vcs[r], bt_d, dl_d, scale=inp.scale, out=out, workspace=ws,
-                          max_context_len=max_ctx, partition_pages=args.partition_pages, kernel=args.kernel)
-            out_h.copy_(out, non_blocking=True)
+                fill(v.new_key, inp.new_key)
+                fill(v.new_value, inp.new_value)
 
-        for i in range(min(args.warmup, 20)):
-            e2e_step(i)
+        def e2e_run(n):
+            for i in range(n):
+                stepper.launch(i, kcs[i % replicas], vcs[i % replicas])
+                if i >= 1:
+                    stepper.result(i - 1)
+            stepper.result(n - 1)
+
+        e2e_run(min(args.warmup, 20) + 1)
         torch.cuda.synchronize()
         Ke = max(1, min(K, args.e2e_steps))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         barrier(world)
         torch.cuda.synchronize()
         e0.record(stream)
-        for i in range(Ke):
-            e2e_step(i)
+        stepper.upload.wait_event(e0)
+        e2e_run(Ke)
         e1.record(stream)
         torch.cuda.synchronize()
         barrier(world)
@@ -618,10 +604,12 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         e_ms = max_over_ranks(e0.elapsed_time(e1), world)
         e_bytes = sum_over_ranks(float(step_bytes) * Ke, world)
         e2e = {"value": round(e_bytes / (e_ms / 1e3) / 1e9, 2), "unit": UNIT, "steps": Ke,
-               "ms_per_step": round(e_ms / Ke, 5), "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-               "note": f"{'pa.decode_append' if fused else 'pa.write_kv + pa.decode'} through the Python API; "
-                       "inputs copied from pinned host memory "
-                       "and the output copied back every step, inside the timed region"}
+               "ms_per_step": round(e_ms / Ke, 5), "h2d_bytes_per_step": int(stepper.h2d_bytes),
+               "d2h_bytes_per_step": int(stepper.d2h_bytes),
+               "note": f"pa.DecodeStepper ({'pa_decode_append' if fused else 'pa_decode'}): every step one upload "
+                       "of the packed inputs (queries" + (", new K/V" if fused else "") + ", block tables, "
+                       "lengths) from pinned host memory and one download of the output, inside the timed "
+                       "region; two slots, the next upload overlapping the current decode"}
 
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")

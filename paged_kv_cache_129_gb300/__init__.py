@@ -24,6 +24,9 @@ from .binding import (  # noqa: F401
 )
 
 
+from .step import DecodeStepper  # noqa: F401,E402
+
+
 def build(force: bool = False) -> str:
     """Compile the CUDA library in-tree (nvcc, sm_103a)."""
     from .native_build import build as _build

@@ -138,8 +138,8 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // 2-D view of a cache: rows = num_blocks * H_kv * bs (one row per slot and head), columns = d.
 // The box is 128 bytes of d by bs rows, loaded with the 128-byte swizzle.
-int encode_cache_map(CUtensorMap* map, const void* base, int dtype, int num_blocks, int num_kv_heads,
-                     int block_size, int head_dim) {
+int encode_cache_map_uncached(CUtensorMap* map, const void* base, int dtype, int num_blocks, int num_kv_heads,
+                              int block_size, int head_dim) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const int eb = elem_bytes(dtype);
@@ -154,6 +154,31 @@ int encode_cache_map(CUtensorMap* map, const void* base, int dtype, int num_bloc
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                         CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     if (r != CUDA_SUCCESS) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled failed (CUresult %d)", (int)r);
+    return PA_OK;
+}
+
+// The same caches are described again on every call of a decode loop: keep the last few
+// descriptors of this thread (a descriptor is a pure function of these arguments).
+int encode_cache_map(CUtensorMap* map, const void* base, int dtype, int num_blocks, int num_kv_heads,
+                     int block_size, int head_dim) {
+    struct Entry {
+        const void* base;
+        int dtype, num_blocks, num_kv_heads, block_size, head_dim;
+        CUtensorMap map;
+    };
+    constexpr int kEntries = 8;
+    thread_local Entry entries[kEntries] = {};
+    thread_local int next = 0;
+    for (const Entry& e : entries)
+        if (e.base == base && e.base && e.dtype == dtype && e.num_blocks == num_blocks &&
+            e.num_kv_heads == num_kv_heads && e.block_size == block_size && e.head_dim == head_dim) {
+            *map = e.map;
+            return PA_OK;
+        }
+    const int st = encode_cache_map_uncached(map, base, dtype, num_blocks, num_kv_heads, block_size, head_dim);
+    if (st != PA_OK) return st;
+    entries[next] = Entry{base, dtype, num_blocks, num_kv_heads, block_size, head_dim, *map};
+    next = (next + 1) % kEntries;
     return PA_OK;
 }
 

@@ -35,6 +35,8 @@
 //    shared memory as fp32), one lane per d-slice for PV.
 #pragma once
 
+#include <atomic>
+
 #include <cfloat>
 #include <type_traits>
 
@@ -1420,16 +1422,16 @@ struct DecodeKernel {
 
     // Resident lean CTAs per SM for a given dynamic shared-memory size (memoised per device and KB).
     static int lean_occupancy(int device, int smem) {
-        static int cache[64][232] = {};
+        static std::atomic<int> cache[64][232];
         const int kb = (smem + 1023) / 1024;
-        int& slot = cache[device & 63][kb < 232 ? kb : 231];
-        if (slot) return slot;
-        int n = 0;
+        std::atomic<int>& slot = cache[device & 63][kb < 232 ? kb : 231];
+        int n = slot.load(std::memory_order_relaxed);
+        if (n > 0) return n;
         if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_lean_kernel<T, D, BS, MMA, GMAX>,
                                                           LC::kThreads, kb * 1024) != cudaSuccess ||
             n <= 0)
             n = 1;
-        slot = n;
+        slot.store(n, std::memory_order_relaxed);
         return n;
     }
 
@@ -1441,12 +1443,18 @@ struct DecodeKernel {
         info->smem_bytes = C::kSmemBytes;
         info->heads_per_cta = C::kHeads;
         info->merge_parts_cap = kMergeMaxParts;
-        info->ctas_per_sm = 1;
-        int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_kernel<T, D, BS, MMA, GMAX>, C::kThreads,
-                                                          C::kSmemBytes) == cudaSuccess &&
-            n > 0)
-            info->ctas_per_sm = n;
+        // resident CTAs per SM of the partitioned-grid kernel, memoised per device (an occupancy
+        // query per call would cost the host several microseconds)
+        static std::atomic<int> grid_occ[64];
+        int n = grid_occ[device & 63].load(std::memory_order_relaxed);
+        if (n <= 0) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_kernel<T, D, BS, MMA, GMAX>,
+                                                              C::kThreads, C::kSmemBytes) != cudaSuccess ||
+                n <= 0)
+                n = 1;
+            grid_occ[device & 63].store(n, std::memory_order_relaxed);
+        }
+        info->ctas_per_sm = n;
         const int seqs = num_seqs < 1 ? 1 : (num_seqs > kLeanMaxSeqs ? kLeanMaxSeqs : num_seqs);
         info->lean_smem_bytes = LC::smem_bytes(seqs);
         info->lean_ctas_per_sm = lean_occupancy(device, info->lean_smem_bytes);

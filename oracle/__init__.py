@@ -56,6 +56,9 @@ def _load() -> ctypes.CDLL:
             lib.oracle_decode_rows.restype = i32
             lib.oracle_decode_rows.argtypes = [p, p, p, i32, p, p, p, i32, p, p, i32, i32, i32, i32,
                                                i32, i32, i32, dbl]
+            lib.oracle_decode_multi_rows.restype = i32
+            lib.oracle_decode_multi_rows.argtypes = [p, p, p, p, i32, p, p, p, i32, p, p, i32, i32, i32, i32,
+                                                     i32, i32, i32, i32, dbl]
             lib.oracle_write_kv.restype = i32
             lib.oracle_write_kv.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, i32]
             lib.oracle_copy_blocks.restype = i32
@@ -112,6 +115,39 @@ def decode(q: np.ndarray, key_cache: np.ndarray, value_cache: np.ndarray, block_
     if status != OK:
         raise ValueError(f"oracle decode failed with status {status}")
     return out.reshape(num_seqs, num_heads, head_dim) if rows is None else out
+
+
+def decode_multi(q: np.ndarray, key_cache: np.ndarray, value_cache: np.ndarray, block_tables: np.ndarray,
+                 context_lens: np.ndarray, dtype: str, scale: float, rows: Optional[Sequence[tuple]] = None
+                 ) -> np.ndarray:
+    """fp64 multi-query decode: ``q`` is ``[B, q_len, H_q, d]``; token t of sequence b sits at position
+    L_b - q_len + t and attends positions 0 .. L_b - q_len + t (causal).
+
+    Returns ``[B, q_len, H_q, d]`` float64, or ``[len(rows), d]`` for rows ``(b, t, qh)``.
+    """
+    lib = _load()
+    q = np.ascontiguousarray(q)
+    key_cache = np.ascontiguousarray(key_cache)
+    value_cache = np.ascontiguousarray(value_cache)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    num_seqs, q_len, num_heads, head_dim = q.shape
+    num_blocks, hkv, block_size, d2 = key_cache.shape
+    assert d2 == head_dim and value_cache.shape == key_cache.shape
+    if rows is None:
+        rb, rt, rh = (x.reshape(-1) for x in np.meshgrid(np.arange(num_seqs), np.arange(q_len), np.arange(num_heads),
+                                                           indexing="ij"))
+    else:
+        rb, rt, rh = (np.array([r[k] for r in rows]) for k in range(3))
+    rb, rt, rh = (np.ascontiguousarray(x, dtype=np.int32) for x in (rb, rt, rh))
+    out = np.zeros((rb.size, head_dim), dtype=np.float64)
+    status = lib.oracle_decode_multi_rows(_ptr(out), _ptr(rb), _ptr(rt), _ptr(rh), int(rb.size), _ptr(q),
+                                          _ptr(key_cache), _ptr(value_cache), DTYPE_CODES[dtype], _ptr(bt), _ptr(lens),
+                                          num_seqs, q_len, num_heads, hkv, head_dim, block_size, bt.shape[1],
+                                          num_blocks, float(scale))
+    if status != OK:
+        raise ValueError(f"oracle multi-query decode failed with status {status}")
+    return out.reshape(num_seqs, q_len, num_heads, head_dim) if rows is None else out
 
 
 def decode_inputs(inp, rows=None) -> np.ndarray:

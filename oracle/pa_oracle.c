@@ -76,14 +76,70 @@ double oracle_element_to_double(const void* base, int dtype, int64_t index) {
 }
 
 /*
+ * One output row: attention of the query row at q_base over positions
+ * 0 .. n_att - 1 of sequence b, kv head kvh (n_att <= 0 gives a zero row).
+ * Address translation (position -> logical block -> table -> physical block ->
+ * offset), fp64 scores, a two-pass softmax (global max, then the normaliser),
+ * then the probability-weighted sum of the value rows.
+ */
+static int attend(double* o, const void* query, int64_t q_base, int n_att, int b, int kvh,
+                  const void* key_cache, const void* value_cache, int dtype, const int32_t* block_tables,
+                  int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
+                  double scale) {
+    for (int i = 0; i < head_dim; ++i) o[i] = 0.0;
+    if (n_att <= 0) return ORACLE_OK;
+    double* s = (double*)malloc(sizeof(double) * (size_t)n_att);
+    int64_t* row_base = (int64_t*)malloc(sizeof(int64_t) * (size_t)n_att);
+    if (!s || !row_base) {
+        free(s);
+        free(row_base);
+        return ORACLE_NO_MEMORY;
+    }
+    /* Pass 1: address translation and scores. */
+    for (int pos = 0; pos < n_att; ++pos) {
+        const int logical_block = pos / block_size;
+        const int off = pos % block_size;
+        const int pb = block_tables[(int64_t)b * max_blocks_per_seq + logical_block];
+        if (pb < 0 || pb >= num_blocks) {
+            free(s);
+            free(row_base);
+            return ORACLE_BAD_TABLE;
+        }
+        row_base[pos] = (((int64_t)pb * num_kv_heads + kvh) * block_size + off) * head_dim;
+        double dot = 0.0;
+        for (int i = 0; i < head_dim; ++i)
+            dot += element(query, dtype, q_base + i) * element(key_cache, dtype, row_base[pos] + i);
+        s[pos] = scale * dot;
+    }
+    /* Pass 2: global max, then the normaliser over all attended positions. */
+    double m = s[0];
+    for (int pos = 1; pos < n_att; ++pos)
+        if (s[pos] > m) m = s[pos];
+    double z = 0.0;
+    for (int pos = 0; pos < n_att; ++pos) {
+        s[pos] = exp(s[pos] - m);
+        z += s[pos];
+    }
+    /* Pass 3: probability-weighted sum of the value rows. */
+    for (int pos = 0; pos < n_att; ++pos) {
+        const double p = s[pos] / z;
+        for (int i = 0; i < head_dim; ++i) o[i] += p * element(value_cache, dtype, row_base[pos] + i);
+    }
+    free(s);
+    free(row_base);
+    return ORACLE_OK;
+}
+
+/*
  * Decode attention for the selected output rows (b, qh).
  *   out           [n_rows, head_dim] doubles
  *   query         [num_seqs, num_heads, head_dim]
  *   caches        [num_blocks, num_kv_heads, block_size, head_dim]
  *   block_tables  [num_seqs, max_blocks_per_seq] int32
  *   context_lens  [num_seqs] int32
- * A context length of 0 gives a zero row.  Returns ORACLE_BAD_TABLE if a table
- * entry that the context needs is outside [0, num_blocks).
+ * Every row attends all L = context_lens[b] positions; L == 0 gives a zero row.
+ * Returns ORACLE_BAD_TABLE if a table entry that the context needs is outside
+ * [0, num_blocks).
  */
 int oracle_decode_rows(double* out, const int32_t* row_seq, const int32_t* row_head, int n_rows,
                        const void* query, const void* key_cache, const void* value_cache, int dtype,
@@ -97,53 +153,45 @@ int oracle_decode_rows(double* out, const int32_t* row_seq, const int32_t* row_h
         const int b = row_seq[r];
         const int qh = row_head[r];
         if (b < 0 || b >= num_seqs || qh < 0 || qh >= num_heads) return ORACLE_BAD_ARG;
-        const int kvh = qh / group;
         const int L = context_lens[b];
-        double* o = out + (int64_t)r * head_dim;
-        for (int i = 0; i < head_dim; ++i) o[i] = 0.0;
         if (L < 0 || L > (int64_t)max_blocks_per_seq * block_size) return ORACLE_BAD_ARG;
-        if (L == 0) continue;
+        const int st = attend(out + (int64_t)r * head_dim, query, ((int64_t)b * num_heads + qh) * head_dim, L, b,
+                              qh / group, key_cache, value_cache, dtype, block_tables, num_kv_heads, head_dim,
+                              block_size, max_blocks_per_seq, num_blocks, scale);
+        if (st != ORACLE_OK) return st;
+    }
+    return ORACLE_OK;
+}
 
-        double* s = (double*)malloc(sizeof(double) * (size_t)L);
-        int64_t* row_base = (int64_t*)malloc(sizeof(int64_t) * (size_t)L);
-        if (!s || !row_base) {
-            free(s);
-            free(row_base);
-            return ORACLE_NO_MEMORY;
-        }
-        const int64_t q_base = ((int64_t)b * num_heads + qh) * head_dim;
-        /* Pass 1: address translation and scores. */
-        for (int pos = 0; pos < L; ++pos) {
-            const int logical_block = pos / block_size;
-            const int off = pos % block_size;
-            const int pb = block_tables[(int64_t)b * max_blocks_per_seq + logical_block];
-            if (pb < 0 || pb >= num_blocks) {
-                free(s);
-                free(row_base);
-                return ORACLE_BAD_TABLE;
-            }
-            row_base[pos] = (((int64_t)pb * num_kv_heads + kvh) * block_size + off) * head_dim;
-            double dot = 0.0;
-            for (int i = 0; i < head_dim; ++i)
-                dot += element(query, dtype, q_base + i) * element(key_cache, dtype, row_base[pos] + i);
-            s[pos] = scale * dot;
-        }
-        /* Pass 2: global max, then the normaliser over all L positions. */
-        double m = s[0];
-        for (int pos = 1; pos < L; ++pos)
-            if (s[pos] > m) m = s[pos];
-        double z = 0.0;
-        for (int pos = 0; pos < L; ++pos) {
-            s[pos] = exp(s[pos] - m);
-            z += s[pos];
-        }
-        /* Pass 3: probability-weighted sum of the value rows. */
-        for (int pos = 0; pos < L; ++pos) {
-            const double p = s[pos] / z;
-            for (int i = 0; i < head_dim; ++i) o[i] += p * element(value_cache, dtype, row_base[pos] + i);
-        }
-        free(s);
-        free(row_base);
+/*
+ * Multi-query decode: the verify (or chunked-prefill tail) step of the vLLM and
+ * PagedAttention page, section "how the attention kernel reads paged KV": each
+ * sequence has a query range and a context length, under a causal mask.
+ * Sequence b has q_len query tokens, at positions L - q_len .. L - 1 of its
+ * context (L = context_lens[b], their K/V already in the cache); query token t
+ * attends positions 0 .. L - q_len + t, none when that bound is negative (a
+ * zero row).
+ *   out    [n_rows, head_dim] doubles for the rows (row_seq, row_tok, row_head)
+ *   query  [num_seqs, q_len, num_heads, head_dim]
+ */
+int oracle_decode_multi_rows(double* out, const int32_t* row_seq, const int32_t* row_tok, const int32_t* row_head,
+                             int n_rows, const void* query, const void* key_cache, const void* value_cache,
+                             int dtype, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                             int q_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                             int max_blocks_per_seq, int num_blocks, double scale) {
+    if (num_kv_heads <= 0 || num_heads % num_kv_heads != 0 || head_dim <= 0 || block_size <= 0 || q_len <= 0)
+        return ORACLE_BAD_ARG;
+    const int group = num_heads / num_kv_heads;
+    for (int r = 0; r < n_rows; ++r) {
+        const int b = row_seq[r], t = row_tok[r], qh = row_head[r];
+        if (b < 0 || b >= num_seqs || t < 0 || t >= q_len || qh < 0 || qh >= num_heads) return ORACLE_BAD_ARG;
+        const int L = context_lens[b];
+        if (L < 0 || L > (int64_t)max_blocks_per_seq * block_size) return ORACLE_BAD_ARG;
+        const int64_t q_base = (((int64_t)b * q_len + t) * num_heads + qh) * head_dim;
+        const int st = attend(out + (int64_t)r * head_dim, query, q_base, L - q_len + t + 1, b, qh / group,
+                              key_cache, value_cache, dtype, block_tables, num_kv_heads, head_dim, block_size,
+                              max_blocks_per_seq, num_blocks, scale);
+        if (st != ORACLE_OK) return st;
     }
     return ORACLE_OK;
 }

@@ -157,7 +157,7 @@ def make_decode_inputs(name: str, *, context_lens, num_heads: int, num_kv_heads:
                        head_dim: int, block_size: int, dtype: str, num_blocks: Optional[int] = None,
                        pool_slack: float = 0.0, seed: int = 0,
                        with_new_token: bool = False, max_blocks: Optional[int] = None,
-                       scale: Optional[float] = None) -> DecodeInputs:
+                       scale: Optional[float] = None, q_len: int = 1) -> DecodeInputs:
     """Build a seeded decode batch.
 
     ``context_lens`` may be a sequence of ints, or a callable that draws them
@@ -178,7 +178,9 @@ def make_decode_inputs(name: str, *, context_lens, num_heads: int, num_kv_heads:
     cache_shape = (num_blocks, num_kv_heads, block_size, head_dim)
     key_cache = _normal(streams[0], cache_shape, dtype)
     value_cache = _normal(streams[1], cache_shape, dtype)
-    q = _normal(streams[2], (len(lens), num_heads, head_dim), dtype)
+    # q_len > 1: the queries of the last q_len positions of every sequence, [B, q_len, H_q, d]
+    q_shape = (len(lens), num_heads, head_dim) if q_len == 1 else (len(lens), q_len, num_heads, head_dim)
+    q = _normal(streams[2], q_shape, dtype)
     inp = DecodeInputs(name=name, dtype=dtype, num_heads=num_heads, num_kv_heads=num_kv_heads,
                        head_dim=head_dim, block_size=block_size, num_blocks=num_blocks, q=q,
                        key_cache=key_cache, value_cache=value_cache, block_tables=tables,

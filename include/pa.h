@@ -185,6 +185,27 @@ int pa_decode_append(void* out, const void* query, const void* new_key, const vo
                      int num_blocks, float scale, int dtype, void* workspace, size_t workspace_bytes,
                      int max_context_len, int partition_pages, int kernel, void* stream);
 
+/*
+ * pa_decode_multi — multi-query decode: the verify step of speculative decoding, or
+ * the tail of a chunked prefill (vLLM and PagedAttention page, section on how the
+ * attention kernel reads paged KV: each sequence's query range and context length,
+ * verify semantics, causal mask).  Sequence b has q_len query tokens, at positions
+ * L_b - q_len .. L_b - 1 of its context (L_b = context_lens[b]; their K/V are in the
+ * cache already, e.g. written with pa_write_kv); query token t attends positions
+ * 0 .. L_b - q_len + t, and a token whose bound is negative gets a zero row.
+ *  query, out  [num_seqs, q_len, num_heads, head_dim].
+ * A kv head serves q_len * g query rows, so each page of the context is read once for
+ * all of them.  Other arguments as pa_decode_ex; q_len == 1 is pa_decode_ex.  The
+ * workspace for the default plan: pa_decode_multi_workspace_size().
+ */
+int pa_decode_multi(void* out, const void* query, const void* key_cache, const void* value_cache,
+                    const int32_t* block_tables, const int32_t* context_lens, int num_seqs, int q_len, int num_heads,
+                    int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
+                    float scale, int dtype, void* workspace, size_t workspace_bytes, int max_context_len,
+                    int partition_pages, int kernel, void* stream);
+size_t pa_decode_multi_workspace_size(int num_seqs, int q_len, int num_heads, int num_kv_heads, int head_dim,
+                                      int block_size, int max_blocks_per_seq, int dtype);
+
 /* The partition plan pa_decode_ex would use on the current device. */
 typedef struct pa_decode_plan {
     int kernel;            /* PA_KERNEL_MMA or PA_KERNEL_SIMT */

@@ -15,6 +15,8 @@ from .binding import (  # noqa: F401
     copy_blocks,
     decode,
     decode_append,
+    decode_multi,
+    decode_multi_workspace_size,
     decode_plan,
     decode_static_scratch,
     decode_workspace_size,

@@ -63,6 +63,8 @@ _SIGNATURES = [
     ("pa_decode_ex", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _I, _I, _I, _P]),
     ("pa_decode_append", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _I, _I, _I,
                               _P]),
+    ("pa_decode_multi", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _I, _I, _I, _P]),
+    ("pa_decode_multi_workspace_size", _SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
     ("pa_decode_make_plan", _I, [_I, _I, _I, _I, _I, _I, _I, _SZ, _I, _I, _I, ctypes.POINTER(DecodePlan)]),
     ("pa_decode_workspace_size", _SZ, [_I, _I, _I, _I, _I, _I, _I]),
     ("pa_decode_static_scratch", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
@@ -222,6 +224,47 @@ def decode(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tens
                                   block_tables.shape[1], num_blocks, float(scale), _dtype_code(query), ws_ptr or None,
                                   ws_bytes, max_context_len, partition_pages, KERNELS[kernel],
                                   _stream_ptr(stream, query.device)))
+    return out
+
+
+def decode_multi_workspace_size(num_seqs: int, q_len: int, num_heads: int, num_kv_heads: int, head_dim: int,
+                                block_size: int, max_blocks_per_seq: int, dtype: torch.dtype) -> int:
+    return int(library().pa_decode_multi_workspace_size(num_seqs, q_len, num_heads, num_kv_heads, head_dim,
+                                                        block_size, max_blocks_per_seq, _TORCH_DTYPES[dtype]))
+
+
+def decode_multi(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor, block_tables: torch.Tensor,
+                 context_lens: torch.Tensor, scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                 workspace: Optional[torch.Tensor] = None, max_context_len: int = 0, partition_pages: int = 0,
+                 kernel: str = "auto", stream=None) -> torch.Tensor:
+    """``pa_decode_multi``: ``query`` ``[B, q_len, H_q, d]``; query token t of sequence b sits at position
+    L_b - q_len + t and attends positions up to its own (causal).  Returns ``out`` of the query's shape."""
+    for name, t in (("query", query), ("key_cache", key_cache), ("value_cache", value_cache),
+                    ("block_tables", block_tables), ("context_lens", context_lens)):
+        _cuda(t, name)
+    _need(key_cache.dim() == 4 and value_cache.shape == key_cache.shape, "caches must be [N, H_kv, bs, d]")
+    num_blocks, hkv, bs, d = key_cache.shape
+    _need(query.dim() == 4 and query.shape[3] == d, "query must be [B, q_len, H_q, d]")
+    b, q_len, hq, _ = query.shape
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == b,
+          "block_tables: int32 [B, max_blocks]")
+    _need(context_lens.dtype == torch.int32 and context_lens.numel() == b, "context_lens: int32 [B]")
+    _need(query.dtype == key_cache.dtype == value_cache.dtype, "query and caches must share a dtype")
+    if out is None:
+        out = torch.empty_like(query)
+    _cuda(out, "out")
+    _need(out.shape == query.shape and out.dtype == query.dtype, "out must match query")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    ws_ptr, ws_bytes = 0, 0
+    if workspace is not None:
+        _cuda(workspace, "workspace")
+        ws_ptr, ws_bytes = workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    _check(library().pa_decode_multi(out.data_ptr(), query.data_ptr(), key_cache.data_ptr(), value_cache.data_ptr(),
+                                     block_tables.data_ptr(), context_lens.data_ptr(), b, q_len, hq, hkv, d, bs,
+                                     block_tables.shape[1], num_blocks, float(scale), _dtype_code(query),
+                                     ws_ptr or None, ws_bytes, max_context_len, partition_pages, KERNELS[kernel],
+                                     _stream_ptr(stream, query.device)))
     return out
 
 

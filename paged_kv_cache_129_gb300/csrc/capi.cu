@@ -184,6 +184,7 @@ int encode_cache_map(CUtensorMap* map, const void* base, int dtype, int num_bloc
 
 struct Plan {
     int kind = 0;
+    int dkind = 0;  // the kernel instantiation: kind, or 3 for the tensor-core kernel with causal bounds
     int schedule = kScheduleGrid;
     int gmax = 8;
     int head_chunks = 1;
@@ -211,8 +212,10 @@ void workspace_layout(int num_seqs, int num_heads, int head_dim, int max_parts, 
 }
 
 // has_ws: false means no workspace is usable (single pass forced).
+// q_len > 1: multi-query decode; a kv head then serves q_len * group query rows.
 int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks, int dtype,
-              bool has_ws, size_t ws_avail, int max_context_len, int partition_pages, int kernel, Plan* plan) {
+              bool has_ws, size_t ws_avail, int max_context_len, int partition_pages, int kernel, Plan* plan,
+              int q_len = 1) {
     if (!dtype_ok(dtype)) return fail(PA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
         return fail(PA_ERR_INVALID_ARG, "num_heads=%d must be a positive multiple of num_kv_heads=%d", num_heads,
@@ -222,8 +225,10 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
                     max_blocks);
     if ((long long)max_blocks * block_size >= (1ll << 31))
         return fail(PA_ERR_INVALID_ARG, "max_blocks_per_seq * block_size must be < 2^31");
+    if (q_len < 1 || (long long)q_len * num_heads >= (1 << 24))
+        return fail(PA_ERR_INVALID_ARG, "q_len=%d must be positive (and q_len * num_heads < 2^24)", q_len);
     Plan p;
-    const int group = num_heads / num_kv_heads;
+    const int rows = q_len * (num_heads / num_kv_heads);  // query rows per kv head
     if (kernel == PA_KERNEL_AUTO) {
         p.kind = dtype == PA_F32 ? PA_KERNEL_SIMT : PA_KERNEL_MMA;
     } else if (kernel == PA_KERNEL_MMA || kernel == PA_KERNEL_SIMT) {
@@ -235,13 +240,14 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
         return fail(PA_ERR_UNSUPPORTED, "the tensor-core kernel needs f16 or bf16");
     p.gmax = 8;
     if (p.kind == PA_KERNEL_SIMT) {
-        const int g = group < 8 ? group : 8;
+        const int g = rows < 8 ? rows : 8;
         p.gmax = g <= 1 ? 1 : g <= 2 ? 2 : g <= 4 ? 4 : 8;
     }
-    if (!decode_kernel_info(dtype, head_dim, block_size, p.kind, p.gmax, num_seqs, &p.ki))
+    p.dkind = (p.kind == PA_KERNEL_MMA && q_len > 1) ? 3 : p.kind;
+    if (!decode_kernel_info(dtype, head_dim, block_size, p.dkind, p.gmax, num_seqs, &p.ki))
         return fail(PA_ERR_UNSUPPORTED, "no %s decode kernel for dtype=%d head_dim=%d block_size=%d",
                     p.kind == PA_KERNEL_MMA ? "tensor-core" : "CUDA-core", dtype, head_dim, block_size);
-    p.head_chunks = (group + p.ki.heads_per_cta - 1) / p.ki.heads_per_cta;
+    p.head_chunks = (rows + p.ki.heads_per_cta - 1) / p.ki.heads_per_cta;
     p.units = num_seqs * num_kv_heads * p.head_chunks;
 
     long long max_ctx = (long long)max_blocks * block_size;
@@ -301,7 +307,7 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
     for (;;) {
         p.partition_pages = pp;
         p.max_parts = (nblk_max + pp - 1) / pp;
-        workspace_layout(num_seqs, num_heads, head_dim, p.max_parts, &p);
+        workspace_layout(num_seqs, num_heads * q_len, head_dim, p.max_parts, &p);
         const bool fits = p.max_parts == 1 || (p.ws_bytes <= ws_avail && p.max_parts <= p.ki.merge_parts_cap);
         if (fits) break;
         if (partition_pages > 0)
@@ -434,7 +440,7 @@ int decode_impl(void* out, const void* query, const void* new_key, const void* n
                 const void* value_cache, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
                 int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
                 int num_blocks, float scale, int dtype, void* workspace, size_t workspace_bytes, int max_context_len,
-                int partition_pages, int kernel, void* stream) {
+                int partition_pages, int kernel, void* stream, int q_len = 1) {
     clear_error();
     if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "pa_decode: num_seqs=%d", num_seqs);
     if (new_key && (!new_value || !aligned(new_key, 16) || !aligned(new_value, 16)))
@@ -455,7 +461,7 @@ int decode_impl(void* out, const void* query, const void* new_key, const void* n
     Plan p;
     int st = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, dtype,
                        workspace != nullptr && workspace_bytes > 0, workspace ? workspace_bytes : 0, max_context_len,
-                       partition_pages, kernel, &p);
+                       partition_pages, kernel, &p, q_len);
     if (st != PA_OK) return st;
     DeviceState* dev = nullptr;
     st = current_device_state(&dev);
@@ -490,6 +496,8 @@ int decode_impl(void* out, const void* query, const void* new_key, const void* n
     a.num_heads = num_heads;
     a.num_kv_heads = num_kv_heads;
     a.group = num_heads / num_kv_heads;
+    a.q_len = q_len;
+    a.rows = q_len * a.group;
     a.head_chunks = p.head_chunks;
     a.max_blocks = max_blocks_per_seq;
     a.num_blocks = num_blocks;
@@ -498,12 +506,11 @@ int decode_impl(void* out, const void* query, const void* new_key, const void* n
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);  // log2(e)
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaError_t e =
-        decode_launch(dtype, head_dim, block_size, p.kind, p.gmax, p.schedule, tk, tv, a, (int)p.grid, num_seqs, s);
+        decode_launch(dtype, head_dim, block_size, p.dkind, p.gmax, p.schedule, tk, tv, a, (int)p.grid, num_seqs, s);
     if (e != cudaSuccess) return cuda_fail(e, "pa_decode: decode kernel launch");
     if (grid_split) {
-        MergeArgs m{out,        context_lens, a.ws_m,     a.ws_l,          a.ws_o,
-                    num_seqs,   num_heads,    block_size, max_blocks_per_seq, p.partition_pages,
-                    p.max_parts};
+        MergeArgs m{out, context_lens, a.ws_m, a.ws_l, a.ws_o, num_seqs, num_heads, block_size, max_blocks_per_seq,
+                    p.partition_pages, p.max_parts, num_kv_heads, a.group, q_len, a.rows};
         e = merge_launch(dtype, head_dim, m, s);
         if (e != cudaSuccess) return cuda_fail(e, "pa_decode: merge kernel launch");
     }
@@ -537,6 +544,25 @@ int pa_decode_append(void* out, const void* query, const void* new_key, const vo
     return decode_impl(out, query, new_key, new_value, key_cache, value_cache, block_tables, context_lens, num_seqs,
                        num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype,
                        workspace, workspace_bytes, max_context_len, partition_pages, kernel, stream);
+}
+
+int pa_decode_multi(void* out, const void* query, const void* key_cache, const void* value_cache,
+                    const int32_t* block_tables, const int32_t* context_lens, int num_seqs, int q_len, int num_heads,
+                    int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq, int num_blocks,
+                    float scale, int dtype, void* workspace, size_t workspace_bytes, int max_context_len,
+                    int partition_pages, int kernel, void* stream) {
+    return decode_impl(out, query, nullptr, nullptr, key_cache, value_cache, block_tables, context_lens, num_seqs,
+                       num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype,
+                       workspace, workspace_bytes, max_context_len, partition_pages, kernel, stream, q_len);
+}
+
+size_t pa_decode_multi_workspace_size(int num_seqs, int q_len, int num_heads, int num_kv_heads, int head_dim,
+                                      int block_size, int max_blocks_per_seq, int dtype) {
+    Plan p;
+    if (make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, dtype, true,
+                  (size_t)-1, 0, 0, PA_KERNEL_AUTO, &p, q_len) != PA_OK)
+        return 0;
+    return p.ws_bytes;
 }
 
 int pa_decode(void* out, const void* query, const void* key_cache, const void* value_cache,

@@ -9,22 +9,30 @@ using T = __nv_bfloat16;
 template <typename F>
 bool dispatch(int d, int bs, int kind, int gmax, F&& f) {
     if (kind == 1) {
-        if (d == 64 && bs == 16) return f(DecodeKernel<T, 64, 16, true, 8>{}), true;
-        if (d == 64 && bs == 32) return f(DecodeKernel<T, 64, 32, true, 8>{}), true;
-        if (d == 128 && bs == 16) return f(DecodeKernel<T, 128, 16, true, 8>{}), true;
-        if (d == 128 && bs == 32) return f(DecodeKernel<T, 128, 32, true, 8>{}), true;
-        if (d == 256 && bs == 16) return f(DecodeKernel<T, 256, 16, true, 8>{}), true;
-        if (d == 256 && bs == 32) return f(DecodeKernel<T, 256, 32, true, 8>{}), true;
+        if (d == 64 && bs == 16) return f(DecodeKernel<T, 64, 16, true, 8, false>{}), true;
+        if (d == 64 && bs == 32) return f(DecodeKernel<T, 64, 32, true, 8, false>{}), true;
+        if (d == 128 && bs == 16) return f(DecodeKernel<T, 128, 16, true, 8, false>{}), true;
+        if (d == 128 && bs == 32) return f(DecodeKernel<T, 128, 32, true, 8, false>{}), true;
+        if (d == 256 && bs == 16) return f(DecodeKernel<T, 256, 16, true, 8, false>{}), true;
+        if (d == 256 && bs == 32) return f(DecodeKernel<T, 256, 32, true, 8, false>{}), true;
+    }
+    if (kind == 3) {  // tensor-core kernels with a causal bound per row (multi-query)
+        if (d == 64 && bs == 16) return f(DecodeKernel<T, 64, 16, true, 8, true>{}), true;
+        if (d == 64 && bs == 32) return f(DecodeKernel<T, 64, 32, true, 8, true>{}), true;
+        if (d == 128 && bs == 16) return f(DecodeKernel<T, 128, 16, true, 8, true>{}), true;
+        if (d == 128 && bs == 32) return f(DecodeKernel<T, 128, 32, true, 8, true>{}), true;
+        if (d == 256 && bs == 16) return f(DecodeKernel<T, 256, 16, true, 8, true>{}), true;
+        if (d == 256 && bs == 32) return f(DecodeKernel<T, 256, 32, true, 8, true>{}), true;
     }
     if (kind == 2) {
-        if (d == 128 && bs == 16 && gmax == 1) return f(DecodeKernel<T, 128, 16, false, 1>{}), true;
-        if (d == 128 && bs == 16 && gmax == 2) return f(DecodeKernel<T, 128, 16, false, 2>{}), true;
-        if (d == 128 && bs == 16 && gmax == 4) return f(DecodeKernel<T, 128, 16, false, 4>{}), true;
-        if (d == 128 && bs == 16 && gmax == 8) return f(DecodeKernel<T, 128, 16, false, 8>{}), true;
-        if (d == 128 && bs == 32 && gmax == 1) return f(DecodeKernel<T, 128, 32, false, 1>{}), true;
-        if (d == 128 && bs == 32 && gmax == 2) return f(DecodeKernel<T, 128, 32, false, 2>{}), true;
-        if (d == 128 && bs == 32 && gmax == 4) return f(DecodeKernel<T, 128, 32, false, 4>{}), true;
-        if (d == 128 && bs == 32 && gmax == 8) return f(DecodeKernel<T, 128, 32, false, 8>{}), true;
+        if (d == 128 && bs == 16 && gmax == 1) return f(DecodeKernel<T, 128, 16, false, 1, false>{}), true;
+        if (d == 128 && bs == 16 && gmax == 2) return f(DecodeKernel<T, 128, 16, false, 2, false>{}), true;
+        if (d == 128 && bs == 16 && gmax == 4) return f(DecodeKernel<T, 128, 16, false, 4, false>{}), true;
+        if (d == 128 && bs == 16 && gmax == 8) return f(DecodeKernel<T, 128, 16, false, 8, false>{}), true;
+        if (d == 128 && bs == 32 && gmax == 1) return f(DecodeKernel<T, 128, 32, false, 1, false>{}), true;
+        if (d == 128 && bs == 32 && gmax == 2) return f(DecodeKernel<T, 128, 32, false, 2, false>{}), true;
+        if (d == 128 && bs == 32 && gmax == 4) return f(DecodeKernel<T, 128, 32, false, 4, false>{}), true;
+        if (d == 128 && bs == 32 && gmax == 8) return f(DecodeKernel<T, 128, 32, false, 8, false>{}), true;
     }
     return false;
 }

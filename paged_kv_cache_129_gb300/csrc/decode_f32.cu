@@ -9,22 +9,22 @@ using T = float;
 template <typename F>
 bool dispatch(int d, int bs, int kind, int gmax, F&& f) {
     if (kind == 2) {
-        if (d == 64 && bs == 16 && gmax == 1) return f(DecodeKernel<T, 64, 16, false, 1>{}), true;
-        if (d == 64 && bs == 16 && gmax == 2) return f(DecodeKernel<T, 64, 16, false, 2>{}), true;
-        if (d == 64 && bs == 16 && gmax == 4) return f(DecodeKernel<T, 64, 16, false, 4>{}), true;
-        if (d == 64 && bs == 16 && gmax == 8) return f(DecodeKernel<T, 64, 16, false, 8>{}), true;
-        if (d == 64 && bs == 32 && gmax == 1) return f(DecodeKernel<T, 64, 32, false, 1>{}), true;
-        if (d == 64 && bs == 32 && gmax == 2) return f(DecodeKernel<T, 64, 32, false, 2>{}), true;
-        if (d == 64 && bs == 32 && gmax == 4) return f(DecodeKernel<T, 64, 32, false, 4>{}), true;
-        if (d == 64 && bs == 32 && gmax == 8) return f(DecodeKernel<T, 64, 32, false, 8>{}), true;
-        if (d == 128 && bs == 16 && gmax == 1) return f(DecodeKernel<T, 128, 16, false, 1>{}), true;
-        if (d == 128 && bs == 16 && gmax == 2) return f(DecodeKernel<T, 128, 16, false, 2>{}), true;
-        if (d == 128 && bs == 16 && gmax == 4) return f(DecodeKernel<T, 128, 16, false, 4>{}), true;
-        if (d == 128 && bs == 16 && gmax == 8) return f(DecodeKernel<T, 128, 16, false, 8>{}), true;
-        if (d == 128 && bs == 32 && gmax == 1) return f(DecodeKernel<T, 128, 32, false, 1>{}), true;
-        if (d == 128 && bs == 32 && gmax == 2) return f(DecodeKernel<T, 128, 32, false, 2>{}), true;
-        if (d == 128 && bs == 32 && gmax == 4) return f(DecodeKernel<T, 128, 32, false, 4>{}), true;
-        if (d == 128 && bs == 32 && gmax == 8) return f(DecodeKernel<T, 128, 32, false, 8>{}), true;
+        if (d == 64 && bs == 16 && gmax == 1) return f(DecodeKernel<T, 64, 16, false, 1, false>{}), true;
+        if (d == 64 && bs == 16 && gmax == 2) return f(DecodeKernel<T, 64, 16, false, 2, false>{}), true;
+        if (d == 64 && bs == 16 && gmax == 4) return f(DecodeKernel<T, 64, 16, false, 4, false>{}), true;
+        if (d == 64 && bs == 16 && gmax == 8) return f(DecodeKernel<T, 64, 16, false, 8, false>{}), true;
+        if (d == 64 && bs == 32 && gmax == 1) return f(DecodeKernel<T, 64, 32, false, 1, false>{}), true;
+        if (d == 64 && bs == 32 && gmax == 2) return f(DecodeKernel<T, 64, 32, false, 2, false>{}), true;
+        if (d == 64 && bs == 32 && gmax == 4) return f(DecodeKernel<T, 64, 32, false, 4, false>{}), true;
+        if (d == 64 && bs == 32 && gmax == 8) return f(DecodeKernel<T, 64, 32, false, 8, false>{}), true;
+        if (d == 128 && bs == 16 && gmax == 1) return f(DecodeKernel<T, 128, 16, false, 1, false>{}), true;
+        if (d == 128 && bs == 16 && gmax == 2) return f(DecodeKernel<T, 128, 16, false, 2, false>{}), true;
+        if (d == 128 && bs == 16 && gmax == 4) return f(DecodeKernel<T, 128, 16, false, 4, false>{}), true;
+        if (d == 128 && bs == 16 && gmax == 8) return f(DecodeKernel<T, 128, 16, false, 8, false>{}), true;
+        if (d == 128 && bs == 32 && gmax == 1) return f(DecodeKernel<T, 128, 32, false, 1, false>{}), true;
+        if (d == 128 && bs == 32 && gmax == 2) return f(DecodeKernel<T, 128, 32, false, 2, false>{}), true;
+        if (d == 128 && bs == 32 && gmax == 4) return f(DecodeKernel<T, 128, 32, false, 4, false>{}), true;
+        if (d == 128 && bs == 32 && gmax == 8) return f(DecodeKernel<T, 128, 32, false, 8, false>{}), true;
     }
     return false;
 }

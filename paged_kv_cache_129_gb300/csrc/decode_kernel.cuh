@@ -84,6 +84,12 @@ struct DecodeCfg {
     static constexpr int kStatBytes = kHeads * (2 + kNW) * 4;
     static constexpr int kFlagOffset = a16(kStatOffset + kStatBytes);
     static constexpr int kSmemBytes = kFlagOffset + 16 + 1024;  // + slack to align the base to 1024
+    // Resident CTAs per SM the register allocation must allow (0: no bound).  Registers are
+    // split between the SM's four sub-partitions, so three CTAs of five warps need <= 128 per
+    // thread.  The 16-token page kernels stay under that unbounded (an explicit bound of 1 makes
+    // the compiler take ~137); the 32-token ones (two sub-tiles per page) would take ~135 and
+    // lose a CTA per SM; head_dim 256 needs ~200 (two CTAs per SM).
+    static constexpr int kMinBlocks = (D <= 128 && BS == 32) ? 3 : 0;
 
     static_assert(D % kBoxElems == 0, "head_dim must be a multiple of 128 bytes");
     static_assert(BS <= 256 && BS >= 8, "TMA box height");
@@ -104,6 +110,26 @@ __device__ __forceinline__ uint32_t swz_offset(int row, int elem) {
     const int chunk = byte >> 4;
     return (uint32_t)(box * BS * 128 + row * 128 + (((chunk ^ (row & 7)) << 4) | (byte & 15)));
 }
+
+// ------------------------------------------------------------------------------------------
+// Query and output rows of a unit.  A kv head serves rows = q_len * group query rows; row
+// v = t * group + h is query token t (position L - q_len + t) of head kvh * group + h, and
+// query / out are [B, q_len, H_q, D] (q_len = 1: [B, H_q, D]).  Row r of a unit is row
+// v0 + r of its kv head.
+struct UnitRows {
+    int b, kvh, v0, q_len, group, num_heads;
+    __device__ __forceinline__ size_t row(int r) const {
+        const int v = v0 + r;
+        const int t = v / group;
+        return ((size_t)b * q_len + t) * num_heads + kvh * group + (v - t * group);
+    }
+    // The last position row r attends (causal bound), for a context of L positions.
+    __device__ __forceinline__ int last_pos(int r, int L) const { return L - q_len + (v0 + r) / group; }
+};
+
+// Weight of a state whose running max is m against a common max mm: 0 for an empty state
+// (m = -inf), also when every state is empty (mm = -inf).
+__device__ __forceinline__ float rescale(float m, float mm) { return m == -INFINITY ? 0.f : exp2f(m - mm); }
 
 // ------------------------------------------------------------------------------------------
 // The step's new token in append mode.  Its K and V rows (D elements each) are held by
@@ -177,29 +203,36 @@ __device__ __noinline__ void append_token(const DecodeArgs& a, int b, int kvh, i
 
 // ------------------------------------------------------------------------------------------
 // Tensor-core consumer (f16 / bf16).
-template <typename T, int D, int BS>
+// CAUSAL: rows carry their own causal bound (multi-query decode); without it every row
+// attends the whole context and the bound checks compile away.
+template <typename T, int D, int BS, bool CAUSAL>
 struct MmaConsumer {
     static constexpr int KS = D / 16;  // k-steps of QK^T, m-tiles of PV
-    uint32_t qa[KS][2];                // Q rows 0..7 (heads) of the A fragment; rows 8..15 are zero
-    float o[KS][4];                    // O^T fragments: rows d, columns heads
+    uint32_t qa[KS][2];                // Q rows 0..7 of the A fragment; rows 8..15 are zero
+    float o[KS][4];                    // O^T fragments: rows d, columns query rows
     float m, l;                        // running max (quad-uniform) and this thread's part of l
+    int lim;                           // the last position this thread's row (lane / 4) attends
 
-    __device__ __forceinline__ void init(const T* q_rows, int gc, int lane) {
-        const int g = lane >> 2, t = lane & 3;
-        const uint32_t* row = reinterpret_cast<const uint32_t*>(q_rows + (size_t)g * D);
+    // q_row: this lane's query row (row lane / 4 of the unit), read only when live.
+    __device__ __forceinline__ void init(const T* q_row, bool live, int last_pos, int lane) {
+        const int t = lane & 3;
+        const uint32_t* row = reinterpret_cast<const uint32_t*>(q_row);
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
-            qa[kk][0] = g < gc ? __ldg(row + (kk * 16 + 2 * t) / 2) : 0u;
-            qa[kk][1] = g < gc ? __ldg(row + (kk * 16 + 8 + 2 * t) / 2) : 0u;
+            qa[kk][0] = live ? __ldg(row + (kk * 16 + 2 * t) / 2) : 0u;
+            qa[kk][1] = live ? __ldg(row + (kk * 16 + 8 + 2 * t) / 2) : 0u;
 #pragma unroll
             for (int e = 0; e < 4; ++e) o[kk][e] = 0.f;
         }
         m = -INFINITY;
         l = 0.f;
+        lim = last_pos;
     }
 
-    // One page (BS tokens, nvalid of them inside the context).
-    __device__ __forceinline__ void page(uint8_t* kpage, uint8_t* vpage, int nvalid, float scale_log2, int lane) {
+    // One page (BS tokens from position pos0, nvalid of them inside the context; a row
+    // attends only the tokens up to its own bound).
+    __device__ __forceinline__ void page(uint8_t* kpage, uint8_t* vpage, int nvalid, int pos0, float scale_log2,
+                                         int lane) {
         const int t = lane & 3;
         const int j = lane >> 3, r8 = lane & 7;
         const uint32_t kbase = smem_addr(kpage);
@@ -233,22 +266,27 @@ struct MmaConsumer {
                 Mma<T>::run(s0, qa[kk][0], 0u, qa[kk][1], 0u, bf[0], bf[1]);
                 Mma<T>::run(s1, qa[kk][0], 0u, qa[kk][1], 0u, bf[2], bf[3]);
             }
-            // ---- online softmax for head g over tokens 2t, 2t+1, 8+2t, 9+2t ----
-            float x0 = (2 * t < nv) ? s0[0] * scale_log2 : -INFINITY;
-            float x1 = (2 * t + 1 < nv) ? s0[1] * scale_log2 : -INFINITY;
-            float x2 = (8 + 2 * t < nv) ? s1[0] * scale_log2 : -INFINITY;
-            float x3 = (9 + 2 * t < nv) ? s1[1] * scale_log2 : -INFINITY;
+            // ---- online softmax for row g over tokens 2t, 2t+1, 8+2t, 9+2t ----
+            const int nr = CAUSAL ? min(nv, lim - (pos0 + sub * 16) + 1) : nv;  // tokens row g attends
+            float x0 = (2 * t < nr) ? s0[0] * scale_log2 : -INFINITY;
+            float x1 = (2 * t + 1 < nr) ? s0[1] * scale_log2 : -INFINITY;
+            float x2 = (8 + 2 * t < nr) ? s1[0] * scale_log2 : -INFINITY;
+            float x3 = (9 + 2 * t < nr) ? s1[1] * scale_log2 : -INFINITY;
             float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
             mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float m_new = fmaxf(m, mx);  // finite: token 0 of a sub-tile is always valid
-            const float alpha = exp2f(m - m_new);
+            // -inf only while a row has attended nothing yet (a causal bound before this
+            // sub-tile): then alpha and p are 0, not NaN.  Without causal bounds token 0 of a
+            // sub-tile is always attended and m_new is finite.
+            const float m_new = fmaxf(m, mx);
+            const float m_ref = (CAUSAL && m_new == -INFINITY) ? 0.f : m_new;
+            const float alpha = exp2f(m - m_ref);
             float r0, r1, r2, r3;
-            const uint32_t pb0 = Mma<T>::pack(exp2f(x0 - m_new), exp2f(x1 - m_new), r0, r1);
-            const uint32_t pb1 = Mma<T>::pack(exp2f(x2 - m_new), exp2f(x3 - m_new), r2, r3);
+            const uint32_t pb0 = Mma<T>::pack(exp2f(x0 - m_ref), exp2f(x1 - m_ref), r0, r1);
+            const uint32_t pb1 = Mma<T>::pack(exp2f(x2 - m_ref), exp2f(x3 - m_ref), r2, r3);
             l = l * alpha + ((r0 + r1) + (r2 + r3));
             m = m_new;
-            // O^T columns 2t and 2t+1 are heads 2t, 2t+1: fetch their rescale factors.
+            // O^T columns 2t and 2t+1 are rows 2t, 2t+1: fetch their rescale factors.
             const float a_lo = __shfl_sync(0xffffffffu, alpha, (2 * t) * 4);
             const float a_hi = __shfl_sync(0xffffffffu, alpha, (2 * t + 1) * 4);
             // ---- O^T += V^T P^T ----
@@ -283,13 +321,16 @@ struct MmaConsumer {
         l = 0.f;
     }
 
-    // out_rows[h * D + d] = o~ / l for the gc heads (after finish()).
-    __device__ __forceinline__ void write_out(T* out_rows, int gc, int lane) const {
+    // out[row(r) * D + d] = o~ / l for the gc rows (after finish()); a row that attended
+    // nothing (l = 0) gets zeros.
+    __device__ __forceinline__ void write_out(T* out, const UnitRows& rows, int gc, int lane) const {
         const int g = lane >> 2, t = lane & 3;
-        const float inv_lo = 1.f / __shfl_sync(0xffffffffu, l, (2 * t) * 4);
-        const float inv_hi = 1.f / __shfl_sync(0xffffffffu, l, (2 * t + 1) * 4);
-        T* lo = out_rows + (size_t)(2 * t) * D;
-        T* hi = out_rows + (size_t)(2 * t + 1) * D;
+        const float l_lo = __shfl_sync(0xffffffffu, l, (2 * t) * 4);
+        const float l_hi = __shfl_sync(0xffffffffu, l, (2 * t + 1) * 4);
+        const float inv_lo = l_lo > 0.f ? 1.f / l_lo : 0.f;
+        const float inv_hi = l_hi > 0.f ? 1.f / l_hi : 0.f;
+        T* lo = out + rows.row(min(2 * t, gc - 1)) * D;
+        T* hi = out + rows.row(min(2 * t + 1, gc - 1)) * D;
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
             if (2 * t < gc) {
@@ -358,8 +399,12 @@ struct SimtConsumer {
     static_assert(VBYTES == 4 || VBYTES == 8 || VBYTES == 16, "PV load width");
     float o[GMAX][DPL];
     float m[GMAX], l[GMAX];
+    int lim0, v0, group;  // row h attends positions up to lim0 + (v0 + h) / group
 
-    __device__ __forceinline__ void init() {
+    __device__ __forceinline__ void init(int lim_base = 0x7fffffff, int first_row = 0, int rows_per_token = 1) {
+        lim0 = lim_base;
+        v0 = first_row;
+        group = rows_per_token;
 #pragma unroll
         for (int h = 0; h < GMAX; ++h) {
             m[h] = -INFINITY;
@@ -385,8 +430,8 @@ struct SimtConsumer {
         }
     }
 
-    __device__ __forceinline__ void page(const uint8_t* kpage, const uint8_t* vpage, int nvalid, float scale_log2,
-                                         const float* q_s, float* p_s, int lane) {
+    __device__ __forceinline__ void page(const uint8_t* kpage, const uint8_t* vpage, int nvalid, int pos0,
+                                         float scale_log2, const float* q_s, float* p_s, int lane) {
         const int tok = lane % BS;
         const int part = lane / BS;
         float acc[GMAX];
@@ -417,13 +462,16 @@ struct SimtConsumer {
             for (int h = 0; h < GMAX; ++h) acc[h] += __shfl_xor_sync(0xffffffffu, acc[h], off);
 #pragma unroll
         for (int h = 0; h < GMAX; ++h) {
-            const float x = tok < nvalid ? acc[h] * scale_log2 : -INFINITY;
+            const int nr = min(nvalid, lim0 == 0x7fffffff ? nvalid : lim0 + (v0 + h) / group - pos0 + 1);
+            const float x = tok < nr ? acc[h] * scale_log2 : -INFINITY;
             float mx = x;
 #pragma unroll
             for (int off = 1; off < BS; off <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-            const float m_new = fmaxf(m[h], mx);  // finite: token 0 of a page is always valid
-            const float alpha = exp2f(m[h] - m_new);
-            const float p = exp2f(x - m_new);
+            // -inf only while the row has attended nothing yet: then alpha and p are 0, not NaN
+            const float m_new = fmaxf(m[h], mx);
+            const float m_ref = m_new == -INFINITY ? 0.f : m_new;
+            const float alpha = exp2f(m[h] - m_ref);
+            const float p = exp2f(x - m_ref);
             l[h] = l[h] * alpha + (part == 0 ? p : 0.f);
             m[h] = m_new;
 #pragma unroll
@@ -451,15 +499,17 @@ struct SimtConsumer {
             for (int off = 1; off < 32; off <<= 1) l[h] += __shfl_xor_sync(0xffffffffu, l[h], off);
     }
 
-    __device__ __forceinline__ void clear() { init(); }
+    __device__ __forceinline__ void clear() { init(lim0, v0, group); }
 
-    __device__ __forceinline__ void write_out(T* out_rows, int gc, int lane) const {
+    // out[row(h) * D + d] = o~ / l for the gc rows; a row that attended nothing gets zeros.
+    __device__ __forceinline__ void write_out(T* out, const UnitRows& rows, int gc, int lane) const {
 #pragma unroll
         for (int h = 0; h < GMAX; ++h) {
             if (h >= gc) break;
-            const float inv = 1.f / l[h];
+            const float inv = l[h] > 0.f ? 1.f / l[h] : 0.f;
+            T* dst = out + rows.row(h) * D;
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) out_rows[(size_t)h * D + lane * DPL + e] = from_float<T>(o[h][e] * inv);
+            for (int e = 0; e < DPL; ++e) dst[lane * DPL + e] = from_float<T>(o[h][e] * inv);
         }
     }
 
@@ -497,8 +547,8 @@ struct SimtConsumer {
 };
 
 // ------------------------------------------------------------------------------------------
-template <typename T, int D, int BS, bool MMA, int GMAX>
-__global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
+template <typename T, int D, int BS, bool MMA, int GMAX, bool CAUSAL>
+__global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (DecodeCfg<T, D, BS, MMA, GMAX>::kMinBlocks))
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                         const DecodeArgs a) {
     using C = DecodeCfg<T, D, BS, MMA, GMAX>;
@@ -529,8 +579,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
     const int bk = unit / a.head_chunks;
     const int kvh = bk % a.num_kv_heads;
     const int b = bk / a.num_kv_heads;
-    const int head0 = kvh * a.group + hc * C::kHeads;
-    const int gc = min(C::kHeads, a.group - hc * C::kHeads);
+    // the unit's query/output rows (built where used, so that no copy lives across the page loop)
+#define PA_UNIT_ROWS UnitRows{b, kvh, hc * C::kHeads, a.q_len, a.group, a.num_heads}
+    const int gc = min(C::kHeads, a.rows - hc * C::kHeads);
 
     int L = __ldg(a.context_lens + b);
     const int l_cap = min(a.max_blocks, a.max_parts * a.partition_pages) * BS;
@@ -542,10 +593,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
     const int nparts = (nblk + a.partition_pages - 1) / a.partition_pages;
     T* out = static_cast<T*>(a.out);
 
-    if (L == 0) {  // empty context: a zero row (partition 0 writes it)
+    if (L == 0) {  // empty context: zero rows (partition 0 writes them)
         if (p == 0)
             for (int idx = tid; idx < gc * D; idx += C::kThreads)
-                out[((size_t)b * a.num_heads + head0 + idx / D) * D + idx % D] = from_float<T>(0.f);
+                out[PA_UNIT_ROWS.row(idx / D) * D + idx % D] = from_float<T>(0.f);
         return;
     }
     const int first = p * a.partition_pages;
@@ -613,15 +664,19 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
         }
     } else {
         // ================= consumer warps =================
-        const T* qrows = static_cast<const T*>(a.q) + ((size_t)b * a.num_heads + head0) * D;
+        const T* q = static_cast<const T*>(a.q);
         // Append mode: the warp that consumes the page holding position L - 1 takes the
         // new token into its staged copy of the page, and (head chunk 0) into the cache.
         // The token is fetched when that page comes up (holding it in registers across the
         // page loop would cost this kernel its occupancy).
         const int i_tok = a.new_key != nullptr ? nblk - 1 - first : -1;  // that page's index here
         if constexpr (MMA) {
-            MmaConsumer<T, D, BS> cons;
-            cons.init(qrows, gc, lane);
+            MmaConsumer<T, D, BS, CAUSAL> cons;
+            {
+                const UnitRows rows = PA_UNIT_ROWS;
+                const int r = min(lane >> 2, gc - 1);
+                cons.init(q + rows.row(r) * D, (lane >> 2) < gc, rows.last_pos(lane >> 2, L), lane);
+            }
             for (int i = warp; i < npages; i += C::kNW) {
                 const int s = i % C::kNSlot;
                 const bool got = mbar_wait_bounded(&full[s], (i / C::kNSlot) & 1, a.err, flags);
@@ -629,7 +684,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
                 const int nvalid = min(BS, L - (first + i) * BS);
                 uint8_t* kp = ring + s * C::kSlotBytes;
                 if (i == i_tok) append_token<T, D, BS>(a, b, kvh, hc, nblk - 1, kp, kp + C::kPageBytes, nvalid, lane);
-                cons.page(kp, kp + C::kPageBytes, nvalid, a.scale_log2, lane);
+                cons.page(kp, kp + C::kPageBytes, nvalid, (first + i) * BS, a.scale_log2, lane);
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
@@ -647,11 +702,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
             float* p_s = reinterpret_cast<float*>(smem + C::kPsOffset) + warp * GMAX * BS;
             for (int idx = tid; idx < GMAX * D; idx += C::kNW * 32) {
                 const int h = idx / D;
-                q_s[idx] = h < gc ? to_float(qrows[idx]) : 0.f;
+                q_s[idx] = h < gc ? to_float(q[PA_UNIT_ROWS.row(h) * D + idx % D]) : 0.f;
             }
             asm volatile("bar.sync 1, %0;" ::"r"(C::kNW * 32) : "memory");
             SimtConsumer<T, D, BS, GMAX> cons;
-            cons.init();
+            cons.init(L - a.q_len, hc * C::kHeads, a.group);
             for (int i = warp; i < npages; i += C::kNW) {
                 const int s = i % C::kNSlot;
                 const bool got = mbar_wait_bounded(&full[s], (i / C::kNSlot) & 1, a.err, flags);
@@ -659,7 +714,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
                 const int nvalid = min(BS, L - (first + i) * BS);
                 uint8_t* kp = ring + s * C::kSlotBytes;
                 if (i == i_tok) append_token<T, D, BS>(a, b, kvh, hc, nblk - 1, kp, kp + C::kPageBytes, nvalid, lane);
-                cons.page(kp, kp + C::kPageBytes, nvalid, a.scale_log2, q_s, p_s, lane);
+                cons.page(kp, kp + C::kPageBytes, nvalid, (first + i) * BS, a.scale_log2, q_s, p_s, lane);
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
             asm volatile("bar.sync 1, %0;" ::"r"(C::kNW * 32) : "memory");
@@ -700,7 +755,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
         float ws = 0.f;
 #pragma unroll
         for (int w = 0; w < C::kNW; ++w) {
-            const float f = exp2f(cm[w * C::kHeads + tid] - mm);  // 0 for a warp that saw no page
+            // 0 for a warp that saw no page, or a row whose bound lies before it
+            const float f = rescale(cm[w * C::kHeads + tid], mm);
             wgt[w * C::kHeads + tid] = f;
             ws += f * cl[w * C::kHeads + tid];
         }
@@ -709,23 +765,25 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads)
     }
     __syncthreads();
     const bool single = nparts == 1;
+    // split-KV partials are indexed by the kv head's row: (b * H_kv + kvh) * rows + v
+    const UnitRows rows = PA_UNIT_ROWS;
+#undef PA_UNIT_ROWS
+    const size_t row0 = ((size_t)b * a.num_kv_heads + kvh) * a.rows + rows.v0;
     for (int idx = tid; idx < gc * D; idx += C::kThreads) {
         const int h = idx / D;
         const int d = idx - h * D;
         float acc = 0.f;
 #pragma unroll
         for (int w = 0; w < C::kNW; ++w) acc += wgt[w * C::kHeads + h] * co[(w * C::kHeads + h) * C::kOStride + d];
-        const size_t row = (size_t)b * a.num_heads + head0 + h;
         if (single) {
-            out[row * D + d] = from_float<T>(acc / stat_w[h]);
+            out[rows.row(h) * D + d] = from_float<T>(stat_w[h] > 0.f ? acc / stat_w[h] : 0.f);
         } else {
-            a.ws_o[(row * a.max_parts + p) * D + d] = acc;
+            a.ws_o[((row0 + h) * a.max_parts + p) * D + d] = acc;
         }
     }
     if (!single && tid < gc) {
-        const size_t row = (size_t)b * a.num_heads + head0 + tid;
-        a.ws_m[row * a.max_parts + p] = stat_m[tid];
-        a.ws_l[row * a.max_parts + p] = stat_w[tid];
+        a.ws_m[(row0 + tid) * a.max_parts + p] = stat_m[tid];
+        a.ws_l[(row0 + tid) * a.max_parts + p] = stat_w[tid];
     }
 }
 
@@ -743,8 +801,8 @@ __global__ void __launch_bounds__(kMergeThreads) splitkv_merge_kernel(const Merg
     __shared__ float wts[kMergeMaxParts];
     __shared__ float red[kWarps];
     __shared__ float part_o[kWarps][D];
-    const int row = blockIdx.x;
-    const int b = row / a.num_heads;
+    const int row = blockIdx.x;  // (b * H_kv + kvh) * rows + v
+    const int b = row / (a.num_kv_heads * a.rows);
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
     // Wait for the decode kernel's partials (programmatic dependent launch); then the
@@ -772,10 +830,11 @@ __global__ void __launch_bounds__(kMergeThreads) splitkv_merge_kernel(const Merg
 #pragma unroll
     for (int w = 1; w < kWarps; ++w) mm = fmaxf(mm, red[w]);
     __syncthreads();
-    // 2) weights and the merged denominator
+    // 2) weights and the merged denominator (a partition a row's causal bound excludes,
+    //    or a row with no position at all, weighs 0)
     float ws = 0.f;
     for (int pp = tid; pp < n; pp += kMergeThreads) {
-        const float f = exp2f(__ldcg(mrow + pp) - mm);
+        const float f = rescale(__ldcg(mrow + pp), mm);
         wts[pp] = f;
         ws += f * __ldcg(lrow + pp);
     }
@@ -812,8 +871,11 @@ __global__ void __launch_bounds__(kMergeThreads) splitkv_merge_kernel(const Merg
 #pragma unroll
     for (int e = 0; e < DPL; ++e) part_o[warp][lane * DPL + e] = acc[e];
     __syncthreads();
-    T* out = static_cast<T*>(a.out) + (size_t)row * D;
-    const float inv = 1.f / ws;
+    const int rest = row - b * a.num_kv_heads * a.rows;
+    const int kvh = rest / a.rows;
+    const UnitRows rows{b, kvh, rest - kvh * a.rows, a.q_len, a.group, a.num_heads};
+    T* out = static_cast<T*>(a.out) + rows.row(0) * D;
+    const float inv = ws > 0.f ? 1.f / ws : 0.f;
     for (int d = tid; d < D; d += kMergeThreads) {
         float s = 0.f;
 #pragma unroll
@@ -929,7 +991,7 @@ __device__ __forceinline__ void lean_locate(const int* pre, int num_seqs, int up
 }
 
 
-template <typename T, int D, int BS, bool MMA, int GMAX>
+template <typename T, int D, int BS, bool MMA, int GMAX, bool CAUSAL>
 __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (LeanCfg<T, D, BS, MMA, GMAX>::kMinBlocks))
     paged_decode_lean_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                              const DecodeArgs a) {
@@ -998,8 +1060,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Lea
     // Empty contexts produce zero rows (spread over the CTAs).
     for (int b = warp; b < B; b += C::kNW + 1)
         if (pre[b] == pre[b + 1] && (b % (int)gridDim.x) == (int)blockIdx.x)
-            for (int idx = lane; idx < a.num_heads * D; idx += 32)
-                out[(size_t)b * a.num_heads * D + idx] = from_float<T>(0.f);
+            for (int idx = lane; idx < a.q_len * a.num_heads * D; idx += 32)
+                out[(size_t)b * a.q_len * a.num_heads * D + idx] = from_float<T>(0.f);
     if (total == 0) return;
 
     int* row_queue = reinterpret_cast<int*>(smem + C::kRowsOffset);        // [kNW][kRowQueue]
@@ -1079,12 +1141,13 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Lea
         const int hi = min(total, lo + q_per_warp);
         const int n = hi - lo;
         int unit_first = 0, unit_last = -1;
-        int b = 0, uu = 0, nb = 0, L = 0, head0 = 0, gc = 0, kvh = 0;
+        int b = 0, uu = 0, nb = 0, L = 0, gc = 0, kvh = 0;
+        UnitRows rows{0, 0, 0, a.q_len, a.group, a.num_heads};
         int wrote = 0;  // bit s: a partial record was written to slot s
         const bool append = a.new_key != nullptr;
         NewToken<T, D, BS> tok;
         bool tok_ready = false, tok_writer = false;
-        std::conditional_t<MMA, MmaConsumer<T, D, BS>, SimtConsumer<T, D, BS, GMAX>> cons;
+        std::conditional_t<MMA, MmaConsumer<T, D, BS, CAUSAL>, SimtConsumer<T, D, BS, GMAX>> cons;
         float* q_s = reinterpret_cast<float*>(smem + C::kQsOffset) + warp * GMAX * D;
         float* p_s = reinterpret_cast<float*>(smem + C::kPsOffset) + warp * GMAX * BS;
         // Page rows for the producer, published in chunks of 32: chunk c + 1 when this warp
@@ -1143,19 +1206,20 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Lea
                 kvh = uu / a.head_chunks;
                 const int hc = uu - kvh * a.head_chunks;
                 tok_writer = hc == 0;
-                head0 = kvh * a.group + hc * C::kHeads;
-                gc = min(C::kHeads, a.group - hc * C::kHeads);
+                rows = UnitRows{b, kvh, hc * C::kHeads, a.q_len, a.group, a.num_heads};
+                gc = min(C::kHeads, a.rows - hc * C::kHeads);
                 L = __ldg(a.context_lens + b);
                 L = L < 0 ? 0 : (L > l_cap ? l_cap : L);
-                const T* qrows = static_cast<const T*>(a.q) + ((size_t)b * a.num_heads + head0) * D;
+                const T* q = static_cast<const T*>(a.q);
                 if constexpr (MMA) {
-                    cons.init(qrows, gc, lane);
+                    const int r = min(lane >> 2, gc - 1);
+                    cons.init(q + rows.row(r) * D, (lane >> 2) < gc, rows.last_pos(lane >> 2, L), lane);
                 } else {
                     __syncwarp();
                     for (int idx = lane; idx < GMAX * D; idx += 32)
-                        q_s[idx] = idx / D < gc ? to_float(qrows[idx]) : 0.f;
+                        q_s[idx] = idx / D < gc ? to_float(q[rows.row(idx / D) * D + idx % D]) : 0.f;
                     __syncwarp();
-                    cons.init();
+                    cons.init(L - a.q_len, rows.v0, a.group);
                 }
             }
             const int j = g - unit_first;
@@ -1178,18 +1242,17 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Lea
                 tok_ready = false;
             }
             if constexpr (MMA) {
-                cons.page(kp, kp + C::kPageBytes, nvalid, a.scale_log2, lane);
+                cons.page(kp, kp + C::kPageBytes, nvalid, j * BS, a.scale_log2, lane);
                 __syncwarp();
             } else {
-                cons.page(kp, kp + C::kPageBytes, nvalid, a.scale_log2, q_s, p_s, lane);
+                cons.page(kp, kp + C::kPageBytes, nvalid, j * BS, a.scale_log2, q_s, p_s, lane);
             }
             if (lane == 0) mbar_arrive(&empty[s]);
 
             if (g == unit_last || off == n - 1) {  // this warp is done with the unit
                 cons.finish();
-                T* out_rows = out + ((size_t)b * a.num_heads + head0) * D;
                 if (unit_first >= lo && unit_last < hi) {
-                    cons.write_out(out_rows, gc, lane);
+                    cons.write_out(out, rows, gc, lane);
                     cons.clear();
                 } else {
                     const int slot = unit_first <= lo ? 0 : 1;  // 0: the warp's first unit, 1: its last
@@ -1318,8 +1381,8 @@ __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_me
         return;
     }
     const int kvh = uu / a.head_chunks, hc = uu - kvh * a.head_chunks;
-    const int head0 = kvh * a.group + hc * H;
-    const int gc = min(H, a.group - hc * H);
+    const UnitRows rows{b, kvh, hc * H, a.q_len, a.group, a.num_heads};
+    const int gc = min(H, a.rows - hc * H);
     const float* base = a.ws_part + (size_t)w_lo * 2 * kRec;
 
     // thread = (float4 column of the gc live heads, slice of the records): each thread folds
@@ -1350,6 +1413,7 @@ __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_me
 #pragma unroll
             for (int k = 0; k < kLeanMergeBatch; ++k) {
                 if (p0 + k * slices < n) {
+                    if (mv[k] == -INFINITY) continue;  // a piece the row's causal bound excludes
                     const float m_new = fmaxf(mm, mv[k]);
                     const float keep = exp2f(mm - m_new);  // 0 on the first record
                     const float f = exp2f(mv[k] - m_new);
@@ -1377,7 +1441,7 @@ __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_me
                 const float m2 = red[0][t];
                 const float m_new = fmaxf(mm, m2);
                 if (m_new == -INFINITY) continue;  // both slices empty
-                const float k1 = exp2f(mm - m_new), k2 = exp2f(m2 - m_new);
+                const float k1 = rescale(mm, m_new), k2 = rescale(m2, m_new);
                 ww = ww * k1 + red[1][t] * k2;
                 acc.x = acc.x * k1 + red[2][t] * k2;
                 acc.y = acc.y * k1 + red[3][t] * k2;
@@ -1388,8 +1452,8 @@ __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_me
         }
     }
     if (slice == 0) {
-        const float inv = 1.f / ww;
-        T* out = static_cast<T*>(a.out) + ((size_t)b * a.num_heads + head0) * D + col * 4;
+        const float inv = ww > 0.f ? 1.f / ww : 0.f;  // 0: the row attends no position
+        T* out = static_cast<T*>(a.out) + rows.row(h) * D + (col - h * (D / 4)) * 4;
         out[0] = from_float<T>(acc.x * inv);
         out[1] = from_float<T>(acc.y * inv);
         out[2] = from_float<T>(acc.z * inv);
@@ -1401,7 +1465,7 @@ __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_me
 
 // ------------------------------------------------------------------------------------------
 // Host-side helpers for the per-dtype translation units.
-template <typename T, int D, int BS, bool MMA, int GMAX>
+template <typename T, int D, int BS, bool MMA, int GMAX, bool CAUSAL>
 struct DecodeKernel {
     using C = DecodeCfg<T, D, BS, MMA, GMAX>;
     using LC = LeanCfg<T, D, BS, MMA, GMAX>;
@@ -1410,10 +1474,10 @@ struct DecodeKernel {
         static unsigned long long done_mask = 0;  // one bit per device (< 64)
         const unsigned long long bit = 1ull << (device & 63);
         if (done_mask & bit) return true;
-        if (cudaFuncSetAttribute(paged_decode_kernel<T, D, BS, MMA, GMAX>,
+        if (cudaFuncSetAttribute(paged_decode_kernel<T, D, BS, MMA, GMAX, CAUSAL>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmemBytes) != cudaSuccess)
             return false;
-        if (cudaFuncSetAttribute(paged_decode_lean_kernel<T, D, BS, MMA, GMAX>,
+        if (cudaFuncSetAttribute(paged_decode_lean_kernel<T, D, BS, MMA, GMAX, CAUSAL>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, LC::kMaxSmemBytes) != cudaSuccess)
             return false;
         done_mask |= bit;
@@ -1427,7 +1491,7 @@ struct DecodeKernel {
         std::atomic<int>& slot = cache[device & 63][kb < 232 ? kb : 231];
         int n = slot.load(std::memory_order_relaxed);
         if (n > 0) return n;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_lean_kernel<T, D, BS, MMA, GMAX>,
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_lean_kernel<T, D, BS, MMA, GMAX, CAUSAL>,
                                                           LC::kThreads, kb * 1024) != cudaSuccess ||
             n <= 0)
             n = 1;
@@ -1448,7 +1512,7 @@ struct DecodeKernel {
         static std::atomic<int> grid_occ[64];
         int n = grid_occ[device & 63].load(std::memory_order_relaxed);
         if (n <= 0) {
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_kernel<T, D, BS, MMA, GMAX>,
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_kernel<T, D, BS, MMA, GMAX, CAUSAL>,
                                                               C::kThreads, C::kSmemBytes) != cudaSuccess ||
                 n <= 0)
                 n = 1;
@@ -1471,7 +1535,7 @@ struct DecodeKernel {
         if (e != cudaSuccess) return e;
         if (!configure(device)) return cudaGetLastError();
         if (schedule == kScheduleLean) {
-            e = launch_pdl(paged_decode_lean_kernel<T, D, BS, MMA, GMAX>, dim3(grid), dim3(LC::kThreads),
+            e = launch_pdl(paged_decode_lean_kernel<T, D, BS, MMA, GMAX, CAUSAL>, dim3(grid), dim3(LC::kThreads),
                            LC::smem_bytes(num_seqs), stream, k, v, a);
             if (e != cudaSuccess) return e;
             DecodeArgs m = a;
@@ -1481,7 +1545,7 @@ struct DecodeKernel {
                               dim3(a.num_seqs * a.num_kv_heads * a.head_chunks), dim3(kLeanMergeThreads), 0, stream,
                               m);
         } else {
-            return launch_pdl(paged_decode_kernel<T, D, BS, MMA, GMAX>, dim3(grid), dim3(C::kThreads), C::kSmemBytes,
+            return launch_pdl(paged_decode_kernel<T, D, BS, MMA, GMAX, CAUSAL>, dim3(grid), dim3(C::kThreads), C::kSmemBytes,
                               stream, k, v, a);
         }
     }
@@ -1489,7 +1553,8 @@ struct DecodeKernel {
 
 template <typename T, int D>
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
-    return launch_pdl(splitkv_merge_kernel<T, D>, dim3(a.num_seqs * a.num_heads), dim3(kMergeThreads), 0, stream, a);
+    return launch_pdl(splitkv_merge_kernel<T, D>, dim3(a.num_seqs * a.num_heads * a.q_len), dim3(kMergeThreads), 0,
+                      stream, a);
 }
 
 }  // namespace pa

@@ -28,6 +28,10 @@ struct DecodeArgs {
     void* key_cache;
     void* value_cache;
     int num_seqs, num_heads, num_kv_heads, group, head_chunks;
+    // Multi-query decode: q_len query tokens per sequence at positions L - q_len .. L - 1
+    // (q_len = 1: single-step decode).  A kv head serves rows = q_len * group query rows,
+    // row v = t * group + h being query token t of head kvh * group + h.
+    int q_len, rows;
     int max_blocks, num_blocks;
     int partition_pages, max_parts;
     float scale_log2;            // softmax scale * log2(e)
@@ -43,6 +47,7 @@ struct MergeArgs {
     const float* ws_l;
     const float* ws_o;
     int num_seqs, num_heads, block_size, max_blocks, partition_pages, max_parts;
+    int num_kv_heads, group, q_len, rows;  // row id = (b * num_kv_heads + kvh) * rows + v
 };
 
 struct KernelInfo {
@@ -60,7 +65,9 @@ struct KernelInfo {
 
 enum Schedule { kScheduleGrid = 0, kScheduleLean = 1 };
 
-// kind: 1 = tensor-core (mma) kernel, 2 = CUDA-core kernel; gmax: head-chunk width of the CUDA-core kernel.
+// kind: 1 = tensor-core (mma) kernel, 2 = CUDA-core kernel, 3 = tensor-core kernel with a causal bound
+// per row (multi-query decode; the CUDA-core kernel always has it); gmax: head-chunk width of the
+// CUDA-core kernel.
 // Return false when the combination is not compiled.
 bool decode_kernel_info(int dtype, int head_dim, int block_size, int kind, int gmax, int num_seqs, KernelInfo* info);
 cudaError_t decode_launch(int dtype, int head_dim, int block_size, int kind, int gmax, int schedule,

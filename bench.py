@@ -54,6 +54,10 @@ WORKLOAD_DESCRIPTIONS = {
                       "context_lens lognormal(median 256, sigma 1) clipped to [16,2048]",
     "mha_short_bs32": "many short requests, MHA: batch 256, 32/32 heads, head_dim 128, fp16, block_size 32, "
                       "context_lens lognormal(median 256, sigma 1) clipped to [16,2048]",
+    "qwen_gqa_verify4": "speculative verify on the Qwen-style GQA layer: batch 64, 28 q / 4 kv heads, head_dim 128, "
+                        "bf16, block_size 16, context_lens uniform in [512,4096] (including the 4 new tokens), pool "
+                        "20000 blocks shuffled; 4 new tokens per sequence written via slot_mapping, then every one "
+                        "attends its prefix causally (pa_decode_multi, q_len 4)",
     "prefix_cow": "prefix sharing: 64 sequences (one parent + 63 forks through the block pool) share a "
                   "2048-token prefix (full shared tail: no copy-on-write), private tails uniform in [1,256], "
                   "28 q / 4 kv heads, head_dim 128, bf16, block_size 16; value = effective GB/s (every "
@@ -71,11 +75,12 @@ def rank_seed(base_seed: int, rank: int) -> int:
 
 
 def decode_bytes(context_lens, num_heads: int, num_kv_heads: int, head_dim: int, elem_bytes: int,
-                 block_size: int) -> int:
-    """Algorithmic bytes of one decode call: K+V of the valid tokens, q, out, table entries, lengths."""
+                 block_size: int, q_len: int = 1) -> int:
+    """Algorithmic bytes of one decode call: K+V of the valid tokens, q, out, table entries, lengths
+    (q_len query tokens per sequence: the context is read once for all of them)."""
     lens = np.asarray(context_lens, dtype=np.int64)
     kv = 2 * int(lens.sum()) * num_kv_heads * head_dim * elem_bytes
-    qo = 2 * len(lens) * num_heads * head_dim * elem_bytes
+    qo = 2 * len(lens) * q_len * num_heads * head_dim * elem_bytes
     tables = 4 * int(((lens + block_size - 1) // block_size).sum())
     return kv + qo + tables + 4 * len(lens)
 
@@ -271,12 +276,18 @@ def time_oracle_parallel(inp, budget_s: float, threads: int):
 
     eb = inp.elem_bytes
 
+    q_len = inp.q.shape[1] if inp.q.ndim == 4 else 1
+
     def seq_bytes(b):
         return decode_bytes([int(inp.context_lens[b])], inp.num_heads, inp.num_kv_heads, inp.head_dim, eb,
-                            inp.block_size)
+                            inp.block_size, q_len)
 
     def run(b):
-        oracle.decode_inputs(inp, rows=[(b, h) for h in range(inp.num_heads)])
+        if q_len == 1:
+            oracle.decode_inputs(inp, rows=[(b, h) for h in range(inp.num_heads)])
+        else:
+            oracle.decode_multi(inp.q, inp.key_cache, inp.value_cache, inp.block_tables, inp.context_lens, inp.dtype,
+                                inp.scale, rows=[(b, t, h) for t in range(q_len) for h in range(inp.num_heads)])
 
     t0 = time.perf_counter()
     run(0)
@@ -324,7 +335,8 @@ def time_oracle(inp, budget_s: float, rows_cap: int = 0):
 def build_batch(workload: str, seed: int):
     from paged_kv_cache_129_gb300 import workloads as wl
 
-    gen = {"qwen_gqa": lambda s: wl.qwen_gqa(s), "long_context": lambda s: wl.long_context(s),
+    gen = {"qwen_gqa": lambda s: wl.qwen_gqa(s), "qwen_gqa_verify4": lambda s: wl.qwen_gqa_verify(s, q_len=4),
+           "long_context": lambda s: wl.long_context(s),
            "mha_short_bs16": lambda s: wl.mha_short(16, s), "mha_short_bs32": lambda s: wl.mha_short(32, s)}[workload]
     return gen(seed)
 
@@ -394,12 +406,17 @@ def pool_tables(inp):
     rng = np.random.default_rng(12345)
     pool = pa.BlockPool(inp.num_blocks, inp.block_size, free_order=rng.permutation(inp.num_blocks))
     ids = [pool.create() for _ in range(inp.num_seqs)]
+    q_len = inp.q.shape[1] if inp.q.ndim == 4 else 1
     for sid, L in zip(ids, inp.context_lens):
-        for _ in range(int(L) - 1):
+        for _ in range(int(L) - q_len):
             pool.append(sid)
     if inp.new_key is not None:
-        slots, pairs = pool.append_batch(ids)
-        assert len(pairs) == 0
+        rounds = []
+        for _ in range(q_len):  # the step's new tokens, one batch append per token
+            slots, pairs = pool.append_batch(ids)
+            assert len(pairs) == 0
+            rounds.append(np.asarray(slots, dtype=np.int64))
+        slots = rounds[0] if q_len == 1 else np.stack(rounds, axis=1).reshape(-1)  # [B, q_len] order
     else:
         for sid in ids:
             pool.append(sid)
@@ -439,7 +456,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
 
     eb = inp.elem_bytes
     B, Hq, Hkv, d, bs = inp.num_seqs, inp.num_heads, inp.num_kv_heads, inp.head_dim, inp.block_size
-    dec_bytes = decode_bytes(lens, Hq, Hkv, d, eb, bs)
+    q_len = inp.q.shape[1] if inp.q.ndim == 4 else 1  # query tokens per sequence (verify step: > 1)
+    dec_bytes = decode_bytes(lens, Hq, Hkv, d, eb, bs, q_len)
     ntok = 0 if slots is None else len(slots)
     wr_bytes = write_bytes(ntok, Hkv, d, eb)
     step_bytes = dec_bytes + wr_bytes
@@ -469,7 +487,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         sl = torch.from_numpy(slots).to(device)
     max_ctx = int(lens.max())
     plan = pa.decode_plan(B, Hq, Hkv, d, bs, tables.shape[1], tdtype, max_context_len=max_ctx,
-                          partition_pages=args.partition_pages, kernel=args.kernel)
+                          partition_pages=args.partition_pages, kernel=args.kernel, q_len=q_len)
     ws = torch.zeros(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
     lib = pa.library()
     stream = torch.cuda.current_stream(device)
@@ -477,7 +495,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     code = {"f32": 0, "f16": 1, "bf16": 2}[inp.dtype]
     kern = pa.KERNELS[args.kernel]
 
-    fused = has_write and args.step == "append"
+    fused = has_write and args.step == "append" and q_len == 1
     if fused:
         # pa_decode_append writes at the slot of position L - 1: the pool handed out exactly those
         live = lens >= 1
@@ -486,8 +504,10 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
 
     # Pre-marshalled C-ABI argument lists (the timed loop only calls the library).
     dec_args = [[out.data_ptr(), q.data_ptr(), kcs[r].data_ptr(), vcs[r].data_ptr(), bt.data_ptr(), dl.data_ptr(),
-                 B, Hq, Hkv, d, bs, tables.shape[1], inp.num_blocks, float(inp.scale), code, ws.data_ptr(),
-                 ws.numel(), max_ctx, args.partition_pages, kern, sptr] for r in range(replicas)]
+                 B] + ([q_len] if q_len > 1 else []) + [Hq, Hkv, d, bs, tables.shape[1], inp.num_blocks,
+                 float(inp.scale), code, ws.data_ptr(), ws.numel(), max_ctx, args.partition_pages, kern, sptr]
+                for r in range(replicas)]
+    decode_fn = lib.pa_decode_multi if q_len > 1 else lib.pa_decode_ex
     wr_args = ([[nk.data_ptr(), nv.data_ptr(), kcs[r].data_ptr(), vcs[r].data_ptr(), sl.data_ptr(), ntok, Hkv, d, bs,
                  inp.num_blocks, code, sptr] for r in range(replicas)] if has_write else None)
     app_args = ([[out.data_ptr(), q.data_ptr(), nk.data_ptr(), nv.data_ptr(), kcs[r].data_ptr(), vcs[r].data_ptr(),
@@ -507,12 +527,12 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
             return
         if has_write and lib.pa_write_kv(*wr_args[r]) != 0:
             raise RuntimeError(lib.pa_last_error_string().decode())
-        if lib.pa_decode_ex(*dec_args[r]) != 0:
+        if decode_fn(*dec_args[r]) != 0:
             raise RuntimeError(lib.pa_last_error_string().decode())
 
     def decode_call(i):
-        # the step's decode call: pa_decode_append (rewriting the same rows) or pa_decode_ex
-        status = lib.pa_decode_append(*app_args[i % replicas]) if fused else lib.pa_decode_ex(*dec_args[i % replicas])
+        # the step's decode call: pa_decode_append (rewriting the same rows), pa_decode_ex or pa_decode_multi
+        status = lib.pa_decode_append(*app_args[i % replicas]) if fused else decode_fn(*dec_args[i % replicas])
         if status != 0:
             raise RuntimeError(lib.pa_last_error_string().decode())
 
@@ -562,7 +582,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     # from pinned host memory, the decode call, one download of the output; two slots, so the upload of
     # step i + 1 overlaps the decode of step i.
     e2e = None
-    if not args.no_e2e and not (has_write and not fused):  # the runner does not split write and decode
+    # the step runner does one decode call per step (no separate write, one query token)
+    if not args.no_e2e and not (has_write and not fused) and q_len == 1:
         stepper = pa.DecodeStepper(kcs[0], vcs[0], B, Hq, tables.shape[1], scale=inp.scale, append=fused,
                                    max_context_len=max_ctx, partition_pages=args.partition_pages,
                                    kernel=args.kernel)
@@ -623,7 +644,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     achieved = call_bytes / (dec_avg_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": stored_traffic(args.workload),
-                "kernel": (("pa_decode_append" if fused else "pa_decode") + " call (" +
+                "kernel": (("pa_decode_append" if fused else "pa_decode_multi" if q_len > 1 else "pa_decode") +
+                           " call (" +
                            ("paged_decode_lean_kernel + lean_merge_kernel)" if plan.schedule == 1 else
                             "paged_decode_kernel" + (" + splitkv_merge_kernel)" if plan.max_parts > 1 else ")"))),
                 "algorithmic_bytes_per_launch": call_bytes, "pages_touched_bytes": touched,
@@ -636,7 +658,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         if has_write:
             import oracle
 
-            oracle.write_kv(inp.new_key, inp.new_value, inp.key_cache, inp.value_cache, slots)
+            oracle.write_kv(inp.new_key.reshape(-1, Hkv, d), inp.new_value.reshape(-1, Hkv, d), inp.key_cache,
+                            inp.value_cache, slots)
         threads = os.cpu_count() or 1
         r = time_oracle_parallel(inp, args.cpu_budget, threads)
         cpu = {"value": round(r["bytes"] / r["seconds"] / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
@@ -693,24 +716,35 @@ def run_reference(args, rank: int, world: int) -> None:
         inp = build_batch(args.workload, rank_seed(args.seed, 0))
         tables, lens, slots = pool_tables(inp)
     inp.block_tables = tables
+    q_len = inp.q.shape[1] if inp.q.ndim == 4 else 1
     if slots is not None:
-        oracle.write_kv(inp.new_key, inp.new_value, inp.key_cache, inp.value_cache, slots)
+        oracle.write_kv(inp.new_key.reshape(-1, inp.num_kv_heads, inp.head_dim),
+                        inp.new_value.reshape(-1, inp.num_kv_heads, inp.head_dim), inp.key_cache, inp.value_cache,
+                        slots)
+
+    def one_row(h):
+        if q_len == 1:
+            oracle.decode_inputs(inp, rows=[(0, h)])
+        else:  # one head, every query token
+            oracle.decode_multi(inp.q, inp.key_cache, inp.value_cache, inp.block_tables, inp.context_lens, inp.dtype,
+                                inp.scale, rows=[(0, t, h) for t in range(q_len)])
+
     threads = os.cpu_count() or 1
     # size the per-step sample (heads of sequence 0, one task per head) so that warmup + steps
     # fit in about two minutes on `threads` threads
     t0 = time.perf_counter()
-    oracle.decode_inputs(inp, rows=[(0, 0)])
+    one_row(0)
     t_row = max(time.perf_counter() - t0, 1e-4)
     n_steps = args.steps + args.warmup
     rows_per_step = int(max(1, min(inp.num_heads, 120.0 * threads / n_steps / t_row)))
     L0 = int(inp.context_lens[0])
     eb = inp.elem_bytes
     bytes_per_step = rows_per_step / inp.num_heads * decode_bytes([L0], inp.num_heads, inp.num_kv_heads,
-                                                                  inp.head_dim, eb, inp.block_size)
+                                                                  inp.head_dim, eb, inp.block_size, q_len)
     used = min(threads, rows_per_step)
     with ThreadPoolExecutor(max_workers=used) as ex:
         def one_step():
-            list(ex.map(lambda h: oracle.decode_inputs(inp, rows=[(0, h)]), range(rows_per_step)))
+            list(ex.map(one_row, range(rows_per_step)))
 
         for _ in range(args.warmup):
             one_step()

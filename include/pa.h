@@ -205,6 +205,11 @@ int pa_decode_multi(void* out, const void* query, const void* key_cache, const v
                     int partition_pages, int kernel, void* stream);
 size_t pa_decode_multi_workspace_size(int num_seqs, int q_len, int num_heads, int num_kv_heads, int head_dim,
                                       int block_size, int max_blocks_per_seq, int dtype);
+/* The plan pa_decode_multi would use (pa_decode_make_plan with q_len query tokens per sequence). */
+struct pa_decode_plan;
+int pa_decode_multi_make_plan(int num_seqs, int q_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                              int max_blocks_per_seq, int dtype, size_t workspace_bytes, int max_context_len,
+                              int partition_pages, int kernel, struct pa_decode_plan* plan);
 
 /* The partition plan pa_decode_ex would use on the current device. */
 typedef struct pa_decode_plan {

@@ -65,6 +65,7 @@ _SIGNATURES = [
                               _P]),
     ("pa_decode_multi", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _I, _I, _I, _P]),
     ("pa_decode_multi_workspace_size", _SZ, [_I, _I, _I, _I, _I, _I, _I, _I]),
+    ("pa_decode_multi_make_plan", _I, [_I, _I, _I, _I, _I, _I, _I, _I, _SZ, _I, _I, _I, ctypes.POINTER(DecodePlan)]),
     ("pa_decode_make_plan", _I, [_I, _I, _I, _I, _I, _I, _I, _SZ, _I, _I, _I, ctypes.POINTER(DecodePlan)]),
     ("pa_decode_workspace_size", _SZ, [_I, _I, _I, _I, _I, _I, _I]),
     ("pa_decode_static_scratch", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
@@ -174,12 +175,19 @@ def copy_blocks(key_cache: torch.Tensor, value_cache: torch.Tensor, src_dst_pair
 
 def decode_plan(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
                 max_blocks_per_seq: int, dtype: torch.dtype, workspace_bytes: int = 1 << 62,
-                max_context_len: int = 0, partition_pages: int = 0, kernel: str = "auto") -> DecodePlan:
-    """The partition plan ``pa_decode_ex`` would use on the current device."""
+                max_context_len: int = 0, partition_pages: int = 0, kernel: str = "auto",
+                q_len: int = 1) -> DecodePlan:
+    """The partition plan ``pa_decode_ex`` (``pa_decode_multi`` for q_len > 1) would use on the current device."""
     plan = DecodePlan()
-    _check(library().pa_decode_make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
-                                         max_blocks_per_seq, _TORCH_DTYPES[dtype], workspace_bytes, max_context_len,
-                                         partition_pages, KERNELS[kernel], ctypes.byref(plan)))
+    if q_len == 1:
+        _check(library().pa_decode_make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                             max_blocks_per_seq, _TORCH_DTYPES[dtype], workspace_bytes,
+                                             max_context_len, partition_pages, KERNELS[kernel], ctypes.byref(plan)))
+    else:
+        _check(library().pa_decode_multi_make_plan(num_seqs, q_len, num_heads, num_kv_heads, head_dim, block_size,
+                                                   max_blocks_per_seq, _TORCH_DTYPES[dtype], workspace_bytes,
+                                                   max_context_len, partition_pages, KERNELS[kernel],
+                                                   ctypes.byref(plan)))
     return plan
 
 

@@ -185,6 +185,7 @@ int encode_cache_map(CUtensorMap* map, const void* base, int dtype, int num_bloc
 struct Plan {
     int kind = 0;
     int dkind = 0;  // the kernel instantiation: kind, or 3 for the tensor-core kernel with causal bounds
+    bool row_split = false;  // one CTA per partition takes all of a kv head's row chunks, a warp each
     int schedule = kScheduleGrid;
     int gmax = 8;
     int head_chunks = 1;
@@ -248,6 +249,13 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
         return fail(PA_ERR_UNSUPPORTED, "no %s decode kernel for dtype=%d head_dim=%d block_size=%d",
                     p.kind == PA_KERNEL_MMA ? "tensor-core" : "CUDA-core", dtype, head_dim, block_size);
     p.head_chunks = (rows + p.ki.heads_per_cta - 1) / p.ki.heads_per_cta;
+    // Multi-query rows of a kv head in 2..4 chunks: row split on the partitioned grid, so that
+    // every page is loaded once for all the chunks (as separate units each chunk would stream
+    // the pages again).
+    if (p.dkind == 3 && p.head_chunks >= 2 && p.head_chunks <= p.ki.lean_warps_per_cta) {
+        p.row_split = true;
+        p.head_chunks = 1;
+    }
     p.units = num_seqs * num_kv_heads * p.head_chunks;
 
     long long max_ctx = (long long)max_blocks * block_size;
@@ -265,7 +273,7 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
     // to keep every SM streaming, and equal shares balance them.  With more units than
     // that, whole-unit CTAs already balance and need no merge.)
     const long long lean_ctas = (long long)dev->num_sms * p.ki.lean_ctas_per_sm;
-    if (partition_pages == 0 && has_ws && num_seqs <= p.ki.lean_max_seqs &&
+    if (partition_pages == 0 && has_ws && !p.row_split && num_seqs <= p.ki.lean_max_seqs &&
         (long long)p.units < lean_ctas * p.ki.lean_warps_per_cta &&
         (long long)num_seqs * max_blocks * num_kv_heads * p.head_chunks < (1ll << 31)) {
         const long long ctas = lean_ctas;
@@ -499,6 +507,7 @@ int decode_impl(void* out, const void* query, const void* new_key, const void* n
     a.q_len = q_len;
     a.rows = q_len * a.group;
     a.head_chunks = p.head_chunks;
+    a.row_split = p.row_split ? 1 : 0;
     a.max_blocks = max_blocks_per_seq;
     a.num_blocks = num_blocks;
     a.partition_pages = p.partition_pages;
@@ -554,6 +563,27 @@ int pa_decode_multi(void* out, const void* query, const void* key_cache, const v
     return decode_impl(out, query, nullptr, nullptr, key_cache, value_cache, block_tables, context_lens, num_seqs,
                        num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype,
                        workspace, workspace_bytes, max_context_len, partition_pages, kernel, stream, q_len);
+}
+
+int pa_decode_multi_make_plan(int num_seqs, int q_len, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                              int max_blocks_per_seq, int dtype, size_t workspace_bytes, int max_context_len,
+                              int partition_pages, int kernel, pa_decode_plan* out) {
+    clear_error();
+    if (!out) return fail(PA_ERR_INVALID_ARG, "pa_decode_multi_make_plan: out is NULL");
+    Plan p;
+    int st = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, dtype,
+                       workspace_bytes > 0, workspace_bytes, max_context_len, partition_pages, kernel, &p, q_len);
+    if (st != PA_OK) return st;
+    out->kernel = p.kind;
+    out->schedule = p.schedule;
+    out->partition_pages = p.partition_pages;
+    out->max_parts = p.max_parts;
+    out->heads_per_cta = p.ki.heads_per_cta;
+    out->grid_ctas = (int)p.grid;
+    out->threads_per_cta = p.ki.threads;
+    out->smem_bytes = p.ki.smem_bytes;
+    out->workspace_bytes = p.ws_bytes;
+    return PA_OK;
 }
 
 size_t pa_decode_multi_workspace_size(int num_seqs, int q_len, int num_heads, int num_kv_heads, int head_dim,

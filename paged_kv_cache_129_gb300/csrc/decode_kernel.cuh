@@ -366,6 +366,30 @@ struct MmaConsumer {
         }
     }
 
+    // Split-KV partials of the gc rows straight into the workspace (after finish()):
+    // ws_m / ws_l [row][part], ws_o [row][part][D], rows row0 .. row0 + gc - 1.
+    __device__ __forceinline__ void write_split(float* ws_m, float* ws_l, float* ws_o, size_t row0, int max_parts,
+                                                int part, int gc, int lane) const {
+        const int g = lane >> 2, t = lane & 3;
+        if (t == 0 && g < gc) {
+            ws_m[(row0 + g) * max_parts + part] = m;
+            ws_l[(row0 + g) * max_parts + part] = l;
+        }
+        float* lo = ws_o + ((row0 + 2 * t) * max_parts + part) * D;
+        float* hi = ws_o + ((row0 + 2 * t + 1) * max_parts + part) * D;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            if (2 * t < gc) {
+                lo[mt * 16 + g] = o[mt][0];
+                lo[mt * 16 + 8 + g] = o[mt][2];
+            }
+            if (2 * t + 1 < gc) {
+                hi[mt * 16 + g] = o[mt][1];
+                hi[mt * 16 + 8 + g] = o[mt][3];
+            }
+        }
+    }
+
     // Write this warp's state into the CTA combine buffer.
     __device__ __forceinline__ void store(float* co, float* cm, float* cl, int warp, int lane, int ostride) {
         const int g = lane >> 2, t = lane & 3;
@@ -579,6 +603,9 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Dec
     const int bk = unit / a.head_chunks;
     const int kvh = bk % a.num_kv_heads;
     const int b = bk / a.num_kv_heads;
+    // Row split: every consumer warp takes one row chunk of the kv head and every page.
+    const bool rs = CAUSAL && a.row_split;
+    const int nchunks = rs ? (a.rows + C::kHeads - 1) / C::kHeads : 1;
     // the unit's query/output rows (built where used, so that no copy lives across the page loop)
 #define PA_UNIT_ROWS UnitRows{b, kvh, hc * C::kHeads, a.q_len, a.group, a.num_heads}
     const int gc = min(C::kHeads, a.rows - hc * C::kHeads);
@@ -595,7 +622,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Dec
 
     if (L == 0) {  // empty context: zero rows (partition 0 writes them)
         if (p == 0)
-            for (int idx = tid; idx < gc * D; idx += C::kThreads)
+            for (int idx = tid; idx < (rs ? a.rows : gc) * D; idx += C::kThreads)
                 out[PA_UNIT_ROWS.row(idx / D) * D + idx % D] = from_float<T>(0.f);
         return;
     }
@@ -606,7 +633,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Dec
     if (tid == 0) {
         for (int s = 0; s < C::kNSlot; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+            mbar_init(&empty[s], nchunks);  // row split: every chunk's warp releases the slot
             issued[s] = 0;
         }
         flags[0] = 0;
@@ -672,12 +699,16 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Dec
         const int i_tok = a.new_key != nullptr ? nblk - 1 - first : -1;  // that page's index here
         if constexpr (MMA) {
             MmaConsumer<T, D, BS, CAUSAL> cons;
-            {
-                const UnitRows rows = PA_UNIT_ROWS;
-                const int r = min(lane >> 2, gc - 1);
-                cons.init(q + rows.row(r) * D, (lane >> 2) < gc, rows.last_pos(lane >> 2, L), lane);
+            const int chunk = rs ? warp : hc;  // this warp's row chunk
+            const int cgc = rs ? min(C::kHeads, a.rows - chunk * C::kHeads) : gc;
+            if (cgc > 0) {
+                const UnitRows rows{b, kvh, chunk * C::kHeads, a.q_len, a.group, a.num_heads};
+                const int r = min(lane >> 2, cgc - 1);
+                cons.init(q + rows.row(r) * D, (lane >> 2) < cgc, rows.last_pos(lane >> 2, L), lane);
             }
-            for (int i = warp; i < npages; i += C::kNW) {
+            // without row split the warps share the pages round-robin; with it a warp whose
+            // chunk is empty (fewer than four chunks) takes no part
+            for (int i = rs ? (cgc > 0 ? 0 : npages) : warp; i < npages; i += rs ? 1 : C::kNW) {
                 const int s = i % C::kNSlot;
                 const bool got = mbar_wait_bounded(&full[s], (i / C::kNSlot) & 1, a.err, flags);
                 if (!__all_sync(0xffffffffu, got)) break;
@@ -688,14 +719,29 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Dec
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
-            // All consumers are past their last page, so every TMA into the ring has
-            // landed and been read: the ring can hold the combine buffer.
-            asm volatile("bar.sync 1, %0;" ::"r"(C::kNW * 32) : "memory");
-            if (!flags[0]) {
-                float* co = reinterpret_cast<float*>(ring);
-                float* cm = co + C::kNW * C::kHeads * C::kOStride;
-                float* cl = cm + C::kNW * C::kHeads;
-                cons.store(co, cm, cl, warp, lane, C::kOStride);
+            if (rs) {
+                // each warp holds whole rows: no combine, its rows go straight out
+                if (cgc > 0 && !flags[0]) {
+                    cons.finish();
+                    if (nparts == 1) {
+                        cons.write_out(out, UnitRows{b, kvh, chunk * C::kHeads, a.q_len, a.group, a.num_heads}, cgc,
+                                       lane);
+                    } else {
+                        cons.write_split(a.ws_m, a.ws_l, a.ws_o,
+                                         ((size_t)b * a.num_kv_heads + kvh) * a.rows + chunk * C::kHeads, a.max_parts,
+                                         p, cgc, lane);
+                    }
+                }
+            } else {
+                // All consumers are past their last page, so every TMA into the ring has
+                // landed and been read: the ring can hold the combine buffer.
+                asm volatile("bar.sync 1, %0;" ::"r"(C::kNW * 32) : "memory");
+                if (!flags[0]) {
+                    float* co = reinterpret_cast<float*>(ring);
+                    float* cm = co + C::kNW * C::kHeads * C::kOStride;
+                    float* cl = cm + C::kNW * C::kHeads;
+                    cons.store(co, cm, cl, warp, lane, C::kOStride);
+                }
             }
         } else {
             float* q_s = reinterpret_cast<float*>(smem + C::kQsOffset);
@@ -740,6 +786,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Dec
                 }
         return;
     }
+    if (rs) return;  // row split: the warps wrote their own rows
 
     // ---- combine the consumer warps' states ----
     const float* co = reinterpret_cast<const float*>(ring);

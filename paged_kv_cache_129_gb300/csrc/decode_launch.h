@@ -32,6 +32,10 @@ struct DecodeArgs {
     // (q_len = 1: single-step decode).  A kv head serves rows = q_len * group query rows,
     // row v = t * group + h being query token t of head kvh * group + h.
     int q_len, rows;
+    // Row split (the tensor-core kernel with per-row bounds, a kv head of 2..4 row chunks):
+    // each consumer warp of a partition's CTA takes one row chunk and consumes every page,
+    // so a page is loaded once for all of the kv head's rows (head_chunks is then 1).
+    int row_split;
     int max_blocks, num_blocks;
     int partition_pages, max_parts;
     float scale_log2;            // softmax scale * log2(e)

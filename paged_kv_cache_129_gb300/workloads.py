@@ -186,12 +186,15 @@ def make_decode_inputs(name: str, *, context_lens, num_heads: int, num_kv_heads:
                        key_cache=key_cache, value_cache=value_cache, block_tables=tables,
                        context_lens=lens, scale=default_scale(head_dim) if scale is None else scale)
     if with_new_token:
-        # The new token of sequence b sits at logical position L_b - 1 (write, then attend).
-        # Its slot is derived by the caller (a block pool, or a test's own translation).
+        # The new token of sequence b sits at logical position L_b - 1 (write, then attend);
+        # with q_len > 1 the q_len new tokens sit at L_b - q_len .. L_b - 1 ([B, q_len, H_kv, d]).
+        # Their slots are derived by the caller (a block pool, or a test's own translation).
         b_count = len(lens)
-        inp.new_key = _normal(streams[3], (b_count, num_kv_heads, head_dim), dtype)
-        inp.new_value = _normal(streams[4], (b_count, num_kv_heads, head_dim), dtype)
-        inp.new_token_pos = (lens.astype(np.int64) - 1)
+        shape = (b_count, num_kv_heads, head_dim) if q_len == 1 else (b_count, q_len, num_kv_heads, head_dim)
+        inp.new_key = _normal(streams[3], shape, dtype)
+        inp.new_value = _normal(streams[4], shape, dtype)
+        inp.new_token_pos = (lens.astype(np.int64) - 1) if q_len == 1 else (
+            lens.astype(np.int64)[:, None] - q_len + np.arange(q_len, dtype=np.int64)[None, :])
     return inp
 
 
@@ -201,6 +204,14 @@ def tiny(seed: int = 0) -> DecodeInputs:
     """4 sequences with context lengths {1, 15, 16, 33}, 4 q / 2 kv heads, d 64, fp32, pool 16."""
     return make_decode_inputs("tiny", context_lens=[1, 15, 16, 33], num_heads=4, num_kv_heads=2,
                               head_dim=64, block_size=16, dtype="f32", num_blocks=16, seed=seed)
+
+
+def qwen_gqa_verify(seed: int = 0, num_seqs: int = 64, q_len: int = 4) -> DecodeInputs:
+    """The Qwen-style GQA batch in a speculative verify step: q_len new tokens per sequence
+    (written, then attended causally), the same context-length distribution and pool."""
+    return make_decode_inputs(f"qwen_gqa_verify{q_len}", context_lens=lambda r: r.integers(512, 4097, size=num_seqs),
+                              num_heads=28, num_kv_heads=4, head_dim=128, block_size=16, dtype="bf16",
+                              num_blocks=20000, seed=seed, with_new_token=True, q_len=q_len)
 
 
 def qwen_gqa(seed: int = 0, num_seqs: int = 64) -> DecodeInputs:

@@ -80,3 +80,17 @@ def test_prefix_setup_through_the_block_pool(workload, copies):
     # distinct pages are far fewer than the pages all sequences read
     touched = bench.pages_touched_bytes(lens, inp.num_kv_heads, inp.head_dim, 2, bs)
     assert unique < touched / 8
+
+
+def test_verify_setup_slots_are_the_last_q_len_positions():
+    from paged_kv_cache_129_gb300 import workloads as wl
+
+    inp = wl.make_decode_inputs("v", context_lens=[5, 16, 40, 33], num_heads=8, num_kv_heads=2, head_dim=64,
+                                block_size=16, dtype="bf16", pool_slack=0.5, seed=1, with_new_token=True, q_len=4)
+    tables, lens, slots = bench.pool_tables(inp)
+    assert slots.shape == (4 * 4,)
+    bs = 16
+    for b in range(4):
+        for t in range(4):
+            pos = int(lens[b]) - 4 + t
+            assert slots[b * 4 + t] == int(tables[b, pos // bs]) * bs + pos % bs

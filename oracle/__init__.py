@@ -63,6 +63,8 @@ def _load() -> ctypes.CDLL:
             lib.oracle_write_kv.argtypes = [p, p, p, p, p, i32, i32, i32, i32, i32, i32]
             lib.oracle_copy_blocks.restype = i32
             lib.oracle_copy_blocks.argtypes = [p, p, p, i32, i64, i32]
+            lib.oracle_swap_blocks.restype = i32
+            lib.oracle_swap_blocks.argtypes = [p, p, p, p, p, i32, i64, i32, i32]
             lib.oracle_element_to_double.restype = dbl
             lib.oracle_element_to_double.argtypes = [p, i32, i64]
             _lib = lib
@@ -178,6 +180,20 @@ def copy_blocks(key_cache: np.ndarray, value_cache: np.ndarray, pairs: np.ndarra
     block_bytes = key_cache.nbytes // num_blocks
     return lib.oracle_copy_blocks(_ptr(key_cache), _ptr(value_cache), _ptr(pairs), int(pairs.shape[0]),
                                   block_bytes, num_blocks)
+
+
+def swap_blocks(dst_key: np.ndarray, dst_value: np.ndarray, src_key: np.ndarray, src_value: np.ndarray,
+                pairs: np.ndarray) -> int:
+    """Block copy between two pools (swap out / swap in): dst block <- src block for every
+    (src, dst) pair, both caches, as bytes; returns the oracle status."""
+    lib = _load()
+    pairs = np.ascontiguousarray(np.asarray(pairs, dtype=np.int64).reshape(-1, 2))
+    assert dst_key.shape[1:] == src_key.shape[1:] and dst_key.dtype == src_key.dtype
+    for a in (dst_key, dst_value, src_key, src_value):
+        assert a.flags["C_CONTIGUOUS"]
+    block_bytes = src_key[0].nbytes if src_key.shape[0] else dst_key[0].nbytes
+    return lib.oracle_swap_blocks(_ptr(dst_key), _ptr(dst_value), _ptr(src_key), _ptr(src_value), _ptr(pairs),
+                                  int(pairs.shape[0]), block_bytes, src_key.shape[0], dst_key.shape[0])
 
 
 def slots_for_positions(block_tables: np.ndarray, seq_ids: Sequence[int], positions: Sequence[int],

@@ -21,7 +21,17 @@ Additions where that page is silent (each one a stated reading):
 * an exhausted pool raises ``MemoryError`` and leaves every structure as it
   was (the page lists OOM rollback among what a real allocator must handle);
 * ``append`` also reports the slot of the new token (block * bs + offset,
-  MiniPaged-Qwen section 8.1) and the (src, dst) pair of a copy-on-write.
+  MiniPaged-Qwen section 8.1) and the (src, dst) pair of a copy-on-write;
+* swap (the vLLM/PagedAttention page lists preemption as releasing or
+  migrating a request's physical blocks while its logical tokens are kept; the
+  LLM-inference page swaps a request's KV blocks to CPU memory and back): a
+  sequence moves from one pool to another pool of the same block size.  Every
+  block of its table, in table order, gets a fresh block of the destination
+  pool (LIFO) holding the same tokens; then the sequence is released in the
+  source pool (so a block it shared stays there for the other holders).  The
+  moved blocks are private (sharing is not carried across a swap).  The
+  destination names the sequence with its own next id.  Too few free blocks in
+  the destination raise ``MemoryError`` with both pools unchanged.
 """
 from __future__ import annotations
 
@@ -130,6 +140,20 @@ class SequencePool:
     def release(self, sid: int) -> None:
         self.pool.release(self.tables.pop(sid))
         del self.lens[sid]
+
+    def swap_to(self, dst: "SequencePool", sid: int):
+        """Move sequence ``sid`` into pool ``dst``; returns (its id there, [(src block, dst block)])."""
+        if dst.block_size != self.block_size:
+            raise ValueError("pools differ in block size")
+        table = self.tables[sid]
+        if len(dst.pool.free) < len(table):
+            raise MemoryError("destination pool exhausted")
+        new_table = [dst.pool._take(self.pool.data[block]) for block in table]
+        new_sid = dst.create()
+        dst.tables[new_sid] = new_table
+        dst.lens[new_sid] = self.lens[sid]
+        self.release(sid)
+        return new_sid, list(zip(table, new_table))
 
     def num_free(self) -> int:
         return len(self.pool.free)

@@ -21,6 +21,10 @@
  *      as a byte copy; a negative slot means "no write".
  *  - copy    (vLLM and PagedAttention page, copy-on-write section): every
  *      (src, dst) pair copies the whole physical block dst <- src, as bytes.
+ *  - swap    (vLLM and PagedAttention page, preemption: physical blocks move
+ *      out of HBM and back; the LLM-inference page's swap of a request's KV
+ *      blocks to CPU memory and back): the same byte copy, but from block src
+ *      of one pool to block dst of another pool of the same block geometry.
  */
 #include <math.h>
 #include <stdint.h>
@@ -244,6 +248,24 @@ int oracle_copy_blocks(void* key_cache, void* value_cache, const int64_t* pairs,
                (size_t)block_bytes);
         memcpy((char*)value_cache + dst * block_bytes, (const char*)value_cache + src * block_bytes,
                (size_t)block_bytes);
+    }
+    return status;
+}
+
+/* Block dst of the destination pool <- block src of the source pool, both caches, as bytes.
+ * A pair with an id outside its own pool is skipped and reported. */
+int oracle_swap_blocks(void* dst_key, void* dst_value, const void* src_key, const void* src_value,
+                       const int64_t* pairs, int num_pairs, int64_t block_bytes, int src_blocks, int dst_blocks) {
+    int status = ORACLE_OK;
+    for (int p = 0; p < num_pairs; ++p) {
+        const int64_t src = pairs[2 * p];
+        const int64_t dst = pairs[2 * p + 1];
+        if (src < 0 || src >= src_blocks || dst < 0 || dst >= dst_blocks) {
+            status = ORACLE_BAD_TABLE;
+            continue;
+        }
+        memcpy((char*)dst_key + dst * block_bytes, (const char*)src_key + src * block_bytes, (size_t)block_bytes);
+        memcpy((char*)dst_value + dst * block_bytes, (const char*)src_value + src * block_bytes, (size_t)block_bytes);
     }
     return status;
 }

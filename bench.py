@@ -64,7 +64,13 @@ WORKLOAD_DESCRIPTIONS = {
                   "sequence's K/V counted), roofline over the unique pages",
     "prefix_cow_2056": "prefix sharing, copy-on-write variant: as prefix_cow with a 2056-token prefix, so the "
                        "first append of 63 sequences copies the shared partial block (pa_copy_blocks)",
+    "swap_qwen": "preemption swap on the Qwen-style GQA layer's cache (4 kv heads, head_dim 128, bf16, "
+                 "block_size 16, pool 20000 blocks, 64 sequences with context_lens uniform in [512,4096] "
+                 "built through the block pool): each step swaps 16 sequences out to a page-locked host pool "
+                 "while the 16 swapped out the step before come back in (pa_seq_swap + pa_swap_blocks, one "
+                 "launch per direction, the two on separate streams)",
 }
+SWAP_GROUP = 16  # sequences preempted per swap step
 DTYPE_NAMES = {"f32": "f32", "f16": "f16", "bf16": "bf16"}
 
 
@@ -586,7 +592,14 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     if not args.no_e2e and not (has_write and not fused) and q_len == 1:
         stepper = pa.DecodeStepper(kcs[0], vcs[0], B, Hq, tables.shape[1], scale=inp.scale, append=fused,
                                    max_context_len=max_ctx, partition_pages=args.partition_pages,
-                                   kernel=args.kernel)
+                                   kernel=args.kernel, tables="deltas")
+        # the device tables are kept by delta uploads: the first step sends every entry, later steps
+        # re-send the tail entry of B / bs rows (the rate at which one token a step opens new blocks)
+        nblk = (lens + bs - 1) // bs
+        full_deltas = np.array([(r, j, tables[r, j]) for r in range(B) for j in range(nblk[r])],
+                               np.int32).reshape(-1, 3)
+        churn = max(1, B // bs)
+        tail = np.maximum(nblk - 1, 0).astype(np.int32)
 
         def fill(view, arr):
             a = np.ascontiguousarray(arr)
@@ -596,20 +609,27 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         for sl in range(stepper.slots):
             v = stepper.inputs(sl)
             fill(v.query, inp.q)
-            v.block_tables.copy_(torch.from_numpy(tables))
             v.context_lens.copy_(torch.from_numpy(lens))
             if fused:
                 fill(v.new_key, inp.new_key)
                 fill(v.new_value, inp.new_value)
 
-        def e2e_run(n):
+        def e2e_run(n, first=False):
             for i in range(n):
-                stepper.launch(i, kcs[i % replicas], vcs[i % replicas])
+                dv = stepper.inputs(i).deltas.numpy()
+                if first and i == 0:
+                    k = len(full_deltas)
+                    dv[:k] = full_deltas
+                else:
+                    rows = (i * churn + np.arange(churn)) % B
+                    k = churn
+                    dv[:k, 0], dv[:k, 1], dv[:k, 2] = rows, tail[rows], tables[rows, tail[rows]]
+                stepper.launch(i, kcs[i % replicas], vcs[i % replicas], num_deltas=k)
                 if i >= 1:
                     stepper.result(i - 1)
             stepper.result(n - 1)
 
-        e2e_run(min(args.warmup, 20) + 1)
+        e2e_run(min(args.warmup, 20) + 1, first=True)
         torch.cuda.synchronize()
         Ke = max(1, min(K, args.e2e_steps))
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -627,10 +647,11 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         e2e = {"value": round(e_bytes / (e_ms / 1e3) / 1e9, 2), "unit": UNIT, "steps": Ke,
                "ms_per_step": round(e_ms / Ke, 5), "h2d_bytes_per_step": int(stepper.h2d_bytes),
                "d2h_bytes_per_step": int(stepper.d2h_bytes),
-               "note": f"pa.DecodeStepper ({'pa_decode_append' if fused else 'pa_decode'}): every step one upload "
-                       "of the packed inputs (queries" + (", new K/V" if fused else "") + ", block tables, "
-                       "lengths) from pinned host memory and one download of the output, inside the timed "
-                       "region; two slots, the next upload overlapping the current decode"}
+               "note": f"pa.DecodeStepper ({'pa_decode_append' if fused else 'pa_decode'}, tables kept on the "
+                       "device by deltas): every step one upload of the packed inputs (queries" +
+                       (", new K/V" if fused else "") + f", lengths, {churn} block-table deltas) from pinned host "
+                       "memory, pa_apply_table_deltas and the decode on the compute stream, one download of the "
+                       "output, inside the timed region; two slots, the next upload overlapping the current decode"}
 
     peaks = measured_peaks()
     peak = peaks.get("hbm_gbs")
@@ -702,6 +723,239 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     print(json.dumps(line), flush=True)
 
 
+def swap_plan(seed: int, steps: int, num_blocks: int = 20000, num_seqs: int = 64, group: int = SWAP_GROUP,
+              block_size: int = 16):
+    """Host side of the swap workload (no GPU).  Sequences are built through the product block pool; the
+    groups of ``group`` sequences take turns: step k swaps group k out to host pool k % 2 and group k - 1
+    back in from host pool (k - 1) % 2, so the two copies of a step can run at once.  Per step the pool
+    decides the swap-in first (its device blocks come from blocks free before this step's swap-out
+    releases any) and then the swap-out (into the other host pool), so the two copies touch disjoint
+    blocks on both sides.  Returns (per-step (out pairs, out host pool, in pairs, in host pool), host pool
+    size, seconds of pool work per step, lengths)."""
+    import paged_kv_cache_129_gb300 as pa
+
+    assert 2 * group <= num_seqs
+    rng = np.random.default_rng(seed)
+    lens = rng.integers(512, 4097, size=num_seqs)
+    dev = pa.BlockPool(num_blocks, block_size, free_order=rng.permutation(num_blocks))
+    ids = [dev.create() for _ in range(num_seqs)]
+    for t in range(int(lens.max())):
+        dev.append_batch([sid for sid, n in zip(ids, lens) if n > t])
+    host_blocks = int(np.sort((lens + block_size - 1) // block_size)[-group:].sum())
+    hosts = [pa.BlockPool(host_blocks, block_size), pa.BlockPool(host_blocks, block_size)]
+    away = {}  # sequence index -> id in its host pool
+    plan, t_pool = [], 0.0
+    none = np.zeros((0, 2), np.int64)
+    for k in range(steps):
+        t0 = time.perf_counter()
+        ins = []
+        if k > 0:
+            for j in range(group):
+                i = ((k - 1) * group + j) % num_seqs
+                ids[i], pairs = hosts[(k - 1) % 2].swap_to(dev, away.pop(i))
+                ins.append(pairs)
+        outs = []
+        for j in range(group):
+            i = (k * group + j) % num_seqs
+            away[i], pairs = dev.swap_to(hosts[k % 2], ids[i])
+            outs.append(pairs)
+        t_pool += time.perf_counter() - t0
+        plan.append((np.concatenate(outs), k % 2, np.concatenate(ins) if ins else none, (k - 1) % 2))
+    for p in [dev] + hosts:
+        p.check_invariants()
+    return plan, host_blocks, t_pool / max(steps, 1), lens
+
+
+def run_swap(args, rank: int, world: int, local_rank: int) -> None:
+    """The swap workload: device time of each step's swap-out and swap-in launches, on two streams."""
+    import torch
+
+    import paged_kv_cache_129_gb300 as pa
+
+    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    lib = pa.library()
+    nb, hkv, bs, d = 20000, 4, 16, 128
+    n_steps = args.warmup + args.steps
+    plan, host_blocks, pool_s, lens = swap_plan(rank_seed(args.seed, rank), n_steps)
+    gen = torch.Generator(device=device).manual_seed(rank_seed(args.seed, rank))
+    kc = torch.randn(nb, hkv, bs, d, device=device, generator=gen).to(torch.bfloat16)
+    vc = torch.randn(nb, hkv, bs, d, device=device, generator=gen).to(torch.bfloat16)
+    hk = [torch.empty(host_blocks, hkv, bs, d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    hv = [torch.empty(host_blocks, hkv, bs, d, dtype=torch.bfloat16).pin_memory() for _ in range(2)]
+    # every step's pairs in page-locked host memory: the kernel reads them there
+    offs, flat, pos = [], [], 0
+    for out_p, _, in_p, _ in plan:
+        offs.append((pos, len(out_p), pos + len(out_p), len(in_p)))
+        flat += [out_p, in_p]
+        pos += len(out_p) + len(in_p)
+    pairs = torch.from_numpy(np.concatenate(flat)).pin_memory()
+    main = torch.cuda.current_stream(device)
+    s_out, s_in = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    block_bytes = hkv * bs * d * 2
+    base = pairs.data_ptr()
+    done_out, done_in = torch.cuda.Event(), torch.cuda.Event()
+
+    def step(k):
+        o0, no, i0, ni = offs[k]
+        _, ho, _, hi = plan[k]
+        # a step's copies start when both copies of the previous step are done (their blocks are reused)
+        s_out.wait_event(done_in)
+        s_in.wait_event(done_out)
+        if lib.pa_swap_blocks(hk[ho].data_ptr(), hv[ho].data_ptr(), kc.data_ptr(), vc.data_ptr(), base + 16 * o0,
+                              no, hkv, d, bs, nb, host_blocks, 2, int(s_out.cuda_stream)) != 0:
+            raise RuntimeError(lib.pa_last_error_string().decode())
+        if ni and lib.pa_swap_blocks(kc.data_ptr(), vc.data_ptr(), hk[hi].data_ptr(), hv[hi].data_ptr(),
+                                     base + 16 * i0, ni, hkv, d, bs, host_blocks, nb, 2,
+                                     int(s_in.cuda_stream)) != 0:
+            raise RuntimeError(lib.pa_last_error_string().decode())
+        done_out.record(s_out)
+        done_in.record(s_in)
+        return (no + ni) * 2 * block_bytes, no * 2 * block_bytes, ni * 2 * block_bytes, 1 + (ni > 0)
+
+    def join():
+        main.wait_stream(s_out)
+        main.wait_stream(s_in)
+
+    sampler = ClockSampler(gpu_selector(device))
+    sampler.start()
+    done_out.record(main)
+    done_in.record(main)
+    for k in range(args.warmup):
+        step(k)
+    join()
+    torch.cuda.synchronize()
+    pa.check_error()
+    link = measure_link(torch, device)
+
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize()
+    t_begin = time.monotonic()
+    moved = d2h = h2d = launches = 0
+    ev0.record(main)
+    s_out.wait_stream(main)
+    s_in.wait_stream(main)
+    for k in range(args.warmup, n_steps):
+        m, o, i, n = step(k)
+        moved, d2h, h2d, launches = moved + m, d2h + o, h2d + i, launches + n
+    join()
+    ev1.record(main)
+    torch.cuda.synchronize()
+    t_end = time.monotonic()
+    barrier(world)
+    sampler.stop()
+    pa.check_error()
+    K = args.steps
+    ms = max_over_ranks(ev0.elapsed_time(ev1), world)
+    value = sum_over_ranks(float(moved), world) / (ms / 1e3) / 1e9
+    e2e_ms = ms + pool_s * 1e3 * K  # plus the host pool's decisions, made before the timed region
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = time_swap_oracle(plan[1], host_blocks, budget_s=min(args.cpu_budget, 10.0))
+        cpu = {"value": r["gbs"], "unit": UNIT, "cores": 1, "kind": "oracle",
+               "sample": f"step 1's {r['pairs']} pairs (out and in), oracle byte copy between two numpy pools, "
+                         f"repeated {r['reps']} times ({r['seconds']:.1f} s)"}
+    clocks = sampler.summary(t_begin, t_end)
+    if rank != 0:
+        return
+    peak = link["both_gbs"]
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms / K, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESCRIPTIONS["swap_qwen"], "name": "swap_qwen",
+                   "step": f"pa_swap_blocks out ({SWAP_GROUP} sequences' blocks, device -> host) on one stream and "
+                           f"pa_swap_blocks in (the previous {SWAP_GROUP}, host -> device) on another, at once; "
+                           "pairs read from page-locked host memory",
+                   "l2": "host side of every copy crosses the link; device blocks change each step",
+                   "host_pool_blocks": host_blocks, "mean_context": float(lens.mean()),
+                   "parallelism": f"{world} independent replicas (one pool per GPU)"},
+        "roofline": {"bound": "host_link", "achieved": round(value, 1), "peak": round(peak, 1), "unit": "GB/s",
+                     "frac": round(value / peak, 4), "traffic": None,
+                     "kernel": "swap_blocks_kernel (one launch per direction per step, two streams)",
+                     "algorithmic_bytes_per_step": int(moved / K), "avg_step_ms": round(ms / K, 5),
+                     "timing": f"CUDA events around {K} steps back to back",
+                     "peak_source": "of measured in this run: cudaMemcpyAsync of one 256 MiB page-locked buffer "
+                                    "to the device and one from it, at once on two streams (best of 5)",
+                     "link_gbs": link},
+        "e2e": {"value": round(sum_over_ranks(float(moved), world) / (e2e_ms / 1e3) / 1e9, 2), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d / K), "d2h_bytes_per_step": int(d2h / K),
+                "note": "device time of the launches plus the host pool's swap decisions (pa_seq_swap for "
+                        f"2 x {SWAP_GROUP} sequences, {pool_s * 1e6:.0f} us per step, measured before the "
+                        "timed region); every copied byte crosses the host link"},
+        "cpu_baseline": cpu,
+        "gpu_launches": launches,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
+def measure_link(torch, device, nbytes: int = 256 << 20, reps: int = 5) -> dict:
+    """The host link's rate as the CUDA runtime reaches it: one contiguous page-locked buffer copied to the
+    device, from it, and both at once on two streams (best of ``reps``, CUDA events)."""
+    hbuf = [torch.empty(nbytes, dtype=torch.uint8).pin_memory() for _ in range(2)]
+    dbuf = [torch.empty(nbytes, dtype=torch.uint8, device=device) for _ in range(2)]
+    main = torch.cuda.current_stream(device)
+    s2 = torch.cuda.Stream(device)
+
+    def best(fn, moved):
+        t = float("inf")
+        for _ in range(reps):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda.synchronize()
+            a.record(main)
+            fn()
+            b.record(main)
+            torch.cuda.synchronize()
+            t = min(t, a.elapsed_time(b))
+        return round(moved / (t / 1e3) / 1e9, 1)
+
+    def both():
+        s2.wait_stream(main)
+        dbuf[0].copy_(hbuf[0], non_blocking=True)
+        with torch.cuda.stream(s2):
+            hbuf[1].copy_(dbuf[1], non_blocking=True)
+        main.wait_stream(s2)
+
+    r = {"h2d_gbs": best(lambda: dbuf[0].copy_(hbuf[0], non_blocking=True), nbytes),
+         "d2h_gbs": best(lambda: hbuf[1].copy_(dbuf[1], non_blocking=True), nbytes),
+         "both_gbs": best(both, 2 * nbytes)}
+    del hbuf, dbuf
+    return r
+
+
+_SWAP_POOLS: dict = {}
+
+
+def time_swap_oracle(pairs_step, host_blocks: int, budget_s: float, nb: int = 20000):
+    """The oracle's byte copy of one swap step (out and in) between two numpy pools of the workload's
+    geometry, repeated for about ``budget_s`` seconds."""
+    import oracle
+
+    out_p, _, in_p, _ = pairs_step
+    key = (nb, host_blocks)
+    if _SWAP_POOLS.get("key") != key:
+        rng = np.random.default_rng(0)
+        _SWAP_POOLS.update(key=key, pools=(rng.integers(0, 2**16, (nb, 4, 16, 128), dtype=np.uint16),
+                                           rng.integers(0, 2**16, (nb, 4, 16, 128), dtype=np.uint16),
+                                           np.zeros((host_blocks, 4, 16, 128), np.uint16),
+                                           np.zeros((host_blocks, 4, 16, 128), np.uint16)))
+    dev_k, dev_v, host_k, host_v = _SWAP_POOLS["pools"]
+    block_bytes = 4 * 16 * 128 * 2
+    reps, t0 = 0, time.perf_counter()
+    while True:
+        oracle.swap_blocks(host_k, host_v, dev_k, dev_v, out_p)
+        oracle.swap_blocks(dev_k, dev_v, host_k, host_v, in_p)
+        reps += 1
+        dt = time.perf_counter() - t0
+        if dt >= budget_s or reps >= 1000:
+            break
+    moved = reps * 2 * (len(out_p) + len(in_p)) * block_bytes
+    return {"gbs": round(moved / dt / 1e9, 3), "pairs": len(out_p) + len(in_p), "reps": reps, "seconds": dt}
+
+
 def run_reference(args, rank: int, world: int) -> None:
     """The oracle as the reference arm: each step decodes a bounded sample of the batch on the host cores."""
     if rank != 0:
@@ -710,6 +964,34 @@ def run_reference(args, rank: int, world: int) -> None:
 
     import oracle
 
+    if args.workload == "swap_qwen":
+        plan, host_blocks, _, _ = swap_plan(rank_seed(args.seed, 0), 2)
+        _, _, in_p, _ = plan[1]
+        out_p = plan[1][0]
+        probe = time_swap_oracle((out_p[:64], None, in_p[:64], None), host_blocks, budget_s=0.5)
+        s_per_pair = probe["seconds"] / (probe["reps"] * probe["pairs"])
+        n_steps = args.warmup + args.steps
+        # pairs per step (out and in each) so that warmup + steps take about a minute
+        n = int(max(1, min(len(out_p), len(in_p), 60.0 / n_steps / s_per_pair / 2)))
+        step_pairs = (out_p[:n], None, in_p[:n], None)
+        for _ in range(args.warmup):
+            time_swap_oracle(step_pairs, host_blocks, budget_s=0.0)
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            time_swap_oracle(step_pairs, host_blocks, budget_s=0.0)
+        dt = time.perf_counter() - t0
+        value = round(args.steps * 2 * n * 2 * 4 * 16 * 128 * 2 / dt / 1e9, 4)
+        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world,
+                "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 4),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+                "data": "synthetic", "config": {"workload": WORKLOAD_DESCRIPTIONS[args.workload],
+                                                "name": args.workload},
+                "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                 "sample": f"{n} of {len(out_p)} pairs of swap step 1, out and in, per step; "
+                                           "oracle byte copy between two numpy pools", "cpu_model": cpu_model()},
+                "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+        print(json.dumps(line), flush=True)
+        return
     if args.workload.startswith("prefix_cow"):
         inp, tables, lens, slots, _, _ = prefix_batch(args.workload, rank_seed(args.seed, 0))
     else:
@@ -799,6 +1081,8 @@ def main(argv=None) -> None:
     try:
         if args.impl == "reference":
             run_reference(args, rank, world)
+        elif args.workload == "swap_qwen":
+            run_swap(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

@@ -109,6 +109,57 @@ int pa_copy_blocks(void* key_cache, void* value_cache, const int64_t* src_dst_pa
                    void* stream);
 
 /*
+ * pa_write_kv_layers — pa_write_kv for every layer of a model in one launch (the
+ * same slot_mapping in every layer: a sequence's physical blocks have the same ids
+ * in each layer's cache).  keys, values, key_caches, value_caches are HOST arrays
+ * of num_layers device pointers (read during the call; the memory they point to
+ * must stay valid until the stream has passed the call): layer l's key/value
+ * [num_tokens, H_kv, d] go into key_caches[l] / value_caches[l]
+ * [num_blocks, H_kv, bs, d] at the slots, exactly as pa_write_kv would.
+ * 1 <= num_layers <= PA_MAX_LAYERS.  A negative slot is skipped; a slot at or
+ * past num_blocks * block_size sets PA_ERR_BAD_SLOT in the device error word.
+ */
+#define PA_MAX_LAYERS 256
+int pa_write_kv_layers(const void* const* keys, const void* const* values, void* const* key_caches,
+                       void* const* value_caches, int num_layers, const int64_t* slot_mapping, int num_tokens,
+                       int num_kv_heads, int head_dim, int block_size, int num_blocks, int dtype, void* stream);
+
+/*
+ * pa_apply_table_deltas — apply a delta export (pa_pool_table_deltas) to a
+ * device block table: block_tables[row * max_blocks_per_seq + j] = block for
+ * every (row, j, block) of deltas [num_deltas, 3] int32.  deltas may be device
+ * memory or page-locked host memory (read directly, no staging copy).  A row
+ * outside [0, num_rows) or j outside [0, max_blocks_per_seq) is skipped and sets
+ * PA_ERR_BAD_TABLE in the device error word.  Launch it on the stream of the
+ * decode that reads the table: stream order keeps it after the previous decode.
+ */
+int pa_apply_table_deltas(int32_t* block_tables, int num_rows, int max_blocks_per_seq, const int32_t* deltas,
+                          int num_deltas, void* stream);
+
+/*
+ * pa_swap_blocks — swap-out / swap-in copy of whole blocks between two caches of
+ * the same block geometry (the vLLM and PagedAttention page's preemption; the
+ * LLM-inference page's swap of KV blocks to CPU memory and back).  For every
+ * (src, dst) row of block_pairs [num_pairs, 2] int64, block dst of dst_key_cache
+ * and dst_value_cache becomes a byte copy of block src of src_key_cache and
+ * src_value_cache (all kv heads, all slots; dtype gives only the element size).
+ *  - each cache and block_pairs may be device memory of the current device or
+ *    page-locked host memory the device can address (cudaHostAlloc, cudaHostRegister,
+ *    torch pin_memory); the kernel reads and writes host memory directly over
+ *    the host link, in one launch for all pairs.  Pageable host memory is
+ *    rejected (PA_ERR_INVALID_ARG);
+ *  - src ids index [0, src_num_blocks), dst ids [0, dst_num_blocks); a pair with
+ *    an id outside its pool is skipped and sets PA_ERR_BAD_TABLE in the device
+ *    error word; the dst ids of one call must be distinct;
+ *  - asynchronous on `stream`: host memory involved must stay allocated and
+ *    untouched by the host until the stream has passed the call.
+ * num_pairs == 0 is a no-op.
+ */
+int pa_swap_blocks(void* dst_key_cache, void* dst_value_cache, const void* src_key_cache,
+                   const void* src_value_cache, const int64_t* block_pairs, int num_pairs, int num_kv_heads,
+                   int head_dim, int block_size, int src_num_blocks, int dst_num_blocks, int dtype, void* stream);
+
+/*
  * pa_decode — single-step decode attention over the paged cache
  * (MiniPaged-Qwen, section 1 formula, sections 5.1-5.2 and 6.2; GQA mapping of
  * section 9.1).
@@ -303,12 +354,49 @@ int pa_seq_fork(pa_pool* pool, int64_t parent_id, int64_t* child_id);
 int pa_seq_release(pa_pool* pool, int64_t seq_id);
 int pa_seq_length(const pa_pool* pool, int64_t seq_id, int64_t* length);
 /*
+ * pa_seq_swap — move sequence seq_id from pool src to pool dst (preemption: the
+ * vLLM and PagedAttention page lets a request's physical blocks be released or
+ * migrated while its logical tokens are kept; the LLM-inference page swaps a
+ * request's KV blocks out to CPU memory and back in).  Typically one pool
+ * indexes the device caches and the other a pinned host copy of the same
+ * geometry; the call works either way round.
+ *  - every block of the sequence's table, in table order, gets a fresh block of
+ *    dst (LIFO) with the same fill; block_pairs [capacity, 2] int64 (host)
+ *    receives (src block, dst block) for each, *num_pairs their count;
+ *  - the sequence is then released in src (a block it shared stays there for
+ *    its other holders); in dst it is *new_seq_id, its blocks private;
+ *  - the caller copies the pairs' data with pa_swap_blocks before using either
+ *    side again.
+ * PA_ERR_POOL_EXHAUSTED (dst has fewer free blocks than the table), or
+ * PA_ERR_INVALID_ARG (block sizes differ, same pool, capacity too small):
+ * both pools unchanged.  PA_ERR_NOT_FOUND for an unknown id.
+ */
+int pa_seq_swap(pa_pool* src, pa_pool* dst, int64_t seq_id, int64_t* new_seq_id, int64_t* block_pairs,
+                int capacity, int* num_pairs);
+/*
  * Host export of block tables: tables [n, max_blocks] int32 (unused entries
  * -1) and lens [n] int32 for the given sequence ids.  PA_ERR_INVALID_ARG if a
  * table is wider than max_blocks.  The caller uploads them.
  */
 int pa_pool_block_tables(const pa_pool* pool, const int64_t* seq_ids, int n, int32_t* tables, int max_blocks,
                          int32_t* lens);
+/*
+ * pa_pool_table_deltas — host export of block-table changes only (MiniPaged-Qwen's
+ * closing notes: richer block metadata at lower host overhead).  Row i of a
+ * device-resident table holds sequence seq_ids[i]; that table is assumed to have
+ * received every earlier delta export of this pool, in order (pa_apply_table_deltas).
+ *  - deltas [capacity, 3] int32 (host) receives (row, logical block, physical
+ *    block) triples, *num_deltas their count; lens [n] int32 every row's length;
+ *  - a sequence exported into the row it held at its last export, with no other
+ *    sequence exported into that row since, sends only the entries that changed
+ *    (a copy-on-write tail) or were added (a new block); otherwise all its entries;
+ *  - entries past a table's end are not touched (the decode never reads them).
+ * PA_ERR_INVALID_ARG (the deltas do not fit, a sequence in two rows) or
+ * PA_ERR_NOT_FOUND: nothing exported and the pool unchanged.  Capacity
+ * n * max_blocks always suffices.
+ */
+int pa_pool_table_deltas(pa_pool* pool, const int64_t* seq_ids, int n, int32_t* deltas, int capacity,
+                         int* num_deltas, int32_t* lens);
 int pa_pool_num_free(const pa_pool* pool);
 int pa_pool_num_blocks(const pa_pool* pool);
 int pa_pool_block_size(const pa_pool* pool);

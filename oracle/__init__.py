@@ -167,6 +167,7 @@ def write_kv(key: np.ndarray, value: np.ndarray, key_cache: np.ndarray, value_ca
     value = np.ascontiguousarray(value)
     slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
     assert key.shape == (slots.size, hkv, head_dim) and value.shape == key.shape
+    assert key.dtype == value.dtype == key_cache.dtype == value_cache.dtype, "element types differ"
     assert key_cache.flags["C_CONTIGUOUS"] and value_cache.flags["C_CONTIGUOUS"]
     return lib.oracle_write_kv(_ptr(key), _ptr(value), _ptr(key_cache), _ptr(value_cache), _ptr(slots),
                                int(slots.size), hkv, head_dim, block_size, num_blocks, key_cache.itemsize)
@@ -180,6 +181,31 @@ def copy_blocks(key_cache: np.ndarray, value_cache: np.ndarray, pairs: np.ndarra
     block_bytes = key_cache.nbytes // num_blocks
     return lib.oracle_copy_blocks(_ptr(key_cache), _ptr(value_cache), _ptr(pairs), int(pairs.shape[0]),
                                   block_bytes, num_blocks)
+
+
+def write_kv_layers(keys, values, key_caches, value_caches, slot_mapping: np.ndarray) -> int:
+    """The paged write for every layer of a model: layer l's rows ``keys[l]`` / ``values[l]`` go into
+    ``key_caches[l]`` / ``value_caches[l]`` at the shared ``slot_mapping`` (a sequence's blocks are the
+    same physical ids in every layer's cache).  Returns the first non-OK oracle status, else OK."""
+    status = OK
+    for k, v, kc, vc in zip(keys, values, key_caches, value_caches):
+        st = write_kv(k, v, kc, vc, slot_mapping)
+        status = st if status == OK else status
+    return status
+
+
+def apply_table_deltas(block_tables: np.ndarray, deltas: np.ndarray) -> int:
+    """Apply block-table deltas in place: every (row, logical block, physical block) row of ``deltas``
+    sets ``block_tables[row, logical block]``; a row or column outside the table is skipped and
+    reported (BAD_TABLE)."""
+    status = OK
+    rows, width = block_tables.shape
+    for row, j, block in np.asarray(deltas, dtype=np.int64).reshape(-1, 3).tolist():
+        if 0 <= row < rows and 0 <= j < width:
+            block_tables[row, j] = block
+        else:
+            status = BAD_TABLE
+    return status
 
 
 def swap_blocks(dst_key: np.ndarray, dst_value: np.ndarray, src_key: np.ndarray, src_value: np.ndarray,

@@ -31,7 +31,17 @@ Additions where that page is silent (each one a stated reading):
   source pool (so a block it shared stays there for the other holders).  The
   moved blocks are private (sharing is not carried across a swap).  The
   destination names the sequence with its own next id.  Too few free blocks in
-  the destination raise ``MemoryError`` with both pools unchanged.
+  the destination raise ``MemoryError`` with both pools unchanged;
+* table deltas (the MiniPaged-Qwen page's closing notes ask for richer block
+  metadata at lower host overhead): instead of every table entry, an export
+  names only the entries a device-resident copy of the tables lacks (one copy,
+  which receives every export in order).  The pool remembers, per sequence, the
+  row it was last exported to and its table then, and per row the sequence last
+  exported into it; exporting a sequence into the row that still holds it
+  yields the entries that changed or were added since (a copy-on-write replaces
+  the tail entry, an append past a full block adds one); exporting it into any
+  other row, or for the first time, yields all of its entries.  Entries past a
+  table's end are never read by the decode, so stale ones are left in place.
 """
 from __future__ import annotations
 
@@ -112,6 +122,8 @@ class SequencePool:
         self.pool = BlockPool(num_blocks, block_size, free_order)
         self.tables: Dict[int, List[int]] = {}
         self.lens: Dict[int, int] = {}
+        self.synced: Dict[int, Tuple[int, List[int]]] = {}  # sequence -> (row, table) at its last delta export
+        self.row_owner: Dict[int, int] = {}  # row -> sequence last exported into it
         self._next_id = 0
 
     @property
@@ -140,6 +152,26 @@ class SequencePool:
     def release(self, sid: int) -> None:
         self.pool.release(self.tables.pop(sid))
         del self.lens[sid]
+        self.synced.pop(sid, None)
+
+    def table_deltas(self, seq_ids: Sequence[int]):
+        """Delta export for rows ``0..n-1`` holding ``seq_ids``: ([(row, logical block, physical block)],
+        [length per row])."""
+        if len(set(seq_ids)) != len(seq_ids):
+            raise ValueError("a sequence in two rows")
+        deltas, lens = [], []
+        for row, sid in enumerate(seq_ids):
+            table = self.tables[sid]
+            last_row, last = self.synced.get(sid, (-1, []))
+            if last_row != row or self.row_owner.get(row) != sid:
+                last = []  # the row holds someone else's entries: send every entry
+            for j, block in enumerate(table):
+                if j >= len(last) or last[j] != block:
+                    deltas.append((row, j, block))
+            self.synced[sid] = (row, list(table))
+            self.row_owner[row] = sid
+            lens.append(self.lens[sid])
+        return deltas, lens
 
     def swap_to(self, dst: "SequencePool", sid: int):
         """Move sequence ``sid`` into pool ``dst``; returns (its id there, [(src block, dst block)])."""

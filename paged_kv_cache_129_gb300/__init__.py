@@ -8,6 +8,7 @@ from .binding import (  # noqa: F401
     STATIC_SCRATCH_BYTES,
     LIB_PATH,
     BlockPool,
+    apply_table_deltas,
     DecodePlan,
     PAError,
     PoolExhausted,
@@ -21,8 +22,10 @@ from .binding import (  # noqa: F401
     decode_static_scratch,
     decode_workspace_size,
     library,
+    swap_blocks,
     version,
     write_kv,
+    write_kv_layers,
 )
 
 

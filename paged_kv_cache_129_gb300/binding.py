@@ -59,6 +59,9 @@ _SIGNATURES = [
     ("pa_check_error", _I, [_P]),
     ("pa_write_kv", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     ("pa_copy_blocks", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    ("pa_swap_blocks", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
+    ("pa_write_kv_layers", _I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P]),
+    ("pa_apply_table_deltas", _I, [_P, _I, _I, _P, _I, _P]),
     ("pa_decode", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
     ("pa_decode_ex", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _I, _I, _I, _P]),
     ("pa_decode_append", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _I, _I, _I,
@@ -77,7 +80,9 @@ _SIGNATURES = [
     ("pa_seq_fork", _I, [_P, _I64, ctypes.POINTER(_I64)]),
     ("pa_seq_release", _I, [_P, _I64]),
     ("pa_seq_length", _I, [_P, _I64, ctypes.POINTER(_I64)]),
+    ("pa_seq_swap", _I, [_P, _P, _I64, ctypes.POINTER(_I64), _P, _I, ctypes.POINTER(_I)]),
     ("pa_pool_block_tables", _I, [_P, _P, _I, _P, _I, _P]),
+    ("pa_pool_table_deltas", _I, [_P, _P, _I, _P, _I, ctypes.POINTER(_I), _P]),
     ("pa_pool_num_free", _I, [_P]),
     ("pa_pool_num_blocks", _I, [_P]),
     ("pa_pool_block_size", _I, [_P]),
@@ -171,6 +176,74 @@ def copy_blocks(key_cache: torch.Tensor, value_cache: torch.Tensor, src_dst_pair
     _check(library().pa_copy_blocks(key_cache.data_ptr(), value_cache.data_ptr(), src_dst_pairs.data_ptr(),
                                     src_dst_pairs.numel() // 2, hkv, d, bs, num_blocks, _dtype_code(key_cache),
                                     _stream_ptr(stream, key_cache.device)))
+
+
+def write_kv_layers(keys, values, key_caches, value_caches, slot_mapping: torch.Tensor, stream=None) -> None:
+    """``pa_write_kv_layers``: ``pa_write_kv`` for every layer in one launch.  ``keys`` / ``values`` are
+    sequences of per-layer ``[T, H_kv, d]`` tensors, ``key_caches`` / ``value_caches`` of per-layer
+    ``[N, H_kv, bs, d]`` caches; ``slot_mapping`` (int64 [T]) is shared by all layers."""
+    n = len(keys)
+    _need(n >= 1 and len(values) == n and len(key_caches) == n and len(value_caches) == n,
+          "one key, value, key cache and value cache per layer")
+    _cuda(slot_mapping, "slot_mapping")
+    _need(slot_mapping.dtype == torch.int64 and slot_mapping.dim() == 1, "slot_mapping: int64 [T]")
+    kc0 = key_caches[0]
+    _need(kc0.dim() == 4, "caches must be [N, H_kv, bs, d]")
+    num_blocks, hkv, bs, d = kc0.shape
+    for l in range(n):
+        for name, t in (("key", keys[l]), ("value", values[l]), ("key_cache", key_caches[l]),
+                        ("value_cache", value_caches[l])):
+            _cuda(t, f"{name}[{l}]")
+            _need(t.dtype == kc0.dtype, "dtypes must match")
+        _need(key_caches[l].shape == kc0.shape and value_caches[l].shape == kc0.shape, "caches differ in shape")
+        _need(keys[l].shape == values[l].shape == (slot_mapping.numel(), hkv, d), "key/value must be [T, H_kv, d]")
+    arr = ctypes.c_void_p * n
+    _check(library().pa_write_kv_layers(arr(*[t.data_ptr() for t in keys]), arr(*[t.data_ptr() for t in values]),
+                                        arr(*[t.data_ptr() for t in key_caches]),
+                                        arr(*[t.data_ptr() for t in value_caches]), n, slot_mapping.data_ptr(),
+                                        slot_mapping.numel(), hkv, d, bs, num_blocks, _dtype_code(kc0),
+                                        _stream_ptr(stream, kc0.device)))
+
+
+def apply_table_deltas(block_tables: torch.Tensor, deltas: torch.Tensor, num_deltas: Optional[int] = None,
+                       stream=None) -> None:
+    """``pa_apply_table_deltas``: ``block_tables[row, j] = block`` for the first ``num_deltas`` (default all)
+    (row, j, block) rows of ``deltas`` (int32 [n, 3], a CUDA tensor or pinned host memory)."""
+    _cuda(block_tables, "block_tables")
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2, "block_tables: int32 [rows, max_blocks]")
+    _need(deltas.dtype == torch.int32 and deltas.is_contiguous() and deltas.numel() % 3 == 0, "deltas: int32 [n, 3]")
+    _need(deltas.is_cuda or deltas.is_pinned(), "deltas must be a CUDA tensor or pinned host memory")
+    n = deltas.numel() // 3 if num_deltas is None else int(num_deltas)
+    _need(0 <= n <= deltas.numel() // 3, "num_deltas out of range")
+    with torch.cuda.device(block_tables.device):
+        _check(library().pa_apply_table_deltas(block_tables.data_ptr(), block_tables.shape[0], block_tables.shape[1],
+                                               deltas.data_ptr(), n, _stream_ptr(stream, block_tables.device)))
+
+
+def swap_blocks(dst_key_cache: torch.Tensor, dst_value_cache: torch.Tensor, src_key_cache: torch.Tensor,
+                src_value_cache: torch.Tensor, block_pairs: torch.Tensor, stream=None) -> None:
+    """``pa_swap_blocks``: block dst of the dst caches <- block src of the src caches for every (src, dst)
+    row of ``block_pairs`` (int64 [n, 2]).  Each tensor is a CUDA tensor or a pinned CPU tensor
+    (``pin_memory()``); the copy runs on the current CUDA device's stream."""
+    tensors = (("dst_key_cache", dst_key_cache), ("dst_value_cache", dst_value_cache),
+               ("src_key_cache", src_key_cache), ("src_value_cache", src_value_cache), ("block_pairs", block_pairs))
+    for name, t in tensors:
+        _need(t.is_contiguous(), f"{name} must be contiguous")
+        _need(t.is_cuda or t.is_pinned(), f"{name} must be a CUDA tensor or pinned host memory")
+    _need(dst_key_cache.dim() == 4 and dst_value_cache.shape == dst_key_cache.shape, "dst caches: [N, H_kv, bs, d]")
+    _need(src_key_cache.dim() == 4 and src_value_cache.shape == src_key_cache.shape, "src caches: [N, H_kv, bs, d]")
+    _need(src_key_cache.shape[1:] == dst_key_cache.shape[1:], "caches differ in block geometry")
+    _need(len({t.dtype for _, t in tensors[:4]}) == 1, "cache dtypes must match")
+    _need(block_pairs.dtype == torch.int64 and block_pairs.numel() % 2 == 0, "block_pairs: int64 [n, 2]")
+    cuda = [t.device for _, t in tensors if t.is_cuda]
+    device = cuda[0] if cuda else torch.device("cuda", torch.cuda.current_device())
+    _, hkv, bs, d = src_key_cache.shape
+    with torch.cuda.device(device):
+        _check(library().pa_swap_blocks(dst_key_cache.data_ptr(), dst_value_cache.data_ptr(),
+                                        src_key_cache.data_ptr(), src_value_cache.data_ptr(), block_pairs.data_ptr(),
+                                        block_pairs.numel() // 2, hkv, d, bs, src_key_cache.shape[0],
+                                        dst_key_cache.shape[0], _dtype_code(src_key_cache),
+                                        _stream_ptr(stream, device)))
 
 
 def decode_plan(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
@@ -408,6 +481,18 @@ class BlockPool:
     def release(self, seq_id: int) -> None:
         _check(self._lib.pa_seq_release(self._h, seq_id))
 
+    def swap_to(self, dst: "BlockPool", seq_id: int):
+        """Move a sequence into pool ``dst``: returns (its id there, int64 [n, 2] numpy (src block, dst block)
+        pairs for ``swap_blocks``)."""
+        import numpy as np
+
+        n = self.length(seq_id)
+        pairs = np.empty((max((n + self.block_size - 1) // self.block_size, 1), 2), dtype=np.int64)
+        new_id, k = _I64(), _I()
+        _check(self._lib.pa_seq_swap(self._h, dst._h, seq_id, ctypes.byref(new_id), pairs.ctypes.data,
+                                     pairs.shape[0], ctypes.byref(k)))
+        return new_id.value, pairs[:k.value].copy()
+
     def length(self, seq_id: int) -> int:
         n = _I64()
         _check(self._lib.pa_seq_length(self._h, seq_id, ctypes.byref(n)))
@@ -423,6 +508,24 @@ class BlockPool:
         _check(self._lib.pa_pool_block_tables(self._h, ids.ctypes.data, ids.size, tables.ctypes.data, max_blocks,
                                               lens.ctypes.data))
         return tables, lens
+
+    def table_deltas(self, seq_ids, out=None, lens_out=None):
+        """Delta export (``pa_pool_table_deltas``) for rows holding ``seq_ids``: returns (deltas int32 [k, 3],
+        lens int32 [n]) as numpy views of ``out`` / ``lens_out`` when given (e.g. pinned staging), else new
+        arrays."""
+        import numpy as np
+
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        if out is None:
+            cap = sum((self.length(int(s)) + self.block_size - 1) // self.block_size for s in ids)
+            out = np.empty((max(cap, 1), 3), dtype=np.int32)
+        if lens_out is None:
+            lens_out = np.empty(ids.size, dtype=np.int32)
+        assert out.dtype == np.int32 and out.flags["C_CONTIGUOUS"] and lens_out.dtype == np.int32
+        k = _I()
+        _check(self._lib.pa_pool_table_deltas(self._h, ids.ctypes.data, ids.size, out.ctypes.data, out.size // 3,
+                                              ctypes.byref(k), lens_out.ctypes.data))
+        return out.reshape(-1, 3)[:k.value], lens_out[:ids.size]
 
     def num_free(self) -> int:
         return self._lib.pa_pool_num_free(self._h)

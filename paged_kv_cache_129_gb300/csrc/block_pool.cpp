@@ -8,6 +8,21 @@
 // Instead of the simulation's token lists the pool keeps a fill count per
 // block, which is all the allocation decisions need.
 //
+// Swap (preemption, on the same page: a request's physical blocks are released
+// or migrated while its logical tokens are kept) moves a sequence to another pool
+// of the same block size, e.g. one that stands for pinned host memory: every
+// block of its table gets a fresh private block there holding the same tokens,
+// then the sequence is released in the source pool.  The caller copies the
+// returned (source block, destination block) pairs with pa_swap_blocks.
+//
+// Table deltas (MiniPaged-Qwen's closing notes: richer block metadata at lower
+// host overhead): pa_pool_table_deltas names only the (row, logical block,
+// physical block) entries a device-resident copy of the tables lacks, given
+// that copy received every earlier export in order.  The pool remembers per
+// sequence the row and table of its last export and per row the sequence last
+// exported into it: a sequence still in its row sends the entries that changed
+// or were added; one in another row, or new, sends all of them.
+//
 // Every failing call leaves the pool exactly as it was: single appends check
 // before mutating; batch appends keep an undo log.
 #include <algorithm>
@@ -24,6 +39,8 @@ struct pa_pool {
     struct Seq {
         std::vector<int32_t> table;
         int64_t length = 0;
+        int synced_row = -1;                // row of its last delta export (-1: never)
+        std::vector<int32_t> synced_table;  // its table as of that export
     };
     int num_blocks = 0;
     int block_size = 0;
@@ -31,6 +48,7 @@ struct pa_pool {
     std::vector<int32_t> refs;       // per block; 0 = free
     std::vector<int32_t> fill;       // tokens stored in the block
     std::unordered_map<int64_t, Seq> seqs;
+    std::unordered_map<int, int64_t> row_owner;  // device table row -> sequence last exported into it
     int64_t next_id = 0;
 };
 
@@ -207,6 +225,8 @@ int pa_seq_fork(pa_pool* pool, int64_t parent_id, int64_t* child_id) {
     const pa_pool::Seq* parent = find_seq(pool, parent_id);
     if (!parent) return pa::fail(PA_ERR_NOT_FOUND, "pa_seq_fork: unknown sequence %lld", (long long)parent_id);
     pa_pool::Seq child = *parent;  // copy before emplace may rehash
+    child.synced_row = -1;         // the child has never been exported
+    child.synced_table.clear();
     for (int32_t b : child.table) pool->refs[b] += 1;
     const int64_t id = pool->next_id++;
     pool->seqs.emplace(id, std::move(child));
@@ -227,11 +247,97 @@ int pa_seq_release(pa_pool* pool, int64_t seq_id) {
     return PA_OK;
 }
 
+int pa_seq_swap(pa_pool* src, pa_pool* dst, int64_t seq_id, int64_t* new_seq_id, int64_t* block_pairs,
+                int capacity, int* num_pairs) {
+    if (!src || !dst || !new_seq_id || !num_pairs || capacity < 0 || (capacity > 0 && !block_pairs))
+        return pa::fail(PA_ERR_INVALID_ARG, "pa_seq_swap: bad arguments");
+    if (src == dst) return pa::fail(PA_ERR_INVALID_ARG, "pa_seq_swap: source and destination are the same pool");
+    if (src->block_size != dst->block_size)
+        return pa::fail(PA_ERR_INVALID_ARG, "pa_seq_swap: block sizes differ (%d vs %d)", src->block_size,
+                        dst->block_size);
+    auto it = src->seqs.find(seq_id);
+    if (it == src->seqs.end())
+        return pa::fail(PA_ERR_NOT_FOUND, "pa_seq_swap: unknown sequence %lld", (long long)seq_id);
+    const std::vector<int32_t>& table = it->second.table;
+    const int n = static_cast<int>(table.size());
+    if (n > capacity)
+        return pa::fail(PA_ERR_INVALID_ARG, "pa_seq_swap: %d pairs do not fit in %d", n, capacity);
+    if (static_cast<int>(dst->free_list.size()) < n)
+        return pa::fail(PA_ERR_POOL_EXHAUSTED, "pa_seq_swap: destination has %zu free blocks, sequence needs %d",
+                        dst->free_list.size(), n);
+    pa_pool::Seq moved;
+    moved.length = it->second.length;
+    moved.table.reserve(n);
+    for (int j = 0; j < n; ++j) {
+        const int32_t b = take_block(dst);
+        dst->fill[b] = src->fill[table[j]];
+        moved.table.push_back(b);
+        block_pairs[2 * j] = table[j];
+        block_pairs[2 * j + 1] = b;
+    }
+    const int64_t id = dst->next_id++;
+    dst->seqs.emplace(id, std::move(moved));
+    for (int32_t b : it->second.table) {
+        src->refs[b] -= 1;
+        if (src->refs[b] == 0) give_back(src, b);
+    }
+    src->seqs.erase(it);
+    *new_seq_id = id;
+    *num_pairs = n;
+    return PA_OK;
+}
+
 int pa_seq_length(const pa_pool* pool, int64_t seq_id, int64_t* length) {
     if (!pool || !length) return pa::fail(PA_ERR_INVALID_ARG, "pa_seq_length: NULL argument");
     const pa_pool::Seq* s = find_seq(pool, seq_id);
     if (!s) return pa::fail(PA_ERR_NOT_FOUND, "pa_seq_length: unknown sequence %lld", (long long)seq_id);
     *length = s->length;
+    return PA_OK;
+}
+
+int pa_pool_table_deltas(pa_pool* pool, const int64_t* seq_ids, int n, int32_t* deltas, int capacity,
+                         int* num_deltas, int32_t* lens) {
+    if (!pool || n < 0 || capacity < 0 || !num_deltas || (n > 0 && (!seq_ids || !lens)) ||
+        (capacity > 0 && !deltas))
+        return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_table_deltas: bad arguments");
+    // count first, so that a failure changes nothing
+    int64_t count = 0;
+    for (int i = 0; i < n; ++i) {
+        const pa_pool::Seq* s = find_seq(pool, seq_ids[i]);
+        if (!s)
+            return pa::fail(PA_ERR_NOT_FOUND, "pa_pool_table_deltas: unknown sequence %lld", (long long)seq_ids[i]);
+        for (int j = i + 1; j < n; ++j)
+            if (seq_ids[j] == seq_ids[i])
+                return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_table_deltas: sequence %lld in two rows",
+                                (long long)seq_ids[i]);
+        if (s->length > INT32_MAX) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_table_deltas: length > int32");
+        auto owner = pool->row_owner.find(i);
+        const bool kept = s->synced_row == i && owner != pool->row_owner.end() && owner->second == seq_ids[i];
+        for (size_t j = 0; j < s->table.size(); ++j)
+            if (!kept || j >= s->synced_table.size() || s->synced_table[j] != s->table[j]) ++count;
+    }
+    if (count > capacity)
+        return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_table_deltas: %lld deltas do not fit in %d", (long long)count,
+                        capacity);
+    int k = 0;
+    for (int i = 0; i < n; ++i) {
+        pa_pool::Seq* s = find_seq(pool, seq_ids[i]);
+        auto owner = pool->row_owner.find(i);
+        const bool kept = s->synced_row == i && owner != pool->row_owner.end() && owner->second == seq_ids[i];
+        for (size_t j = 0; j < s->table.size(); ++j) {
+            if (!kept || j >= s->synced_table.size() || s->synced_table[j] != s->table[j]) {
+                deltas[3 * k] = i;
+                deltas[3 * k + 1] = static_cast<int32_t>(j);
+                deltas[3 * k + 2] = s->table[j];
+                ++k;
+            }
+        }
+        s->synced_row = i;
+        s->synced_table = s->table;
+        pool->row_owner[i] = seq_ids[i];
+        lens[i] = static_cast<int32_t>(s->length);
+    }
+    *num_deltas = k;
     return PA_OK;
 }
 

@@ -408,6 +408,149 @@ int pa_copy_blocks(void* key_cache, void* value_cache, const int64_t* src_dst_pa
     return PA_OK;
 }
 
+namespace {
+
+// The address at which the current device reaches p: device memory of that device as is,
+// page-locked host memory through its device mapping.  Pageable host memory and memory of
+// another device are refused.
+int device_address(const void* p, int device, const char* what, const void** out) {
+    cudaPointerAttributes at{};
+    cudaError_t e = cudaPointerGetAttributes(&at, p);
+    if (e != cudaSuccess) {
+        cudaGetLastError();
+        return fail(PA_ERR_INVALID_ARG, "%s is not memory the CUDA runtime knows (%s)", what,
+                    cudaGetErrorName(e));
+    }
+    switch (at.type) {
+        case cudaMemoryTypeDevice:
+            if (at.device != device)
+                return fail(PA_ERR_INVALID_ARG, "%s is memory of device %d, not of the current %d",
+                            what, at.device, device);
+            *out = p;
+            return PA_OK;
+        case cudaMemoryTypeManaged:
+            *out = p;
+            return PA_OK;
+        case cudaMemoryTypeHost:
+            if (!at.devicePointer)
+                return fail(PA_ERR_INVALID_ARG, "%s is page-locked but not mapped for the device", what);
+            *out = at.devicePointer;
+            return PA_OK;
+        default:
+            return fail(PA_ERR_INVALID_ARG,
+                        "%s is pageable host memory; page-lock it (cudaHostAlloc, cudaHostRegister)",
+                        what);
+    }
+}
+
+}  // namespace
+
+static_assert(PA_MAX_LAYERS == kMaxLayers, "the header's layer limit is the kernel's");
+
+int pa_write_kv_layers(const void* const* keys, const void* const* values, void* const* key_caches,
+                       void* const* value_caches, int num_layers, const int64_t* slot_mapping, int num_tokens,
+                       int num_kv_heads, int head_dim, int block_size, int num_blocks, int dtype, void* stream) {
+    clear_error();
+    if (!dtype_ok(dtype)) return fail(PA_ERR_INVALID_ARG, "pa_write_kv_layers: unknown dtype %d", dtype);
+    if (num_layers < 1 || num_layers > kMaxLayers)
+        return fail(PA_ERR_INVALID_ARG, "pa_write_kv_layers: num_layers=%d outside [1, %d]", num_layers, kMaxLayers);
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
+        return fail(PA_ERR_INVALID_ARG, "pa_write_kv_layers: bad sizes");
+    if (!keys || !values || !key_caches || !value_caches)
+        return fail(PA_ERR_INVALID_ARG, "pa_write_kv_layers: NULL pointer array");
+    if (num_tokens == 0) return PA_OK;
+    if (!slot_mapping || !aligned(slot_mapping, 8))
+        return fail(PA_ERR_INVALID_ARG, "pa_write_kv_layers: slot_mapping must be non-NULL and 8-byte aligned");
+    const int eb = elem_bytes(dtype);
+    LayerPtrs ptrs;
+    for (int l = 0; l < num_layers; ++l) {
+        if (!keys[l] || !values[l] || !key_caches[l] || !value_caches[l])
+            return fail(PA_ERR_INVALID_ARG, "pa_write_kv_layers: NULL pointer for layer %d", l);
+        if (!aligned(keys[l], eb) || !aligned(values[l], eb) || !aligned(key_caches[l], eb) ||
+            !aligned(value_caches[l], eb))
+            return fail(PA_ERR_INVALID_ARG, "pa_write_kv_layers: layer %d buffers not aligned to the element size", l);
+        ptrs.key[l] = keys[l];
+        ptrs.value[l] = values[l];
+        ptrs.key_cache[l] = key_caches[l];
+        ptrs.value_cache[l] = value_caches[l];
+    }
+    DeviceState* dev = nullptr;
+    int st = current_device_state(&dev);
+    if (st != PA_OK) return st;
+    WriteLayersArgs a{&ptrs, num_layers, slot_mapping, num_tokens, num_kv_heads, head_dim, block_size, num_blocks, eb,
+                      dev->error_word};
+    cudaError_t e = write_kv_layers_launch(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pa_write_kv_layers launch");
+    return PA_OK;
+}
+
+int pa_apply_table_deltas(int32_t* block_tables, int num_rows, int max_blocks_per_seq, const int32_t* deltas,
+                          int num_deltas, void* stream) {
+    clear_error();
+    if (num_rows < 0 || max_blocks_per_seq < 0 || num_deltas < 0)
+        return fail(PA_ERR_INVALID_ARG, "pa_apply_table_deltas: bad sizes");
+    if (num_deltas == 0) return PA_OK;
+    if (!block_tables || !deltas) return fail(PA_ERR_INVALID_ARG, "pa_apply_table_deltas: NULL pointer");
+    if (!aligned(block_tables, 4) || !aligned(deltas, 4))
+        return fail(PA_ERR_INVALID_ARG, "pa_apply_table_deltas: tables and deltas must be 4-byte aligned");
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    const void* dd = nullptr;
+    const void* tt = nullptr;
+    int st = device_address(deltas, device, "deltas", &dd);
+    if (st == PA_OK) st = device_address(block_tables, device, "block_tables", &tt);
+    if (st != PA_OK) return st;
+    DeviceState* dev = nullptr;
+    st = current_device_state(&dev);
+    if (st != PA_OK) return st;
+    DeltaArgs a{static_cast<int32_t*>(const_cast<void*>(tt)), num_rows, max_blocks_per_seq,
+                static_cast<const int32_t*>(dd), num_deltas, dev->error_word};
+    e = apply_table_deltas_launch(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pa_apply_table_deltas launch");
+    return PA_OK;
+}
+
+int pa_swap_blocks(void* dst_key_cache, void* dst_value_cache, const void* src_key_cache, const void* src_value_cache,
+                   const int64_t* block_pairs, int num_pairs, int num_kv_heads, int head_dim, int block_size,
+                   int src_num_blocks, int dst_num_blocks, int dtype, void* stream) {
+    clear_error();
+    if (!dtype_ok(dtype)) return fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: unknown dtype %d", dtype);
+    if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || src_num_blocks < 0 ||
+        dst_num_blocks < 0)
+        return fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: bad sizes");
+    if (num_pairs == 0) return PA_OK;
+    if (!dst_key_cache || !dst_value_cache || !src_key_cache || !src_value_cache || !block_pairs)
+        return fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: NULL pointer");
+    if (!aligned(block_pairs, 8)) return fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: pairs must be 8-byte aligned");
+    const int eb = elem_bytes(dtype);
+    if (!aligned(dst_key_cache, eb) || !aligned(dst_value_cache, eb) || !aligned(src_key_cache, eb) ||
+        !aligned(src_value_cache, eb))
+        return fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: caches must be aligned to the element size");
+    int device = 0;
+    cudaError_t e = cudaGetDevice(&device);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    const void* dk = nullptr;
+    const void* dv = nullptr;
+    const void* sk = nullptr;
+    const void* sv = nullptr;
+    const void* pr = nullptr;
+    int st = device_address(dst_key_cache, device, "dst_key_cache", &dk);
+    if (st == PA_OK) st = device_address(dst_value_cache, device, "dst_value_cache", &dv);
+    if (st == PA_OK) st = device_address(src_key_cache, device, "src_key_cache", &sk);
+    if (st == PA_OK) st = device_address(src_value_cache, device, "src_value_cache", &sv);
+    if (st == PA_OK) st = device_address(block_pairs, device, "block_pairs", &pr);
+    if (st != PA_OK) return st;
+    DeviceState* dev = nullptr;
+    st = current_device_state(&dev);
+    if (st != PA_OK) return st;
+    SwapArgs a{const_cast<void*>(dk), const_cast<void*>(dv), sk, sv, static_cast<const int64_t*>(pr), num_pairs,
+               num_kv_heads, head_dim, block_size, src_num_blocks, dst_num_blocks, eb, dev->num_sms, dev->error_word};
+    e = swap_blocks_launch(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pa_swap_blocks launch");
+    return PA_OK;
+}
+
 int pa_decode_make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
                         int max_blocks_per_seq, int dtype, size_t workspace_bytes, int max_context_len,
                         int partition_pages, int kernel, pa_decode_plan* out) {

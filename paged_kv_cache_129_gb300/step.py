@@ -47,11 +47,21 @@ class DecodeStepper:
     and, in append mode, ``new_key`` / ``new_value``), call ``launch(i)``, and
     ``result(i)`` returns the host view of step i's output once it has arrived.
     Step i uses slot ``i % slots``: refill that slot only after ``result(i)``.
+
+    With ``tables="deltas"`` the block tables live on the device
+    (``device_block_tables``, all -1 at first) and a step uploads only their
+    changes: fill ``inputs(i).deltas`` with the pool's delta export
+    (``BlockPool.table_deltas(seq_ids, out=inputs(i).deltas.numpy(),
+    lens_out=inputs(i).context_lens.numpy())``) and pass its count to
+    ``launch(i, num_deltas=k)``.  The deltas are applied on the decode's
+    stream just before the decode, so stream order keeps them after the
+    previous step's decode has read the table.
     """
 
     def __init__(self, key_cache: torch.Tensor, value_cache: torch.Tensor, num_seqs: int, num_heads: int,
                  max_blocks_per_seq: int, scale: Optional[float] = None, append: bool = True, slots: int = 2,
-                 max_context_len: int = 0, partition_pages: int = 0, kernel: str = "auto"):
+                 max_context_len: int = 0, partition_pages: int = 0, kernel: str = "auto", tables: str = "full"):
+        assert tables in ("full", "deltas")
         assert key_cache.is_cuda and key_cache.shape == value_cache.shape and key_cache.dim() == 4
         self.device = key_cache.device
         self.key_cache, self.value_cache = key_cache, value_cache
@@ -64,9 +74,18 @@ class DecodeStepper:
         fields = [("query", (num_seqs, num_heads, d), dt)]
         if append:
             fields += [("new_key", (num_seqs, hkv, d), dt), ("new_value", (num_seqs, hkv, d), dt)]
-        fields += [("block_tables", (num_seqs, max_blocks_per_seq), torch.int32),
-                   ("context_lens", (num_seqs,), torch.int32)]
+        self.deltas_mode = tables == "deltas"
+        if self.deltas_mode:
+            # the deltas go last, so that a step uploads only the prefix it uses
+            fields += [("context_lens", (num_seqs,), torch.int32),
+                       ("deltas", (num_seqs * max_blocks_per_seq, 3), torch.int32)]
+            self.device_block_tables = torch.full((num_seqs, max_blocks_per_seq), -1, dtype=torch.int32,
+                                                  device=self.device)
+        else:
+            fields += [("block_tables", (num_seqs, max_blocks_per_seq), torch.int32),
+                       ("context_lens", (num_seqs,), torch.int32)]
         self._in, self._in_bytes = _layout(fields)
+        self._last_h2d = self._in_bytes
         self._out, self._out_bytes = _layout([("out", (num_seqs, num_heads, d), dt)])
         self._h_in = [torch.empty(self._in_bytes, dtype=torch.uint8).pin_memory() for _ in range(slots)]
         self._d_in = [torch.empty(self._in_bytes, dtype=torch.uint8, device=self.device) for _ in range(slots)]
@@ -102,14 +121,15 @@ class DecodeStepper:
             stream = int(self.compute.cuda_stream)
             code = binding._dtype_code(kc)
             kern = binding.KERNELS[self.kernel]
+            tables = self.device_block_tables if self.deltas_mode else dv.block_tables
             if self.append:
                 args = [out.data_ptr(), dv.query.data_ptr(), dv.new_key.data_ptr(), dv.new_value.data_ptr(),
-                        kc.data_ptr(), vc.data_ptr(), dv.block_tables.data_ptr(), dv.context_lens.data_ptr(),
+                        kc.data_ptr(), vc.data_ptr(), tables.data_ptr(), dv.context_lens.data_ptr(),
                         num_seqs, num_heads, hkv, d, bs, max_blocks, num_blocks, self.scale, code, ws_ptr,
                         ws_bytes, self.max_context_len, self.partition_pages, kern, stream]
             else:
                 args = [out.data_ptr(), dv.query.data_ptr(), kc.data_ptr(), vc.data_ptr(),
-                        dv.block_tables.data_ptr(), dv.context_lens.data_ptr(), num_seqs, num_heads, hkv, d, bs,
+                        tables.data_ptr(), dv.context_lens.data_ptr(), num_seqs, num_heads, hkv, d, bs,
                         max_blocks, num_blocks, self.scale, code, ws_ptr, ws_bytes, self.max_context_len,
                         self.partition_pages, kern, stream]
             self._args[key] = args
@@ -117,7 +137,8 @@ class DecodeStepper:
 
     @property
     def h2d_bytes(self) -> int:
-        return self._in_bytes
+        """Bytes the last launch uploaded (the whole staging area unless deltas are used)."""
+        return self._last_h2d
 
     @property
     def d2h_bytes(self) -> int:
@@ -128,7 +149,7 @@ class DecodeStepper:
         return self._hv_in[i % self.slots]
 
     def launch(self, i: int, key_cache: Optional[torch.Tensor] = None,
-               value_cache: Optional[torch.Tensor] = None) -> None:
+               value_cache: Optional[torch.Tensor] = None, num_deltas: int = 0) -> None:
         """Upload slot i % slots, decode it on the current stream, download its output.
 
         Three streams: the upload of a slot waits until the slot's previous decode has read
@@ -142,15 +163,26 @@ class DecodeStepper:
         up, comp, down = self.upload, self.compute, self.download
         if self._used[s]:
             up.wait_event(self._decoded[s])
+        nbytes = self._in_bytes
+        if self.deltas_mode:
+            off, shape, _, _ = self._in["deltas"]
+            assert 0 <= num_deltas <= shape[0], "num_deltas out of range"
+            nbytes = off + 12 * num_deltas
         torch.cuda.set_stream(up)
         try:
-            self._d_in[s].copy_(self._h_in[s], non_blocking=True)
+            self._d_in[s][:nbytes].copy_(self._h_in[s][:nbytes], non_blocking=True)
         finally:
             torch.cuda.set_stream(comp)
+        self._last_h2d = nbytes
         self._uploaded[s].record(up)
         comp.wait_event(self._uploaded[s])
         if self._used[s]:
             comp.wait_event(self._downloaded[s])
+        if self.deltas_mode and num_deltas:
+            t = self.device_block_tables
+            binding._check(self._lib.pa_apply_table_deltas(t.data_ptr(), t.shape[0], t.shape[1],
+                                                           self._dv_in[s].deltas.data_ptr(), num_deltas,
+                                                           int(comp.cuda_stream)))
         args = self._call_args(s, kc, vc)
         status = (self._lib.pa_decode_append if self.append else self._lib.pa_decode_ex)(*args)
         binding._check(status)

@@ -94,3 +94,28 @@ def test_verify_setup_slots_are_the_last_q_len_positions():
         for t in range(4):
             pos = int(lens[b]) - 4 + t
             assert slots[b * 4 + t] == int(tables[b, pos // bs]) * bs + pos % bs
+
+
+def test_swap_plan_moves_each_group_out_and_back():
+    import paged_kv_cache_129_gb300 as pa
+
+    pa.build()
+    plan, host_blocks, pool_s, lens = bench.swap_plan(seed=3, steps=4, num_blocks=2100, num_seqs=8, group=3,
+                                                      block_size=16)
+    need = (lens + 15) // 16
+    assert host_blocks == int(np.sort(need)[-3:].sum())  # room for the three longest sequences
+    for k, (out_p, ho, in_p, hi) in enumerate(plan):
+        out_seqs = [(k * 3 + j) % 8 for j in range(3)]
+        assert len(out_p) == int(need[out_seqs].sum()) and ho == k % 2
+        assert len(set(out_p[:, 0].tolist())) == len(out_p) and len(set(out_p[:, 1].tolist())) == len(out_p)
+        assert (out_p[:, 0] < 2100).all() and (out_p[:, 1] < host_blocks).all()
+        if k == 0:
+            assert len(in_p) == 0
+            continue
+        prev_out, prev_ho = plan[k - 1][0], plan[k - 1][1]
+        # the previous group comes back from the host pool it went to
+        assert hi == prev_ho and sorted(in_p[:, 0].tolist()) == sorted(prev_out[:, 1].tolist())
+        # the two copies of a step touch disjoint blocks: device side and host side
+        assert set(in_p[:, 1].tolist()).isdisjoint(out_p[:, 0].tolist())
+        assert hi != ho
+    assert pool_s >= 0

@@ -228,3 +228,157 @@ def test_static_scratch_size_matches_the_header():
     text = open(os.path.join(ROOT, "include", "pa.h")).read()
     m = re.search(r"#define PA_STATIC_SCRATCH_BYTES \((\d+)u \* 1024u \* 1024u\)", text)
     assert m and int(m.group(1)) * 1024 * 1024 == pa.STATIC_SCRATCH_BYTES
+
+
+# ---- swap between two pools (preemption) ------------------------------------------------------
+@pytest.mark.parametrize("seed", [0, 1])
+def test_pool_swap_matches_allocator_model(lib, seed):
+    rng = np.random.default_rng(seed)
+    bs, sizes = 4, (40, 24)
+    orders = [rng.permutation(n) for n in sizes]
+    pools = [pa.BlockPool(n, bs, free_order=o) for n, o in zip(sizes, orders)]
+    models = [SequencePool(n, bs, free_order=o) for n, o in zip(sizes, orders)]
+    live = []  # [pool index, c++ id, model id]
+    for step in range(1200):
+        op = rng.integers(0, 10)
+        if op == 0 or not live:
+            i = int(rng.integers(2))
+            live.append([i, pools[i].create(), models[i].create()])
+            continue
+        k = int(rng.integers(len(live)))
+        i, c, m = live[k]
+        if op == 1:
+            live.append([i, pools[i].fork(c), models[i].fork(m)])
+        elif op == 2:
+            pools[i].release(c)
+            models[i].release(m)
+            live.pop(k)
+        elif op <= 4:
+            try:
+                new_c, pairs = pools[i].swap_to(pools[1 - i], c)
+            except pa.PoolExhausted:
+                with pytest.raises(MemoryError):
+                    models[i].swap_to(models[1 - i], m)
+            else:
+                new_m, exp = models[i].swap_to(models[1 - i], m)
+                assert pairs.tolist() == [list(p) for p in exp]
+                live[k] = [1 - i, new_c, new_m]
+        else:
+            try:
+                slot, cow = pools[i].append(c)
+            except pa.PoolExhausted:
+                with pytest.raises(MemoryError):
+                    models[i].append(m)
+            else:
+                r = models[i].append(m)
+                assert slot == r.slot and cow == r.cow
+        if step % 50 == 0 or step > 1150:
+            for j in range(2):
+                pools[j].check_invariants()
+                assert models[j].invariants() == []
+                ids = [(c, m) for pi, c, m in live if pi == j]
+                assert pool_state(pools[j], [c for c, _ in ids], sizes[j]) == \
+                    model_state(models[j], [m for _, m in ids], sizes[j])
+
+
+def test_pool_swap_refusals_leave_both_pools_unchanged(lib):
+    dev, host = pa.BlockPool(8, 2), pa.BlockPool(2, 2)
+    a = dev.create()
+    for _ in range(5):
+        dev.append(a)
+    before = (pool_state(dev, [a], 8), pool_state(host, [], 2))
+    with pytest.raises(pa.PoolExhausted):
+        dev.swap_to(host, a)
+    with pytest.raises(pa.PAError):
+        dev.swap_to(pa.BlockPool(8, 4), a)  # other block size
+    with pytest.raises(pa.PAError):
+        dev.swap_to(dev, a)  # same pool
+    with pytest.raises(pa.PAError):
+        dev.swap_to(host, 12345)  # unknown sequence
+    assert (pool_state(dev, [a], 8), pool_state(host, [], 2)) == before
+
+
+def test_swap_blocks_rejects_bad_arguments(lib):
+    assert lib.pa_swap_blocks(FAKE, FAKE, FAKE, FAKE, FAKE, 0, 2, 64, 16, 4, 4, 0, None) == 0  # nothing to do
+    assert lib.pa_swap_blocks(None, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 16, 4, 4, 0, None) == 1
+    assert lib.pa_swap_blocks(FAKE, FAKE, FAKE, FAKE, FAKE + 4, 2, 2, 64, 16, 4, 4, 0, None) == 1  # pairs misaligned
+    assert lib.pa_swap_blocks(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 16, -1, 4, 0, None) == 1  # bad pool size
+    assert lib.pa_swap_blocks(FAKE, FAKE, FAKE, FAKE, FAKE, 2, 2, 64, 16, 4, 4, 9, None) == 1  # dtype
+
+
+# ---- block-table deltas -----------------------------------------------------------------------
+@pytest.mark.parametrize("seed", [0, 1])
+def test_pool_table_deltas_match_allocator_model(lib, seed):
+    rng = np.random.default_rng(seed)
+    nb, bs, rows = 160, 4, 10
+    order = rng.permutation(nb)
+    pool = pa.BlockPool(nb, bs, free_order=order)
+    model = SequencePool(nb, bs, free_order=order)
+    live = []  # (c++ id, model id)
+    for step in range(600):
+        op = rng.integers(0, 9)
+        if op == 0 or not live:
+            live.append((pool.create(), model.create()))
+        elif op == 1:
+            c, m = live[rng.integers(len(live))]
+            live.append((pool.fork(c), model.fork(m)))
+        elif op == 2:
+            c, m = live.pop(rng.integers(len(live)))
+            pool.release(c)
+            model.release(m)
+        elif op == 3:
+            k = rng.permutation(len(live))[:rows]
+            deltas, lens = pool.table_deltas([live[i][0] for i in k])
+            exp, exp_lens = model.table_deltas([live[i][1] for i in k])
+            assert deltas.tolist() == [list(x) for x in exp] and lens.tolist() == exp_lens
+        else:
+            c, m = live[rng.integers(len(live))]
+            try:
+                pool.append(c)
+            except pa.PoolExhausted:
+                with pytest.raises(MemoryError):
+                    model.append(m)
+            else:
+                model.append(m)
+
+
+def test_pool_table_deltas_refusals_change_nothing(lib):
+    pool = pa.BlockPool(16, 2)
+    a, b = pool.create(), pool.create()
+    for _ in range(5):
+        pool.append(a)
+    pool.append(b)
+    small = np.empty((2, 3), np.int32)
+    with pytest.raises(pa.PAError):
+        pool.table_deltas([a, b], out=small)  # 4 deltas do not fit in 2
+    with pytest.raises(pa.PAError):
+        pool.table_deltas([a, a])  # a sequence in two rows
+    with pytest.raises(pa.PAError):
+        pool.table_deltas([a, 999])
+    deltas, lens = pool.table_deltas([a, b])  # nothing was recorded by the refused calls
+    assert deltas.tolist() == [[0, 0, pool.block_tables([a], 4)[0][0, 0]], [0, 1, pool.block_tables([a], 4)[0][0, 1]],
+                               [0, 2, pool.block_tables([a], 4)[0][0, 2]], [1, 0, pool.block_tables([b], 4)[0][0, 0]]]
+    assert lens.tolist() == [5, 1]
+    again, _ = pool.table_deltas([a, b])
+    assert again.shape == (0, 3)
+    pool.append(a)  # fills block 2 of a: no new entry
+    pool.append(a)  # a new block
+    d, _ = pool.table_deltas([a, b])
+    assert d.tolist() == [[0, 3, pool.block_tables([a], 4)[0][0, 3]]]
+    d, _ = pool.table_deltas([b, a])  # rows swapped: everything again
+    assert [tuple(x[:2]) for x in d.tolist()] == [(0, 0), (1, 0), (1, 1), (1, 2), (1, 3)]
+
+
+def test_write_layers_and_deltas_reject_bad_arguments(lib):
+    import ctypes
+
+    arr = (ctypes.c_void_p * 1)(FAKE)
+    assert lib.pa_write_kv_layers(arr, arr, arr, arr, 1, FAKE, 0, 2, 64, 16, 4, 0, None) == 0  # no tokens
+    assert lib.pa_write_kv_layers(arr, arr, arr, arr, 0, FAKE, 3, 2, 64, 16, 4, 0, None) == 1  # no layers
+    assert lib.pa_write_kv_layers(arr, arr, arr, arr, 257, FAKE, 3, 2, 64, 16, 4, 0, None) == 1  # too many
+    assert lib.pa_write_kv_layers(arr, arr, arr, arr, 1, FAKE + 4, 3, 2, 64, 16, 4, 0, None) == 1  # slots
+    nul = (ctypes.c_void_p * 1)(None)
+    assert lib.pa_write_kv_layers(arr, nul, arr, arr, 1, FAKE, 3, 2, 64, 16, 4, 0, None) == 1
+    assert lib.pa_apply_table_deltas(FAKE, 4, 8, FAKE, 0, None) == 0
+    assert lib.pa_apply_table_deltas(None, 4, 8, FAKE, 2, None) == 1
+    assert lib.pa_apply_table_deltas(FAKE, 4, 8, FAKE + 2, 2, None) == 1

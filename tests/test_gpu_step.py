@@ -74,3 +74,60 @@ def test_stepper_matches_direct_calls(append, dtype, hq, hkv, lens):
         assert torch.equal(got[i].view(torch.int16), ref.cpu().view(torch.int16)), f"step {i}"
     assert torch.equal(kc, kc_ref) and torch.equal(vc, vc_ref)
     pa.check_error()
+
+
+def test_stepper_with_table_deltas_matches_full_tables():
+    """Sequences grow by one token a step through the block pool (new blocks, a fork's
+    copy-on-write tail); the stepper keeps the device tables current with the pool's delta
+    exports only, and every step's output and the caches equal direct pa_decode_append calls
+    given the full tables."""
+    rng = np.random.default_rng(5)
+    nb, hkv, hq, bs, d, B, width, steps = 300, 4, 28, 16, 128, 6, 24, 40
+    pool = pa.BlockPool(nb, bs, free_order=rng.permutation(nb))
+    seqs = [pool.create() for _ in range(B - 1)]
+    for sid, n in zip(seqs, rng.integers(1, 200, B - 1)):
+        for _ in range(int(n)):
+            pool.append(sid)
+    seqs.append(pool.fork(seqs[0]))  # shares seqs[0]'s blocks; its first append copies a partial tail
+    kc = torch.randn(nb, hkv, bs, d, device="cuda").to(torch.bfloat16)
+    vc = torch.randn(nb, hkv, bs, d, device="cuda").to(torch.bfloat16)
+    kc_ref, vc_ref = kc.clone(), vc.clone()
+    stepper = pa.DecodeStepper(kc, vc, B, hq, width, append=True, tables="deltas")
+    got, refs, sent = [], [], []
+    for i in range(steps):
+        if i >= stepper.slots:
+            got.append(stepper.result(i - stepper.slots).clone())
+        cow = []
+        for sid in seqs:
+            _, pair = pool.append(sid)
+            if pair:
+                cow.append(pair)
+        if cow:  # the copy-on-write copies, on both caches, before this step's decode
+            pairs = torch.tensor(cow, dtype=torch.int64, device="cuda")
+            pa.copy_blocks(kc, vc, pairs)
+            pa.copy_blocks(kc_ref, vc_ref, pairs)
+        v = stepper.inputs(i)
+        deltas, lens = pool.table_deltas(seqs, out=v.deltas.numpy(), lens_out=v.context_lens.numpy())
+        sent.append(len(deltas))
+        if i == 0:
+            entries0 = sum((pool.length(sid) + bs - 1) // bs for sid in seqs)
+        q = torch.randn(B, hq, d).to(torch.bfloat16)
+        nk = torch.randn(B, hkv, d).to(torch.bfloat16)
+        nv = torch.randn(B, hkv, d).to(torch.bfloat16)
+        v.query.copy_(q)
+        v.new_key.copy_(nk)
+        v.new_value.copy_(nv)
+        stepper.launch(i, num_deltas=len(deltas))
+        full, full_lens = pool.block_tables(seqs, width)
+        refs.append(pa.decode_append(q.cuda(), nk.cuda(), nv.cuda(), kc_ref, vc_ref, torch.from_numpy(full).cuda(),
+                                     torch.from_numpy(full_lens).cuda()))
+    for i in range(steps - stepper.slots, steps):
+        got.append(stepper.result(i).clone())
+    torch.cuda.synchronize()
+    pa.check_error()
+    for i in range(steps):
+        assert torch.equal(got[i].view(torch.int16), refs[i].cpu().view(torch.int16)), f"step {i}"
+    assert torch.equal(kc, kc_ref) and torch.equal(vc, vc_ref)
+    # the first step sends every entry; later steps only the new blocks and copied tails
+    assert sent[0] == entries0
+    assert max(sent[1:]) <= B and sum(sent[1:]) < steps * B / 4

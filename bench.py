@@ -64,6 +64,10 @@ WORKLOAD_DESCRIPTIONS = {
                   "sequence's K/V counted), roofline over the unique pages",
     "prefix_cow_2056": "prefix sharing, copy-on-write variant: as prefix_cow with a 2056-token prefix, so the "
                        "first append of 63 sequences copies the shared partial block (pa_copy_blocks)",
+    "qwen_gqa_layers28": "a whole-model decode step over 28 Qwen-style GQA layers (each: batch 64, 28 q / 4 kv "
+                         "heads, head_dim 128, bf16, block_size 16, context_lens uniform in [512,4096], pool 20000 "
+                         "blocks): every layer's new token written in one pa_write_kv_layers launch, then one "
+                         "pa_decode per layer",
     "swap_qwen": "preemption swap on the Qwen-style GQA layer's cache (4 kv heads, head_dim 128, bf16, "
                  "block_size 16, pool 20000 blocks, 64 sequences with context_lens uniform in [512,4096] "
                  "built through the block pool): each step swaps 16 sequences out to a page-locked host pool "
@@ -342,6 +346,7 @@ def build_batch(workload: str, seed: int):
     from paged_kv_cache_129_gb300 import workloads as wl
 
     gen = {"qwen_gqa": lambda s: wl.qwen_gqa(s), "qwen_gqa_verify4": lambda s: wl.qwen_gqa_verify(s, q_len=4),
+           "qwen_gqa_layers28": lambda s: wl.qwen_gqa(s),  # every layer has the Qwen layer's shape
            "long_context": lambda s: wl.long_context(s),
            "mha_short_bs16": lambda s: wl.mha_short(16, s), "mha_short_bs32": lambda s: wl.mha_short(32, s)}[workload]
     return gen(seed)
@@ -723,6 +728,128 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     print(json.dumps(line), flush=True)
 
 
+LAYERS = 28
+
+
+def run_layers(args, rank: int, world: int, local_rank: int) -> None:
+    """Whole-model step: pa_write_kv_layers for all layers, then pa_decode_ex per layer."""
+    import torch
+
+    import paged_kv_cache_129_gb300 as pa
+
+    assert torch.cuda.is_available(), "bench.py needs a CUDA GPU"
+    torch.cuda.set_device(local_rank)
+    device = torch.device("cuda", local_rank)
+    lib = pa.library()
+    seed = rank_seed(args.seed, rank)
+    inp = build_batch("qwen_gqa", seed)  # lengths, tables and slots of the layer batch
+    tables, lens, slots = pool_tables(inp)
+    B, Hq, Hkv, d, bs, nb = inp.num_seqs, inp.num_heads, inp.num_kv_heads, inp.head_dim, inp.block_size, inp.num_blocks
+    gen = torch.Generator(device=device).manual_seed(seed)
+
+    def randn(*shape):
+        return torch.randn(*shape, device=device, generator=gen).to(torch.bfloat16)
+
+    kcs = [randn(nb, Hkv, bs, d) for _ in range(LAYERS)]
+    vcs = [randn(nb, Hkv, bs, d) for _ in range(LAYERS)]
+    qs = [randn(B, Hq, d) for _ in range(LAYERS)]
+    nks = [randn(B, Hkv, d) for _ in range(LAYERS)]
+    nvs = [randn(B, Hkv, d) for _ in range(LAYERS)]
+    outs = [torch.empty_like(q) for q in qs]
+    bt = torch.from_numpy(tables).to(device)
+    dl = torch.from_numpy(lens).to(device)
+    sl = torch.from_numpy(slots).to(device)
+    max_ctx = int(lens.max())
+    plan = pa.decode_plan(B, Hq, Hkv, d, bs, tables.shape[1], torch.bfloat16, max_context_len=max_ctx)
+    ws = torch.zeros(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    sptr = int(stream.cuda_stream)
+    import ctypes
+
+    arr = ctypes.c_void_p * LAYERS
+    wl_args = [arr(*[t.data_ptr() for t in nks]), arr(*[t.data_ptr() for t in nvs]),
+               arr(*[t.data_ptr() for t in kcs]), arr(*[t.data_ptr() for t in vcs]), LAYERS, sl.data_ptr(), B, Hkv,
+               d, bs, nb, 2, sptr]
+    dec_args = [[outs[l].data_ptr(), qs[l].data_ptr(), kcs[l].data_ptr(), vcs[l].data_ptr(), bt.data_ptr(),
+                 dl.data_ptr(), B, Hq, Hkv, d, bs, tables.shape[1], nb, float(inp.scale), 2, ws.data_ptr(),
+                 ws.numel(), max_ctx, 0, 0, sptr] for l in range(LAYERS)]
+
+    def write_all():
+        if lib.pa_write_kv_layers(*wl_args) != 0:
+            raise RuntimeError(lib.pa_last_error_string().decode())
+
+    def decode_all():
+        for l in range(LAYERS):
+            if lib.pa_decode_ex(*dec_args[l]) != 0:
+                raise RuntimeError(lib.pa_last_error_string().decode())
+
+    def region(fn, k):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda.synchronize()
+        a.record(stream)
+        for _ in range(k):
+            fn()
+        b.record(stream)
+        torch.cuda.synchronize()
+        return a.elapsed_time(b)
+
+    sampler = ClockSampler(gpu_selector(device))
+    sampler.start()
+    for _ in range(args.warmup):
+        write_all()
+        decode_all()
+    torch.cuda.synchronize()
+    pa.check_error()
+    K = args.steps
+    barrier(world)
+    t_begin = time.monotonic()
+    step_ms = region(lambda: (write_all(), decode_all()), K)
+    write_ms = region(write_all, K)
+    t_end = time.monotonic()
+    barrier(world)
+    sampler.stop()
+    pa.check_error()
+    dec_bytes = decode_bytes(lens, Hq, Hkv, d, 2, bs)
+    wr_bytes = write_bytes(B, Hkv, d, 2)
+    step_bytes = LAYERS * (dec_bytes + wr_bytes)
+    ms = max_over_ranks(step_ms, world)
+    value = sum_over_ranks(float(step_bytes) * K, world) / (ms / 1e3) / 1e9
+    peaks = measured_peaks()
+    peak = float(peaks.get("hbm_gbs") or FALLBACK_HBM_GBS)
+    dec_avg_ms = (step_ms - write_ms) / (K * LAYERS)
+    write_avg_ms = write_ms / K
+    clocks = sampler.summary(t_begin, t_end)
+    if rank != 0:
+        return
+    merge = 1 if (plan.schedule == 1 or plan.max_parts > 1) else 0
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
+        "warmup": args.warmup, "ms_per_step": round(ms / K, 5), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESCRIPTIONS["qwen_gqa_layers28"], "name": "qwen_gqa_layers28",
+                   "layers": LAYERS, "step": "pa_write_kv_layers (28 layers, one launch) + 28 x pa_decode_ex",
+                   "l2": f"28 layers' pages per step ({LAYERS * pages_touched_bytes(lens, Hkv, d, 2, bs) / 1e9:.1f} "
+                         "GB) pass through L2 once",
+                   "parallelism": f"{world} independent replicas (one model per GPU)"},
+        "pct_of_hbm_peak": round(100 * value / peak, 2),
+        "queries_per_s": round(B * K / (ms / 1e3), 1),
+        "step_bytes": step_bytes,
+        "roofline": {"bound": "hbm", "achieved": round(dec_bytes / (dec_avg_ms / 1e3) / 1e9, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(dec_bytes / (dec_avg_ms / 1e3) / 1e9 / peak, 4),
+                     "traffic": None, "kernel": "pa_decode call per layer (decode step time minus the write's)",
+                     "algorithmic_bytes_per_launch": dec_bytes, "avg_launch_ms": round(dec_avg_ms, 5),
+                     "peak_source": "of measured (MEASURED_PEAKS.json hbm_gbs)",
+                     "write_kv_layers": {"bytes_per_launch": LAYERS * wr_bytes, "avg_launch_ms": round(write_avg_ms, 5),
+                                         "achieved_gbs": round(LAYERS * wr_bytes / (write_avg_ms / 1e3) / 1e9, 1),
+                                         "timing": f"CUDA events around {K} back-to-back launches"}},
+        "cpu_baseline": None,
+        "e2e": None,
+        "gpu_launches": K * (1 + LAYERS * (1 + merge)),
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def swap_plan(seed: int, steps: int, num_blocks: int = 20000, num_seqs: int = 64, group: int = SWAP_GROUP,
               block_size: int = 16):
     """Host side of the swap workload (no GPU).  Sequences are built through the product block pool; the
@@ -1083,6 +1210,8 @@ def main(argv=None) -> None:
             run_reference(args, rank, world)
         elif args.workload == "swap_qwen":
             run_swap(args, rank, world, local_rank)
+        elif args.workload == "qwen_gqa_layers28":
+            run_layers(args, rank, world, local_rank)
         else:
             run_ours(args, rank, world, local_rank)
     finally:

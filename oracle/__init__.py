@@ -30,8 +30,8 @@ _LIB_PATH = os.path.join(_BUILD_DIR, "liboracle.so")
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
 
-DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2}
-ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2}
+DTYPE_CODES = {"f32": 0, "f16": 1, "bf16": 2, "e4m3": 3}
+ELEM_BYTES = {"f32": 4, "f16": 2, "bf16": 2, "e4m3": 1}
 
 OK, BAD_ARG, BAD_TABLE, BAD_SLOT, NO_MEMORY = 0, -1, -2, -3, -4
 
@@ -65,6 +65,13 @@ def _load() -> ctypes.CDLL:
             lib.oracle_copy_blocks.argtypes = [p, p, p, i32, i64, i32]
             lib.oracle_swap_blocks.restype = i32
             lib.oracle_swap_blocks.argtypes = [p, p, p, p, p, i32, i64, i32, i32]
+            lib.oracle_decode_fp8_rows.restype = i32
+            lib.oracle_decode_fp8_rows.argtypes = [p, p, p, i32, p, i32, p, p, p, p, p, p, i32, i32, i32, i32,
+                                                   i32, i32, i32, dbl]
+            lib.oracle_write_kv_fp8.restype = i32
+            lib.oracle_write_kv_fp8.argtypes = [p, p, i32, p, p, p, p, p, i32, i32, i32, i32, i32]
+            lib.oracle_e4m3_encode.restype = i32
+            lib.oracle_e4m3_encode.argtypes = [p, i64, p]
             lib.oracle_element_to_double.restype = dbl
             lib.oracle_element_to_double.argtypes = [p, i32, i64]
             _lib = lib
@@ -116,6 +123,65 @@ def decode(q: np.ndarray, key_cache: np.ndarray, value_cache: np.ndarray, block_
                                     num_heads, hkv, head_dim, block_size, bt.shape[1], num_blocks, float(scale))
     if status != OK:
         raise ValueError(f"oracle decode failed with status {status}")
+    return out.reshape(num_seqs, num_heads, head_dim) if rows is None else out
+
+
+def e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """float32 values -> E4M3 codes (uint8): nearest, ties to even, saturating at 448."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    out = np.empty(x.shape, dtype=np.uint8)
+    _load().oracle_e4m3_encode(_ptr(x), int(x.size), _ptr(out))
+    return out
+
+
+def write_kv_fp8(key: np.ndarray, value: np.ndarray, dtype: str, key_cache: np.ndarray, value_cache: np.ndarray,
+                 k_scale: np.ndarray, v_scale: np.ndarray, slot_mapping: np.ndarray) -> int:
+    """In-place paged write into an E4M3 cache (uint8 [N, H_kv, bs, d]) with per-(block, kv head) float32
+    scales [N, H_kv]: code = e4m3(float32(x) / scale).  Returns the oracle status."""
+    lib = _load()
+    num_blocks, hkv, block_size, head_dim = key_cache.shape
+    key, value = np.ascontiguousarray(key), np.ascontiguousarray(value)
+    slots = np.ascontiguousarray(slot_mapping, dtype=np.int64)
+    ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+    vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+    assert key.shape == (slots.size, hkv, head_dim) and value.shape == key.shape
+    assert key_cache.dtype == np.uint8 and value_cache.shape == key_cache.shape and value_cache.dtype == np.uint8
+    assert key_cache.flags["C_CONTIGUOUS"] and value_cache.flags["C_CONTIGUOUS"]
+    assert ks.shape == (num_blocks, hkv) and vs.shape == ks.shape
+    return lib.oracle_write_kv_fp8(_ptr(key), _ptr(value), DTYPE_CODES[dtype], _ptr(key_cache), _ptr(value_cache),
+                                   _ptr(ks), _ptr(vs), _ptr(slots), int(slots.size), hkv, head_dim, block_size,
+                                   num_blocks)
+
+
+def decode_fp8(q: np.ndarray, dtype: str, key_cache: np.ndarray, value_cache: np.ndarray, k_scale: np.ndarray,
+               v_scale: np.ndarray, block_tables: np.ndarray, context_lens: np.ndarray, scale: float,
+               rows: Optional[Sequence[tuple]] = None) -> np.ndarray:
+    """fp64 decode attention over an E4M3 cache with per-(block, kv head) scales; ``q`` in ``dtype``
+    storage form.  Returns ``[B, H_q, d]`` float64, or ``[len(rows), d]`` for rows ``(b, qh)``."""
+    lib = _load()
+    q = np.ascontiguousarray(q)
+    kc, vc = np.ascontiguousarray(key_cache), np.ascontiguousarray(value_cache)
+    ks = np.ascontiguousarray(k_scale, dtype=np.float32)
+    vs = np.ascontiguousarray(v_scale, dtype=np.float32)
+    bt = np.ascontiguousarray(block_tables, dtype=np.int32)
+    lens = np.ascontiguousarray(context_lens, dtype=np.int32)
+    num_seqs, num_heads, head_dim = q.shape
+    num_blocks, hkv, block_size, d2 = kc.shape
+    assert d2 == head_dim and vc.shape == kc.shape and kc.dtype == np.uint8 and ks.shape == (num_blocks, hkv)
+    if rows is None:
+        rb, rh = np.meshgrid(np.arange(num_seqs), np.arange(num_heads), indexing="ij")
+        rb, rh = rb.reshape(-1), rh.reshape(-1)
+    else:
+        rb = np.array([r[0] for r in rows]) if len(rows) else np.zeros(0)
+        rh = np.array([r[1] for r in rows]) if len(rows) else np.zeros(0)
+    rb = np.ascontiguousarray(rb, dtype=np.int32)
+    rh = np.ascontiguousarray(rh, dtype=np.int32)
+    out = np.zeros((rb.size, head_dim), dtype=np.float64)
+    status = lib.oracle_decode_fp8_rows(_ptr(out), _ptr(rb), _ptr(rh), int(rb.size), _ptr(q), DTYPE_CODES[dtype],
+                                        _ptr(kc), _ptr(vc), _ptr(ks), _ptr(vs), _ptr(bt), _ptr(lens), num_seqs,
+                                        num_heads, hkv, head_dim, block_size, bt.shape[1], num_blocks, float(scale))
+    if status != OK:
+        raise ValueError(f"oracle fp8 decode failed with status {status}")
     return out.reshape(num_seqs, num_heads, head_dim) if rows is None else out
 
 

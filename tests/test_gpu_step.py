@@ -93,6 +93,9 @@ def test_stepper_with_table_deltas_matches_full_tables():
     vc = torch.randn(nb, hkv, bs, d, device="cuda").to(torch.bfloat16)
     kc_ref, vc_ref = kc.clone(), vc.clone()
     stepper = pa.DecodeStepper(kc, vc, B, hq, width, append=True, tables="deltas")
+    # the same plan as the stepper's (its workspace size), so the direct calls take the same schedule
+    ws_bytes = pa.decode_workspace_size(B, hq, hkv, d, bs, width, torch.bfloat16)
+    ws = torch.empty(max(ws_bytes, 256), dtype=torch.uint8, device="cuda") if ws_bytes else None
     got, refs, sent = [], [], []
     for i in range(steps):
         if i >= stepper.slots:
@@ -120,7 +123,7 @@ def test_stepper_with_table_deltas_matches_full_tables():
         stepper.launch(i, num_deltas=len(deltas))
         full, full_lens = pool.block_tables(seqs, width)
         refs.append(pa.decode_append(q.cuda(), nk.cuda(), nv.cuda(), kc_ref, vc_ref, torch.from_numpy(full).cuda(),
-                                     torch.from_numpy(full_lens).cuda()))
+                                     torch.from_numpy(full_lens).cuda(), workspace=ws))
     for i in range(steps - stepper.slots, steps):
         got.append(stepper.result(i).clone())
     torch.cuda.synchronize()

@@ -237,6 +237,40 @@ int pa_decode_append(void* out, const void* query, const void* new_key, const vo
                      int max_context_len, int partition_pages, int kernel, void* stream);
 
 /*
+ * FP8 KV cache (the LLM-inference page's quantised KV cache, FP8 among the remedies
+ * when the pool runs out; the vLLM and PagedAttention page's attention metadata: KV
+ * dtype and quantisation scales).  A cache element is an OCP FP8 E4M3 code (bias 7,
+ * no infinities, largest finite 448, S.1111.111 = NaN), one byte, in the same layout
+ * [num_blocks, H_kv, block_size, head_dim]; k_scale and v_scale are float32
+ * [num_blocks, H_kv] (device), one scale per (physical block, kv head), positive and
+ * finite.  The value attended is code * scale.  Choosing the scales (e.g. from the
+ * block's first tokens, or one per layer) is the caller's policy.
+ *
+ * pa_write_kv_fp8 — pa_write_kv into an FP8 cache: element i of token t, kv head h
+ * is stored as e4m3(x / scale[slot / block_size, h]) with x the source element
+ * (dtype PA_F32, PA_F16 or PA_BF16) as float32, the division in float32, round to
+ * nearest even, magnitudes above 448 saturating to 448, NaN staying NaN.
+ * head_dim a multiple of 4.  Slots as pa_write_kv.
+ */
+int pa_write_kv_fp8(const void* key, const void* value, void* key_cache, void* value_cache, const float* k_scale,
+                    const float* v_scale, const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
+                    int block_size, int num_blocks, int dtype, void* stream);
+/*
+ * pa_decode_fp8 — pa_decode over an FP8 cache; query and out in `dtype` (PA_F16 or
+ * PA_BF16).  Compiled for head_dim 128, block_size 16 and 32 (PA_ERR_UNSUPPORTED
+ * otherwise).  Runs the lean schedule (equal page shares per warp + merge) and
+ * needs a workspace of pa_decode_fp8_workspace_size() bytes (PA_ERR_INVALID_ARG
+ * without it); query and out 16-byte aligned.  The codes are widened to f16 exactly and multiplied on the tensor
+ * cores with fp32 accumulation; the scales are applied in fp32.
+ */
+int pa_decode_fp8(void* out, const void* query, const void* key_cache, const void* value_cache, const float* k_scale,
+                  const float* v_scale, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                  int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                  int num_blocks, float scale, int dtype, void* workspace, size_t workspace_bytes, void* stream);
+size_t pa_decode_fp8_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                    int max_blocks_per_seq, int dtype);
+
+/*
  * pa_decode_multi — multi-query decode: the verify step of speculative decoding, or
  * the tail of a chunked prefill (vLLM and PagedAttention page, section on how the
  * attention kernel reads paged KV: each sequence's query range and context length,

@@ -16,6 +16,8 @@ from .binding import (  # noqa: F401
     copy_blocks,
     decode,
     decode_append,
+    decode_fp8,
+    decode_fp8_workspace_size,
     decode_multi,
     decode_multi_workspace_size,
     decode_plan,
@@ -25,6 +27,7 @@ from .binding import (  # noqa: F401
     swap_blocks,
     version,
     write_kv,
+    write_kv_fp8,
     write_kv_layers,
 )
 

@@ -60,6 +60,9 @@ _SIGNATURES = [
     ("pa_write_kv", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     ("pa_copy_blocks", _I, [_P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     ("pa_swap_blocks", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
+    ("pa_write_kv_fp8", _I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
+    ("pa_decode_fp8", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    ("pa_decode_fp8_workspace_size", _SZ, [_I, _I, _I, _I, _I, _I, _I]),
     ("pa_write_kv_layers", _I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P]),
     ("pa_apply_table_deltas", _I, [_P, _I, _I, _P, _I, _P]),
     ("pa_decode", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
@@ -305,6 +308,71 @@ def decode(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tens
                                   block_tables.shape[1], num_blocks, float(scale), _dtype_code(query), ws_ptr or None,
                                   ws_bytes, max_context_len, partition_pages, KERNELS[kernel],
                                   _stream_ptr(stream, query.device)))
+    return out
+
+
+def _fp8_cache(key_cache: torch.Tensor, value_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor):
+    for name, t in (("key_cache", key_cache), ("value_cache", value_cache), ("k_scale", k_scale),
+                    ("v_scale", v_scale)):
+        _cuda(t, name)
+    _need(key_cache.dim() == 4 and value_cache.shape == key_cache.shape, "caches must be [N, H_kv, bs, d]")
+    _need(key_cache.dtype == value_cache.dtype and key_cache.dtype in (torch.uint8, torch.float8_e4m3fn),
+          "FP8 caches hold E4M3 codes (uint8 or float8_e4m3fn)")
+    _need(k_scale.dtype == v_scale.dtype == torch.float32 and k_scale.shape == v_scale.shape == key_cache.shape[:2],
+          "k_scale / v_scale: float32 [N, H_kv]")
+    return key_cache.shape
+
+
+def write_kv_fp8(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+                 k_scale: torch.Tensor, v_scale: torch.Tensor, slot_mapping: torch.Tensor, stream=None) -> None:
+    """``pa_write_kv_fp8``: quantise key/value ``[T, H_kv, d]`` (f32/f16/bf16) into the E4M3 caches at
+    ``slot_mapping`` with the (block, kv head) scales."""
+    num_blocks, hkv, bs, d = _fp8_cache(key_cache, value_cache, k_scale, v_scale)
+    for name, t in (("key", key), ("value", value), ("slot_mapping", slot_mapping)):
+        _cuda(t, name)
+    _need(key.shape == value.shape and key.dim() == 3 and key.shape[1:] == (hkv, d), "key/value must be [T, H_kv, d]")
+    _need(key.dtype == value.dtype, "key and value must share a dtype")
+    _need(slot_mapping.dtype == torch.int64 and slot_mapping.numel() == key.shape[0], "slot_mapping: int64 [T]")
+    _check(library().pa_write_kv_fp8(key.data_ptr(), value.data_ptr(), key_cache.data_ptr(), value_cache.data_ptr(),
+                                     k_scale.data_ptr(), v_scale.data_ptr(), slot_mapping.data_ptr(), key.shape[0],
+                                     hkv, d, bs, num_blocks, _dtype_code(key), _stream_ptr(stream, key.device)))
+
+
+def decode_fp8_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int, block_size: int,
+                              max_blocks_per_seq: int, dtype: torch.dtype) -> int:
+    return int(library().pa_decode_fp8_workspace_size(num_seqs, num_heads, num_kv_heads, head_dim, block_size,
+                                                      max_blocks_per_seq, _TORCH_DTYPES[dtype]))
+
+
+def decode_fp8(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor, k_scale: torch.Tensor,
+               v_scale: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
+               scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+               workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """``pa_decode_fp8``: paged decode attention over E4M3 caches with (block, kv head) scales; ``query``
+    f16/bf16 ``[B, H_q, d]``.  ``workspace`` defaults to a fresh one of the plan's size."""
+    num_blocks, hkv, bs, d = _fp8_cache(key_cache, value_cache, k_scale, v_scale)
+    for name, t in (("query", query), ("block_tables", block_tables), ("context_lens", context_lens)):
+        _cuda(t, name)
+    _need(query.dim() == 3 and query.shape[2] == d, "query must be [B, H_q, d]")
+    b, hq, _ = query.shape
+    _need(block_tables.dtype == torch.int32 and block_tables.dim() == 2 and block_tables.shape[0] == b,
+          "block_tables: int32 [B, max_blocks]")
+    _need(context_lens.dtype == torch.int32 and context_lens.numel() == b, "context_lens: int32 [B]")
+    if out is None:
+        out = torch.empty_like(query)
+    _cuda(out, "out")
+    _need(out.shape == query.shape and out.dtype == query.dtype, "out must match query")
+    if scale is None:
+        scale = 1.0 / math.sqrt(d)
+    if workspace is None:
+        n = decode_fp8_workspace_size(b, hq, hkv, d, bs, block_tables.shape[1], query.dtype)
+        workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=query.device)
+    _cuda(workspace, "workspace")
+    _check(library().pa_decode_fp8(out.data_ptr(), query.data_ptr(), key_cache.data_ptr(), value_cache.data_ptr(),
+                                   k_scale.data_ptr(), v_scale.data_ptr(), block_tables.data_ptr(),
+                                   context_lens.data_ptr(), b, hq, hkv, d, bs, block_tables.shape[1], num_blocks,
+                                   float(scale), _dtype_code(query), workspace.data_ptr(),
+                                   workspace.numel() * workspace.element_size(), _stream_ptr(stream, query.device)))
     return out
 
 

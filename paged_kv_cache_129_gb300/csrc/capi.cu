@@ -71,7 +71,10 @@ cudaError_t merge_launch(int dtype, int head_dim, const MergeArgs& a, cudaStream
 
 namespace {
 
-int elem_bytes(int dtype) { return dtype == PA_F32 ? 4 : 2; }
+// Internal element code of an FP8 (E4M3) cache, for the tensor-map cache (not a public dtype).
+constexpr int kCacheE4M3 = 16;
+
+int elem_bytes(int dtype) { return dtype == PA_F32 ? 4 : dtype == kCacheE4M3 ? 1 : 2; }
 bool dtype_ok(int dtype) { return dtype == PA_F32 || dtype == PA_F16 || dtype == PA_BF16; }
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -143,9 +146,10 @@ int encode_cache_map_uncached(CUtensorMap* map, const void* base, int dtype, int
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const int eb = elem_bytes(dtype);
-    const CUtensorMapDataType type = dtype == PA_F32   ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
-                                     : dtype == PA_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
-                                                       : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
+    const CUtensorMapDataType type = dtype == PA_F32       ? CU_TENSOR_MAP_DATA_TYPE_FLOAT32
+                                     : dtype == PA_F16     ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                     : dtype == kCacheE4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
+                                                           : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
     cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)num_blocks * num_kv_heads * block_size};
     cuuint64_t strides[1] = {(cuuint64_t)head_dim * eb};
     cuuint32_t box[2] = {(cuuint32_t)(128 / eb), (cuuint32_t)block_size};
@@ -216,7 +220,7 @@ void workspace_layout(int num_seqs, int num_heads, int head_dim, int max_parts, 
 // q_len > 1: multi-query decode; a kv head then serves q_len * group query rows.
 int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks, int dtype,
               bool has_ws, size_t ws_avail, int max_context_len, int partition_pages, int kernel, Plan* plan,
-              int q_len = 1) {
+              int q_len = 1, bool fp8 = false) {
     if (!dtype_ok(dtype)) return fail(PA_ERR_INVALID_ARG, "unknown dtype %d", dtype);
     if (num_seqs < 0 || num_heads <= 0 || num_kv_heads <= 0 || num_heads % num_kv_heads != 0)
         return fail(PA_ERR_INVALID_ARG, "num_heads=%d must be a positive multiple of num_kv_heads=%d", num_heads,
@@ -230,6 +234,46 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
         return fail(PA_ERR_INVALID_ARG, "q_len=%d must be positive (and q_len * num_heads < 2^24)", q_len);
     Plan p;
     const int rows = q_len * (num_heads / num_kv_heads);  // query rows per kv head
+    if (fp8) {
+        // FP8 caches: the lean schedule with the FP8 tensor-core consumer, single-query decode.
+        if (dtype != PA_F16 && dtype != PA_BF16)
+            return fail(PA_ERR_UNSUPPORTED, "FP8 decode needs f16 or bf16 queries");
+        if (kernel != PA_KERNEL_AUTO && kernel != PA_KERNEL_MMA)
+            return fail(PA_ERR_UNSUPPORTED, "FP8 decode has only the tensor-core kernel");
+        if (q_len != 1) return fail(PA_ERR_UNSUPPORTED, "FP8 decode is single-query");
+        if (partition_pages != 0)
+            return fail(PA_ERR_UNSUPPORTED, "FP8 decode has only the lean schedule (partition_pages must be 0)");
+        p.kind = PA_KERNEL_MMA;
+        p.dkind = 4;
+        if (!decode_kernel_info_fp8(dtype, head_dim, block_size, num_seqs, &p.ki))
+            return fail(PA_ERR_UNSUPPORTED, "no FP8 decode kernel for dtype=%d head_dim=%d block_size=%d", dtype,
+                        head_dim, block_size);
+        p.head_chunks = (rows + p.ki.heads_per_cta - 1) / p.ki.heads_per_cta;
+        p.units = num_seqs * num_kv_heads * p.head_chunks;
+        if (num_seqs > p.ki.lean_max_seqs)
+            return fail(PA_ERR_UNSUPPORTED, "FP8 decode: num_seqs=%d > %d", num_seqs, p.ki.lean_max_seqs);
+        if ((long long)num_seqs * max_blocks * num_kv_heads * p.head_chunks >= (1ll << 31))
+            return fail(PA_ERR_UNSUPPORTED, "FP8 decode: num_seqs * max_blocks * units is too large");
+        DeviceState* dev = nullptr;
+        int st = current_device_state(&dev);
+        if (st != PA_OK) return st;
+        const long long ctas = (long long)dev->num_sms * p.ki.lean_ctas_per_sm;
+        const size_t records = (size_t)ctas * p.ki.lean_warps_per_cta * 2;
+        const size_t off_flag = align256(records * (size_t)p.ki.lean_record_floats * sizeof(float));
+        const size_t need = off_flag + align256(records * sizeof(unsigned long long));
+        if (!has_ws || need > ws_avail)
+            return fail(PA_ERR_INVALID_ARG, "FP8 decode needs a workspace of %zu bytes (%zu given)", need,
+                        has_ws ? ws_avail : (size_t)0);
+        p.schedule = kScheduleLean;
+        p.partition_pages = 0;
+        p.max_parts = 0;
+        p.grid = ctas;
+        p.ws_bytes = need;
+        p.off_part = 0;
+        p.off_flag = off_flag;
+        *plan = p;
+        return PA_OK;
+    }
     if (kernel == PA_KERNEL_AUTO) {
         p.kind = dtype == PA_F32 ? PA_KERNEL_SIMT : PA_KERNEL_MMA;
     } else if (kernel == PA_KERNEL_MMA || kernel == PA_KERNEL_SIMT) {
@@ -591,8 +635,14 @@ int decode_impl(void* out, const void* query, const void* new_key, const void* n
                 const void* value_cache, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
                 int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
                 int num_blocks, float scale, int dtype, void* workspace, size_t workspace_bytes, int max_context_len,
-                int partition_pages, int kernel, void* stream, int q_len = 1) {
+                int partition_pages, int kernel, void* stream, int q_len = 1, const float* k_scale = nullptr,
+                const float* v_scale = nullptr) {
     clear_error();
+    const bool fp8 = k_scale != nullptr;
+    if (fp8 && (!v_scale || !aligned(k_scale, 4) || !aligned(v_scale, 4)))
+        return fail(PA_ERR_INVALID_ARG, "pa_decode_fp8: k_scale/v_scale must be non-NULL and 4-byte aligned");
+    if (fp8 && (!aligned(query, 16) || !aligned(out, 16)))
+        return fail(PA_ERR_INVALID_ARG, "pa_decode_fp8: query and out must be 16-byte aligned");
     if (num_seqs < 0) return fail(PA_ERR_INVALID_ARG, "pa_decode: num_seqs=%d", num_seqs);
     if (new_key && (!new_value || !aligned(new_key, 16) || !aligned(new_value, 16)))
         return fail(PA_ERR_INVALID_ARG, "pa_decode_append: new_key/new_value must be non-NULL and 16-byte aligned");
@@ -612,16 +662,17 @@ int decode_impl(void* out, const void* query, const void* new_key, const void* n
     Plan p;
     int st = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, dtype,
                        workspace != nullptr && workspace_bytes > 0, workspace ? workspace_bytes : 0, max_context_len,
-                       partition_pages, kernel, &p, q_len);
+                       partition_pages, kernel, &p, q_len, fp8);
     if (st != PA_OK) return st;
     DeviceState* dev = nullptr;
     st = current_device_state(&dev);
     if (st != PA_OK) return st;
 
     CUtensorMap tk, tv;
-    st = encode_cache_map(&tk, key_cache, dtype, num_blocks, num_kv_heads, block_size, head_dim);
+    const int cache_type = fp8 ? kCacheE4M3 : dtype;
+    st = encode_cache_map(&tk, key_cache, cache_type, num_blocks, num_kv_heads, block_size, head_dim);
     if (st != PA_OK) return st;
-    st = encode_cache_map(&tv, value_cache, dtype, num_blocks, num_kv_heads, block_size, head_dim);
+    st = encode_cache_map(&tv, value_cache, cache_type, num_blocks, num_kv_heads, block_size, head_dim);
     if (st != PA_OK) return st;
 
     DecodeArgs a{};
@@ -641,6 +692,8 @@ int decode_impl(void* out, const void* query, const void* new_key, const void* n
     a.new_value = new_key ? new_value : nullptr;
     a.key_cache = new_key ? const_cast<void*>(key_cache) : nullptr;
     a.value_cache = new_key ? const_cast<void*>(value_cache) : nullptr;
+    a.k_scale = k_scale;
+    a.v_scale = v_scale;
     a.lean_warps_per_cta = p.ki.lean_warps_per_cta;
     a.err = dev->error_word;
     a.num_seqs = num_seqs;
@@ -657,8 +710,9 @@ int decode_impl(void* out, const void* query, const void* new_key, const void* n
     a.max_parts = p.max_parts;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);  // log2(e)
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaError_t e =
-        decode_launch(dtype, head_dim, block_size, p.dkind, p.gmax, p.schedule, tk, tv, a, (int)p.grid, num_seqs, s);
+    cudaError_t e = fp8 ? decode_launch_fp8(dtype, head_dim, block_size, tk, tv, a, (int)p.grid, num_seqs, s)
+                        : decode_launch(dtype, head_dim, block_size, p.dkind, p.gmax, p.schedule, tk, tv, a,
+                                        (int)p.grid, num_seqs, s);
     if (e != cudaSuccess) return cuda_fail(e, "pa_decode: decode kernel launch");
     if (grid_split) {
         MergeArgs m{out, context_lens, a.ws_m, a.ws_l, a.ws_o, num_seqs, num_heads, block_size, max_blocks_per_seq,
@@ -736,6 +790,54 @@ size_t pa_decode_multi_workspace_size(int num_seqs, int q_len, int num_heads, in
                   (size_t)-1, 0, 0, PA_KERNEL_AUTO, &p, q_len) != PA_OK)
         return 0;
     return p.ws_bytes;
+}
+
+int pa_decode_fp8(void* out, const void* query, const void* key_cache, const void* value_cache, const float* k_scale,
+                  const float* v_scale, const int32_t* block_tables, const int32_t* context_lens, int num_seqs,
+                  int num_heads, int num_kv_heads, int head_dim, int block_size, int max_blocks_per_seq,
+                  int num_blocks, float scale, int dtype, void* workspace, size_t workspace_bytes, void* stream) {
+    if (!k_scale) {
+        clear_error();
+        return fail(PA_ERR_INVALID_ARG, "pa_decode_fp8: k_scale is NULL");
+    }
+    return decode_impl(out, query, nullptr, nullptr, key_cache, value_cache, block_tables, context_lens, num_seqs,
+                       num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype,
+                       workspace, workspace_bytes, 0, 0, PA_KERNEL_AUTO, stream, 1, k_scale, v_scale);
+}
+
+size_t pa_decode_fp8_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
+                                    int max_blocks_per_seq, int dtype) {
+    Plan p;
+    if (make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, dtype, true,
+                  (size_t)-1, 0, 0, PA_KERNEL_AUTO, &p, 1, true) != PA_OK)
+        return 0;
+    return p.ws_bytes;
+}
+
+int pa_write_kv_fp8(const void* key, const void* value, void* key_cache, void* value_cache, const float* k_scale,
+                    const float* v_scale, const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
+                    int block_size, int num_blocks, int dtype, void* stream) {
+    clear_error();
+    if (!dtype_ok(dtype)) return fail(PA_ERR_INVALID_ARG, "pa_write_kv_fp8: unknown source dtype %d", dtype);
+    if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || head_dim % 4 != 0 || block_size <= 0 ||
+        num_blocks < 0)
+        return fail(PA_ERR_INVALID_ARG, "pa_write_kv_fp8: bad sizes (head_dim must be a multiple of 4)");
+    if (num_tokens == 0) return PA_OK;
+    if (!key || !value || !key_cache || !value_cache || !k_scale || !v_scale || !slot_mapping)
+        return fail(PA_ERR_INVALID_ARG, "pa_write_kv_fp8: NULL pointer");
+    const int eb = elem_bytes(dtype);
+    if (!aligned(slot_mapping, 8) || !aligned(key, eb) || !aligned(value, eb) || !aligned(key_cache, 4) ||
+        !aligned(value_cache, 4) || !aligned(k_scale, 4) || !aligned(v_scale, 4))
+        return fail(PA_ERR_INVALID_ARG, "pa_write_kv_fp8: misaligned buffer");
+    DeviceState* dev = nullptr;
+    int st = current_device_state(&dev);
+    if (st != PA_OK) return st;
+    WriteFp8Args a{key, value, static_cast<uint8_t*>(key_cache), static_cast<uint8_t*>(value_cache), k_scale, v_scale,
+                   slot_mapping, num_tokens, num_kv_heads, head_dim, block_size, num_blocks, dtype,
+                   dev->error_word};
+    cudaError_t e = write_kv_fp8_launch(a, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pa_write_kv_fp8 launch");
+    return PA_OK;
 }
 
 int pa_decode(void* out, const void* query, const void* key_cache, const void* value_cache,

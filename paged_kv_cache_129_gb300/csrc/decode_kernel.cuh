@@ -40,6 +40,8 @@
 #include <cfloat>
 #include <type_traits>
 
+#include <cuda_fp8.h>
+
 #include "decode_launch.h"
 #include "pa_common.cuh"
 
@@ -407,6 +409,210 @@ struct MmaConsumer {
             hi[mt * 16 + g] = o[mt][1];
             lo[mt * 16 + 8 + g] = o[mt][2];
             hi[mt * 16 + 8 + g] = o[mt][3];
+        }
+    }
+};
+
+// ------------------------------------------------------------------------------------------
+// Tensor-core consumer for an FP8 (E4M3) cache with a float32 scale per (physical block,
+// kv head) for K and for V.  The codes are widened to f16 exactly (e4m3x2 -> f16x2) and
+// multiplied on the f16 tensor path with fp32 accumulation; the page's K scale multiplies
+// its scores, its V scale enters through the running output's rescale factor (the output
+// is kept in units of the current page's V scale).  The query row is brought to f16 exactly
+// by a power of two (its largest magnitude lands in [2^14, 2^15)), undone in the score
+// factor, so bf16 and f16 queries of any range stay exact.
+//
+// Fragment layouts (m16n8k16 f16, g = lane / 4, c = lane % 4):
+//  * S = Q K^T: the k index of a k-step is a permutation of d shared by both operands:
+//    lane c owns d in [32c, 32c + 32) and k-step kk takes its bytes 4kk .. 4kk + 3
+//    (k = 2c, 2c+1 -> 32c + 4kk + {0, 1};  k = 2c+8, 2c+9 -> 32c + 4kk + {2, 3}), so a
+//    token's K row is two 16-byte shared-memory loads per lane.
+//  * O^T += V^T P^T: m-tile i maps row g to d = 16g + 2i and row g+8 to d = 16g + 2i + 1,
+//    so lane g reads bytes 16g .. 16g+15 of four V rows (one 16-byte load each) and the
+//    token pairs of the A fragment come from byte permutes; the lane ends up holding
+//    d = 16g .. 16g+15 of its two output rows.
+// Both patterns are free of bank conflicts under the 128-byte swizzle.
+__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair16) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair16), __NV_E4M3);
+    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+}
+
+template <typename T, int D, int BS>
+struct MmaConsumerF8 {
+    static_assert(D == 128, "the FP8 consumer's lane layout is for head_dim 128");
+    static_assert(BS % 16 == 0, "16-token sub-tiles");
+    static constexpr int KS = D / 16;  // k-steps of QK^T, m-tiles of PV
+    uint32_t qa[KS][2];                // f16 Q fragments, rows 0..7 (rows 8..15 are zero)
+    float o[KS][4];                    // O^T fragments, in units of vs_cur
+    float m, l;
+    float qf;                          // this row's score factor: 2^-e * scale * log2(e)
+    float vs_cur;                      // V scale o is expressed in (0 before the first page)
+
+    // q_row: this lane's query row (row lane / 4 of the unit), read only when live.
+    __device__ __forceinline__ void init(const T* q_row, bool live, float scale_log2, int lane) {
+        const int c = lane & 3;
+        float x[32];
+        const uint4* src = reinterpret_cast<const uint4*>(q_row + c * (D / 4));
+#pragma unroll
+        for (int i = 0; i < 4; ++i) unpack16<T>(live ? __ldg(src + i) : make_uint4(0u, 0u, 0u, 0u), x + 8 * i);
+        float amax = 0.f;
+#pragma unroll
+        for (int i = 0; i < 32; ++i) amax = fmaxf(amax, fabsf(x[i]));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        int e = 0;
+        if (amax > 0.f) {
+            int ex;
+            frexpf(amax, &ex);  // amax = f * 2^ex, f in [0.5, 1)
+            e = min(max(15 - ex, -126), 127);
+        }
+        const float p2 = __int_as_float((e + 127) << 23);  // 2^e, exact
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            const __half2 lo = __floats2half2_rn(x[4 * kk] * p2, x[4 * kk + 1] * p2);
+            const __half2 hi = __floats2half2_rn(x[4 * kk + 2] * p2, x[4 * kk + 3] * p2);
+            qa[kk][0] = *reinterpret_cast<const uint32_t*>(&lo);
+            qa[kk][1] = *reinterpret_cast<const uint32_t*>(&hi);
+#pragma unroll
+            for (int r = 0; r < 4; ++r) o[kk][r] = 0.f;
+        }
+        qf = scale_log2 * __int_as_float((127 - e) << 23);  // 2^-e
+        m = -INFINITY;
+        l = 0.f;
+        vs_cur = 0.f;
+    }
+
+    // One page (BS tokens, nvalid of them inside the context) with its K and V scales.
+    __device__ __forceinline__ void page(const uint8_t* kpage, uint8_t* vpage, int nvalid, float ks, float vs,
+                                         int lane) {
+        const int g = lane >> 2, c = lane & 3;
+        float vr = vs_cur == 0.f ? 1.f : vs_cur / vs;  // o into units of this page's V scale
+        vs_cur = vs;
+        const float sf = qf * ks;
+#pragma unroll
+        for (int sub = 0; sub < BS / 16; ++sub) {
+            const int nv = nvalid - sub * 16;
+            if (nv <= 0) break;
+            if (nv < 16) {
+                // V rows past the context may hold anything (NaN codes included): zero them.
+                for (int idx = lane; idx < (16 - nv) * 8; idx += 32)
+                    *reinterpret_cast<uint4*>(vpage + (sub * 16 + nv + idx / 8) * 128 + (idx % 8) * 16) =
+                        make_uint4(0u, 0u, 0u, 0u);
+                fence_proxy_async_smem();
+                __syncwarp();
+            }
+            // ---- S = Q K^T: two n-tiles of 8 tokens ----
+            float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int tok = sub * 16 + nt * 8 + g;
+                const uint8_t* row = kpage + tok * 128;
+                const uint4 k0 = *reinterpret_cast<const uint4*>(row + (((2 * c) ^ (tok & 7)) << 4));
+                const uint4 k1 = *reinterpret_cast<const uint4*>(row + (((2 * c + 1) ^ (tok & 7)) << 4));
+                const uint32_t w[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
+#pragma unroll
+                for (int kk = 0; kk < KS; ++kk)
+                    Mma<__half>::run(s[nt], qa[kk][0], 0u, qa[kk][1], 0u, e4m3x2_to_f16x2(w[kk] & 0xffffu),
+                                     e4m3x2_to_f16x2(w[kk] >> 16));
+            }
+            // ---- online softmax for row g over tokens 2c, 2c+1, 8+2c, 9+2c ----
+            const float x0 = (2 * c < nv) ? s[0][0] * sf : -INFINITY;
+            const float x1 = (2 * c + 1 < nv) ? s[0][1] * sf : -INFINITY;
+            const float x2 = (8 + 2 * c < nv) ? s[1][0] * sf : -INFINITY;
+            const float x3 = (9 + 2 * c < nv) ? s[1][1] * sf : -INFINITY;
+            float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float m_new = fmaxf(m, mx);  // token 0 of the sub-tile is attended: finite
+            const float alpha = exp2f(m - m_new);
+            float r0, r1, r2, r3;
+            const uint32_t pb0 = Mma<__half>::pack(exp2f(x0 - m_new), exp2f(x1 - m_new), r0, r1);
+            const uint32_t pb1 = Mma<__half>::pack(exp2f(x2 - m_new), exp2f(x3 - m_new), r2, r3);
+            l = l * alpha + ((r0 + r1) + (r2 + r3));
+            m = m_new;
+            const float a_lo = __shfl_sync(0xffffffffu, alpha, (2 * c) * 4) * vr;
+            const float a_hi = __shfl_sync(0xffffffffu, alpha, (2 * c + 1) * 4) * vr;
+            vr = 1.f;
+            // ---- O^T += V^T P^T ----
+            const int t0 = sub * 16 + 2 * c;
+            const uint4 v0 = *reinterpret_cast<const uint4*>(vpage + t0 * 128 + ((g ^ (t0 & 7)) << 4));
+            const uint4 v1 = *reinterpret_cast<const uint4*>(vpage + (t0 + 1) * 128 + ((g ^ ((t0 + 1) & 7)) << 4));
+            const uint4 v2 = *reinterpret_cast<const uint4*>(vpage + (t0 + 8) * 128 + ((g ^ ((t0 + 8) & 7)) << 4));
+            const uint4 v3 = *reinterpret_cast<const uint4*>(vpage + (t0 + 9) * 128 + ((g ^ ((t0 + 9) & 7)) << 4));
+            const uint32_t w0[4] = {v0.x, v0.y, v0.z, v0.w}, w1[4] = {v1.x, v1.y, v1.z, v1.w};
+            const uint32_t w2[4] = {v2.x, v2.y, v2.z, v2.w}, w3[4] = {v3.x, v3.y, v3.z, v3.w};
+#pragma unroll
+            for (int i = 0; i < KS; ++i) {
+                const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;  // bytes 2(i&1), 2(i&1)+1 of both words
+                const uint32_t p01 = __byte_perm(w0[i >> 1], w1[i >> 1], sel);
+                const uint32_t p23 = __byte_perm(w2[i >> 1], w3[i >> 1], sel);
+                o[i][0] *= a_lo;
+                o[i][1] *= a_hi;
+                o[i][2] *= a_lo;
+                o[i][3] *= a_hi;
+                Mma<__half>::run(o[i], e4m3x2_to_f16x2(p01 & 0xffffu), e4m3x2_to_f16x2(p01 >> 16),
+                                 e4m3x2_to_f16x2(p23 & 0xffffu), e4m3x2_to_f16x2(p23 >> 16), pb0, pb1);
+            }
+        }
+    }
+
+    __device__ __forceinline__ void finish() {
+        l += __shfl_xor_sync(0xffffffffu, l, 1);
+        l += __shfl_xor_sync(0xffffffffu, l, 2);
+    }
+
+    __device__ __forceinline__ void clear() {
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            qa[kk][0] = qa[kk][1] = 0u;
+#pragma unroll
+            for (int e = 0; e < 4; ++e) o[kk][e] = 0.f;
+        }
+        m = -INFINITY;
+        l = 0.f;
+        vs_cur = 0.f;
+    }
+
+    // out[row(r) * D + d] = o~ / l for the gc rows (after finish()); a row with l = 0 gets zeros.
+    __device__ __forceinline__ void write_out(T* out, const UnitRows& rows, int gc, int lane) const {
+        const int g = lane >> 2, c = lane & 3;
+        const float l_lo = __shfl_sync(0xffffffffu, l, (2 * c) * 4);
+        const float l_hi = __shfl_sync(0xffffffffu, l, (2 * c + 1) * 4);
+        const float f_lo = l_lo > 0.f ? vs_cur / l_lo : 0.f;
+        const float f_hi = l_hi > 0.f ? vs_cur / l_hi : 0.f;
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int r = 2 * c + half;
+            if (r >= gc) continue;
+            const float f = half ? f_hi : f_lo;
+            T v[16];
+#pragma unroll
+            for (int i = 0; i < KS; ++i) {
+                v[2 * i] = from_float<T>(o[i][half] * f);
+                v[2 * i + 1] = from_float<T>(o[i][2 + half] * f);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(out + rows.row(r) * D + 16 * g);
+            dst[0] = *reinterpret_cast<const uint4*>(v);
+            dst[1] = *reinterpret_cast<const uint4*>(v + 8);
+        }
+    }
+
+    // Partial record of 8 rows: m[8], l[8], o~[8][D] in true units (after finish()).
+    __device__ __forceinline__ void write_partial(float* rec, int gc, int lane) const {
+        const int g = lane >> 2, c = lane & 3;
+        if (c == 0 && g < gc) {
+            rec[g] = m;
+            rec[8 + g] = l;
+        }
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            const int r = 2 * c + half;
+            if (r >= gc) continue;
+            float4* dst = reinterpret_cast<float4*>(rec + 16 + (size_t)r * D + 16 * g);
+#pragma unroll
+            for (int q4 = 0; q4 < 4; ++q4)
+                dst[q4] = make_float4(o[2 * q4][half] * vs_cur, o[2 * q4][2 + half] * vs_cur,
+                                      o[2 * q4 + 1][half] * vs_cur, o[2 * q4 + 1][2 + half] * vs_cur);
         }
     }
 };
@@ -1038,11 +1244,15 @@ __device__ __forceinline__ void lean_locate(const int* pre, int num_seqs, int up
 }
 
 
-template <typename T, int D, int BS, bool MMA, int GMAX, bool CAUSAL>
-__global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (LeanCfg<T, D, BS, MMA, GMAX>::kMinBlocks))
+// F8: the caches hold E4M3 codes with a scale per (block, kv head) (MmaConsumerF8); T is then
+// the query and output type.
+template <typename T, int D, int BS, bool MMA, int GMAX, bool CAUSAL, bool F8 = false>
+__global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
+                                  (LeanCfg<std::conditional_t<F8, uint8_t, T>, D, BS, MMA, GMAX>::kMinBlocks))
     paged_decode_lean_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                              const DecodeArgs a) {
-    using C = LeanCfg<T, D, BS, MMA, GMAX>;
+    using C = LeanCfg<std::conditional_t<F8, uint8_t, T>, D, BS, MMA, GMAX>;
+    static_assert(!F8 || (MMA && !CAUSAL), "the FP8 path is the single-query tensor-core consumer");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* ring = smem;
@@ -1191,10 +1401,15 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Lea
         int b = 0, uu = 0, nb = 0, L = 0, gc = 0, kvh = 0;
         UnitRows rows{0, 0, 0, a.q_len, a.group, a.num_heads};
         int wrote = 0;  // bit s: a partial record was written to slot s
-        const bool append = a.new_key != nullptr;
+        const bool append = !F8 && a.new_key != nullptr;
         NewToken<T, D, BS> tok;
         bool tok_ready = false, tok_writer = false;
-        std::conditional_t<MMA, MmaConsumer<T, D, BS, CAUSAL>, SimtConsumer<T, D, BS, GMAX>> cons;
+        std::conditional_t<F8, MmaConsumerF8<T, D, BS>,
+                           std::conditional_t<MMA, MmaConsumer<T, D, BS, CAUSAL>, SimtConsumer<T, D, BS, GMAX>>>
+            cons;
+        // FP8: lane i holds the K and V scales of page 32 * chunk + i of the current chunk
+        // (cur_*) and of the next one (pend_*, loaded when that chunk is published).
+        float cur_ks = 0.f, cur_vs = 0.f, pend_ks = 0.f, pend_vs = 0.f;
         float* q_s = reinterpret_cast<float*>(smem + C::kQsOffset) + warp * GMAX * D;
         float* p_s = reinterpret_cast<float*>(smem + C::kPsOffset) + warp * GMAX * BS;
         // Page rows for the producer, published in chunks of 32: chunk c + 1 when this warp
@@ -1211,6 +1426,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Lea
                 pend_pb = __ldg(a.block_tables + (size_t)sb * a.max_blocks + sj);
             }
             if (chunk == 0) {
+                if constexpr (F8) {
+                    const bool ok = page < n && (unsigned)pend_pb < (unsigned)a.num_blocks;
+                    cur_ks = ok ? __ldg(a.k_scale + pend_pb * a.num_kv_heads + pend_kvh) : 0.f;
+                    cur_vs = ok ? __ldg(a.v_scale + pend_pb * a.num_kv_heads + pend_kvh) : 0.f;
+                }
                 if (page < n)
                     queue[page] = (unsigned)pend_pb < (unsigned)a.num_blocks
                                       ? (pend_pb * a.num_kv_heads + pend_kvh) * BS
@@ -1223,9 +1443,20 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Lea
             }
         }
         for (int off = 0; off < n; ++off) {
+            if constexpr (F8) {
+                if ((off & 31) == 0 && off > 0) {
+                    cur_ks = pend_ks;
+                    cur_vs = pend_vs;
+                }
+            }
             if ((off & 31) == 16) {
                 const int c = (off >> 5) + 1;  // the chunk published now
                 const int page = 32 * c + lane;
+                if constexpr (F8) {
+                    const bool ok = page < n && (unsigned)pend_pb < (unsigned)a.num_blocks;
+                    pend_ks = ok ? __ldg(a.k_scale + pend_pb * a.num_kv_heads + pend_kvh) : 0.f;
+                    pend_vs = ok ? __ldg(a.v_scale + pend_pb * a.num_kv_heads + pend_kvh) : 0.f;
+                }
                 if (page < n)
                     queue[page % C::kRowQueue] = (unsigned)pend_pb < (unsigned)a.num_blocks
                                                      ? (pend_pb * a.num_kv_heads + pend_kvh) * BS
@@ -1258,7 +1489,10 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Lea
                 L = __ldg(a.context_lens + b);
                 L = L < 0 ? 0 : (L > l_cap ? l_cap : L);
                 const T* q = static_cast<const T*>(a.q);
-                if constexpr (MMA) {
+                if constexpr (F8) {
+                    const int r = min(lane >> 2, gc - 1);
+                    cons.init(q + rows.row(r) * D, (lane >> 2) < gc, a.scale_log2, lane);
+                } else if constexpr (MMA) {
                     const int r = min(lane >> 2, gc - 1);
                     cons.init(q + rows.row(r) * D, (lane >> 2) < gc, rows.last_pos(lane >> 2, L), lane);
                 } else {
@@ -1288,7 +1522,12 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Lea
                 if (tok_writer && row >= 0) tok.store(a.key_cache, a.value_cache, row + nvalid - 1, lane);
                 tok_ready = false;
             }
-            if constexpr (MMA) {
+            if constexpr (F8) {
+                const float ks = __shfl_sync(0xffffffffu, cur_ks, off & 31);
+                const float vs = __shfl_sync(0xffffffffu, cur_vs, off & 31);
+                cons.page(kp, kp + C::kPageBytes, nvalid, ks, vs, lane);
+                __syncwarp();
+            } else if constexpr (MMA) {
                 cons.page(kp, kp + C::kPageBytes, nvalid, j * BS, a.scale_log2, lane);
                 __syncwarp();
             } else {
@@ -1595,6 +1834,68 @@ struct DecodeKernel {
             return launch_pdl(paged_decode_kernel<T, D, BS, MMA, GMAX, CAUSAL>, dim3(grid), dim3(C::kThreads), C::kSmemBytes,
                               stream, k, v, a);
         }
+    }
+};
+
+// FP8 caches: the lean decode with the FP8 consumer and the lean merge (no partitioned grid).
+template <typename T, int D, int BS>
+struct DecodeKernelF8 {
+    using LC = LeanCfg<uint8_t, D, BS, true, 8>;
+
+    static bool configure(int device) {
+        static unsigned long long done_mask = 0;
+        const unsigned long long bit = 1ull << (device & 63);
+        if (done_mask & bit) return true;
+        if (cudaFuncSetAttribute(paged_decode_lean_kernel<T, D, BS, true, 8, false, true>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize, LC::kMaxSmemBytes) != cudaSuccess)
+            return false;
+        done_mask |= bit;
+        return true;
+    }
+
+    static bool info(int num_seqs, KernelInfo* info) {
+        int device = 0;
+        if (cudaGetDevice(&device) != cudaSuccess) return false;
+        if (!configure(device)) return false;
+        const int seqs = num_seqs < 1 ? 1 : (num_seqs > kLeanMaxSeqs ? kLeanMaxSeqs : num_seqs);
+        const int smem = LC::smem_bytes(seqs);
+        static std::atomic<int> cache[64][232];
+        const int kb = (smem + 1023) / 1024;
+        std::atomic<int>& slot = cache[device & 63][kb < 232 ? kb : 231];
+        int n = slot.load(std::memory_order_relaxed);
+        if (n <= 0) {
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_lean_kernel<T, D, BS, true, 8, false, true>,
+                                                              LC::kThreads, kb * 1024) != cudaSuccess ||
+                n <= 0)
+                n = 1;
+            slot.store(n, std::memory_order_relaxed);
+        }
+        info->threads = LC::kThreads;
+        info->smem_bytes = 0;
+        info->heads_per_cta = LC::kHeads;
+        info->ctas_per_sm = 0;
+        info->merge_parts_cap = 0;
+        info->lean_smem_bytes = smem;
+        info->lean_ctas_per_sm = n;
+        info->lean_warps_per_cta = LC::kNW;
+        info->lean_record_floats = LC::kRecFloats;
+        info->lean_max_seqs = kLeanMaxSeqs;
+        return true;
+    }
+
+    static cudaError_t launch(const CUtensorMap& k, const CUtensorMap& v, const DecodeArgs& a, int grid, int num_seqs,
+                              cudaStream_t stream) {
+        int device = 0;
+        cudaError_t e = cudaGetDevice(&device);
+        if (e != cudaSuccess) return e;
+        if (!configure(device)) return cudaGetLastError();
+        e = launch_pdl(paged_decode_lean_kernel<T, D, BS, true, 8, false, true>, dim3(grid), dim3(LC::kThreads),
+                       LC::smem_bytes(num_seqs), stream, k, v, a);
+        if (e != cudaSuccess) return e;
+        DecodeArgs m = a;
+        m.lean_grid = grid;
+        return launch_pdl(lean_merge_kernel<T, D, LC::kHeads, BS>, dim3(a.num_seqs * a.num_kv_heads * a.head_chunks),
+                          dim3(kLeanMergeThreads), 0, stream, m);
     }
 };
 

@@ -27,6 +27,9 @@ struct DecodeArgs {
     const void* new_value;
     void* key_cache;
     void* value_cache;
+    // FP8 caches (E4M3 codes): float32 scales [num_blocks, num_kv_heads] for K and V.
+    const float* k_scale;
+    const float* v_scale;
     int num_seqs, num_heads, num_kv_heads, group, head_chunks;
     // Multi-query decode: q_len query tokens per sequence at positions L - q_len .. L - 1
     // (q_len = 1: single-step decode).  A kv head serves rows = q_len * group query rows,
@@ -92,6 +95,12 @@ cudaError_t decode_launch_f16(int head_dim, int block_size, int kind, int gmax, 
 cudaError_t decode_launch_bf16(int head_dim, int block_size, int kind, int gmax, int schedule,
                               const CUtensorMap& tmap_k, const CUtensorMap& tmap_v, const DecodeArgs& args,
                               int grid, int num_seqs, cudaStream_t stream);
+// FP8 (E4M3) caches: the lean schedule with the FP8 tensor-core consumer; dtype is the
+// query/output type (PA_F16 or PA_BF16).
+bool decode_kernel_info_fp8(int dtype, int head_dim, int block_size, int num_seqs, KernelInfo* info);
+cudaError_t decode_launch_fp8(int dtype, int head_dim, int block_size, const CUtensorMap& tmap_k,
+                              const CUtensorMap& tmap_v, const DecodeArgs& args, int grid, int num_seqs,
+                              cudaStream_t stream);
 cudaError_t merge_launch_f32(int head_dim, const MergeArgs& args, cudaStream_t stream);
 cudaError_t merge_launch_f16(int head_dim, const MergeArgs& args, cudaStream_t stream);
 cudaError_t merge_launch_bf16(int head_dim, const MergeArgs& args, cudaStream_t stream);

@@ -4,6 +4,8 @@
 #include <algorithm>
 #include <cstdint>
 
+#include <cuda_fp8.h>
+
 #include "kv_ops.h"
 #include "pa_common.cuh"
 
@@ -71,6 +73,55 @@ __global__ void __launch_bounds__(256) write_kv_layers_kernel(const LayerPtrs la
     for (int i = lane; i < row_vecs; i += 32) {
         key_cache[dst + i] = __ldg(key + src + i);
         value_cache[dst + i] = __ldg(value + src + i);
+    }
+}
+
+// Paged write into an FP8 (E4M3) cache: one warp per (token, kv head); element i of the row
+// becomes e4m3(x / scale[block, head]) (the division in float32, round to nearest even,
+// saturating to +-448, NaN kept), four elements per lane and step.
+template <typename S>
+__global__ void __launch_bounds__(256) write_kv_fp8_kernel(const S* __restrict__ key, const S* __restrict__ value,
+                                                           uint8_t* __restrict__ key_cache,
+                                                           uint8_t* __restrict__ value_cache,
+                                                           const float* __restrict__ k_scale,
+                                                           const float* __restrict__ v_scale,
+                                                           const int64_t* __restrict__ slots, int num_tokens,
+                                                           int num_kv_heads, int head_dim, int block_size,
+                                                           long long num_slots, unsigned* err) {
+    griddep_wait();
+    griddep_launch_dependents();
+    const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
+    if (gw >= (long long)num_tokens * num_kv_heads) return;
+    const int lane = threadIdx.x & 31;
+    const int t = (int)(gw / num_kv_heads);
+    const int h = (int)(gw - (long long)t * num_kv_heads);
+    const long long slot = __ldg(slots + t);
+    if (slot < 0) return;
+    if (slot >= num_slots) {
+        if (lane == 0 && h == 0) atomicOr(err, kErrBadSlot);
+        return;
+    }
+    const long long blk = slot / block_size;
+    const long long off = slot - blk * block_size;
+    const float ks = __ldg(k_scale + blk * num_kv_heads + h);
+    const float vs = __ldg(v_scale + blk * num_kv_heads + h);
+    const size_t src = ((size_t)t * num_kv_heads + h) * head_dim;
+    const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + off) * head_dim;
+    for (int i = 4 * lane; i < head_dim; i += 128) {
+        float xk[4], xv[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            xk[e] = to_float(key[src + i + e]) / ks;
+            xv[e] = to_float(value[src + i + e]) / vs;
+        }
+        const uint32_t ck = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(xk[0], xk[1]), __NV_SATFINITE, __NV_E4M3) |
+                            ((uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(xk[2], xk[3]), __NV_SATFINITE, __NV_E4M3)
+                             << 16);
+        const uint32_t cv = (uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(xv[0], xv[1]), __NV_SATFINITE, __NV_E4M3) |
+                            ((uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(xv[2], xv[3]), __NV_SATFINITE, __NV_E4M3)
+                             << 16);
+        *reinterpret_cast<uint32_t*>(key_cache + dst + i) = ck;
+        *reinterpret_cast<uint32_t*>(value_cache + dst + i) = cv;
     }
 }
 
@@ -235,6 +286,32 @@ cudaError_t write_kv_layers_launch(const WriteLayersArgs& a, cudaStream_t stream
         case 4: return write_layers_typed<uint32_t>(a, row_bytes, stream);
         case 2: return write_layers_typed<uint16_t>(a, row_bytes, stream);
         default: return write_layers_typed<uint8_t>(a, row_bytes, stream);
+    }
+}
+
+cudaError_t write_kv_fp8_launch(const WriteFp8Args& a, cudaStream_t stream) {
+    const long long warps = (long long)a.num_tokens * a.num_kv_heads;
+    const int threads = 256;
+    const long long grid = (warps + (threads / 32) - 1) / (threads / 32);
+    const long long num_slots = (long long)a.num_blocks * a.block_size;
+    switch (a.src_dtype) {
+        case 0:
+            return launch_pdl(write_kv_fp8_kernel<float>, dim3((unsigned)grid), dim3(threads), 0, stream,
+                              static_cast<const float*>(a.key), static_cast<const float*>(a.value), a.key_cache,
+                              a.value_cache, a.k_scale, a.v_scale, a.slot_mapping, a.num_tokens, a.num_kv_heads,
+                              a.head_dim, a.block_size, num_slots, a.err);
+        case 1:
+            return launch_pdl(write_kv_fp8_kernel<__half>, dim3((unsigned)grid), dim3(threads), 0, stream,
+                              static_cast<const __half*>(a.key), static_cast<const __half*>(a.value), a.key_cache,
+                              a.value_cache, a.k_scale, a.v_scale, a.slot_mapping, a.num_tokens, a.num_kv_heads,
+                              a.head_dim, a.block_size, num_slots, a.err);
+        case 2:
+            return launch_pdl(write_kv_fp8_kernel<__nv_bfloat16>, dim3((unsigned)grid), dim3(threads), 0, stream,
+                              static_cast<const __nv_bfloat16*>(a.key), static_cast<const __nv_bfloat16*>(a.value),
+                              a.key_cache, a.value_cache, a.k_scale, a.v_scale, a.slot_mapping, a.num_tokens,
+                              a.num_kv_heads, a.head_dim, a.block_size, num_slots, a.err);
+        default:
+            return cudaErrorInvalidValue;
     }
 }
 

@@ -61,10 +61,24 @@ struct DeltaArgs {
     unsigned* err;
 };
 
+struct WriteFp8Args {
+    const void* key;
+    const void* value;
+    uint8_t* key_cache;
+    uint8_t* value_cache;
+    const float* k_scale;
+    const float* v_scale;
+    const int64_t* slot_mapping;
+    int num_tokens, num_kv_heads, head_dim, block_size, num_blocks;
+    int src_dtype;  // PA_F32, PA_F16 or PA_BF16
+    unsigned* err;
+};
+
 cudaError_t write_kv_launch(const WriteArgs& args, cudaStream_t stream);
 cudaError_t copy_blocks_launch(const CopyArgs& args, cudaStream_t stream);
 cudaError_t swap_blocks_launch(const SwapArgs& args, cudaStream_t stream);
 cudaError_t write_kv_layers_launch(const WriteLayersArgs& args, cudaStream_t stream);
 cudaError_t apply_table_deltas_launch(const DeltaArgs& args, cudaStream_t stream);
+cudaError_t write_kv_fp8_launch(const WriteFp8Args& args, cudaStream_t stream);
 
 }  // namespace pa

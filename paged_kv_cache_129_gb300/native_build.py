@@ -20,7 +20,8 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libpagedkv.so")
 
-CUDA_SOURCES = ["capi.cu", "kv_ops.cu", "decode_f32.cu", "decode_f16.cu", "decode_bf16.cu", "decode_static_scratch.cu"]
+CUDA_SOURCES = ["capi.cu", "kv_ops.cu", "decode_f32.cu", "decode_f16.cu", "decode_bf16.cu", "decode_fp8.cu",
+                "decode_static_scratch.cu"]
 CXX_SOURCES = ["block_pool.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

@@ -64,6 +64,19 @@ def cast_from_f32(x: np.ndarray, dtype: str) -> np.ndarray:
     raise ValueError(f"unknown dtype {dtype!r}")
 
 
+def fp8_scales(cache: np.ndarray, dtype: str) -> np.ndarray:
+    """Input construction for FP8 caches: a float32 scale per (block, kv head) that maps the
+    largest magnitude of that block's source values onto 448, the largest E4M3 code
+    (``cache`` is a source cache ``[N, H_kv, bs, d]`` in ``dtype`` storage form).  Choosing the
+    scales is the caller's policy; this is the one the tests and the benchmark use."""
+    if dtype == "bf16":
+        vals = (cache.astype(np.uint32) << np.uint32(16)).view(np.float32)
+    else:
+        vals = cache.astype(np.float32)
+    amax = np.abs(vals).max(axis=(2, 3))
+    return (np.maximum(amax, np.float32(2.0 ** -10)) / np.float32(448.0)).astype(np.float32)
+
+
 def default_scale(head_dim: int) -> float:
     """1/sqrt(d), rounded to float32 (the value the C ABI receives)."""
     return float(np.float32(1.0 / math.sqrt(head_dim)))

@@ -1,0 +1,163 @@
+"""GPU parity of the FP8 (E4M3) KV-cache path against the oracle.
+
+* pa_write_kv_fp8: bit-exact against the oracle's quantiser for bf16 / f16 / f32 sources,
+  saturating and NaN inputs, padding slots, a bad slot flagged;
+* pa_decode_fp8: within the bf16/f16 tolerance (|err| <= 2e-2 + 1e-2 |ref|) of the oracle's
+  fp64 attention over the same codes and scales, on ragged contexts (L = 0, 1, 15, 16, 17, ...)
+  at block sizes 16 and 32, NaN codes in the slots past each context, scales that differ per
+  (block, kv head), and queries of magnitudes far outside f16's range;
+* the Qwen-shaped layer at full size (the shape the benchmark times): the caches written by
+  the GPU writer equal the oracle's byte for byte, and sampled output rows match the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import paged_kv_cache_129_gb300 as pa
+from paged_kv_cache_129_gb300 import workloads as wl
+from helpers import TORCH_DTYPE, assert_decode_close, to_device, to_f64
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def gpu():
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device; the CUDA path has no fallback"
+    pa.build()
+    pa.library()
+    yield
+    pa.check_error()
+
+
+def _src(rng, shape, dtype, mult=1.0):
+    x = (rng.standard_normal(shape) * mult).astype(np.float32)
+    return wl.cast_from_f32(x, dtype)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16", "f32"])
+def test_write_kv_fp8_bit_exact(dtype):
+    rng = np.random.default_rng(11)
+    nb, hkv, bs, d, T = 9, 4, 16, 128, 40
+    kc = rng.integers(0, 256, (nb, hkv, bs, d), dtype=np.uint8)
+    vc = rng.integers(0, 256, (nb, hkv, bs, d), dtype=np.uint8)
+    ks = rng.uniform(0.004, 0.05, (nb, hkv)).astype(np.float32)
+    vs = rng.uniform(0.004, 0.05, (nb, hkv)).astype(np.float32)
+    key = _src(rng, (T, hkv, d), dtype, 3.0)
+    val = _src(rng, (T, hkv, d), dtype, 3.0)
+    if dtype == "f32":
+        key[0, 0, :4] = [1e6, -1e6, np.nan, 1e-30]  # saturating, NaN and tiny inputs
+    slots = rng.choice(nb * bs, T, replace=False).astype(np.int64)
+    slots[::9] = -1
+    dk, dv = torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda()
+    pa.write_kv_fp8(to_device(key, dtype), to_device(val, dtype), dk, dv, torch.from_numpy(ks).cuda(),
+                    torch.from_numpy(vs).cuda(), torch.from_numpy(slots).cuda())
+    torch.cuda.synchronize()
+    assert oracle.write_kv_fp8(key, val, dtype, kc, vc, ks, vs, slots) == oracle.OK
+    assert np.array_equal(dk.cpu().numpy(), kc) and np.array_equal(dv.cpu().numpy(), vc)
+    pa.check_error()
+
+
+def test_write_kv_fp8_flags_a_bad_slot():
+    nb, hkv, bs, d = 2, 1, 16, 128
+    dk = torch.zeros(nb, hkv, bs, d, dtype=torch.uint8, device="cuda")
+    dv = torch.zeros_like(dk)
+    one = torch.ones(nb, hkv, device="cuda")
+    rows = torch.ones(2, hkv, d, device="cuda")
+    pa.write_kv_fp8(rows, rows, dk, dv, one, one, torch.tensor([3, nb * bs], dtype=torch.int64, device="cuda"))
+    with pytest.raises(pa.PAError) as e:
+        pa.check_error()
+    assert e.value.status == 6
+    assert int((dk != 0).sum()) == d  # slot 3 written with code(1.0) = 0x38, nothing else
+    assert int(dk[0, 0, 3, 0]) == 0x38
+
+
+def _case(seed, lens, hq, hkv, bs, dtype, q_mult=1.0, slack=2):
+    rng = np.random.default_rng(seed)
+    d = 128
+    lens = np.asarray(lens, np.int32)
+    nblk = (lens + bs - 1) // bs
+    nb = int(nblk.sum()) + slack
+    perm = rng.permutation(nb)
+    width = max(1, int(nblk.max()))
+    bt = np.full((len(lens), width), -1, np.int32)
+    k = 0
+    for b, n in enumerate(nblk):
+        bt[b, :n] = perm[k:k + n]
+        k += n
+    kc = rng.integers(0, 256, (nb, hkv, bs, d), dtype=np.uint8)
+    vc = rng.integers(0, 256, (nb, hkv, bs, d), dtype=np.uint8)
+    kc[(kc & 0x7F) == 0x7F] = 0x3A  # no NaN codes inside the contexts ...
+    vc[(vc & 0x7F) == 0x7F] = 0x3B
+    for b, L in enumerate(lens):  # ... but NaN codes in every slot past a context
+        if L % bs:
+            blk = bt[b, L // bs]
+            kc[blk, :, L % bs:] = 0x7F
+            vc[blk, :, L % bs:] = 0xFF
+    ks = rng.uniform(0.002, 0.02, (nb, hkv)).astype(np.float32)
+    vs = rng.uniform(0.002, 0.02, (nb, hkv)).astype(np.float32)
+    q = _src(rng, (len(lens), hq, d), dtype, q_mult)
+    return q, kc, vc, ks, vs, bt, lens
+
+
+def _run(q, kc, vc, ks, vs, bt, lens, dtype):
+    out = pa.decode_fp8(to_device(q, dtype), torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda(),
+                        torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda(), torch.from_numpy(bt).cuda(),
+                        torch.from_numpy(lens).cuda())
+    torch.cuda.synchronize()
+    return to_f64(out)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("bs", [16, 32])
+@pytest.mark.parametrize("hq,hkv", [(28, 4), (8, 8), (32, 8)])
+def test_decode_fp8_matches_oracle(dtype, bs, hq, hkv):
+    lens = [0, 1, 15, 16, 17, 33, 250, 1000, 2047, 64]
+    q, kc, vc, ks, vs, bt, lens = _case(hq * bs + hkv, lens, hq, hkv, bs, dtype)
+    got = _run(q, kc, vc, ks, vs, bt, lens, dtype)
+    ref = oracle.decode_fp8(q, dtype, kc, vc, ks, vs, bt, lens, 1 / np.sqrt(128))
+    assert_decode_close(got, ref, dtype)
+    assert np.all(got[0] == 0)  # empty context: a zero row
+    pa.check_error()
+
+
+@pytest.mark.parametrize("dtype,q_mult", [("bf16", 3e5), ("bf16", 1e-6), ("f16", 2000.0)])
+def test_decode_fp8_queries_outside_f16_range(dtype, q_mult):
+    # the query row is scaled by a power of two into f16 range: exact for any magnitude
+    q, kc, vc, ks, vs, bt, lens = _case(7, [40, 300, 5], 28, 4, 16, dtype, q_mult=q_mult)
+    scale = 1 / np.sqrt(128)
+    got = _run(q, kc, vc, ks, vs, bt, lens, dtype)
+    ref = oracle.decode_fp8(q, dtype, kc, vc, ks, vs, bt, lens, scale)
+    assert_decode_close(got, ref, dtype)
+
+
+def test_qwen_layer_fp8_full_size():
+    """The Qwen-shaped layer (batch 64, 28/4 heads, d 128, bs 16, L ~ U[512, 4096], pool 20000) with
+    per-(block, head) scales from the block's source values: the caches the GPU writer quantises equal
+    the oracle's byte for byte; sampled output rows match the oracle."""
+    inp = wl.qwen_gqa(0)
+    ks, vs = wl.fp8_scales(inp.key_cache, inp.dtype), wl.fp8_scales(inp.value_cache, inp.dtype)
+    nb, hkv, bs, d = inp.key_cache.shape
+    # quantise the whole pool: every slot written once through the writer
+    slots = np.arange(nb * bs, dtype=np.int64)
+    src_k = np.ascontiguousarray(inp.key_cache.transpose(0, 2, 1, 3).reshape(nb * bs, hkv, d))
+    src_v = np.ascontiguousarray(inp.value_cache.transpose(0, 2, 1, 3).reshape(nb * bs, hkv, d))
+    dk = torch.empty(nb, hkv, bs, d, dtype=torch.uint8, device="cuda")
+    dv = torch.empty_like(dk)
+    dks, dvs = torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda()
+    pa.write_kv_fp8(to_device(src_k, inp.dtype), to_device(src_v, inp.dtype), dk, dv, dks, dvs,
+                    torch.from_numpy(slots).cuda())
+    kc = np.zeros((nb, hkv, bs, d), np.uint8)
+    vc = np.zeros_like(kc)
+    assert oracle.write_kv_fp8(src_k, src_v, inp.dtype, kc, vc, ks, vs, slots) == oracle.OK
+    torch.cuda.synchronize()
+    assert np.array_equal(dk.cpu().numpy(), kc) and np.array_equal(dv.cpu().numpy(), vc)
+    out = pa.decode_fp8(to_device(inp.q, inp.dtype), dk, dv, dks, dvs, torch.from_numpy(inp.block_tables).cuda(),
+                        torch.from_numpy(inp.context_lens).cuda())
+    torch.cuda.synchronize()
+    got = to_f64(out)
+    rng = np.random.default_rng(1)
+    rows = [(int(b), int(h)) for b, h in zip(rng.integers(0, 64, 48), rng.integers(0, 28, 48))]
+    ref = oracle.decode_fp8(inp.q, inp.dtype, kc, vc, ks, vs, inp.block_tables, inp.context_lens, inp.scale, rows)
+    assert_decode_close(np.stack([got[b, h] for b, h in rows]), ref, inp.dtype)
+    pa.check_error()

@@ -64,6 +64,16 @@ WORKLOAD_DESCRIPTIONS = {
                   "sequence's K/V counted), roofline over the unique pages",
     "prefix_cow_2056": "prefix sharing, copy-on-write variant: as prefix_cow with a 2056-token prefix, so the "
                        "first append of 63 sequences copies the shared partial block (pa_copy_blocks)",
+    "qwen_gqa_fp8": "the Qwen-style GQA layer with an FP8 (E4M3) KV cache: batch 64, 28 q / 4 kv heads, head_dim 128, "
+                    "bf16 queries, block_size 16, context_lens uniform in [512,4096], pool 20000 blocks shuffled; "
+                    "q/K/V ~ N(0,1) in bf16, K/V quantised with one scale per (block, kv head) = block max / 448; "
+                    "one new token per sequence quantised into its slot (pa_write_kv_fp8) before the decode",
+    "long_context_fp8": "long-context split-KV with an FP8 (E4M3) KV cache: batch 8, 32 q / 8 kv heads, head_dim 128, "
+                        "bf16 queries, block_size 16, context_lens uniform in [32768,131072]; scales per (block, kv "
+                        "head) = block max / 448",
+    "mha_short_bs16_fp8": "many short requests, MHA, FP8 (E4M3) KV cache: batch 256, 32/32 heads, head_dim 128, "
+                          "fp16 queries, block_size 16, context_lens lognormal(median 256, sigma 1) clipped to "
+                          "[16,2048]; scales per (block, kv head) = block max / 448",
     "qwen_gqa_layers28": "a whole-model decode step over 28 Qwen-style GQA layers (each: batch 64, 28 q / 4 kv "
                          "heads, head_dim 128, bf16, block_size 16, context_lens uniform in [512,4096], pool 20000 "
                          "blocks): every layer's new token written in one pa_write_kv_layers launch, then one "
@@ -93,6 +103,23 @@ def decode_bytes(context_lens, num_heads: int, num_kv_heads: int, head_dim: int,
     qo = 2 * len(lens) * q_len * num_heads * head_dim * elem_bytes
     tables = 4 * int(((lens + block_size - 1) // block_size).sum())
     return kv + qo + tables + 4 * len(lens)
+
+
+def decode_bytes_fp8(context_lens, num_heads: int, num_kv_heads: int, head_dim: int, q_bytes: int,
+                     block_size: int) -> int:
+    """Algorithmic bytes of one FP8 decode call: K+V codes of the valid tokens (one byte each), the K and V
+    scale of every (page, kv head), q, out, table entries, lengths."""
+    lens = np.asarray(context_lens, dtype=np.int64)
+    pages = int(((lens + block_size - 1) // block_size).sum())
+    kv = 2 * int(lens.sum()) * num_kv_heads * head_dim
+    scales = 8 * pages * num_kv_heads
+    qo = 2 * len(lens) * num_heads * head_dim * q_bytes
+    return kv + scales + qo + 4 * pages + 4 * len(lens)
+
+
+def write_bytes_fp8(num_tokens: int, num_kv_heads: int, head_dim: int, src_bytes: int) -> int:
+    """Read new K and V, write their codes, read the slots and the scales."""
+    return (2 * src_bytes + 2) * num_tokens * num_kv_heads * head_dim + 8 * num_tokens + 8 * num_tokens * num_kv_heads
 
 
 def pages_touched_bytes(context_lens, num_kv_heads: int, head_dim: int, elem_bytes: int, block_size: int) -> int:
@@ -272,7 +299,7 @@ def cpu_model() -> str:
         return os.uname().machine
 
 
-def time_oracle_parallel(inp, budget_s: float, threads: int):
+def time_oracle_parallel(inp, budget_s: float, threads: int, fp8=None):
     """Time the fp64 oracle over whole sequences (all heads) on `threads` host threads.
 
     One sequence is timed alone first; then as many sequences as fit in about
@@ -289,11 +316,17 @@ def time_oracle_parallel(inp, budget_s: float, threads: int):
     q_len = inp.q.shape[1] if inp.q.ndim == 4 else 1
 
     def seq_bytes(b):
+        if fp8 is not None:
+            return decode_bytes_fp8([int(inp.context_lens[b])], inp.num_heads, inp.num_kv_heads, inp.head_dim, eb,
+                                    inp.block_size)
         return decode_bytes([int(inp.context_lens[b])], inp.num_heads, inp.num_kv_heads, inp.head_dim, eb,
                             inp.block_size, q_len)
 
     def run(b):
-        if q_len == 1:
+        if fp8 is not None:  # (key codes, value codes, key scales, value scales)
+            oracle.decode_fp8(inp.q, inp.dtype, fp8[0], fp8[1], fp8[2], fp8[3], inp.block_tables, inp.context_lens,
+                              inp.scale, rows=[(b, h) for h in range(inp.num_heads)])
+        elif q_len == 1:
             oracle.decode_inputs(inp, rows=[(b, h) for h in range(inp.num_heads)])
         else:
             oracle.decode_multi(inp.q, inp.key_cache, inp.value_cache, inp.block_tables, inp.context_lens, inp.dtype,
@@ -347,6 +380,8 @@ def build_batch(workload: str, seed: int):
 
     gen = {"qwen_gqa": lambda s: wl.qwen_gqa(s), "qwen_gqa_verify4": lambda s: wl.qwen_gqa_verify(s, q_len=4),
            "qwen_gqa_layers28": lambda s: wl.qwen_gqa(s),  # every layer has the Qwen layer's shape
+           "qwen_gqa_fp8": lambda s: wl.qwen_gqa(s), "long_context_fp8": lambda s: wl.long_context(s),
+           "mha_short_bs16_fp8": lambda s: wl.mha_short(16, s),
            "long_context": lambda s: wl.long_context(s),
            "mha_short_bs16": lambda s: wl.mha_short(16, s), "mha_short_bs32": lambda s: wl.mha_short(32, s)}[workload]
     return gen(seed)
@@ -468,11 +503,15 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     eb = inp.elem_bytes
     B, Hq, Hkv, d, bs = inp.num_seqs, inp.num_heads, inp.num_kv_heads, inp.head_dim, inp.block_size
     q_len = inp.q.shape[1] if inp.q.ndim == 4 else 1  # query tokens per sequence (verify step: > 1)
+    fp8 = args.workload.endswith("_fp8")  # E4M3 caches with a scale per (block, kv head)
     dec_bytes = decode_bytes(lens, Hq, Hkv, d, eb, bs, q_len)
     ntok = 0 if slots is None else len(slots)
     wr_bytes = write_bytes(ntok, Hkv, d, eb)
+    if fp8:
+        dec_bytes = decode_bytes_fp8(lens, Hq, Hkv, d, eb, bs)
+        wr_bytes = write_bytes_fp8(ntok, Hkv, d, eb)
     step_bytes = dec_bytes + wr_bytes
-    touched = pages_touched_bytes(lens, Hkv, d, eb, bs)
+    touched = pages_touched_bytes(lens, Hkv, d, 1 if fp8 else eb, bs)
     if prefix:
         touched = unique_bytes  # shared pages are read once per step
 
@@ -484,6 +523,21 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     # Rotate over cache replicas so that a step never finds its pages in L2 from the previous one.
     replicas = 1 if touched >= 3 * l2 else max(2, math.ceil(2 * l2 / touched) + 1)
     kc0, vc0 = up(inp.key_cache), up(inp.value_cache)
+    if fp8:
+        # quantise the whole pool through the product writer (every slot once), then drop the sources
+        from paged_kv_cache_129_gb300 import workloads as wl
+
+        ks_np, vs_np = wl.fp8_scales(inp.key_cache, inp.dtype), wl.fp8_scales(inp.value_cache, inp.dtype)
+        ksd, vsd = torch.from_numpy(ks_np).to(device), torch.from_numpy(vs_np).to(device)
+        nb_ = inp.num_blocks
+        all_slots = torch.arange(nb_ * bs, dtype=torch.int64, device=device)
+        q8k = torch.empty(nb_, Hkv, bs, d, dtype=torch.uint8, device=device)
+        q8v = torch.empty_like(q8k)
+        pa.write_kv_fp8(kc0.permute(0, 2, 1, 3).reshape(nb_ * bs, Hkv, d).contiguous(),
+                        vc0.permute(0, 2, 1, 3).reshape(nb_ * bs, Hkv, d).contiguous(), q8k, q8v, ksd, vsd, all_slots)
+        torch.cuda.synchronize()
+        del kc0, vc0, all_slots
+        kc0, vc0 = q8k, q8v
     kcs, vcs = [kc0], [vc0]
     for _ in range(replicas - 1):
         kcs.append(kc0.clone())
@@ -497,8 +551,14 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         nk, nv = up(inp.new_key), up(inp.new_value)
         sl = torch.from_numpy(slots).to(device)
     max_ctx = int(lens.max())
-    plan = pa.decode_plan(B, Hq, Hkv, d, bs, tables.shape[1], tdtype, max_context_len=max_ctx,
-                          partition_pages=args.partition_pages, kernel=args.kernel, q_len=q_len)
+    if fp8:
+        plan = pa.DecodePlan()
+        plan.kernel, plan.schedule, plan.partition_pages, plan.max_parts = 1, 1, 0, 0
+        plan.workspace_bytes = pa.decode_fp8_workspace_size(B, Hq, Hkv, d, bs, tables.shape[1], tdtype)
+        plan.grid_ctas = 0
+    else:
+        plan = pa.decode_plan(B, Hq, Hkv, d, bs, tables.shape[1], tdtype, max_context_len=max_ctx,
+                              partition_pages=args.partition_pages, kernel=args.kernel, q_len=q_len)
     ws = torch.zeros(max(plan.workspace_bytes, 256), dtype=torch.uint8, device=device)
     lib = pa.library()
     stream = torch.cuda.current_stream(device)
@@ -506,7 +566,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     code = {"f32": 0, "f16": 1, "bf16": 2}[inp.dtype]
     kern = pa.KERNELS[args.kernel]
 
-    fused = has_write and args.step == "append" and q_len == 1
+    fused = has_write and args.step == "append" and q_len == 1 and not args.workload.endswith("_fp8")
     if fused:
         # pa_decode_append writes at the slot of position L - 1: the pool handed out exactly those
         live = lens >= 1
@@ -521,6 +581,18 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     decode_fn = lib.pa_decode_multi if q_len > 1 else lib.pa_decode_ex
     wr_args = ([[nk.data_ptr(), nv.data_ptr(), kcs[r].data_ptr(), vcs[r].data_ptr(), sl.data_ptr(), ntok, Hkv, d, bs,
                  inp.num_blocks, code, sptr] for r in range(replicas)] if has_write else None)
+    if fp8:
+        decode_fn = lib.pa_decode_fp8
+        dec_args = [[out.data_ptr(), q.data_ptr(), kcs[r].data_ptr(), vcs[r].data_ptr(), ksd.data_ptr(),
+                     vsd.data_ptr(), bt.data_ptr(), dl.data_ptr(), B, Hq, Hkv, d, bs, tables.shape[1], inp.num_blocks,
+                     float(inp.scale), code, ws.data_ptr(), ws.numel(), sptr] for r in range(replicas)]
+        write_fn = lib.pa_write_kv_fp8
+        if has_write:
+            wr_args = [[nk.data_ptr(), nv.data_ptr(), kcs[r].data_ptr(), vcs[r].data_ptr(), ksd.data_ptr(),
+                        vsd.data_ptr(), sl.data_ptr(), ntok, Hkv, d, bs, inp.num_blocks, code, sptr]
+                       for r in range(replicas)]
+    else:
+        write_fn = lib.pa_write_kv
     app_args = ([[out.data_ptr(), q.data_ptr(), nk.data_ptr(), nv.data_ptr(), kcs[r].data_ptr(), vcs[r].data_ptr(),
                   bt.data_ptr(), dl.data_ptr(), B, Hq, Hkv, d, bs, tables.shape[1], inp.num_blocks, float(inp.scale),
                   code, ws.data_ptr(), ws.numel(), max_ctx, args.partition_pages, kern, sptr]
@@ -536,7 +608,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
             if lib.pa_decode_append(*app_args[r]) != 0:
                 raise RuntimeError(lib.pa_last_error_string().decode())
             return
-        if has_write and lib.pa_write_kv(*wr_args[r]) != 0:
+        if has_write and write_fn(*wr_args[r]) != 0:
             raise RuntimeError(lib.pa_last_error_string().decode())
         if decode_fn(*dec_args[r]) != 0:
             raise RuntimeError(lib.pa_last_error_string().decode())
@@ -594,7 +666,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     # step i + 1 overlaps the decode of step i.
     e2e = None
     # the step runner does one decode call per step (no separate write, one query token)
-    if not args.no_e2e and not (has_write and not fused) and q_len == 1:
+    if not args.no_e2e and not (has_write and not fused) and q_len == 1 and not fp8:
         stepper = pa.DecodeStepper(kcs[0], vcs[0], B, Hq, tables.shape[1], scale=inp.scale, append=fused,
                                    max_context_len=max_ctx, partition_pages=args.partition_pages,
                                    kernel=args.kernel, tables="deltas")
@@ -670,7 +742,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     achieved = call_bytes / (dec_avg_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": stored_traffic(args.workload),
-                "kernel": (("pa_decode_append" if fused else "pa_decode_multi" if q_len > 1 else "pa_decode") +
+                "kernel": (("pa_decode_append" if fused else "pa_decode_multi" if q_len > 1 else
+                            "pa_decode_fp8" if fp8 else "pa_decode") +
                            " call (" +
                            ("paged_decode_lean_kernel + lean_merge_kernel)" if plan.schedule == 1 else
                             "paged_decode_kernel" + (" + splitkv_merge_kernel)" if plan.max_parts > 1 else ")"))),
@@ -681,13 +754,25 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        if has_write:
-            import oracle
+        import oracle
 
+        fp8_host = None
+        if fp8:
+            # the oracle quantises its own copy of the pool (every slot), then the step's new tokens
+            nb_ = inp.num_blocks
+            kq, vq = np.zeros((nb_, Hkv, bs, d), np.uint8), np.zeros((nb_, Hkv, bs, d), np.uint8)
+            oracle.write_kv_fp8(np.ascontiguousarray(inp.key_cache.transpose(0, 2, 1, 3).reshape(nb_ * bs, Hkv, d)),
+                                np.ascontiguousarray(inp.value_cache.transpose(0, 2, 1, 3).reshape(nb_ * bs, Hkv, d)),
+                                inp.dtype, kq, vq, ks_np, vs_np, np.arange(nb_ * bs, dtype=np.int64))
+            if has_write:
+                oracle.write_kv_fp8(inp.new_key.reshape(-1, Hkv, d), inp.new_value.reshape(-1, Hkv, d), inp.dtype,
+                                    kq, vq, ks_np, vs_np, slots)
+            fp8_host = (kq, vq, ks_np, vs_np)
+        elif has_write:
             oracle.write_kv(inp.new_key.reshape(-1, Hkv, d), inp.new_value.reshape(-1, Hkv, d), inp.key_cache,
                             inp.value_cache, slots)
         threads = os.cpu_count() or 1
-        r = time_oracle_parallel(inp, args.cpu_budget, threads)
+        r = time_oracle_parallel(inp, args.cpu_budget, threads, fp8_host)
         cpu = {"value": round(r["bytes"] / r["seconds"] / 1e9, 4), "unit": UNIT, "cores": threads, "kind": "oracle",
                "sample": f"first {r['seqs']} of {B} sequences, all {Hq} heads ({r['rows']} output rows), "
                          f"fp64 C oracle, one sequence per task on {threads} threads, {r['seconds']:.1f} s",
@@ -704,7 +789,10 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAMES[inp.dtype], "data": "synthetic",
         "config": {"workload": WORKLOAD_DESCRIPTIONS[args.workload], "name": args.workload,
                    "step": ("pa_decode_append (new token per sequence written at L - 1, then decode)" if fused
-                            else "pa_write_kv (new token per sequence) + pa_decode"),
+                            else "pa_write_kv_fp8 (new token per sequence) + pa_decode_fp8" if fp8 and has_write
+                            else "pa_decode_fp8" if fp8
+                            else "pa_write_kv (new token per sequence) + pa_decode" if has_write
+                            else "pa_decode_multi" if q_len > 1 else "pa_decode"),
                    "l2": f"{replicas} cache replicas rotated per step (pages touched per step "
                          f"{touched / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB)",
                    **({"copy_on_write_copies": n_cow, "unique_page_bytes": unique_bytes,

@@ -179,7 +179,7 @@ def kernel_sources_digest() -> str:
     """sha256 over the decode kernel's sources: ties a stored ncu traffic figure to the code it measured."""
     h = hashlib.sha256()
     for name in ("decode_kernel.cuh", "pa_common.cuh", "decode_launch.h", "decode_bf16.cu", "decode_f16.cu",
-                 "decode_f32.cu"):
+                 "decode_f32.cu", "decode_fp8.cu"):
         with open(os.path.join(ROOT, "paged_kv_cache_129_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()

@@ -53,6 +53,15 @@
 #ifndef PA_LEAN_RING_KB
 #define PA_LEAN_RING_KB 64
 #endif
+// Resident lean CTAs per SM the FP8 kernel's register allocation aims for.
+#ifndef PA_LEAN_F8_MIN_BLOCKS
+#define PA_LEAN_F8_MIN_BLOCKS 3
+#endif
+// Idle nap of the lean producer lane between polls of its warps' slots (ns): every poll takes
+// issue slots from the consumers that share its SM sub-partition.
+#ifndef PA_PRODUCER_NAP_NS
+#define PA_PRODUCER_NAP_NS 20
+#endif
 
 namespace pa {
 
@@ -432,9 +441,13 @@ struct MmaConsumer {
 //    token pairs of the A fragment come from byte permutes; the lane ends up holding
 //    d = 16g .. 16g+15 of its two output rows.
 // Both patterns are free of bank conflicts under the 128-byte swizzle.
-__device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair16) {
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(pair16), __NV_E4M3);
-    return (uint32_t)h.x | ((uint32_t)h.y << 16);
+// Four E4M3 codes (bytes 0..3 of w) -> two f16x2: lo = (byte 0, byte 1), hi = (byte 2, byte 3), the
+// lower byte in the lower half (exact: every E4M3 value is an f16 value).
+__device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+    asm("{\n\t.reg .b16 a, b;\n\tmov.b32 {a, b}, %2;\n\tcvt.rn.f16x2.e4m3x2 %0, a;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, b;\n\t}"
+        : "=r"(lo), "=r"(hi)
+        : "r"(w));
 }
 
 template <typename T, int D, int BS>
@@ -501,8 +514,10 @@ struct MmaConsumerF8 {
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            // ---- S = Q K^T: two n-tiles of 8 tokens ----
+            // ---- S = Q K^T: two n-tiles of 8 tokens, each summed over two independent accumulators
+            // (even and odd k-steps) so that the MMA dependency chains are half as long ----
             float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
                 const int tok = sub * 16 + nt * 8 + g;
@@ -511,9 +526,13 @@ struct MmaConsumerF8 {
                 const uint4 k1 = *reinterpret_cast<const uint4*>(row + (((2 * c + 1) ^ (tok & 7)) << 4));
                 const uint32_t w[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
 #pragma unroll
-                for (int kk = 0; kk < KS; ++kk)
-                    Mma<__half>::run(s[nt], qa[kk][0], 0u, qa[kk][1], 0u, e4m3x2_to_f16x2(w[kk] & 0xffffu),
-                                     e4m3x2_to_f16x2(w[kk] >> 16));
+                for (int kk = 0; kk < KS; ++kk) {
+                    uint32_t b0, b1;
+                    e4m3x4_to_f16x2x2(w[kk], b0, b1);
+                    Mma<__half>::run((kk & 1) ? s2[nt] : s[nt], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
+                }
+#pragma unroll
+                for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
             }
             // ---- online softmax for row g over tokens 2c, 2c+1, 8+2c, 9+2c ----
             const float x0 = (2 * c < nv) ? s[0][0] * sf : -INFINITY;
@@ -546,12 +565,14 @@ struct MmaConsumerF8 {
                 const uint32_t sel = (i & 1) ? 0x7362u : 0x5140u;  // bytes 2(i&1), 2(i&1)+1 of both words
                 const uint32_t p01 = __byte_perm(w0[i >> 1], w1[i >> 1], sel);
                 const uint32_t p23 = __byte_perm(w2[i >> 1], w3[i >> 1], sel);
+                uint32_t a0, a1, a2, a3;
+                e4m3x4_to_f16x2x2(p01, a0, a1);
+                e4m3x4_to_f16x2x2(p23, a2, a3);
                 o[i][0] *= a_lo;
                 o[i][1] *= a_hi;
                 o[i][2] *= a_lo;
                 o[i][3] *= a_hi;
-                Mma<__half>::run(o[i], e4m3x2_to_f16x2(p01 & 0xffffu), e4m3x2_to_f16x2(p01 >> 16),
-                                 e4m3x2_to_f16x2(p23 & 0xffffu), e4m3x2_to_f16x2(p23 >> 16), pb0, pb1);
+                Mma<__half>::run(o[i], a0, a1, a2, a3, pb0, pb1);
             }
         }
     }
@@ -1248,7 +1269,7 @@ __device__ __forceinline__ void lean_locate(const int* pre, int num_seqs, int up
 // the query and output type.
 template <typename T, int D, int BS, bool MMA, int GMAX, bool CAUSAL, bool F8 = false>
 __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
-                                  (LeanCfg<std::conditional_t<F8, uint8_t, T>, D, BS, MMA, GMAX>::kMinBlocks))
+                                  (F8 ? PA_LEAN_F8_MIN_BLOCKS : LeanCfg<T, D, BS, MMA, GMAX>::kMinBlocks))
     paged_decode_lean_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                              const DecodeArgs a) {
     using C = LeanCfg<std::conditional_t<F8, uint8_t, T>, D, BS, MMA, GMAX>;
@@ -1387,7 +1408,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
                         flags[0] = 1;
                         break;
                     }
-                    __nanosleep(20);
+                    __nanosleep(PA_PRODUCER_NAP_NS);
                 }
             }
         }

@@ -666,10 +666,15 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     # step i + 1 overlaps the decode of step i.
     e2e = None
     # the step runner does one decode call per step (no separate write, one query token)
-    if not args.no_e2e and not (has_write and not fused) and q_len == 1 and not fp8:
-        stepper = pa.DecodeStepper(kcs[0], vcs[0], B, Hq, tables.shape[1], scale=inp.scale, append=fused,
-                                   max_context_len=max_ctx, partition_pages=args.partition_pages,
-                                   kernel=args.kernel, tables="deltas")
+    if not args.no_e2e and (fused or fp8 or not has_write) and q_len == 1:
+        step_append = fused or (fp8 and has_write)
+        if fp8:
+            stepper = pa.DecodeStepper(kcs[0], vcs[0], B, Hq, tables.shape[1], scale=inp.scale, append=step_append,
+                                       tables="deltas", k_scale=ksd, v_scale=vsd, query_dtype=tdtype)
+        else:
+            stepper = pa.DecodeStepper(kcs[0], vcs[0], B, Hq, tables.shape[1], scale=inp.scale, append=fused,
+                                       max_context_len=max_ctx, partition_pages=args.partition_pages,
+                                       kernel=args.kernel, tables="deltas")
         # the device tables are kept by delta uploads: the first step sends every entry, later steps
         # re-send the tail entry of B / bs rows (the rate at which one token a step opens new blocks)
         nblk = (lens + bs - 1) // bs
@@ -687,9 +692,11 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
             v = stepper.inputs(sl)
             fill(v.query, inp.q)
             v.context_lens.copy_(torch.from_numpy(lens))
-            if fused:
+            if step_append:
                 fill(v.new_key, inp.new_key)
                 fill(v.new_value, inp.new_value)
+            if fp8 and step_append:
+                v.slots.copy_(torch.from_numpy(np.asarray(slots, dtype=np.int64)))
 
         def e2e_run(n, first=False):
             for i in range(n):
@@ -724,9 +731,10 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         e2e = {"value": round(e_bytes / (e_ms / 1e3) / 1e9, 2), "unit": UNIT, "steps": Ke,
                "ms_per_step": round(e_ms / Ke, 5), "h2d_bytes_per_step": int(stepper.h2d_bytes),
                "d2h_bytes_per_step": int(stepper.d2h_bytes),
-               "note": f"pa.DecodeStepper ({'pa_decode_append' if fused else 'pa_decode'}, tables kept on the "
+               "note": f"pa.DecodeStepper ({'pa_decode_append' if fused else 'pa_write_kv_fp8 + pa_decode_fp8' if fp8 and step_append else 'pa_decode_fp8' if fp8 else 'pa_decode'}, tables kept on the "
                        "device by deltas): every step one upload of the packed inputs (queries" +
-                       (", new K/V" if fused else "") + f", lengths, {churn} block-table deltas) from pinned host "
+                       (", new K/V" if step_append else "") + (", slots" if fp8 and step_append else "") +
+                       f", lengths, {churn} block-table deltas) from pinned host "
                        "memory, pa_apply_table_deltas and the decode on the compute stream, one download of the "
                        "output, inside the timed region; two slots, the next upload overlapping the current decode"}
 

@@ -56,17 +56,28 @@ class DecodeStepper:
     ``launch(i, num_deltas=k)``.  The deltas are applied on the decode's
     stream just before the decode, so stream order keeps them after the
     previous step's decode has read the table.
+
+    FP8 caches (``k_scale`` / ``v_scale`` given, E4M3 codes in the caches,
+    ``query_dtype`` f16 or bf16): a step is ``pa_write_kv_fp8`` of the new
+    tokens at ``inputs(i).slots`` (int64) when ``append``, then
+    ``pa_decode_fp8``.
     """
 
     def __init__(self, key_cache: torch.Tensor, value_cache: torch.Tensor, num_seqs: int, num_heads: int,
                  max_blocks_per_seq: int, scale: Optional[float] = None, append: bool = True, slots: int = 2,
-                 max_context_len: int = 0, partition_pages: int = 0, kernel: str = "auto", tables: str = "full"):
+                 max_context_len: int = 0, partition_pages: int = 0, kernel: str = "auto", tables: str = "full",
+                 k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
+                 query_dtype: Optional[torch.dtype] = None):
         assert tables in ("full", "deltas")
         assert key_cache.is_cuda and key_cache.shape == value_cache.shape and key_cache.dim() == 4
         self.device = key_cache.device
         self.key_cache, self.value_cache = key_cache, value_cache
         num_blocks, hkv, bs, d = key_cache.shape
-        dt = key_cache.dtype
+        self.fp8 = k_scale is not None
+        if self.fp8:
+            assert v_scale is not None and query_dtype in (torch.float16, torch.bfloat16)
+            self.k_scale, self.v_scale = k_scale, v_scale
+        dt = query_dtype if self.fp8 else key_cache.dtype
         self.shape = (num_seqs, num_heads, hkv, d, bs, max_blocks_per_seq, num_blocks)
         self.scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
         self.append, self.slots = append, slots
@@ -74,6 +85,8 @@ class DecodeStepper:
         fields = [("query", (num_seqs, num_heads, d), dt)]
         if append:
             fields += [("new_key", (num_seqs, hkv, d), dt), ("new_value", (num_seqs, hkv, d), dt)]
+            if self.fp8:
+                fields += [("slots", (num_seqs,), torch.int64)]
         self.deltas_mode = tables == "deltas"
         if self.deltas_mode:
             # the deltas go last, so that a step uploads only the prefix it uses
@@ -95,7 +108,9 @@ class DecodeStepper:
         self._dv_in = [_views(b, self._in) for b in self._d_in]
         self._hv_out = [_views(b, self._out).out for b in self._h_out]
         self._dv_out = [_views(b, self._out).out for b in self._d_out]
-        ws_bytes = binding.decode_workspace_size(num_seqs, num_heads, hkv, d, bs, max_blocks_per_seq, dt)
+        ws_bytes = (binding.decode_fp8_workspace_size(num_seqs, num_heads, hkv, d, bs, max_blocks_per_seq, dt)
+                    if self.fp8 else
+                    binding.decode_workspace_size(num_seqs, num_heads, hkv, d, bs, max_blocks_per_seq, dt))
         # one workspace per slot: consecutive steps may overlap on the GPU
         self._ws = [torch.empty(max(ws_bytes, _ALIGN), dtype=torch.uint8, device=self.device) if ws_bytes else None
                     for _ in range(slots)]
@@ -119,10 +134,18 @@ class DecodeStepper:
             dv, out, ws = self._dv_in[s], self._dv_out[s], self._ws[s]
             ws_ptr, ws_bytes = (ws.data_ptr(), ws.numel()) if ws is not None else (None, 0)
             stream = int(self.compute.cuda_stream)
-            code = binding._dtype_code(kc)
+            code = binding._dtype_code(dv.query)
             kern = binding.KERNELS[self.kernel]
             tables = self.device_block_tables if self.deltas_mode else dv.block_tables
-            if self.append:
+            if self.fp8:
+                ks, vs = self.k_scale.data_ptr(), self.v_scale.data_ptr()
+                args = [out.data_ptr(), dv.query.data_ptr(), kc.data_ptr(), vc.data_ptr(), ks, vs, tables.data_ptr(),
+                        dv.context_lens.data_ptr(), num_seqs, num_heads, hkv, d, bs, max_blocks, num_blocks,
+                        self.scale, code, ws_ptr, ws_bytes, stream]
+                if self.append:
+                    args = (args, [dv.new_key.data_ptr(), dv.new_value.data_ptr(), kc.data_ptr(), vc.data_ptr(), ks,
+                                   vs, dv.slots.data_ptr(), num_seqs, hkv, d, bs, num_blocks, code, stream])
+            elif self.append:
                 args = [out.data_ptr(), dv.query.data_ptr(), dv.new_key.data_ptr(), dv.new_value.data_ptr(),
                         kc.data_ptr(), vc.data_ptr(), tables.data_ptr(), dv.context_lens.data_ptr(),
                         num_seqs, num_heads, hkv, d, bs, max_blocks, num_blocks, self.scale, code, ws_ptr,
@@ -184,7 +207,13 @@ class DecodeStepper:
                                                            self._dv_in[s].deltas.data_ptr(), num_deltas,
                                                            int(comp.cuda_stream)))
         args = self._call_args(s, kc, vc)
-        status = (self._lib.pa_decode_append if self.append else self._lib.pa_decode_ex)(*args)
+        if self.fp8:
+            if self.append:  # the new tokens' codes first, then the decode over them
+                binding._check(self._lib.pa_write_kv_fp8(*args[1]))
+                args = args[0]
+            status = self._lib.pa_decode_fp8(*args)
+        else:
+            status = (self._lib.pa_decode_append if self.append else self._lib.pa_decode_ex)(*args)
         binding._check(status)
         self._decoded[s].record(comp)
         down.wait_event(self._decoded[s])

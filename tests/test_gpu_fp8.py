@@ -161,3 +161,57 @@ def test_qwen_layer_fp8_full_size():
     ref = oracle.decode_fp8(inp.q, inp.dtype, kc, vc, ks, vs, inp.block_tables, inp.context_lens, inp.scale, rows)
     assert_decode_close(np.stack([got[b, h] for b, h in rows]), ref, inp.dtype)
     pa.check_error()
+
+
+def test_stepper_fp8_matches_direct_calls():
+    """pa.DecodeStepper over FP8 caches (new tokens quantised at their slots, then the FP8 decode; block
+    tables kept by deltas) gives the same bytes as direct pa_write_kv_fp8 + pa_decode_fp8 calls."""
+    rng = np.random.default_rng(21)
+    B, hq, hkv, bs, d, steps = 6, 28, 4, 16, 128, 5
+    lens = rng.integers(1, 300, B).astype(np.int32)
+    nblk = (lens + bs - 1) // bs
+    nb = int(nblk.sum()) + 4
+    perm = rng.permutation(nb)
+    width = int(nblk.max())
+    bt = np.full((B, width), -1, np.int32)
+    k = 0
+    for b, n in enumerate(nblk):
+        bt[b, :n] = perm[k:k + n]
+        k += n
+    slots = np.array([bt[b, (L - 1) // bs] * bs + (L - 1) % bs for b, L in enumerate(lens)], np.int64)
+    kc = torch.from_numpy(rng.integers(0, 0x7E, (nb, hkv, bs, d), dtype=np.uint8)).cuda()
+    vc = torch.from_numpy(rng.integers(0, 0x7E, (nb, hkv, bs, d), dtype=np.uint8)).cuda()
+    ks = torch.from_numpy(rng.uniform(0.005, 0.02, (nb, hkv)).astype(np.float32)).cuda()
+    vs = torch.from_numpy(rng.uniform(0.005, 0.02, (nb, hkv)).astype(np.float32)).cuda()
+    kc_ref, vc_ref = kc.clone(), vc.clone()
+    stepper = pa.DecodeStepper(kc, vc, B, hq, width, append=True, tables="deltas", k_scale=ks, v_scale=vs,
+                               query_dtype=torch.bfloat16)
+    deltas = np.array([(r, j, bt[r, j]) for r in range(B) for j in range(nblk[r])], np.int32)
+    got, refs = [], []
+    ws = torch.empty(max(pa.decode_fp8_workspace_size(B, hq, hkv, d, bs, width, torch.bfloat16), 256),
+                     dtype=torch.uint8, device="cuda")
+    for i in range(steps):
+        if i >= stepper.slots:
+            got.append(stepper.result(i - stepper.slots).clone())
+        q = torch.randn(B, hq, d).to(torch.bfloat16)
+        nk = torch.randn(B, hkv, d).to(torch.bfloat16)
+        nv = torch.randn(B, hkv, d).to(torch.bfloat16)
+        v = stepper.inputs(i)
+        v.query.copy_(q)
+        v.new_key.copy_(nk)
+        v.new_value.copy_(nv)
+        v.slots.copy_(torch.from_numpy(slots))
+        v.context_lens.copy_(torch.from_numpy(lens))
+        n = len(deltas) if i == 0 else 0
+        v.deltas.numpy()[:n] = deltas[:n]
+        stepper.launch(i, num_deltas=n)
+        pa.write_kv_fp8(nk.cuda(), nv.cuda(), kc_ref, vc_ref, ks, vs, torch.from_numpy(slots).cuda())
+        refs.append(pa.decode_fp8(q.cuda(), kc_ref, vc_ref, ks, vs, torch.from_numpy(bt).cuda(),
+                                  torch.from_numpy(lens).cuda(), workspace=ws))
+    for i in range(steps - stepper.slots, steps):
+        got.append(stepper.result(i).clone())
+    torch.cuda.synchronize()
+    pa.check_error()
+    for i in range(steps):
+        assert torch.equal(got[i].view(torch.int16), refs[i].cpu().view(torch.int16)), f"step {i}"
+    assert torch.equal(kc, kc_ref) and torch.equal(vc, vc_ref)

@@ -352,6 +352,60 @@ int pa_decode_static_scratch(void* out, const void* query, const void* key_cache
                              int num_heads, int num_kv_heads, int head_dim, int block_size,
                              int max_blocks_per_seq, int num_blocks, float scale, int dtype, void* stream);
 
+/*
+ * pa_stepper — one decode step fed from page-locked host staging, sequenced in native
+ * code: per step one host-to-device copy of the step's packed inputs on an upload
+ * stream, the block-table deltas (if any) and the decode on a compute stream, one
+ * device-to-host copy of the output on a download stream, ordered by events so that
+ * with two or more slots the upload of step i + 1 overlaps the decode of step i.
+ * (The step of a serving loop: queries, new K/V and lengths arrive from the host
+ * every step, the outputs go back; MiniPaged-Qwen's closing notes ask for lower host
+ * overhead per step.)  Memory is the caller's: pa_stepper_set_slot gives each slot's
+ * host and device staging and output buffers, pa_stepper_set_call the decode call of
+ * a slot (pointers into that slot's device staging, the caches, the workspace).  The
+ * library creates only its own events.  Not thread-safe; one stepper per loop.
+ *
+ * kind: PA_STEP_DECODE (pa_decode_ex), PA_STEP_APPEND (pa_decode_append),
+ * PA_STEP_FP8 (pa_decode_fp8), PA_STEP_FP8_WRITE (pa_write_kv_fp8 of the new tokens at
+ * `slots`, then pa_decode_fp8).  With deltas != NULL, pa_apply_table_deltas(
+ * block_tables, num_seqs, max_blocks_per_seq, deltas, num_deltas) runs first.
+ */
+enum { PA_STEP_DECODE = 0, PA_STEP_APPEND = 1, PA_STEP_FP8 = 2, PA_STEP_FP8_WRITE = 3 };
+typedef struct pa_step_call {
+    int kind;
+    void* out;
+    const void* query;
+    const void* new_key;     /* PA_STEP_APPEND, PA_STEP_FP8_WRITE */
+    const void* new_value;
+    const int64_t* slots;    /* PA_STEP_FP8_WRITE: int64 [num_seqs] */
+    void* key_cache;
+    void* value_cache;
+    const float* k_scale;    /* FP8 kinds */
+    const float* v_scale;
+    int32_t* block_tables;
+    const int32_t* context_lens;
+    const int32_t* deltas;   /* NULL: no table deltas */
+    int num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks;
+    float scale;
+    int dtype;               /* query / output type */
+    void* workspace;
+    size_t workspace_bytes;
+    int max_context_len, partition_pages, kernel;
+} pa_step_call;
+typedef struct pa_stepper pa_stepper;
+int pa_stepper_create(int slots, void* upload_stream, void* compute_stream, void* download_stream,
+                      pa_stepper** out);
+void pa_stepper_destroy(pa_stepper* st);
+int pa_stepper_set_slot(pa_stepper* st, int slot, const void* host_in, void* dev_in, size_t in_bytes,
+                        void* host_out, const void* dev_out, size_t out_bytes);
+int pa_stepper_set_call(pa_stepper* st, int slot, const pa_step_call* call);
+/* Launch step `step` on slot step % slots: upload its first upload_bytes (<= in_bytes), apply
+ * num_deltas deltas, decode, download.  Asynchronous; the slot's host staging must not be
+ * refilled before pa_stepper_wait of the step that last used the slot. */
+int pa_stepper_launch(pa_stepper* st, int step, size_t upload_bytes, int num_deltas);
+/* Block the host until the output of `step` has arrived in its slot's host buffer. */
+int pa_stepper_wait(pa_stepper* st, int step);
+
 /* ---- host block pool ----------------------------------------------------------------- */
 /*
  * Fixed-size block allocator with reference counts, fork and copy-on-write

@@ -41,6 +41,22 @@ class PoolExhausted(PAError, MemoryError):
     pass
 
 
+STEP_DECODE, STEP_APPEND, STEP_FP8, STEP_FP8_WRITE = 0, 1, 2, 3
+
+
+class StepCall(ctypes.Structure):
+    """``pa_step_call``: the decode call of one step-runner slot."""
+    _fields_ = [("kind", ctypes.c_int), ("out", ctypes.c_void_p), ("query", ctypes.c_void_p),
+                ("new_key", ctypes.c_void_p), ("new_value", ctypes.c_void_p), ("slots", ctypes.c_void_p),
+                ("key_cache", ctypes.c_void_p), ("value_cache", ctypes.c_void_p), ("k_scale", ctypes.c_void_p),
+                ("v_scale", ctypes.c_void_p), ("block_tables", ctypes.c_void_p), ("context_lens", ctypes.c_void_p),
+                ("deltas", ctypes.c_void_p), ("num_seqs", ctypes.c_int), ("num_heads", ctypes.c_int),
+                ("num_kv_heads", ctypes.c_int), ("head_dim", ctypes.c_int), ("block_size", ctypes.c_int),
+                ("max_blocks_per_seq", ctypes.c_int), ("num_blocks", ctypes.c_int), ("scale", ctypes.c_float),
+                ("dtype", ctypes.c_int), ("workspace", ctypes.c_void_p), ("workspace_bytes", ctypes.c_size_t),
+                ("max_context_len", ctypes.c_int), ("partition_pages", ctypes.c_int), ("kernel", ctypes.c_int)]
+
+
 class DecodePlan(ctypes.Structure):
     _fields_ = [("kernel", ctypes.c_int), ("schedule", ctypes.c_int), ("partition_pages", ctypes.c_int),
                 ("max_parts", ctypes.c_int),
@@ -75,6 +91,12 @@ _SIGNATURES = [
     ("pa_decode_make_plan", _I, [_I, _I, _I, _I, _I, _I, _I, _SZ, _I, _I, _I, ctypes.POINTER(DecodePlan)]),
     ("pa_decode_workspace_size", _SZ, [_I, _I, _I, _I, _I, _I, _I]),
     ("pa_decode_static_scratch", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
+    ("pa_stepper_create", _I, [_I, _P, _P, _P, ctypes.POINTER(_P)]),
+    ("pa_stepper_destroy", None, [_P]),
+    ("pa_stepper_set_slot", _I, [_P, _I, _P, _P, _SZ, _P, _P, _SZ]),
+    ("pa_stepper_set_call", _I, [_P, _I, _P]),
+    ("pa_stepper_launch", _I, [_P, _I, _SZ, _I]),
+    ("pa_stepper_wait", _I, [_P, _I]),
     ("pa_pool_create", _I, [_I, _I, _P, ctypes.POINTER(_P)]),
     ("pa_pool_destroy", None, [_P]),
     ("pa_seq_create", _I, [_P, ctypes.POINTER(_I64)]),

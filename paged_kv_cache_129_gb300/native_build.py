@@ -22,7 +22,7 @@ LIB = os.path.join(BUILD, "libpagedkv.so")
 
 CUDA_SOURCES = ["capi.cu", "kv_ops.cu", "decode_f32.cu", "decode_f16.cu", "decode_bf16.cu", "decode_fp8.cu",
                 "decode_static_scratch.cu"]
-CXX_SOURCES = ["block_pool.cpp"]
+CXX_SOURCES = ["block_pool.cpp", "stepper.cpp"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

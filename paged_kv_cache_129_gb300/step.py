@@ -10,10 +10,13 @@ one device-to-host copy.  With two slots the upload of step i + 1 runs on a copy
 stream while step i decodes.
 
 Every byte moved or computed is moved by the CUDA runtime or computed by the
-library's kernels; this module only orders them.
+library's kernels, and the per-step sequence of copies, waits and calls runs in
+the library's native step runner (pa_stepper_*); this module only lays out the
+staging buffers and fills the call.
 """
 from __future__ import annotations
 
+import ctypes
 import math
 from types import SimpleNamespace
 from typing import List, Optional, Tuple
@@ -117,46 +120,50 @@ class DecodeStepper:
         self.upload = torch.cuda.Stream(self.device)
         self.download = torch.cuda.Stream(self.device)
         self.compute = torch.cuda.current_stream(self.device)
-        self._uploaded = [torch.cuda.Event() for _ in range(slots)]
-        self._decoded = [torch.cuda.Event() for _ in range(slots)]
-        self._downloaded = [torch.cuda.Event() for _ in range(slots)]
-        self._used = [False] * slots
         self._lib = binding.library()
-        self._args = {}  # (slot, key cache, value cache) -> the C-ABI argument list
+        handle = ctypes.c_void_p()
+        binding._check(self._lib.pa_stepper_create(slots, int(self.upload.cuda_stream),
+                                                   int(self.compute.cuda_stream), int(self.download.cuda_stream),
+                                                   ctypes.byref(handle)))
+        self._st = handle
+        for sl in range(slots):
+            binding._check(self._lib.pa_stepper_set_slot(
+                self._st, sl, self._h_in[sl].data_ptr(), self._d_in[sl].data_ptr(), self._in_bytes,
+                self._h_out[sl].data_ptr(), self._d_out[sl].data_ptr(), self._out_bytes))
+        self._slot_call = [None] * slots  # (key cache, value cache) each slot's call was set for
 
-    def _call_args(self, s: int, kc: torch.Tensor, vc: torch.Tensor) -> list:
-        key = (s, kc.data_ptr(), vc.data_ptr())
-        args = self._args.get(key)
-        if args is None:
-            # assembled once per (slot, caches); the library still checks them on every call
-            num_seqs, num_heads, hkv, d, bs, max_blocks, num_blocks = self.shape
-            assert kc.shape == self.key_cache.shape and vc.shape == kc.shape and kc.dtype == self.key_cache.dtype
-            dv, out, ws = self._dv_in[s], self._dv_out[s], self._ws[s]
-            ws_ptr, ws_bytes = (ws.data_ptr(), ws.numel()) if ws is not None else (None, 0)
-            stream = int(self.compute.cuda_stream)
-            code = binding._dtype_code(dv.query)
-            kern = binding.KERNELS[self.kernel]
-            tables = self.device_block_tables if self.deltas_mode else dv.block_tables
+    def _set_call(self, s: int, kc: torch.Tensor, vc: torch.Tensor) -> None:
+        """Give slot s its decode call (once per slot and pair of caches)."""
+        key = (kc.data_ptr(), vc.data_ptr())
+        if self._slot_call[s] == key:
+            return
+        num_seqs, num_heads, hkv, d, bs, max_blocks, num_blocks = self.shape
+        assert kc.shape == self.key_cache.shape and vc.shape == kc.shape and kc.dtype == self.key_cache.dtype
+        dv, out, ws = self._dv_in[s], self._dv_out[s], self._ws[s]
+        tables = self.device_block_tables if self.deltas_mode else dv.block_tables
+        c = binding.StepCall()
+        c.kind = ((binding.STEP_FP8_WRITE if self.append else binding.STEP_FP8) if self.fp8 else
+                  binding.STEP_APPEND if self.append else binding.STEP_DECODE)
+        c.out, c.query = out.data_ptr(), dv.query.data_ptr()
+        if self.append:
+            c.new_key, c.new_value = dv.new_key.data_ptr(), dv.new_value.data_ptr()
             if self.fp8:
-                ks, vs = self.k_scale.data_ptr(), self.v_scale.data_ptr()
-                args = [out.data_ptr(), dv.query.data_ptr(), kc.data_ptr(), vc.data_ptr(), ks, vs, tables.data_ptr(),
-                        dv.context_lens.data_ptr(), num_seqs, num_heads, hkv, d, bs, max_blocks, num_blocks,
-                        self.scale, code, ws_ptr, ws_bytes, stream]
-                if self.append:
-                    args = (args, [dv.new_key.data_ptr(), dv.new_value.data_ptr(), kc.data_ptr(), vc.data_ptr(), ks,
-                                   vs, dv.slots.data_ptr(), num_seqs, hkv, d, bs, num_blocks, code, stream])
-            elif self.append:
-                args = [out.data_ptr(), dv.query.data_ptr(), dv.new_key.data_ptr(), dv.new_value.data_ptr(),
-                        kc.data_ptr(), vc.data_ptr(), tables.data_ptr(), dv.context_lens.data_ptr(),
-                        num_seqs, num_heads, hkv, d, bs, max_blocks, num_blocks, self.scale, code, ws_ptr,
-                        ws_bytes, self.max_context_len, self.partition_pages, kern, stream]
-            else:
-                args = [out.data_ptr(), dv.query.data_ptr(), kc.data_ptr(), vc.data_ptr(),
-                        tables.data_ptr(), dv.context_lens.data_ptr(), num_seqs, num_heads, hkv, d, bs,
-                        max_blocks, num_blocks, self.scale, code, ws_ptr, ws_bytes, self.max_context_len,
-                        self.partition_pages, kern, stream]
-            self._args[key] = args
-        return args
+                c.slots = dv.slots.data_ptr()
+        c.key_cache, c.value_cache = kc.data_ptr(), vc.data_ptr()
+        if self.fp8:
+            c.k_scale, c.v_scale = self.k_scale.data_ptr(), self.v_scale.data_ptr()
+        c.block_tables, c.context_lens = tables.data_ptr(), dv.context_lens.data_ptr()
+        c.deltas = dv.deltas.data_ptr() if self.deltas_mode else None
+        (c.num_seqs, c.num_heads, c.num_kv_heads, c.head_dim, c.block_size, c.max_blocks_per_seq,
+         c.num_blocks) = num_seqs, num_heads, hkv, d, bs, max_blocks, num_blocks
+        c.scale = self.scale
+        c.dtype = binding._dtype_code(dv.query)
+        if ws is not None:
+            c.workspace, c.workspace_bytes = ws.data_ptr(), ws.numel()
+        c.max_context_len, c.partition_pages = self.max_context_len, self.partition_pages
+        c.kernel = binding.KERNELS[self.kernel]
+        binding._check(self._lib.pa_stepper_set_call(self._st, s, ctypes.byref(c)))
+        self._slot_call[s] = key
 
     @property
     def h2d_bytes(self) -> int:
@@ -175,58 +182,39 @@ class DecodeStepper:
                value_cache: Optional[torch.Tensor] = None, num_deltas: int = 0) -> None:
         """Upload slot i % slots, decode it on the current stream, download its output.
 
-        Three streams: the upload of a slot waits until the slot's previous decode has read
-        its inputs; the decode waits for its upload (and for the previous download of the
-        slot's output buffer); the download waits for the decode.  The decode stream thus
-        holds only decodes and waits, and consecutive decodes keep overlapping.
+        The sequence runs in native code (pa_stepper_launch) on three streams: the upload of a
+        slot waits until the slot's previous decode has read its inputs; the decode waits for its
+        upload (and for the previous download of the slot's output buffer); the download waits for
+        the decode.  The decode stream thus holds only decodes and waits, and consecutive decodes
+        keep overlapping.
         """
         s = i % self.slots
         kc = self.key_cache if key_cache is None else key_cache
         vc = self.value_cache if value_cache is None else value_cache
-        up, comp, down = self.upload, self.compute, self.download
-        if self._used[s]:
-            up.wait_event(self._decoded[s])
         nbytes = self._in_bytes
         if self.deltas_mode:
             off, shape, _, _ = self._in["deltas"]
             assert 0 <= num_deltas <= shape[0], "num_deltas out of range"
             nbytes = off + 12 * num_deltas
-        torch.cuda.set_stream(up)
-        try:
-            self._d_in[s][:nbytes].copy_(self._h_in[s][:nbytes], non_blocking=True)
-        finally:
-            torch.cuda.set_stream(comp)
-        self._last_h2d = nbytes
-        self._uploaded[s].record(up)
-        comp.wait_event(self._uploaded[s])
-        if self._used[s]:
-            comp.wait_event(self._downloaded[s])
-        if self.deltas_mode and num_deltas:
-            t = self.device_block_tables
-            binding._check(self._lib.pa_apply_table_deltas(t.data_ptr(), t.shape[0], t.shape[1],
-                                                           self._dv_in[s].deltas.data_ptr(), num_deltas,
-                                                           int(comp.cuda_stream)))
-        args = self._call_args(s, kc, vc)
-        if self.fp8:
-            if self.append:  # the new tokens' codes first, then the decode over them
-                binding._check(self._lib.pa_write_kv_fp8(*args[1]))
-                args = args[0]
-            status = self._lib.pa_decode_fp8(*args)
         else:
-            status = (self._lib.pa_decode_append if self.append else self._lib.pa_decode_ex)(*args)
-        binding._check(status)
-        self._decoded[s].record(comp)
-        down.wait_event(self._decoded[s])
-        torch.cuda.set_stream(down)
+            num_deltas = 0
+        self._set_call(s, kc, vc)
+        binding._check(self._lib.pa_stepper_launch(self._st, i, nbytes, num_deltas))
+        self._last_h2d = nbytes
+
+    def close(self) -> None:
+        if getattr(self, "_st", None):
+            torch.cuda.synchronize(self.device)
+            self._lib.pa_stepper_destroy(self._st)
+            self._st = None
+
+    def __del__(self):
         try:
-            self._h_out[s].copy_(self._d_out[s], non_blocking=True)
-        finally:
-            torch.cuda.set_stream(comp)
-        self._downloaded[s].record(down)
-        self._used[s] = True
+            self.close()
+        except Exception:
+            pass
 
     def result(self, i: int) -> torch.Tensor:
         """Host view of step i's output, once its download has finished."""
-        s = i % self.slots
-        self._downloaded[s].synchronize()
-        return self._hv_out[s]
+        binding._check(self._lib.pa_stepper_wait(self._st, i))
+        return self._hv_out[i % self.slots]

@@ -382,3 +382,16 @@ def test_write_layers_and_deltas_reject_bad_arguments(lib):
     assert lib.pa_apply_table_deltas(FAKE, 4, 8, FAKE, 0, None) == 0
     assert lib.pa_apply_table_deltas(None, 4, 8, FAKE, 2, None) == 1
     assert lib.pa_apply_table_deltas(FAKE, 4, 8, FAKE + 2, 2, None) == 1
+
+
+def test_stepper_rejects_bad_arguments(lib):
+    import ctypes
+
+    h = ctypes.c_void_p()
+    assert lib.pa_stepper_create(0, None, None, None, ctypes.byref(h)) == 1 and not h.value
+    assert lib.pa_stepper_create(2, None, None, None, None) == 1
+    assert lib.pa_stepper_set_slot(None, 0, FAKE, FAKE, 16, FAKE, FAKE, 16) == 1
+    assert lib.pa_stepper_set_call(None, 0, None) == 1
+    assert lib.pa_stepper_launch(None, 0, 0, 0) == 1
+    assert lib.pa_stepper_wait(None, 0) == 1
+    lib.pa_stepper_destroy(None)  # a no-op

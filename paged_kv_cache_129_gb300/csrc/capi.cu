@@ -11,6 +11,7 @@
 #include <string>
 
 #include <cudaTypedefs.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "decode_launch.h"
 #include "kv_ops.h"
@@ -27,6 +28,15 @@ namespace {
 thread_local std::string g_message;
 constexpr int kMaxDevices = 64;
 }  // namespace
+
+// An NVTX range around a C-ABI call, so that profilers show each call by name (a no-op when no
+// tool is attached).
+struct CallRange {
+    explicit CallRange(const char* name) { nvtxRangePushA(name); }
+    ~CallRange() { nvtxRangePop(); }
+    CallRange(const CallRange&) = delete;
+    CallRange& operator=(const CallRange&) = delete;
+};
 
 int fail(int code, const char* fmt, ...) {
     char buf[512];
@@ -409,6 +419,7 @@ int pa_check_error(void* stream) {
 int pa_write_kv(const void* key, const void* value, void* key_cache, void* value_cache, const int64_t* slot_mapping,
                 int num_tokens, int num_kv_heads, int head_dim, int block_size, int num_blocks, int dtype,
                 void* stream) {
+    CallRange nvtx_range("pa_write_kv");
     clear_error();
     if (!dtype_ok(dtype)) return fail(PA_ERR_INVALID_ARG, "pa_write_kv: unknown dtype %d", dtype);
     if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
@@ -432,6 +443,7 @@ int pa_write_kv(const void* key, const void* value, void* key_cache, void* value
 
 int pa_copy_blocks(void* key_cache, void* value_cache, const int64_t* src_dst_pairs, int num_pairs, int num_kv_heads,
                    int head_dim, int block_size, int num_blocks, int dtype, void* stream) {
+    CallRange nvtx_range("pa_copy_blocks");
     clear_error();
     if (!dtype_ok(dtype)) return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: unknown dtype %d", dtype);
     if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
@@ -494,6 +506,7 @@ static_assert(PA_MAX_LAYERS == kMaxLayers, "the header's layer limit is the kern
 int pa_write_kv_layers(const void* const* keys, const void* const* values, void* const* key_caches,
                        void* const* value_caches, int num_layers, const int64_t* slot_mapping, int num_tokens,
                        int num_kv_heads, int head_dim, int block_size, int num_blocks, int dtype, void* stream) {
+    CallRange nvtx_range("pa_write_kv_layers");
     clear_error();
     if (!dtype_ok(dtype)) return fail(PA_ERR_INVALID_ARG, "pa_write_kv_layers: unknown dtype %d", dtype);
     if (num_layers < 1 || num_layers > kMaxLayers)
@@ -530,6 +543,7 @@ int pa_write_kv_layers(const void* const* keys, const void* const* values, void*
 
 int pa_apply_table_deltas(int32_t* block_tables, int num_rows, int max_blocks_per_seq, const int32_t* deltas,
                           int num_deltas, void* stream) {
+    CallRange nvtx_range("pa_apply_table_deltas");
     clear_error();
     if (num_rows < 0 || max_blocks_per_seq < 0 || num_deltas < 0)
         return fail(PA_ERR_INVALID_ARG, "pa_apply_table_deltas: bad sizes");
@@ -558,6 +572,7 @@ int pa_apply_table_deltas(int32_t* block_tables, int num_rows, int max_blocks_pe
 int pa_swap_blocks(void* dst_key_cache, void* dst_value_cache, const void* src_key_cache, const void* src_value_cache,
                    const int64_t* block_pairs, int num_pairs, int num_kv_heads, int head_dim, int block_size,
                    int src_num_blocks, int dst_num_blocks, int dtype, void* stream) {
+    CallRange nvtx_range("pa_swap_blocks");
     clear_error();
     if (!dtype_ok(dtype)) return fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: unknown dtype %d", dtype);
     if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || src_num_blocks < 0 ||
@@ -637,6 +652,7 @@ int decode_impl(void* out, const void* query, const void* new_key, const void* n
                 int num_blocks, float scale, int dtype, void* workspace, size_t workspace_bytes, int max_context_len,
                 int partition_pages, int kernel, void* stream, int q_len = 1, const float* k_scale = nullptr,
                 const float* v_scale = nullptr) {
+    CallRange nvtx_range("pa_decode");
     clear_error();
     const bool fp8 = k_scale != nullptr;
     if (fp8 && (!v_scale || !aligned(k_scale, 4) || !aligned(v_scale, 4)))
@@ -817,6 +833,7 @@ size_t pa_decode_fp8_workspace_size(int num_seqs, int num_heads, int num_kv_head
 int pa_write_kv_fp8(const void* key, const void* value, void* key_cache, void* value_cache, const float* k_scale,
                     const float* v_scale, const int64_t* slot_mapping, int num_tokens, int num_kv_heads, int head_dim,
                     int block_size, int num_blocks, int dtype, void* stream) {
+    CallRange nvtx_range("pa_write_kv_fp8");
     clear_error();
     if (!dtype_ok(dtype)) return fail(PA_ERR_INVALID_ARG, "pa_write_kv_fp8: unknown source dtype %d", dtype);
     if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || head_dim % 4 != 0 || block_size <= 0 ||

@@ -496,6 +496,17 @@ int pa_pool_refcount(const pa_pool* pool, int32_t block);
  * ceil(len / block_size) blocks).  PA_OK or PA_ERR_INVALID_ARG with a message.
  */
 int pa_pool_check_invariants(const pa_pool* pool);
+/*
+ * Checkpoint / resume of a pool: pa_pool_save writes the whole state (free list in
+ * order, reference counts, fills, every sequence's table and length, the delta-export
+ * bookkeeping) as a flat byte image of pa_pool_state_size() bytes; pa_pool_load
+ * builds a new pool from an image, which then behaves exactly as the saved pool
+ * (same ids, slots, copies and deltas for the same calls).  A truncated, corrupt or
+ * inconsistent image is refused (PA_ERR_INVALID_ARG).  Host memory only.
+ */
+size_t pa_pool_state_size(const pa_pool* pool);
+int pa_pool_save(const pa_pool* pool, void* buffer, size_t capacity, size_t* written);
+int pa_pool_load(const void* buffer, size_t size, pa_pool** out);
 /* Copy the free list (bottom first) into out[capacity]; returns its length or -1. */
 int pa_pool_free_list(const pa_pool* pool, int32_t* out, int capacity);
 

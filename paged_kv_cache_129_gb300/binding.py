@@ -114,6 +114,9 @@ _SIGNATURES = [
     ("pa_pool_refcount", _I, [_P, ctypes.c_int32]),
     ("pa_pool_check_invariants", _I, [_P]),
     ("pa_pool_free_list", _I, [_P, _P, _I]),
+    ("pa_pool_state_size", _SZ, [_P]),
+    ("pa_pool_save", _I, [_P, _P, _SZ, ctypes.POINTER(_SZ)]),
+    ("pa_pool_load", _I, [_P, _SZ, ctypes.POINTER(_P)]),
 ]
 
 
@@ -632,3 +635,23 @@ class BlockPool:
 
     def check_invariants(self) -> None:
         _check(self._lib.pa_pool_check_invariants(self._h))
+
+    def save(self) -> bytes:
+        """Checkpoint: the pool's whole state as bytes (``pa_pool_save``)."""
+        n = self._lib.pa_pool_state_size(self._h)
+        buf = ctypes.create_string_buffer(max(n, 1))
+        written = _SZ()
+        _check(self._lib.pa_pool_save(self._h, buf, n, ctypes.byref(written)))
+        return buf.raw[:written.value]
+
+    @classmethod
+    def load(cls, state: bytes) -> "BlockPool":
+        """Resume: a new pool from a ``save()`` image (``pa_pool_load``)."""
+        lib = library()
+        handle = _P()
+        _check(lib.pa_pool_load(state, len(state), ctypes.byref(handle)))
+        pool = cls.__new__(cls)
+        pool._h, pool._lib = handle, lib
+        pool.num_blocks = lib.pa_pool_num_blocks(handle)
+        pool.block_size = lib.pa_pool_block_size(handle)
+        return pool

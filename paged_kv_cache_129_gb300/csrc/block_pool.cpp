@@ -381,6 +381,148 @@ int pa_pool_free_list(const pa_pool* pool, int32_t* out, int capacity) {
     return n;
 }
 
+// ---- checkpoint / resume: the whole pool state as a flat little-endian byte image ----
+namespace {
+
+constexpr uint64_t kPoolMagic = 0x314c4f4f50415055ull;  // "UPAPOOL1"
+
+struct Writer {
+    uint8_t* p;
+    size_t cap, n = 0;
+    void put(const void* v, size_t bytes) {
+        if (p && n + bytes <= cap) std::memcpy(p + n, v, bytes);
+        n += bytes;
+    }
+    void i64(int64_t v) { put(&v, 8); }
+    void i32s(const std::vector<int32_t>& v) {
+        i64(static_cast<int64_t>(v.size()));
+        if (!v.empty()) put(v.data(), v.size() * 4);
+    }
+};
+
+struct Reader {
+    const uint8_t* p;
+    size_t size, n = 0;
+    bool ok = true;
+    bool get(void* v, size_t bytes) {
+        if (!ok || n + bytes > size) return ok = false;
+        std::memcpy(v, p + n, bytes);
+        n += bytes;
+        return true;
+    }
+    int64_t i64() {
+        int64_t v = 0;
+        get(&v, 8);
+        return v;
+    }
+    bool i32s(std::vector<int32_t>& v, int64_t max_len) {
+        const int64_t len = i64();
+        if (!ok || len < 0 || len > max_len) return ok = false;
+        v.resize(static_cast<size_t>(len));
+        return len == 0 || get(v.data(), static_cast<size_t>(len) * 4);
+    }
+};
+
+size_t write_state(const pa_pool* pool, uint8_t* buf, size_t cap) {
+    Writer w{buf, cap};
+    w.i64(static_cast<int64_t>(kPoolMagic));
+    w.i64(pool->num_blocks);
+    w.i64(pool->block_size);
+    w.i64(pool->next_id);
+    w.i32s(pool->free_list);
+    w.i32s(pool->refs);
+    w.i32s(pool->fill);
+    // sequences in id order, so that equal pools give equal images
+    std::vector<int64_t> ids;
+    ids.reserve(pool->seqs.size());
+    for (const auto& kv : pool->seqs) ids.push_back(kv.first);
+    std::sort(ids.begin(), ids.end());
+    w.i64(static_cast<int64_t>(ids.size()));
+    for (int64_t id : ids) {
+        const pa_pool::Seq& s = pool->seqs.at(id);
+        w.i64(id);
+        w.i64(s.length);
+        w.i64(s.synced_row);
+        w.i32s(s.table);
+        w.i32s(s.synced_table);
+    }
+    std::vector<std::pair<int, int64_t>> rows(pool->row_owner.begin(), pool->row_owner.end());
+    std::sort(rows.begin(), rows.end());
+    w.i64(static_cast<int64_t>(rows.size()));
+    for (const auto& r : rows) {
+        w.i64(r.first);
+        w.i64(r.second);
+    }
+    return w.n;
+}
+
+}  // namespace
+
+size_t pa_pool_state_size(const pa_pool* pool) { return pool ? write_state(pool, nullptr, 0) : 0; }
+
+int pa_pool_save(const pa_pool* pool, void* buffer, size_t capacity, size_t* written) {
+    if (!pool || !written || (capacity > 0 && !buffer))
+        return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_save: bad arguments");
+    const size_t need = write_state(pool, nullptr, 0);
+    if (need > capacity) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_save: %zu bytes needed, %zu given", need, capacity);
+    *written = write_state(pool, static_cast<uint8_t*>(buffer), capacity);
+    return PA_OK;
+}
+
+int pa_pool_load(const void* buffer, size_t size, pa_pool** out) {
+    if (!buffer || !out) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_load: NULL argument");
+    *out = nullptr;
+    Reader r{static_cast<const uint8_t*>(buffer), size};
+    if (static_cast<uint64_t>(r.i64()) != kPoolMagic || !r.ok)
+        return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_load: not a pool image");
+    const int64_t nb = r.i64(), bs = r.i64(), next_id = r.i64();
+    if (!r.ok || nb < 0 || nb > INT32_MAX || bs <= 0 || bs > INT32_MAX || next_id < 0)
+        return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_load: bad header");
+    pa_pool* p = new (std::nothrow) pa_pool();
+    if (!p) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_load: out of host memory");
+    p->num_blocks = static_cast<int>(nb);
+    p->block_size = static_cast<int>(bs);
+    p->next_id = next_id;
+    bool ok = r.i32s(p->free_list, nb) && r.i32s(p->refs, nb) && r.i32s(p->fill, nb) &&
+              static_cast<int64_t>(p->refs.size()) == nb && static_cast<int64_t>(p->fill.size()) == nb;
+    const int64_t nseq = ok ? r.i64() : -1;
+    ok = ok && r.ok && nseq >= 0 && nseq <= (int64_t)1 << 40;
+    for (int64_t i = 0; ok && i < nseq; ++i) {
+        const int64_t id = r.i64();
+        pa_pool::Seq s;
+        s.length = r.i64();
+        const int64_t row = r.i64();
+        ok = r.ok && id >= 0 && id < next_id && s.length >= 0 && row >= -1 && row <= INT32_MAX &&
+             r.i32s(s.table, nb) && r.i32s(s.synced_table, (int64_t)1 << 31) && !p->seqs.count(id);
+        if (ok) {
+            s.synced_row = static_cast<int>(row);
+            p->seqs.emplace(id, std::move(s));
+        }
+    }
+    const int64_t nrows = ok ? r.i64() : -1;
+    ok = ok && r.ok && nrows >= 0 && nrows <= (int64_t)1 << 31;
+    for (int64_t i = 0; ok && i < nrows; ++i) {
+        const int64_t row = r.i64(), id = r.i64();
+        ok = r.ok && row >= 0 && row <= INT32_MAX;
+        if (ok) p->row_owner[static_cast<int>(row)] = id;
+    }
+    ok = ok && r.n == size;
+    if (ok) {
+        // the image must describe a consistent pool
+        for (int32_t b : p->free_list) ok = ok && b >= 0 && b < nb && p->refs[b] == 0;
+        for (const auto& kv : p->seqs)
+            for (int32_t b : kv.second.table) ok = ok && b >= 0 && b < nb;
+        if (ok && pa_pool_check_invariants(p) != PA_OK) ok = false;
+    }
+    if (!ok) {
+        delete p;
+        return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_load: corrupt or inconsistent pool image");
+    }
+    *out = p;
+    pa::clear_error();
+    return PA_OK;
+}
+
 int pa_pool_check_invariants(const pa_pool* pool) {
     if (!pool) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_check_invariants: NULL pool");
     const int bs = pool->block_size;

@@ -395,3 +395,62 @@ def test_stepper_rejects_bad_arguments(lib):
     assert lib.pa_stepper_launch(None, 0, 0, 0) == 1
     assert lib.pa_stepper_wait(None, 0) == 1
     lib.pa_stepper_destroy(None)  # a no-op
+
+
+# ---- checkpoint / resume of the pool ----------------------------------------------------------
+def _drive(pool, live, rng, steps):
+    """Random operations; returns everything the pool answered, for comparing two pools."""
+    log = []
+    for _ in range(steps):
+        op = int(rng.integers(0, 8))
+        try:
+            if op == 0 or not live:
+                live.append(pool.create())
+                log.append(("create", live[-1]))
+            elif op == 1:
+                live.append(pool.fork(live[int(rng.integers(len(live)))]))
+                log.append(("fork", live[-1]))
+            elif op == 2:
+                pool.release(live.pop(int(rng.integers(len(live)))))
+                log.append(("release",))
+            elif op == 3:
+                k = rng.permutation(len(live))[:6]
+                d, lens = pool.table_deltas([live[i] for i in k])
+                log.append(("deltas", d.tolist(), lens.tolist()))
+            else:
+                log.append(("append", pool.append(live[int(rng.integers(len(live)))])))
+        except pa.PoolExhausted:
+            log.append(("exhausted",))
+    return log
+
+
+def test_pool_save_load_resumes_exactly(lib):
+    rng = np.random.default_rng(7)
+    pool = pa.BlockPool(96, 4, free_order=rng.permutation(96))
+    live = []
+    _drive(pool, live, rng, 500)
+    state = pool.save()
+    assert len(state) == lib.pa_pool_state_size(pool._h)
+    twin = pa.BlockPool.load(state)
+    twin.check_invariants()
+    assert twin.save() == state  # the same image
+    seed = int(rng.integers(1 << 30))
+    a = _drive(pool, list(live), np.random.default_rng(seed), 800)
+    b = _drive(twin, list(live), np.random.default_rng(seed), 800)
+    assert a == b
+    assert pool.save() == twin.save()
+
+
+def test_pool_load_refuses_bad_images(lib):
+    pool = pa.BlockPool(8, 2)
+    s = pool.create()
+    for _ in range(5):
+        pool.append(s)
+    state = bytearray(pool.save())
+    for bad in (bytes(state[:-1]), bytes(state) + b"\0", b"\0" * len(state)):
+        with pytest.raises(pa.PAError):
+            pa.BlockPool.load(bad)
+    corrupt = bytearray(state)
+    corrupt[8 * 4 + 8] ^= 0x01  # the first free-list entry
+    with pytest.raises(pa.PAError):
+        pa.BlockPool.load(bytes(corrupt))

@@ -531,17 +531,21 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         ksd, vsd = torch.from_numpy(ks_np).to(device), torch.from_numpy(vs_np).to(device)
         nb_ = inp.num_blocks
         all_slots = torch.arange(nb_ * bs, dtype=torch.int64, device=device)
-        q8k = torch.empty(nb_, Hkv, bs, d, dtype=torch.uint8, device=device)
-        q8v = torch.empty_like(q8k)
+        interleaved = args.fp8_layout == "interleaved"
+        if interleaved:  # [N, H_kv, 2, bs, d]: one record per (block, kv head), K rows then V rows
+            q8k, q8v = torch.empty(nb_, Hkv, 2, bs, d, dtype=torch.uint8, device=device), None
+        else:
+            q8k = torch.empty(nb_, Hkv, bs, d, dtype=torch.uint8, device=device)
+            q8v = torch.empty_like(q8k)
         pa.write_kv_fp8(kc0.permute(0, 2, 1, 3).reshape(nb_ * bs, Hkv, d).contiguous(),
                         vc0.permute(0, 2, 1, 3).reshape(nb_ * bs, Hkv, d).contiguous(), q8k, q8v, ksd, vsd, all_slots)
         torch.cuda.synchronize()
         del kc0, vc0, all_slots
-        kc0, vc0 = q8k, q8v
+        kc0, vc0 = q8k, q8v  # q8v None: the interleaved layout
     kcs, vcs = [kc0], [vc0]
     for _ in range(replicas - 1):
         kcs.append(kc0.clone())
-        vcs.append(vc0.clone())
+        vcs.append(vc0.clone() if vc0 is not None else None)
     q = up(inp.q)
     bt = torch.from_numpy(tables).to(device)
     dl = torch.from_numpy(lens).to(device)
@@ -574,26 +578,30 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         assert np.array_equal(np.asarray(slots)[live], derived[live])
 
     # Pre-marshalled C-ABI argument lists (the timed loop only calls the library).
-    dec_args = [[out.data_ptr(), q.data_ptr(), kcs[r].data_ptr(), vcs[r].data_ptr(), bt.data_ptr(), dl.data_ptr(),
+    def ptr(t):
+        return t.data_ptr() if t is not None else None
+
+    dec_args = [[out.data_ptr(), q.data_ptr(), kcs[r].data_ptr(), ptr(vcs[r]), bt.data_ptr(), dl.data_ptr(),
                  B] + ([q_len] if q_len > 1 else []) + [Hq, Hkv, d, bs, tables.shape[1], inp.num_blocks,
                  float(inp.scale), code, ws.data_ptr(), ws.numel(), max_ctx, args.partition_pages, kern, sptr]
                 for r in range(replicas)]
     decode_fn = lib.pa_decode_multi if q_len > 1 else lib.pa_decode_ex
-    wr_args = ([[nk.data_ptr(), nv.data_ptr(), kcs[r].data_ptr(), vcs[r].data_ptr(), sl.data_ptr(), ntok, Hkv, d, bs,
+    wr_args = ([[nk.data_ptr(), nv.data_ptr(), kcs[r].data_ptr(), ptr(vcs[r]), sl.data_ptr(), ntok, Hkv, d, bs,
                  inp.num_blocks, code, sptr] for r in range(replicas)] if has_write else None)
     if fp8:
         decode_fn = lib.pa_decode_fp8
-        dec_args = [[out.data_ptr(), q.data_ptr(), kcs[r].data_ptr(), vcs[r].data_ptr(), ksd.data_ptr(),
+        vptr = [vcs[r].data_ptr() if vcs[r] is not None else None for r in range(replicas)]
+        dec_args = [[out.data_ptr(), q.data_ptr(), kcs[r].data_ptr(), vptr[r], ksd.data_ptr(),
                      vsd.data_ptr(), bt.data_ptr(), dl.data_ptr(), B, Hq, Hkv, d, bs, tables.shape[1], inp.num_blocks,
                      float(inp.scale), code, ws.data_ptr(), ws.numel(), sptr] for r in range(replicas)]
         write_fn = lib.pa_write_kv_fp8
         if has_write:
-            wr_args = [[nk.data_ptr(), nv.data_ptr(), kcs[r].data_ptr(), vcs[r].data_ptr(), ksd.data_ptr(),
+            wr_args = [[nk.data_ptr(), nv.data_ptr(), kcs[r].data_ptr(), vptr[r], ksd.data_ptr(),
                         vsd.data_ptr(), sl.data_ptr(), ntok, Hkv, d, bs, inp.num_blocks, code, sptr]
                        for r in range(replicas)]
     else:
         write_fn = lib.pa_write_kv
-    app_args = ([[out.data_ptr(), q.data_ptr(), nk.data_ptr(), nv.data_ptr(), kcs[r].data_ptr(), vcs[r].data_ptr(),
+    app_args = ([[out.data_ptr(), q.data_ptr(), nk.data_ptr(), nv.data_ptr(), kcs[r].data_ptr(), ptr(vcs[r]),
                   bt.data_ptr(), dl.data_ptr(), B, Hq, Hkv, d, bs, tables.shape[1], inp.num_blocks, float(inp.scale),
                   code, ws.data_ptr(), ws.numel(), max_ctx, args.partition_pages, kern, sptr]
                  for r in range(replicas)] if fused else None)
@@ -1287,6 +1295,8 @@ def main(argv=None) -> None:
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--fp8-layout", choices=["interleaved", "separate"], default="interleaved",
+                    help="FP8 workloads: K and V of a (block, kv head) in one record, or two caches")
     args = ap.parse_args(argv)
     args.warmup = max(args.warmup, 3)
 

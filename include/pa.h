@@ -245,6 +245,10 @@ int pa_decode_append(void* out, const void* query, const void* new_key, const vo
  * [num_blocks, H_kv] (device), one scale per (physical block, kv head), positive and
  * finite.  The value attended is code * scale.  Choosing the scales (e.g. from the
  * block's first tokens, or one per layer) is the caller's policy.
+ * Interleaved layout: with value_cache == NULL, key_cache holds [num_blocks, H_kv, 2,
+ * block_size, head_dim] bytes, the K rows then the V rows of every (block, kv head),
+ * so that the decode brings a page's K and V in one contiguous 2 * block_size * head_dim
+ * byte copy (the same layout for pa_write_kv_fp8 and pa_decode_fp8).
  *
  * pa_write_kv_fp8 — pa_write_kv into an FP8 cache: element i of token t, kv head h
  * is stored as e4m3(x / scale[slot / block_size, h]) with x the source element

@@ -336,29 +336,38 @@ def decode(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tens
     return out
 
 
-def _fp8_cache(key_cache: torch.Tensor, value_cache: torch.Tensor, k_scale: torch.Tensor, v_scale: torch.Tensor):
-    for name, t in (("key_cache", key_cache), ("value_cache", value_cache), ("k_scale", k_scale),
-                    ("v_scale", v_scale)):
+def _fp8_cache(key_cache: torch.Tensor, value_cache: Optional[torch.Tensor], k_scale: torch.Tensor,
+               v_scale: torch.Tensor):
+    """Checks FP8 caches; value_cache None means the interleaved layout [N, H_kv, 2, bs, d] in key_cache.
+    Returns (num_blocks, H_kv, bs, d)."""
+    for name, t in (("key_cache", key_cache), ("k_scale", k_scale), ("v_scale", v_scale)):
         _cuda(t, name)
-    _need(key_cache.dim() == 4 and value_cache.shape == key_cache.shape, "caches must be [N, H_kv, bs, d]")
-    _need(key_cache.dtype == value_cache.dtype and key_cache.dtype in (torch.uint8, torch.float8_e4m3fn),
-          "FP8 caches hold E4M3 codes (uint8 or float8_e4m3fn)")
-    _need(k_scale.dtype == v_scale.dtype == torch.float32 and k_scale.shape == v_scale.shape == key_cache.shape[:2],
+    _need(key_cache.dtype in (torch.uint8, torch.float8_e4m3fn), "FP8 caches hold E4M3 codes (uint8 or float8_e4m3fn)")
+    if value_cache is None:
+        _need(key_cache.dim() == 5 and key_cache.shape[2] == 2, "interleaved FP8 cache: [N, H_kv, 2, bs, d]")
+        shape = (key_cache.shape[0], key_cache.shape[1], key_cache.shape[3], key_cache.shape[4])
+    else:
+        _cuda(value_cache, "value_cache")
+        _need(key_cache.dim() == 4 and value_cache.shape == key_cache.shape, "caches must be [N, H_kv, bs, d]")
+        _need(value_cache.dtype == key_cache.dtype, "caches must share a dtype")
+        shape = tuple(key_cache.shape)
+    _need(k_scale.dtype == v_scale.dtype == torch.float32 and k_scale.shape == v_scale.shape == shape[:2],
           "k_scale / v_scale: float32 [N, H_kv]")
-    return key_cache.shape
+    return shape
 
 
-def write_kv_fp8(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor,
+def write_kv_fp8(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor, value_cache: Optional[torch.Tensor],
                  k_scale: torch.Tensor, v_scale: torch.Tensor, slot_mapping: torch.Tensor, stream=None) -> None:
     """``pa_write_kv_fp8``: quantise key/value ``[T, H_kv, d]`` (f32/f16/bf16) into the E4M3 caches at
-    ``slot_mapping`` with the (block, kv head) scales."""
+    ``slot_mapping`` with the (block, kv head) scales (``value_cache`` None: the interleaved layout)."""
     num_blocks, hkv, bs, d = _fp8_cache(key_cache, value_cache, k_scale, v_scale)
     for name, t in (("key", key), ("value", value), ("slot_mapping", slot_mapping)):
         _cuda(t, name)
     _need(key.shape == value.shape and key.dim() == 3 and key.shape[1:] == (hkv, d), "key/value must be [T, H_kv, d]")
     _need(key.dtype == value.dtype, "key and value must share a dtype")
     _need(slot_mapping.dtype == torch.int64 and slot_mapping.numel() == key.shape[0], "slot_mapping: int64 [T]")
-    _check(library().pa_write_kv_fp8(key.data_ptr(), value.data_ptr(), key_cache.data_ptr(), value_cache.data_ptr(),
+    vptr = value_cache.data_ptr() if value_cache is not None else None
+    _check(library().pa_write_kv_fp8(key.data_ptr(), value.data_ptr(), key_cache.data_ptr(), vptr,
                                      k_scale.data_ptr(), v_scale.data_ptr(), slot_mapping.data_ptr(), key.shape[0],
                                      hkv, d, bs, num_blocks, _dtype_code(key), _stream_ptr(stream, key.device)))
 
@@ -369,7 +378,7 @@ def decode_fp8_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, 
                                                       max_blocks_per_seq, _TORCH_DTYPES[dtype]))
 
 
-def decode_fp8(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.Tensor, k_scale: torch.Tensor,
+def decode_fp8(query: torch.Tensor, key_cache: torch.Tensor, value_cache: Optional[torch.Tensor], k_scale: torch.Tensor,
                v_scale: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
                scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
                workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
@@ -393,7 +402,8 @@ def decode_fp8(query: torch.Tensor, key_cache: torch.Tensor, value_cache: torch.
         n = decode_fp8_workspace_size(b, hq, hkv, d, bs, block_tables.shape[1], query.dtype)
         workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=query.device)
     _cuda(workspace, "workspace")
-    _check(library().pa_decode_fp8(out.data_ptr(), query.data_ptr(), key_cache.data_ptr(), value_cache.data_ptr(),
+    vptr = value_cache.data_ptr() if value_cache is not None else None
+    _check(library().pa_decode_fp8(out.data_ptr(), query.data_ptr(), key_cache.data_ptr(), vptr,
                                    k_scale.data_ptr(), v_scale.data_ptr(), block_tables.data_ptr(),
                                    context_lens.data_ptr(), b, hq, hkv, d, bs, block_tables.shape[1], num_blocks,
                                    float(scale), _dtype_code(query), workspace.data_ptr(),

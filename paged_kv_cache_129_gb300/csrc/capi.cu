@@ -151,8 +151,10 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
 
 // 2-D view of a cache: rows = num_blocks * H_kv * bs (one row per slot and head), columns = d.
 // The box is 128 bytes of d by bs rows, loaded with the 128-byte swizzle.
+// interleave = 2: an FP8 cache holding K then V of every (block, kv head) ([N, H_kv, 2, bs, d]): twice
+// the rows, and a box of 2 * bs rows that brings a page's K and V in one copy.
 int encode_cache_map_uncached(CUtensorMap* map, const void* base, int dtype, int num_blocks, int num_kv_heads,
-                              int block_size, int head_dim) {
+                              int block_size, int head_dim, int interleave = 1) {
     PFN_cuTensorMapEncodeTiled_v12000 encode = tensor_map_encoder();
     if (!encode) return fail(PA_ERR_CUDA, "cuTensorMapEncodeTiled is not available from the driver");
     const int eb = elem_bytes(dtype);
@@ -160,9 +162,9 @@ int encode_cache_map_uncached(CUtensorMap* map, const void* base, int dtype, int
                                      : dtype == PA_F16     ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                      : dtype == kCacheE4M3 ? CU_TENSOR_MAP_DATA_TYPE_UINT8
                                                            : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)num_blocks * num_kv_heads * block_size};
+    cuuint64_t dims[2] = {(cuuint64_t)head_dim, (cuuint64_t)num_blocks * num_kv_heads * block_size * interleave};
     cuuint64_t strides[1] = {(cuuint64_t)head_dim * eb};
-    cuuint32_t box[2] = {(cuuint32_t)(128 / eb), (cuuint32_t)block_size};
+    cuuint32_t box[2] = {(cuuint32_t)(128 / eb), (cuuint32_t)(block_size * interleave)};
     cuuint32_t estrides[2] = {1, 1};
     CUresult r = encode(map, type, 2, const_cast<void*>(base), dims, strides, box, estrides,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
@@ -174,10 +176,10 @@ int encode_cache_map_uncached(CUtensorMap* map, const void* base, int dtype, int
 // The same caches are described again on every call of a decode loop: keep the last few
 // descriptors of this thread (a descriptor is a pure function of these arguments).
 int encode_cache_map(CUtensorMap* map, const void* base, int dtype, int num_blocks, int num_kv_heads,
-                     int block_size, int head_dim) {
+                     int block_size, int head_dim, int interleave = 1) {
     struct Entry {
         const void* base;
-        int dtype, num_blocks, num_kv_heads, block_size, head_dim;
+        int dtype, num_blocks, num_kv_heads, block_size, head_dim, interleave;
         CUtensorMap map;
     };
     constexpr int kEntries = 8;
@@ -185,13 +187,15 @@ int encode_cache_map(CUtensorMap* map, const void* base, int dtype, int num_bloc
     thread_local int next = 0;
     for (const Entry& e : entries)
         if (e.base == base && e.base && e.dtype == dtype && e.num_blocks == num_blocks &&
-            e.num_kv_heads == num_kv_heads && e.block_size == block_size && e.head_dim == head_dim) {
+            e.num_kv_heads == num_kv_heads && e.block_size == block_size && e.head_dim == head_dim &&
+            e.interleave == interleave) {
             *map = e.map;
             return PA_OK;
         }
-    const int st = encode_cache_map_uncached(map, base, dtype, num_blocks, num_kv_heads, block_size, head_dim);
+    const int st =
+        encode_cache_map_uncached(map, base, dtype, num_blocks, num_kv_heads, block_size, head_dim, interleave);
     if (st != PA_OK) return st;
-    entries[next] = Entry{base, dtype, num_blocks, num_kv_heads, block_size, head_dim, *map};
+    entries[next] = Entry{base, dtype, num_blocks, num_kv_heads, block_size, head_dim, interleave, *map};
     next = (next + 1) % kEntries;
     return PA_OK;
 }
@@ -663,13 +667,13 @@ int decode_impl(void* out, const void* query, const void* new_key, const void* n
     if (new_key && (!new_value || !aligned(new_key, 16) || !aligned(new_value, 16)))
         return fail(PA_ERR_INVALID_ARG, "pa_decode_append: new_key/new_value must be non-NULL and 16-byte aligned");
     if (num_seqs == 0) return PA_OK;
-    if (!out || !query || !key_cache || !value_cache || !block_tables || !context_lens)
+    if (!out || !query || !key_cache || (!value_cache && !fp8) || !block_tables || !context_lens)
         return fail(PA_ERR_INVALID_ARG, "pa_decode: NULL pointer");
     if (num_blocks <= 0) return fail(PA_ERR_INVALID_ARG, "pa_decode: num_blocks=%d", num_blocks);
     if (num_kv_heads <= 0 || (long long)num_blocks * num_kv_heads * block_size >= (1ll << 31))
         return fail(PA_ERR_INVALID_ARG, "pa_decode: num_blocks * num_kv_heads * block_size must be < 2^31");
     if (!std::isfinite(scale)) return fail(PA_ERR_INVALID_ARG, "pa_decode: scale is not finite");
-    if (!aligned(key_cache, 16) || !aligned(value_cache, 16))
+    if (!aligned(key_cache, 16) || !aligned(value_cache, 16))  // (a NULL value cache is aligned)
         return fail(PA_ERR_INVALID_ARG, "pa_decode: caches must be 16-byte aligned");
     if (!aligned(query, 4) || !aligned(out, 4) || !aligned(block_tables, 4) || !aligned(context_lens, 4))
         return fail(PA_ERR_INVALID_ARG, "pa_decode: query/out/tables/lens must be 4-byte aligned");
@@ -686,10 +690,16 @@ int decode_impl(void* out, const void* query, const void* new_key, const void* n
 
     CUtensorMap tk, tv;
     const int cache_type = fp8 ? kCacheE4M3 : dtype;
-    st = encode_cache_map(&tk, key_cache, cache_type, num_blocks, num_kv_heads, block_size, head_dim);
+    const bool interleaved = fp8 && value_cache == nullptr;  // K and V of a (block, head) in one record
+    st = encode_cache_map(&tk, key_cache, cache_type, num_blocks, num_kv_heads, block_size, head_dim,
+                          interleaved ? 2 : 1);
     if (st != PA_OK) return st;
-    st = encode_cache_map(&tv, value_cache, cache_type, num_blocks, num_kv_heads, block_size, head_dim);
-    if (st != PA_OK) return st;
+    if (interleaved) {
+        tv = tk;
+    } else {
+        st = encode_cache_map(&tv, value_cache, cache_type, num_blocks, num_kv_heads, block_size, head_dim);
+        if (st != PA_OK) return st;
+    }
 
     DecodeArgs a{};
     a.out = out;
@@ -710,6 +720,7 @@ int decode_impl(void* out, const void* query, const void* new_key, const void* n
     a.value_cache = new_key ? const_cast<void*>(value_cache) : nullptr;
     a.k_scale = k_scale;
     a.v_scale = v_scale;
+    a.kv_interleaved = interleaved ? 1 : 0;
     a.lean_warps_per_cta = p.ki.lean_warps_per_cta;
     a.err = dev->error_word;
     a.num_seqs = num_seqs;
@@ -840,7 +851,7 @@ int pa_write_kv_fp8(const void* key, const void* value, void* key_cache, void* v
         num_blocks < 0)
         return fail(PA_ERR_INVALID_ARG, "pa_write_kv_fp8: bad sizes (head_dim must be a multiple of 4)");
     if (num_tokens == 0) return PA_OK;
-    if (!key || !value || !key_cache || !value_cache || !k_scale || !v_scale || !slot_mapping)
+    if (!key || !value || !key_cache || !k_scale || !v_scale || !slot_mapping)  // value_cache NULL: interleaved
         return fail(PA_ERR_INVALID_ARG, "pa_write_kv_fp8: NULL pointer");
     const int eb = elem_bytes(dtype);
     if (!aligned(slot_mapping, 8) || !aligned(key, eb) || !aligned(value, eb) || !aligned(key_cache, 4) ||

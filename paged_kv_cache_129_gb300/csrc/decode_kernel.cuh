@@ -1381,14 +1381,21 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
                             mbar_arrive_expect_tx(&full[s], C::kSlotBytes);
                             uint8_t* kdst = ring + s * C::kSlotBytes;
                             uint8_t* vdst = kdst + C::kPageBytes;
+                            if (F8 && a.kv_interleaved) {
+                                // K rows 2r .. 2r + BS - 1, then V: one box of 2 * BS rows (one 128-byte box
+                                // a row at head_dim 128), landing as the K page followed by the V page
+                                static_assert(!F8 || C::Base::kNBox == 1, "one box per FP8 row");
+                                tma_load_2d_hint(kdst, &tmap_k, 0, 2 * r, &full[s], stream_policy);
+                            } else {
 #pragma unroll
-                            for (int bx = 0; bx < C::Base::kNBox; ++bx)
-                                tma_load_2d_hint(kdst + bx * C::Base::kBoxBytes, &tmap_k, bx * C::Base::kBoxElems, r,
-                                                 &full[s], stream_policy);
+                                for (int bx = 0; bx < C::Base::kNBox; ++bx)
+                                    tma_load_2d_hint(kdst + bx * C::Base::kBoxBytes, &tmap_k, bx * C::Base::kBoxElems,
+                                                     r, &full[s], stream_policy);
 #pragma unroll
-                            for (int bx = 0; bx < C::Base::kNBox; ++bx)
-                                tma_load_2d_hint(vdst + bx * C::Base::kBoxBytes, &tmap_v, bx * C::Base::kBoxElems, r,
-                                                 &full[s], stream_policy);
+                                for (int bx = 0; bx < C::Base::kNBox; ++bx)
+                                    tma_load_2d_hint(vdst + bx * C::Base::kBoxBytes, &tmap_v, bx * C::Base::kBoxElems,
+                                                     r, &full[s], stream_policy);
+                            }
                         } else {
                             atomicOr(a.err, kErrBadTable);  // skip the load; the slot keeps stale data
                             mbar_arrive(&full[s]);

@@ -30,6 +30,9 @@ struct DecodeArgs {
     // FP8 caches (E4M3 codes): float32 scales [num_blocks, num_kv_heads] for K and V.
     const float* k_scale;
     const float* v_scale;
+    // FP8 cache layout [N, H_kv, 2, bs, D] (K then V of each (block, kv head)), one tensor map whose
+    // 2 * bs-row box brings a page's K and V in one copy; 0: separate K and V caches.
+    int kv_interleaved;
     int num_seqs, num_heads, num_kv_heads, group, head_chunks;
     // Multi-query decode: q_len query tokens per sequence at positions L - q_len .. L - 1
     // (q_len = 1: single-step decode).  A kv head serves rows = q_len * group query rows,

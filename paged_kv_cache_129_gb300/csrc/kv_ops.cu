@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(256) write_kv_fp8_kernel(const S* __restrict__
                                                            const float* __restrict__ v_scale,
                                                            const int64_t* __restrict__ slots, int num_tokens,
                                                            int num_kv_heads, int head_dim, int block_size,
-                                                           long long num_slots, unsigned* err) {
+                                                           long long num_slots, int interleaved, unsigned* err) {
     griddep_wait();
     griddep_launch_dependents();
     const long long gw = (long long)blockIdx.x * (blockDim.x >> 5) + (threadIdx.x >> 5);
@@ -106,7 +106,11 @@ __global__ void __launch_bounds__(256) write_kv_fp8_kernel(const S* __restrict__
     const float ks = __ldg(k_scale + blk * num_kv_heads + h);
     const float vs = __ldg(v_scale + blk * num_kv_heads + h);
     const size_t src = ((size_t)t * num_kv_heads + h) * head_dim;
-    const size_t dst = (((size_t)blk * num_kv_heads + h) * block_size + off) * head_dim;
+    // separate caches: row (blk, h, off) of each; interleaved ([N, H_kv, 2, bs, d] in key_cache):
+    // the K row, and the V row bs rows further
+    const size_t rec = (size_t)blk * num_kv_heads + h;
+    const size_t dst = interleaved ? (rec * 2 * block_size + off) * head_dim : (rec * block_size + off) * head_dim;
+    const size_t dst_v = interleaved ? dst + (size_t)block_size * head_dim : dst;
     for (int i = 4 * lane; i < head_dim; i += 128) {
         float xk[4], xv[4];
 #pragma unroll
@@ -121,7 +125,7 @@ __global__ void __launch_bounds__(256) write_kv_fp8_kernel(const S* __restrict__
                             ((uint32_t)__nv_cvt_float2_to_fp8x2(make_float2(xv[2], xv[3]), __NV_SATFINITE, __NV_E4M3)
                              << 16);
         *reinterpret_cast<uint32_t*>(key_cache + dst + i) = ck;
-        *reinterpret_cast<uint32_t*>(value_cache + dst + i) = cv;
+        *reinterpret_cast<uint32_t*>(value_cache + dst_v + i) = cv;
     }
 }
 
@@ -294,22 +298,24 @@ cudaError_t write_kv_fp8_launch(const WriteFp8Args& a, cudaStream_t stream) {
     const int threads = 256;
     const long long grid = (warps + (threads / 32) - 1) / (threads / 32);
     const long long num_slots = (long long)a.num_blocks * a.block_size;
+    const int interleaved = a.value_cache == nullptr ? 1 : 0;
+    uint8_t* vc = interleaved ? a.key_cache : a.value_cache;
     switch (a.src_dtype) {
         case 0:
             return launch_pdl(write_kv_fp8_kernel<float>, dim3((unsigned)grid), dim3(threads), 0, stream,
                               static_cast<const float*>(a.key), static_cast<const float*>(a.value), a.key_cache,
-                              a.value_cache, a.k_scale, a.v_scale, a.slot_mapping, a.num_tokens, a.num_kv_heads,
-                              a.head_dim, a.block_size, num_slots, a.err);
+                              vc, a.k_scale, a.v_scale, a.slot_mapping, a.num_tokens, a.num_kv_heads,
+                              a.head_dim, a.block_size, num_slots, interleaved, a.err);
         case 1:
             return launch_pdl(write_kv_fp8_kernel<__half>, dim3((unsigned)grid), dim3(threads), 0, stream,
                               static_cast<const __half*>(a.key), static_cast<const __half*>(a.value), a.key_cache,
-                              a.value_cache, a.k_scale, a.v_scale, a.slot_mapping, a.num_tokens, a.num_kv_heads,
-                              a.head_dim, a.block_size, num_slots, a.err);
+                              vc, a.k_scale, a.v_scale, a.slot_mapping, a.num_tokens, a.num_kv_heads,
+                              a.head_dim, a.block_size, num_slots, interleaved, a.err);
         case 2:
             return launch_pdl(write_kv_fp8_kernel<__nv_bfloat16>, dim3((unsigned)grid), dim3(threads), 0, stream,
                               static_cast<const __nv_bfloat16*>(a.key), static_cast<const __nv_bfloat16*>(a.value),
-                              a.key_cache, a.value_cache, a.k_scale, a.v_scale, a.slot_mapping, a.num_tokens,
-                              a.num_kv_heads, a.head_dim, a.block_size, num_slots, a.err);
+                              a.key_cache, vc, a.k_scale, a.v_scale, a.slot_mapping, a.num_tokens,
+                              a.num_kv_heads, a.head_dim, a.block_size, num_slots, interleaved, a.err);
         default:
             return cudaErrorInvalidValue;
     }

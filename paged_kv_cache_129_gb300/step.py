@@ -72,11 +72,15 @@ class DecodeStepper:
                  k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
                  query_dtype: Optional[torch.dtype] = None):
         assert tables in ("full", "deltas")
-        assert key_cache.is_cuda and key_cache.shape == value_cache.shape and key_cache.dim() == 4
+        self.fp8 = k_scale is not None
+        if self.fp8 and value_cache is None:  # interleaved FP8 layout [N, H_kv, 2, bs, d]
+            assert key_cache.is_cuda and key_cache.dim() == 5 and key_cache.shape[2] == 2
+            num_blocks, hkv, _, bs, d = key_cache.shape
+        else:
+            assert key_cache.is_cuda and key_cache.shape == value_cache.shape and key_cache.dim() == 4
+            num_blocks, hkv, bs, d = key_cache.shape
         self.device = key_cache.device
         self.key_cache, self.value_cache = key_cache, value_cache
-        num_blocks, hkv, bs, d = key_cache.shape
-        self.fp8 = k_scale is not None
         if self.fp8:
             assert v_scale is not None and query_dtype in (torch.float16, torch.bfloat16)
             self.k_scale, self.v_scale = k_scale, v_scale
@@ -134,11 +138,12 @@ class DecodeStepper:
 
     def _set_call(self, s: int, kc: torch.Tensor, vc: torch.Tensor) -> None:
         """Give slot s its decode call (once per slot and pair of caches)."""
-        key = (kc.data_ptr(), vc.data_ptr())
+        key = (kc.data_ptr(), vc.data_ptr() if vc is not None else None)
         if self._slot_call[s] == key:
             return
         num_seqs, num_heads, hkv, d, bs, max_blocks, num_blocks = self.shape
-        assert kc.shape == self.key_cache.shape and vc.shape == kc.shape and kc.dtype == self.key_cache.dtype
+        assert kc.shape == self.key_cache.shape and kc.dtype == self.key_cache.dtype
+        assert (vc is None) == (self.value_cache is None) and (vc is None or vc.shape == kc.shape)
         dv, out, ws = self._dv_in[s], self._dv_out[s], self._ws[s]
         tables = self.device_block_tables if self.deltas_mode else dv.block_tables
         c = binding.StepCall()
@@ -149,7 +154,7 @@ class DecodeStepper:
             c.new_key, c.new_value = dv.new_key.data_ptr(), dv.new_value.data_ptr()
             if self.fp8:
                 c.slots = dv.slots.data_ptr()
-        c.key_cache, c.value_cache = kc.data_ptr(), vc.data_ptr()
+        c.key_cache, c.value_cache = kc.data_ptr(), (vc.data_ptr() if vc is not None else None)
         if self.fp8:
             c.k_scale, c.v_scale = self.k_scale.data_ptr(), self.v_scale.data_ptr()
         c.block_tables, c.context_lens = tables.data_ptr(), dv.context_lens.data_ptr()

@@ -215,3 +215,37 @@ def test_stepper_fp8_matches_direct_calls():
     for i in range(steps):
         assert torch.equal(got[i].view(torch.int16), refs[i].cpu().view(torch.int16)), f"step {i}"
     assert torch.equal(kc, kc_ref) and torch.equal(vc, vc_ref)
+
+
+@pytest.mark.parametrize("bs", [16, 32])
+def test_interleaved_layout_matches_separate_caches(bs):
+    """The interleaved FP8 layout ([N, H_kv, 2, bs, d]: K rows then V rows of each (block, kv head), one
+    copy per page): the writer stores the same codes as into separate caches (bit-exact against the oracle),
+    and the decode gives the same bits as over separate caches, within tolerance of the oracle."""
+    rng = np.random.default_rng(bs)
+    hq, hkv, d = 28, 4, 128
+    q, kc, vc, ks, vs, bt, lens = _case(40 + bs, [1, 17, 300, 1000, 64, 0], hq, hkv, bs, "bf16")
+    nb = kc.shape[0]
+    # the writer: every slot of the pool from bf16 sources
+    src_k = _src(rng, (nb * bs, hkv, d), "bf16", 2.0)
+    src_v = _src(rng, (nb * bs, hkv, d), "bf16", 2.0)
+    slots = np.arange(nb * bs, dtype=np.int64)
+    kv = torch.empty(nb, hkv, 2, bs, d, dtype=torch.uint8, device="cuda")
+    dks, dvs = torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda()
+    pa.write_kv_fp8(to_device(src_k, "bf16"), to_device(src_v, "bf16"), kv, None, dks, dvs,
+                    torch.from_numpy(slots).cuda())
+    exp_k, exp_v = np.zeros_like(kc), np.zeros_like(vc)
+    assert oracle.write_kv_fp8(src_k, src_v, "bf16", exp_k, exp_v, ks, vs, slots) == oracle.OK
+    torch.cuda.synchronize()
+    got = kv.cpu().numpy()
+    assert np.array_equal(got[:, :, 0], exp_k) and np.array_equal(got[:, :, 1], exp_v)
+    # the decode over the interleaved layout vs separate caches and the oracle
+    kv2 = torch.from_numpy(np.ascontiguousarray(np.stack([kc, vc], axis=2))).cuda()
+    dq, dbt, dl = to_device(q, "bf16"), torch.from_numpy(bt).cuda(), torch.from_numpy(lens).cuda()
+    inter = pa.decode_fp8(dq, kv2, None, dks, dvs, dbt, dl)
+    sep = pa.decode_fp8(dq, torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda(), dks, dvs, dbt, dl)
+    torch.cuda.synchronize()
+    assert torch.equal(inter.view(torch.int16), sep.view(torch.int16))
+    ref = oracle.decode_fp8(q, "bf16", kc, vc, ks, vs, bt, lens, 1 / np.sqrt(d))
+    assert_decode_close(to_f64(inter), ref, "bf16")
+    pa.check_error()

@@ -50,7 +50,7 @@ enum {
 };
 
 /* ---- element types ------------------------------------------------------------------- */
-enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2 };
+enum { PA_F32 = 0, PA_F16 = 1, PA_BF16 = 2, PA_E4M3 = 3 /* one-byte FP8 codes: pa_copy_blocks, pa_swap_blocks */ };
 
 /* ---- decode kernel choice (pa_decode_ex) ---------------------------------------------- */
 enum {
@@ -100,7 +100,9 @@ int pa_write_kv(const void* key, const void* value, void* key_cache, void* value
  * ids.  For every pair, block dst of key_cache and of value_cache becomes a
  * byte copy of block src (all kv heads, all slots).  The dst ids of one call
  * must be distinct and no dst may be a src of the same call (otherwise the
- * result depends on scheduling).  An id outside [0, num_blocks) skips the pair
+ * result depends on scheduling).  dtype gives the element size only (PA_E4M3 for
+ * FP8 caches); value_cache NULL: the interleaved FP8 layout, key_cache holding
+ * [num_blocks, H_kv, 2, block_size, head_dim] and the whole record copied.  An id outside [0, num_blocks) skips the pair
  * and sets PA_ERR_BAD_TABLE in the device error word.  num_pairs == 0 is a
  * no-op.
  */
@@ -142,7 +144,9 @@ int pa_apply_table_deltas(int32_t* block_tables, int num_rows, int max_blocks_pe
  * LLM-inference page's swap of KV blocks to CPU memory and back).  For every
  * (src, dst) row of block_pairs [num_pairs, 2] int64, block dst of dst_key_cache
  * and dst_value_cache becomes a byte copy of block src of src_key_cache and
- * src_value_cache (all kv heads, all slots; dtype gives only the element size).
+ * src_value_cache (all kv heads, all slots; dtype gives only the element size, PA_E4M3
+ * for FP8 caches).  dst_value_cache and src_value_cache both NULL: the interleaved FP8
+ * layout ([num_blocks, H_kv, 2, block_size, head_dim] records, each copied whole).
  *  - each cache and block_pairs may be device memory of the current device or
  *    page-locked host memory the device can address (cudaHostAlloc, cudaHostRegister,
  *    torch pin_memory); the kernel reads and writes host memory directly over

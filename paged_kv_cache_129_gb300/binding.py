@@ -25,6 +25,7 @@ STATUS_NAMES = {
 PA_F32, PA_F16, PA_BF16 = 0, 1, 2
 KERNELS = {"auto": 0, "mma": 1, "simt": 2}
 STATIC_SCRATCH_BYTES = 16 * 1024 * 1024  # PA_STATIC_SCRATCH_BYTES
+PA_E4M3 = 3  # one-byte FP8 codes (byte movers)
 _TORCH_DTYPES = {torch.float32: PA_F32, torch.float16: PA_F16, torch.bfloat16: PA_BF16}
 
 _lock = threading.Lock()
@@ -194,16 +195,32 @@ def write_kv(key: torch.Tensor, value: torch.Tensor, key_cache: torch.Tensor, va
                                  _dtype_code(key_cache), _stream_ptr(stream, key_cache.device)))
 
 
-def copy_blocks(key_cache: torch.Tensor, value_cache: torch.Tensor, src_dst_pairs: torch.Tensor, stream=None) -> None:
-    """``pa_copy_blocks``: for each (src, dst) row of ``src_dst_pairs`` (int64 [n, 2]) copy block src -> dst."""
-    for name, t in (("key_cache", key_cache), ("value_cache", value_cache), ("src_dst_pairs", src_dst_pairs)):
+def _block_geometry(key_cache: torch.Tensor, value_cache: Optional[torch.Tensor]):
+    """(num_blocks, H_kv, bs, d, element code) of a cache pair, or of one interleaved FP8 cache
+    ``[N, H_kv, 2, bs, d]`` when ``value_cache`` is None."""
+    if value_cache is None:
+        _need(key_cache.dim() == 5 and key_cache.shape[2] == 2, "one cache: interleaved FP8 [N, H_kv, 2, bs, d]")
+        n, h, _, bs, d = key_cache.shape
+    else:
+        _need(key_cache.dim() == 4 and value_cache.shape == key_cache.shape and value_cache.dtype == key_cache.dtype,
+              "caches must be [N, H_kv, bs, d] of one dtype")
+        n, h, bs, d = key_cache.shape
+    code = PA_E4M3 if key_cache.dtype in (torch.uint8, torch.float8_e4m3fn) else _dtype_code(key_cache)
+    return n, h, bs, d, code
+
+
+def copy_blocks(key_cache: torch.Tensor, value_cache: Optional[torch.Tensor], src_dst_pairs: torch.Tensor,
+                stream=None) -> None:
+    """``pa_copy_blocks``: for each (src, dst) row of ``src_dst_pairs`` (int64 [n, 2]) copy block src -> dst
+    (``value_cache`` None: one interleaved FP8 cache, whole records)."""
+    for name, t in (("key_cache", key_cache), ("src_dst_pairs", src_dst_pairs)) + (
+            (("value_cache", value_cache),) if value_cache is not None else ()):
         _cuda(t, name)
-    _need(key_cache.dim() == 4 and value_cache.shape == key_cache.shape, "caches must be [N, H_kv, bs, d]")
     _need(src_dst_pairs.dtype == torch.int64 and (src_dst_pairs.numel() % 2 == 0), "pairs: int64 [n, 2]")
-    num_blocks, hkv, bs, d = key_cache.shape
-    _check(library().pa_copy_blocks(key_cache.data_ptr(), value_cache.data_ptr(), src_dst_pairs.data_ptr(),
-                                    src_dst_pairs.numel() // 2, hkv, d, bs, num_blocks, _dtype_code(key_cache),
-                                    _stream_ptr(stream, key_cache.device)))
+    num_blocks, hkv, bs, d, code = _block_geometry(key_cache, value_cache)
+    _check(library().pa_copy_blocks(key_cache.data_ptr(), value_cache.data_ptr() if value_cache is not None else None,
+                                    src_dst_pairs.data_ptr(), src_dst_pairs.numel() // 2, hkv, d, bs, num_blocks,
+                                    code, _stream_ptr(stream, key_cache.device)))
 
 
 def write_kv_layers(keys, values, key_caches, value_caches, slot_mapping: torch.Tensor, stream=None) -> None:
@@ -248,30 +265,32 @@ def apply_table_deltas(block_tables: torch.Tensor, deltas: torch.Tensor, num_del
                                                deltas.data_ptr(), n, _stream_ptr(stream, block_tables.device)))
 
 
-def swap_blocks(dst_key_cache: torch.Tensor, dst_value_cache: torch.Tensor, src_key_cache: torch.Tensor,
-                src_value_cache: torch.Tensor, block_pairs: torch.Tensor, stream=None) -> None:
+def swap_blocks(dst_key_cache: torch.Tensor, dst_value_cache: Optional[torch.Tensor], src_key_cache: torch.Tensor,
+                src_value_cache: Optional[torch.Tensor], block_pairs: torch.Tensor, stream=None) -> None:
     """``pa_swap_blocks``: block dst of the dst caches <- block src of the src caches for every (src, dst)
     row of ``block_pairs`` (int64 [n, 2]).  Each tensor is a CUDA tensor or a pinned CPU tensor
     (``pin_memory()``); the copy runs on the current CUDA device's stream."""
-    tensors = (("dst_key_cache", dst_key_cache), ("dst_value_cache", dst_value_cache),
-               ("src_key_cache", src_key_cache), ("src_value_cache", src_value_cache), ("block_pairs", block_pairs))
+    _need((dst_value_cache is None) == (src_value_cache is None), "value caches: both or neither")
+    tensors = tuple((n, t) for n, t in (("dst_key_cache", dst_key_cache), ("dst_value_cache", dst_value_cache),
+                                        ("src_key_cache", src_key_cache), ("src_value_cache", src_value_cache),
+                                        ("block_pairs", block_pairs)) if t is not None)
     for name, t in tensors:
         _need(t.is_contiguous(), f"{name} must be contiguous")
         _need(t.is_cuda or t.is_pinned(), f"{name} must be a CUDA tensor or pinned host memory")
-    _need(dst_key_cache.dim() == 4 and dst_value_cache.shape == dst_key_cache.shape, "dst caches: [N, H_kv, bs, d]")
-    _need(src_key_cache.dim() == 4 and src_value_cache.shape == src_key_cache.shape, "src caches: [N, H_kv, bs, d]")
-    _need(src_key_cache.shape[1:] == dst_key_cache.shape[1:], "caches differ in block geometry")
-    _need(len({t.dtype for _, t in tensors[:4]}) == 1, "cache dtypes must match")
+    src_n, hkv, bs, d, code = _block_geometry(src_key_cache, src_value_cache)
+    dst_n, *dst_geo = _block_geometry(dst_key_cache, dst_value_cache)
+    _need(tuple(dst_geo) == (hkv, bs, d, code), "caches differ in block geometry or element type")
     _need(block_pairs.dtype == torch.int64 and block_pairs.numel() % 2 == 0, "block_pairs: int64 [n, 2]")
     cuda = [t.device for _, t in tensors if t.is_cuda]
     device = cuda[0] if cuda else torch.device("cuda", torch.cuda.current_device())
-    _, hkv, bs, d = src_key_cache.shape
+
+    def ptr(t):
+        return t.data_ptr() if t is not None else None
+
     with torch.cuda.device(device):
-        _check(library().pa_swap_blocks(dst_key_cache.data_ptr(), dst_value_cache.data_ptr(),
-                                        src_key_cache.data_ptr(), src_value_cache.data_ptr(), block_pairs.data_ptr(),
-                                        block_pairs.numel() // 2, hkv, d, bs, src_key_cache.shape[0],
-                                        dst_key_cache.shape[0], _dtype_code(src_key_cache),
-                                        _stream_ptr(stream, device)))
+        _check(library().pa_swap_blocks(ptr(dst_key_cache), ptr(dst_value_cache), ptr(src_key_cache),
+                                        ptr(src_value_cache), block_pairs.data_ptr(), block_pairs.numel() // 2, hkv,
+                                        d, bs, src_n, dst_n, code, _stream_ptr(stream, device)))
 
 
 def decode_plan(num_seqs: int, num_heads: int, num_kv_heads: int, head_dim: int, block_size: int,

@@ -84,7 +84,9 @@ namespace {
 // Internal element code of an FP8 (E4M3) cache, for the tensor-map cache (not a public dtype).
 constexpr int kCacheE4M3 = 16;
 
-int elem_bytes(int dtype) { return dtype == PA_F32 ? 4 : dtype == kCacheE4M3 ? 1 : 2; }
+int elem_bytes(int dtype) { return dtype == PA_F32 ? 4 : (dtype == kCacheE4M3 || dtype == PA_E4M3) ? 1 : 2; }
+// element types the byte movers (block copy, swap) accept
+bool bytes_dtype_ok(int dtype) { return dtype == PA_F32 || dtype == PA_F16 || dtype == PA_BF16 || dtype == PA_E4M3; }
 bool dtype_ok(int dtype) { return dtype == PA_F32 || dtype == PA_F16 || dtype == PA_BF16; }
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -449,11 +451,13 @@ int pa_copy_blocks(void* key_cache, void* value_cache, const int64_t* src_dst_pa
                    int head_dim, int block_size, int num_blocks, int dtype, void* stream) {
     CallRange nvtx_range("pa_copy_blocks");
     clear_error();
-    if (!dtype_ok(dtype)) return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: unknown dtype %d", dtype);
+    if (!bytes_dtype_ok(dtype)) return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: unknown dtype %d", dtype);
     if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
         return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: bad sizes");
     if (num_pairs == 0) return PA_OK;
-    if (!key_cache || !value_cache || !src_dst_pairs) return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: NULL pointer");
+    if (!key_cache || !src_dst_pairs) return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: NULL pointer");
+    // value_cache NULL: one cache of [N, H_kv, 2, bs, d] records (interleaved FP8), each copied whole
+    const bool single = value_cache == nullptr;
     if (!aligned(src_dst_pairs, 8)) return fail(PA_ERR_INVALID_ARG, "pa_copy_blocks: pairs must be 8-byte aligned");
     const int eb = elem_bytes(dtype);
     if (!aligned(key_cache, eb) || !aligned(value_cache, eb))
@@ -461,7 +465,8 @@ int pa_copy_blocks(void* key_cache, void* value_cache, const int64_t* src_dst_pa
     DeviceState* dev = nullptr;
     int st = current_device_state(&dev);
     if (st != PA_OK) return st;
-    CopyArgs a{key_cache, value_cache, src_dst_pairs, num_pairs, num_kv_heads, head_dim, block_size, num_blocks, eb,
+    CopyArgs a{key_cache, single ? key_cache : value_cache, src_dst_pairs, num_pairs,
+               single ? 2 * num_kv_heads : num_kv_heads, head_dim, block_size, num_blocks, eb, single ? 1 : 0,
                dev->error_word};
     cudaError_t e = copy_blocks_launch(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "pa_copy_blocks launch");
@@ -578,13 +583,15 @@ int pa_swap_blocks(void* dst_key_cache, void* dst_value_cache, const void* src_k
                    int src_num_blocks, int dst_num_blocks, int dtype, void* stream) {
     CallRange nvtx_range("pa_swap_blocks");
     clear_error();
-    if (!dtype_ok(dtype)) return fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: unknown dtype %d", dtype);
+    if (!bytes_dtype_ok(dtype)) return fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: unknown dtype %d", dtype);
     if (num_pairs < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || src_num_blocks < 0 ||
         dst_num_blocks < 0)
         return fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: bad sizes");
     if (num_pairs == 0) return PA_OK;
-    if (!dst_key_cache || !dst_value_cache || !src_key_cache || !src_value_cache || !block_pairs)
-        return fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: NULL pointer");
+    if (!dst_key_cache || !src_key_cache || !block_pairs || (!dst_value_cache != !src_value_cache))
+        return fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: NULL pointer (value caches: both or neither)");
+    // both value caches NULL: [N, H_kv, 2, bs, d] records (interleaved FP8), each copied whole
+    const bool single = dst_value_cache == nullptr;
     if (!aligned(block_pairs, 8)) return fail(PA_ERR_INVALID_ARG, "pa_swap_blocks: pairs must be 8-byte aligned");
     const int eb = elem_bytes(dtype);
     if (!aligned(dst_key_cache, eb) || !aligned(dst_value_cache, eb) || !aligned(src_key_cache, eb) ||
@@ -599,16 +606,21 @@ int pa_swap_blocks(void* dst_key_cache, void* dst_value_cache, const void* src_k
     const void* sv = nullptr;
     const void* pr = nullptr;
     int st = device_address(dst_key_cache, device, "dst_key_cache", &dk);
-    if (st == PA_OK) st = device_address(dst_value_cache, device, "dst_value_cache", &dv);
+    if (st == PA_OK && !single) st = device_address(dst_value_cache, device, "dst_value_cache", &dv);
     if (st == PA_OK) st = device_address(src_key_cache, device, "src_key_cache", &sk);
-    if (st == PA_OK) st = device_address(src_value_cache, device, "src_value_cache", &sv);
+    if (st == PA_OK && !single) st = device_address(src_value_cache, device, "src_value_cache", &sv);
+    if (single) {
+        dv = dk;
+        sv = sk;
+    }
     if (st == PA_OK) st = device_address(block_pairs, device, "block_pairs", &pr);
     if (st != PA_OK) return st;
     DeviceState* dev = nullptr;
     st = current_device_state(&dev);
     if (st != PA_OK) return st;
     SwapArgs a{const_cast<void*>(dk), const_cast<void*>(dv), sk, sv, static_cast<const int64_t*>(pr), num_pairs,
-               num_kv_heads, head_dim, block_size, src_num_blocks, dst_num_blocks, eb, dev->num_sms, dev->error_word};
+               single ? 2 * num_kv_heads : num_kv_heads, head_dim, block_size, src_num_blocks, dst_num_blocks, eb,
+               dev->num_sms, single ? 1 : 0, dev->error_word};
     e = swap_blocks_launch(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "pa_swap_blocks launch");
     return PA_OK;

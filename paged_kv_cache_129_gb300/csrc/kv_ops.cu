@@ -181,14 +181,15 @@ template <typename V>
 __global__ void __launch_bounds__(kSwapThreads) swap_blocks_kernel(V* dst_key, V* dst_value, const V* src_key,
                                                                    const V* src_value, const int64_t* pairs,
                                                                    long long block_vecs, int chunks, long long units,
-                                                                   int src_blocks, int dst_blocks, unsigned* err) {
+                                                                   int src_blocks, int dst_blocks, int caches,
+                                                                   unsigned* err) {
     griddep_wait();
     griddep_launch_dependents();
     for (long long u0 = blockIdx.x; u0 < units; u0 += gridDim.x) {
         const int chunk = (int)(u0 % chunks);
         const long long pc = u0 / chunks;
-        const int cache = (int)(pc & 1);
-        const long long pidx = pc >> 1;
+        const int cache = (int)(pc % caches);  // caches: 2 (K, V) or 1 (one cache)
+        const long long pidx = pc / caches;
         // the pairs may live in host memory: plain loads
         const long long src = pairs[2 * pidx];
         const long long dst = pairs[2 * pidx + 1];
@@ -245,7 +246,7 @@ cudaError_t copy_typed(const CopyArgs& a, long long block_bytes, cudaStream_t st
     const int threads = 256;
     long long chunks = (block_vecs + threads * 4 - 1) / (threads * 4);
     if (chunks > 65535) chunks = 65535;
-    dim3 grid((unsigned)a.num_pairs, 2, (unsigned)chunks);
+    dim3 grid((unsigned)a.num_pairs, a.single ? 1u : 2u, (unsigned)chunks);
     return launch_pdl(copy_blocks_kernel<V>, grid, dim3(threads), 0, stream, static_cast<V*>(a.key_cache),
                       static_cast<V*>(a.value_cache), a.pairs, block_vecs, a.num_blocks, a.err);
 }
@@ -256,12 +257,13 @@ cudaError_t swap_typed(const SwapArgs& a, long long block_bytes, cudaStream_t st
     const long long per_cta = (long long)kSwapThreads * kSwapUnroll;
     const long long chunks = (block_vecs + per_cta - 1) / per_cta;
     if (chunks > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
-    const long long units = (long long)a.num_pairs * 2 * chunks;
+    const int caches = a.single ? 1 : 2;
+    const long long units = (long long)a.num_pairs * caches * chunks;
     const long long grid = std::min<long long>(units, (long long)kSwapCtasPerSm * std::max(a.num_sms, 1));
     return launch_pdl(swap_blocks_kernel<V>, dim3((unsigned)grid), dim3(kSwapThreads), 0, stream,
                       static_cast<V*>(a.dst_key), static_cast<V*>(a.dst_value), static_cast<const V*>(a.src_key),
                       static_cast<const V*>(a.src_value), a.pairs, block_vecs, (int)chunks, units, a.src_num_blocks,
-                      a.dst_num_blocks, a.err);
+                      a.dst_num_blocks, caches, a.err);
 }
 
 template <typename V>

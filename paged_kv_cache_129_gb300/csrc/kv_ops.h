@@ -21,6 +21,7 @@ struct CopyArgs {
     void* value_cache;
     const int64_t* pairs;
     int num_pairs, num_kv_heads, head_dim, block_size, num_blocks, elem_bytes;
+    int single;  // 1: one cache (key_cache), its blocks copied whole
     unsigned* err;
 };
 
@@ -32,6 +33,7 @@ struct SwapArgs {
     const int64_t* pairs;  // device addresses (host memory through its device mapping)
     int num_pairs, num_kv_heads, head_dim, block_size, src_num_blocks, dst_num_blocks, elem_bytes;
     int num_sms;  // the grid is capped at a few CTAs per SM
+    int single;   // 1: one cache per side (dst_key, src_key), its blocks copied whole
     unsigned* err;
 };
 

@@ -249,3 +249,42 @@ def test_interleaved_layout_matches_separate_caches(bs):
     ref = oracle.decode_fp8(q, "bf16", kc, vc, ks, vs, bt, lens, 1 / np.sqrt(d))
     assert_decode_close(to_f64(inter), ref, "bf16")
     pa.check_error()
+
+
+@pytest.mark.parametrize("layout", ["separate", "interleaved"])
+def test_fp8_copy_and_swap_bit_exact(layout):
+    """Copy-on-write block copies and swaps of FP8 caches (one-byte elements; the interleaved layout copies
+    each [H_kv, 2, bs, d] record whole) equal the oracle's byte copies."""
+    rng = np.random.default_rng(31)
+    nb, hkv, bs, d = 12, 4, 16, 128
+    shape = (nb, hkv, 2, bs, d) if layout == "interleaved" else (nb, hkv, bs, d)
+    kc = rng.integers(0, 256, shape, dtype=np.uint8)
+    vc = None if layout == "interleaved" else rng.integers(0, 256, shape, dtype=np.uint8)
+    pairs = np.array([[1, 7], [3, 9], [0, 11]], np.int64)
+    dk = torch.from_numpy(kc).cuda()
+    dv = torch.from_numpy(vc).cuda() if vc is not None else None
+    pa.copy_blocks(dk, dv, torch.from_numpy(pairs).cuda())
+    exp_k = kc.copy()
+    exp_v = vc.copy() if vc is not None else exp_k
+    assert oracle.copy_blocks(exp_k, exp_v, pairs) == oracle.OK
+    torch.cuda.synchronize()
+    assert np.array_equal(dk.cpu().numpy(), exp_k)
+    if vc is not None:
+        assert np.array_equal(dv.cpu().numpy(), exp_v)
+    # swap out to page-locked host memory and back into other blocks
+    hk = torch.zeros((5,) + shape[1:], dtype=torch.uint8).pin_memory()
+    hv = torch.zeros_like(hk).pin_memory() if vc is not None else None
+    out_pairs = np.array([[7, 0], [9, 3], [2, 4]], np.int64)
+    pa.swap_blocks(hk, hv, dk, dv, torch.from_numpy(out_pairs).cuda())
+    in_pairs = np.array([[0, 5], [3, 6], [4, 8]], np.int64)
+    in_host = torch.from_numpy(in_pairs).pin_memory()
+    pa.swap_blocks(dk, dv, hk, hv, in_host)
+    torch.cuda.synchronize()
+    h_exp_k = np.zeros((5,) + shape[1:], np.uint8)
+    h_exp_v = np.zeros_like(h_exp_k) if vc is not None else h_exp_k
+    assert oracle.swap_blocks(h_exp_k, h_exp_v, exp_k, exp_v, out_pairs) == oracle.OK
+    assert oracle.swap_blocks(exp_k, exp_v, h_exp_k, h_exp_v, in_pairs) == oracle.OK
+    assert np.array_equal(hk.numpy(), h_exp_k) and np.array_equal(dk.cpu().numpy(), exp_k)
+    if vc is not None:
+        assert np.array_equal(hv.numpy(), h_exp_v) and np.array_equal(dv.cpu().numpy(), exp_v)
+    pa.check_error()

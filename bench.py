@@ -1235,8 +1235,24 @@ def run_reference(args, rank: int, world: int) -> None:
                         inp.new_value.reshape(-1, inp.num_kv_heads, inp.head_dim), inp.key_cache, inp.value_cache,
                         slots)
 
+    fp8 = None
+    if args.workload.endswith("_fp8"):
+        # the oracle's own quantised pool (every slot through its writer), as the GPU arm's
+        from paged_kv_cache_129_gb300 import workloads as wl
+
+        nb_, hkv_, bs_, d_ = inp.key_cache.shape
+        ks_, vs_ = wl.fp8_scales(inp.key_cache, inp.dtype), wl.fp8_scales(inp.value_cache, inp.dtype)
+        kq, vq = np.zeros(inp.key_cache.shape, np.uint8), np.zeros(inp.key_cache.shape, np.uint8)
+        oracle.write_kv_fp8(np.ascontiguousarray(inp.key_cache.transpose(0, 2, 1, 3).reshape(nb_ * bs_, hkv_, d_)),
+                            np.ascontiguousarray(inp.value_cache.transpose(0, 2, 1, 3).reshape(nb_ * bs_, hkv_, d_)),
+                            inp.dtype, kq, vq, ks_, vs_, np.arange(nb_ * bs_, dtype=np.int64))
+        fp8 = (kq, vq, ks_, vs_)
+
     def one_row(h):
-        if q_len == 1:
+        if fp8 is not None:
+            oracle.decode_fp8(inp.q, inp.dtype, fp8[0], fp8[1], fp8[2], fp8[3], inp.block_tables, inp.context_lens,
+                              inp.scale, rows=[(0, h)])
+        elif q_len == 1:
             oracle.decode_inputs(inp, rows=[(0, h)])
         else:  # one head, every query token
             oracle.decode_multi(inp.q, inp.key_cache, inp.value_cache, inp.block_tables, inp.context_lens, inp.dtype,
@@ -1252,8 +1268,10 @@ def run_reference(args, rank: int, world: int) -> None:
     rows_per_step = int(max(1, min(inp.num_heads, 120.0 * threads / n_steps / t_row)))
     L0 = int(inp.context_lens[0])
     eb = inp.elem_bytes
-    bytes_per_step = rows_per_step / inp.num_heads * decode_bytes([L0], inp.num_heads, inp.num_kv_heads,
-                                                                  inp.head_dim, eb, inp.block_size, q_len)
+    seq_bytes = (decode_bytes_fp8([L0], inp.num_heads, inp.num_kv_heads, inp.head_dim, eb, inp.block_size)
+                 if fp8 is not None else
+                 decode_bytes([L0], inp.num_heads, inp.num_kv_heads, inp.head_dim, eb, inp.block_size, q_len))
+    bytes_per_step = rows_per_step / inp.num_heads * seq_bytes
     used = min(threads, rows_per_step)
     with ThreadPoolExecutor(max_workers=used) as ex:
         def one_step():
@@ -1267,7 +1285,7 @@ def run_reference(args, rank: int, world: int) -> None:
         dt = time.perf_counter() - t0
     value = bytes_per_step * args.steps / dt / 1e9
     sample = (f"sequence 0 (L={L0}), {rows_per_step} of {inp.num_heads} heads per step, one head per task, "
-              f"fp64 C oracle on {used} threads")
+              f"fp64 C oracle{' over its own E4M3 pool' if fp8 is not None else ''} on {used} threads")
     line = {"impl": "reference", "metric": METRIC, "value": round(value, 5), "unit": UNIT, "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(dt * 1e3 / args.steps, 4),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAMES[inp.dtype],

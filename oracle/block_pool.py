@@ -187,6 +187,20 @@ class SequencePool:
         self.release(sid)
         return new_sid, list(zip(table, new_table))
 
+    def blocks_needed(self, seq_ids: Sequence[int], counts: Sequence[int]) -> int:
+        """Reservation check (the vLLM/PagedAttention page's continuous batching: an iteration may admit
+        only the growth the pool can hold): the free blocks that appending counts[i] tokens to seq_ids[i], in
+        order, would take -- by doing it on a copy of the pool and counting."""
+        import copy
+
+        trial = copy.deepcopy(self)
+        before = len(trial.pool.free)
+        trial.pool.free = trial.pool.free + [-1 - i for i in range(sum(counts) + 1)]  # never runs out
+        for sid, n in zip(seq_ids, counts):
+            for _ in range(n):
+                trial.append(sid)
+        return before + sum(counts) + 1 - len(trial.pool.free)
+
     def num_free(self) -> int:
         return len(self.pool.free)
 

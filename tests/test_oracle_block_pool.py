@@ -145,3 +145,50 @@ def test_random_operations_keep_invariants():
             sid = live.pop(rng.integers(len(live)))
             pool.release(sid)
         assert pool.invariants() == [], step
+
+
+def test_blocks_needed_hand_cases():
+    pool = SequencePool(20, 4)
+    a = pool.create()
+    for t in range(4):  # a full tail
+        pool.append(a, t)
+    assert pool.blocks_needed([a], [1]) == 1 and pool.blocks_needed([a], [4]) == 1
+    assert pool.blocks_needed([a], [5]) == 2
+    b = pool.create()
+    assert pool.blocks_needed([b], [0]) == 0 and pool.blocks_needed([b], [5]) == 2  # empty: fresh blocks
+    c = pool.create()
+    for t in range(6):  # one full block + a partial tail of 2
+        pool.append(c, t)
+    d = pool.fork(c)
+    # both holders of the shared partial tail append: the first copies, the second then holds it alone
+    assert pool.blocks_needed([c, d], [1, 1]) == 1
+    assert pool.blocks_needed([c], [1]) == 1 and pool.blocks_needed([c], [3]) == 2
+    free = pool.num_free()
+    assert pool.blocks_needed([c, d, a], [2, 3, 1]) == 3
+    assert pool.num_free() == free  # nothing changed
+
+
+def test_blocks_needed_equals_the_blocks_the_appends_take():
+    rng = np.random.default_rng(5)
+    pool = SequencePool(400, 4)
+    live = [pool.create()]
+    for step in range(300):
+        op = rng.integers(0, 6)
+        if op == 0:
+            live.append(pool.create())
+        elif op == 1:
+            live.append(pool.fork(live[rng.integers(len(live))]))
+        elif op == 2 and len(live) > 1:
+            pool.release(live.pop(rng.integers(len(live))))
+        else:
+            ids = [live[i] for i in rng.integers(0, len(live), 4)]
+            counts = [int(x) for x in rng.integers(0, 7, 4)]
+            need = pool.blocks_needed(ids, counts)
+            if need > pool.num_free():
+                continue
+            free = pool.num_free()
+            for sid, n in zip(ids, counts):
+                for _ in range(n):
+                    pool.append(sid)
+            assert free - pool.num_free() == need
+            assert pool.invariants() == []

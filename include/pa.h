@@ -450,6 +450,18 @@ int pa_seq_fork(pa_pool* pool, int64_t parent_id, int64_t* child_id);
 int pa_seq_release(pa_pool* pool, int64_t seq_id);
 int pa_seq_length(const pa_pool* pool, int64_t seq_id, int64_t* length);
 /*
+ * pa_pool_blocks_needed — the reservation check of an iteration-level scheduler (the
+ * vLLM and PagedAttention page, continuous batching: before an iteration, the blocks the
+ * admitted sequences may grow into must be available): *needed receives the number of
+ * free blocks that appending counts[i] tokens to seq_ids[i], for i = 0 .. n-1 in that
+ * order, would take — fresh blocks past full tails and copy-on-write copies of shared
+ * partial tails, exactly as pa_seq_append would, including a shared tail whose other
+ * holders copied away first.  Nothing changes; the appends fit iff *needed <=
+ * pa_pool_num_free().  A sequence may appear more than once.
+ */
+int pa_pool_blocks_needed(const pa_pool* pool, const int64_t* seq_ids, const int32_t* counts, int n,
+                          int64_t* needed);
+/*
  * pa_seq_swap — move sequence seq_id from pool src to pool dst (preemption: the
  * vLLM and PagedAttention page lets a request's physical blocks be released or
  * migrated while its logical tokens are kept; the LLM-inference page swaps a

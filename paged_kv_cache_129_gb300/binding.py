@@ -106,6 +106,7 @@ _SIGNATURES = [
     ("pa_seq_fork", _I, [_P, _I64, ctypes.POINTER(_I64)]),
     ("pa_seq_release", _I, [_P, _I64]),
     ("pa_seq_length", _I, [_P, _I64, ctypes.POINTER(_I64)]),
+    ("pa_pool_blocks_needed", _I, [_P, _P, _P, _I, ctypes.POINTER(_I64)]),
     ("pa_seq_swap", _I, [_P, _P, _I64, ctypes.POINTER(_I64), _P, _I, ctypes.POINTER(_I)]),
     ("pa_pool_block_tables", _I, [_P, _P, _I, _P, _I, _P]),
     ("pa_pool_table_deltas", _I, [_P, _P, _I, _P, _I, ctypes.POINTER(_I), _P]),
@@ -602,6 +603,19 @@ class BlockPool:
 
     def release(self, seq_id: int) -> None:
         _check(self._lib.pa_seq_release(self._h, seq_id))
+
+    def blocks_needed(self, seq_ids, counts) -> int:
+        """Free blocks that appending counts[i] tokens to seq_ids[i] (in order) would take
+        (``pa_pool_blocks_needed``; nothing changes)."""
+        import numpy as np
+
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        cnt = np.ascontiguousarray(counts, dtype=np.int32)
+        assert ids.shape == cnt.shape
+        out = _I64()
+        _check(self._lib.pa_pool_blocks_needed(self._h, ids.ctypes.data, cnt.ctypes.data, ids.size,
+                                               ctypes.byref(out)))
+        return out.value
 
     def swap_to(self, dst: "BlockPool", seq_id: int):
         """Move a sequence into pool ``dst``: returns (its id there, int64 [n, 2] numpy (src block, dst block)

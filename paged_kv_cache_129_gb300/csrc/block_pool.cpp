@@ -287,6 +287,52 @@ int pa_seq_swap(pa_pool* src, pa_pool* dst, int64_t seq_id, int64_t* new_seq_id,
     return PA_OK;
 }
 
+int pa_pool_blocks_needed(const pa_pool* pool, const int64_t* seq_ids, const int32_t* counts, int n,
+                          int64_t* needed) {
+    if (!pool || !needed || n < 0 || (n > 0 && (!seq_ids || !counts)))
+        return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_blocks_needed: bad arguments");
+    // Dry run of the appends, in order, on overlays of the touched state (nothing changes).
+    struct Tail {
+        int32_t block;  // the tail block (>= 0 real, < 0 a block taken in the dry run)
+        int32_t fill;
+    };
+    std::unordered_map<int64_t, Tail> tails;       // sequence -> its tail after the dry-run appends so far
+    std::unordered_map<int32_t, int32_t> refs_of;  // real block -> reference count after the dry run
+    int64_t taken = 0;
+    for (int i = 0; i < n; ++i) {
+        if (counts[i] < 0) return pa::fail(PA_ERR_INVALID_ARG, "pa_pool_blocks_needed: negative count");
+        auto it = pool->seqs.find(seq_ids[i]);
+        if (it == pool->seqs.end())
+            return pa::fail(PA_ERR_NOT_FOUND, "pa_pool_blocks_needed: unknown sequence %lld",
+                            (long long)seq_ids[i]);
+        auto t = tails.find(seq_ids[i]);
+        if (t == tails.end()) {
+            const auto& tab = it->second.table;
+            Tail cur{-1, pool->block_size};  // an empty table behaves as a full tail
+            if (!tab.empty()) cur = Tail{tab.back(), pool->fill[tab.back()]};
+            t = tails.emplace(seq_ids[i], cur).first;
+        }
+        for (int32_t k = 0; k < counts[i]; ++k) {
+            Tail& tl = t->second;
+            if (tl.fill == pool->block_size) {
+                tl = Tail{(int32_t)(-1 - taken), 0};  // a fresh block
+                ++taken;
+            } else if (tl.block >= 0) {
+                auto r = refs_of.find(tl.block);
+                int32_t& refs = r == refs_of.end() ? (refs_of[tl.block] = pool->refs[tl.block]) : r->second;
+                if (refs > 1) {  // copy-on-write: this sequence leaves the shared tail
+                    refs -= 1;
+                    tl = Tail{(int32_t)(-1 - taken), tl.fill};
+                    ++taken;
+                }
+            }
+            tl.fill += 1;
+        }
+    }
+    *needed = taken;
+    return PA_OK;
+}
+
 int pa_seq_length(const pa_pool* pool, int64_t seq_id, int64_t* length) {
     if (!pool || !length) return pa::fail(PA_ERR_INVALID_ARG, "pa_seq_length: NULL argument");
     const pa_pool::Seq* s = find_seq(pool, seq_id);

@@ -454,3 +454,35 @@ def test_pool_load_refuses_bad_images(lib):
     corrupt[8 * 4 + 8] ^= 0x01  # the first free-list entry
     with pytest.raises(pa.PAError):
         pa.BlockPool.load(bytes(corrupt))
+
+
+def test_pool_blocks_needed_matches_allocator_model(lib):
+    rng = np.random.default_rng(13)
+    nb, bs = 300, 4
+    order = rng.permutation(nb)
+    pool = pa.BlockPool(nb, bs, free_order=order)
+    model = SequencePool(nb, bs, free_order=order)
+    live = [(pool.create(), model.create())]
+    for step in range(400):
+        op = rng.integers(0, 6)
+        if op == 0:
+            live.append((pool.create(), model.create()))
+        elif op == 1:
+            c, m = live[rng.integers(len(live))]
+            live.append((pool.fork(c), model.fork(m)))
+        elif op == 2 and len(live) > 1:
+            c, m = live.pop(rng.integers(len(live)))
+            pool.release(c)
+            model.release(m)
+        else:
+            k = rng.integers(0, len(live), 5)
+            counts = [int(x) for x in rng.integers(0, 9, 5)]
+            need = pool.blocks_needed([live[i][0] for i in k], counts)
+            assert need == model.blocks_needed([live[i][1] for i in k], counts)
+            if need <= pool.num_free():
+                for i, n in zip(k, counts):
+                    for _ in range(n):
+                        pool.append(live[i][0])
+                        model.append(live[i][1])
+    with pytest.raises(pa.PAError):
+        pool.blocks_needed([123456], [1])

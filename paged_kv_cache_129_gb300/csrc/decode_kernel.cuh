@@ -57,6 +57,10 @@
 #ifndef PA_LEAN_F8_MIN_BLOCKS
 #define PA_LEAN_F8_MIN_BLOCKS 3
 #endif
+// Prefetch the context lengths and block tables into L2 before the lean kernel's dependency wait.
+#ifndef PA_LEAN_L2_PREFETCH
+#define PA_LEAN_L2_PREFETCH 1
+#endif
 // Idle nap of the lean producer lane between polls of its warps' slots (ns): every poll takes
 // issue slots from the consumers that share its SM sub-partition.
 #ifndef PA_PRODUCER_NAP_NS
@@ -1291,6 +1295,20 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
     const int l_cap = a.max_blocks * BS;
     T* out = static_cast<T*>(a.out);
 
+#if PA_LEAN_L2_PREFETCH
+    // While the previous grid drains: warm L2 with the context lengths and this CTA's share of
+    // the block tables (prefetches return no data, so a value the previous grid is still writing
+    // is read only after the wait, coherently, from L2).
+    {
+        const char* lens = reinterpret_cast<const char*>(a.context_lens);
+        for (int off = tid * 128; off < B * 4; off += C::kThreads * 128) prefetch_l2(lens + off);
+        const long long tab_bytes = (long long)B * a.max_blocks * 4;
+        const long long share = (tab_bytes + gridDim.x - 1) / gridDim.x;
+        const char* tab = reinterpret_cast<const char*>(a.block_tables) + share * blockIdx.x;
+        for (long long off = tid * 128; off < share && share * blockIdx.x + off < tab_bytes; off += C::kThreads * 128)
+            prefetch_l2(tab + off);
+    }
+#endif
     // Wait for the previous grid in the stream, then let the merge kernel get scheduled as
     // early as possible; it reads nothing this kernel writes before its own wait.
     griddep_wait();

@@ -151,6 +151,11 @@ __device__ __forceinline__ unsigned long long ld_acquire_gpu(const unsigned long
 // that its CTAs can become resident while the previous grid in the stream drains.  Each
 // kernel calls griddep_wait() before it touches global memory: that returns once the
 // previous grid has completed and its writes are visible (at once when there is none).
+// Bring the 128-byte line holding p into L2 (no data returned to the thread).
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 __device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 
 // Let the next grid in the stream start launching (it still waits for this grid's

@@ -486,3 +486,26 @@ def test_pool_blocks_needed_matches_allocator_model(lib):
                         model.append(live[i][1])
     with pytest.raises(pa.PAError):
         pool.blocks_needed([123456], [1])
+
+
+def test_fp8_entry_points_reject_bad_arguments(lib):
+    f = float(1 / 128 ** 0.5)
+    # pa_write_kv_fp8: unknown source dtype, head_dim not a multiple of 4, NULL scales; no tokens is a no-op
+    assert lib.pa_write_kv_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 128, 16, 8, 7, None) == 1
+    assert lib.pa_write_kv_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 4, 2, 126, 16, 8, 2, None) == 1
+    assert lib.pa_write_kv_fp8(FAKE, FAKE, FAKE, FAKE, None, FAKE, FAKE, 4, 2, 128, 16, 8, 2, None) == 1
+    assert lib.pa_write_kv_fp8(FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 0, 2, 128, 16, 8, 2, None) == 0
+    # pa_decode_fp8: NULL scales, misaligned query, f32 queries (no FP8 kernel for them)
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 128, 16, 4, 10, f, 2, FAKE, 1 << 20, None]
+    bad = list(args)
+    bad[4] = None
+    assert lib.pa_decode_fp8(*bad) == 1
+    bad = list(args)
+    bad[1] = FAKE + 4
+    assert lib.pa_decode_fp8(*bad) == 1
+    bad = list(args)
+    bad[16] = 0  # PA_F32
+    assert lib.pa_decode_fp8(*bad) == 2
+    zero = list(args)
+    zero[8] = 0  # no sequences
+    assert lib.pa_decode_fp8(*zero) == 0

@@ -67,7 +67,8 @@ WORKLOAD_DESCRIPTIONS = {
     "qwen_gqa_fp8": "the Qwen-style GQA layer with an FP8 (E4M3) KV cache: batch 64, 28 q / 4 kv heads, head_dim 128, "
                     "bf16 queries, block_size 16, context_lens uniform in [512,4096], pool 20000 blocks shuffled; "
                     "q/K/V ~ N(0,1) in bf16, K/V quantised with one scale per (block, kv head) = block max / 448; "
-                    "one new token per sequence quantised into its slot (pa_write_kv_fp8) before the decode",
+                    "one new token per sequence quantised into the slot of position L - 1 inside the decode "
+                    "(pa_decode_fp8_append)",
     "long_context_fp8": "long-context split-KV with an FP8 (E4M3) KV cache: batch 8, 32 q / 8 kv heads, head_dim 128, "
                         "bf16 queries, block_size 16, context_lens uniform in [32768,131072]; scales per (block, kv "
                         "head) = block max / 448",
@@ -570,9 +571,10 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     code = {"f32": 0, "f16": 1, "bf16": 2}[inp.dtype]
     kern = pa.KERNELS[args.kernel]
 
-    fused = has_write and args.step == "append" and q_len == 1 and not args.workload.endswith("_fp8")
+    fused = has_write and args.step == "append" and q_len == 1
     if fused:
-        # pa_decode_append writes at the slot of position L - 1: the pool handed out exactly those
+        # pa_decode_append / pa_decode_fp8_append write at the slot of position L - 1: the pool handed
+        # out exactly those
         live = lens >= 1
         derived = tables[np.arange(B), (lens - 1) // bs].astype(np.int64) * bs + (lens - 1) % bs
         assert np.array_equal(np.asarray(slots)[live], derived[live])
@@ -605,6 +607,13 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
                   bt.data_ptr(), dl.data_ptr(), B, Hq, Hkv, d, bs, tables.shape[1], inp.num_blocks, float(inp.scale),
                   code, ws.data_ptr(), ws.numel(), max_ctx, args.partition_pages, kern, sptr]
                  for r in range(replicas)] if fused else None)
+    append_fn = lib.pa_decode_append
+    if fused and fp8:
+        append_fn = lib.pa_decode_fp8_append
+        app_args = [[out.data_ptr(), q.data_ptr(), nk.data_ptr(), nv.data_ptr(), kcs[r].data_ptr(), ptr(vcs[r]),
+                     ksd.data_ptr(), vsd.data_ptr(), bt.data_ptr(), dl.data_ptr(), B, Hq, Hkv, d, bs, tables.shape[1],
+                     inp.num_blocks, float(inp.scale), code, ws.data_ptr(), ws.numel(), sptr]
+                    for r in range(replicas)]
     # the decode kernel, plus the merge kernel (always for the lean schedule, when split for
     # the grid one), plus the write kernel when it is a call of its own
     merge_launches = 1 if (plan.schedule == 1 or plan.max_parts > 1) else 0
@@ -613,7 +622,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     def step(i):
         r = i % replicas
         if fused:
-            if lib.pa_decode_append(*app_args[r]) != 0:
+            if append_fn(*app_args[r]) != 0:
                 raise RuntimeError(lib.pa_last_error_string().decode())
             return
         if has_write and write_fn(*wr_args[r]) != 0:
@@ -622,8 +631,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
             raise RuntimeError(lib.pa_last_error_string().decode())
 
     def decode_call(i):
-        # the step's decode call: pa_decode_append (rewriting the same rows), pa_decode_ex or pa_decode_multi
-        status = lib.pa_decode_append(*app_args[i % replicas]) if fused else decode_fn(*dec_args[i % replicas])
+        # the step's decode call: pa_decode_append / pa_decode_fp8_append (rewriting the same rows),
+        # pa_decode_ex, pa_decode_multi or pa_decode_fp8
+        status = append_fn(*app_args[i % replicas]) if fused else decode_fn(*dec_args[i % replicas])
         if status != 0:
             raise RuntimeError(lib.pa_last_error_string().decode())
 
@@ -678,7 +688,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         step_append = fused or (fp8 and has_write)
         if fp8:
             stepper = pa.DecodeStepper(kcs[0], vcs[0], B, Hq, tables.shape[1], scale=inp.scale, append=step_append,
-                                       tables="deltas", k_scale=ksd, v_scale=vsd, query_dtype=tdtype)
+                                       tables="deltas", k_scale=ksd, v_scale=vsd, query_dtype=tdtype,
+                                       fp8_write="fused" if fused else "separate")
         else:
             stepper = pa.DecodeStepper(kcs[0], vcs[0], B, Hq, tables.shape[1], scale=inp.scale, append=fused,
                                        max_context_len=max_ctx, partition_pages=args.partition_pages,
@@ -703,7 +714,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
             if step_append:
                 fill(v.new_key, inp.new_key)
                 fill(v.new_value, inp.new_value)
-            if fp8 and step_append:
+            if fp8 and step_append and not fused:
                 v.slots.copy_(torch.from_numpy(np.asarray(slots, dtype=np.int64)))
 
         def e2e_run(n, first=False):
@@ -739,9 +750,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         e2e = {"value": round(e_bytes / (e_ms / 1e3) / 1e9, 2), "unit": UNIT, "steps": Ke,
                "ms_per_step": round(e_ms / Ke, 5), "h2d_bytes_per_step": int(stepper.h2d_bytes),
                "d2h_bytes_per_step": int(stepper.d2h_bytes),
-               "note": f"pa.DecodeStepper ({'pa_decode_append' if fused else 'pa_write_kv_fp8 + pa_decode_fp8' if fp8 and step_append else 'pa_decode_fp8' if fp8 else 'pa_decode'}, tables kept on the "
+               "note": f"pa.DecodeStepper ({'pa_decode_fp8_append' if fused and fp8 else 'pa_decode_append' if fused else 'pa_write_kv_fp8 + pa_decode_fp8' if fp8 and step_append else 'pa_decode_fp8' if fp8 else 'pa_decode'}, tables kept on the "
                        "device by deltas): every step one upload of the packed inputs (queries" +
-                       (", new K/V" if step_append else "") + (", slots" if fp8 and step_append else "") +
+                       (", new K/V" if step_append else "") + (", slots" if fp8 and step_append and not fused else "") +
                        f", lengths, {churn} block-table deltas) from pinned host "
                        "memory, pa_apply_table_deltas and the decode on the compute stream, one download of the "
                        "output, inside the timed region; two slots, the next upload overlapping the current decode"}
@@ -758,7 +769,8 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     achieved = call_bytes / (dec_avg_ms / 1e3) / 1e9
     roofline = {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "frac": round(achieved / peak, 4), "traffic": stored_traffic(args.workload),
-                "kernel": (("pa_decode_append" if fused else "pa_decode_multi" if q_len > 1 else
+                "kernel": (("pa_decode_fp8_append" if fused and fp8 else "pa_decode_append" if fused else
+                            "pa_decode_multi" if q_len > 1 else
                             "pa_decode_fp8" if fp8 else "pa_decode") +
                            " call (" +
                            ("paged_decode_lean_kernel + lean_merge_kernel)" if plan.schedule == 1 else
@@ -804,7 +816,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": DTYPE_NAMES[inp.dtype], "data": "synthetic",
         "config": {"workload": WORKLOAD_DESCRIPTIONS[args.workload], "name": args.workload,
-                   "step": ("pa_decode_append (new token per sequence written at L - 1, then decode)" if fused
+                   "step": ("pa_decode_fp8_append (new token per sequence quantised at L - 1, then decode)"
+                            if fused and fp8
+                            else "pa_decode_append (new token per sequence written at L - 1, then decode)" if fused
                             else "pa_write_kv_fp8 (new token per sequence) + pa_decode_fp8" if fp8 and has_write
                             else "pa_decode_fp8" if fp8
                             else "pa_write_kv (new token per sequence) + pa_decode" if has_write

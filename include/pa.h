@@ -277,6 +277,18 @@ int pa_decode_fp8(void* out, const void* query, const void* key_cache, const voi
                   int num_blocks, float scale, int dtype, void* workspace, size_t workspace_bytes, void* stream);
 size_t pa_decode_fp8_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
                                     int max_blocks_per_seq, int dtype);
+/*
+ * pa_decode_fp8_append — pa_decode_fp8 with the step's write folded in, as pa_decode_append: the
+ * new token of sequence b (new_key / new_value [num_seqs, H_kv, head_dim] in `dtype`, 16-byte
+ * aligned) is quantised with the scales of the block that receives it and stored at the slot the
+ * block table gives position L_b - 1, then attended.  Same cache bytes and output bits as
+ * pa_write_kv_fp8 at those slots followed by pa_decode_fp8.  value_cache NULL: interleaved layout.
+ */
+int pa_decode_fp8_append(void* out, const void* query, const void* new_key, const void* new_value, void* key_cache,
+                         void* value_cache, const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                         const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                         int block_size, int max_blocks_per_seq, int num_blocks, float scale, int dtype,
+                         void* workspace, size_t workspace_bytes, void* stream);
 
 /*
  * pa_decode_multi — multi-query decode: the verify step of speculative decoding, or
@@ -375,15 +387,16 @@ int pa_decode_static_scratch(void* out, const void* query, const void* key_cache
  *
  * kind: PA_STEP_DECODE (pa_decode_ex), PA_STEP_APPEND (pa_decode_append),
  * PA_STEP_FP8 (pa_decode_fp8), PA_STEP_FP8_WRITE (pa_write_kv_fp8 of the new tokens at
- * `slots`, then pa_decode_fp8).  With deltas != NULL, pa_apply_table_deltas(
+ * `slots`, then pa_decode_fp8), PA_STEP_FP8_APPEND (pa_decode_fp8_append).  With
+ * deltas != NULL, pa_apply_table_deltas(
  * block_tables, num_seqs, max_blocks_per_seq, deltas, num_deltas) runs first.
  */
-enum { PA_STEP_DECODE = 0, PA_STEP_APPEND = 1, PA_STEP_FP8 = 2, PA_STEP_FP8_WRITE = 3 };
+enum { PA_STEP_DECODE = 0, PA_STEP_APPEND = 1, PA_STEP_FP8 = 2, PA_STEP_FP8_WRITE = 3, PA_STEP_FP8_APPEND = 4 };
 typedef struct pa_step_call {
     int kind;
     void* out;
     const void* query;
-    const void* new_key;     /* PA_STEP_APPEND, PA_STEP_FP8_WRITE */
+    const void* new_key;     /* PA_STEP_APPEND, PA_STEP_FP8_WRITE, PA_STEP_FP8_APPEND */
     const void* new_value;
     const int64_t* slots;    /* PA_STEP_FP8_WRITE: int64 [num_seqs] */
     void* key_cache;

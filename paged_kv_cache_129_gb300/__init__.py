@@ -17,6 +17,7 @@ from .binding import (  # noqa: F401
     decode,
     decode_append,
     decode_fp8,
+    decode_fp8_append,
     decode_fp8_workspace_size,
     decode_multi,
     decode_multi_workspace_size,

@@ -42,7 +42,7 @@ class PoolExhausted(PAError, MemoryError):
     pass
 
 
-STEP_DECODE, STEP_APPEND, STEP_FP8, STEP_FP8_WRITE = 0, 1, 2, 3
+STEP_DECODE, STEP_APPEND, STEP_FP8, STEP_FP8_WRITE, STEP_FP8_APPEND = 0, 1, 2, 3, 4
 
 
 class StepCall(ctypes.Structure):
@@ -79,6 +79,8 @@ _SIGNATURES = [
     ("pa_swap_blocks", _I, [_P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _P]),
     ("pa_write_kv_fp8", _I, [_P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _P]),
     ("pa_decode_fp8", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P, _SZ, _P]),
+    ("pa_decode_fp8_append", _I, [_P, _P, _P, _P, _P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P,
+                                  _SZ, _P]),
     ("pa_decode_fp8_workspace_size", _SZ, [_I, _I, _I, _I, _I, _I, _I]),
     ("pa_write_kv_layers", _I, [_P, _P, _P, _P, _I, _P, _I, _I, _I, _I, _I, _I, _P]),
     ("pa_apply_table_deltas", _I, [_P, _I, _I, _P, _I, _P]),
@@ -401,10 +403,23 @@ def decode_fp8_workspace_size(num_seqs: int, num_heads: int, num_kv_heads: int, 
 def decode_fp8(query: torch.Tensor, key_cache: torch.Tensor, value_cache: Optional[torch.Tensor], k_scale: torch.Tensor,
                v_scale: torch.Tensor, block_tables: torch.Tensor, context_lens: torch.Tensor,
                scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
-               workspace: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+               workspace: Optional[torch.Tensor] = None, stream=None, new_key: Optional[torch.Tensor] = None,
+               new_value: Optional[torch.Tensor] = None) -> torch.Tensor:
     """``pa_decode_fp8``: paged decode attention over E4M3 caches with (block, kv head) scales; ``query``
-    f16/bf16 ``[B, H_q, d]``.  ``workspace`` defaults to a fresh one of the plan's size."""
+    f16/bf16 ``[B, H_q, d]``.  ``workspace`` defaults to a fresh one of the plan's size.
+
+    With ``new_key`` / ``new_value`` (``[B, H_kv, d]``, the query's dtype) it is
+    ``pa_decode_fp8_append``: each sequence's new token is quantised into the slot of position
+    L - 1 inside the decode, the same codes ``write_kv_fp8`` would store there.
+    """
     num_blocks, hkv, bs, d = _fp8_cache(key_cache, value_cache, k_scale, v_scale)
+    if new_key is not None or new_value is not None:
+        _need(new_key is not None and new_value is not None, "new_key and new_value go together")
+        _cuda(new_key, "new_key")
+        _cuda(new_value, "new_value")
+        _need(new_key.shape == (query.shape[0], hkv, d) and new_value.shape == new_key.shape,
+              "new_key/new_value must be [B, H_kv, d]")
+        _need(new_key.dtype == new_value.dtype == query.dtype, "new_key/new_value must have the query's dtype")
     for name, t in (("query", query), ("block_tables", block_tables), ("context_lens", context_lens)):
         _cuda(t, name)
     _need(query.dim() == 3 and query.shape[2] == d, "query must be [B, H_q, d]")
@@ -423,12 +438,28 @@ def decode_fp8(query: torch.Tensor, key_cache: torch.Tensor, value_cache: Option
         workspace = torch.empty(max(n, 256), dtype=torch.uint8, device=query.device)
     _cuda(workspace, "workspace")
     vptr = value_cache.data_ptr() if value_cache is not None else None
-    _check(library().pa_decode_fp8(out.data_ptr(), query.data_ptr(), key_cache.data_ptr(), vptr,
-                                   k_scale.data_ptr(), v_scale.data_ptr(), block_tables.data_ptr(),
-                                   context_lens.data_ptr(), b, hq, hkv, d, bs, block_tables.shape[1], num_blocks,
-                                   float(scale), _dtype_code(query), workspace.data_ptr(),
-                                   workspace.numel() * workspace.element_size(), _stream_ptr(stream, query.device)))
+    tail = (block_tables.data_ptr(), context_lens.data_ptr(), b, hq, hkv, d, bs, block_tables.shape[1], num_blocks,
+            float(scale), _dtype_code(query), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+            _stream_ptr(stream, query.device))
+    if new_key is None:
+        _check(library().pa_decode_fp8(out.data_ptr(), query.data_ptr(), key_cache.data_ptr(), vptr,
+                                       k_scale.data_ptr(), v_scale.data_ptr(), *tail))
+    else:
+        _check(library().pa_decode_fp8_append(out.data_ptr(), query.data_ptr(), new_key.data_ptr(),
+                                              new_value.data_ptr(), key_cache.data_ptr(), vptr, k_scale.data_ptr(),
+                                              v_scale.data_ptr(), *tail))
     return out
+
+
+def decode_fp8_append(query: torch.Tensor, new_key: torch.Tensor, new_value: torch.Tensor, key_cache: torch.Tensor,
+                      value_cache: Optional[torch.Tensor], k_scale: torch.Tensor, v_scale: torch.Tensor,
+                      block_tables: torch.Tensor, context_lens: torch.Tensor, scale: Optional[float] = None,
+                      out: Optional[torch.Tensor] = None, workspace: Optional[torch.Tensor] = None,
+                      stream=None) -> torch.Tensor:
+    """``pa_decode_fp8_append``: ``write_kv_fp8`` of each sequence's new token at position L - 1
+    followed by ``decode_fp8``, in one kernel."""
+    return decode_fp8(query, key_cache, value_cache, k_scale, v_scale, block_tables, context_lens, scale=scale,
+                      out=out, workspace=workspace, stream=stream, new_key=new_key, new_value=new_value)
 
 
 def decode_multi_workspace_size(num_seqs: int, q_len: int, num_heads: int, num_kv_heads: int, head_dim: int,

@@ -844,6 +844,20 @@ int pa_decode_fp8(void* out, const void* query, const void* key_cache, const voi
                        workspace, workspace_bytes, 0, 0, PA_KERNEL_AUTO, stream, 1, k_scale, v_scale);
 }
 
+int pa_decode_fp8_append(void* out, const void* query, const void* new_key, const void* new_value, void* key_cache,
+                         void* value_cache, const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                         const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads, int head_dim,
+                         int block_size, int max_blocks_per_seq, int num_blocks, float scale, int dtype,
+                         void* workspace, size_t workspace_bytes, void* stream) {
+    if (!k_scale || !new_key) {
+        clear_error();
+        return fail(PA_ERR_INVALID_ARG, "pa_decode_fp8_append: k_scale or new_key is NULL");
+    }
+    return decode_impl(out, query, new_key, new_value, key_cache, value_cache, block_tables, context_lens, num_seqs,
+                       num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, num_blocks, scale, dtype,
+                       workspace, workspace_bytes, 0, 0, PA_KERNEL_AUTO, stream, 1, k_scale, v_scale);
+}
+
 size_t pa_decode_fp8_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int block_size,
                                     int max_blocks_per_seq, int dtype) {
     Plan p;

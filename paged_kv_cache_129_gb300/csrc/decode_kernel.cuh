@@ -454,6 +454,59 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint
         : "r"(w));
 }
 
+// The step's new token for an FP8 cache (append mode of pa_decode_fp8_append): the new K and V rows
+// (D elements of T each, one 16-byte chunk per lane: lanes 0..15 K, 16..31 V) are quantised with the
+// scale of the block that receives them, exactly as pa_write_kv_fp8 does (float32 division, E4M3 with
+// round-to-nearest-even and saturation), patched into the staged page and stored into the cache.
+template <typename T, int D, int BS>
+struct NewTokenF8 {
+    static_assert(D * (int)sizeof(T) == 256, "one 16-byte chunk of K or V per lane at head_dim 128");
+    uint4 c;     // this lane's 8 source elements
+    uint2 code;  // their E4M3 codes (after patch())
+
+    __device__ __forceinline__ void load(const T* key_row, const T* value_row, int lane) {
+        c = __ldg(reinterpret_cast<const uint4*>(lane < 16 ? key_row : value_row) + (lane & 15));
+    }
+
+    // Quantise with the block's K / V scale and overwrite row r of the staged K and V tiles.
+    __device__ __forceinline__ void patch(uint8_t* kpage, uint8_t* vpage, int r, float ks, float vs, int lane) {
+        float x[8];
+        unpack16<T>(c, x);
+        const float sc = lane < 16 ? ks : vs;
+        uint32_t w[2];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const uint32_t lo = __nv_cvt_float2_to_fp8x2(make_float2(x[4 * h] / sc, x[4 * h + 1] / sc), __NV_SATFINITE,
+                                                         __NV_E4M3);
+            const uint32_t hi = __nv_cvt_float2_to_fp8x2(make_float2(x[4 * h + 2] / sc, x[4 * h + 3] / sc),
+                                                         __NV_SATFINITE, __NV_E4M3);
+            w[h] = lo | (hi << 16);
+        }
+        code = make_uint2(w[0], w[1]);
+        const int ch = lane & 15;  // bytes 8ch .. 8ch + 7 of the 128-byte row
+        uint8_t* tile = lane < 16 ? kpage : vpage;
+        *reinterpret_cast<uint2*>(tile + r * 128 + ((((ch >> 1) ^ (r & 7))) << 4) + (ch & 1) * 8) = code;
+        fence_proxy_async_smem();
+        __syncwarp();
+    }
+
+    // Store the codes at row `off` of record row `rec_row` = (pb * Hkv + kvh) * BS of the caches.
+    __device__ __forceinline__ void store(void* key_cache, void* value_cache, int rec_row, int off, bool interleaved,
+                                          int lane) const {
+        const int ch = lane & 15;
+        size_t at;
+        uint8_t* base;
+        if (interleaved) {  // [N, H_kv, 2, BS, D] in key_cache
+            at = ((size_t)2 * rec_row + (lane < 16 ? 0 : BS) + off) * D;
+            base = static_cast<uint8_t*>(key_cache);
+        } else {
+            at = ((size_t)rec_row + off) * D;
+            base = static_cast<uint8_t*>(lane < 16 ? key_cache : value_cache);
+        }
+        *reinterpret_cast<uint2*>(base + at + ch * 8) = code;
+    }
+};
+
 template <typename T, int D, int BS>
 struct MmaConsumerF8 {
     static_assert(D == 128, "the FP8 consumer's lane layout is for head_dim 128");
@@ -1271,7 +1324,11 @@ __device__ __forceinline__ void lean_locate(const int* pre, int num_seqs, int up
 
 // F8: the caches hold E4M3 codes with a scale per (block, kv head) (MmaConsumerF8); T is then
 // the query and output type.
-template <typename T, int D, int BS, bool MMA, int GMAX, bool CAUSAL, bool F8 = false>
+// F8: E4M3 pages with per-(block, kv head) scales.  The append mode (the step's new token
+// written inside the decode) is a runtime choice (new_key != nullptr) for the 16/32-bit caches
+// and a separate instantiation (F8_APPEND) for FP8, whose consumer has no registers to spare
+// for a path it does not take.
+template <typename T, int D, int BS, bool MMA, int GMAX, bool CAUSAL, bool F8 = false, bool F8_APPEND = false>
 __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
                                   (F8 ? PA_LEAN_F8_MIN_BLOCKS : LeanCfg<T, D, BS, MMA, GMAX>::kMinBlocks))
     paged_decode_lean_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
@@ -1447,8 +1504,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
         int b = 0, uu = 0, nb = 0, L = 0, gc = 0, kvh = 0;
         UnitRows rows{0, 0, 0, a.q_len, a.group, a.num_heads};
         int wrote = 0;  // bit s: a partial record was written to slot s
-        const bool append = !F8 && a.new_key != nullptr;
-        NewToken<T, D, BS> tok;
+        const bool append = F8 ? F8_APPEND : a.new_key != nullptr;
+        std::conditional_t<F8, NewTokenF8<T, D, BS>, NewToken<T, D, BS>> tok;
         bool tok_ready = false, tok_writer = false;
         std::conditional_t<F8, MmaConsumerF8<T, D, BS>,
                            std::conditional_t<MMA, MmaConsumer<T, D, BS, CAUSAL>, SimtConsumer<T, D, BS, GMAX>>>
@@ -1562,15 +1619,24 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
             if (!__all_sync(0xffffffffu, got)) break;
             const int nvalid = min(BS, L - j * BS);
             uint8_t* kp = ring + s * C::kSlotBytes;
+            float ks = 0.f, vs = 0.f;  // FP8: this page's K and V scales
+            if constexpr (F8) {
+                ks = __shfl_sync(0xffffffffu, cur_ks, off & 31);
+                vs = __shfl_sync(0xffffffffu, cur_vs, off & 31);
+            }
             if (tok_page) {
-                tok.patch(kp, kp + C::kPageBytes, nvalid - 1, lane);
                 const int row = queue[off % C::kRowQueue];  // (pb * Hkv + kvh) * BS, or -1
-                if (tok_writer && row >= 0) tok.store(a.key_cache, a.value_cache, row + nvalid - 1, lane);
+                if constexpr (F8) {
+                    tok.patch(kp, kp + C::kPageBytes, nvalid - 1, ks, vs, lane);
+                    if (tok_writer && row >= 0)
+                        tok.store(a.key_cache, a.value_cache, row, nvalid - 1, a.kv_interleaved != 0, lane);
+                } else {
+                    tok.patch(kp, kp + C::kPageBytes, nvalid - 1, lane);
+                    if (tok_writer && row >= 0) tok.store(a.key_cache, a.value_cache, row + nvalid - 1, lane);
+                }
                 tok_ready = false;
             }
             if constexpr (F8) {
-                const float ks = __shfl_sync(0xffffffffu, cur_ks, off & 31);
-                const float vs = __shfl_sync(0xffffffffu, cur_vs, off & 31);
                 cons.page(kp, kp + C::kPageBytes, nvalid, ks, vs, lane);
                 __syncwarp();
             } else if constexpr (MMA) {
@@ -1887,14 +1953,20 @@ struct DecodeKernel {
 template <typename T, int D, int BS>
 struct DecodeKernelF8 {
     using LC = LeanCfg<uint8_t, D, BS, true, 8>;
+    using Fn = void (*)(const CUtensorMap, const CUtensorMap, const DecodeArgs);
+    static Fn kernel(bool append) {
+        return append ? paged_decode_lean_kernel<T, D, BS, true, 8, false, true, true>
+                      : paged_decode_lean_kernel<T, D, BS, true, 8, false, true, false>;
+    }
 
     static bool configure(int device) {
         static unsigned long long done_mask = 0;
         const unsigned long long bit = 1ull << (device & 63);
         if (done_mask & bit) return true;
-        if (cudaFuncSetAttribute(paged_decode_lean_kernel<T, D, BS, true, 8, false, true>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize, LC::kMaxSmemBytes) != cudaSuccess)
-            return false;
+        for (const bool append : {false, true})
+            if (cudaFuncSetAttribute(kernel(append), cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     LC::kMaxSmemBytes) != cudaSuccess)
+                return false;
         done_mask |= bit;
         return true;
     }
@@ -1910,8 +1982,8 @@ struct DecodeKernelF8 {
         std::atomic<int>& slot = cache[device & 63][kb < 232 ? kb : 231];
         int n = slot.load(std::memory_order_relaxed);
         if (n <= 0) {
-            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, paged_decode_lean_kernel<T, D, BS, true, 8, false, true>,
-                                                              LC::kThreads, kb * 1024) != cudaSuccess ||
+            if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel(false), LC::kThreads, kb * 1024) !=
+                    cudaSuccess ||
                 n <= 0)
                 n = 1;
             slot.store(n, std::memory_order_relaxed);
@@ -1935,8 +2007,8 @@ struct DecodeKernelF8 {
         cudaError_t e = cudaGetDevice(&device);
         if (e != cudaSuccess) return e;
         if (!configure(device)) return cudaGetLastError();
-        e = launch_pdl(paged_decode_lean_kernel<T, D, BS, true, 8, false, true>, dim3(grid), dim3(LC::kThreads),
-                       LC::smem_bytes(num_seqs), stream, k, v, a);
+        e = launch_pdl(kernel(a.new_key != nullptr), dim3(grid), dim3(LC::kThreads), LC::smem_bytes(num_seqs), stream,
+                       k, v, a);
         if (e != cudaSuccess) return e;
         DecodeArgs m = a;
         m.lean_grid = grid;

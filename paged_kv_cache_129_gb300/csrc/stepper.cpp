@@ -74,6 +74,11 @@ int run_call(const pa_step_call& c, int num_deltas, cudaStream_t stream) {
                                  c.context_lens, c.num_seqs, c.num_heads, c.num_kv_heads, c.head_dim, c.block_size,
                                  c.max_blocks_per_seq, c.num_blocks, c.scale, c.dtype, c.workspace,
                                  c.workspace_bytes, sp);
+        case PA_STEP_FP8_APPEND:
+            return pa_decode_fp8_append(c.out, c.query, c.new_key, c.new_value, c.key_cache, c.value_cache, c.k_scale,
+                                        c.v_scale, c.block_tables, c.context_lens, c.num_seqs, c.num_heads,
+                                        c.num_kv_heads, c.head_dim, c.block_size, c.max_blocks_per_seq, c.num_blocks,
+                                        c.scale, c.dtype, c.workspace, c.workspace_bytes, sp);
         default:
             return pa::fail(PA_ERR_INVALID_ARG, "pa_stepper: unknown step kind %d", c.kind);
     }
@@ -133,7 +138,7 @@ int pa_stepper_set_slot(pa_stepper* st, int slot, const void* host_in, void* dev
 int pa_stepper_set_call(pa_stepper* st, int slot, const pa_step_call* call) {
     if (!st || slot < 0 || slot >= (int)st->slots.size() || !call)
         return pa::fail(PA_ERR_INVALID_ARG, "pa_stepper_set_call: bad stepper, slot %d or call", slot);
-    if (call->kind < PA_STEP_DECODE || call->kind > PA_STEP_FP8_WRITE)
+    if (call->kind < PA_STEP_DECODE || call->kind > PA_STEP_FP8_APPEND)
         return pa::fail(PA_ERR_INVALID_ARG, "pa_stepper_set_call: unknown step kind %d", call->kind);
     st->slots[slot].call = *call;
     st->slots[slot].has_call = true;

@@ -61,17 +61,19 @@ class DecodeStepper:
     previous step's decode has read the table.
 
     FP8 caches (``k_scale`` / ``v_scale`` given, E4M3 codes in the caches,
-    ``query_dtype`` f16 or bf16): a step is ``pa_write_kv_fp8`` of the new
-    tokens at ``inputs(i).slots`` (int64) when ``append``, then
-    ``pa_decode_fp8``.
+    ``query_dtype`` f16 or bf16): with ``append`` a step is
+    ``pa_decode_fp8_append`` (the new tokens quantised into position L - 1
+    inside the decode), or with ``fp8_write="separate"`` ``pa_write_kv_fp8``
+    of the new tokens at ``inputs(i).slots`` (int64) then ``pa_decode_fp8``;
+    without ``append`` it is ``pa_decode_fp8``.
     """
 
     def __init__(self, key_cache: torch.Tensor, value_cache: torch.Tensor, num_seqs: int, num_heads: int,
                  max_blocks_per_seq: int, scale: Optional[float] = None, append: bool = True, slots: int = 2,
                  max_context_len: int = 0, partition_pages: int = 0, kernel: str = "auto", tables: str = "full",
                  k_scale: Optional[torch.Tensor] = None, v_scale: Optional[torch.Tensor] = None,
-                 query_dtype: Optional[torch.dtype] = None):
-        assert tables in ("full", "deltas")
+                 query_dtype: Optional[torch.dtype] = None, fp8_write: str = "fused"):
+        assert tables in ("full", "deltas") and fp8_write in ("fused", "separate")
         self.fp8 = k_scale is not None
         if self.fp8 and value_cache is None:  # interleaved FP8 layout [N, H_kv, 2, bs, d]
             assert key_cache.is_cuda and key_cache.dim() == 5 and key_cache.shape[2] == 2
@@ -88,11 +90,12 @@ class DecodeStepper:
         self.shape = (num_seqs, num_heads, hkv, d, bs, max_blocks_per_seq, num_blocks)
         self.scale = 1.0 / math.sqrt(d) if scale is None else float(scale)
         self.append, self.slots = append, slots
+        self.fp8_slots = self.fp8 and append and fp8_write == "separate"
         self.max_context_len, self.partition_pages, self.kernel = max_context_len, partition_pages, kernel
         fields = [("query", (num_seqs, num_heads, d), dt)]
         if append:
             fields += [("new_key", (num_seqs, hkv, d), dt), ("new_value", (num_seqs, hkv, d), dt)]
-            if self.fp8:
+            if self.fp8_slots:
                 fields += [("slots", (num_seqs,), torch.int64)]
         self.deltas_mode = tables == "deltas"
         if self.deltas_mode:
@@ -147,12 +150,15 @@ class DecodeStepper:
         dv, out, ws = self._dv_in[s], self._dv_out[s], self._ws[s]
         tables = self.device_block_tables if self.deltas_mode else dv.block_tables
         c = binding.StepCall()
-        c.kind = ((binding.STEP_FP8_WRITE if self.append else binding.STEP_FP8) if self.fp8 else
-                  binding.STEP_APPEND if self.append else binding.STEP_DECODE)
+        if self.fp8:
+            c.kind = (binding.STEP_FP8_WRITE if self.fp8_slots else
+                      binding.STEP_FP8_APPEND if self.append else binding.STEP_FP8)
+        else:
+            c.kind = binding.STEP_APPEND if self.append else binding.STEP_DECODE
         c.out, c.query = out.data_ptr(), dv.query.data_ptr()
         if self.append:
             c.new_key, c.new_value = dv.new_key.data_ptr(), dv.new_value.data_ptr()
-            if self.fp8:
+            if self.fp8_slots:
                 c.slots = dv.slots.data_ptr()
         c.key_cache, c.value_cache = kc.data_ptr(), (vc.data_ptr() if vc is not None else None)
         if self.fp8:

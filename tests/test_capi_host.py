@@ -509,3 +509,16 @@ def test_fp8_entry_points_reject_bad_arguments(lib):
     zero = list(args)
     zero[8] = 0  # no sequences
     assert lib.pa_decode_fp8(*zero) == 0
+    # pa_decode_fp8_append: NULL or misaligned new rows, NULL scales, f32 queries; no sequences is a no-op
+    args = [FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 2, 8, 2, 128, 16, 4, 10, f, 2, FAKE, 1 << 20,
+            None]
+    for i, v in ((2, None), (3, None), (3, FAKE + 8), (6, None), (7, None)):
+        bad = list(args)
+        bad[i] = v
+        assert lib.pa_decode_fp8_append(*bad) == 1, i
+    bad = list(args)
+    bad[18] = 0  # PA_F32
+    assert lib.pa_decode_fp8_append(*bad) == 2
+    zero = list(args)
+    zero[10] = 0
+    assert lib.pa_decode_fp8_append(*zero) == 0

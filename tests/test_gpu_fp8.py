@@ -7,7 +7,11 @@
   at block sizes 16 and 32, NaN codes in the slots past each context, scales that differ per
   (block, kv head), and queries of magnitudes far outside f16's range;
 * the Qwen-shaped layer at full size (the shape the benchmark times): the caches written by
-  the GPU writer equal the oracle's byte for byte, and sampled output rows match the oracle.
+  the GPU writer equal the oracle's byte for byte, and sampled output rows match the oracle;
+* pa_decode_fp8_append (the new token quantised at position L - 1 inside the decode): the
+  caches equal the oracle's writer at those slots byte for byte, the output is bit-identical to
+  pa_write_kv_fp8 + pa_decode_fp8 and within tolerance of the oracle, for both layouts, block
+  sizes 16 and 32, GQA groups that take one and two head chunks, and at full Qwen size.
 """
 import numpy as np
 import pytest
@@ -163,9 +167,10 @@ def test_qwen_layer_fp8_full_size():
     pa.check_error()
 
 
-def test_stepper_fp8_matches_direct_calls():
-    """pa.DecodeStepper over FP8 caches (new tokens quantised at their slots, then the FP8 decode; block
-    tables kept by deltas) gives the same bytes as direct pa_write_kv_fp8 + pa_decode_fp8 calls."""
+@pytest.mark.parametrize("fp8_write", ["separate", "fused"])
+def test_stepper_fp8_matches_direct_calls(fp8_write):
+    """pa.DecodeStepper over FP8 caches (new tokens quantised at their slots then the FP8 decode, or the
+    fused pa_decode_fp8_append; block tables kept by deltas) gives the same bytes as the direct calls."""
     rng = np.random.default_rng(21)
     B, hq, hkv, bs, d, steps = 6, 28, 4, 16, 128, 5
     lens = rng.integers(1, 300, B).astype(np.int32)
@@ -185,7 +190,7 @@ def test_stepper_fp8_matches_direct_calls():
     vs = torch.from_numpy(rng.uniform(0.005, 0.02, (nb, hkv)).astype(np.float32)).cuda()
     kc_ref, vc_ref = kc.clone(), vc.clone()
     stepper = pa.DecodeStepper(kc, vc, B, hq, width, append=True, tables="deltas", k_scale=ks, v_scale=vs,
-                               query_dtype=torch.bfloat16)
+                               query_dtype=torch.bfloat16, fp8_write=fp8_write)
     deltas = np.array([(r, j, bt[r, j]) for r in range(B) for j in range(nblk[r])], np.int32)
     got, refs = [], []
     ws = torch.empty(max(pa.decode_fp8_workspace_size(B, hq, hkv, d, bs, width, torch.bfloat16), 256),
@@ -200,14 +205,21 @@ def test_stepper_fp8_matches_direct_calls():
         v.query.copy_(q)
         v.new_key.copy_(nk)
         v.new_value.copy_(nv)
-        v.slots.copy_(torch.from_numpy(slots))
+        if fp8_write == "separate":
+            v.slots.copy_(torch.from_numpy(slots))
+        else:
+            assert not hasattr(v, "slots")  # the fused step derives the slots from the tables
         v.context_lens.copy_(torch.from_numpy(lens))
         n = len(deltas) if i == 0 else 0
         v.deltas.numpy()[:n] = deltas[:n]
         stepper.launch(i, num_deltas=n)
-        pa.write_kv_fp8(nk.cuda(), nv.cuda(), kc_ref, vc_ref, ks, vs, torch.from_numpy(slots).cuda())
-        refs.append(pa.decode_fp8(q.cuda(), kc_ref, vc_ref, ks, vs, torch.from_numpy(bt).cuda(),
-                                  torch.from_numpy(lens).cuda(), workspace=ws))
+        dbt, dl = torch.from_numpy(bt).cuda(), torch.from_numpy(lens).cuda()
+        if fp8_write == "separate":
+            pa.write_kv_fp8(nk.cuda(), nv.cuda(), kc_ref, vc_ref, ks, vs, torch.from_numpy(slots).cuda())
+            refs.append(pa.decode_fp8(q.cuda(), kc_ref, vc_ref, ks, vs, dbt, dl, workspace=ws))
+        else:
+            refs.append(pa.decode_fp8_append(q.cuda(), nk.cuda(), nv.cuda(), kc_ref, vc_ref, ks, vs, dbt, dl,
+                                             workspace=ws))
     for i in range(steps - stepper.slots, steps):
         got.append(stepper.result(i).clone())
     torch.cuda.synchronize()
@@ -287,4 +299,90 @@ def test_fp8_copy_and_swap_bit_exact(layout):
     assert np.array_equal(hk.numpy(), h_exp_k) and np.array_equal(dk.cpu().numpy(), exp_k)
     if vc is not None:
         assert np.array_equal(hv.numpy(), h_exp_v) and np.array_equal(dv.cpu().numpy(), exp_v)
+    pa.check_error()
+
+
+def _new_token_slots(bt, lens, bs):
+    """Slots of positions L - 1 through the block tables (-1 for an empty context)."""
+    return np.array([bt[b, (L - 1) // bs] * bs + (L - 1) % bs if L >= 1 else -1 for b, L in enumerate(lens)],
+                    np.int64)
+
+
+@pytest.mark.parametrize("dtype", ["bf16", "f16"])
+@pytest.mark.parametrize("bs", [16, 32])
+@pytest.mark.parametrize("layout", ["separate", "interleaved"])
+@pytest.mark.parametrize("hq,hkv", [(28, 4), (8, 8), (32, 2)])
+def test_decode_fp8_append_matches_write_then_decode(dtype, bs, layout, hq, hkv):
+    """pa_decode_fp8_append: the new token of each sequence quantised with its block's scales at position
+    L - 1 (the first, a middle and the last row of a page; L = 0 writes nothing), then attended.  Group 16
+    (32 / 2 heads) splits each kv head into two head chunks, which patch the staged page alike while
+    only the first stores it."""
+    d = 128
+    lens = [0, 1, 15, 16, 17, 33, 250, 1000, 64, 2]
+    q, kc, vc, ks, vs, bt, lens = _case(hq * bs + hkv + 5, lens, hq, hkv, bs, dtype)
+    rng = np.random.default_rng(hq + bs)
+    nk = _src(rng, (len(lens), hkv, d), dtype, 1.5)  # |x| / scale spans normal codes and saturation
+    nv = _src(rng, (len(lens), hkv, d), dtype, 1.5)
+    slots = _new_token_slots(bt, lens, bs)
+    ek, ev = kc.copy(), vc.copy()
+    assert oracle.write_kv_fp8(nk, nv, dtype, ek, ev, ks, vs, slots) == oracle.OK
+    ref = oracle.decode_fp8(q, dtype, ek, ev, ks, vs, bt, lens, 1 / np.sqrt(d))
+
+    def caches():
+        if layout == "interleaved":
+            return torch.from_numpy(np.ascontiguousarray(np.stack([kc, vc], axis=2))).cuda(), None
+        return torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda()
+
+    dks, dvs = torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda()
+    dq, dbt, dl = to_device(q, dtype), torch.from_numpy(bt).cuda(), torch.from_numpy(lens).cuda()
+    dnk, dnv = to_device(nk, dtype), to_device(nv, dtype)
+    ws = torch.empty(max(pa.decode_fp8_workspace_size(len(lens), hq, hkv, d, bs, bt.shape[1], TORCH_DTYPE[dtype]),
+                         256), dtype=torch.uint8, device="cuda")
+    fk, fv = caches()
+    fused = pa.decode_fp8_append(dq, dnk, dnv, fk, fv, dks, dvs, dbt, dl, workspace=ws)
+    uk, uv = caches()
+    pa.write_kv_fp8(dnk, dnv, uk, uv, dks, dvs, torch.from_numpy(slots).cuda())
+    unfused = pa.decode_fp8(dq, uk, uv, dks, dvs, dbt, dl, workspace=ws)
+    torch.cuda.synchronize()
+    if layout == "interleaved":
+        assert np.array_equal(fk.cpu().numpy(), np.stack([ek, ev], axis=2))
+    else:
+        assert np.array_equal(fk.cpu().numpy(), ek) and np.array_equal(fv.cpu().numpy(), ev)
+    assert torch.equal(fused.view(torch.int16), unfused.view(torch.int16))
+    got = to_f64(fused)
+    assert_decode_close(got, ref, dtype)
+    assert np.all(got[0] == 0)
+    pa.check_error()
+
+
+def test_qwen_layer_fp8_append_full_size():
+    """The step the benchmark times for the FP8 Qwen-shaped layer (batch 64, 28/4 heads, d 128, bs 16,
+    L ~ U[512, 4096], pool 20000, interleaved layout): after pa_decode_fp8_append the whole pool equals the
+    oracle's (its quantised pool plus the new tokens at positions L - 1) byte for byte, and sampled output
+    rows match the oracle's decode over it."""
+    inp = wl.qwen_gqa(0)
+    ks, vs = wl.fp8_scales(inp.key_cache, inp.dtype), wl.fp8_scales(inp.value_cache, inp.dtype)
+    nb, hkv, bs, d = inp.key_cache.shape
+    slots = np.arange(nb * bs, dtype=np.int64)
+    src_k = np.ascontiguousarray(inp.key_cache.transpose(0, 2, 1, 3).reshape(nb * bs, hkv, d))
+    src_v = np.ascontiguousarray(inp.value_cache.transpose(0, 2, 1, 3).reshape(nb * bs, hkv, d))
+    kv = torch.empty(nb, hkv, 2, bs, d, dtype=torch.uint8, device="cuda")
+    dks, dvs = torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda()
+    pa.write_kv_fp8(to_device(src_k, inp.dtype), to_device(src_v, inp.dtype), kv, None, dks, dvs,
+                    torch.from_numpy(slots).cuda())
+    kc = np.zeros((nb, hkv, bs, d), np.uint8)
+    vc = np.zeros_like(kc)
+    assert oracle.write_kv_fp8(src_k, src_v, inp.dtype, kc, vc, ks, vs, slots) == oracle.OK
+    new_slots = _new_token_slots(inp.block_tables, inp.context_lens, bs)
+    assert oracle.write_kv_fp8(inp.new_key, inp.new_value, inp.dtype, kc, vc, ks, vs, new_slots) == oracle.OK
+    out = pa.decode_fp8_append(to_device(inp.q, inp.dtype), to_device(inp.new_key, inp.dtype),
+                               to_device(inp.new_value, inp.dtype), kv, None, dks, dvs,
+                               torch.from_numpy(inp.block_tables).cuda(), torch.from_numpy(inp.context_lens).cuda())
+    torch.cuda.synchronize()
+    assert np.array_equal(kv.cpu().numpy(), np.stack([kc, vc], axis=2))
+    got = to_f64(out)
+    rng = np.random.default_rng(2)
+    rows = [(int(b), int(h)) for b, h in zip(rng.integers(0, 64, 48), rng.integers(0, 28, 48))]
+    ref = oracle.decode_fp8(inp.q, inp.dtype, kc, vc, ks, vs, inp.block_tables, inp.context_lens, inp.scale, rows)
+    assert_decode_close(np.stack([got[b, h] for b, h in rows]), ref, inp.dtype)
     pa.check_error()

@@ -461,17 +461,21 @@ __device__ __forceinline__ void e4m3x4_to_f16x2x2(uint32_t w, uint32_t& lo, uint
 template <typename T, int D, int BS>
 struct NewTokenF8 {
     static_assert(D * (int)sizeof(T) == 256, "one 16-byte chunk of K or V per lane at head_dim 128");
-    uint4 c;     // this lane's 8 source elements
-    uint2 code;  // their E4M3 codes (after patch())
+    uint8_t* stage;  // this warp's 512-byte staging area in shared memory
+    uint2 code;      // this lane's E4M3 codes (after patch())
 
+    // Start the copy of this lane's 8 source elements into the staging area (no registers held
+    // while the pages before the token's page are consumed).
     __device__ __forceinline__ void load(const T* key_row, const T* value_row, int lane) {
-        c = __ldg(reinterpret_cast<const uint4*>(lane < 16 ? key_row : value_row) + (lane & 15));
+        cp_async_16(stage + 16 * lane, reinterpret_cast<const uint4*>(lane < 16 ? key_row : value_row) + (lane & 15));
+        cp_async_commit();
     }
 
     // Quantise with the block's K / V scale and overwrite row r of the staged K and V tiles.
     __device__ __forceinline__ void patch(uint8_t* kpage, uint8_t* vpage, int r, float ks, float vs, int lane) {
+        cp_async_wait_all();  // this lane's own 16 bytes
         float x[8];
-        unpack16<T>(c, x);
+        unpack16<T>(*reinterpret_cast<const uint4*>(stage + 16 * lane), x);
         const float sc = lane < 16 ? ks : vs;
         uint32_t w[2];
 #pragma unroll
@@ -1256,7 +1260,10 @@ struct LeanCfg {
     static constexpr int kQsBytes = MMA ? 0 : kNW * GMAX * D * 4;
     static constexpr int kPsOffset = a16(kQsOffset + kQsBytes);                     // fp32 p per warp
     static constexpr int kPsBytes = MMA ? 0 : kNW * GMAX * BS * 4;
-    static constexpr int kPrefixOffset = a16(kPsOffset + kPsBytes);                 // (num_seqs + 1) ints
+    // FP8 append: the new token's 16-bit K and V source rows per warp, staged by cp.async
+    static constexpr int kTokOffset = a16(kPsOffset + kPsBytes);
+    static constexpr int kTokBytes = sizeof(T) == 1 ? kNW * 2 * D * 2 : 0;
+    static constexpr int kPrefixOffset = a16(kTokOffset + kTokBytes);               // (num_seqs + 1) ints
     static constexpr int kFixedSmemBytes = kPrefixOffset + 1024;      // + slack to align the base
     static constexpr int kMaxSmemBytes = kFixedSmemBytes + (kLeanMaxSeqs + 1) * 4;
     static int smem_bytes(int num_seqs) { return kFixedSmemBytes + (num_seqs + 1) * 4; }
@@ -1506,6 +1513,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
         int wrote = 0;  // bit s: a partial record was written to slot s
         const bool append = F8 ? F8_APPEND : a.new_key != nullptr;
         std::conditional_t<F8, NewTokenF8<T, D, BS>, NewToken<T, D, BS>> tok;
+        if constexpr (F8) tok.stage = smem + C::kTokOffset + warp * 4 * D;
         bool tok_ready = false, tok_writer = false;
         std::conditional_t<F8, MmaConsumerF8<T, D, BS>,
                            std::conditional_t<MMA, MmaConsumer<T, D, BS, CAUSAL>, SimtConsumer<T, D, BS, GMAX>>>
@@ -1671,6 +1679,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
                 }
             }
         }
+        // A token copy may still be in flight when a wait gave up before its page.
+        if constexpr (F8 && F8_APPEND) cp_async_wait_all();
     }
     __syncthreads();
     if (flags[0]) {

@@ -1453,7 +1453,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
                 for (int wi = 0; wi < C::kNW; ++wi) {
                     const int avail = fill_cnt[wi];
                     __threadfence_block();  // the rows below were written before fill_cnt
-                    while (iss[wi] < avail) {
+                    // FP8 pages (4 KB, four slots a warp): at most one page per warp and pass,
+                    // round robin over the warps (measured: 13 % on long contexts, 9 % on the
+                    // Qwen-shaped step); 16-bit pages (two slots a warp): every free slot at once
+                    // (one page per pass cost 2 % there).
+                    for (int burst = 0; iss[wi] < avail && (!F8 || burst == 0); ++burst) {
                         const int s = wi * C::kSPW + iss[wi] % C::kSPW;
                         const int use = iss[wi] / C::kSPW;
                         if (use >= 1 && !mbar_test_wait(&empty[s], (use - 1) & 1)) break;
@@ -1464,19 +1468,20 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
                             uint8_t* kdst = ring + s * C::kSlotBytes;
                             uint8_t* vdst = kdst + C::kPageBytes;
                             if (F8 && a.kv_interleaved) {
-                                // K rows 2r .. 2r + BS - 1, then V: one box of 2 * BS rows (one 128-byte box
-                                // a row at head_dim 128), landing as the K page followed by the V page
+                                // K rows 2r .. 2r + BS - 1, then V: one box of 2 * BS rows (one
+                                // 128-byte box a row at head_dim 128), landing as the K page
+                                // followed by the V page
                                 static_assert(!F8 || C::Base::kNBox == 1, "one box per FP8 row");
                                 tma_load_2d_hint(kdst, &tmap_k, 0, 2 * r, &full[s], stream_policy);
                             } else {
 #pragma unroll
                                 for (int bx = 0; bx < C::Base::kNBox; ++bx)
-                                    tma_load_2d_hint(kdst + bx * C::Base::kBoxBytes, &tmap_k, bx * C::Base::kBoxElems,
-                                                     r, &full[s], stream_policy);
+                                    tma_load_2d_hint(kdst + bx * C::Base::kBoxBytes, &tmap_k,
+                                                     bx * C::Base::kBoxElems, r, &full[s], stream_policy);
 #pragma unroll
                                 for (int bx = 0; bx < C::Base::kNBox; ++bx)
-                                    tma_load_2d_hint(vdst + bx * C::Base::kBoxBytes, &tmap_v, bx * C::Base::kBoxElems,
-                                                     r, &full[s], stream_policy);
+                                    tma_load_2d_hint(vdst + bx * C::Base::kBoxBytes, &tmap_v,
+                                                     bx * C::Base::kBoxElems, r, &full[s], stream_policy);
                             }
                         } else {
                             atomicOr(a.err, kErrBadTable);  // skip the load; the slot keeps stale data

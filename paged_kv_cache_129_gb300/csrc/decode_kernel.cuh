@@ -318,6 +318,88 @@ struct MmaConsumer {
         }
     }
 
+    // Zero V rows nv .. 15 of a one-sub-tile page (rows past the context may hold anything).
+    __device__ __forceinline__ static void zero_tail(uint8_t* vpage, int nv, int lane) {
+        if (nv >= 16) return;
+        constexpr int kChunksPerRow = (D * (int)sizeof(T)) / 16;
+        for (int idx = lane; idx < (16 - nv) * kChunksPerRow; idx += 32) {
+            const int r = nv + idx / kChunksPerRow;
+            const int c = idx % kChunksPerRow;
+            *reinterpret_cast<uint4*>(vpage + (c / 8) * BS * 128 + r * 128 + (c % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+    }
+
+    // Two 16-token pages (each with at least one token in the context, starting at positions
+    // pos0 and pos1) in one online-softmax step: their QK^T chains run side by side and the
+    // running max, the rescale and its factor shuffles are taken once for the 32 tokens.
+    __device__ __forceinline__ void page_pair(uint8_t* kp0, uint8_t* vp0, int nv0, int pos0, uint8_t* kp1,
+                                              uint8_t* vp1, int nv1, int pos1, float scale_log2, int lane) {
+        static_assert(BS == 16, "pairs of one-sub-tile pages");
+        const int t = lane & 3;
+        const int j = lane >> 3, r8 = lane & 7;
+        zero_tail(vp0, nv0, lane);
+        zero_tail(vp1, nv1, lane);
+        const uint32_t kb0 = smem_addr(kp0), kb1 = smem_addr(kp1);
+        const uint32_t vb0 = smem_addr(vp0), vb1 = smem_addr(vp1);
+        // ---- S = Q K^T: page 0 tokens 0-7, 8-15, page 1 tokens 0-7, 8-15 ----
+        float s[4][4];
+#pragma unroll
+        for (int n = 0; n < 4; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
+        const int row = (j >> 1) * 8 + r8;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+            uint32_t b0[4], b1[4];
+            ldmatrix_x4(b0, kb0 + swz_offset<T, BS>(row, kk * 16 + (j & 1) * 8));
+            ldmatrix_x4(b1, kb1 + swz_offset<T, BS>(row, kk * 16 + (j & 1) * 8));
+            Mma<T>::run(s[0], qa[kk][0], 0u, qa[kk][1], 0u, b0[0], b0[1]);
+            Mma<T>::run(s[1], qa[kk][0], 0u, qa[kk][1], 0u, b0[2], b0[3]);
+            Mma<T>::run(s[2], qa[kk][0], 0u, qa[kk][1], 0u, b1[0], b1[1]);
+            Mma<T>::run(s[3], qa[kk][0], 0u, qa[kk][1], 0u, b1[2], b1[3]);
+        }
+        // ---- online softmax for row g over tokens 2t, 2t+1, 8+2t, 9+2t of both pages ----
+        const int nr0 = CAUSAL ? min(nv0, lim - pos0 + 1) : nv0;
+        const int nr1 = CAUSAL ? min(nv1, lim - pos1 + 1) : nv1;
+        float x[8];
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int nr = h ? nr1 : nr0;
+            x[4 * h + 0] = (2 * t < nr) ? s[2 * h][0] * scale_log2 : -INFINITY;
+            x[4 * h + 1] = (2 * t + 1 < nr) ? s[2 * h][1] * scale_log2 : -INFINITY;
+            x[4 * h + 2] = (8 + 2 * t < nr) ? s[2 * h + 1][0] * scale_log2 : -INFINITY;
+            x[4 * h + 3] = (9 + 2 * t < nr) ? s[2 * h + 1][1] * scale_log2 : -INFINITY;
+        }
+        float mx = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])), fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+        const float m_new = fmaxf(m, mx);
+        const float m_ref = (CAUSAL && m_new == -INFINITY) ? 0.f : m_new;
+        const float alpha = exp2f(m - m_ref);
+        float r[8];
+        uint32_t pb[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            pb[e] = Mma<T>::pack(exp2f(x[2 * e] - m_ref), exp2f(x[2 * e + 1] - m_ref), r[2 * e], r[2 * e + 1]);
+        l = l * alpha + (((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7])));
+        m = m_new;
+        const float a_lo = __shfl_sync(0xffffffffu, alpha, (2 * t) * 4);
+        const float a_hi = __shfl_sync(0xffffffffu, alpha, (2 * t + 1) * 4);
+        // ---- O^T += V^T P^T over both pages ----
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+            o[mt][0] *= a_lo;
+            o[mt][1] *= a_hi;
+            o[mt][2] *= a_lo;
+            o[mt][3] *= a_hi;
+            uint32_t af[4], ag[4];
+            ldmatrix_x4_trans(af, vb0 + swz_offset<T, BS>(row, mt * 16 + (j & 1) * 8));
+            ldmatrix_x4_trans(ag, vb1 + swz_offset<T, BS>(row, mt * 16 + (j & 1) * 8));
+            Mma<T>::run(o[mt], af[0], af[1], af[2], af[3], pb[0], pb[1]);
+            Mma<T>::run(o[mt], ag[0], ag[1], ag[2], ag[3], pb[2], pb[3]);
+        }
+    }
+
     // Complete the per-head denominators (sum over the quad); call once after a unit's last page.
     __device__ __forceinline__ void finish() {
         l += __shfl_xor_sync(0xffffffffu, l, 1);
@@ -860,7 +942,9 @@ struct SimtConsumer {
 
 // ------------------------------------------------------------------------------------------
 template <typename T, int D, int BS, bool MMA, int GMAX, bool CAUSAL>
-__global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (DecodeCfg<T, D, BS, MMA, GMAX>::kMinBlocks))
+__global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
+                                  ((MMA && CAUSAL && BS == 16 && D <= 128) ? 3
+                                                                           : DecodeCfg<T, D, BS, MMA, GMAX>::kMinBlocks))
     paged_decode_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
                         const DecodeArgs a) {
     using C = DecodeCfg<T, D, BS, MMA, GMAX>;
@@ -996,7 +1080,37 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads, (Dec
             }
             // without row split the warps share the pages round-robin; with it a warp whose
             // chunk is empty (fewer than four chunks) takes no part
-            for (int i = rs ? (cgc > 0 ? 0 : npages) : warp; i < npages; i += rs ? 1 : C::kNW) {
+            int i0 = rs ? (cgc > 0 ? 0 : npages) : warp;
+            if constexpr (CAUSAL && BS == 16) {
+                // Row split: every warp consumes every page, two at a time (one softmax step
+                // per 32 tokens); an odd last page goes through the loop below.
+                if (rs) {
+                    for (; i0 + 1 < npages; i0 += 2) {
+                        const int s0 = i0 % C::kNSlot, s1 = (i0 + 1) % C::kNSlot;
+                        const bool got = mbar_wait_bounded(&full[s0], (i0 / C::kNSlot) & 1, a.err, flags) &&
+                                         mbar_wait_bounded(&full[s1], ((i0 + 1) / C::kNSlot) & 1, a.err, flags);
+                        if (!__all_sync(0xffffffffu, got)) {
+                            i0 = npages;
+                            break;
+                        }
+                        const int nv0 = min(BS, L - (first + i0) * BS), nv1 = min(BS, L - (first + i0 + 1) * BS);
+                        uint8_t* kp0 = ring + s0 * C::kSlotBytes;
+                        uint8_t* kp1 = ring + s1 * C::kSlotBytes;
+                        if (i0 == i_tok)
+                            append_token<T, D, BS>(a, b, kvh, hc, nblk - 1, kp0, kp0 + C::kPageBytes, nv0, lane);
+                        if (i0 + 1 == i_tok)
+                            append_token<T, D, BS>(a, b, kvh, hc, nblk - 1, kp1, kp1 + C::kPageBytes, nv1, lane);
+                        cons.page_pair(kp0, kp0 + C::kPageBytes, nv0, (first + i0) * BS, kp1, kp1 + C::kPageBytes,
+                                       nv1, (first + i0 + 1) * BS, a.scale_log2, lane);
+                        __syncwarp();
+                        if (lane == 0) {
+                            mbar_arrive(&empty[s0]);
+                            mbar_arrive(&empty[s1]);
+                        }
+                    }
+                }
+            }
+            for (int i = i0; i < npages; i += rs ? 1 : C::kNW) {
                 const int s = i % C::kNSlot;
                 const bool got = mbar_wait_bounded(&full[s], (i / C::kNSlot) & 1, a.err, flags);
                 if (!__all_sync(0xffffffffu, got)) break;

@@ -1839,6 +1839,17 @@ constexpr int kLeanMergeBatch = 8;  // records whose loads a thread keeps in fli
 // this grid starts only once every decode CTA has passed its own wait for the grids
 // before it.  Every thread merges its own float4 columns of o~ over all records on its
 // own: no barriers, all loads of a batch of records issued before any is used.
+// Merge launch of a lean decode of `grid` CTAs: one CTA per unit, or, when units outnumber the
+// decode's consumer warps, one per boundary between two warps' shares (a unit is cut only at
+// such a boundary).  Sets the merge's fields of m; returns its grid size.
+inline int lean_merge_setup(DecodeArgs& m, int grid) {
+    const long long units = (long long)m.num_seqs * m.num_kv_heads * m.head_chunks;
+    const long long warps = (long long)grid * m.lean_warps_per_cta;
+    m.lean_grid = grid;
+    m.lean_merge_by_boundary = units > warps ? 1 : 0;
+    return (int)(m.lean_merge_by_boundary ? (warps > 1 ? warps - 1 : 1) : units);
+}
+
 template <typename T, int D, int H, int BS>
 __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_merge_kernel(const DecodeArgs a) {
     constexpr int kOOff = ((2 * H + 3) / 4) * 4;
@@ -1848,33 +1859,72 @@ __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_me
     griddep_launch_dependents();  // the next grid waits for this one's completion itself
     const int tid = threadIdx.x;
     const int upb = a.num_kv_heads * a.head_chunks;
-    const int u = blockIdx.x;
-    const int b = u / upb, uu = u - b * upb;
     const int B = a.num_seqs;
     const int l_cap = a.max_blocks * BS;
-
-    // pages per sequence (clamped like the decode), their total, and the prefix up to b
-    int before = 0, all = 0;
-    for (int s = tid; s < B; s += kLeanMergeThreads) {
+    const int warps = a.lean_grid * a.lean_warps_per_cta;
+    auto pages_of = [&](int s) {  // pages of sequence s, its length clamped like the decode's
         int L = __ldg(a.context_lens + s);
         L = L < 0 ? 0 : (L > l_cap ? l_cap : L);
-        const int n = (L + BS - 1) / BS;
-        all += n;
-        if (s < b) before += n;
-        if (s == b) seq_before[1] = n;
+        return (L + BS - 1) / BS;
+    };
+
+    // This CTA's unit (b, uu): its sequence's page count nb, the pages of the sequences before
+    // it (pre_b) and the total tot.  One CTA per unit, or, when units outnumber the decode's
+    // warps, one per boundary w = blockIdx.x + 1 between the shares of warps w - 1 and w: the
+    // CTA takes the unit holding the boundary's first page and merges it only if this is the
+    // first boundary inside it (so every cut unit is merged once, with far fewer CTAs).
+    int b, uu, nb, pre_b, tot, q;
+    bool skip = false;
+    if (!a.lean_merge_by_boundary) {
+        b = blockIdx.x / upb;
+        uu = blockIdx.x - b * upb;
+        int before = 0, all = 0;
+        for (int s = tid; s < B; s += kLeanMergeThreads) {
+            const int n = pages_of(s);
+            all += n;
+            if (s < b) before += n;
+            if (s == b) seq_before[1] = n;
+        }
+        block_exclusive_scan(all, warp_sums, kLeanMergeThreads / 32, &tot);
+        __syncthreads();
+        block_exclusive_scan(before, warp_sums, kLeanMergeThreads / 32, &pre_b);
+        __syncthreads();
+        nb = seq_before[1];
+        q = (tot * upb + warps - 1) / warps;
+    } else {
+        // contiguous runs of sequences per thread, so that a thread's scan base is their prefix
+        const int chunk = (B + kLeanMergeThreads - 1) / kLeanMergeThreads;
+        const int s0 = min(B, tid * chunk), s1 = min(B, s0 + chunk);
+        int mine = 0;
+        for (int s = s0; s < s1; ++s) mine += pages_of(s);
+        if (tid == 0) seq_before[0] = -1;
+        int run = block_exclusive_scan(mine, warp_sums, kLeanMergeThreads / 32, &tot);
+        __syncthreads();
+        q = (tot * upb + warps - 1) / warps;
+        const int P = (blockIdx.x + 1) * q;  // first page of warp blockIdx.x + 1
+        for (int s = s0; s < s1; ++s) {
+            const int n = pages_of(s);
+            if (P >= run * upb && P < (run + n) * upb) {
+                seq_before[0] = s;
+                seq_before[1] = n;
+                warp_sums[0] = run;  // (the scan is done with warp_sums)
+            }
+            run += n;
+        }
+        __syncthreads();
+        b = seq_before[0];
+        nb = seq_before[1];
+        pre_b = warp_sums[0];
+        skip = b < 0;
+        if (!skip) {
+            uu = (P - pre_b * upb) / nb;
+            const int first = pre_b * upb + uu * nb;
+            skip = first == P || first / q + 1 != (int)blockIdx.x + 1;
+        }
     }
-    int tot = 0, pre_b = 0;
-    block_exclusive_scan(all, warp_sums, kLeanMergeThreads / 32, &tot);
-    __syncthreads();
-    block_exclusive_scan(before, warp_sums, kLeanMergeThreads / 32, &pre_b);
-    __syncthreads();
-    const int nb = seq_before[1];
-    const int total = tot * upb;
-    const int warps = a.lean_grid * a.lean_warps_per_cta;
-    const int q = (total + warps - 1) / warps;
-    const int first = pre_b * upb + uu * nb;
+    const int first = skip ? 0 : pre_b * upb + uu * nb;
     const int w_lo = q > 0 ? first / q : 0, w_hi = q > 0 ? (first + nb - 1) / q : 0;
-    if (nb == 0 || q <= 0 || w_lo == w_hi) {
+    if (skip || nb == 0 || q <= 0 || w_lo == w_hi) {
         // Nothing to merge (the decode kernel finished the unit).  Every CTA still waits
         // for the decode grid before it ends: a grid that follows this one waits only for
         // this grid, so this grid must not end before the decode has.
@@ -2066,11 +2116,9 @@ struct DecodeKernel {
                            LC::smem_bytes(num_seqs), stream, k, v, a);
             if (e != cudaSuccess) return e;
             DecodeArgs m = a;
-            m.lean_grid = grid;
-            // one CTA per unit
-            return launch_pdl(lean_merge_kernel<T, D, LC::kHeads, BS>,
-                              dim3(a.num_seqs * a.num_kv_heads * a.head_chunks), dim3(kLeanMergeThreads), 0, stream,
-                              m);
+            const int mgrid = lean_merge_setup(m, grid);
+            return launch_pdl(lean_merge_kernel<T, D, LC::kHeads, BS>, dim3(mgrid), dim3(kLeanMergeThreads), 0,
+                              stream, m);
         } else {
             return launch_pdl(paged_decode_kernel<T, D, BS, MMA, GMAX, CAUSAL>, dim3(grid), dim3(C::kThreads), C::kSmemBytes,
                               stream, k, v, a);
@@ -2140,9 +2188,9 @@ struct DecodeKernelF8 {
                        k, v, a);
         if (e != cudaSuccess) return e;
         DecodeArgs m = a;
-        m.lean_grid = grid;
-        return launch_pdl(lean_merge_kernel<T, D, LC::kHeads, BS>, dim3(a.num_seqs * a.num_kv_heads * a.head_chunks),
-                          dim3(kLeanMergeThreads), 0, stream, m);
+        const int mgrid = lean_merge_setup(m, grid);
+        return launch_pdl(lean_merge_kernel<T, D, LC::kHeads, BS>, dim3(mgrid), dim3(kLeanMergeThreads), 0, stream,
+                          m);
     }
 };
 

@@ -47,6 +47,7 @@ struct DecodeArgs {
     float scale_log2;            // softmax scale * log2(e)
     int lean_warps_per_cta;      // consumer warps per lean CTA
     int lean_grid;               // CTAs of the lean decode launch (set for the merge kernel)
+    int lean_merge_by_boundary;  // merge grid: one CTA per boundary between warp shares, not per unit
 };
 
 // Arguments of the split-KV merge kernel.

@@ -386,3 +386,26 @@ def test_qwen_layer_fp8_append_full_size():
     ref = oracle.decode_fp8(inp.q, inp.dtype, kc, vc, ks, vs, inp.block_tables, inp.context_lens, inp.scale, rows)
     assert_decode_close(np.stack([got[b, h] for b, h in rows]), ref, inp.dtype)
     pa.check_error()
+
+
+@pytest.mark.parametrize("layout", ["separate", "interleaved"])
+def test_decode_fp8_more_units_than_warps(layout):
+    """More (sequence, kv head) units than the lean decode has consumer warps (300 x 8 = 2400 units
+    against 152 SMs x 3 CTAs x 4 warps): the merge then runs one CTA per boundary between two warps'
+    shares, merging each cut unit once; every output row matches the oracle."""
+    rng = np.random.default_rng(77)
+    lens = rng.integers(1, 200, 300).astype(np.int32)
+    lens[::37] = 16  # units that end exactly on a page edge
+    q, kc, vc, ks, vs, bt, lens = _case(78, lens, 8, 8, 16, "f16")
+    assert len(lens) * 8 > torch.cuda.get_device_properties(0).multi_processor_count * 3 * 4
+    dks, dvs = torch.from_numpy(ks).cuda(), torch.from_numpy(vs).cuda()
+    dq, dbt, dl = to_device(q, "f16"), torch.from_numpy(bt).cuda(), torch.from_numpy(lens).cuda()
+    if layout == "interleaved":
+        got = pa.decode_fp8(dq, torch.from_numpy(np.ascontiguousarray(np.stack([kc, vc], axis=2))).cuda(), None, dks,
+                            dvs, dbt, dl)
+    else:
+        got = pa.decode_fp8(dq, torch.from_numpy(kc).cuda(), torch.from_numpy(vc).cuda(), dks, dvs, dbt, dl)
+    torch.cuda.synchronize()
+    ref = oracle.decode_fp8(q, "f16", kc, vc, ks, vs, bt, lens, 1 / np.sqrt(128))
+    assert_decode_close(to_f64(got), ref, "f16")
+    pa.check_error()

@@ -279,10 +279,13 @@ size_t pa_decode_fp8_workspace_size(int num_seqs, int num_heads, int num_kv_head
                                     int max_blocks_per_seq, int dtype);
 /*
  * pa_decode_fp8_append — pa_decode_fp8 with the step's write folded in, as pa_decode_append: the
- * new token of sequence b (new_key / new_value [num_seqs, H_kv, head_dim] in `dtype`, 16-byte
- * aligned) is quantised with the scales of the block that receives it and stored at the slot the
- * block table gives position L_b - 1, then attended.  Same cache bytes and output bits as
- * pa_write_kv_fp8 at those slots followed by pa_decode_fp8.  value_cache NULL: interleaved layout.
+ * new token of sequence b (new_key / new_value [num_seqs, H_kv, head_dim] in `dtype`, device,
+ * 16-byte aligned, read only) is quantised with the scales of the block that receives it and
+ * stored at the slot the block table gives position L_b - 1, then attended.  Same cache bytes and
+ * output bits as pa_write_kv_fp8 at those slots followed by pa_decode_fp8 with the same workspace.
+ * value_cache NULL: interleaved layout.  A sequence with L_b == 0 writes nothing; a block id
+ * outside the pool skips the store and sets PA_ERR_BAD_TABLE in the device error word; a NULL or
+ * misaligned new_key / new_value, k_scale or v_scale returns PA_ERR_INVALID_ARG.
  */
 int pa_decode_fp8_append(void* out, const void* query, const void* new_key, const void* new_value, void* key_cache,
                          void* value_cache, const float* k_scale, const float* v_scale, const int32_t* block_tables,

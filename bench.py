@@ -388,8 +388,9 @@ def build_batch(workload: str, seed: int):
     return gen(seed)
 
 
-def prefix_batch(workload: str, seed: int):
-    """The prefix-sharing workload built through the product block pool.
+def prefix_batch(workload: str, seed: int, model: bool = False):
+    """The prefix-sharing workload built through the product block pool (``model``: the
+    oracle's allocator model, for the reference arm; both give the same tables).
 
     A parent appends the shared prefix, 63 forks share it; every sequence then
     appends its tail but the last token (copy-on-write pairs are copied, tail
@@ -398,13 +399,12 @@ def prefix_batch(workload: str, seed: int):
     decode inputs, tables, lengths, new-token slots, the number of copy-on-write
     copies, and the bytes of the distinct pages the decode reads.
     """
-    import paged_kv_cache_129_gb300 as pa
     from paged_kv_cache_129_gb300 import workloads as wl
 
     prefix = 2056 if workload == "prefix_cow_2056" else 2048
     w = wl.prefix_cow(seed, prefix_len=prefix)
     bs = w.block_size
-    pool = pa.BlockPool(w.num_blocks, bs, free_order=np.random.default_rng(12345).permutation(w.num_blocks))
+    pool = make_pool(w.num_blocks, bs, np.random.default_rng(12345).permutation(w.num_blocks), model)
     parent = pool.create()
     for _ in range(prefix):
         pool.append(parent)
@@ -442,16 +442,64 @@ def prefix_batch(workload: str, seed: int):
     return inp, tables, lens, np.asarray(slots, dtype=np.int64), n_cow, unique_bytes
 
 
-def pool_tables(inp):
+class _ModelPool:
+    """The oracle's allocator model behind the product pool's method names (reference arm only)."""
+
+    def __init__(self, num_blocks: int, block_size: int, free_order):
+        from oracle.block_pool import SequencePool
+
+        self.m = SequencePool(num_blocks, block_size, free_order=free_order)
+
+    def create(self):
+        return self.m.create()
+
+    def fork(self, sid):
+        return self.m.fork(sid)
+
+    def append(self, sid):
+        res = self.m.append(sid)
+        return res.slot, res.cow
+
+    def append_batch(self, ids):
+        slots, pairs = [], []
+        for sid in ids:
+            slot, pair = self.append(sid)
+            slots.append(slot)
+            if pair:
+                pairs.append(pair)
+        return np.asarray(slots, dtype=np.int64), pairs
+
+    def block_tables(self, ids, width):
+        return self.m.block_tables(ids, width)
+
+    def swap_to(self, dst, sid):
+        new_sid, pairs = self.m.swap_to(dst.m, sid)
+        return new_sid, np.asarray(pairs, dtype=np.int64).reshape(-1, 2)
+
+    def check_invariants(self):
+        bad = self.m.invariants()
+        assert not bad, bad
+
+
+def make_pool(num_blocks: int, block_size: int, free_order, model: bool = False):
+    """The product block pool, or (``model``) the oracle's allocator model with the same free order."""
+    if model:
+        return _ModelPool(num_blocks, block_size, free_order)
+    import paged_kv_cache_129_gb300 as pa
+
+    return pa.BlockPool(num_blocks, block_size, free_order=free_order)
+
+
+def pool_tables(inp, model: bool = False):
     """Block tables and new-token slots from the host block pool (a shuffled free list).
 
     Each sequence appends its L-1 context tokens, then the step's new token is
-    appended for all sequences at once; the decode attends over L tokens.
+    appended for all sequences at once; the decode attends over L tokens.  With
+    ``model`` the oracle's allocator model stands in for the product pool (the
+    reference arm maps no product code); both give the same tables and slots.
     """
-    import paged_kv_cache_129_gb300 as pa
-
     rng = np.random.default_rng(12345)
-    pool = pa.BlockPool(inp.num_blocks, inp.block_size, free_order=rng.permutation(inp.num_blocks))
+    pool = make_pool(inp.num_blocks, inp.block_size, rng.permutation(inp.num_blocks), model)
     ids = [pool.create() for _ in range(inp.num_seqs)]
     q_len = inp.q.shape[1] if inp.q.ndim == 4 else 1
     for sid, L in zip(ids, inp.context_lens):
@@ -976,25 +1024,24 @@ def run_layers(args, rank: int, world: int, local_rank: int) -> None:
 
 
 def swap_plan(seed: int, steps: int, num_blocks: int = 20000, num_seqs: int = 64, group: int = SWAP_GROUP,
-              block_size: int = 16):
-    """Host side of the swap workload (no GPU).  Sequences are built through the product block pool; the
+              block_size: int = 16, model: bool = False):
+    """Host side of the swap workload (no GPU).  Sequences are built through the product block pool (the
+    oracle's allocator model with ``model``, for the reference arm: the same pairs); the
     groups of ``group`` sequences take turns: step k swaps group k out to host pool k % 2 and group k - 1
     back in from host pool (k - 1) % 2, so the two copies of a step can run at once.  Per step the pool
     decides the swap-in first (its device blocks come from blocks free before this step's swap-out
     releases any) and then the swap-out (into the other host pool), so the two copies touch disjoint
     blocks on both sides.  Returns (per-step (out pairs, out host pool, in pairs, in host pool), host pool
     size, seconds of pool work per step, lengths)."""
-    import paged_kv_cache_129_gb300 as pa
-
     assert 2 * group <= num_seqs
     rng = np.random.default_rng(seed)
     lens = rng.integers(512, 4097, size=num_seqs)
-    dev = pa.BlockPool(num_blocks, block_size, free_order=rng.permutation(num_blocks))
+    dev = make_pool(num_blocks, block_size, rng.permutation(num_blocks), model)
     ids = [dev.create() for _ in range(num_seqs)]
     for t in range(int(lens.max())):
         dev.append_batch([sid for sid, n in zip(ids, lens) if n > t])
     host_blocks = int(np.sort((lens + block_size - 1) // block_size)[-group:].sum())
-    hosts = [pa.BlockPool(host_blocks, block_size), pa.BlockPool(host_blocks, block_size)]
+    hosts = [make_pool(host_blocks, block_size, np.arange(host_blocks), model) for _ in range(2)]
     away = {}  # sequence index -> id in its host pool
     plan, t_pool = [], 0.0
     none = np.zeros((0, 2), np.int64)
@@ -1217,7 +1264,7 @@ def run_reference(args, rank: int, world: int) -> None:
     import oracle
 
     if args.workload == "swap_qwen":
-        plan, host_blocks, _, _ = swap_plan(rank_seed(args.seed, 0), 2)
+        plan, host_blocks, _, _ = swap_plan(rank_seed(args.seed, 0), 2, model=True)
         _, _, in_p, _ = plan[1]
         out_p = plan[1][0]
         probe = time_swap_oracle((out_p[:64], None, in_p[:64], None), host_blocks, budget_s=0.5)
@@ -1245,10 +1292,10 @@ def run_reference(args, rank: int, world: int) -> None:
         print(json.dumps(line), flush=True)
         return
     if args.workload.startswith("prefix_cow"):
-        inp, tables, lens, slots, _, _ = prefix_batch(args.workload, rank_seed(args.seed, 0))
+        inp, tables, lens, slots, _, _ = prefix_batch(args.workload, rank_seed(args.seed, 0), model=True)
     else:
         inp = build_batch(args.workload, rank_seed(args.seed, 0))
-        tables, lens, slots = pool_tables(inp)
+        tables, lens, slots = pool_tables(inp, model=True)
     inp.block_tables = tables
     q_len = inp.q.shape[1] if inp.q.ndim == 4 else 1
     if slots is not None:

@@ -119,3 +119,47 @@ def test_swap_plan_moves_each_group_out_and_back():
         assert set(in_p[:, 1].tolist()).isdisjoint(out_p[:, 0].tolist())
         assert hi != ho
     assert pool_s >= 0
+
+
+def test_reference_arm_tables_come_from_the_allocator_model_and_match_the_product_pool():
+    # The reference arm builds tables, slots, copy-on-write pairs and swap pairs with the oracle's
+    # allocator model; with the same free order they equal the product pool's, so both arms time the
+    # same workload.
+    import paged_kv_cache_129_gb300 as pa
+    from paged_kv_cache_129_gb300 import workloads as wl
+
+    pa.build()
+    inp = wl.make_decode_inputs("v", context_lens=[5, 16, 40, 33, 2], num_heads=8, num_kv_heads=2, head_dim=64,
+                                block_size=16, dtype="bf16", pool_slack=0.5, seed=2, with_new_token=True, q_len=2)
+    for got, want in zip(bench.pool_tables(inp, model=True), bench.pool_tables(inp)):
+        assert np.array_equal(got, want)
+    for workload in ("prefix_cow", "prefix_cow_2056"):
+        m = bench.prefix_batch(workload, 0, model=True)
+        p = bench.prefix_batch(workload, 0)
+        for i in (1, 2, 3):
+            assert np.array_equal(m[i], p[i])
+        assert m[4] == p[4] and m[5] == p[5]
+        assert np.array_equal(m[0].key_cache, p[0].key_cache) and np.array_equal(m[0].value_cache, p[0].value_cache)
+    mp_, mh, _, ml = bench.swap_plan(seed=3, steps=3, num_blocks=2100, num_seqs=8, group=3, model=True)
+    pp, ph, _, pl = bench.swap_plan(seed=3, steps=3, num_blocks=2100, num_seqs=8, group=3)
+    assert mh == ph and np.array_equal(ml, pl)
+    for a, b in zip(mp_, pp):
+        assert np.array_equal(a[0], b[0]) and a[1] == b[1] and np.array_equal(a[2], b[2]) and a[3] == b[3]
+
+
+def test_reference_arm_setup_maps_no_product_library():
+    # Built with the allocator model, the reference arm's inputs need nothing from the CUDA library.
+    import subprocess
+    import sys
+
+    code = ("import bench, numpy as np\n"
+            "from paged_kv_cache_129_gb300 import workloads as wl\n"
+            "inp = wl.make_decode_inputs('v', context_lens=[5, 40], num_heads=4, num_kv_heads=2, head_dim=64,"
+            " block_size=16, dtype='bf16', pool_slack=0.5, seed=2, with_new_token=True)\n"
+            "bench.pool_tables(inp, model=True)\n"
+            "bench.prefix_batch('prefix_cow_2056', 0, model=True)\n"
+            "bench.swap_plan(seed=3, steps=2, num_blocks=2100, num_seqs=8, group=3, model=True)\n"
+            "maps = open('/proc/self/maps').read()\n"
+            "assert 'libpagedkv' not in maps, 'product library mapped'\n")
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    subprocess.run([sys.executable, "-c", code], cwd=root, check=True, timeout=300)

@@ -192,3 +192,53 @@ def test_blocks_needed_equals_the_blocks_the_appends_take():
                     pool.append(sid)
             assert free - pool.num_free() == need
             assert pool.invariants() == []
+
+
+def test_slots_for_positions_hand_case():
+    # MiniPaged-Qwen, section 8.1: the slot of a token is its physical block times the block size plus
+    # its offset in that block.  Table [7, 3] with 16-token blocks: positions 0 and 15 sit in block 7
+    # (slots 112 and 127), positions 16 and 19 in block 3 (slots 48 and 51).
+    from oracle import slots_for_positions
+
+    tables = np.array([[7, 3], [5, -1]], dtype=np.int32)
+    got = slots_for_positions(tables, [0, 0, 0, 0, 1, 1], [0, 15, 16, 19, 0, 9], 16)
+    assert got.tolist() == [112, 127, 48, 51, 80, 89]
+    assert got.dtype == np.int64
+
+
+def test_slots_for_positions_agree_with_the_allocator_model():
+    # The slot the allocator model's append hands back for a token, and the block and offset where
+    # the model stores it, are what slots_for_positions derives from the table afterwards -- through
+    # forks, copy-on-write tails and releases (the vLLM/PagedAttention page's BlockPool simulation).
+    from oracle import slots_for_positions
+
+    rng = np.random.default_rng(11)
+    bs = 4
+    pool = SequencePool(600, bs, free_order=rng.permutation(600))
+    live = [pool.create()]
+    checked = 0
+    for step in range(800):
+        op = rng.integers(0, 8)
+        if op == 0:
+            live.append(pool.create())
+        elif op == 1:
+            live.append(pool.fork(live[rng.integers(len(live))]))
+        elif op == 2 and len(live) > 1:
+            pool.release(live.pop(rng.integers(len(live))))
+        elif pool.num_free() > 2:
+            sid = live[rng.integers(len(live))]
+            res = pool.append(sid, (sid, step))
+            pos = pool.lens[sid] - 1
+            tables, _ = pool.block_tables([sid], max(1, len(pool.tables[sid])))
+            assert slots_for_positions(tables, [0], [pos], bs)[0] == res.slot
+            checked += 1
+    assert checked > 300
+    # every stored token of every live sequence sits at the slot its position maps to
+    width = max(len(pool.tables[s]) for s in live) or 1
+    tables, lens = pool.block_tables(live, width)
+    for row, sid in enumerate(live):
+        tokens = pool.pool.read(pool.tables[sid])
+        positions = list(range(int(lens[row])))
+        slots = slots_for_positions(tables, [row] * len(positions), positions, bs)
+        for pos, slot in zip(positions, slots):
+            assert pool.pool.data[int(slot) // bs][int(slot) % bs] == tokens[pos]

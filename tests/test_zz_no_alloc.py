@@ -2,8 +2,10 @@
 
 Each case runs two calls in a row through the static-scratch entry point
 (different queries, so the second call cannot lean on what the first left in
-the scratch) and compares both with pa_decode given a caller-allocated
-workspace.  The file runs last on purpose, after every other GPU test has used
+the scratch).  Both outputs are checked against the CPU oracle at the decode
+tolerance, and must be bit-identical to pa_decode given a caller-allocated
+workspace of the same size (the same plan, so the same arithmetic in the same
+order).  The file runs last on purpose, after every other GPU test has used
 the library, and also passes on its own in a fresh process.
 """
 import ctypes
@@ -12,6 +14,7 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
 import paged_kv_cache_129_gb300 as pa
 from paged_kv_cache_129_gb300 import workloads as wl
 from helpers import TORCH_DTYPE, assert_decode_close, to_device, to_f64
@@ -37,13 +40,17 @@ def need_bytes(inp):
                                     inp.max_blocks_per_seq, TORCH_DTYPE[inp.dtype])
 
 
-def with_workspace(q, dev, inp):
+def with_workspace(q, dev, inp, raw=False):
     ws_bytes = need_bytes(inp)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device="cuda") if ws_bytes else None
     out = pa.decode(q, dev["kc"], dev["vc"], dev["bt"], dev["lens"], scale=inp.scale, workspace=ws)
     torch.cuda.synchronize()
     pa.check_error()
-    return to_f64(out)
+    return out if raw else to_f64(out)
+
+
+def bits(t):
+    return t.view(torch.int32 if t.dtype == torch.float32 else torch.int16)
 
 
 def alloc_count():
@@ -93,8 +100,13 @@ def test_two_calls_match_pa_decode(name):
     torch.cuda.synchronize()
     assert alloc_count() == before
     pa.check_error()
-    assert_decode_close(to_f64(out1), with_workspace(q1, dev, inp), inp.dtype)
-    assert_decode_close(to_f64(out2), with_workspace(q2, dev, inp), inp.dtype)
+    inp2 = make_case(spec, seed=202)
+    for out, q, case in ((out1, q1, inp), (out2, q2, inp2)):
+        # against the CPU oracle, at the decode tolerance
+        case.key_cache, case.value_cache, case.block_tables = inp.key_cache, inp.value_cache, inp.block_tables
+        assert_decode_close(to_f64(out), oracle.decode_inputs(case), inp.dtype)
+        # and bit for bit what pa_decode computes with a workspace of the same size (the same plan)
+        assert torch.equal(bits(out), bits(with_workspace(q, dev, inp, raw=True)))
 
 
 def test_sizes_beyond_the_static_scratch_are_refused():

@@ -188,8 +188,12 @@ int pa_swap_blocks(void* dst_key_cache, void* dst_value_cache, const void* src_k
  *                 small merge kernel that combines the contexts cut at share
  *                 boundaries.  A smaller workspace selects partitioned
  *                 contexts (a decode kernel plus a merge kernel).  No
- *                 initialisation is needed.  256-byte aligned.  Calls that
- *                 share a workspace must not overlap on the GPU.
+ *                 initialisation is needed: the lean merge tells this call's
+ *                 partial records from stale ones by a per-call 64-bit epoch,
+ *                 and clears every flag it consumed, so a call captured in a
+ *                 CUDA graph (which replays one epoch) stays correct on every
+ *                 replay.  256-byte aligned.  Calls that share a workspace
+ *                 must not overlap on the GPU.
  * Requires num_heads % num_kv_heads == 0, head_dim in {64, 128, 256},
  * block_size in {16, 32} (f32: head_dim in {64, 128}), 16-byte aligned caches,
  * 4-byte aligned query/out, num_blocks * num_kv_heads * block_size < 2^31.
@@ -342,6 +346,20 @@ int pa_decode_make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_
  */
 size_t pa_decode_workspace_size(int num_seqs, int num_heads, int num_kv_heads, int head_dim,
                                 int block_size, int max_blocks_per_seq, int dtype);
+
+/*
+ * Diagnostics of the bounded device waits (no counterpart on the pages).  Launches the
+ * split-KV merge of the lean schedule on its own, for the plan pa_decode would use with this
+ * workspace, as if the decode grid had published none of its partial records: the merge's
+ * wait for them can only run out.  Each merge CTA with a cut unit gives up after
+ * wait_limit_ns nanoseconds (1 .. 2e9), sets the timeout bit of the device error word
+ * (pa_check_error then returns PA_ERR_TIMEOUT) and writes nothing to out; the device stays
+ * usable.  Arguments as for pa_decode; PA_ERR_INVALID_ARG when these sizes do not take the
+ * lean schedule.  Asynchronous on `stream`.
+ */
+int pa_diag_merge_timeout(void* out, const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                          int head_dim, int block_size, int max_blocks_per_seq, int dtype, void* workspace,
+                          size_t workspace_bytes, unsigned long long wait_limit_ns, void* stream);
 
 /*
  * pa_decode without a caller workspace: the split-KV scratch comes from one

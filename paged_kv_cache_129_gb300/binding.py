@@ -94,6 +94,7 @@ _SIGNATURES = [
     ("pa_decode_make_plan", _I, [_I, _I, _I, _I, _I, _I, _I, _SZ, _I, _I, _I, ctypes.POINTER(DecodePlan)]),
     ("pa_decode_workspace_size", _SZ, [_I, _I, _I, _I, _I, _I, _I]),
     ("pa_decode_static_scratch", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
+    ("pa_diag_merge_timeout", _I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _SZ, ctypes.c_ulonglong, _P]),
     ("pa_stepper_create", _I, [_I, _P, _P, _P, ctypes.POINTER(_P)]),
     ("pa_stepper_destroy", None, [_P]),
     ("pa_stepper_set_slot", _I, [_P, _I, _P, _P, _SZ, _P, _P, _SZ]),
@@ -170,6 +171,20 @@ def _need(cond: bool, what: str) -> None:
 def _cuda(t: torch.Tensor, name: str) -> None:
     _need(t.is_cuda, f"{name} must be a CUDA tensor")
     _need(t.is_contiguous(), f"{name} must be contiguous")
+
+
+def diag_merge_timeout(out: torch.Tensor, context_lens: torch.Tensor, num_kv_heads: int, block_size: int,
+                       max_blocks_per_seq: int, workspace: torch.Tensor, wait_limit_ns: int, stream=None) -> None:
+    """``pa_diag_merge_timeout``: the lean merge alone, waiting for records no decode publishes, so that
+    its bounded wait runs out after ``wait_limit_ns`` (the device error word then reports a timeout)."""
+    for name, t in (("out", out), ("context_lens", context_lens), ("workspace", workspace)):
+        _cuda(t, name)
+    _need(out.dim() == 3, "out must be [B, H_q, d]")
+    b, hq, d = out.shape
+    _check(library().pa_diag_merge_timeout(out.data_ptr(), context_lens.data_ptr(), b, hq, num_kv_heads, d, block_size,
+                                           max_blocks_per_seq, _dtype_code(out), workspace.data_ptr(),
+                                           workspace.numel() * workspace.element_size(), int(wait_limit_ns),
+                                           _stream_ptr(stream, out.device)))
 
 
 def version() -> str:

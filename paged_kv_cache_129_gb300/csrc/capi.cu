@@ -726,6 +726,7 @@ int decode_impl(void* out, const void* query, const void* new_key, const void* n
     a.ws_part = p.schedule == kScheduleLean ? reinterpret_cast<float*>(ws + p.off_part) : nullptr;
     a.ws_flag = p.schedule == kScheduleLean ? reinterpret_cast<unsigned long long*>(ws + p.off_flag) : nullptr;
     a.epoch = p.schedule == kScheduleLean ? next_epoch() : 0;
+    a.wait_ns = kWaitLimitNs;
     a.new_key = new_key;
     a.new_value = new_key ? new_value : nullptr;
     a.key_cache = new_key ? const_cast<void*>(key_cache) : nullptr;
@@ -891,6 +892,52 @@ int pa_write_kv_fp8(const void* key, const void* value, void* key_cache, void* v
                    dev->error_word};
     cudaError_t e = write_kv_fp8_launch(a, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "pa_write_kv_fp8 launch");
+    return PA_OK;
+}
+
+int pa_diag_merge_timeout(void* out, const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
+                          int head_dim, int block_size, int max_blocks_per_seq, int dtype, void* workspace,
+                          size_t workspace_bytes, unsigned long long wait_limit_ns, void* stream) {
+    CallRange nvtx_range("pa_diag_merge_timeout");
+    clear_error();
+    if (num_seqs <= 0 || !out || !context_lens || !workspace)
+        return fail(PA_ERR_INVALID_ARG, "pa_diag_merge_timeout: needs num_seqs > 0, out, context_lens, workspace");
+    if (!aligned(workspace, 256) || !aligned(out, 4) || !aligned(context_lens, 4))
+        return fail(PA_ERR_INVALID_ARG, "pa_diag_merge_timeout: misaligned pointer");
+    if (wait_limit_ns == 0 || wait_limit_ns > kWaitLimitNs)
+        return fail(PA_ERR_INVALID_ARG, "pa_diag_merge_timeout: wait_limit_ns must be in (0, %llu]", kWaitLimitNs);
+    Plan p;
+    int st = make_plan(num_seqs, num_heads, num_kv_heads, head_dim, block_size, max_blocks_per_seq, dtype, true,
+                       workspace_bytes, 0, 0, PA_KERNEL_AUTO, &p);
+    if (st != PA_OK) return st;
+    if (p.schedule != kScheduleLean)
+        return fail(PA_ERR_INVALID_ARG, "pa_diag_merge_timeout: these sizes do not take the lean schedule");
+    DeviceState* dev = nullptr;
+    st = current_device_state(&dev);
+    if (st != PA_OK) return st;
+    DecodeArgs a{};
+    a.out = out;
+    a.context_lens = context_lens;
+    char* ws = static_cast<char*>(workspace);
+    a.ws_part = reinterpret_cast<float*>(ws + p.off_part);
+    a.ws_flag = reinterpret_cast<unsigned long long*>(ws + p.off_flag);
+    a.epoch = next_epoch();  // no decode grid publishes this epoch
+    a.wait_ns = wait_limit_ns;
+    a.lean_warps_per_cta = p.ki.lean_warps_per_cta;
+    a.err = dev->error_word;
+    a.num_seqs = num_seqs;
+    a.num_heads = num_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.group = num_heads / num_kv_heads;
+    a.q_len = 1;
+    a.rows = a.group;
+    a.head_chunks = p.head_chunks;
+    a.max_blocks = max_blocks_per_seq;
+    a.partition_pages = p.partition_pages;
+    CUtensorMap none{};
+    cudaError_t e = decode_launch(dtype, head_dim, block_size, p.dkind, p.gmax, kScheduleLeanMergeOnly, none, none, a,
+                                  (int)p.grid, num_seqs, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "pa_diag_merge_timeout: merge kernel launch");
     return PA_OK;
 }
 

@@ -1944,7 +1944,7 @@ __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_me
         if (ld_acquire_gpu(f) == a.epoch) continue;
         const unsigned long long start = global_timer_ns();
         while (ld_acquire_gpu(f) != a.epoch) {
-            if (gave_up || global_timer_ns() - start > kWaitLimitNs) {
+            if (gave_up || global_timer_ns() - start > a.wait_ns) {
                 if (!gave_up) atomicOr(a.err, kErrTimeout);
                 gave_up = 1;
                 break;
@@ -1957,6 +1957,10 @@ __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_me
         griddep_wait();
         return;
     }
+    // Every flag is read by this CTA alone: clear the ones it consumed, so that the next call on
+    // this workspace starts from zeros even if it reuses this call's epoch (a replayed capture).
+    for (int p = tid; p < n; p += kLeanMergeThreads)
+        a.ws_flag[(size_t)(w_lo + p) * 2 + (p == 0 ? slot0 : 0)] = 0ull;
     const int kvh = uu / a.head_chunks, hc = uu - kvh * a.head_chunks;
     const UnitRows rows{b, kvh, hc * H, a.q_len, a.group, a.num_heads};
     const int gc = min(H, a.rows - hc * H);
@@ -2111,10 +2115,12 @@ struct DecodeKernel {
         cudaError_t e = cudaGetDevice(&device);
         if (e != cudaSuccess) return e;
         if (!configure(device)) return cudaGetLastError();
-        if (schedule == kScheduleLean) {
-            e = launch_pdl(paged_decode_lean_kernel<T, D, BS, MMA, GMAX, CAUSAL>, dim3(grid), dim3(LC::kThreads),
-                           LC::smem_bytes(num_seqs), stream, k, v, a);
-            if (e != cudaSuccess) return e;
+        if (schedule == kScheduleLean || schedule == kScheduleLeanMergeOnly) {
+            if (schedule == kScheduleLean) {
+                e = launch_pdl(paged_decode_lean_kernel<T, D, BS, MMA, GMAX, CAUSAL>, dim3(grid), dim3(LC::kThreads),
+                               LC::smem_bytes(num_seqs), stream, k, v, a);
+                if (e != cudaSuccess) return e;
+            }
             DecodeArgs m = a;
             const int mgrid = lean_merge_setup(m, grid);
             return launch_pdl(lean_merge_kernel<T, D, LC::kHeads, BS>, dim3(mgrid), dim3(kLeanMergeThreads), 0,

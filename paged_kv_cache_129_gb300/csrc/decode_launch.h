@@ -19,6 +19,7 @@ struct DecodeArgs {
     float* ws_part;              // lean schedule: two partial records per consumer warp
     unsigned long long* ws_flag; // lean schedule: one flag per record, set to `epoch` when published
     unsigned long long epoch;    // lean schedule: a value no earlier call has used (never 0)
+    unsigned long long wait_ns;  // lean merge: bound of its wait for the partial records (ns)
     unsigned* err;               // device error word
     // Append mode (new_key != nullptr): the new token of sequence b, new_key/new_value
     // [B, Hkv, D], sits at position L_b - 1; the kernel copies it into its staged copy of
@@ -74,7 +75,8 @@ struct KernelInfo {
     int lean_max_seqs;
 };
 
-enum Schedule { kScheduleGrid = 0, kScheduleLean = 1 };
+// kScheduleLeanMergeOnly: the lean merge kernel alone (diagnostics of its bounded wait).
+enum Schedule { kScheduleGrid = 0, kScheduleLean = 1, kScheduleLeanMergeOnly = 2 };
 
 // kind: 1 = tensor-core (mma) kernel, 2 = CUDA-core kernel, 3 = tensor-core kernel with a causal bound
 // per row (multi-query decode; the CUDA-core kernel always has it); gmax: head-chunk width of the

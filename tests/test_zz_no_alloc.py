@@ -104,6 +104,7 @@ def test_two_calls_match_pa_decode(name):
     for out, q, case in ((out1, q1, inp), (out2, q2, inp2)):
         # against the CPU oracle, at the decode tolerance
         case.key_cache, case.value_cache, case.block_tables = inp.key_cache, inp.value_cache, inp.block_tables
+        case.context_lens = inp.context_lens
         assert_decode_close(to_f64(out), oracle.decode_inputs(case), inp.dtype)
         # and bit for bit what pa_decode computes with a workspace of the same size (the same plan)
         assert torch.equal(bits(out), bits(with_workspace(q, dev, inp, raw=True)))

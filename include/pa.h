@@ -362,6 +362,17 @@ int pa_diag_merge_timeout(void* out, const int32_t* context_lens, int num_seqs, 
                           size_t workspace_bytes, unsigned long long wait_limit_ns, void* stream);
 
 /*
+ * Diagnostics of the lean schedule's early set-up (no counterpart on the pages).  The lean
+ * decode reads the context lengths and the first block-table rows of every warp before it
+ * waits for the previous kernel in the stream, issues the first page loads from them as soon
+ * as the wait returns, and reads both again to check them; a CTA whose early reads differ
+ * (the previous kernel changed them) discards those pages and sets up again.  With on != 0
+ * every later lean decode of this process takes that second path in every CTA, so that tests
+ * can check it; results are the same either way.  Not for production use.
+ */
+void pa_diag_force_restart(int on);
+
+/*
  * pa_decode without a caller workspace: the split-KV scratch comes from one
  * fixed array of PA_STATIC_SCRATCH_BYTES compiled into the library (one copy
  * per device).  The method on the pages has no counterpart to this call; it is

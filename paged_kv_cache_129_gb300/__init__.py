@@ -24,6 +24,7 @@ from .binding import (  # noqa: F401
     decode_plan,
     decode_static_scratch,
     decode_workspace_size,
+    diag_force_restart,
     diag_merge_timeout,
     library,
     swap_blocks,

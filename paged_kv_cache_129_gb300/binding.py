@@ -94,6 +94,7 @@ _SIGNATURES = [
     ("pa_decode_make_plan", _I, [_I, _I, _I, _I, _I, _I, _I, _SZ, _I, _I, _I, ctypes.POINTER(DecodePlan)]),
     ("pa_decode_workspace_size", _SZ, [_I, _I, _I, _I, _I, _I, _I]),
     ("pa_decode_static_scratch", _I, [_P, _P, _P, _P, _P, _P, _I, _I, _I, _I, _I, _I, _I, _F, _I, _P]),
+    ("pa_diag_force_restart", None, [_I]),
     ("pa_diag_merge_timeout", _I, [_P, _P, _I, _I, _I, _I, _I, _I, _I, _P, _SZ, ctypes.c_ulonglong, _P]),
     ("pa_stepper_create", _I, [_I, _P, _P, _P, ctypes.POINTER(_P)]),
     ("pa_stepper_destroy", None, [_P]),
@@ -185,6 +186,11 @@ def diag_merge_timeout(out: torch.Tensor, context_lens: torch.Tensor, num_kv_hea
                                            max_blocks_per_seq, _dtype_code(out), workspace.data_ptr(),
                                            workspace.numel() * workspace.element_size(), int(wait_limit_ns),
                                            _stream_ptr(stream, out.device)))
+
+
+def diag_force_restart(on: bool) -> None:
+    """``pa_diag_force_restart``: make every later lean decode redo its early set-up (tests only)."""
+    library().pa_diag_force_restart(1 if on else 0)
 
 
 def version() -> str:

@@ -27,6 +27,7 @@ namespace pa {
 namespace {
 thread_local std::string g_message;
 constexpr int kMaxDevices = 64;
+std::atomic<int> g_force_restart{0};  // pa_diag_force_restart
 }  // namespace
 
 // An NVTX range around a C-ABI call, so that profilers show each call by name (a no-op when no
@@ -727,6 +728,7 @@ int decode_impl(void* out, const void* query, const void* new_key, const void* n
     a.ws_flag = p.schedule == kScheduleLean ? reinterpret_cast<unsigned long long*>(ws + p.off_flag) : nullptr;
     a.epoch = p.schedule == kScheduleLean ? next_epoch() : 0;
     a.wait_ns = kWaitLimitNs;
+    a.force_restart = g_force_restart.load(std::memory_order_relaxed);
     a.new_key = new_key;
     a.new_value = new_key ? new_value : nullptr;
     a.key_cache = new_key ? const_cast<void*>(key_cache) : nullptr;
@@ -894,6 +896,8 @@ int pa_write_kv_fp8(const void* key, const void* value, void* key_cache, void* v
     if (e != cudaSuccess) return cuda_fail(e, "pa_write_kv_fp8 launch");
     return PA_OK;
 }
+
+void pa_diag_force_restart(int on) { g_force_restart.store(on ? 1 : 0, std::memory_order_relaxed); }
 
 int pa_diag_merge_timeout(void* out, const int32_t* context_lens, int num_seqs, int num_heads, int num_kv_heads,
                           int head_dim, int block_size, int max_blocks_per_seq, int dtype, void* workspace,

@@ -1366,8 +1366,8 @@ struct LeanCfg {
     static constexpr int a16(int x) { return (x + 15) & ~15; }
     static constexpr int kBarOffset = kRingBytes;                                   // full[], empty[]
     static constexpr int kIssuedOffset = a16(kBarOffset + 2 * kNSlot * 8);          // int issued[kNSlot]
-    static constexpr int kFlagOffset = a16(kIssuedOffset + kNSlot * 4);             // int abort flag
-    static constexpr int kScanOffset = a16(kFlagOffset + 4);                        // int warp sums[8]
+    static constexpr int kFlagOffset = a16(kIssuedOffset + kNSlot * 4);             // int flags[2]: abort, redo
+    static constexpr int kScanOffset = a16(kFlagOffset + 8);                        // int warp sums[8]
     static constexpr int kRowsOffset = a16(kScanOffset + 8 * 4);                    // int rows[kNW][kRowQueue]
     static constexpr int kCountOffset = a16(kRowsOffset + kNW * kRowQueue * 4);     // int fill_cnt[kNW]
     static constexpr int kQsOffset = a16(kCountOffset + kNW * 4);                   // fp32 q per warp
@@ -1377,10 +1377,11 @@ struct LeanCfg {
     // FP8 append: the new token's 16-bit K and V source rows per warp, staged by cp.async
     static constexpr int kTokOffset = a16(kPsOffset + kPsBytes);
     static constexpr int kTokBytes = sizeof(T) == 1 ? kNW * 2 * D * 2 : 0;
-    static constexpr int kPrefixOffset = a16(kTokOffset + kTokBytes);               // (num_seqs + 1) ints
+    // (num_seqs + 1) ints of page prefix sums, then num_seqs clamped context lengths
+    static constexpr int kPrefixOffset = a16(kTokOffset + kTokBytes);
     static constexpr int kFixedSmemBytes = kPrefixOffset + 1024;      // + slack to align the base
-    static constexpr int kMaxSmemBytes = kFixedSmemBytes + (kLeanMaxSeqs + 1) * 4;
-    static int smem_bytes(int num_seqs) { return kFixedSmemBytes + (num_seqs + 1) * 4; }
+    static constexpr int kMaxSmemBytes = kFixedSmemBytes + (2 * kLeanMaxSeqs + 1) * 4;
+    static int smem_bytes(int num_seqs) { return kFixedSmemBytes + (2 * num_seqs + 1) * 4; }
     // Resident CTAs per SM the register allocation aims for: PA_LEAN_MIN_BLOCKS, but no more
     // than shared memory allows (for short batches), and 2 for head_dim 256 (larger fragments).
     static constexpr int kSmemBlocks = (228 * 1024) / (kFixedSmemBytes + 1024);
@@ -1465,6 +1466,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
     volatile int* flags = reinterpret_cast<volatile int*>(smem + C::kFlagOffset);  // [0]: abort
     int* warp_sums = reinterpret_cast<int*>(smem + C::kScanOffset);
     int* pre = reinterpret_cast<int*>(smem + C::kPrefixOffset);
+    int* lens_s = pre + (a.num_seqs + 1);  // the context lengths, clamped to the tables
 
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -1473,13 +1475,155 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
     const int l_cap = a.max_blocks * BS;
     T* out = static_cast<T*>(a.out);
 
+    // ---- set-up, started before the dependency wait ----
+    // The shared-memory pipeline state touches no global memory: initialise it first.
+    if (tid == 0) {
+        for (int s = 0; s < C::kNSlot; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+            issued[s] = 0;
+        }
+        flags[0] = 0;  // abort
+        flags[1] = 0;  // the set-up guess was wrong
+        fence_barrier_init();
+    }
+    int* row_queue = reinterpret_cast<int*>(smem + C::kRowsOffset);                   // [kNW][kRowQueue]
+    volatile int* fill_cnt = reinterpret_cast<volatile int*>(smem + C::kCountOffset);  // [kNW]
+    int* queue = row_queue + min(warp, C::kNW - 1) * C::kRowQueue;                     // this consumer warp's rows
+    const int upb = a.num_kv_heads * a.head_chunks;  // units per sequence
+    const int wg = (int)blockIdx.x * C::kNW + warp;   // a consumer warp's share index
+    const int per = (B + C::kThreads - 1) / C::kThreads;
+    const int b_lo = min(B, tid * per);
+    const int b_hi = min(B, b_lo + per);
+    int total = 0, q_per_warp = 0, lo = 0, hi = 0, n = 0;
+    int my_len = 0;  // the (clamped) length of this thread's sequence when it has exactly one
+    int first_pb = -1, first_kvh = 0;  // a consumer lane's page `lane` of its share: block id, kv head
+    size_t first_at = 0;               // and its block-table index
+    // Pages per sequence (context lengths clamped to the table), their prefix sums, this warp's
+    // share and the tensor rows of its first 32 pages (published to the producer).  `guess`: run
+    // before the wait, while the previous grid in the stream may still be writing the lengths or
+    // the tables; every load goes through L2 only (no stale line may stay in L1), and whatever it
+    // read is read again and compared after the wait.
+    auto setup = [&](bool guess) {
+        int mine = 0;
+        for (int b = b_lo; b < b_hi; ++b) {
+            int L = __ldcg(a.context_lens + b);
+            if (L < 0 || L > l_cap) {
+                if (!guess && blockIdx.x == 0) atomicOr(a.err, kErrBadContext);
+                L = L < 0 ? 0 : l_cap;
+            }
+            lens_s[b] = L;
+            my_len = L;
+            pre[b] = (L + BS - 1) / BS;
+            mine += pre[b];
+        }
+        int total_pages = 0;
+        int acc = block_exclusive_scan(mine, warp_sums, C::kNW + 1, &total_pages);
+        for (int b = b_lo; b < b_hi; ++b) {
+            const int nb_ = pre[b];
+            pre[b] = acc;
+            acc += nb_;
+        }
+        if (tid == 0) {
+            pre[B] = total_pages;
+            for (int w = 0; w < C::kNW; ++w) fill_cnt[w] = 0;  // no page rows published yet
+        }
+        __syncthreads();
+        total = total_pages * upb;
+        q_per_warp = (total + (int)gridDim.x * C::kNW - 1) / ((int)gridDim.x * C::kNW);
+        lo = min(total, wg * q_per_warp);
+        hi = min(total, lo + q_per_warp);
+        n = warp < C::kNW ? hi - lo : 0;
+        first_pb = -1;
+        if (lane < n) {
+            int sb, su, sj, sn;
+            lean_locate(pre, B, upb, lo + lane, sb, su, sj, sn);
+            first_kvh = su / a.head_chunks;
+            first_at = (size_t)sb * a.max_blocks + sj;
+            first_pb = __ldcg(a.block_tables + first_at);
+            queue[lane] = (unsigned)first_pb < (unsigned)a.num_blocks ? (first_pb * a.num_kv_heads + first_kvh) * BS
+                                                                      : -1;
+        }
+        __syncwarp();
+        if (warp < C::kNW && lane == 0) {
+            __threadfence_block();
+            fill_cnt[warp] = min(n, 32);
+        }
+        __syncthreads();  // every warp's first rows are published before the producer's first pass
+    };
+
+    // The producer lane's state (lane 0 of warp kNW).  Each consumer warp publishes the TMA rows
+    // of its own pages well ahead (row_queue / fill_cnt); the producer only polls the page slots
+    // and issues the next published page of every warp that has a free slot.  It never waits on
+    // global memory and never waits behind one particular warp.
+    static_assert(C::kNW == 4, "the issue loop is unrolled for four consumer warps");
+    int iss[C::kNW], n_w[C::kNW];
+    const bool producer = warp == C::kNW && lane == 0;
+    // Pages are read once per call: let them leave L2 first, so that the partial records the merge
+    // reads stay resident.
+    const uint64_t stream_policy = producer ? l2_policy_evict_first() : 0;
+    auto producer_start = [&]() {
+#pragma unroll
+        for (int wi = 0; wi < C::kNW; ++wi) {
+            iss[wi] = 0;
+            const int lo_w = min(total, ((int)blockIdx.x * C::kNW + wi) * q_per_warp);
+            n_w[wi] = min(total, lo_w + q_per_warp) - lo_w;
+        }
+    };
+    // One pass over the consumer warps; returns whether every page of the CTA has been issued.
+    auto issue_pass = [&](bool& progress, bool one_each = false) -> bool {
+        bool done = true;
+#pragma unroll
+        for (int wi = 0; wi < C::kNW; ++wi) {
+            const int avail = fill_cnt[wi];
+            __threadfence_block();  // the rows below were written before fill_cnt
+            // FP8 pages (4 KB, four slots a warp): at most one page per warp and pass, round robin
+            // over the warps (measured: 13 % on long contexts, 9 % on the Qwen-shaped step);
+            // 16-bit pages (two slots a warp): every free slot at once (one page per pass cost 2 %
+            // there).
+            for (int burst = 0; iss[wi] < avail && (!(F8 || one_each) || burst == 0); ++burst) {
+                const int s = wi * C::kSPW + iss[wi] % C::kSPW;
+                const int use = iss[wi] / C::kSPW;
+                if (use >= 1 && !mbar_test_wait(&empty[s], (use - 1) & 1)) break;
+                const int r = row_queue[wi * C::kRowQueue + iss[wi] % C::kRowQueue];
+                issued[s] += 1;
+                if (r >= 0) {
+                    mbar_arrive_expect_tx(&full[s], C::kSlotBytes);
+                    uint8_t* kdst = ring + s * C::kSlotBytes;
+                    uint8_t* vdst = kdst + C::kPageBytes;
+                    if (F8 && a.kv_interleaved) {
+                        // K rows 2r .. 2r + BS - 1, then V: one box of 2 * BS rows (one 128-byte box
+                        // a row at head_dim 128), landing as the K page followed by the V page
+                        static_assert(!F8 || C::Base::kNBox == 1, "one box per FP8 row");
+                        tma_load_2d_hint(kdst, &tmap_k, 0, 2 * r, &full[s], stream_policy);
+                    } else {
+#pragma unroll
+                        for (int bx = 0; bx < C::Base::kNBox; ++bx)
+                            tma_load_2d_hint(kdst + bx * C::Base::kBoxBytes, &tmap_k, bx * C::Base::kBoxElems, r,
+                                             &full[s], stream_policy);
+#pragma unroll
+                        for (int bx = 0; bx < C::Base::kNBox; ++bx)
+                            tma_load_2d_hint(vdst + bx * C::Base::kBoxBytes, &tmap_v, bx * C::Base::kBoxElems, r,
+                                             &full[s], stream_policy);
+                    }
+                } else {
+                    atomicOr(a.err, kErrBadTable);  // skip the load; the slot keeps stale data
+                    mbar_arrive(&full[s]);
+                }
+                ++iss[wi];
+                progress = true;
+            }
+            done = done && iss[wi] >= n_w[wi];
+        }
+        return done;
+    };
+
+    if (producer) {
+        tma_prefetch_desc(&tmap_k);
+        tma_prefetch_desc(&tmap_v);
+    }
 #if PA_LEAN_L2_PREFETCH
-    // While the previous grid drains: warm L2 with the context lengths and this CTA's share of
-    // the block tables (prefetches return no data, so a value the previous grid is still writing
-    // is read only after the wait, coherently, from L2).
-    {
-        const char* lens = reinterpret_cast<const char*>(a.context_lens);
-        for (int off = tid * 128; off < B * 4; off += C::kThreads * 128) prefetch_l2(lens + off);
+    {   // warm L2 with this CTA's share of the block tables (prefetches return no data)
         const long long tab_bytes = (long long)B * a.max_blocks * 4;
         const long long share = (tab_bytes + gridDim.x - 1) / gridDim.x;
         const char* tab = reinterpret_cast<const char*>(a.block_tables) + share * blockIdx.x;
@@ -1487,126 +1631,143 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
             prefetch_l2(tab + off);
     }
 #endif
+    __syncthreads();  // barrier initialisation before any use
+    setup(true);
     // Wait for the previous grid in the stream, then let the merge kernel get scheduled as
     // early as possible; it reads nothing this kernel writes before its own wait.
     griddep_wait();
     griddep_launch_dependents();
+    // ---- consumer state (consumer warps only) ----
+    int unit_first = 0, unit_last = -1;
+    int b = 0, uu = 0, nb = 0, L = 0, gc = 0, kvh = 0;
+    UnitRows rows{0, 0, 0, a.q_len, a.group, a.num_heads};
+    int wrote = 0;  // bit s: a partial record was written to slot s
+    const bool append = F8 ? F8_APPEND : a.new_key != nullptr;
+    std::conditional_t<F8, NewTokenF8<T, D, BS>, NewToken<T, D, BS>> tok;
+    if constexpr (F8) tok.stage = smem + C::kTokOffset + min(warp, C::kNW - 1) * 4 * D;
+    bool tok_ready = false, tok_writer = false;
+    std::conditional_t<F8, MmaConsumerF8<T, D, BS>,
+                       std::conditional_t<MMA, MmaConsumer<T, D, BS, CAUSAL>, SimtConsumer<T, D, BS, GMAX>>>
+        cons;
+    float* q_s = reinterpret_cast<float*>(smem + C::kQsOffset) + min(warp, C::kNW - 1) * GMAX * D;
+    float* p_s = reinterpret_cast<float*>(smem + C::kPsOffset) + min(warp, C::kNW - 1) * GMAX * BS;
+    // The unit holding global page g starts: its place, its length (from shared memory) and its
+    // query rows (loaded here; a load on the consumer's critical path).
+    auto start_unit = [&](int g) {
+        int j0;
+        lean_locate(pre, B, upb, g, b, uu, j0, nb);
+        unit_first = g - j0;
+        unit_last = unit_first + nb - 1;
+        kvh = uu / a.head_chunks;
+        const int hc = uu - kvh * a.head_chunks;
+        tok_writer = hc == 0;
+        rows = UnitRows{b, kvh, hc * C::kHeads, a.q_len, a.group, a.num_heads};
+        gc = min(C::kHeads, a.rows - hc * C::kHeads);
+        L = lens_s[b];
+        const T* q = static_cast<const T*>(a.q);
+        if constexpr (F8) {
+            const int r = min(lane >> 2, gc - 1);
+            cons.init(q + rows.row(r) * D, (lane >> 2) < gc, a.scale_log2, lane);
+        } else if constexpr (MMA) {
+            const int r = min(lane >> 2, gc - 1);
+            cons.init(q + rows.row(r) * D, (lane >> 2) < gc, rows.last_pos(lane >> 2, L), lane);
+        } else {
+            __syncwarp();
+            for (int idx = lane; idx < GMAX * D; idx += 32)
+                q_s[idx] = idx / D < gc ? to_float(q[rows.row(idx / D) * D + idx % D]) : 0.f;
+            __syncwarp();
+            cons.init(L - a.q_len, rows.v0, a.group);
+        }
+    };
 
-    // ---- pages per sequence (context lengths clamped to the table), prefix sums ----
-    const int per = (B + C::kThreads - 1) / C::kThreads;
-    const int b_lo = min(B, tid * per);
-    const int b_hi = min(B, b_lo + per);
-    int mine = 0;
-    for (int b = b_lo; b < b_hi; ++b) {
-        int L = __ldg(a.context_lens + b);
-        if (L < 0 || L > l_cap) {
-            if (blockIdx.x == 0) atomicOr(a.err, kErrBadContext);
-            L = L < 0 ? 0 : l_cap;
-        }
-        pre[b] = (L + BS - 1) / BS;
-        mine += pre[b];
-    }
-    int total_pages = 0;
-    int acc = block_exclusive_scan(mine, warp_sums, C::kNW + 1, &total_pages);
-    for (int b = b_lo; b < b_hi; ++b) {
-        const int n = pre[b];
-        pre[b] = acc;
-        acc += n;
-    }
-    if (tid == 0) {
-        pre[B] = total_pages;
-        for (int s = 0; s < C::kNSlot; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-            issued[s] = 0;
-        }
-        int* fills = reinterpret_cast<int*>(smem + C::kCountOffset);
-        for (int w = 0; w < C::kNW; ++w) fills[w] = 0;  // no page rows published yet
-        flags[0] = 0;
-        fence_barrier_init();
-    }
+    // After the wait, in this order: the small loads (the re-reads that check the guess, every
+    // consumer warp's first query rows), the producer's first page loads, then the check; the
+    // consumers then go straight to their first page.  Between the first page loads and the
+    // first page nothing here touches shared memory (the check compares registers and decides
+    // with one barrier): while a burst of page copies is being issued, other memory
+    // instructions of the SM wait behind it.
+    int chk_len = 0, chk_pb = 0;
+    for (int bb = b_lo; bb < b_hi; ++bb) chk_len = __ldcg(a.context_lens + bb);  // B <= threads: one each
+    if (lane < n) chk_pb = __ldcg(a.block_tables + first_at);
+    if (warp < C::kNW && n > 0) start_unit(lo);
     __syncthreads();
+    if (producer) {  // the first pages go out at once, on the guess: one per warp (a smaller burst)
+        producer_start();
+        bool progress = false;
+        issue_pass(progress, true);
+    }
+    bool bad = a.force_restart != 0;
+    if (b_hi - b_lo == 1) {
+        int Lc = chk_len;
+        if (Lc < 0 || Lc > l_cap) {
+            if (blockIdx.x == 0) atomicOr(a.err, kErrBadContext);
+            Lc = Lc < 0 ? 0 : l_cap;
+        }
+        bad = bad || Lc != my_len;
+    } else {
+        for (int bb = b_lo; bb < b_hi; ++bb) {
+            int Lc = __ldcg(a.context_lens + bb);
+            if (Lc < 0 || Lc > l_cap) {
+                if (blockIdx.x == 0) atomicOr(a.err, kErrBadContext);
+                Lc = Lc < 0 ? 0 : l_cap;
+            }
+            bad = bad || Lc != lens_s[bb];
+        }
+    }
+    if (lane < n && chk_pb != first_pb) bad = true;
+    bool aborted = false;
+    if (__syncthreads_or(bad)) {
+        // The guess was wrong (rare: the previous grid changed the lengths or the tables).  Let the
+        // copies issued from it land, discard them, and set up again from the values read now.
+        bool drained = true;
+        if (tid == 0) {
+            for (int s = 0; s < C::kNSlot; ++s) {
+                if (issued[s] == 0) continue;
+                const unsigned long long start = global_timer_ns();
+                while (!mbar_try_wait(&full[s], (issued[s] - 1) & 1)) {
+                    if (global_timer_ns() - start > kWaitLimitNs) {
+                        drained = false;
+                        break;
+                    }
+                }
+            }
+            if (drained) {
+                for (int s = 0; s < C::kNSlot; ++s) {
+                    mbar_inval(&full[s]);
+                    mbar_inval(&empty[s]);
+                    mbar_init(&full[s], 1);
+                    mbar_init(&empty[s], 1);
+                    issued[s] = 0;
+                }
+                fence_barrier_init();
+            } else {
+                atomicOr(a.err, kErrTimeout);
+                flags[0] = 1;  // the copies never landed: give up (the exit path drains again)
+            }
+        }
+        aborted = __syncthreads_or(!drained) != 0;
+        if (!aborted) {
+            setup(false);
+            if (producer) producer_start();
+            if (warp < C::kNW && n > 0) start_unit(lo);
+        }
+    }
+    if (total == 0 && !aborted) {
+        // Nothing to stream: only the zero rows of empty contexts (spread over the CTAs).
+        for (int bz = warp; bz < B; bz += C::kNW + 1)
+            if ((bz % (int)gridDim.x) == (int)blockIdx.x)
+                for (int idx = lane; idx < a.q_len * a.num_heads * D; idx += 32)
+                    out[(size_t)bz * a.q_len * a.num_heads * D + idx] = from_float<T>(0.f);
+        return;
+    }
 
-    const int upb = a.num_kv_heads * a.head_chunks;  // units per sequence
-    const int total = total_pages * upb;
-    const int q_per_warp = (total + (int)gridDim.x * C::kNW - 1) / ((int)gridDim.x * C::kNW);
-
-    // Empty contexts produce zero rows (spread over the CTAs).
-    for (int b = warp; b < B; b += C::kNW + 1)
-        if (pre[b] == pre[b + 1] && (b % (int)gridDim.x) == (int)blockIdx.x)
-            for (int idx = lane; idx < a.q_len * a.num_heads * D; idx += 32)
-                out[(size_t)b * a.q_len * a.num_heads * D + idx] = from_float<T>(0.f);
-    if (total == 0) return;
-
-    int* row_queue = reinterpret_cast<int*>(smem + C::kRowsOffset);        // [kNW][kRowQueue]
-    volatile int* fill_cnt = reinterpret_cast<volatile int*>(smem + C::kCountOffset);  // [kNW]
     if (warp == C::kNW) {
         // ================= producer warp =================
-        // Each consumer warp publishes the TMA rows of its own pages well ahead
-        // (row_queue / fill_cnt); lane 0 only polls the page slots and issues the
-        // next published page of every warp that has a free slot.  It never
-        // waits on global memory and never waits behind one particular warp.
-        if (lane == 0) {
-            tma_prefetch_desc(&tmap_k);
-            tma_prefetch_desc(&tmap_v);
-            // Pages are read once per call: let them leave L2 first, so that the partial
-            // records the merge reads stay resident.
-            const uint64_t stream_policy = l2_policy_evict_first();
-            static_assert(C::kNW == 4, "the issue loop is unrolled for four consumer warps");
-            int iss[C::kNW], n_w[C::kNW];
-#pragma unroll
-            for (int wi = 0; wi < C::kNW; ++wi) {
-                iss[wi] = 0;
-                const int lo_w = min(total, ((int)blockIdx.x * C::kNW + wi) * q_per_warp);
-                n_w[wi] = min(total, lo_w + q_per_warp) - lo_w;
-            }
+        if (producer && !aborted) {
             unsigned long long last_progress = global_timer_ns();
             while (true) {
-                bool progress = false, done = true;
-#pragma unroll
-                for (int wi = 0; wi < C::kNW; ++wi) {
-                    const int avail = fill_cnt[wi];
-                    __threadfence_block();  // the rows below were written before fill_cnt
-                    // FP8 pages (4 KB, four slots a warp): at most one page per warp and pass,
-                    // round robin over the warps (measured: 13 % on long contexts, 9 % on the
-                    // Qwen-shaped step); 16-bit pages (two slots a warp): every free slot at once
-                    // (one page per pass cost 2 % there).
-                    for (int burst = 0; iss[wi] < avail && (!F8 || burst == 0); ++burst) {
-                        const int s = wi * C::kSPW + iss[wi] % C::kSPW;
-                        const int use = iss[wi] / C::kSPW;
-                        if (use >= 1 && !mbar_test_wait(&empty[s], (use - 1) & 1)) break;
-                        const int r = row_queue[wi * C::kRowQueue + iss[wi] % C::kRowQueue];
-                        issued[s] += 1;
-                        if (r >= 0) {
-                            mbar_arrive_expect_tx(&full[s], C::kSlotBytes);
-                            uint8_t* kdst = ring + s * C::kSlotBytes;
-                            uint8_t* vdst = kdst + C::kPageBytes;
-                            if (F8 && a.kv_interleaved) {
-                                // K rows 2r .. 2r + BS - 1, then V: one box of 2 * BS rows (one
-                                // 128-byte box a row at head_dim 128), landing as the K page
-                                // followed by the V page
-                                static_assert(!F8 || C::Base::kNBox == 1, "one box per FP8 row");
-                                tma_load_2d_hint(kdst, &tmap_k, 0, 2 * r, &full[s], stream_policy);
-                            } else {
-#pragma unroll
-                                for (int bx = 0; bx < C::Base::kNBox; ++bx)
-                                    tma_load_2d_hint(kdst + bx * C::Base::kBoxBytes, &tmap_k,
-                                                     bx * C::Base::kBoxElems, r, &full[s], stream_policy);
-#pragma unroll
-                                for (int bx = 0; bx < C::Base::kNBox; ++bx)
-                                    tma_load_2d_hint(vdst + bx * C::Base::kBoxBytes, &tmap_v,
-                                                     bx * C::Base::kBoxElems, r, &full[s], stream_policy);
-                            }
-                        } else {
-                            atomicOr(a.err, kErrBadTable);  // skip the load; the slot keeps stale data
-                            mbar_arrive(&full[s]);
-                        }
-                        ++iss[wi];
-                        progress = true;
-                    }
-                    done = done && iss[wi] >= n_w[wi];
-                }
-                if (done) break;
+                bool progress = false;
+                if (issue_pass(progress)) break;
                 if (progress) {
                     last_progress = global_timer_ns();
                 } else {
@@ -1620,57 +1781,24 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
                 }
             }
         }
-    } else {
+    } else if (!aborted) {
         // ================= consumer warps =================
-        const int wg = (int)blockIdx.x * C::kNW + warp;
-        const int lo = min(total, wg * q_per_warp);
-        const int hi = min(total, lo + q_per_warp);
-        const int n = hi - lo;
-        int unit_first = 0, unit_last = -1;
-        int b = 0, uu = 0, nb = 0, L = 0, gc = 0, kvh = 0;
-        UnitRows rows{0, 0, 0, a.q_len, a.group, a.num_heads};
-        int wrote = 0;  // bit s: a partial record was written to slot s
-        const bool append = F8 ? F8_APPEND : a.new_key != nullptr;
-        std::conditional_t<F8, NewTokenF8<T, D, BS>, NewToken<T, D, BS>> tok;
-        if constexpr (F8) tok.stage = smem + C::kTokOffset + warp * 4 * D;
-        bool tok_ready = false, tok_writer = false;
-        std::conditional_t<F8, MmaConsumerF8<T, D, BS>,
-                           std::conditional_t<MMA, MmaConsumer<T, D, BS, CAUSAL>, SimtConsumer<T, D, BS, GMAX>>>
-            cons;
         // FP8: lane i holds the K and V scales of page 32 * chunk + i of the current chunk
         // (cur_*) and of the next one (pend_*, loaded when that chunk is published).
         float cur_ks = 0.f, cur_vs = 0.f, pend_ks = 0.f, pend_vs = 0.f;
-        float* q_s = reinterpret_cast<float*>(smem + C::kQsOffset) + warp * GMAX * D;
-        float* p_s = reinterpret_cast<float*>(smem + C::kPsOffset) + warp * GMAX * BS;
+        if constexpr (F8) {
+            const bool ok = lane < n && (unsigned)first_pb < (unsigned)a.num_blocks;
+            cur_ks = ok ? __ldg(a.k_scale + first_pb * a.num_kv_heads + first_kvh) : 0.f;
+            cur_vs = ok ? __ldg(a.v_scale + first_pb * a.num_kv_heads + first_kvh) : 0.f;
+        }
         // Page rows for the producer, published in chunks of 32: chunk c + 1 when this warp
         // reaches page 32c + 16, with the block-table loads of chunk c + 2 then left in flight.
-        int* queue = row_queue + warp * C::kRowQueue;
         int pend_pb = -1, pend_kvh = 0;
-        for (int chunk = 0; chunk < 2; ++chunk) {
-            const int page = 32 * chunk + lane;
-            pend_pb = -1;
-            if (page < n) {
-                int sb, su, sj, sn;
-                lean_locate(pre, B, upb, lo + page, sb, su, sj, sn);
-                pend_kvh = su / a.head_chunks;
-                pend_pb = __ldg(a.block_tables + (size_t)sb * a.max_blocks + sj);
-            }
-            if (chunk == 0) {
-                if constexpr (F8) {
-                    const bool ok = page < n && (unsigned)pend_pb < (unsigned)a.num_blocks;
-                    cur_ks = ok ? __ldg(a.k_scale + pend_pb * a.num_kv_heads + pend_kvh) : 0.f;
-                    cur_vs = ok ? __ldg(a.v_scale + pend_pb * a.num_kv_heads + pend_kvh) : 0.f;
-                }
-                if (page < n)
-                    queue[page] = (unsigned)pend_pb < (unsigned)a.num_blocks
-                                      ? (pend_pb * a.num_kv_heads + pend_kvh) * BS
-                                      : -1;
-                __syncwarp();
-                if (lane == 0) {
-                    __threadfence_block();
-                    fill_cnt[warp] = min(n, 32);
-                }
-            }
+        if (32 + lane < n) {
+            int sb, su, sj, sn;
+            lean_locate(pre, B, upb, lo + 32 + lane, sb, su, sj, sn);
+            pend_kvh = su / a.head_chunks;
+            pend_pb = __ldg(a.block_tables + (size_t)sb * a.max_blocks + sj);
         }
         for (int off = 0; off < n; ++off) {
             if constexpr (F8) {
@@ -1706,33 +1834,7 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
                 }
             }
             const int g = lo + off;
-            if (g > unit_last) {  // a new unit starts
-                int j0;
-                lean_locate(pre, B, upb, g, b, uu, j0, nb);
-                unit_first = g - j0;
-                unit_last = unit_first + nb - 1;
-                kvh = uu / a.head_chunks;
-                const int hc = uu - kvh * a.head_chunks;
-                tok_writer = hc == 0;
-                rows = UnitRows{b, kvh, hc * C::kHeads, a.q_len, a.group, a.num_heads};
-                gc = min(C::kHeads, a.rows - hc * C::kHeads);
-                L = __ldg(a.context_lens + b);
-                L = L < 0 ? 0 : (L > l_cap ? l_cap : L);
-                const T* q = static_cast<const T*>(a.q);
-                if constexpr (F8) {
-                    const int r = min(lane >> 2, gc - 1);
-                    cons.init(q + rows.row(r) * D, (lane >> 2) < gc, a.scale_log2, lane);
-                } else if constexpr (MMA) {
-                    const int r = min(lane >> 2, gc - 1);
-                    cons.init(q + rows.row(r) * D, (lane >> 2) < gc, rows.last_pos(lane >> 2, L), lane);
-                } else {
-                    __syncwarp();
-                    for (int idx = lane; idx < GMAX * D; idx += 32)
-                        q_s[idx] = idx / D < gc ? to_float(q[rows.row(idx / D) * D + idx % D]) : 0.f;
-                    __syncwarp();
-                    cons.init(L - a.q_len, rows.v0, a.group);
-                }
-            }
+            if (g > unit_last) start_unit(g);  // a new unit starts
             const int j = g - unit_first;
             // Append mode: fetch the new token one page ahead of the page holding L - 1.
             const bool tok_page = append && g == unit_last;
@@ -1800,6 +1902,11 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
         }
         // A token copy may still be in flight when a wait gave up before its page.
         if constexpr (F8 && F8_APPEND) cp_async_wait_all();
+        // Empty contexts produce zero rows (spread over the CTAs), written once the pages are done.
+        for (int bz = warp; bz < B; bz += C::kNW)
+            if (pre[bz] == pre[bz + 1] && (bz % (int)gridDim.x) == (int)blockIdx.x)
+                for (int idx = lane; idx < a.q_len * a.num_heads * D; idx += 32)
+                    out[(size_t)bz * a.q_len * a.num_heads * D + idx] = from_float<T>(0.f);
     }
     __syncthreads();
     if (flags[0]) {

@@ -49,6 +49,7 @@ struct DecodeArgs {
     int lean_warps_per_cta;      // consumer warps per lean CTA
     int lean_grid;               // CTAs of the lean decode launch (set for the merge kernel)
     int lean_merge_by_boundary;  // merge grid: one CTA per boundary between warp shares, not per unit
+    int lean_share_warps;        // lean schedule: consumer warps the pages are cut for (<= all of them)
     int force_restart;           // lean decode: treat the set-up made before the wait as wrong (tests)
 };
 

@@ -2045,34 +2045,14 @@ __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_me
     }
     const int n = w_hi - w_lo + 1;
     const int slot0 = first != w_lo * q ? 1 : 0;  // w_lo holds the unit in slot 1 unless its range starts here
-    // Wait until every piece's record is published (flag == epoch), not for the whole
-    // decode grid: the merge of a unit starts as soon as the warps holding it are done.
-    // Bounded; a wait that gives up reports kErrTimeout and merges nothing.
+    // The pieces' records are folded batch by batch, each batch as soon as the flags of its pieces
+    // read this call's epoch (each warp of the decode publishes its records once its pages are
+    // done), not after the whole decode grid nor after every piece: a batch whose pieces are
+    // done is folded while the pieces of a later batch are still streaming.  Each wait is
+    // bounded; one that gives up reports kErrTimeout and the CTA writes nothing.
     __shared__ volatile int gave_up;
     if (tid == 0) gave_up = 0;
     __syncthreads();
-    for (int p = tid; p < n; p += kLeanMergeThreads) {
-        const unsigned long long* f = a.ws_flag + (size_t)(w_lo + p) * 2 + (p == 0 ? slot0 : 0);
-        if (ld_acquire_gpu(f) == a.epoch) continue;
-        const unsigned long long start = global_timer_ns();
-        while (ld_acquire_gpu(f) != a.epoch) {
-            if (gave_up || global_timer_ns() - start > a.wait_ns) {
-                if (!gave_up) atomicOr(a.err, kErrTimeout);
-                gave_up = 1;
-                break;
-            }
-            __nanosleep(32);
-        }
-    }
-    __syncthreads();
-    if (gave_up) {
-        griddep_wait();
-        return;
-    }
-    // Every flag is read by this CTA alone: clear the ones it consumed, so that the next call on
-    // this workspace starts from zeros even if it reuses this call's epoch (a replayed capture).
-    for (int p = tid; p < n; p += kLeanMergeThreads)
-        a.ws_flag[(size_t)(w_lo + p) * 2 + (p == 0 ? slot0 : 0)] = 0ull;
     const int kvh = uu / a.head_chunks, hc = uu - kvh * a.head_chunks;
     const UnitRows rows{b, kvh, hc * H, a.q_len, a.group, a.num_heads};
     const int gc = min(H, a.rows - hc * H);
@@ -2083,14 +2063,31 @@ __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_me
     __shared__ float red[6][kLeanMergeThreads];
     const int cols = gc * (D / 4);
     const int slices = kLeanMergeThreads >= cols ? kLeanMergeThreads / cols : 1;
+    const int per_batch = kLeanMergeBatch * slices;  // records of one batch, over all slices
     for (int cbase = 0; cbase < cols; cbase += kLeanMergeThreads) {
     const int col = slices > 1 ? tid % cols : cbase + tid;
     const int slice = slices > 1 ? tid / cols : (col < cols ? 0 : 1);
     const int h = col / (D / 4);
     float mm = -INFINITY, ww = 0.f;
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (slice < slices) {
-        for (int p0 = slice; p0 < n; p0 += kLeanMergeBatch * slices) {
+    for (int pb = 0; pb < n; pb += per_batch) {
+        for (int p = pb + tid; p < min(n, pb + per_batch); p += kLeanMergeThreads) {
+            const unsigned long long* f = a.ws_flag + (size_t)(w_lo + p) * 2 + (p == 0 ? slot0 : 0);
+            if (ld_acquire_gpu(f) == a.epoch) continue;
+            const unsigned long long start = global_timer_ns();
+            while (ld_acquire_gpu(f) != a.epoch) {
+                if (gave_up || global_timer_ns() - start > a.wait_ns) {
+                    if (!gave_up) atomicOr(a.err, kErrTimeout);
+                    gave_up = 1;
+                    break;
+                }
+                __nanosleep(32);
+            }
+        }
+        __syncthreads();
+        if (gave_up) break;
+        if (slice < slices) {
+            const int p0 = pb + slice;
             float mv[kLeanMergeBatch], lv[kLeanMergeBatch];
             float4 ov[kLeanMergeBatch];
 #pragma unroll
@@ -2120,6 +2117,7 @@ __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_me
             }
         }
     }
+    if (gave_up) break;
     if (slices > 1) {
         red[0][tid] = mm;
         red[1][tid] = ww;
@@ -2153,6 +2151,11 @@ __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_me
         out[3] = from_float<T>(acc.w * inv);
     }
     }
+    // Every flag is read by this CTA alone: clear the ones it consumed, so that the next call on
+    // this workspace starts from zeros even if it reuses this call's epoch (a replayed capture).
+    if (!gave_up)
+        for (int p = tid; p < n; p += kLeanMergeThreads)
+            a.ws_flag[(size_t)(w_lo + p) * 2 + (p == 0 ? slot0 : 0)] = 0ull;
     griddep_wait();  // this grid must not end before the decode grid has
 }
 

@@ -44,6 +44,9 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES_DEFAULT = 129 * 1024 * 1024
 
+# Timed beside the headline in the default run, one side record each.
+SIDE_WORKLOADS = ("qwen_gqa_fp8", "qwen_gqa_verify4", "mha_short_bs16", "long_context_fp8")
+
 WORKLOAD_DESCRIPTIONS = {
     "qwen_gqa": "Qwen-style GQA layer: batch 64, 28 q / 4 kv heads, head_dim 128, bf16, block_size 16, "
                 "context_lens uniform in [512,4096], pool 20000 blocks shuffled, q/K/V ~ N(0,1), "
@@ -620,7 +623,9 @@ def long_context_leg(args, device, peak: float, steps: int, warmup: int) -> dict
             "l2": f"pages touched per step {pages_touched_bytes(lens, Hkv, d, 2, bs) / 1e6:.0f} MB, above L2"}
 
 
-def run_ours(args, rank: int, world: int, local_rank: int) -> None:
+def run_ours(args, rank: int, world: int, local_rank: int, sub: bool = False):
+    """Time one workload. sub=False: the headline run (prints the JSON line); sub=True: a side
+    record for the headline line (returned as a dict: no clock sampler, e2e or CPU leg of its own)."""
     import torch
 
     import paged_kv_cache_129_gb300 as pa
@@ -782,8 +787,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
         if status != 0:
             raise RuntimeError(lib.pa_last_error_string().decode())
 
-    sampler = ClockSampler(gpu_selector(device))
-    sampler.start()
+    sampler = None if sub else ClockSampler(gpu_selector(device))
+    if sampler is not None:
+        sampler.start()
     for i in range(args.warmup):
         step(i)
     torch.cuda.synchronize()
@@ -827,12 +833,25 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     peak = float(peak or FALLBACK_HBM_GBS)
     # The long-context configuration (the other >= 70 % of HBM target), timed in the same run.
     long_leg = None
-    if args.workload == "qwen_gqa" and not args.no_long_context and world == 1:
+    if not sub and args.workload == "qwen_gqa" and not args.no_long_context and world == 1:
         long_leg = long_context_leg(args, device, peak, steps=max(K, 20), warmup=args.warmup)
         windows.append(long_leg.pop("window"))
+    # The other hot-path rows (FP8 cache, speculative verify, many short MHA requests), each a
+    # side record timed the same way in the same run.
+    side = []
+    if not sub and args.workload == "qwen_gqa" and not args.no_side_workloads and world == 1:
+        for w in SIDE_WORKLOADS:
+            sargs = argparse.Namespace(**vars(args))
+            sargs.workload, sargs.kernel, sargs.partition_pages = w, "auto", 0
+            sargs.no_e2e = sargs.no_cpu_baseline = sargs.no_long_context = sargs.no_side_workloads = True
+            sargs.steps = max(K, 20)
+            rec = run_ours(sargs, rank, world, local_rank, sub=True)
+            windows.append(rec.pop("window"))
+            side.append(rec)
     t_end = time.monotonic()
     barrier(world)
-    sampler.stop()
+    if sampler is not None:
+        sampler.stop()
     elapsed_ms_max = max_over_ranks(elapsed_ms, world)
     total_bytes = sum_over_ranks(float(step_bytes) * K, world)
     total_seqs = sum_over_ranks(float(B) * K, world)
@@ -894,7 +913,7 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
 
         e2e_run(min(args.warmup, 20) + 1, first=True)
         torch.cuda.synchronize()
-        Ke = max(1, min(K, args.e2e_steps))
+        Ke = max(1, args.e2e_steps)  # a steady-state run, whatever K is (K = 20 would be mostly pipeline fill)
         # three timed runs of Ke steps each; the line reports the median run (the host thread paces
         # this leg, and one run can lose its core to another process)
         runs = []
@@ -943,6 +962,17 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
                 "timing": f"CUDA events around {K} back-to-back calls on the launch stream",
                 "peak_source": peak_src}
 
+    if sub:
+        return {"window": windows[0], "workload": WORKLOAD_DESCRIPTIONS[args.workload], "name": args.workload,
+                "step": roofline["kernel"].split(" call")[0], "dtype": DTYPE_NAMES[inp.dtype],
+                "value": round(value, 2), "unit": UNIT, "pct_of_hbm_peak": round(100 * value / peak, 2),
+                "steps": K, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+                "queries_per_s": round(total_seqs / (elapsed_ms_max / 1e3), 1),
+                "step_bytes": step_bytes, "roofline": roofline,
+                "per_rep": rep_summary(rep_ms, step_bytes, per_rep, "whole steps"),
+                "gpu_launches": launches_per_step * K,
+                "l2": f"{replicas} cache replicas rotated per step (pages touched per step "
+                      f"{touched / 1e6:.0f} MB, L2 {l2 / 1e6:.0f} MB)"}
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         import oracle
@@ -1009,6 +1039,9 @@ def run_ours(args, rank: int, world: int, local_rank: int) -> None:
     }
     if long_leg is not None:
         line["long_context"] = long_leg
+    if side:
+        line["side_workloads"] = {r["name"]: r for r in side}
+        line["gpu_launches_side_workloads"] = sum(r["gpu_launches"] for r in side)
     print(json.dumps(line), flush=True)
 
 
@@ -1492,6 +1525,8 @@ def main(argv=None) -> None:
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-side-workloads", action="store_true",
+                    help="qwen_gqa: skip the FP8, verify and MHA side records of the default line")
     ap.add_argument("--no-long-context", action="store_true",
                     help="qwen_gqa: skip the long-context configuration timed in the same run")
     ap.add_argument("--fp8-layout", choices=["interleaved", "separate"], default="interleaved",

@@ -44,6 +44,10 @@ UNIT = "GB/s"
 FALLBACK_HBM_GBS = 6800.0
 L2_BYTES_DEFAULT = 129 * 1024 * 1024
 
+# pa_decode_plan.schedule values
+SCHEDULE_NAMES = {0: "partitioned grid", 1: "lean persistent wave + merge",
+                  2: "persistent row-split wave + merge"}
+
 # Timed beside the headline in the default run, one side record each.
 SIDE_WORKLOADS = ("qwen_gqa_fp8", "qwen_gqa_verify4", "mha_short_bs16", "long_context_fp8")
 
@@ -609,7 +613,7 @@ def long_context_leg(args, device, peak: float, steps: int, warmup: int) -> dict
     pa.check_error()
     value = nbytes / (ms / 1e3) / 1e9
     return {"window": (t_begin, t_end), "workload": WORKLOAD_DESCRIPTIONS["long_context"], "name": "long_context", "step": "pa_decode",
-            "schedule": {0: "partitioned grid", 1: "lean persistent wave + merge"}[plan.schedule],
+            "schedule": SCHEDULE_NAMES[plan.schedule],
             "value": round(value, 2), "unit": UNIT, "pct_of_hbm_peak": round(100 * value / peak, 2),
             "steps": steps, "warmup": warmup, "ms_per_step": round(ms, 5),
             "queries_per_s": round(B / (ms / 1e3), 1),
@@ -619,7 +623,7 @@ def long_context_leg(args, device, peak: float, steps: int, warmup: int) -> dict
                          "kernel": "pa_decode call (paged_decode_lean_kernel + lean_merge_kernel)"
                                    if plan.schedule == 1 else "pa_decode call (paged_decode_kernel)"},
             "per_rep": rep_summary(reps, nbytes, per_rep, "pa_decode calls"),
-            "gpu_launches": steps * (2 if (plan.schedule == 1 or plan.max_parts > 1) else 1),
+            "gpu_launches": steps * (2 if (plan.schedule in (1, 2) or plan.max_parts > 1) else 1),
             "l2": f"pages touched per step {pages_touched_bytes(lens, Hkv, d, 2, bs) / 1e6:.0f} MB, above L2"}
 
 
@@ -766,7 +770,7 @@ def run_ours(args, rank: int, world: int, local_rank: int, sub: bool = False):
                     for r in range(replicas)]
     # the decode kernel, plus the merge kernel (always for the lean schedule, when split for
     # the grid one), plus the write kernel when it is a call of its own
-    merge_launches = 1 if (plan.schedule == 1 or plan.max_parts > 1) else 0
+    merge_launches = 1 if (plan.schedule in (1, 2) or plan.max_parts > 1) else 0
     launches_per_step = (1 if (has_write and not fused) else 0) + 1 + merge_launches
 
     def step(i):
@@ -956,6 +960,7 @@ def run_ours(args, rank: int, world: int, local_rank: int, sub: bool = False):
                             "pa_decode_fp8" if fp8 else "pa_decode") +
                            " call (" +
                            ("paged_decode_lean_kernel + lean_merge_kernel)" if plan.schedule == 1 else
+                            "paged_decode_rs_lean_kernel + rs_lean_merge_kernel)" if plan.schedule == 2 else
                             "paged_decode_kernel" + (" + splitkv_merge_kernel)" if plan.max_parts > 1 else ")"))),
                 "algorithmic_bytes_per_launch": call_bytes, "pages_touched_bytes": touched,
                 "avg_launch_ms": round(dec_avg_ms, 5),
@@ -1022,7 +1027,7 @@ def run_ours(args, rank: int, world: int, local_rank: int, sub: bool = False):
                        "value_kind": "effective GB/s: every sequence's K/V counted, shared pages once per "
                                      "sequence (above HBM peak through L2 hits)"} if prefix else {}),
                    "kernel": {1: "mma", 2: "simt"}[plan.kernel],
-                   "schedule": {0: "partitioned grid", 1: "lean persistent wave + merge"}[plan.schedule],
+                   "schedule": SCHEDULE_NAMES[plan.schedule],
                    "partition_pages": plan.partition_pages,
                    "max_parts": plan.max_parts, "grid_ctas": plan.grid_ctas,
                    "parallelism": f"{world} independent replicas (one batch per GPU)"},
@@ -1138,7 +1143,7 @@ def run_layers(args, rank: int, world: int, local_rank: int) -> None:
     clocks = sampler.summary(t_begin, t_end)
     if rank != 0:
         return
-    merge = 1 if (plan.schedule == 1 or plan.max_parts > 1) else 0
+    merge = 1 if (plan.schedule in (1, 2) or plan.max_parts > 1) else 0
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms / K, 5), "higher_is_better": True, "scaling": "weak",

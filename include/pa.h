@@ -326,9 +326,11 @@ int pa_decode_multi_make_plan(int num_seqs, int q_len, int num_heads, int num_kv
 /* The partition plan pa_decode_ex would use on the current device. */
 typedef struct pa_decode_plan {
     int kernel;            /* PA_KERNEL_MMA or PA_KERNEL_SIMT */
-    int schedule;          /* 0: partitioned grid (+ merge kernel), 1: lean persistent wave */
-    int partition_pages;   /* pages per CTA partition (grid schedule; 0 for lean) */
-    int max_parts;         /* partitions of the longest context (grid schedule; 0 for lean) */
+    int schedule;          /* 0: partitioned grid (+ merge kernel), 1: lean persistent wave,
+                              2: persistent row-split wave (pa_decode_multi with 9..32 query rows
+                              per kv head: a warp per chunk of 8 rows, equal page shares per CTA) */
+    int partition_pages;   /* pages per CTA partition (grid schedule; 0 otherwise) */
+    int max_parts;         /* partitions of the longest context (grid schedule; 0 otherwise) */
     int heads_per_cta;     /* query heads handled by one CTA */
     int grid_ctas;         /* CTAs launched */
     int threads_per_cta;

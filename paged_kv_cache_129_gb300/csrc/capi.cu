@@ -355,6 +355,24 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
         }
     }
 
+    // Row split (multi-query decode, 2..4 row chunks per kv head): one persistent wave, every CTA an
+    // equal share of all pages, each page read once for all of its kv head's rows.
+    if (p.row_split && partition_pages == 0 && has_ws && p.ki.rs_ctas_per_sm > 0 && num_seqs <= p.ki.lean_max_seqs &&
+        (long long)num_seqs * max_blocks * num_kv_heads < (1ll << 31)) {
+        const long long ctas = (long long)dev->num_sms * p.ki.rs_ctas_per_sm;
+        const size_t need = align256((size_t)ctas * 2 * 4 * p.ki.rs_record_floats * sizeof(float));
+        if (need <= ws_avail) {
+            p.schedule = kScheduleRowSplit;
+            p.partition_pages = 0;
+            p.max_parts = 0;
+            p.grid = ctas;
+            p.ws_bytes = need;
+            p.off_part = 0;
+            *plan = p;
+            return PA_OK;
+        }
+    }
+
     int pp;
     if (partition_pages < 0 || !has_ws) {
         if (partition_pages > 0 && partition_pages < nblk_max)
@@ -643,7 +661,9 @@ int pa_decode_make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_
     out->heads_per_cta = p.ki.heads_per_cta;
     out->grid_ctas = (int)p.grid;
     out->threads_per_cta = p.ki.threads;
-    out->smem_bytes = p.ki.smem_bytes;
+    out->smem_bytes = p.schedule == kScheduleRowSplit ? p.ki.rs_smem_bytes
+                      : p.schedule == kScheduleLean   ? p.ki.lean_smem_bytes
+                                                      : p.ki.smem_bytes;
     out->workspace_bytes = p.ws_bytes;
     return PA_OK;
 }
@@ -724,7 +744,9 @@ int decode_impl(void* out, const void* query, const void* new_key, const void* n
     a.ws_m = grid_split ? reinterpret_cast<float*>(ws + p.off_m) : nullptr;
     a.ws_l = grid_split ? reinterpret_cast<float*>(ws + p.off_l) : nullptr;
     a.ws_o = grid_split ? reinterpret_cast<float*>(ws + p.off_o) : nullptr;
-    a.ws_part = p.schedule == kScheduleLean ? reinterpret_cast<float*>(ws + p.off_part) : nullptr;
+    a.ws_part = (p.schedule == kScheduleLean || p.schedule == kScheduleRowSplit)
+                    ? reinterpret_cast<float*>(ws + p.off_part)
+                    : nullptr;
     a.ws_flag = p.schedule == kScheduleLean ? reinterpret_cast<unsigned long long*>(ws + p.off_flag) : nullptr;
     a.epoch = p.schedule == kScheduleLean ? next_epoch() : 0;
     a.wait_ns = kWaitLimitNs;
@@ -820,7 +842,9 @@ int pa_decode_multi_make_plan(int num_seqs, int q_len, int num_heads, int num_kv
     out->heads_per_cta = p.ki.heads_per_cta;
     out->grid_ctas = (int)p.grid;
     out->threads_per_cta = p.ki.threads;
-    out->smem_bytes = p.ki.smem_bytes;
+    out->smem_bytes = p.schedule == kScheduleRowSplit ? p.ki.rs_smem_bytes
+                      : p.schedule == kScheduleLean   ? p.ki.lean_smem_bytes
+                                                      : p.ki.smem_bytes;
     out->workspace_bytes = p.ws_bytes;
     return PA_OK;
 }

@@ -220,110 +220,106 @@ __device__ __noinline__ void append_token(const DecodeArgs& a, int b, int kvh, i
 // Tensor-core consumer (f16 / bf16).
 // CAUSAL: rows carry their own causal bound (multi-query decode); without it every row
 // attends the whole context and the bound checks compile away.
+//
+// Both products keep the page's tokens or head dimensions on the M side of m16n8k16 and the
+// (up to) 8 query rows on the N side, so no half of an operand is padding:
+//  * S^T = K Q^T: A = 16 tokens x 16 dims of K (ldmatrix), B = Q^T (lane g holds query row g);
+//    the accumulator gives lane (g, t) tokens g, g + 8 of query rows 2t, 2t + 1.
+//  * O^T += V^T P^T: A = 16 dims x 16 tokens of V (ldmatrix.trans), B = P^T, which is the
+//    scores' accumulator layout transposed per 8 x 8 block (movmatrix); the accumulator gives
+//    lane (g, t) dims g, g + 8 of every 16 for query rows 2t, 2t + 1, so the rescale factors of
+//    a lane's output columns are its own rows' and need no shuffle.
+// The running max of rows 2t, 2t + 1 is uniform over the 8 lanes of a column (t); each lane
+// keeps its part of the denominators (its two tokens of every sub-tile) until finish().
 template <typename T, int D, int BS, bool CAUSAL>
 struct MmaConsumer {
-    static constexpr int KS = D / 16;  // k-steps of QK^T, m-tiles of PV
-    uint32_t qa[KS][2];                // Q rows 0..7 of the A fragment; rows 8..15 are zero
-    float o[KS][4];                    // O^T fragments: rows d, columns query rows
-    float m, l;                        // running max (quad-uniform) and this thread's part of l
-    int lim;                           // the last position this thread's row (lane / 4) attends
+    static constexpr int KS = D / 16;  // k-steps of K Q^T, m-tiles of V^T P^T
+    uint32_t qb[KS][2];                // Q^T B fragment: row g, dims 16kk + 2t, +1 and 16kk + 8 + 2t, +1
+    float o[KS][4];                    // O^T fragments: rows d, columns query rows 2t, 2t + 1
+    float m_lo, m_hi;                  // running max (log2 domain) of rows 2t, 2t + 1
+    float l_lo, l_hi;                  // this lane's part of their denominators
+    int lim_lo, lim_hi;                // the last positions rows 2t, 2t + 1 attend
 
-    // q_row: this lane's query row (row lane / 4 of the unit), read only when live.
-    __device__ __forceinline__ void init(const T* q_row, bool live, int last_pos, int lane) {
+    // q_row: query row lane / 4 of the unit, read only when live; last_lo / last_hi: the causal
+    // bounds of rows 2 (lane % 4) and 2 (lane % 4) + 1.
+    __device__ __forceinline__ void init(const T* q_row, bool live, int last_lo, int last_hi, int lane) {
         const int t = lane & 3;
         const uint32_t* row = reinterpret_cast<const uint32_t*>(q_row);
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
-            qa[kk][0] = live ? __ldg(row + (kk * 16 + 2 * t) / 2) : 0u;
-            qa[kk][1] = live ? __ldg(row + (kk * 16 + 8 + 2 * t) / 2) : 0u;
+            qb[kk][0] = live ? __ldg(row + (kk * 16 + 2 * t) / 2) : 0u;
+            qb[kk][1] = live ? __ldg(row + (kk * 16 + 8 + 2 * t) / 2) : 0u;
 #pragma unroll
             for (int e = 0; e < 4; ++e) o[kk][e] = 0.f;
         }
-        m = -INFINITY;
-        l = 0.f;
-        lim = last_pos;
+        m_lo = m_hi = -INFINITY;
+        l_lo = l_hi = 0.f;
+        lim_lo = last_lo;
+        lim_hi = last_hi;
     }
 
-    // One page (BS tokens from position pos0, nvalid of them inside the context; a row
-    // attends only the tokens up to its own bound).
-    __device__ __forceinline__ void page(uint8_t* kpage, uint8_t* vpage, int nvalid, int pos0, float scale_log2,
-                                         int lane) {
-        const int t = lane & 3;
+    // 8 x 8 b16 transpose across the warp: lane (g, t) gives elements (g, 2t), (g, 2t + 1) and
+    // gets (2t, g), (2t + 1, g).
+    static __device__ __forceinline__ uint32_t transpose8(uint32_t x) {
+        uint32_t y;
+        asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+        return y;
+    }
+
+    // Max over the 8 lanes of a column (lanes t, t + 4, ..., t + 28).
+    static __device__ __forceinline__ float column_max(float v) {
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 4));
+        v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 8));
+        return fmaxf(v, __shfl_xor_sync(0xffffffffu, v, 16));
+    }
+
+    // S^T of N 16-token sub-tiles (rows row0[i] .. row0[i] + 15 of staged K page kbase[i]), each
+    // accumulated over the dims in two chains (even and odd k-steps); all 2N chains run side by side.
+    template <int N>
+    __device__ __forceinline__ void scores(float (&s)[N][4], const uint32_t (&kbase)[N], const int (&row0)[N],
+                                           int lane) const {
         const int j = lane >> 3, r8 = lane & 7;
-        const uint32_t kbase = smem_addr(kpage);
-        const uint32_t vbase = smem_addr(vpage);
+        const int acol = (j >> 1) * 8;  // ldmatrix order: A0 rows 0-7, A1 rows 8-15, A2/A3 dims 8-15
+        float e[N][4], f[N][4];
 #pragma unroll
-        for (int sub = 0; sub < BS / 16; ++sub) {
-            const int nv = nvalid - sub * 16;
-            if (nv <= 0) break;
-            if (nv < 16) {
-                // Rows past the context may hold anything (NaN included): zero them so
-                // that p = 0 times v stays 0 in the MMA.
-                const int rows = 16 - nv;
-                constexpr int kChunksPerRow = (D * (int)sizeof(T)) / 16;
-                for (int idx = lane; idx < rows * kChunksPerRow; idx += 32) {
-                    const int r = sub * 16 + nv + idx / kChunksPerRow;
-                    const int c = idx % kChunksPerRow;
-                    *reinterpret_cast<uint4*>(vpage + (c / 8) * BS * 128 + r * 128 + (c % 8) * 16) =
-                        make_uint4(0u, 0u, 0u, 0u);
-                }
-                fence_proxy_async_smem();
-                __syncwarp();
-            }
-            // ---- S = Q K^T : two n-tiles of 8 tokens ----
-            float s0[4] = {0.f, 0.f, 0.f, 0.f};
-            float s1[4] = {0.f, 0.f, 0.f, 0.f};
-            const int row = sub * 16 + (j >> 1) * 8 + r8;
+        for (int i = 0; i < N; ++i)
 #pragma unroll
-            for (int kk = 0; kk < KS; ++kk) {
-                uint32_t bf[4];
-                ldmatrix_x4(bf, kbase + swz_offset<T, BS>(row, kk * 16 + (j & 1) * 8));
-                Mma<T>::run(s0, qa[kk][0], 0u, qa[kk][1], 0u, bf[0], bf[1]);
-                Mma<T>::run(s1, qa[kk][0], 0u, qa[kk][1], 0u, bf[2], bf[3]);
-            }
-            // ---- online softmax for row g over tokens 2t, 2t+1, 8+2t, 9+2t ----
-            const int nr = CAUSAL ? min(nv, lim - (pos0 + sub * 16) + 1) : nv;  // tokens row g attends
-            float x0 = (2 * t < nr) ? s0[0] * scale_log2 : -INFINITY;
-            float x1 = (2 * t + 1 < nr) ? s0[1] * scale_log2 : -INFINITY;
-            float x2 = (8 + 2 * t < nr) ? s1[0] * scale_log2 : -INFINITY;
-            float x3 = (9 + 2 * t < nr) ? s1[1] * scale_log2 : -INFINITY;
-            float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            // -inf only while a row has attended nothing yet (a causal bound before this
-            // sub-tile): then alpha and p are 0, not NaN.  Without causal bounds token 0 of a
-            // sub-tile is always attended and m_new is finite.
-            const float m_new = fmaxf(m, mx);
-            const float m_ref = (CAUSAL && m_new == -INFINITY) ? 0.f : m_new;
-            const float alpha = exp2f(m - m_ref);
-            float r0, r1, r2, r3;
-            const uint32_t pb0 = Mma<T>::pack(exp2f(x0 - m_ref), exp2f(x1 - m_ref), r0, r1);
-            const uint32_t pb1 = Mma<T>::pack(exp2f(x2 - m_ref), exp2f(x3 - m_ref), r2, r3);
-            l = l * alpha + ((r0 + r1) + (r2 + r3));
-            m = m_new;
-            // O^T columns 2t and 2t+1 are rows 2t, 2t+1: fetch their rescale factors.
-            const float a_lo = __shfl_sync(0xffffffffu, alpha, (2 * t) * 4);
-            const float a_hi = __shfl_sync(0xffffffffu, alpha, (2 * t + 1) * 4);
-            // ---- O^T += V^T P^T ----
+            for (int c = 0; c < 4; ++c) e[i][c] = f[i][c] = 0.f;
 #pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-                o[mt][0] *= a_lo;
-                o[mt][1] *= a_hi;
-                o[mt][2] *= a_lo;
-                o[mt][3] *= a_hi;
+        for (int kk = 0; kk < KS; ++kk) {
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
                 uint32_t af[4];
-                ldmatrix_x4_trans(af, vbase + swz_offset<T, BS>(row, mt * 16 + (j & 1) * 8));
-                Mma<T>::run(o[mt], af[0], af[1], af[2], af[3], pb0, pb1);
+                ldmatrix_x4(af, kbase[i] + swz_offset<T, BS>(row0[i] + (j & 1) * 8 + r8, kk * 16 + acol));
+                Mma<T>::run((kk & 1) ? f[i] : e[i], af[0], af[1], af[2], af[3], qb[kk][0], qb[kk][1]);
             }
         }
+#pragma unroll
+        for (int i = 0; i < N; ++i)
+#pragma unroll
+            for (int c = 0; c < 4; ++c) s[i][c] = e[i][c] + f[i][c];
     }
 
-    // Zero V rows nv .. 15 of a one-sub-tile page (rows past the context may hold anything).
-    __device__ __forceinline__ static void zero_tail(uint8_t* vpage, int nv, int lane) {
+    // Scaled scores of a sub-tile with the tokens a row does not attend set to -inf: tokens g,
+    // g + 8 of the sub-tile starting at position base, nv of its tokens in the context.
+    __device__ __forceinline__ void mask(float (&x)[4], const float (&s)[4], int nv, int base, float scale_log2,
+                                         int lane) const {
+        const int g = lane >> 2;
+        const int n_lo = CAUSAL ? min(nv, lim_lo - base + 1) : nv;
+        const int n_hi = CAUSAL ? min(nv, lim_hi - base + 1) : nv;
+        x[0] = g < n_lo ? s[0] * scale_log2 : -INFINITY;
+        x[1] = g < n_hi ? s[1] * scale_log2 : -INFINITY;
+        x[2] = g + 8 < n_lo ? s[2] * scale_log2 : -INFINITY;
+        x[3] = g + 8 < n_hi ? s[3] * scale_log2 : -INFINITY;
+    }
+
+    // Zero V rows nv .. 15 of a sub-tile (rows past the context may hold anything, NaN included:
+    // p = 0 times them must stay 0 in the MMA).
+    __device__ __forceinline__ static void zero_tail(uint8_t* vpage, int row0, int nv, int lane) {
         if (nv >= 16) return;
         constexpr int kChunksPerRow = (D * (int)sizeof(T)) / 16;
         for (int idx = lane; idx < (16 - nv) * kChunksPerRow; idx += 32) {
-            const int r = nv + idx / kChunksPerRow;
+            const int r = row0 + nv + idx / kChunksPerRow;
             const int c = idx % kChunksPerRow;
             *reinterpret_cast<uint4*>(vpage + (c / 8) * BS * 128 + r * 128 + (c % 8) * 16) = make_uint4(0u, 0u, 0u, 0u);
         }
@@ -331,99 +327,138 @@ struct MmaConsumer {
         __syncwarp();
     }
 
-    // Two 16-token pages (each with at least one token in the context, starting at positions
-    // pos0 and pos1) in one online-softmax step: their QK^T chains run side by side and the
-    // running max, the rescale and its factor shuffles are taken once for the 32 tokens.
-    __device__ __forceinline__ void page_pair(uint8_t* kp0, uint8_t* vp0, int nv0, int pos0, uint8_t* kp1,
-                                              uint8_t* vp1, int nv1, int pos1, float scale_log2, int lane) {
-        static_assert(BS == 16, "pairs of one-sub-tile pages");
-        const int t = lane & 3;
+    // Online-softmax step over the masked scores of n sub-tiles (x[4 * i ..] for sub-tile i):
+    // returns the P^T B fragments (two per sub-tile) and leaves the rescale factors of rows 2t,
+    // 2t + 1 in alpha_lo / alpha_hi.
+    template <int N>
+    __device__ __forceinline__ void softmax(const float (&x)[4 * N], uint32_t (&pb)[2 * N], float& alpha_lo,
+                                            float& alpha_hi) {
+        float mx_lo = x[0], mx_hi = x[1];
+#pragma unroll
+        for (int i = 0; i < 2 * N; ++i) {
+            mx_lo = fmaxf(mx_lo, x[2 * i]);
+            mx_hi = fmaxf(mx_hi, x[2 * i + 1]);
+        }
+        mx_lo = column_max(mx_lo);
+        mx_hi = column_max(mx_hi);
+        // -inf only while a row has attended nothing yet (a causal bound before these tokens):
+        // then alpha and p are 0, not NaN.  Without causal bounds token 0 is always attended.
+        const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+        const float ref_lo = (CAUSAL && mn_lo == -INFINITY) ? 0.f : mn_lo;
+        const float ref_hi = (CAUSAL && mn_hi == -INFINITY) ? 0.f : mn_hi;
+        alpha_lo = exp2f(m_lo - ref_lo);
+        alpha_hi = exp2f(m_hi - ref_hi);
+        float sum_lo = 0.f, sum_hi = 0.f;
+#pragma unroll
+        for (int i = 0; i < 2 * N; ++i) {
+            float r0, r1;
+            pb[i] = transpose8(Mma<T>::pack(exp2f(x[2 * i] - ref_lo), exp2f(x[2 * i + 1] - ref_hi), r0, r1));
+            sum_lo += r0;
+            sum_hi += r1;
+        }
+        l_lo = l_lo * alpha_lo + sum_lo;
+        l_hi = l_hi * alpha_hi + sum_hi;
+        m_lo = mn_lo;
+        m_hi = mn_hi;
+    }
+
+    // O^T = alpha O^T + V^T P^T over n sub-tiles (vrow0[i]: the first V row of sub-tile i).
+    template <int N>
+    __device__ __forceinline__ void accumulate(const uint32_t (&vbase)[N], const int (&vrow0)[N],
+                                               const uint32_t (&pb)[2 * N], float alpha_lo, float alpha_hi,
+                                               int lane) {
         const int j = lane >> 3, r8 = lane & 7;
-        zero_tail(vp0, nv0, lane);
-        zero_tail(vp1, nv1, lane);
-        const uint32_t kb0 = smem_addr(kp0), kb1 = smem_addr(kp1);
-        const uint32_t vb0 = smem_addr(vp0), vb1 = smem_addr(vp1);
-        // ---- S = Q K^T: page 0 tokens 0-7, 8-15, page 1 tokens 0-7, 8-15 ----
-        float s[4][4];
-#pragma unroll
-        for (int n = 0; n < 4; ++n) s[n][0] = s[n][1] = s[n][2] = s[n][3] = 0.f;
-        const int row = (j >> 1) * 8 + r8;
-#pragma unroll
-        for (int kk = 0; kk < KS; ++kk) {
-            uint32_t b0[4], b1[4];
-            ldmatrix_x4(b0, kb0 + swz_offset<T, BS>(row, kk * 16 + (j & 1) * 8));
-            ldmatrix_x4(b1, kb1 + swz_offset<T, BS>(row, kk * 16 + (j & 1) * 8));
-            Mma<T>::run(s[0], qa[kk][0], 0u, qa[kk][1], 0u, b0[0], b0[1]);
-            Mma<T>::run(s[1], qa[kk][0], 0u, qa[kk][1], 0u, b0[2], b0[3]);
-            Mma<T>::run(s[2], qa[kk][0], 0u, qa[kk][1], 0u, b1[0], b1[1]);
-            Mma<T>::run(s[3], qa[kk][0], 0u, qa[kk][1], 0u, b1[2], b1[3]);
-        }
-        // ---- online softmax for row g over tokens 2t, 2t+1, 8+2t, 9+2t of both pages ----
-        const int nr0 = CAUSAL ? min(nv0, lim - pos0 + 1) : nv0;
-        const int nr1 = CAUSAL ? min(nv1, lim - pos1 + 1) : nv1;
-        float x[8];
-#pragma unroll
-        for (int h = 0; h < 2; ++h) {
-            const int nr = h ? nr1 : nr0;
-            x[4 * h + 0] = (2 * t < nr) ? s[2 * h][0] * scale_log2 : -INFINITY;
-            x[4 * h + 1] = (2 * t + 1 < nr) ? s[2 * h][1] * scale_log2 : -INFINITY;
-            x[4 * h + 2] = (8 + 2 * t < nr) ? s[2 * h + 1][0] * scale_log2 : -INFINITY;
-            x[4 * h + 3] = (9 + 2 * t < nr) ? s[2 * h + 1][1] * scale_log2 : -INFINITY;
-        }
-        float mx = fmaxf(fmaxf(fmaxf(x[0], x[1]), fmaxf(x[2], x[3])), fmaxf(fmaxf(x[4], x[5]), fmaxf(x[6], x[7])));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-        const float m_new = fmaxf(m, mx);
-        const float m_ref = (CAUSAL && m_new == -INFINITY) ? 0.f : m_new;
-        const float alpha = exp2f(m - m_ref);
-        float r[8];
-        uint32_t pb[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            pb[e] = Mma<T>::pack(exp2f(x[2 * e] - m_ref), exp2f(x[2 * e + 1] - m_ref), r[2 * e], r[2 * e + 1]);
-        l = l * alpha + (((r[0] + r[1]) + (r[2] + r[3])) + ((r[4] + r[5]) + (r[6] + r[7])));
-        m = m_new;
-        const float a_lo = __shfl_sync(0xffffffffu, alpha, (2 * t) * 4);
-        const float a_hi = __shfl_sync(0xffffffffu, alpha, (2 * t + 1) * 4);
-        // ---- O^T += V^T P^T over both pages ----
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
-            o[mt][0] *= a_lo;
-            o[mt][1] *= a_hi;
-            o[mt][2] *= a_lo;
-            o[mt][3] *= a_hi;
-            uint32_t af[4], ag[4];
-            ldmatrix_x4_trans(af, vb0 + swz_offset<T, BS>(row, mt * 16 + (j & 1) * 8));
-            ldmatrix_x4_trans(ag, vb1 + swz_offset<T, BS>(row, mt * 16 + (j & 1) * 8));
-            Mma<T>::run(o[mt], af[0], af[1], af[2], af[3], pb[0], pb[1]);
-            Mma<T>::run(o[mt], ag[0], ag[1], ag[2], ag[3], pb[2], pb[3]);
+            o[mt][0] *= alpha_lo;
+            o[mt][1] *= alpha_hi;
+            o[mt][2] *= alpha_lo;
+            o[mt][3] *= alpha_hi;
+#pragma unroll
+            for (int i = 0; i < N; ++i) {
+                uint32_t af[4];
+                ldmatrix_x4_trans(af, vbase[i] + swz_offset<T, BS>(vrow0[i] + (j >> 1) * 8 + r8, mt * 16 + (j & 1) * 8));
+                Mma<T>::run(o[mt], af[0], af[1], af[2], af[3], pb[2 * i], pb[2 * i + 1]);
+            }
         }
     }
 
-    // Complete the per-head denominators (sum over the quad); call once after a unit's last page.
+    // One page (BS tokens from position pos0, nvalid of them inside the context; a row
+    // attends only the tokens up to its own bound).
+    __device__ __forceinline__ void page(uint8_t* kpage, uint8_t* vpage, int nvalid, int pos0, float scale_log2,
+                                         int lane) {
+        const uint32_t kbase = smem_addr(kpage);
+        const uint32_t vbase[1] = {smem_addr(vpage)};
+#pragma unroll
+        for (int sub = 0; sub < BS / 16; ++sub) {
+            const int nv = nvalid - sub * 16;
+            if (nv <= 0) break;
+            zero_tail(vpage, sub * 16, nv, lane);
+            float s[1][4], x[4];
+            const uint32_t kb[1] = {kbase};
+            const int row0[1] = {sub * 16};
+            scores<1>(s, kb, row0, lane);
+            mask(x, s[0], nv, pos0 + sub * 16, scale_log2, lane);
+            uint32_t pb[2];
+            float alpha_lo, alpha_hi;
+            softmax<1>(x, pb, alpha_lo, alpha_hi);
+            const int vrow0[1] = {sub * 16};
+            accumulate<1>(vbase, vrow0, pb, alpha_lo, alpha_hi, lane);
+        }
+    }
+
+    // Two 16-token pages (each with at least one token in the context, starting at positions
+    // pos0 and pos1) in one online-softmax step: their score chains run side by side and the
+    // running max and the rescale are taken once for the 32 tokens.
+    __device__ __forceinline__ void page_pair(uint8_t* kp0, uint8_t* vp0, int nv0, int pos0, uint8_t* kp1,
+                                              uint8_t* vp1, int nv1, int pos1, float scale_log2, int lane) {
+        static_assert(BS == 16, "pairs of one-sub-tile pages");
+        zero_tail(vp0, 0, nv0, lane);
+        zero_tail(vp1, 0, nv1, lane);
+        float sc[2][4], x[8];
+        const uint32_t kb[2] = {smem_addr(kp0), smem_addr(kp1)};
+        const int row0[2] = {0, 0};
+        scores<2>(sc, kb, row0, lane);
+        float x0[4], x1[4];
+        mask(x0, sc[0], nv0, pos0, scale_log2, lane);
+        mask(x1, sc[1], nv1, pos1, scale_log2, lane);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            x[i] = x0[i];
+            x[4 + i] = x1[i];
+        }
+        uint32_t pb[4];
+        float alpha_lo, alpha_hi;
+        softmax<2>(x, pb, alpha_lo, alpha_hi);
+        const uint32_t vbase[2] = {smem_addr(vp0), smem_addr(vp1)};
+        accumulate<2>(vbase, row0, pb, alpha_lo, alpha_hi, lane);
+    }
+
+    // Complete the denominators (sum over the column's 8 lanes); call once after a unit's last page.
     __device__ __forceinline__ void finish() {
-        l += __shfl_xor_sync(0xffffffffu, l, 1);
-        l += __shfl_xor_sync(0xffffffffu, l, 2);
+#pragma unroll
+        for (int w = 4; w < 32; w <<= 1) {
+            l_lo += __shfl_xor_sync(0xffffffffu, l_lo, w);
+            l_hi += __shfl_xor_sync(0xffffffffu, l_hi, w);
+        }
     }
 
     // Forget the unit (init() sets everything again): keeps its registers free meanwhile.
     __device__ __forceinline__ void clear() {
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
-            qa[kk][0] = qa[kk][1] = 0u;
+            qb[kk][0] = qb[kk][1] = 0u;
 #pragma unroll
             for (int e = 0; e < 4; ++e) o[kk][e] = 0.f;
         }
-        m = -INFINITY;
-        l = 0.f;
+        m_lo = m_hi = -INFINITY;
+        l_lo = l_hi = 0.f;
     }
 
     // out[row(r) * D + d] = o~ / l for the gc rows (after finish()); a row that attended
     // nothing (l = 0) gets zeros.
     __device__ __forceinline__ void write_out(T* out, const UnitRows& rows, int gc, int lane) const {
         const int g = lane >> 2, t = lane & 3;
-        const float l_lo = __shfl_sync(0xffffffffu, l, (2 * t) * 4);
-        const float l_hi = __shfl_sync(0xffffffffu, l, (2 * t + 1) * 4);
         const float inv_lo = l_lo > 0.f ? 1.f / l_lo : 0.f;
         const float inv_hi = l_hi > 0.f ? 1.f / l_hi : 0.f;
         T* lo = out + rows.row(min(2 * t, gc - 1)) * D;
@@ -441,15 +476,24 @@ struct MmaConsumer {
         }
     }
 
-    // Partial record of kHeads = 8 heads: m[8], l[8], o~[8][D] (after finish()).
-    __device__ __forceinline__ void write_partial(float* rec, int gc, int lane) const {
+    // Store m, l of rows 2t, 2t + 1 (lanes of g = 0) at m_at[r], l_at[r] (after finish()).
+    __device__ __forceinline__ void write_stats(float* m_at, float* l_at, size_t stride, int gc, int lane) const {
         const int g = lane >> 2, t = lane & 3;
-        if (t == 0 && g < gc) {
-            rec[g] = m;
-            rec[8 + g] = l;
+        if (g == 0) {
+            if (2 * t < gc) {
+                m_at[(size_t)(2 * t) * stride] = m_lo;
+                l_at[(size_t)(2 * t) * stride] = l_lo;
+            }
+            if (2 * t + 1 < gc) {
+                m_at[(size_t)(2 * t + 1) * stride] = m_hi;
+                l_at[(size_t)(2 * t + 1) * stride] = l_hi;
+            }
         }
-        float* lo = rec + 16 + (size_t)(2 * t) * D;
-        float* hi = rec + 16 + (size_t)(2 * t + 1) * D;
+    }
+
+    // o~ of rows 2t, 2t + 1 at lo[d], hi[d].
+    __device__ __forceinline__ void write_o(float* lo, float* hi, int gc, int lane) const {
+        const int g = lane >> 2, t = lane & 3;
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
             if (2 * t < gc) {
@@ -461,50 +505,31 @@ struct MmaConsumer {
                 hi[mt * 16 + 8 + g] = o[mt][3];
             }
         }
+    }
+
+    // Partial record of kHeads = 8 heads: m[8], l[8], o~[8][D] (after finish()).
+    __device__ __forceinline__ void write_partial(float* rec, int gc, int lane) const {
+        const int t = lane & 3;
+        write_stats(rec, rec + 8, 1, gc, lane);
+        write_o(rec + 16 + (size_t)(2 * t) * D, rec + 16 + (size_t)(2 * t + 1) * D, gc, lane);
     }
 
     // Split-KV partials of the gc rows straight into the workspace (after finish()):
     // ws_m / ws_l [row][part], ws_o [row][part][D], rows row0 .. row0 + gc - 1.
     __device__ __forceinline__ void write_split(float* ws_m, float* ws_l, float* ws_o, size_t row0, int max_parts,
                                                 int part, int gc, int lane) const {
-        const int g = lane >> 2, t = lane & 3;
-        if (t == 0 && g < gc) {
-            ws_m[(row0 + g) * max_parts + part] = m;
-            ws_l[(row0 + g) * max_parts + part] = l;
-        }
-        float* lo = ws_o + ((row0 + 2 * t) * max_parts + part) * D;
-        float* hi = ws_o + ((row0 + 2 * t + 1) * max_parts + part) * D;
-#pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-            if (2 * t < gc) {
-                lo[mt * 16 + g] = o[mt][0];
-                lo[mt * 16 + 8 + g] = o[mt][2];
-            }
-            if (2 * t + 1 < gc) {
-                hi[mt * 16 + g] = o[mt][1];
-                hi[mt * 16 + 8 + g] = o[mt][3];
-            }
-        }
+        const int t = lane & 3;
+        write_stats(ws_m + row0 * max_parts + part, ws_l + row0 * max_parts + part, (size_t)max_parts, gc, lane);
+        write_o(ws_o + ((row0 + 2 * t) * max_parts + part) * D, ws_o + ((row0 + 2 * t + 1) * max_parts + part) * D,
+                gc, lane);
     }
 
-    // Write this warp's state into the CTA combine buffer.
+    // Write this warp's state (all 8 rows) into the CTA combine buffer.
     __device__ __forceinline__ void store(float* co, float* cm, float* cl, int warp, int lane, int ostride) {
-        const int g = lane >> 2, t = lane & 3;
-        l += __shfl_xor_sync(0xffffffffu, l, 1);
-        l += __shfl_xor_sync(0xffffffffu, l, 2);
-        if (t == 0) {
-            cm[warp * 8 + g] = m;
-            cl[warp * 8 + g] = l;
-        }
-        float* lo = co + (size_t)(warp * 8 + 2 * t) * ostride;
-        float* hi = co + (size_t)(warp * 8 + 2 * t + 1) * ostride;
-#pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-            lo[mt * 16 + g] = o[mt][0];
-            hi[mt * 16 + g] = o[mt][1];
-            lo[mt * 16 + 8 + g] = o[mt][2];
-            hi[mt * 16 + 8 + g] = o[mt][3];
-        }
+        const int t = lane & 3;
+        finish();
+        write_stats(cm + warp * 8, cl + warp * 8, 1, 8, lane);
+        write_o(co + (size_t)(warp * 8 + 2 * t) * ostride, co + (size_t)(warp * 8 + 2 * t + 1) * ostride, 8, lane);
     }
 };
 
@@ -1076,7 +1101,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
             if (cgc > 0) {
                 const UnitRows rows{b, kvh, chunk * C::kHeads, a.q_len, a.group, a.num_heads};
                 const int r = min(lane >> 2, cgc - 1);
-                cons.init(q + rows.row(r) * D, (lane >> 2) < cgc, rows.last_pos(lane >> 2, L), lane);
+                cons.init(q + rows.row(r) * D, (lane >> 2) < cgc, rows.last_pos(2 * (lane & 3), L),
+                          rows.last_pos(2 * (lane & 3) + 1, L), lane);
             }
             // without row split the warps share the pages round-robin; with it a warp whose
             // chunk is empty (fewer than four chunks) takes no part
@@ -1243,94 +1269,121 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
 constexpr int kMergeThreads = 256;
 constexpr int kMergeMaxParts = 4096;
 
+// One warp per output row: lane p holds partition p's m and l (32 partitions at a time), and
+// lane i holds dims i * DPL .. i * DPL + DPL - 1 of the merged row.  The m, l and the first
+// kMergePre partial outputs of a row are loaded together, so a row of up to kMergePre
+// partitions costs one round trip to memory.
+constexpr int kMergePre = 8;
+
+template <int DPL>
+__device__ __forceinline__ void load_dims(float (&v)[DPL], const float* src) {
+    if constexpr (DPL % 4 == 0) {
+#pragma unroll
+        for (int e = 0; e < DPL; e += 4) {
+            const float4 x = __ldcg(reinterpret_cast<const float4*>(src + e));
+            v[e] = x.x;
+            v[e + 1] = x.y;
+            v[e + 2] = x.z;
+            v[e + 3] = x.w;
+        }
+    } else if constexpr (DPL == 2) {
+        const float2 x = __ldcg(reinterpret_cast<const float2*>(src));
+        v[0] = x.x;
+        v[1] = x.y;
+    } else {
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) v[e] = __ldcg(src + e);
+    }
+}
+
 template <typename T, int D>
 __global__ void __launch_bounds__(kMergeThreads) splitkv_merge_kernel(const MergeArgs a) {
-    constexpr int kWarps = kMergeThreads / 32;
+    static_assert(D % 32 == 0, "whole dims per lane");
+    static_assert(32 % kMergePre == 0, "partition batches inside a 32-partition chunk");
     constexpr int DPL = D / 32;
-    __shared__ float wts[kMergeMaxParts];
-    __shared__ float red[kWarps];
-    __shared__ float part_o[kWarps][D];
-    const int row = blockIdx.x;  // (b * H_kv + kvh) * rows + v
-    const int b = row / (a.num_kv_heads * a.rows);
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * (kMergeThreads / 32) + (threadIdx.x >> 5);  // (b * H_kv + kvh) * rows + v
 
     // Wait for the decode kernel's partials (programmatic dependent launch); then the
     // next grid in the stream may start launching.
     griddep_wait();
     griddep_launch_dependents();
+    if (row >= a.num_seqs * a.num_kv_heads * a.rows) return;
+    const int b = row / (a.num_kv_heads * a.rows);
 
     int L = __ldg(a.context_lens + b);
     const int l_cap = min(a.max_blocks, a.max_parts * a.partition_pages) * a.block_size;
     L = L < 0 ? 0 : (L > l_cap ? l_cap : L);
     const int nblk = (L + a.block_size - 1) / a.block_size;
     const int n = (nblk + a.partition_pages - 1) / a.partition_pages;
-    if (n <= 1) return;
+    if (n <= 1) return;  // the decode kernel wrote the row itself
 
     const float* mrow = a.ws_m + (size_t)row * a.max_parts;
     const float* lrow = a.ws_l + (size_t)row * a.max_parts;
-    // 1) global max over partitions
-    float mm = -INFINITY;
-    for (int pp = tid; pp < n; pp += kMergeThreads) mm = fmaxf(mm, __ldcg(mrow + pp));
+    const float* obase = a.ws_o + (size_t)row * a.max_parts * D + lane * DPL;
+    const float m0 = lane < n ? __ldcg(mrow + lane) : -INFINITY;
+    const float l0 = lane < n ? __ldcg(lrow + lane) : 0.f;
+    float v[kMergePre][DPL];
+#pragma unroll
+    for (int i = 0; i < kMergePre; ++i) {
+        if (i < n) {
+            load_dims<DPL>(v[i], obase + (size_t)i * D);
+        } else {
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) v[i][e] = 0.f;
+        }
+    }
+    // 1) the common max over the partitions
+    float mm = m0;
+    for (int c = 32; c < n; c += 32)
+        if (c + lane < n) mm = fmaxf(mm, __ldcg(mrow + c + lane));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) mm = fmaxf(mm, __shfl_xor_sync(0xffffffffu, mm, off));
-    if (lane == 0) red[warp] = mm;
-    __syncthreads();
-    mm = red[0];
-#pragma unroll
-    for (int w = 1; w < kWarps; ++w) mm = fmaxf(mm, red[w]);
-    __syncthreads();
-    // 2) weights and the merged denominator (a partition a row's causal bound excludes,
-    //    or a row with no position at all, weighs 0)
-    float ws = 0.f;
-    for (int pp = tid; pp < n; pp += kMergeThreads) {
-        const float f = rescale(__ldcg(mrow + pp), mm);
-        wts[pp] = f;
-        ws += f * __ldcg(lrow + pp);
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, off);
-    if (lane == 0) red[warp] = ws;
-    __syncthreads();
-    ws = 0.f;
-#pragma unroll
-    for (int w = 0; w < kWarps; ++w) ws += red[w];
-    // 3) weighted sum of the partial outputs: warp w takes partitions w, w + 8, ...
+    // 2) weights (a partition a row's causal bound excludes weighs 0) and the merged
+    //    denominator; 3) the weighted sum of the partial outputs
+    float f = rescale(m0, mm);  // weight of partition c + lane of the current chunk
+    float ws = f * l0;
     float acc[DPL];
 #pragma unroll
     for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
-    const float* obase = a.ws_o + (size_t)row * a.max_parts * D + lane * DPL;
-#pragma unroll 4
-    for (int pp = warp; pp < n; pp += kWarps) {
-        const float f = wts[pp];
-        const float* src = obase + (size_t)pp * D;
-        if constexpr (DPL % 4 == 0) {
 #pragma unroll
-            for (int e = 0; e < DPL; e += 4) {
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(src + e));
-                acc[e] += f * v.x;
-                acc[e + 1] += f * v.y;
-                acc[e + 2] += f * v.z;
-                acc[e + 3] += f * v.w;
+    for (int i = 0; i < kMergePre; ++i) {
+        const float fi = __shfl_sync(0xffffffffu, f, i);
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[e] += fi * v[i][e];
+    }
+    for (int q0 = kMergePre; q0 < n; q0 += kMergePre) {
+        if (q0 % 32 == 0) {
+            const int q = q0 + lane;
+            f = q < n ? rescale(__ldcg(mrow + q), mm) : 0.f;
+            ws += q < n ? f * __ldcg(lrow + q) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kMergePre; ++i) {
+            if (q0 + i < n) {
+                load_dims<DPL>(v[i], obase + (size_t)(q0 + i) * D);
+            } else {
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) v[i][e] = 0.f;
             }
-        } else {
+        }
 #pragma unroll
-            for (int e = 0; e < DPL; ++e) acc[e] += f * __ldcg(src + e);
+        for (int i = 0; i < kMergePre; ++i) {
+            const float fi = __shfl_sync(0xffffffffu, f, (q0 + i) % 32);
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc[e] += fi * v[i][e];
         }
     }
 #pragma unroll
-    for (int e = 0; e < DPL; ++e) part_o[warp][lane * DPL + e] = acc[e];
-    __syncthreads();
+    for (int off = 16; off > 0; off >>= 1) ws += __shfl_xor_sync(0xffffffffu, ws, off);
+
     const int rest = row - b * a.num_kv_heads * a.rows;
     const int kvh = rest / a.rows;
     const UnitRows rows{b, kvh, rest - kvh * a.rows, a.q_len, a.group, a.num_heads};
-    T* out = static_cast<T*>(a.out) + rows.row(0) * D;
+    T* out = static_cast<T*>(a.out) + rows.row(0) * D + lane * DPL;
     const float inv = ws > 0.f ? 1.f / ws : 0.f;
-    for (int d = tid; d < D; d += kMergeThreads) {
-        float s = 0.f;
 #pragma unroll
-        for (int w = 0; w < kWarps; ++w) s += part_o[w][d];
-        out[d] = from_float<T>(s * inv);
-    }
+    for (int e = 0; e < DPL; ++e) out[e] = from_float<T>(acc[e] * inv);
 }
 
 
@@ -1672,7 +1725,8 @@ __global__ void __launch_bounds__(DecodeCfg<T, D, BS, MMA, GMAX>::kThreads,
             cons.init(q + rows.row(r) * D, (lane >> 2) < gc, a.scale_log2, lane);
         } else if constexpr (MMA) {
             const int r = min(lane >> 2, gc - 1);
-            cons.init(q + rows.row(r) * D, (lane >> 2) < gc, rows.last_pos(lane >> 2, L), lane);
+            cons.init(q + rows.row(r) * D, (lane >> 2) < gc, rows.last_pos(2 * (lane & 3), L),
+                      rows.last_pos(2 * (lane & 3) + 1, L), lane);
         } else {
             __syncwarp();
             for (int idx = lane; idx < GMAX * D; idx += 32)
@@ -2160,11 +2214,353 @@ __global__ void __launch_bounds__(kLeanMergeThreads, PA_LEAN_MERGE_MINB) lean_me
 }
 
 // ------------------------------------------------------------------------------------------
+// ------------------------------------------------------------------------------------------
+// Persistent row-split schedule (multi-query decode: a kv head's rows in 2..4 chunks of 8).
+// One wave of CTAs.  The pages of all (sequence, kv head) units, laid end to end (sequence-major,
+// then kv head, pages in logical order), are cut into equal contiguous shares, one per CTA.  The
+// producer warp streams its share's pages once through the ring and consumer warp w takes row
+// chunk w of every page, so each page is read once for all of its kv head's rows and every CTA
+// streams the same number of pages whatever the context lengths are.  A unit that lies wholly
+// inside a share is written out by its CTA; a unit cut by a share boundary leaves one partial
+// record per row chunk in each CTA it spans (slot 0: the share's first unit, slot 1: its last
+// unit), and rs_lean_merge_kernel combines them.
+template <typename T, int D, int BS>
+struct RsLeanCfg {
+    using C = DecodeCfg<T, D, BS, true, 8>;
+    static constexpr int kMaxChunks = 4;
+    static constexpr int kRecFloats = 16 + 8 * D;  // m[8], l[8], o~[8][D] (MmaConsumer::write_partial)
+    // (num_seqs + 1) ints of page prefix sums, then num_seqs clamped context lengths
+    static constexpr int kPrefixOffset = C::a16(C::kFlagOffset + 16);
+    static int smem_bytes(int num_seqs) { return kPrefixOffset + (2 * num_seqs + 1) * 4 + 1024; }
+    static constexpr int kMaxSmemBytes = kPrefixOffset + (2 * kLeanMaxSeqs + 1) * 4 + 1024;
+    static_assert(C::kStatBytes >= (C::kNW + 1) * 4, "the scan's warp sums live in the stat area");
+    static_assert(C::kNW >= kMaxChunks, "a consumer warp per row chunk");
+};
+
+// Pages per sequence (context lengths clamped to the tables: [0, max_blocks * BS]) and their
+// exclusive prefix sums into pre[0 .. B]; lens[b] receives the clamped length.  Every thread of
+// the CTA calls it.
+template <int BS>
+__device__ __forceinline__ void rs_page_prefix(const int32_t* context_lens, int B, int max_blocks, int* pre, int* lens,
+                                               int* warp_sums, int nwarps, bool report, unsigned* err) {
+    const int nthreads = nwarps * 32;
+    const int l_cap = max_blocks * BS;
+    const int per = (B + nthreads - 1) / nthreads;
+    const int b_lo = min(B, (int)threadIdx.x * per);
+    const int b_hi = min(B, b_lo + per);
+    int mine = 0;
+    for (int b = b_lo; b < b_hi; ++b) {
+        int L = __ldcg(context_lens + b);
+        if (L < 0 || L > l_cap) {
+            if (report) atomicOr(err, kErrBadContext);
+            L = L < 0 ? 0 : l_cap;
+        }
+        if (lens) lens[b] = L;
+        pre[b] = (L + BS - 1) / BS;
+        mine += pre[b];
+    }
+    int total = 0;
+    int acc = block_exclusive_scan(mine, warp_sums, nwarps, &total);
+    for (int b = b_lo; b < b_hi; ++b) {
+        const int nb = pre[b];
+        pre[b] = acc;
+        acc += nb;
+    }
+    if (threadIdx.x == 0) pre[B] = total;
+    __syncthreads();
+}
+
+template <typename T, int D, int BS>
+__global__ void __launch_bounds__(DecodeCfg<T, D, BS, true, 8>::kThreads, D <= 128 ? 3 : 2)
+    paged_decode_rs_lean_kernel(const __grid_constant__ CUtensorMap tmap_k, const __grid_constant__ CUtensorMap tmap_v,
+                                const DecodeArgs a) {
+    using R = RsLeanCfg<T, D, BS>;
+    using C = typename R::C;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint8_t* ring = smem;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + C::kBarOffset);
+    uint64_t* empty = full + C::kNSlot;
+    int* issued = reinterpret_cast<int*>(smem + C::kIssuedOffset);
+    int* warp_sums = reinterpret_cast<int*>(smem + C::kStatOffset);
+    volatile int* flags = reinterpret_cast<volatile int*>(smem + C::kFlagOffset);  // [0]: abort
+    int* pre = reinterpret_cast<int*>(smem + R::kPrefixOffset);
+    int* lens_s = pre + (a.num_seqs + 1);
+
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    const int B = a.num_seqs;
+    const int nchunks = (a.rows + C::kHeads - 1) / C::kHeads;  // 2..4 (the plan takes this schedule only then)
+
+    if (tid == 0) {
+        for (int s = 0; s < C::kNSlot; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], nchunks);  // every chunk's warp releases the slot
+            issued[s] = 0;
+        }
+        flags[0] = 0;
+        fence_barrier_init();
+    }
+    // Wait for the previous grid in the stream (it may write the lengths, the tables or the
+    // queries); the merge grid may launch at once, it waits for this grid's completion itself.
+    griddep_wait();
+    griddep_launch_dependents();
+
+    rs_page_prefix<BS>(a.context_lens, B, a.max_blocks, pre, lens_s, warp_sums, C::kNW + 1, blockIdx.x == 0, a.err);
+    const int upb = a.num_kv_heads;  // units per sequence
+    const int total = pre[B] * upb;
+    const int share = (total + (int)gridDim.x - 1) / (int)gridDim.x;
+    const int g0 = min(total, (int)blockIdx.x * share);
+    const int g1 = min(total, g0 + share);
+    if (g0 >= g1) return;  // no pages for this CTA (fewer pages than CTAs)
+
+    if (warp == C::kNW) {
+        // ================= producer warp =================
+        if (lane == 0) {
+            tma_prefetch_desc(&tmap_k);
+            tma_prefetch_desc(&tmap_v);
+        }
+        // Pages are read once per call: let them leave L2 first.
+        const uint64_t stream_policy = l2_policy_evict_first();
+        int i = 0;  // the page's index in the share; its ring slot is i % kNSlot
+        bool ok = true;
+        for (int g = g0; g < g1 && ok;) {
+            int b, kvh, j, nb;
+            lean_locate(pre, B, upb, g, b, kvh, j, nb);
+            const int cnt = min(g1 - g, nb - j);  // this unit's pages in the share
+            const int32_t* bt = a.block_tables + (size_t)b * a.max_blocks + j;
+            for (int c = 0; c < cnt && ok; c += 32) {
+                const int pbl = c + lane < cnt ? __ldcg(bt + c + lane) : 0;
+                const int m = min(32, cnt - c);
+                for (int jj = 0; jj < m; ++jj) {
+                    const int pb = __shfl_sync(0xffffffffu, pbl, jj);
+                    int good = 1;
+                    if (lane == 0) {
+                        const int s = i % C::kNSlot;
+                        if (i >= C::kNSlot)
+                            good = mbar_wait_bounded(&empty[s], ((i / C::kNSlot) - 1) & 1, a.err, flags) ? 1 : 0;
+                        if (good) {
+                            issued[s] += 1;
+                            if ((unsigned)pb < (unsigned)a.num_blocks) {
+                                mbar_arrive_expect_tx(&full[s], C::kSlotBytes);
+                                const int row = (pb * a.num_kv_heads + kvh) * BS;
+                                uint8_t* kdst = ring + s * C::kSlotBytes;
+                                uint8_t* vdst = kdst + C::kPageBytes;
+#pragma unroll
+                                for (int bx = 0; bx < C::kNBox; ++bx)
+                                    tma_load_2d_hint(kdst + bx * C::kBoxBytes, &tmap_k, bx * C::kBoxElems, row,
+                                                     &full[s], stream_policy);
+#pragma unroll
+                                for (int bx = 0; bx < C::kNBox; ++bx)
+                                    tma_load_2d_hint(vdst + bx * C::kBoxBytes, &tmap_v, bx * C::kBoxElems, row,
+                                                     &full[s], stream_policy);
+                            } else {
+                                atomicOr(a.err, kErrBadTable);  // skip the load; the slot keeps stale data
+                                mbar_arrive(&full[s]);
+                            }
+                        }
+                    }
+                    ok = __shfl_sync(0xffffffffu, good, 0) != 0;
+                    if (!ok) break;
+                    ++i;
+                }
+            }
+            g += cnt;
+        }
+    } else if (warp < nchunks) {
+        // ================= consumer warps: warp w takes row chunk w =================
+        const T* q = static_cast<const T*>(a.q);
+        T* out = static_cast<T*>(a.out);
+        MmaConsumer<T, D, BS, true> cons;
+        const int cgc = min(C::kHeads, a.rows - warp * C::kHeads);  // this chunk's rows
+        int i = 0;
+        bool alive = true;
+        for (int g = g0; g < g1 && alive;) {
+            int j, nb, cnt, L;
+            {
+                int b, kvh;
+                lean_locate(pre, B, upb, g, b, kvh, j, nb);
+                cnt = min(g1 - g, nb - j);
+                L = lens_s[b];
+                const UnitRows rows{b, kvh, warp * C::kHeads, a.q_len, a.group, a.num_heads};
+                const int r = min(lane >> 2, cgc - 1);
+                cons.init(q + rows.row(r) * D, (lane >> 2) < cgc, rows.last_pos(2 * (lane & 3), L),
+                          rows.last_pos(2 * (lane & 3) + 1, L), lane);
+            }
+            int k = 0;
+            if constexpr (BS == 16) {
+                // two pages at a time (one softmax step per 32 tokens); an odd last page below
+                for (; k + 1 < cnt; k += 2) {
+                    const int i0 = i + k;
+                    const int s0 = i0 % C::kNSlot, s1 = (i0 + 1) % C::kNSlot;
+                    const bool got = mbar_wait_bounded(&full[s0], (i0 / C::kNSlot) & 1, a.err, flags) &&
+                                     mbar_wait_bounded(&full[s1], ((i0 + 1) / C::kNSlot) & 1, a.err, flags);
+                    if (!__all_sync(0xffffffffu, got)) {
+                        alive = false;
+                        break;
+                    }
+                    const int p0 = j + k;  // the pair's first page in the unit
+                    uint8_t* kp0 = ring + s0 * C::kSlotBytes;
+                    uint8_t* kp1 = ring + s1 * C::kSlotBytes;
+                    cons.page_pair(kp0, kp0 + C::kPageBytes, min(BS, L - p0 * BS), p0 * BS, kp1, kp1 + C::kPageBytes,
+                                   min(BS, L - (p0 + 1) * BS), (p0 + 1) * BS, a.scale_log2, lane);
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(&empty[s0]);
+                        mbar_arrive(&empty[s1]);
+                    }
+                }
+            }
+            for (; alive && k < cnt; ++k) {
+                const int i0 = i + k;
+                const int s = i0 % C::kNSlot;
+                const bool got = mbar_wait_bounded(&full[s], (i0 / C::kNSlot) & 1, a.err, flags);
+                if (!__all_sync(0xffffffffu, got)) {
+                    alive = false;
+                    break;
+                }
+                const int p = j + k;
+                uint8_t* kp = ring + s * C::kSlotBytes;
+                cons.page(kp, kp + C::kPageBytes, min(BS, L - p * BS), p * BS, a.scale_log2, lane);
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&empty[s]);
+            }
+            if (!alive) break;
+            i += cnt;
+            cons.finish();
+            if (cnt == nb) {
+                // the whole unit lies in this share (its sequence and kv head found again: fewer
+                // registers live across the page loop)
+                int b, kvh, jj, nn;
+                lean_locate(pre, B, upb, g, b, kvh, jj, nn);
+                cons.write_out(out, UnitRows{b, kvh, warp * C::kHeads, a.q_len, a.group, a.num_heads}, cgc, lane);
+            } else {
+                const int slot = g == g0 ? 0 : 1;
+                float* rec = a.ws_part + (((size_t)blockIdx.x * 2 + slot) * R::kMaxChunks + warp) * R::kRecFloats;
+                cons.write_partial(rec, cgc, lane);
+            }
+            g += cnt;
+        }
+    }
+    __syncthreads();  // pipeline finished (or abandoned)
+    if (flags[0] && tid == 0) {
+        // A wait gave up: let every issued copy land before the CTA's shared memory goes away.
+        for (int s = 0; s < C::kNSlot; ++s)
+            if (issued[s] > 0) {
+                const unsigned long long start = global_timer_ns();
+                while (!mbar_try_wait(&full[s], (issued[s] - 1) & 1) && global_timer_ns() - start < kWaitLimitNs) {
+                }
+            }
+    }
+}
+
+// Combines the partial records of the units that the row-split schedule's shares cut: one warp
+// per output row (b, kv head, row v of the kv head), with the page layout and share size
+// recomputed from the lengths exactly as the decode grid computed them (a.lean_grid CTAs).  A
+// sequence with an empty context gets zero rows here.
+template <typename T, int D, int BS>
+__global__ void __launch_bounds__(kMergeThreads) rs_lean_merge_kernel(const DecodeArgs a) {
+    using R = RsLeanCfg<T, D, BS>;
+    static_assert(D % 32 == 0, "whole dims per lane");
+    constexpr int DPL = D / 32;
+    constexpr int kWarps = kMergeThreads / 32;
+    extern __shared__ int mpre[];  // [num_seqs + 1] page prefix sums
+    __shared__ int msums[kWarps];
+    const int lane = threadIdx.x & 31;
+    const int row = blockIdx.x * kWarps + (threadIdx.x >> 5);  // (b * H_kv + kvh) * rows + v
+
+    griddep_wait();  // the decode grid's records and rows are complete
+    griddep_launch_dependents();
+    const int B = a.num_seqs;
+    rs_page_prefix<BS>(a.context_lens, B, a.max_blocks, mpre, nullptr, msums, kWarps, false, a.err);
+    if (row >= B * a.num_kv_heads * a.rows) return;
+    const int b = row / (a.num_kv_heads * a.rows);
+    const int rest = row - b * a.num_kv_heads * a.rows;
+    const int kvh = rest / a.rows;
+    const int v = rest - kvh * a.rows;
+    const UnitRows rows{b, kvh, v, a.q_len, a.group, a.num_heads};
+    T* out = static_cast<T*>(a.out) + rows.row(0) * D + lane * DPL;
+    const int nb = mpre[b + 1] - mpre[b];
+    if (nb == 0) {
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) out[e] = from_float<T>(0.f);
+        return;
+    }
+    const int total = mpre[B] * a.num_kv_heads;
+    const int share = (total + a.lean_grid - 1) / a.lean_grid;
+    const int start = mpre[b] * a.num_kv_heads + kvh * nb;
+    const int c0 = start / share;
+    const int n = (start + nb - 1) / share - c0 + 1;  // CTAs whose shares hold pages of the unit
+    if (n <= 1) return;                               // the decode grid wrote the row itself
+    const int chunk = v >> 3, r = v & 7;
+    // CTA c0 holds the unit as its last unit unless the unit starts its share; later CTAs as their first
+    const int slot0 = start == c0 * share ? 0 : 1;
+    auto rec = [&](int p) {
+        return a.ws_part + (((size_t)(c0 + p) * 2 + (p == 0 ? slot0 : 0)) * R::kMaxChunks + chunk) * R::kRecFloats;
+    };
+    const float m0 = lane < n ? __ldcg(rec(lane) + r) : -INFINITY;
+    const float l0 = lane < n ? __ldcg(rec(lane) + 8 + r) : 0.f;
+    float vals[kMergePre][DPL];
+#pragma unroll
+    for (int i = 0; i < kMergePre; ++i) {
+        if (i < n) {
+            load_dims<DPL>(vals[i], rec(i) + 16 + r * D + lane * DPL);
+        } else {
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) vals[i][e] = 0.f;
+        }
+    }
+    float mm = m0;
+    for (int c = 32; c < n; c += 32)
+        if (c + lane < n) mm = fmaxf(mm, __ldcg(rec(c + lane) + r));
+    mm = warp_max(mm);
+    float f = rescale(m0, mm);
+    float ws = f * l0;
+    float acc[DPL];
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) acc[e] = 0.f;
+#pragma unroll
+    for (int i = 0; i < kMergePre; ++i) {
+        const float fi = __shfl_sync(0xffffffffu, f, i);
+#pragma unroll
+        for (int e = 0; e < DPL; ++e) acc[e] += fi * vals[i][e];
+    }
+    for (int q0 = kMergePre; q0 < n; q0 += kMergePre) {
+        if (q0 % 32 == 0) {
+            const int qq = q0 + lane;
+            f = qq < n ? rescale(__ldcg(rec(qq) + r), mm) : 0.f;
+            ws += qq < n ? f * __ldcg(rec(qq) + 8 + r) : 0.f;
+        }
+#pragma unroll
+        for (int i = 0; i < kMergePre; ++i) {
+            if (q0 + i < n) {
+                load_dims<DPL>(vals[i], rec(q0 + i) + 16 + r * D + lane * DPL);
+            } else {
+#pragma unroll
+                for (int e = 0; e < DPL; ++e) vals[i][e] = 0.f;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < kMergePre; ++i) {
+            const float fi = __shfl_sync(0xffffffffu, f, (q0 + i) % 32);
+#pragma unroll
+            for (int e = 0; e < DPL; ++e) acc[e] += fi * vals[i][e];
+        }
+    }
+    ws = warp_sum(ws);
+    const float inv = ws > 0.f ? 1.f / ws : 0.f;
+#pragma unroll
+    for (int e = 0; e < DPL; ++e) out[e] = from_float<T>(acc[e] * inv);
+}
+
 // Host-side helpers for the per-dtype translation units.
 template <typename T, int D, int BS, bool MMA, int GMAX, bool CAUSAL>
 struct DecodeKernel {
     using C = DecodeCfg<T, D, BS, MMA, GMAX>;
     using LC = LeanCfg<T, D, BS, MMA, GMAX>;
+    // the persistent row-split schedule: tensor-core kernel with causal bounds, 16-bit types
+    static constexpr bool kRowSplit = MMA && CAUSAL && sizeof(T) == 2;
 
     static bool configure(int device) {
         static unsigned long long done_mask = 0;  // one bit per device (< 64)
@@ -2176,6 +2572,11 @@ struct DecodeKernel {
         if (cudaFuncSetAttribute(paged_decode_lean_kernel<T, D, BS, MMA, GMAX, CAUSAL>,
                                  cudaFuncAttributeMaxDynamicSharedMemorySize, LC::kMaxSmemBytes) != cudaSuccess)
             return false;
+        if constexpr (kRowSplit) {
+            if (cudaFuncSetAttribute(paged_decode_rs_lean_kernel<T, D, BS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     RsLeanCfg<T, D, BS>::kMaxSmemBytes) != cudaSuccess)
+                return false;
+        }
         done_mask |= bit;
         return true;
     }
@@ -2221,6 +2622,25 @@ struct DecodeKernel {
         info->lean_warps_per_cta = LC::kNW;
         info->lean_record_floats = LC::kRecFloats;
         info->lean_max_seqs = kLeanMaxSeqs;
+        info->rs_ctas_per_sm = 0;
+        info->rs_smem_bytes = 0;
+        info->rs_record_floats = 0;
+        if constexpr (kRowSplit) {
+            using R = RsLeanCfg<T, D, BS>;
+            info->rs_smem_bytes = R::smem_bytes(seqs);
+            info->rs_record_floats = R::kRecFloats;
+            static std::atomic<int> rs_occ[64][232];
+            const int kb = (info->rs_smem_bytes + 1023) / 1024;
+            std::atomic<int>& slot = rs_occ[device & 63][kb < 232 ? kb : 231];
+            int r = slot.load(std::memory_order_relaxed);
+            if (r <= 0) {
+                if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, paged_decode_rs_lean_kernel<T, D, BS>,
+                                                                  C::kThreads, kb * 1024) != cudaSuccess)
+                    r = 0;
+                slot.store(r > 0 ? r : -1, std::memory_order_relaxed);
+            }
+            info->rs_ctas_per_sm = r > 0 ? r : 0;
+        }
         return true;
     }
 
@@ -2245,6 +2665,21 @@ struct DecodeKernel {
             const int mgrid = lean_merge_setup(m, grid);
             return launch_pdl(lean_merge_kernel<T, D, LC::kHeads, BS>, dim3(mgrid), dim3(kLeanMergeThreads), 0,
                               stream, m);
+        } else if (schedule == kScheduleRowSplit) {
+            if constexpr (kRowSplit) {
+                using R = RsLeanCfg<T, D, BS>;
+                DecodeArgs d = a;
+                d.lean_grid = grid;
+                e = launch_pdl(paged_decode_rs_lean_kernel<T, D, BS>, dim3(grid), dim3(C::kThreads),
+                               R::smem_bytes(num_seqs), stream, k, v, d);
+                if (e != cudaSuccess) return e;
+                const int rows = a.num_seqs * a.num_kv_heads * a.rows;
+                constexpr int kRowsPerCta = kMergeThreads / 32;
+                return launch_pdl(rs_lean_merge_kernel<T, D, BS>, dim3((rows + kRowsPerCta - 1) / kRowsPerCta),
+                                  dim3(kMergeThreads), (num_seqs + 1) * (int)sizeof(int), stream, d);
+            } else {
+                return cudaErrorInvalidValue;
+            }
         } else {
             return launch_pdl(paged_decode_kernel<T, D, BS, MMA, GMAX, CAUSAL>, dim3(grid), dim3(C::kThreads), C::kSmemBytes,
                               stream, k, v, a);
@@ -2301,6 +2736,9 @@ struct DecodeKernelF8 {
         info->lean_warps_per_cta = LC::kNW;
         info->lean_record_floats = LC::kRecFloats;
         info->lean_max_seqs = kLeanMaxSeqs;
+        info->rs_ctas_per_sm = 0;
+        info->rs_smem_bytes = 0;
+        info->rs_record_floats = 0;
         return true;
     }
 
@@ -2326,7 +2764,9 @@ struct DecodeKernelF8 {
 
 template <typename T, int D>
 cudaError_t launch_merge(const MergeArgs& a, cudaStream_t stream) {
-    return launch_pdl(splitkv_merge_kernel<T, D>, dim3(a.num_seqs * a.num_heads * a.q_len), dim3(kMergeThreads), 0,
+    constexpr int kRowsPerCta = kMergeThreads / 32;
+    const int merge_rows = a.num_seqs * a.num_heads * a.q_len;
+    return launch_pdl(splitkv_merge_kernel<T, D>, dim3((merge_rows + kRowsPerCta - 1) / kRowsPerCta), dim3(kMergeThreads), 0,
                       stream, a);
 }
 

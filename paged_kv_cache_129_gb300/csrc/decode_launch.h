@@ -16,7 +16,7 @@ struct DecodeArgs {
     float* ws_m;                 // [B * Hq, max_parts]   running max (log2 domain) per partition
     float* ws_l;                 // [B * Hq, max_parts]   running denominator per partition
     float* ws_o;                 // [B * Hq, max_parts, D] unnormalised output per partition
-    float* ws_part;              // lean schedule: two partial records per consumer warp
+    float* ws_part;              // lean schedule: two partial records per consumer warp; row-split: two per CTA and chunk
     unsigned long long* ws_flag; // lean schedule: one flag per record, set to `epoch` when published
     unsigned long long epoch;    // lean schedule: a value no earlier call has used (never 0)
     unsigned long long wait_ns;  // lean merge: bound of its wait for the partial records (ns)
@@ -47,7 +47,7 @@ struct DecodeArgs {
     int partition_pages, max_parts;
     float scale_log2;            // softmax scale * log2(e)
     int lean_warps_per_cta;      // consumer warps per lean CTA
-    int lean_grid;               // CTAs of the lean decode launch (set for the merge kernel)
+    int lean_grid;               // CTAs of the lean / row-split decode launch (set for their merge kernels)
     int lean_merge_by_boundary;  // merge grid: one CTA per boundary between warp shares, not per unit
     int lean_share_warps;        // lean schedule: consumer warps the pages are cut for (<= all of them)
     int force_restart;           // lean decode: treat the set-up made before the wait as wrong (tests)
@@ -75,10 +75,15 @@ struct KernelInfo {
     int lean_warps_per_cta;
     int lean_record_floats; // floats of one partial record
     int lean_max_seqs;
+    int rs_ctas_per_sm;     // resident CTAs per SM, persistent row-split schedule (0: not compiled)
+    int rs_smem_bytes;      // its dynamic shared memory per CTA for the given num_seqs
+    int rs_record_floats;   // floats of one of its partial records (8 rows of a chunk)
 };
 
-// kScheduleLeanMergeOnly: the lean merge kernel alone (diagnostics of its bounded wait).
-enum Schedule { kScheduleGrid = 0, kScheduleLean = 1, kScheduleLeanMergeOnly = 2 };
+// kScheduleRowSplit: the persistent row-split wave (multi-query decode with 2..4 row chunks per kv
+// head) and its merge.  kScheduleLeanMergeOnly: the lean merge kernel alone (diagnostics of its
+// bounded wait; never a plan's schedule).
+enum Schedule { kScheduleGrid = 0, kScheduleLean = 1, kScheduleRowSplit = 2, kScheduleLeanMergeOnly = 3 };
 
 // kind: 1 = tensor-core (mma) kernel, 2 = CUDA-core kernel, 3 = tensor-core kernel with a causal bound
 // per row (multi-query decode; the CUDA-core kernel always has it); gmax: head-chunk width of the

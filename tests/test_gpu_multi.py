@@ -101,3 +101,16 @@ def test_multi_qwen_shape_sampled_rows():
     ref = oracle.decode_multi(inp.q, inp.key_cache, inp.value_cache, inp.block_tables, inp.context_lens, "bf16",
                               inp.scale, rows=rows)
     assert_decode_close(np.stack([got[b, t, h] for b, t, h in rows]), ref, "bf16")
+
+
+@pytest.mark.parametrize("q_len", [2, 3, 4])
+@pytest.mark.parametrize("lens,hkv", [((4096,), 1), ((0, 5000, 3), 2), ((700, 1, 0, 2049, 16, 17), 4)])
+def test_row_split_schedule_cut_units(lens, hkv, q_len):
+    # 9..32 rows per kv head take the persistent row-split wave.  With few pages against one wave of
+    # CTAs a share holds one or two pages, so a unit spans up to hundreds of shares and the merge
+    # folds more than 32 partial records into a row; empty and shorter-than-q_len contexts included.
+    inp = mq_case("bf16", 128, 16, 7 * hkv, hkv, q_len, lens=lens, seed=len(lens) * 10 + q_len)
+    plan = pa.decode_plan(inp.num_seqs, inp.num_heads, inp.num_kv_heads, 128, 16, inp.max_blocks_per_seq,
+                          torch.bfloat16, q_len=q_len)
+    assert plan.schedule == 2 and plan.grid_ctas > 0
+    assert_decode_close(run_multi(inp).reshape(-1, 128), oracle_multi(inp).reshape(-1, 128), "bf16")

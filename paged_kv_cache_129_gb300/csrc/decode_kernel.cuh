@@ -623,10 +623,11 @@ struct MmaConsumerF8 {
     static_assert(D == 128, "the FP8 consumer's lane layout is for head_dim 128");
     static_assert(BS % 16 == 0, "16-token sub-tiles");
     static constexpr int KS = D / 16;  // k-steps of QK^T, m-tiles of PV
-    uint32_t qa[KS][2];                // f16 Q fragments, rows 0..7 (rows 8..15 are zero)
-    float o[KS][4];                    // O^T fragments, in units of vs_cur
-    float m, l;
-    float qf;                          // this row's score factor: 2^-e * scale * log2(e)
+    uint32_t qa[KS][2];                // f16 Q^T B fragments of query row lane / 4
+    float o[KS][4];                    // O^T fragments (columns: query rows 2c, 2c + 1), in units of vs_cur
+    float m_lo, m_hi;                  // running max of rows 2c, 2c + 1 (uniform over the column's lanes)
+    float l_lo, l_hi;                  // this lane's part of their denominators
+    float qf_lo, qf_hi;                // their score factors: 2^-e * scale * log2(e)
     float vs_cur;                      // V scale o is expressed in (0 before the first page)
 
     // q_row: this lane's query row (row lane / 4 of the unit), read only when live.
@@ -657,9 +658,11 @@ struct MmaConsumerF8 {
 #pragma unroll
             for (int r = 0; r < 4; ++r) o[kk][r] = 0.f;
         }
-        qf = scale_log2 * __int_as_float((127 - e) << 23);  // 2^-e
-        m = -INFINITY;
-        l = 0.f;
+        const float qf = scale_log2 * __int_as_float((127 - e) << 23);  // row lane / 4's factor, 2^-e
+        qf_lo = __shfl_sync(0xffffffffu, qf, (2 * c) * 4);
+        qf_hi = __shfl_sync(0xffffffffu, qf, (2 * c + 1) * 4);
+        m_lo = m_hi = -INFINITY;
+        l_lo = l_hi = 0.f;
         vs_cur = 0.f;
     }
 
@@ -669,7 +672,7 @@ struct MmaConsumerF8 {
         const int g = lane >> 2, c = lane & 3;
         float vr = vs_cur == 0.f ? 1.f : vs_cur / vs;  // o into units of this page's V scale
         vs_cur = vs;
-        const float sf = qf * ks;
+        const float sf_lo = qf_lo * ks, sf_hi = qf_hi * ks;
 #pragma unroll
         for (int sub = 0; sub < BS / 16; ++sub) {
             const int nv = nvalid - sub * 16;
@@ -682,43 +685,52 @@ struct MmaConsumerF8 {
                 fence_proxy_async_smem();
                 __syncwarp();
             }
-            // ---- S = Q K^T: two n-tiles of 8 tokens, each summed over two independent accumulators
-            // (even and odd k-steps) so that the MMA dependency chains are half as long ----
-            float s[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-            float s2[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+            // ---- S^T = K Q^T: the sub-tile's 16 tokens on the MMA's rows (tokens g and g + 8 here), the
+            // query rows on its columns; summed in two chains (even and odd k-steps) ----
+            const int tok = sub * 16 + g;
+            const uint8_t* rk0 = kpage + tok * 128;
+            const uint8_t* rk1 = rk0 + 8 * 128;  // token g + 8: the same swizzle phase
+            const int sw = tok & 7;
+            const uint4 k00 = *reinterpret_cast<const uint4*>(rk0 + (((2 * c) ^ sw) << 4));
+            const uint4 k01 = *reinterpret_cast<const uint4*>(rk0 + (((2 * c + 1) ^ sw) << 4));
+            const uint4 k10 = *reinterpret_cast<const uint4*>(rk1 + (((2 * c) ^ sw) << 4));
+            const uint4 k11 = *reinterpret_cast<const uint4*>(rk1 + (((2 * c + 1) ^ sw) << 4));
+            const uint32_t kw0[8] = {k00.x, k00.y, k00.z, k00.w, k01.x, k01.y, k01.z, k01.w};
+            const uint32_t kw1[8] = {k10.x, k10.y, k10.z, k10.w, k11.x, k11.y, k11.z, k11.w};
+            float se[4] = {0.f, 0.f, 0.f, 0.f};
+            float so[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                const int tok = sub * 16 + nt * 8 + g;
-                const uint8_t* row = kpage + tok * 128;
-                const uint4 k0 = *reinterpret_cast<const uint4*>(row + (((2 * c) ^ (tok & 7)) << 4));
-                const uint4 k1 = *reinterpret_cast<const uint4*>(row + (((2 * c + 1) ^ (tok & 7)) << 4));
-                const uint32_t w[8] = {k0.x, k0.y, k0.z, k0.w, k1.x, k1.y, k1.z, k1.w};
-#pragma unroll
-                for (int kk = 0; kk < KS; ++kk) {
-                    uint32_t b0, b1;
-                    e4m3x4_to_f16x2x2(w[kk], b0, b1);
-                    Mma<__half>::run((kk & 1) ? s2[nt] : s[nt], qa[kk][0], 0u, qa[kk][1], 0u, b0, b1);
-                }
-#pragma unroll
-                for (int e = 0; e < 4; ++e) s[nt][e] += s2[nt][e];
+            for (int kk = 0; kk < KS; ++kk) {
+                uint32_t a0, a1, a2, a3;
+                e4m3x4_to_f16x2x2(kw0[kk], a0, a2);  // token g: k = 2c, 2c + 1 | 2c + 8, 2c + 9
+                e4m3x4_to_f16x2x2(kw1[kk], a1, a3);  // token g + 8
+                Mma<__half>::run((kk & 1) ? so : se, a0, a1, a2, a3, qa[kk][0], qa[kk][1]);
             }
-            // ---- online softmax for row g over tokens 2c, 2c+1, 8+2c, 9+2c ----
-            const float x0 = (2 * c < nv) ? s[0][0] * sf : -INFINITY;
-            const float x1 = (2 * c + 1 < nv) ? s[0][1] * sf : -INFINITY;
-            const float x2 = (8 + 2 * c < nv) ? s[1][0] * sf : -INFINITY;
-            const float x3 = (9 + 2 * c < nv) ? s[1][1] * sf : -INFINITY;
-            float mx = fmaxf(fmaxf(x0, x1), fmaxf(x2, x3));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
-            const float m_new = fmaxf(m, mx);  // token 0 of the sub-tile is attended: finite
-            const float alpha = exp2f(m - m_new);
+            // ---- online softmax for rows 2c, 2c + 1 over tokens g, g + 8 (token 0 is attended: finite max) ----
+            const float x0 = g < nv ? (se[0] + so[0]) * sf_lo : -INFINITY;
+            const float x1 = g < nv ? (se[1] + so[1]) * sf_hi : -INFINITY;
+            const float x2 = g + 8 < nv ? (se[2] + so[2]) * sf_lo : -INFINITY;
+            const float x3 = g + 8 < nv ? (se[3] + so[3]) * sf_hi : -INFINITY;
+            float mx_lo = fmaxf(x0, x2), mx_hi = fmaxf(x1, x3);
+#pragma unroll
+            for (int w = 4; w < 32; w <<= 1) {
+                mx_lo = fmaxf(mx_lo, __shfl_xor_sync(0xffffffffu, mx_lo, w));
+                mx_hi = fmaxf(mx_hi, __shfl_xor_sync(0xffffffffu, mx_hi, w));
+            }
+            const float mn_lo = fmaxf(m_lo, mx_lo), mn_hi = fmaxf(m_hi, mx_hi);
+            const float alpha_lo = exp2f(m_lo - mn_lo), alpha_hi = exp2f(m_hi - mn_hi);
             float r0, r1, r2, r3;
-            const uint32_t pb0 = Mma<__half>::pack(exp2f(x0 - m_new), exp2f(x1 - m_new), r0, r1);
-            const uint32_t pb1 = Mma<__half>::pack(exp2f(x2 - m_new), exp2f(x3 - m_new), r2, r3);
-            l = l * alpha + ((r0 + r1) + (r2 + r3));
-            m = m_new;
-            const float a_lo = __shfl_sync(0xffffffffu, alpha, (2 * c) * 4) * vr;
-            const float a_hi = __shfl_sync(0xffffffffu, alpha, (2 * c + 1) * 4) * vr;
+            const uint32_t pk0 = Mma<__half>::pack(exp2f(x0 - mn_lo), exp2f(x1 - mn_hi), r0, r1);
+            const uint32_t pk1 = Mma<__half>::pack(exp2f(x2 - mn_lo), exp2f(x3 - mn_hi), r2, r3);
+            l_lo = l_lo * alpha_lo + (r0 + r2);
+            l_hi = l_hi * alpha_hi + (r1 + r3);
+            m_lo = mn_lo;
+            m_hi = mn_hi;
+            // P^T B fragments (tokens 2c, 2c + 1 | 2c + 8, 2c + 9 of query row g): the 8 x 8 blocks transposed
+            const uint32_t pb0 = transpose8(pk0);
+            const uint32_t pb1 = transpose8(pk1);
+            const float a_lo = alpha_lo * vr;
+            const float a_hi = alpha_hi * vr;
             vr = 1.f;
             // ---- O^T += V^T P^T ----
             const int t0 = sub * 16 + 2 * c;
@@ -745,9 +757,19 @@ struct MmaConsumerF8 {
         }
     }
 
+    // 8 x 8 b16 transpose across the warp: lane (g, c) gives elements (g, 2c), (g, 2c + 1), gets (2c, g), (2c + 1, g).
+    static __device__ __forceinline__ uint32_t transpose8(uint32_t x) {
+        uint32_t y;
+        asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+        return y;
+    }
+
     __device__ __forceinline__ void finish() {
-        l += __shfl_xor_sync(0xffffffffu, l, 1);
-        l += __shfl_xor_sync(0xffffffffu, l, 2);
+#pragma unroll
+        for (int w = 4; w < 32; w <<= 1) {
+            l_lo += __shfl_xor_sync(0xffffffffu, l_lo, w);
+            l_hi += __shfl_xor_sync(0xffffffffu, l_hi, w);
+        }
     }
 
     __device__ __forceinline__ void clear() {
@@ -757,16 +779,14 @@ struct MmaConsumerF8 {
 #pragma unroll
             for (int e = 0; e < 4; ++e) o[kk][e] = 0.f;
         }
-        m = -INFINITY;
-        l = 0.f;
+        m_lo = m_hi = -INFINITY;
+        l_lo = l_hi = 0.f;
         vs_cur = 0.f;
     }
 
     // out[row(r) * D + d] = o~ / l for the gc rows (after finish()); a row with l = 0 gets zeros.
     __device__ __forceinline__ void write_out(T* out, const UnitRows& rows, int gc, int lane) const {
         const int g = lane >> 2, c = lane & 3;
-        const float l_lo = __shfl_sync(0xffffffffu, l, (2 * c) * 4);
-        const float l_hi = __shfl_sync(0xffffffffu, l, (2 * c + 1) * 4);
         const float f_lo = l_lo > 0.f ? vs_cur / l_lo : 0.f;
         const float f_hi = l_hi > 0.f ? vs_cur / l_hi : 0.f;
 #pragma unroll
@@ -789,9 +809,15 @@ struct MmaConsumerF8 {
     // Partial record of 8 rows: m[8], l[8], o~[8][D] in true units (after finish()).
     __device__ __forceinline__ void write_partial(float* rec, int gc, int lane) const {
         const int g = lane >> 2, c = lane & 3;
-        if (c == 0 && g < gc) {
-            rec[g] = m;
-            rec[8 + g] = l;
+        if (g == 0) {
+            if (2 * c < gc) {
+                rec[2 * c] = m_lo;
+                rec[8 + 2 * c] = l_lo;
+            }
+            if (2 * c + 1 < gc) {
+                rec[2 * c + 1] = m_hi;
+                rec[9 + 2 * c] = l_hi;
+            }
         }
 #pragma unroll
         for (int half = 0; half < 2; ++half) {

@@ -332,7 +332,8 @@ int make_plan(int num_seqs, int num_heads, int num_kv_heads, int head_dim, int b
     // Lean schedule: one persistent wave; every consumer warp streams an equal share of all pages.
     // (Worth it when there are fewer units than consumer warps: then units must be split
     // to keep every SM streaming, and equal shares balance them.  With more units than
-    // that, whole-unit CTAs already balance and need no merge.)
+    // that, whole-unit CTAs already balance and need no merge.  So a 16/32-bit lean plan always
+    // merges with one CTA per unit; the merge grid by share boundary serves FP8 plans alone.)
     const long long lean_ctas = (long long)dev->num_sms * p.ki.lean_ctas_per_sm;
     if (partition_pages == 0 && has_ws && !p.row_split && num_seqs <= p.ki.lean_max_seqs &&
         (long long)p.units < lean_ctas * p.ki.lean_warps_per_cta &&

@@ -163,3 +163,11 @@ def test_reference_arm_setup_maps_no_product_library():
             "assert 'libpagedkv' not in maps, 'product library mapped'\n")
     root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
     subprocess.run([sys.executable, "-c", code], cwd=root, check=True, timeout=300)
+
+
+def test_default_line_side_records_and_schedule_names():
+    # every side record of the default line is a known workload, and every plan schedule the library
+    # reports (0 grid, 1 lean, 2 row split) has a name in the line
+    assert set(bench.SIDE_WORKLOADS) <= set(bench.WORKLOAD_DESCRIPTIONS)
+    assert "qwen_gqa" not in bench.SIDE_WORKLOADS
+    assert set(bench.SCHEDULE_NAMES) == {0, 1, 2}
